@@ -1,0 +1,789 @@
+// C ABI of the drafter library: handle, weight packing, caches, workspaces
+// and the ingest / draft step orchestration (see include/dspark.h).
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "../../include/dspark.h"
+#include "kernels.cuh"
+#include "tc_gemm.cuh"
+
+using namespace dspark;
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+struct DevBuf {
+    void* p = nullptr;
+    size_t bytes = 0;
+};
+
+// Kernel classes of the step, timed by dspark_profile.
+enum Cat {
+    CAT_INGEST_PROJ, CAT_INGEST_NORM, CAT_INGEST_KV, CAT_BLOCK, CAT_NORM, CAT_QKV, CAT_ATTN, CAT_O, CAT_GATE_UP,
+    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_COUNT
+};
+const char* const kCatNames[CAT_COUNT] = {"ingest_proj", "ingest_norm", "ingest_kv", "block_build", "rmsnorm",
+                                          "qkv_proj", "attention", "o_proj", "gate_up_proj", "down_proj",
+                                          "out_proj", "markov_argmax"};
+
+struct ProfRange {
+    int cat;
+    cudaEvent_t a, b;
+    long long launches;
+};
+
+}  // namespace
+
+struct dspark_handle {
+    dspark_config cfg{};
+    int device = 0;
+    int num_sms = 148;
+    int dt = DT_BF16;
+    size_t esz = 2;
+    int d = 0, F = 0, hd = 0, mH = 0, R = 0;  // R: rows of the largest draft batch (max_seqs * gamma)
+
+    std::vector<void*> allocs;
+    // packed weights (library-owned)
+    void* W_c = nullptr;
+    float* ctx_norm = nullptr;
+    const void* embed = nullptr;
+    void* tok_proj = nullptr;
+    float* block_const = nullptr;            // [gamma, d]
+    std::vector<void*> wqkv, wo, wgu, wd;    // wqkv [3d, d]; wgu [2F, d] rows (gate f, up f) interleaved
+    std::vector<float*> attn_norm, ff_norm;
+    float** attn_norm_dev = nullptr;         // device array of the attn_norm pointers
+    float* out_norm = nullptr;
+    void* out_proj = nullptr;
+    void* w1 = nullptr;
+    void* w2 = nullptr;
+    float* conf_wb = nullptr;                // [d + r + 1]
+    TcWeight tc_wc, tc_out_proj;             // tensor-core views (bf16 only)
+    std::vector<TcWeight> tc_kv, tc_qkv, tc_wo, tc_wgu, tc_wd;
+    TcWeight tc_tok_proj;
+    // caches: [layer][seq][K|V][rows][d]
+    void* cache = nullptr;
+    int64_t rows = 0, seq_stride = 0, kv_off = 0, layer_stride = 0;
+    int* d_len = nullptr;
+    int* d_err = nullptr;
+    std::vector<int> len_host;
+    std::vector<char> len_known;
+    // draft workspaces
+    float *x = nullptr, *act = nullptr, *hbuf = nullptr, *q = nullptr, *y = nullptr, *U = nullptr;
+    void* act_lp = nullptr;                  // bf16 copies of A operands for the tensor-core path
+    void* h_lp = nullptr;
+    float* attn_part = nullptr;
+    size_t attn_part_floats = 0;
+    float* mk_v = nullptr;
+    int* mk_i = nullptr;
+    unsigned int* mk_cnt = nullptr;
+    int mk_ctas = 1;
+    float* ws = nullptr;
+    size_t ws_floats = 0;
+    int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
+    int* safe_anchors = nullptr;             // [max_seqs] batched anchors clamped into [0, V)
+    // ingest workspaces
+    int ingest_rows = 0;
+    float* P = nullptr;
+    void* Nbuf = nullptr;
+    DevBuf rowmap;                           // row_seq, row_pos (grow-only)
+    DevBuf stage_in, stage_out;              // host-call staging (grow-only)
+
+    std::string err = "no error";
+    long long launches_at_create = 0;
+    // profiling
+    bool prof_on = false;
+    uint32_t prof_mask = 0;
+    std::vector<ProfRange> prof_ranges;
+    std::vector<cudaEvent_t> prof_pool;
+    size_t prof_next = 0;
+};
+
+namespace {
+
+dspark_status fail(dspark_handle* h, dspark_status st, const std::string& msg) {
+    if (h) h->err = msg;
+    else g_create_error = msg;
+    return st;
+}
+
+#define CUDA_TRY(h, expr)                                                                     \
+    do {                                                                                      \
+        cudaError_t _e = (expr);                                                              \
+        if (_e != cudaSuccess)                                                                \
+            return fail((h), _e == cudaErrorMemoryAllocation ? DSPARK_ERR_OOM : DSPARK_ERR_CUDA, \
+                        std::string(#expr) + ": " + cudaGetErrorString(_e));                  \
+    } while (0)
+
+cudaError_t dalloc(dspark_handle* h, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) h->allocs.push_back(*p);
+    return e;
+}
+
+cudaError_t grow(DevBuf& b, size_t bytes) {
+    if (b.bytes >= bytes) return cudaSuccess;
+    if (b.p) cudaFree(b.p);
+    b.p = nullptr;
+    b.bytes = 0;
+    size_t want = std::max<size_t>(bytes, 1 << 20);
+    cudaError_t e = cudaMalloc(&b.p, want);
+    if (e == cudaSuccess) b.bytes = want;
+    return e;
+}
+
+int attn_chunks(const dspark_handle* h, int B, int max_keys) {
+    // enough CTAs for two per SM, but at least 32 keys per chunk
+    const int nh = h->cfg.n_heads;
+    int want = (2 * h->num_sms + nh * B - 1) / (nh * B);
+    int by_keys = (max_keys + 31) / 32;
+    return std::max(1, std::min(want, by_keys));
+}
+
+// acc = A . W^T with the best kernel for the shape.
+cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, const int* a_rows, int a_row0,
+                 const void* W, const TcWeight* tcw, int M, int N, int K, const EpiParams& ep, cudaStream_t st) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (M <= 16 && skinny_ok(M, K))
+        return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
+    if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_gemm_ok(M, N, K))
+        return tc_gemm((const char*)A + (size_t)a_row0 * lda * 2, lda, *tcw, M, N, K, ep, h->num_sms, st);
+    const char* a = (const char*)A;
+    if (!a_rows) a += (size_t)a_row0 * lda * (a_dtype == DT_BF16 ? 2 : 4);
+    return gemm_simt(a_dtype, a, lda, a_rows, h->dt, W, M, N, K, ep, st);
+}
+
+// Records an event pair around one class of launches when profiling is on.
+struct Prof {
+    dspark_handle* h;
+    cudaStream_t st;
+    int idx = -1;
+    long long l0 = 0;
+    cudaEvent_t ev() {
+        if (h->prof_next >= h->prof_pool.size()) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+            h->prof_pool.push_back(e);
+        }
+        return h->prof_pool[h->prof_next++];
+    }
+    Prof(dspark_handle* h_, int cat, cudaStream_t st_) : h(h_), st(st_) {
+        if (!h->prof_on || !(h->prof_mask & (1u << cat))) return;
+        cudaEvent_t a = ev(), b = ev();
+        if (!a || !b) return;
+        cudaEventRecord(a, st);
+        h->prof_ranges.push_back({cat, a, b, 0});
+        idx = (int)h->prof_ranges.size() - 1;
+        l0 = launch_count();
+    }
+    void end() {
+        if (idx < 0) return;
+        cudaEventRecord(h->prof_ranges[idx].b, st);
+        h->prof_ranges[idx].launches = launch_count() - l0;
+        idx = -1;
+    }
+    ~Prof() { end(); }
+};
+
+EpiParams cache_epi(const dspark_handle* h, int layer) {
+    EpiParams ep;
+    ep.cache = (char*)h->cache + (size_t)layer * h->layer_stride * h->esz;
+    ep.cache_dtype = h->dt;
+    ep.seq_stride = h->seq_stride;
+    ep.kv_off = h->kv_off;
+    ep.d = h->d;
+    ep.max_rows = (int)h->rows;
+    ep.seq_len = h->d_len;
+    return ep;
+}
+
+dspark_status check_cfg(const dspark_config* c, std::string& why) {
+    if (!c) { why = "config is NULL"; return DSPARK_ERR_INVALID_ARG; }
+    if (c->hidden <= 0 || c->n_taps <= 0 || c->d_draft <= 0 || c->n_heads <= 0 || c->n_layers <= 0 ||
+        c->ff_mult <= 0 || c->gamma <= 0 || c->vocab <= 0 || c->markov_rank <= 0 || c->max_ctx < 0 ||
+        c->max_seqs <= 0 || !(c->eps >= 0.f)) {
+        why = "config has a non-positive dimension";
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (c->d_draft % c->n_heads != 0) {
+        why = "d_draft " + std::to_string(c->d_draft) + " not divisible by n_heads " + std::to_string(c->n_heads);
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (c->dtype != DSPARK_BF16 && c->dtype != DSPARK_FP32) { why = "unknown dtype"; return DSPARK_ERR_INVALID_ARG; }
+    if (c->act != DSPARK_ACT_SILU && c->act != DSPARK_ACT_GELU_TANH) { why = "unknown act"; return DSPARK_ERR_INVALID_ARG; }
+    const int hd = c->d_draft / c->n_heads;
+    if (c->gamma > 16) { why = "gamma > 16"; return DSPARK_ERR_UNSUPPORTED; }
+    if (hd > 256 || hd % 8 != 0) { why = "head_dim must be a multiple of 8 and <= 256"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->d_draft % 64 != 0) { why = "d_draft must be a multiple of 64"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->markov_rank % 8 != 0 || c->markov_rank > 1024) { why = "markov_rank must be a multiple of 8, <= 1024"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
+    if ((int64_t)c->max_ctx + c->gamma > (1 << 30)) { why = "max_ctx too large"; return DSPARK_ERR_UNSUPPORTED; }
+    return DSPARK_OK;
+}
+
+dspark_status sync_len(dspark_handle* h, int slot) {
+    if (h->len_known[slot]) return DSPARK_OK;
+    int v = 0;
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    CUDA_TRY(h, cudaMemcpy(&v, h->d_len + slot, sizeof(int), cudaMemcpyDeviceToHost));
+    h->len_host[slot] = v;
+    h->len_known[slot] = 1;
+    return DSPARK_OK;
+}
+
+// Eq 2 + Eq 3 for `T` feature rows; rows map to (slot, position) through
+// row_seq/row_pos (batched) or slot 0 at len[0] + t (row_seq == nullptr).
+dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int* row_seq, const int* row_pos,
+                          cudaStream_t st) {
+    const int d = h->d, nL = h->cfg.n_layers;
+    for (int t0 = 0; t0 < T; t0 += h->ingest_rows) {
+        const int n = std::min(h->ingest_rows, T - t0);
+        const void* X = (const char*)feats + (size_t)t0 * h->mH * h->esz;
+        EpiParams ep;
+        ep.kind = EPI_STORE_F32;
+        ep.out_f32 = h->P;
+        ep.ldo = d;
+        {
+            Prof pr(h, CAT_INGEST_PROJ, st);
+            CUDA_TRY(h, gemm(h, h->dt, X, h->mH, nullptr, 0, h->W_c, &h->tc_wc, n, d, h->mH, ep, st));
+        }
+        const int lp = h->dt;  // normalised rows in the storage type (bf16 feeds the tensor cores)
+        {
+            Prof pr(h, CAT_INGEST_NORM, st);
+            CUDA_TRY(h, ingest_norm(h->P, n, d, h->cfg.eps, h->ctx_norm, h->attn_norm_dev, nL, lp, h->Nbuf,
+                                    (int64_t)h->ingest_rows * d, st));
+        }
+        Prof pr_kv(h, CAT_INGEST_KV, st);
+        for (int i = 0; i < nL; ++i) {
+            EpiParams kv = cache_epi(h, i);
+            kv.kind = EPI_KV_CACHE;
+            if (row_seq) {
+                kv.row_seq = row_seq + t0;
+                kv.row_pos = row_pos + t0;
+            }
+            // otherwise slot 0 at len[0] + m: the device length advances after every chunk
+            const void* Ni = (const char*)h->Nbuf + (size_t)i * h->ingest_rows * d * h->esz;
+            const void* Wkv = (const char*)h->wqkv[i] + (size_t)d * d * h->esz;  // rows [d, 3d) = [W_k; W_v]
+            CUDA_TRY(h, gemm(h, lp, Ni, d, nullptr, 0, Wkv, h->tc_kv.empty() ? nullptr : &h->tc_kv[i], n, 2 * d, d,
+                             kv, st));
+        }
+        if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
+    }
+    return DSPARK_OK;
+}
+
+// The draft step for B sequences (slots seq_ids[b], or slot b when NULL).
+dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
+                         int* tokens, float* conf, float* logits, cudaStream_t st) {
+    const dspark_config& c = h->cfg;
+    const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
+    Prof pr_block(h, CAT_BLOCK, st);
+    CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st));
+    {
+        EpiParams ep;
+        ep.kind = EPI_ADD_F32;
+        ep.out_f32 = h->x;
+        ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
+        CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor, h->tok_proj, nullptr, B,
+                         d, c.hidden, ep, st));
+    }
+    const bool lowp = (h->dt == DT_BF16) && R > 16;  // tensor-core path takes bf16 A operands
+    void* actA = lowp ? h->act_lp : (void*)h->act;
+    const int adt = lowp ? DT_BF16 : DT_F32;
+    for (int i = 0; i < c.n_layers; ++i) {
+        if (i == 0) pr_block.end();
+        {
+            Prof pr(h, CAT_NORM, st);
+            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->attn_norm[i], R, d, c.eps, adt, actA, d, st));
+        }
+        EpiParams qkv = cache_epi(h, i);
+        qkv.kind = EPI_QKV;
+        qkv.out_f32 = h->q;
+        qkv.ldo = d;
+        qkv.gamma = c.gamma;
+        qkv.seq_ids = seq_ids;
+        {
+            Prof pr(h, CAT_QKV, st);
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wqkv[i], h->tc_qkv.empty() ? nullptr : &h->tc_qkv[i], R,
+                             3 * d, d, qkv, st));
+        }
+        AttnParams ap;
+        ap.q = h->q;
+        ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
+        ap.cache_dtype = h->dt;
+        ap.seq_stride = h->seq_stride;
+        ap.kv_off = h->kv_off;
+        ap.seq_len = h->d_len;
+        ap.seq_ids = seq_ids;
+        ap.B = B;
+        ap.gamma = c.gamma;
+        ap.d = d;
+        ap.n_heads = c.n_heads;
+        ap.n_chunks = attn_chunks(h, B, max_keys);
+        ap.part = h->attn_part;
+        ap.out = actA;
+        ap.out_dtype = adt;
+        if (attn_scratch_floats(B, c.n_heads, ap.n_chunks, c.gamma, h->hd) > h->attn_part_floats)
+            return fail(h, DSPARK_ERR_CAPACITY, "attention scratch too small");
+        {
+            Prof pr(h, CAT_ATTN, st);
+            CUDA_TRY(h, attention(ap, st));
+        }
+        EpiParams res;
+        res.kind = EPI_ADD_F32;
+        res.out_f32 = h->x;
+        res.ldo = d;
+        {
+            Prof pr(h, CAT_O, st);
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wo[i], h->tc_wo.empty() ? nullptr : &h->tc_wo[i], R, d,
+                             d, res, st));
+        }
+        {
+            Prof pr(h, CAT_NORM, st);
+            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->ff_norm[i], R, d, c.eps, adt, actA, d, st));
+        }
+        EpiParams sw;
+        sw.kind = EPI_SWIGLU;
+        sw.out_act = lowp ? h->h_lp : (void*)h->hbuf;
+        sw.act_dtype = adt;
+        sw.ld_act = F;
+        sw.act = c.act;
+        {
+            Prof pr(h, CAT_GATE_UP, st);
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wgu[i], h->tc_wgu.empty() ? nullptr : &h->tc_wgu[i], R,
+                             2 * F, d, sw, st));
+        }
+        {
+            Prof pr(h, CAT_DOWN, st);
+            CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0, h->wd[i], h->tc_wd.empty() ? nullptr : &h->tc_wd[i], R,
+                             d, F, res, st));
+        }
+    }
+    {
+        Prof pr(h, CAT_NORM, st);
+        CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
+    }
+    {
+        Prof pr(h, CAT_OUT_PROJ, st);
+        EpiParams ep;
+        ep.kind = EPI_STORE_F32;
+        ep.out_f32 = h->U;
+        ep.ldo = V;
+        const void* A = h->y;
+        int adt2 = DT_F32;
+        if (lowp) {
+            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_BF16, h->act_lp, d, st));
+            A = h->act_lp;
+            adt2 = DT_BF16;
+        }
+        CUDA_TRY(h, gemm(h, adt2, A, d, nullptr, 0, h->out_proj, &h->tc_out_proj, R, V, d, ep, st));
+    }
+    MarkovParams mp;
+    mp.U = h->U;
+    mp.w1 = h->w1;
+    mp.w2 = h->w2;
+    mp.w_dtype = h->dt;
+    mp.y = h->y;
+    mp.conf_w = h->conf_wb;
+    mp.B = B;
+    mp.gamma = c.gamma;
+    mp.V = V;
+    mp.r = c.markov_rank;
+    mp.d = d;
+    mp.anchors = anchors_dev;
+    mp.anchor = anchor;
+    mp.tokens = tokens;
+    mp.conf = conf;
+    mp.logits = logits;
+    mp.part_v = h->mk_v;
+    mp.part_i = h->mk_i;
+    mp.counters = h->mk_cnt;
+    mp.err = h->d_err;
+    mp.ctas = h->mk_ctas;
+    Prof pr(h, CAT_MARKOV, st);
+    for (int k = 0; k < c.gamma; ++k) {
+        mp.k = k;
+        CUDA_TRY(h, markov_step(mp, st));
+    }
+    return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dspark_status dspark_profile(dspark_handle* h, int32_t class_mask) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (class_mask) {
+        CUDA_TRY(h, cudaDeviceSynchronize());
+        h->prof_ranges.clear();
+        h->prof_next = 0;
+    }
+    h->prof_on = class_mask != 0;
+    h->prof_mask = (uint32_t)class_mask;
+    return DSPARK_OK;
+}
+
+int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_host, double* ms_host,
+                            int64_t* ranges_host, int64_t* launches_host) {
+    if (!h) return -1;
+    double ms[CAT_COUNT] = {0};
+    int64_t nr[CAT_COUNT] = {0}, nl[CAT_COUNT] = {0};
+    for (auto& r : h->prof_ranges) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+        ms[r.cat] += t;
+        nr[r.cat] += 1;
+        nl[r.cat] += r.launches;
+    }
+    for (int c = 0; c < CAT_COUNT && c < max; ++c) {
+        if (names_host) names_host[c] = kCatNames[c];
+        if (ms_host) ms_host[c] = ms[c];
+        if (ranges_host) ranges_host[c] = nr[c];
+        if (launches_host) launches_host[c] = nl[c];
+    }
+    return CAT_COUNT;
+}
+
+const char* dspark_version(void) { return "dspark-gb300 0.1"; }
+
+const char* dspark_last_error(const dspark_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+int64_t dspark_launch_count(const dspark_handle* h) {
+    return h ? (int64_t)(launch_count() - h->launches_at_create) : (int64_t)launch_count();
+}
+
+void dspark_destroy(dspark_handle* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    for (void* p : h->allocs) cudaFree(p);
+    if (h->rowmap.p) cudaFree(h->rowmap.p);
+    if (h->stage_in.p) cudaFree(h->stage_in.p);
+    if (h->stage_out.p) cudaFree(h->stage_out.p);
+    for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
+    tc_release(h->tc_wc);
+    tc_release(h->tc_out_proj);
+    tc_release(h->tc_tok_proj);
+    for (auto* v : {&h->tc_kv, &h->tc_qkv, &h->tc_wo, &h->tc_wgu, &h->tc_wd})
+        for (auto& w : *v) tc_release(w);
+    delete h;
+}
+
+dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, void* stream, dspark_handle** out) {
+    if (!out) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    std::string why;
+    dspark_status s = check_cfg(cfg, why);
+    if (s != DSPARK_OK) return fail(nullptr, s, why);
+    if (!w) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "weights are NULL");
+    const int nL = cfg->n_layers;
+    if (!w->W_c || !w->ctx_norm || !w->embed || !w->tok_proj || !w->block_pos || (cfg->gamma > 1 && !w->mask_emb) ||
+        !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->ff_norm || !w->w_gate || !w->w_up ||
+        !w->w_down || !w->out_norm || !w->out_proj || !w->markov_w1 || !w->markov_w2 || !w->conf_w || !w->conf_b)
+        return fail(nullptr, DSPARK_ERR_INVALID_ARG, "a weight pointer is NULL");
+    for (int i = 0; i < nL; ++i)
+        if (!w->attn_norm[i] || !w->wq[i] || !w->wk[i] || !w->wv[i] || !w->wo[i] || !w->ff_norm[i] ||
+            !w->w_gate[i] || !w->w_up[i] || !w->w_down[i])
+            return fail(nullptr, DSPARK_ERR_INVALID_ARG, "layer " + std::to_string(i) + " has a NULL weight");
+
+    dspark_handle* h = new dspark_handle();
+    h->cfg = *cfg;
+    h->launches_at_create = launch_count();
+    cudaStream_t st = (cudaStream_t)stream;
+    auto bail = [&](dspark_status code) {
+        g_create_error = h->err;
+        dspark_destroy(h);
+        return code;
+    };
+#define CTRY(expr)                                                                                   \
+    do {                                                                                             \
+        cudaError_t _e = (expr);                                                                     \
+        if (_e != cudaSuccess) {                                                                     \
+            h->err = std::string(#expr) + ": " + cudaGetErrorString(_e);                             \
+            return bail(_e == cudaErrorMemoryAllocation ? DSPARK_ERR_OOM : DSPARK_ERR_CUDA);         \
+        }                                                                                            \
+    } while (0)
+    CTRY(cudaGetDevice(&h->device));
+    CTRY(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
+    h->dt = cfg->dtype == DSPARK_BF16 ? DT_BF16 : DT_F32;
+    h->esz = h->dt == DT_BF16 ? 2 : 4;
+    const int d = cfg->d_draft, F = cfg->ff_mult * d, H = cfg->hidden, V = cfg->vocab, r = cfg->markov_rank;
+    const size_t es = h->esz;
+    h->d = d;
+    h->F = F;
+    h->hd = d / cfg->n_heads;
+    h->mH = cfg->n_taps * H;
+    h->R = cfg->max_seqs * cfg->gamma;
+    const int R = h->R;
+
+    auto copy_mat = [&](void** dst, const void* src, size_t elems) -> cudaError_t {
+        cudaError_t e = dalloc(h, dst, elems * es);
+        if (e != cudaSuccess) return e;
+        return cudaMemcpyAsync(*dst, src, elems * es, cudaMemcpyDeviceToDevice, st);
+    };
+    auto copy_f32 = [&](float** dst, const float* src, size_t n) -> cudaError_t {
+        cudaError_t e = dalloc(h, (void**)dst, n * 4);
+        if (e != cudaSuccess) return e;
+        return cudaMemcpyAsync(*dst, src, n * 4, cudaMemcpyDeviceToDevice, st);
+    };
+    CTRY(copy_mat(&h->W_c, w->W_c, (size_t)d * h->mH));
+    CTRY(copy_f32(&h->ctx_norm, w->ctx_norm, d));
+    h->embed = w->embed;
+    CTRY(copy_mat(&h->tok_proj, w->tok_proj, (size_t)d * H));
+    CTRY(dalloc(h, (void**)&h->block_const, (size_t)cfg->gamma * d * 4));
+    CTRY(block_const_init(h->dt, cfg->gamma > 1 ? w->mask_emb : w->block_pos, w->block_pos, cfg->gamma, d,
+                          h->block_const, st));
+    h->wqkv.resize(nL);
+    h->wo.resize(nL);
+    h->wgu.resize(nL);
+    h->wd.resize(nL);
+    h->attn_norm.resize(nL);
+    h->ff_norm.resize(nL);
+    for (int i = 0; i < nL; ++i) {
+        const size_t dd = (size_t)d * d;
+        CTRY(dalloc(h, &h->wqkv[i], 3 * dd * es));
+        CTRY(cudaMemcpyAsync(h->wqkv[i], w->wq[i], dd * es, cudaMemcpyDeviceToDevice, st));
+        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + dd * es, w->wk[i], dd * es, cudaMemcpyDeviceToDevice, st));
+        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + 2 * dd * es, w->wv[i], dd * es, cudaMemcpyDeviceToDevice, st));
+        CTRY(copy_mat(&h->wo[i], w->wo[i], dd));
+        CTRY(dalloc(h, &h->wgu[i], 2 * (size_t)F * d * es));
+        CTRY(cudaMemcpy2DAsync(h->wgu[i], 2 * d * es, w->w_gate[i], d * es, d * es, F, cudaMemcpyDeviceToDevice, st));
+        CTRY(cudaMemcpy2DAsync((char*)h->wgu[i] + d * es, 2 * d * es, w->w_up[i], d * es, d * es, F,
+                               cudaMemcpyDeviceToDevice, st));
+        CTRY(copy_mat(&h->wd[i], w->w_down[i], (size_t)d * F));
+        CTRY(copy_f32(&h->attn_norm[i], w->attn_norm[i], d));
+        CTRY(copy_f32(&h->ff_norm[i], w->ff_norm[i], d));
+    }
+    CTRY(dalloc(h, (void**)&h->attn_norm_dev, sizeof(float*) * nL));
+    CTRY(cudaMemcpyAsync(h->attn_norm_dev, h->attn_norm.data(), sizeof(float*) * nL, cudaMemcpyHostToDevice, st));
+    CTRY(copy_f32(&h->out_norm, w->out_norm, d));
+    CTRY(copy_mat(&h->out_proj, w->out_proj, (size_t)V * d));
+    CTRY(copy_mat(&h->w1, w->markov_w1, (size_t)V * r));
+    CTRY(copy_mat(&h->w2, w->markov_w2, (size_t)V * r));
+    CTRY(dalloc(h, (void**)&h->conf_wb, (size_t)(d + r + 1) * 4));
+    CTRY(to_float(h->dt, w->conf_w, d + r, h->conf_wb, st));
+    CTRY(to_float(h->dt, w->conf_b, 1, h->conf_wb + d + r, st));
+
+    // caches
+    h->rows = (int64_t)cfg->max_ctx + cfg->gamma;
+    h->kv_off = h->rows * d;
+    h->seq_stride = 2 * h->kv_off;
+    h->layer_stride = h->seq_stride * cfg->max_seqs;
+    CTRY(dalloc(h, &h->cache, (size_t)h->layer_stride * nL * es));
+    CTRY(dalloc(h, (void**)&h->d_len, sizeof(int) * cfg->max_seqs));
+    CTRY(cudaMemsetAsync(h->d_len, 0, sizeof(int) * cfg->max_seqs, st));
+    CTRY(dalloc(h, (void**)&h->d_err, sizeof(int)));
+    CTRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), st));
+    h->len_host.assign(cfg->max_seqs, 0);
+    h->len_known.assign(cfg->max_seqs, 1);
+
+    // draft workspaces
+    const int wide = std::max(d, F);
+    CTRY(dalloc(h, (void**)&h->x, (size_t)R * d * 4));
+    CTRY(dalloc(h, (void**)&h->act, (size_t)R * wide * 4));
+    CTRY(dalloc(h, (void**)&h->hbuf, (size_t)R * F * 4));
+    CTRY(dalloc(h, (void**)&h->q, (size_t)R * d * 4));
+    CTRY(dalloc(h, (void**)&h->y, (size_t)R * d * 4));
+    CTRY(dalloc(h, (void**)&h->U, (size_t)R * V * 4));
+    CTRY(dalloc(h, &h->act_lp, (size_t)R * wide * 2));
+    CTRY(dalloc(h, &h->h_lp, (size_t)R * F * 2));
+    {
+        size_t worst = 0;
+        for (int B : {1, cfg->max_seqs}) {
+            int ch = attn_chunks(h, B, cfg->max_ctx + cfg->gamma);
+            worst = std::max(worst, attn_scratch_floats(B, cfg->n_heads, ch, cfg->gamma, h->hd));
+        }
+        h->attn_part_floats = worst;
+        CTRY(dalloc(h, (void**)&h->attn_part, worst * 4));
+    }
+    h->mk_ctas = markov_ctas(V);
+    CTRY(dalloc(h, (void**)&h->mk_v, (size_t)cfg->max_seqs * h->mk_ctas * 4));
+    CTRY(dalloc(h, (void**)&h->mk_i, (size_t)cfg->max_seqs * h->mk_ctas * 4));
+    CTRY(dalloc(h, (void**)&h->mk_cnt, (size_t)cfg->max_seqs * 4));
+    CTRY(dalloc(h, (void**)&h->safe_ids, (size_t)cfg->max_seqs * 4));
+    CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));
+    CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
+    h->ws_floats = (size_t)4 << 20;
+    CTRY(dalloc(h, (void**)&h->ws, h->ws_floats * 4));
+    // ingest workspaces
+    h->ingest_rows = std::max(1, std::min(std::max(cfg->max_ctx, 16), 16384));
+    CTRY(dalloc(h, (void**)&h->P, (size_t)h->ingest_rows * d * 4));
+    CTRY(dalloc(h, &h->Nbuf, (size_t)nL * h->ingest_rows * d * es));
+
+    // tensor-core views of the big weights (bf16 only)
+    if (h->dt == DT_BF16 && tc_available()) {
+        CTRY(tc_prepare(h->tc_wc, h->W_c, d, h->mH));
+        CTRY(tc_prepare(h->tc_out_proj, h->out_proj, V, d));
+        h->tc_kv.resize(nL);
+        h->tc_qkv.resize(nL);
+        h->tc_wo.resize(nL);
+        h->tc_wgu.resize(nL);
+        h->tc_wd.resize(nL);
+        for (int i = 0; i < nL; ++i) {
+            CTRY(tc_prepare(h->tc_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * d, d));
+            CTRY(tc_prepare(h->tc_qkv[i], h->wqkv[i], 3 * d, d));
+            CTRY(tc_prepare(h->tc_wo[i], h->wo[i], d, d));
+            CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));
+            CTRY(tc_prepare(h->tc_wd[i], h->wd[i], d, F));
+        }
+    }
+    CTRY(cudaStreamSynchronize(st));
+#undef CTRY
+    *out = h;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_ingest_context(dspark_handle* h, const void* feats_dev, int32_t T, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0) return fail(h, DSPARK_ERR_INVALID_ARG, "T < 0");
+    if (T == 0) return DSPARK_OK;
+    if (!feats_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "feats is NULL");
+    dspark_status s = sync_len(h, 0);
+    if (s != DSPARK_OK) return s;
+    if ((int64_t)h->len_host[0] + T > h->cfg.max_ctx)
+        return fail(h, DSPARK_ERR_CAPACITY, "context would exceed max_ctx (" + std::to_string(h->len_host[0]) + " + " +
+                                                std::to_string(T) + " > " + std::to_string(h->cfg.max_ctx) + ")");
+    s = ingest_rows(h, feats_dev, T, nullptr, nullptr, (cudaStream_t)stream);
+    if (s != DSPARK_OK) return s;
+    h->len_host[0] += T;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens_dev, float* conf_dev,
+                           float* logits_dev, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (!tokens_dev || !conf_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "tokens or conf is NULL");
+    if (last_token < 0 || last_token >= h->cfg.vocab)
+        return fail(h, DSPARK_ERR_INVALID_ARG, "last_token " + std::to_string(last_token) + " outside [0, vocab)");
+    dspark_status s = sync_len(h, 0);
+    if (s != DSPARK_OK) return s;
+    return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
+                      logits_dev, (cudaStream_t)stream);
+}
+
+dspark_status dspark_ingest_context_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,
+                                            const int32_t* cu_tokens_dev, const void* feats_dev, int32_t total_tokens,
+                                            void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (n_seqs < 0 || total_tokens < 0) return fail(h, DSPARK_ERR_INVALID_ARG, "negative count");
+    if (n_seqs == 0 || total_tokens == 0) return DSPARK_OK;
+    if (n_seqs > h->cfg.max_seqs) return fail(h, DSPARK_ERR_CAPACITY, "n_seqs > max_seqs");
+    if (!seq_ids_dev || !cu_tokens_dev || !feats_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "a pointer is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    CUDA_TRY(h, grow(h->rowmap, (size_t)total_tokens * 2 * sizeof(int)));
+    int* row_seq = (int*)h->rowmap.p;
+    int* row_pos = row_seq + total_tokens;
+    CUDA_TRY(h, ingest_rowmap(seq_ids_dev, cu_tokens_dev, n_seqs, total_tokens, h->d_len, h->cfg.max_seqs,
+                              h->cfg.max_ctx, row_seq, row_pos, h->d_err, st));
+    dspark_status s = ingest_rows(h, feats_dev, total_tokens, row_seq, row_pos, st);
+    if (s != DSPARK_OK) return s;
+    CUDA_TRY(h, ingest_commit(seq_ids_dev, cu_tokens_dev, n_seqs, h->d_len, h->cfg.max_seqs, h->cfg.max_ctx, st));
+    std::fill(h->len_known.begin(), h->len_known.end(), 0);
+    return DSPARK_OK;
+}
+
+dspark_status dspark_draft_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,
+                                   const int32_t* last_tokens_dev, int32_t* tokens_dev, float* conf_dev,
+                                   float* logits_dev, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (n_seqs < 0) return fail(h, DSPARK_ERR_INVALID_ARG, "n_seqs < 0");
+    if (n_seqs == 0) return DSPARK_OK;
+    if (n_seqs > h->cfg.max_seqs) return fail(h, DSPARK_ERR_CAPACITY, "n_seqs > max_seqs");
+    if (!seq_ids_dev || !last_tokens_dev || !tokens_dev || !conf_dev)
+        return fail(h, DSPARK_ERR_INVALID_ARG, "a pointer is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    CUDA_TRY(h, check_draft_inputs(seq_ids_dev, last_tokens_dev, n_seqs, h->cfg.max_seqs, h->cfg.vocab, h->d_err,
+                                   h->safe_ids, h->safe_anchors, st));
+    return draft_rows(h, n_seqs, h->safe_ids, h->safe_anchors, 0, h->cfg.max_ctx + h->cfg.gamma, tokens_dev, conf_dev,
+                      logits_dev, st);
+}
+
+dspark_status dspark_ingest_context_host(dspark_handle* h, const void* feats_host, int32_t T, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0) return fail(h, DSPARK_ERR_INVALID_ARG, "T < 0");
+    if (T == 0) return DSPARK_OK;
+    if (!feats_host) return fail(h, DSPARK_ERR_INVALID_ARG, "feats is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t bytes = (size_t)T * h->mH * h->esz;
+    CUDA_TRY(h, grow(h->stage_in, bytes));
+    CUDA_TRY(h, cudaMemcpyAsync(h->stage_in.p, feats_host, bytes, cudaMemcpyHostToDevice, st));
+    dspark_status s = dspark_ingest_context(h, h->stage_in.p, T, stream);
+    if (s != DSPARK_OK) return s;
+    CUDA_TRY(h, cudaStreamSynchronize(st));
+    return DSPARK_OK;
+}
+
+dspark_status dspark_draft_host(dspark_handle* h, int32_t last_token, int32_t* tokens_host, float* conf_host,
+                                float* logits_host, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (!tokens_host || !conf_host) return fail(h, DSPARK_ERR_INVALID_ARG, "tokens or conf is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int g = h->cfg.gamma;
+    const size_t lbytes = logits_host ? (size_t)g * h->cfg.vocab * 4 : 0;
+    CUDA_TRY(h, grow(h->stage_out, (size_t)g * 8 + 256 + lbytes));
+    int* tok = (int*)h->stage_out.p;
+    float* cf = (float*)((char*)h->stage_out.p + 128);
+    float* lg = logits_host ? (float*)((char*)h->stage_out.p + 256) : nullptr;
+    dspark_status s = dspark_draft(h, last_token, tok, cf, lg, stream);
+    if (s != DSPARK_OK) return s;
+    CUDA_TRY(h, cudaMemcpyAsync(tokens_host, tok, (size_t)g * 4, cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(h, cudaMemcpyAsync(conf_host, cf, (size_t)g * 4, cudaMemcpyDeviceToHost, st));
+    if (logits_host) CUDA_TRY(h, cudaMemcpyAsync(logits_host, lg, lbytes, cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(h, cudaStreamSynchronize(st));
+    return DSPARK_OK;
+}
+
+dspark_status dspark_reset(dspark_handle* h, int32_t seq_id, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (seq_id < 0 || seq_id >= h->cfg.max_seqs) return fail(h, DSPARK_ERR_INVALID_ARG, "seq_id out of range");
+    CUDA_TRY(h, set_len(h->d_len, seq_id, 0, (cudaStream_t)stream));
+    h->len_host[seq_id] = 0;
+    h->len_known[seq_id] = 1;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_check(dspark_handle* h, int32_t* word_host) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    int v = 0;
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    CUDA_TRY(h, cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(h, cudaMemset(h->d_err, 0, sizeof(int)));
+    if (word_host) *word_host = v;
+    if (v) return fail(h, DSPARK_ERR_DEVICE, "device error word " + std::to_string(v));
+    return DSPARK_OK;
+}
+
+dspark_status dspark_context_length(dspark_handle* h, int32_t seq_id, int32_t* out_host) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (!out_host) return fail(h, DSPARK_ERR_INVALID_ARG, "out is NULL");
+    if (seq_id < 0 || seq_id >= h->cfg.max_seqs) return fail(h, DSPARK_ERR_INVALID_ARG, "seq_id out of range");
+    int v = 0, e = 0;
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    CUDA_TRY(h, cudaMemcpy(&v, h->d_len + seq_id, sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(h, cudaMemcpy(&e, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+    *out_host = v;
+    h->len_host[seq_id] = v;
+    h->len_known[seq_id] = 1;
+    if (e) return fail(h, DSPARK_ERR_DEVICE, "device error word " + std::to_string(e));
+    return DSPARK_OK;
+}
+
+dspark_status dspark_get_cache(dspark_handle* h, int32_t seq_id, int32_t layer, const void** k_dev,
+                               const void** v_dev) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (seq_id < 0 || seq_id >= h->cfg.max_seqs || layer < 0 || layer >= h->cfg.n_layers)
+        return fail(h, DSPARK_ERR_INVALID_ARG, "seq_id or layer out of range");
+    const char* base = (const char*)h->cache + ((size_t)layer * h->layer_stride + (size_t)seq_id * h->seq_stride) * h->esz;
+    if (k_dev) *k_dev = base;
+    if (v_dev) *v_dev = base + (size_t)h->kv_off * h->esz;
+    return DSPARK_OK;
+}
+
+}  // extern "C"

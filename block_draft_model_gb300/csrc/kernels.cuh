@@ -1,0 +1,141 @@
+// Internal launchers of the drafter kernels (host side).  Every launcher
+// enqueues on `st` and returns cudaGetLastError() of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dspark {
+
+enum DType { DT_BF16 = 0, DT_F32 = 1 };
+
+// ------------------------------------------------------------------ GEMM epilogues
+// Every GEMM here computes acc[m, n] = sum_k A[m, k] * W[n, k] (W is [N, K],
+// K contiguous) and hands acc to one of these epilogues.
+enum EpiKind {
+    EPI_STORE_F32 = 0,  // out_f32[m * ldo + n] = acc
+    EPI_ADD_F32 = 1,    // out_f32[m * ldo + n] += acc            (residual add)
+    EPI_SWIGLU = 2,     // columns come in (gate, up) pairs: out_act[m * ld_act + n/2] = act(gate) * up
+    EPI_KV_CACHE = 3,   // columns [0, d) -> K cache, [d, 2d) -> V cache, row -> (seq, position)
+    EPI_QKV = 4,        // columns [0, d) -> out_f32 (Q), [d, 2d) -> K cache, [2d, 3d) -> V cache
+};
+
+struct EpiParams {
+    int kind = EPI_STORE_F32;
+    float* out_f32 = nullptr;
+    int64_t ldo = 0;
+    void* out_act = nullptr;     // EPI_SWIGLU output, element type act_dtype
+    int act_dtype = DT_F32;
+    int64_t ld_act = 0;
+    int act = 0;                 // 0 SiLU, 1 tanh-GELU
+    // cache epilogues
+    void* cache = nullptr;       // layer base: K of seq s at cache + s*seq_stride, V at + kv_off
+    int cache_dtype = DT_BF16;
+    int64_t seq_stride = 0;      // elements between sequences
+    int64_t kv_off = 0;          // elements from K to V of one sequence
+    int d = 0;
+    int max_rows = 0;            // rows per sequence cache (positions must be < max_rows)
+    const int* row_seq = nullptr;  // EPI_KV_CACHE: sequence slot per GEMM row (nullptr: slot 0)
+    const int* row_pos = nullptr;  // EPI_KV_CACHE: position per GEMM row, -1 = drop (nullptr: len[slot] + m)
+    const int* seq_len = nullptr;  // device context lengths per slot
+    int gamma = 1;                 // EPI_QKV: GEMM row m is block row m % gamma of sequence m / gamma
+    const int* seq_ids = nullptr;  // EPI_QKV: slot of sequence b (nullptr: slot b)
+};
+
+// Generic tiled SIMT GEMM (fp32 FMA), any M, N, K.  A rows may be gathered:
+// A row m is at A + (a_rows ? a_rows[m] : m) * lda.
+cudaError_t gemm_simt(int a_dtype, const void* A, int64_t lda, const int* a_rows, int w_dtype, const void* W,
+                      int M, int N, int K, const EpiParams& ep, cudaStream_t st);
+
+// Weight-streaming GEMM for M <= 16 activation rows: W is read once from HBM
+// with 16-byte non-allocating loads, fp32 FMA.  A (fp32, or w_dtype when
+// a_dtype says so) row m is at A + (a_rows ? a_rows[m] : a_row0 + m) * lda.
+// K must be a multiple of 8.  When the rows of W alone cannot fill the GPU, K
+// is split over CTAs; the partial sums go to `ws` (ws_floats capacity) and are
+// added in a fixed order, so results do not depend on scheduling.
+bool skinny_ok(int M, int K);
+cudaError_t gemm_skinny(int a_dtype, const void* A, int64_t lda, const int* a_rows, int a_row0, int w_dtype,
+                        const void* W, int M, int N, int K, const EpiParams& ep, float* ws, size_t ws_floats,
+                        int num_sms, cudaStream_t st);
+
+// ------------------------------------------------------------------ norms and block set-up
+// out[r] = x[r] / sqrt(mean(x[r]^2) + eps) * w   (rows of length n, x fp32)
+cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, int n, float eps, int out_dtype,
+                         void* out, int64_t ldo, cudaStream_t st);
+
+// Ingest normalisation: H = RMSNorm(P) * ctx_norm, then for each layer i
+// N_i = RMSNorm(H) * attn_norm_i, written to out + i * layer_stride (out_dtype).
+cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
+                        const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
+                        int64_t layer_stride, cudaStream_t st);
+
+// x[b * gamma + j] = block_const[j] for b < B, j < gamma (fp32).
+cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st);
+// block_const[0] = block_pos[0]; block_const[j] = mask_emb[j-1] + block_pos[j] (fp32 out).
+cudaError_t block_const_init(int dtype, const void* mask_emb, const void* block_pos, int gamma, int d, float* out,
+                             cudaStream_t st);
+// out[i] = float(in[i]) for n elements of dtype.
+cudaError_t to_float(int dtype, const void* in, int64_t n, float* out, cudaStream_t st);
+
+// Kernel launches issued by this library so far (all handles); for accounting.
+long long launch_count();
+void note_launch(int n = 1);
+
+// ------------------------------------------------------------------ attention
+struct AttnParams {
+    const float* q;          // [B*gamma, d], row b*gamma + j
+    const void* cache;       // layer base (see EpiParams)
+    int cache_dtype;
+    int64_t seq_stride, kv_off;
+    const int* seq_len;      // context length per slot (block rows sit at len .. len+gamma-1)
+    const int* seq_ids;      // slot of sequence b (nullptr: b)
+    int B, gamma, d, n_heads;
+    int n_chunks;            // split of the (len + gamma) keys of one sequence
+    float* part;             // scratch: B * n_heads * n_chunks * gamma * (head_dim + 2) floats
+    void* out;               // [B*gamma, d] attention output, out_dtype
+    int out_dtype;
+};
+size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim);
+cudaError_t attention(const AttnParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ Markov chain, argmax, confidence
+struct MarkovParams {
+    const float* U;          // [B*gamma, V] base logits
+    const void* w1;          // [V, r], w_dtype
+    const void* w2;          // [V, r], w_dtype
+    int w_dtype;
+    const float* y;          // [B*gamma, d] out-normed block rows
+    const float* conf_w;     // [d + r + 1] fp32: weight, then the bias
+    int B, gamma, V, r, d;
+    int k;                   // block position
+    const int* anchors;      // [B] device, or nullptr: use `anchor`
+    int anchor;
+    int* tokens;             // [B, gamma]
+    float* conf;             // [B, gamma]
+    float* logits;           // [B, gamma, V] or nullptr
+    float* part_v;           // scratch: B * ctas floats
+    int* part_i;             // scratch: B * ctas ints
+    unsigned int* counters;  // scratch: B counters, zero between launches
+    int* err;                // device error word
+    int ctas;                // CTAs per sequence over V
+};
+int markov_ctas(int V);
+cudaError_t markov_step(const MarkovParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ bookkeeping kernels
+// For a batched ingest: per feature row t, its slot and cache position
+// (len[slot] + t - cu[i]); -1 and an error bit if over capacity or bad id.
+cudaError_t ingest_rowmap(const int* seq_ids, const int* cu, int n_seqs, int total, const int* seq_len,
+                          int max_seqs, int max_ctx, int* row_seq, int* row_pos, int* err, cudaStream_t st);
+// len[slot] += cu[i+1] - cu[i] for sequences whose rows were all accepted.
+cudaError_t ingest_commit(const int* seq_ids, const int* cu, int n_seqs, int* seq_len, int max_seqs, int max_ctx,
+                          cudaStream_t st);
+cudaError_t add_len(int* seq_len, int slot, int delta, cudaStream_t st);
+cudaError_t set_len(int* seq_len, int slot, int value, cudaStream_t st);
+// Validate batched draft inputs: ids in [0, max_seqs), anchors in [0, V).
+// Bad entries set err bits; safe_ids gets -1 for a bad id (the sequence is then
+// skipped by every kernel) and safe_anchors the anchor clamped into [0, V).
+cudaError_t check_draft_inputs(const int* seq_ids, const int* anchors, int n, int max_seqs, int V, int* err,
+                               int* safe_ids, int* safe_anchors, cudaStream_t st);
+
+}  // namespace dspark

@@ -1,0 +1,164 @@
+// One position k of the sequential Markov chain ("module-dflash.ts",
+// forwardInfer / #markov / #confidence; "src/dspark-runtime.js", propose:
+// markovEmbed, markov, addBias, argmax, argmaxFinal):
+//   e       = w1[prev]            prev = anchor (k = 0) or the token drafted at k-1
+//   logits  = U_k + w2 e          (w2 stored [V, r], one row per vocabulary entry)
+//   token_k = argmax logits       (lowest index on ties)
+//   conf_k  = sigmoid(conf_w . [y_k ; e] + conf_b)
+// One fused launch per position: every CTA streams a slice of w2, adds the
+// base logits, keeps its best (value, index); the last CTA to finish (ticket
+// counter, no spinning) reduces the CTA results in a fixed order, writes the
+// token and the confidence, and re-arms the counter.  The token stays on the
+// device, where the next position's launch reads it.
+#include <climits>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int NT = 256;
+constexpr int RW = 4;          // rows per warp in flight
+constexpr int RMAX = 1024;     // largest Markov rank
+
+template <typename TW>
+__global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
+    constexpr int VE = Vec16<TW>::N;
+    __shared__ __align__(16) float e[RMAX];
+    __shared__ float red_v[NT / 32];
+    __shared__ int red_i[NT / 32];
+    __shared__ int is_last;
+    __shared__ float redf[32];
+
+    const int b = blockIdx.y, k = p.k, r = p.r, V = p.V;
+    int prev = (k == 0) ? (p.anchors ? p.anchors[b] : p.anchor) : p.tokens[b * p.gamma + k - 1];
+    prev = min(max(prev, 0), V - 1);
+    const TW* w1 = reinterpret_cast<const TW*>(p.w1);
+    const TW* w2 = reinterpret_cast<const TW*>(p.w2);
+    for (int c = threadIdx.x; c < r; c += NT) e[c] = to_f32(w1[(int64_t)prev * r + c]);
+    __syncthreads();
+
+    const int rows = (V + gridDim.x - 1) / gridDim.x;
+    const int v_begin = blockIdx.x * rows, v_end = min(V, v_begin + rows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t urow = (int64_t)(b * p.gamma + k) * V;
+    const int nvec = r / VE;
+
+    ArgBest best{-INFINITY, INT_MAX};
+    for (int v0 = v_begin + warp * RW; v0 < v_end; v0 += (NT / 32) * RW) {
+        float acc[RW];
+#pragma unroll
+        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+        for (int vi = lane; vi < nvec; vi += 32) {
+            uint4 u[RW];
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                const int v = min(v0 + i, v_end - 1);
+                u[i] = ld_stream16(w2 + (int64_t)v * r + vi * VE);
+            }
+            const float* ep = e + vi * VE;
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                float f[VE];
+                Vec16<TW>::unpack(u[i], f);
+#pragma unroll
+                for (int q = 0; q < VE; ++q) acc[i] = fmaf(f[q], ep[q], acc[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            const float bias = warp_sum(acc[i]);
+            const int v = v0 + i;
+            if (v < v_end) {
+                const float l = p.U[urow + v] + bias;
+                if (p.logits && lane == 0) p.logits[urow + v] = l;
+                if (better(l, v, best.v, best.i)) {
+                    best.v = l;
+                    best.i = v;
+                }
+            }
+        }
+    }
+    best = warp_argbest(best);
+    if (lane == 0) {
+        red_v[warp] = best.v;
+        red_i[warp] = best.i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ArgBest cb{-INFINITY, INT_MAX};
+        for (int w = 0; w < NT / 32; ++w)
+            if (better(red_v[w], red_i[w], cb.v, cb.i)) {
+                cb.v = red_v[w];
+                cb.i = red_i[w];
+            }
+        p.part_v[b * gridDim.x + blockIdx.x] = cb.v;
+        p.part_i[b * gridDim.x + blockIdx.x] = cb.i;
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&p.counters[b], 1u);
+        is_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // last CTA of this sequence: fixed-order reduction of the CTA results
+    ArgBest fb{-INFINITY, INT_MAX};
+    for (int c = threadIdx.x; c < (int)gridDim.x; c += NT) {
+        const float v = __ldcg(p.part_v + b * gridDim.x + c);
+        const int i = __ldcg(p.part_i + b * gridDim.x + c);
+        if (better(v, i, fb.v, fb.i)) {
+            fb.v = v;
+            fb.i = i;
+        }
+    }
+    fb = warp_argbest(fb);
+    if (lane == 0) {
+        red_v[warp] = fb.v;
+        red_i[warp] = fb.i;
+    }
+    // confidence: sigmoid(conf_w . [y_k ; e] + conf_b)
+    const float* yr = p.y + (int64_t)(b * p.gamma + k) * p.d;
+    float z = 0.f;
+    for (int c = threadIdx.x; c < p.d; c += NT) z = fmaf(yr[c], p.conf_w[c], z);
+    for (int c = threadIdx.x; c < r; c += NT) z = fmaf(e[c], p.conf_w[p.d + c], z);
+    z = block_sum(z, redf);  // contains __syncthreads, so red_v/red_i are complete
+    if (threadIdx.x == 0) {
+        ArgBest tb{-INFINITY, INT_MAX};
+        for (int w = 0; w < NT / 32; ++w)
+            if (better(red_v[w], red_i[w], tb.v, tb.i)) {
+                tb.v = red_v[w];
+                tb.i = red_i[w];
+            }
+        int tok = tb.i;
+        if (tok == INT_MAX || !(tb.v > -INFINITY)) {
+            atomicOr(p.err, 8);
+            tok = 0;
+        }
+        p.tokens[b * p.gamma + k] = tok;
+        p.conf[b * p.gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + r])));
+        p.counters[b] = 0u;
+    }
+}
+
+}  // namespace
+
+int markov_ctas(int V) {
+    int c = (V + 511) / 512;
+    return c < 1 ? 1 : (c > 1024 ? 1024 : c);
+}
+
+cudaError_t markov_step(const MarkovParams& p, cudaStream_t st) {
+    if (p.r > RMAX || p.r % 8 != 0) return cudaErrorInvalidValue;
+    dim3 grid(p.ctas, p.B);
+    if (p.w_dtype == DT_BF16)
+        k_markov<bf16><<<grid, NT, 0, st>>>(p);
+    else
+        k_markov<float><<<grid, NT, 0, st>>>(p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,241 @@
+// Row normalisations, block set-up and per-sequence bookkeeping kernels.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int NT = 256;
+
+template <typename TO>
+__global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x, int64_t ldx,
+                                                     const float* __restrict__ w, int n, float eps, TO* out,
+                                                     int64_t ldo) {
+    __shared__ float red[32];
+    const float* xr = x + (int64_t)blockIdx.x * ldx;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < n; c += NT) {
+        float v = xr[c];
+        ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float s = rsqrtf(ss / (float)n + eps);
+    TO* o = out + (int64_t)blockIdx.x * ldo;
+    for (int c = threadIdx.x; c < n; c += NT) o[c] = from_f32<TO>(xr[c] * s * w[c]);
+}
+
+// One CTA per context row: H = RMSNorm(P) * ctx_norm (kept in shared memory),
+// then every layer's normalised copy RMSNorm(H) * attn_norm_i.
+template <typename TO>
+__global__ void __launch_bounds__(NT) k_ingest_norm(const float* __restrict__ P, int d, float eps,
+                                                    const float* __restrict__ ctx_norm,
+                                                    const float* const* __restrict__ attn_norm, int n_layers, TO* out,
+                                                    int64_t layer_stride) {
+    extern __shared__ float h[];
+    __shared__ float red[32];
+    const float* pr = P + (int64_t)blockIdx.x * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += NT) {
+        float v = pr[c];
+        ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float s1 = rsqrtf(ss / (float)d + eps);
+    float ss2 = 0.f;
+    for (int c = threadIdx.x; c < d; c += NT) {
+        float v = pr[c] * s1 * ctx_norm[c];
+        h[c] = v;
+        ss2 = fmaf(v, v, ss2);
+    }
+    ss2 = block_sum(ss2, red);
+    const float s2 = rsqrtf(ss2 / (float)d + eps);
+    for (int i = 0; i < n_layers; ++i) {
+        const float* an = attn_norm[i];
+        TO* o = out + i * layer_stride + (int64_t)blockIdx.x * d;
+        for (int c = threadIdx.x; c < d; c += NT) o[c] = from_f32<TO>(h[c] * s2 * an[c]);
+    }
+}
+
+__global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc, int B, int gamma, int d) {
+    const int64_t total = (int64_t)B * gamma * d, per = (int64_t)gamma * d;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+        x[i] = bc[i % per];
+}
+
+__global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int total,
+                                const int* __restrict__ seq_len, int max_seqs, int max_ctx, int* row_seq, int* row_pos,
+                                int* err) {
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+        // sequence i with cu[i] <= t < cu[i+1] (binary search over the prefix sums)
+        int lo = 0, hi = n_seqs - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const int sid = seq_ids[lo];
+        if (sid < 0 || sid >= max_seqs) {
+            row_seq[t] = 0;
+            row_pos[t] = -1;
+            atomicOr(err, 2);
+            continue;
+        }
+        const int cnt = cu[lo + 1] - cu[lo];
+        const int len = seq_len[sid];
+        row_seq[t] = sid;
+        if (len + cnt > max_ctx) {
+            row_pos[t] = -1;
+            if (t == cu[lo]) atomicOr(err, 4);
+        } else {
+            row_pos[t] = len + (t - cu[lo]);
+        }
+    }
+}
+
+__global__ void k_ingest_commit(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int* seq_len,
+                                int max_seqs, int max_ctx) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seqs; i += gridDim.x * blockDim.x) {
+        const int sid = seq_ids[i];
+        if (sid < 0 || sid >= max_seqs) continue;
+        const int cnt = cu[i + 1] - cu[i];
+        if (seq_len[sid] + cnt <= max_ctx) seq_len[sid] += cnt;
+    }
+}
+
+__global__ void k_add_len(int* seq_len, int slot, int delta) { seq_len[slot] += delta; }
+__global__ void k_set_len(int* seq_len, int slot, int value) { seq_len[slot] = value; }
+
+__global__ void k_check_draft(const int* __restrict__ seq_ids, const int* __restrict__ anchors, int n, int max_seqs,
+                              int V, int* err, int* safe_ids, int* safe_anchors) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int sid = seq_ids[i];
+        const bool bad_id = sid < 0 || sid >= max_seqs;
+        if (bad_id) atomicOr(err, 2);
+        safe_ids[i] = bad_id ? -1 : sid;
+        const int a = anchors[i];
+        if (a < 0 || a >= V) atomicOr(err, 1);
+        safe_anchors[i] = min(max(a, 0), V - 1);
+    }
+}
+
+template <typename T>
+__global__ void k_block_const(const T* __restrict__ mask_emb, const T* __restrict__ block_pos, int gamma, int d,
+                              float* __restrict__ out) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < gamma * d; i += gridDim.x * blockDim.x) {
+        const int j = i / d;
+        float v = to_f32(block_pos[i]);
+        if (j > 0) v += to_f32(mask_emb[i - d]);
+        out[i] = v;
+    }
+}
+
+template <typename T>
+__global__ void k_to_float(const T* __restrict__ in, int64_t n, float* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = to_f32(in[i]);
+}
+
+}  // namespace
+
+static long long g_launches = 0;
+long long launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+void note_launch(int n) { __atomic_fetch_add(&g_launches, (long long)n, __ATOMIC_RELAXED); }
+
+cudaError_t block_const_init(int dtype, const void* mask_emb, const void* block_pos, int gamma, int d, float* out,
+                             cudaStream_t st) {
+    const int blocks = std::max(1, std::min((gamma * d + 255) / 256, 1024));
+    if (dtype == DT_BF16)
+        k_block_const<bf16><<<blocks, 256, 0, st>>>((const bf16*)mask_emb, (const bf16*)block_pos, gamma, d, out);
+    else
+        k_block_const<float><<<blocks, 256, 0, st>>>((const float*)mask_emb, (const float*)block_pos, gamma, d, out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t to_float(int dtype, const void* in, int64_t n, float* out, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024));
+    if (dtype == DT_BF16)
+        k_to_float<bf16><<<blocks, 256, 0, st>>>((const bf16*)in, n, out);
+    else
+        k_to_float<float><<<blocks, 256, 0, st>>>((const float*)in, n, out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, int n, float eps, int out_dtype,
+                         void* out, int64_t ldo, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (out_dtype == DT_BF16)
+        k_rmsnorm_rows<bf16><<<rows, NT, 0, st>>>(x, ldx, w, n, eps, (bf16*)out, ldo);
+    else
+        k_rmsnorm_rows<float><<<rows, NT, 0, st>>>(x, ldx, w, n, eps, (float*)out, ldo);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
+                        const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
+                        int64_t layer_stride, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    size_t sm = (size_t)d * sizeof(float);
+    if (out_dtype == DT_BF16)
+        k_ingest_norm<bf16><<<rows, NT, sm, st>>>(P, d, eps, ctx_norm, attn_norm_dev, n_layers, (bf16*)out,
+                                                  layer_stride);
+    else
+        k_ingest_norm<float><<<rows, NT, sm, st>>>(P, d, eps, ctx_norm, attn_norm_dev, n_layers, (float*)out,
+                                                   layer_stride);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st) {
+    int64_t total = (int64_t)B * gamma * d;
+    int blocks = (int)std::min<int64_t>((total + 255) / 256, 1024);
+    k_block_init<<<blocks, 256, 0, st>>>(x, block_const, B, gamma, d);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t ingest_rowmap(const int* seq_ids, const int* cu, int n_seqs, int total, const int* seq_len, int max_seqs,
+                          int max_ctx, int* row_seq, int* row_pos, int* err, cudaStream_t st) {
+    if (total <= 0) return cudaSuccess;
+    int blocks = std::min((total + 255) / 256, 1024);
+    k_ingest_rowmap<<<blocks, 256, 0, st>>>(seq_ids, cu, n_seqs, total, seq_len, max_seqs, max_ctx, row_seq, row_pos,
+                                            err);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t ingest_commit(const int* seq_ids, const int* cu, int n_seqs, int* seq_len, int max_seqs, int max_ctx,
+                          cudaStream_t st) {
+    if (n_seqs <= 0) return cudaSuccess;
+    k_ingest_commit<<<(n_seqs + 255) / 256, 256, 0, st>>>(seq_ids, cu, n_seqs, seq_len, max_seqs, max_ctx);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t add_len(int* seq_len, int slot, int delta, cudaStream_t st) {
+    k_add_len<<<1, 1, 0, st>>>(seq_len, slot, delta);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t set_len(int* seq_len, int slot, int value, cudaStream_t st) {
+    k_set_len<<<1, 1, 0, st>>>(seq_len, slot, value);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t check_draft_inputs(const int* seq_ids, const int* anchors, int n, int max_seqs, int V, int* err,
+                               int* safe_ids, int* safe_anchors, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    k_check_draft<<<(n + 255) / 256, 256, 0, st>>>(seq_ids, anchors, n, max_seqs, V, err, safe_ids, safe_anchors);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

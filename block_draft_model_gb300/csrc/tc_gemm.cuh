@@ -1,0 +1,27 @@
+// Tensor-core GEMM (tcgen05 + TMA + TMEM) for bf16 operands:
+// acc[m, n] = sum_k A[m, k] W[n, k], fp32 accumulation, GEMM epilogues of epilogue.cuh.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.cuh"
+
+namespace dspark {
+
+// A weight matrix W [N, K] (bf16, K contiguous) with its TMA descriptor.
+struct TcWeight {
+    bool ready = false;
+    const void* ptr = nullptr;
+    int N = 0, K = 0;
+    alignas(64) unsigned char tmap[128];
+};
+
+bool tc_available();
+cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K);
+void tc_release(TcWeight& w);
+bool tc_gemm_ok(int M, int N, int K);
+cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
+                    int num_sms, cudaStream_t st);
+
+}  // namespace dspark

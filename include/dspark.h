@@ -1,0 +1,216 @@
+/*
+ * dspark.h - C ABI of the GB300 DSpark/DFlash block drafter.
+ *
+ * The drafter reads the target model's hidden states at m tapped layers for
+ * every context token, keeps a per-layer context K/V cache, and drafts a block
+ * of gamma tokens in one parallel pass followed by a short sequential Markov
+ * chain.  Sources (by page and section):
+ *   "module-dflash.ts" (mlx-bun 0.0.7 -> 0.0.9): the header comment (Eq 2,
+ *       Eq 3), #buildContext, #buildBlock, #maskBias, #layer, #backbone,
+ *       #baseLogits, #markov, #confidence, forwardInfer, initFromDims;
+ *   "src/dspark-runtime.js" (minicpm5-2b-webgpu): updateContext (context
+ *       K/V computed once per token and stored per layer), propose (draft
+ *       step with the Markov chain and argmax kept on the device).
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev are CUDA device pointers on the handle's device;
+ *     pointers named *_host are host pointers (pageable or pinned).
+ *   - Matrices are row-major [out, in] (the input dimension is contiguous).
+ *   - "dtype" tensors are bf16 (raw 16-bit patterns) when cfg.dtype is
+ *     DSPARK_BF16 and IEEE float32 when it is DSPARK_FP32.  Norm vectors are
+ *     always float32.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device-pointer
+ *     calls are asynchronous on it and never synchronise the host; *_host calls
+ *     synchronise `stream` before they return.
+ *   - Errors the host can see (bad configuration, NULL pointer, token outside
+ *     [0, vocab), context over capacity) are returned at once and nothing is
+ *     launched.  Violations only the device can see (a batched token or
+ *     sequence id out of range, a batched context over capacity) set a device
+ *     error word; dspark_check() and dspark_context_length() report it as
+ *     DSPARK_ERR_DEVICE.  dspark_last_error() describes the last failure.
+ *   - A handle is not thread-safe; calls on one handle are ordered by the
+ *     caller.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = 1,  /* bad config, NULL pointer, token out of range          */
+    DSPARK_ERR_CAPACITY = 2,     /* context longer than max_ctx, too many sequences        */
+    DSPARK_ERR_CUDA = 3,         /* a CUDA runtime call failed (message in last_error)     */
+    DSPARK_ERR_UNSUPPORTED = 4,  /* shape outside what the kernels implement                */
+    DSPARK_ERR_TIMEOUT = 5,      /* a bounded device wait gave up                           */
+    DSPARK_ERR_OOM = 6,          /* device allocation failed                                */
+    DSPARK_ERR_DEVICE = 7        /* the device error word was set (see dspark_check)        */
+} dspark_status;
+
+typedef enum { DSPARK_BF16 = 0, DSPARK_FP32 = 1 } dspark_dtype;
+
+/* FFN activation of the gated FFN in #layer: SiLU(gate)*up (the "silu" kernel of
+ * "src/dspark-runtime.js", propose) or tanh-GELU(gate)*up (MLX geluApprox). */
+typedef enum { DSPARK_ACT_SILU = 0, DSPARK_ACT_GELU_TANH = 1 } dspark_act;
+
+/* Drafter dimensions: DflashConfig and TargetDims of "module-dflash.ts". */
+typedef struct dspark_config {
+    int32_t hidden;       /* H: target hidden size                                     */
+    int32_t n_taps;       /* m: tapped target layers; features are [T, m*H]             */
+    int32_t d_draft;      /* d: drafter width; multiple of 64                           */
+    int32_t n_heads;      /* d % n_heads == 0; head_dim = d / n_heads, <= 256, even     */
+    int32_t n_layers;     /* draft layers                                               */
+    int32_t ff_mult;      /* F = ff_mult * d                                            */
+    int32_t gamma;        /* block size, 1 <= gamma <= 16                               */
+    int32_t vocab;        /* V                                                          */
+    int32_t markov_rank;  /* r, multiple of 8, <= 1024                                  */
+    float eps;            /* RMSNorm epsilon                                            */
+    int32_t dtype;        /* dspark_dtype                                               */
+    int32_t act;          /* dspark_act                                                 */
+    int32_t max_ctx;      /* context capacity per sequence (tokens)                     */
+    int32_t max_seqs;     /* number of sequences with their own caches (>= 1)           */
+} dspark_config;
+
+/* Weights, as device pointers in cfg.dtype unless noted (norm vectors float32).
+ * Names follow buildNames of "module-dflash.ts"; shapes are [out, in]. */
+typedef struct dspark_weights {
+    const void* W_c;          /* [d, m*H]      Eq 2 projection                           */
+    const float* ctx_norm;    /* [d]                                                     */
+    const void* embed;        /* [V, H]        the target's token embedding (BORROWED:   */
+                              /*               must stay valid while the handle lives)   */
+    const void* tok_proj;     /* [d, H]                                                  */
+    const void* mask_emb;     /* [gamma-1, d]  (may be NULL when gamma == 1)             */
+    const void* block_pos;    /* [gamma, d]                                              */
+    const float* const* attn_norm;  /* host array of n_layers device pointers, each [d]  */
+    const void* const* wq;          /* ... each [d, d]                                   */
+    const void* const* wk;          /* ... each [d, d]                                   */
+    const void* const* wv;          /* ... each [d, d]                                   */
+    const void* const* wo;          /* ... each [d, d]                                   */
+    const float* const* ff_norm;    /* ... each [d]                                      */
+    const void* const* w_gate;      /* ... each [F, d]                                   */
+    const void* const* w_up;        /* ... each [F, d]                                   */
+    const void* const* w_down;      /* ... each [d, F]                                   */
+    const float* out_norm;    /* [d]                                                     */
+    const void* out_proj;     /* [V, d]        d -> vocab head                           */
+    const void* markov_w1;    /* [V, r]        previous-token factor (row gather)        */
+    const void* markov_w2;    /* [V, r]        vocab factor (bias = w2 . w1[prev])       */
+    const void* conf_w;       /* [d + r]       confidence head weight                    */
+    const void* conf_b;       /* [1]           confidence head bias                      */
+} dspark_weights;
+
+typedef struct dspark_handle dspark_handle;
+
+/* Create a drafter on the current CUDA device.  Copies and repacks every weight
+ * except `embed` into library-owned device memory (the caller may free them
+ * once this returns, after synchronising `stream`), and allocates the context
+ * caches: n_layers x max_seqs x 2 x (max_ctx + gamma) x d elements of dtype.
+ * Source: initFromDims / DflashDrafter constructor ("module-dflash.ts"), which
+ * also rejects d % n_heads != 0.  Returns DSPARK_ERR_INVALID_ARG for a bad
+ * config or NULL weight, DSPARK_ERR_UNSUPPORTED for shapes outside the limits
+ * above, DSPARK_ERR_OOM if the device is full.  *out is NULL on failure. */
+dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, void* stream,
+                            dspark_handle** out);
+
+/* Free every library-owned buffer.  Synchronises the device first.  NULL is a no-op. */
+void dspark_destroy(dspark_handle* h);
+
+/* Context ingest for sequence 0 (Eq 2 + Eq 3; "src/dspark-runtime.js"
+ * updateContext): for T new context rows feats_dev [T, m*H] (dtype, taps
+ * concatenated on the feature axis), compute H_ctx = RMSNorm(W_c x) * ctx_norm
+ * and, for every layer i, append W_k,i n and W_v,i n with
+ * n = RMSNorm(H_ctx) * attn_norm_i to the layer's cache.  T = 0 is a no-op.
+ * DSPARK_ERR_CAPACITY if the context would exceed max_ctx (nothing launched). */
+dspark_status dspark_ingest_context(dspark_handle* h, const void* feats_dev, int32_t T, void* stream);
+
+/* Draft one block for sequence 0 ("module-dflash.ts" forwardInfer, greedy):
+ * block rows (#buildBlock: tok_proj E[last_token] + block_pos[0], then
+ * mask_emb[j-1] + block_pos[j]), n_layers of #layer attending over
+ * [context ++ block] with no mask, out_norm, base logits U = out_proj y, then
+ * for k = 0..gamma-1: logits_k = U_k + w2 w1[prev_k] (prev_0 = last_token,
+ * prev_k = token_{k-1}), token_k = argmax (lowest index on ties),
+ * conf_k = sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b).
+ * Outputs: tokens_dev [gamma] int32, conf_dev [gamma] float, and, if not NULL,
+ * logits_dev [gamma, V] float.  The context is not modified. */
+dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens_dev, float* conf_dev,
+                           float* logits_dev, void* stream);
+
+/* Batched ingest: sequences seq_ids_dev[i] (i < n_seqs) receive the feature rows
+ * cu_tokens_dev[i] .. cu_tokens_dev[i+1]-1 of feats_dev [total_tokens, m*H]
+ * (cu_tokens_dev: n_seqs+1 prefix sums, cu[0] = 0, cu[n] = total_tokens).  Each
+ * sequence is ingested exactly as dspark_ingest_context would.  Sequence ids
+ * must be distinct.  A sequence whose context would exceed max_ctx is left
+ * unchanged and sets the device error word. */
+dspark_status dspark_ingest_context_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,
+                                            const int32_t* cu_tokens_dev, const void* feats_dev,
+                                            int32_t total_tokens, void* stream);
+
+/* Batched draft: one block per sequence seq_ids_dev[i] with anchor
+ * last_tokens_dev[i]; outputs tokens_dev [n_seqs, gamma], conf_dev [n_seqs, gamma],
+ * logits_dev [n_seqs, gamma, V] or NULL.  Results equal n_seqs calls of
+ * dspark_draft on the sequences' own caches.  n_seqs <= max_seqs. */
+dspark_status dspark_draft_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,
+                                   const int32_t* last_tokens_dev, int32_t* tokens_dev, float* conf_dev,
+                                   float* logits_dev, void* stream);
+
+/* Host-buffer forms of ingest and draft for sequence 0: the library copies
+ * feats_host [T, m*H] in, runs the step, copies tokens/conf (and logits, if
+ * logits_host is not NULL) out, and synchronises `stream`.  Same arithmetic
+ * as the device-pointer calls. */
+dspark_status dspark_ingest_context_host(dspark_handle* h, const void* feats_host, int32_t T, void* stream);
+dspark_status dspark_draft_host(dspark_handle* h, int32_t last_token, int32_t* tokens_host, float* conf_host,
+                                float* logits_host, void* stream);
+
+/* Set the context length of seq_id to 0 (stream-ordered on `stream`). */
+dspark_status dspark_reset(dspark_handle* h, int32_t seq_id, void* stream);
+
+/* Context length of seq_id, read from the device (synchronises the device);
+ * returns DSPARK_ERR_DEVICE if the device error word is set. */
+dspark_status dspark_context_length(dspark_handle* h, int32_t seq_id, int32_t* out_host);
+
+/* Read and clear the device error word (synchronises the device).  *word_host
+ * (may be NULL) receives it: 0 = none, otherwise a DSPARK_DEVERR_* bit set. */
+#define DSPARK_DEVERR_TOKEN_RANGE 1   /* a batched anchor token outside [0, V)        */
+#define DSPARK_DEVERR_SEQ_RANGE 2     /* a batched sequence id outside [0, max_seqs)  */
+#define DSPARK_DEVERR_CAPACITY 4      /* a batched ingest would exceed max_ctx        */
+#define DSPARK_DEVERR_NONFINITE 8     /* a logit row had no finite maximum            */
+dspark_status dspark_check(dspark_handle* h, int32_t* word_host);
+
+/* Device pointers to the library-owned cache of (seq_id, layer): K and V rows
+ * [max_ctx + gamma, d] of dtype, row stride d elements; rows [0, length) hold
+ * the context.  For inspection only: the pointers stay valid until destroy. */
+dspark_status dspark_get_cache(dspark_handle* h, int32_t seq_id, int32_t layer, const void** k_dev,
+                               const void** v_dev);
+
+/* Description of the last error on this handle (or of the last failed create
+ * when h is NULL).  Never NULL. */
+const char* dspark_last_error(const dspark_handle* h);
+
+/* Timing of the step's kernel classes with CUDA events recorded on the calls'
+ * own stream around each class of launches (no extra synchronisation).
+ * dspark_profile(h, mask) with mask != 0 clears the counters and starts
+ * recording the classes whose bit is set (bit i = the i-th class name that
+ * dspark_profile_read reports; -1 = all); mask 0 stops.
+ * dspark_profile_read fills up to `max` entries (class name, summed device
+ * milliseconds, number of timed ranges, kernel launches in those ranges),
+ * synchronising the recorded events first, and returns the number of classes
+ * (negative on error). */
+dspark_status dspark_profile(dspark_handle* h, int32_t class_mask);
+int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_host, double* ms_host,
+                            int64_t* ranges_host, int64_t* launches_host);
+
+/* Number of kernel launches issued by this handle since creation (all calls). */
+int64_t dspark_launch_count(const dspark_handle* h);
+
+/* Library version string. */
+const char* dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -13,10 +13,12 @@
  *   key(s, t)   = mix(mix(s) ^ (t * 0xd1b54a32d192ed03))
  *   word(s,t,i) = mix(key(s, t) + i)
  *   unit53(w)   = (w >> 11) * 2^-53                       in [0, 1)
- *   normal pair p (elements 2p and 2p+1), Box-Muller (Box & Muller 1958):
- *       u1 = 1 - unit53(word(2p)) in (0, 1],  u2 = unit53(word(2p+1))
+ *   unit24(w)   = (w >> 40) * 2^-24                       in [0, 1), exact in float
+ *   normal pair p (elements 2p and 2p+1), Box-Muller (Box & Muller 1958), one
+ *   64-bit word per pair:
+ *       u1 = 1 - unit24(word(p)) in (0, 1],  u2 = unit24(word(p) << 24)
  *       r  = sqrt(-2 ln u1), out[2p] = r cos(2 pi u2), out[2p+1] = r sin(2 pi u2)
- *     computed in double, scaled by std, rounded once to float.
+ *     computed in float with the C library's logf/sinf/cosf, then scaled by std.
  *   bf16 values are the round-to-nearest-even bf16 of that float.
  *   uniform integer in [lo, hi]: lo + floor(unit53(word(i)) * (hi - lo + 1)).
  *
@@ -52,13 +54,16 @@ static inline uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
-static void normal_pair(uint64_t key, int64_t p, double std, float* a, float* b) {
-    double u1 = 1.0 - unit53(mix(key + (uint64_t)(2 * p)));
-    double u2 = unit53(mix(key + (uint64_t)(2 * p + 1)));
-    double r = sqrt(-2.0 * log(u1));
-    double th = 6.283185307179586476925286766559 * u2;
-    *a = (float)(r * cos(th) * std);
-    *b = (float)(r * sin(th) * std);
+static inline float unit24(uint64_t w) { return (float)(w >> 40) * (1.0f / 16777216.0f); }
+
+static void normal_pair(uint64_t key, int64_t p, float std, float* a, float* b) {
+    uint64_t w = mix(key + (uint64_t)p);
+    float u1 = 1.0f - unit24(w);
+    float u2 = unit24(w << 24);
+    float r = sqrtf(-2.0f * logf(u1));
+    float th = 6.28318530717958647692f * u2;
+    *a = r * cosf(th) * std;
+    *b = r * sinf(th) * std;
 }
 
 void synth_normal_f32(uint64_t seed, uint64_t stream, int64_t n, double std, float* out) {
@@ -67,7 +72,7 @@ void synth_normal_f32(uint64_t seed, uint64_t stream, int64_t n, double std, flo
 #pragma omp parallel for schedule(static)
     for (int64_t p = 0; p < npairs; ++p) {
         float a, b;
-        normal_pair(key, p, std, &a, &b);
+        normal_pair(key, p, (float)std, &a, &b);
         out[2 * p] = a;
         if (2 * p + 1 < n) out[2 * p + 1] = b;
     }
@@ -79,7 +84,7 @@ void synth_normal_bf16(uint64_t seed, uint64_t stream, int64_t n, double std, ui
 #pragma omp parallel for schedule(static)
     for (int64_t p = 0; p < npairs; ++p) {
         float a, b;
-        normal_pair(key, p, std, &a, &b);
+        normal_pair(key, p, (float)std, &a, &b);
         out[2 * p] = f32_to_bf16_rne(a);
         if (2 * p + 1 < n) out[2 * p + 1] = f32_to_bf16_rne(b);
     }

@@ -1,0 +1,342 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.
+
+Small configurations are compared element by element (every cache row, every
+logit); the full-size drafters are compared on sampled steps, sequences and
+cache rows, which the oracle computes exactly (ingest is row-wise and the
+draft steps are open-loop, so any step can be checked on its own).
+Tolerances: logits and cache rows max|d| <= 2e-2 * max|ref| in bf16 and
+1e-4 * max|ref| in fp32; tokens exactly wherever the oracle's top-2 margin
+exceeds that tolerance, otherwise one of the oracle's near-tied chains.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from helpers import (check_block, check_cache, make_gpu_drafter, rel_tol, tensor_to_f64, to_torch,
+                     weights_to_device)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_draft_model_gb300 as bdm
+    bdm.build()
+    bdm.load()
+
+
+def _draft(gdr, cfg, anchor, want_logits=True):
+    tok = torch.empty(cfg.gamma, dtype=torch.int32, device="cuda")
+    conf = torch.empty(cfg.gamma, dtype=torch.float32, device="cuda")
+    lg = torch.empty(cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda") if want_logits else None
+    gdr.draft(anchor, tok, conf, lg)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), conf.cpu().numpy(), (lg.cpu().numpy() if want_logits else None)
+
+
+def _small(cfg, L, seed, chunks, anchors, norm_std=0.1, max_ctx=None):
+    W = syn.make_weights(cfg, seed=seed, norm_std=norm_std)
+    X = syn.make_feats(cfg, L, seed=seed)
+    dr = oracle.Drafter(cfg, W)
+    dr.ingest(X)
+    gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=max_ctx or L + 8)
+    Xd = to_torch(X)
+    lo = 0
+    for hi in chunks + [L]:
+        gdr.ingest_context(Xd[lo:hi])
+        lo = hi
+    assert gdr.context_length() == L
+    rel = rel_tol(cfg)
+    check_cache(dr, gdr, cfg, 0, np.arange(L), rel, label="cache")
+    for a in anchors:
+        tok, conf, lg = _draft(gdr, cfg, a)
+        check_block(dr, 0, a, tok, conf, lg, rel=rel, label=f"anchor {a}")
+    assert gdr.check() == 0
+    return dr, gdr, W
+
+
+def test_tiny_fp32_drafter():
+    """4 heads of 32, 2 layers, gamma 4, V 1024, r 32, 64 context rows, fp32 (1e-4)."""
+    cfg = syn.WORKLOADS["tiny_fp32"].cfg
+    _small(cfg, 64, seed=0, chunks=[5, 6, 40], anchors=[0, 17, 1023], norm_std=0.0)
+
+
+def test_tiny_fp32_random_norms_gelu():
+    cfg = syn.DrafterConfig(**{**syn.WORKLOADS["tiny_fp32"].cfg.__dict__, "act": "gelu_tanh"})
+    _small(cfg, 64, seed=1, chunks=[33], anchors=[5, 900])
+
+
+def test_bf16_ragged_multi_tile():
+    """Shapes that are not multiples of the tiles: d 192 (3 heads of 64), F 384,
+    m*H 960, V 1000, r 24, gamma 5, 77 + 3 context rows, random norm weights."""
+    cfg = syn.DrafterConfig(hidden=320, n_taps=3, d_draft=192, n_heads=3, n_layers=2, ff_mult=2, gamma=5,
+                            vocab=1000, markov_rank=24)
+    _small(cfg, 80, seed=2, chunks=[77], anchors=[0, 999, 321])
+
+
+def test_bf16_single_position_and_empty_context():
+    """gamma = 1 (no mask rows) and a draft with no context at all."""
+    cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=2, ff_mult=2, gamma=1,
+                            vocab=512, markov_rank=16)
+    W = syn.make_weights(cfg, seed=3, norm_std=0.1)
+    dr = oracle.Drafter(cfg, W)
+    gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=32)
+    tok, conf, lg = _draft(gdr, cfg, 7)
+    check_block(dr, 0, 7, tok, conf, lg, label="empty context")
+    X = syn.make_feats(cfg, 3, seed=3)
+    dr.ingest(X)
+    gdr.ingest_context(to_torch(X))
+    tok, conf, lg = _draft(gdr, cfg, 8)
+    check_block(dr, 0, 8, tok, conf, lg, label="3 rows")
+
+
+def test_chunked_ingest_matches_one_shot_on_gpu():
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=128, n_heads=2, n_layers=2, ff_mult=2, gamma=4,
+                            vocab=640, markov_rank=16)
+    W = syn.make_weights(cfg, seed=4)
+    Wd = weights_to_device(W)
+    X = to_torch(syn.make_feats(cfg, 50, seed=4))
+    a = make_gpu_drafter(cfg, Wd, max_ctx=64)
+    a.ingest_context(X)
+    b = make_gpu_drafter(cfg, Wd, max_ctx=64)
+    for lo, hi in ((0, 3), (3, 20), (20, 50)):
+        b.ingest_context(X[lo:hi])
+    for i in range(cfg.n_layers):
+        ka, va = a.cache(0, i, 50)
+        kb, vb = b.cache(0, i, 50)
+        # different kernels may serve different chunk sizes: compare within the bf16 tolerance
+        assert (ka.float() - kb.float()).abs().max().item() <= 2e-2 * ka.float().abs().max().item()
+        assert (va.float() - vb.float()).abs().max().item() <= 2e-2 * va.float().abs().max().item()
+
+
+def test_host_buffer_calls_match_device_calls():
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=3,
+                            vocab=700, markov_rank=16)
+    W = syn.make_weights(cfg, seed=5)
+    Wd = weights_to_device(W)
+    X = syn.make_feats(cfg, 20, seed=5)
+    a = make_gpu_drafter(cfg, Wd, max_ctx=32)
+    a.ingest_context(to_torch(X))
+    ta, ca, la = _draft(a, cfg, 11)
+    b = make_gpu_drafter(cfg, Wd, max_ctx=32)
+    Xh = torch.from_numpy(X.view(np.int16)).pin_memory()
+    b.ingest_context_host(Xh)
+    tb = torch.empty(cfg.gamma, dtype=torch.int32).pin_memory()
+    cb = torch.empty(cfg.gamma, dtype=torch.float32).pin_memory()
+    lb = torch.empty(cfg.gamma, cfg.vocab, dtype=torch.float32).pin_memory()
+    b.draft_host(11, tb, cb, lb)
+    assert np.array_equal(ta, tb.numpy())
+    assert np.array_equal(ca, cb.numpy())
+    assert np.array_equal(la, lb.numpy())
+
+
+def test_batched_equals_per_sequence():
+    """Three sequences through the batched calls == each sequence on its own handle."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=128, n_heads=4, n_layers=2, ff_mult=2, gamma=4,
+                            vocab=777, markov_rank=32)
+    W = syn.make_weights(cfg, seed=6, norm_std=0.1)
+    Wd = weights_to_device(W)
+    lens = [9, 0, 23]
+    feats = [syn.make_feats(cfg, n, seed=6, seq=i) for i, n in enumerate(lens)]
+    gb = make_gpu_drafter(cfg, Wd, max_ctx=40, max_seqs=5)
+    ids = torch.tensor([4, 1, 2], dtype=torch.int32, device="cuda")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    allx = to_torch(np.concatenate(feats, axis=0))
+    gb.ingest_context_batched(ids, cu, allx)
+    anchors = torch.tensor([3, 500, 776], dtype=torch.int32, device="cuda")
+    tok = torch.empty(3, cfg.gamma, dtype=torch.int32, device="cuda")
+    conf = torch.empty(3, cfg.gamma, dtype=torch.float32, device="cuda")
+    lg = torch.empty(3, cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda")
+    gb.draft_batched(ids, anchors, tok, conf, lg)
+    torch.cuda.synchronize()
+    assert gb.check() == 0
+    assert [gb.context_length(s) for s in (4, 1, 2, 0)] == [9, 0, 23, 0]
+    dr = oracle.Drafter(cfg, W)
+    for i, n in enumerate(lens):
+        if n:
+            dr.ingest(feats[i], seq=i)
+    for i in range(3):
+        check_block(dr, i, int(anchors[i]), tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
+                    label=f"seq {i}")
+    # cache placement of slot 4 (sequence 0) and slot 2 (sequence 2)
+    for slot, i in ((4, 0), (2, 2)):
+        for layer in range(cfg.n_layers):
+            K, V = dr.cache(i, layer)
+            gk, gv = gb.cache(slot, layer, lens[i])
+            assert np.max(np.abs(tensor_to_f64(gk) - K)) <= 2e-2 * np.max(np.abs(K))
+            assert np.max(np.abs(tensor_to_f64(gv) - V)) <= 2e-2 * np.max(np.abs(V))
+
+
+def test_host_checked_errors():
+    import block_draft_model_gb300 as bdm
+    cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=2,
+                            vocab=300, markov_rank=8)
+    W = syn.make_weights(cfg, seed=7)
+    gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=10)
+    X = to_torch(syn.make_feats(cfg, 11, seed=7))
+    with pytest.raises(bdm.DsparkError) as e:
+        gdr.ingest_context(X)
+    assert e.value.status == bdm.ERR_CAPACITY
+    assert gdr.context_length() == 0
+    gdr.ingest_context(X[:10])
+    assert gdr.context_length() == 10
+    tok = torch.empty(2, dtype=torch.int32, device="cuda")
+    conf = torch.empty(2, dtype=torch.float32, device="cuda")
+    for bad in (-1, 300):
+        with pytest.raises(bdm.DsparkError) as e:
+            gdr.draft(bad, tok, conf)
+        assert e.value.status == bdm.ERR_INVALID_ARG
+    gdr.reset()
+    assert gdr.context_length() == 0
+    # device-side checks of the batched calls: a bad anchor and a bad slot set bits of the error word
+    ids = torch.tensor([0], dtype=torch.int32, device="cuda")
+    gdr.draft_batched(ids, torch.tensor([300], dtype=torch.int32, device="cuda"), tok.view(1, 2), conf.view(1, 2))
+    assert gdr.check() & 1
+    gdr.draft_batched(torch.tensor([3], dtype=torch.int32, device="cuda"),
+                      torch.tensor([1], dtype=torch.int32, device="cuda"), tok.view(1, 2), conf.view(1, 2))
+    assert gdr.check() & 2
+    cu = torch.tensor([0, 11], dtype=torch.int32, device="cuda")
+    gdr.ingest_context_batched(ids, cu, X)
+    assert gdr.check() & 4
+    assert gdr.context_length() == 0
+    assert gdr.check() == 0
+
+
+# --------------------------------------------------------------------------- full-size drafters
+
+def test_minicpm_shaped_full_size():
+    """MiniCPM-shaped drafter (H 2048, m 5, d 2048, 16 heads, 5 layers, gamma 8,
+    V 73448, r 256), 1024 context rows, then draft; every cache row of sampled
+    rows and every logit of two blocks are compared."""
+    wl = syn.WORKLOADS["minicpm_L1024"]
+    cfg = wl.cfg
+    W = syn.make_weights(cfg, seed=0)
+    X = syn.make_feats(cfg, wl.ctx_len, seed=0)
+    gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=wl.ctx_len + 64)
+    gdr.ingest_context(to_torch(X))
+    anchors = syn.anchors(wl)[:, 0]
+    outs = [_draft(gdr, cfg, int(a)) for a in (anchors[0], 12345)]
+    assert gdr.check() == 0
+    dr = oracle.Drafter(cfg, W)
+    dr.ingest(X)
+    rows = np.unique(np.concatenate([[0, 1, 511, 1023], syn.uniform_int(9, 9, (28,), 0, 1023)]))
+    check_cache(dr, gdr, cfg, 0, rows, label="minicpm cache")
+    for a, (tok, conf, lg) in zip((anchors[0], 12345), outs):
+        check_block(dr, 0, int(a), tok, conf, lg, label=f"minicpm anchor {a}")
+
+
+@pytest.fixture(scope="module")
+def gemma():
+    cfg = syn.GEMMA
+    W = syn.make_weights(cfg, seed=0)
+    Wd = weights_to_device(W)
+    dr = oracle.Drafter(cfg, W)
+    return cfg, W, Wd, dr
+
+
+def test_gemma_shaped_streaming_steps(gemma):
+    """Gemma-shaped default DFlash (H 2560, m 4, d 1024, 8 heads, 5 layers,
+    gamma 5, V 262144, r 256): 4096 context rows, then 64 steps that each ingest
+    1-6 new rows and draft; steps 0, 1, 31 and 63 are checked."""
+    cfg, W, Wd, dr = gemma
+    wl = syn.WORKLOADS["gemma_L4096_stream"]
+    anchors, counts = syn.anchors(wl)[:, 0], syn.step_counts(wl)[:, 0]
+    total = wl.ctx_len + int(counts.sum())
+    gdr = make_gpu_drafter(cfg, Wd, max_ctx=total + 8)
+    X0 = syn.make_feats(cfg, wl.ctx_len, seed=0)
+    gdr.ingest_context(to_torch(X0))
+    dr.reset(0)
+    dr.ingest(X0)
+    check_at = {0, 1, 31, 63}
+    for s in range(wl.steps):
+        Xs = syn.make_feats(cfg, int(counts[s]), seed=0, step=s)
+        gdr.ingest_context(to_torch(Xs))
+        dr.ingest(Xs)
+        want = s in check_at
+        tok, conf, lg = _draft(gdr, cfg, int(anchors[s]), want_logits=want)
+        if want:
+            check_block(dr, 0, int(anchors[s]), tok, conf, lg, label=f"gemma step {s}")
+    assert gdr.context_length() == total
+    rows = np.array([0, 4095, 4096, total - 1])
+    check_cache(dr, gdr, cfg, 0, rows, label="gemma cache")
+    assert gdr.check() == 0
+    dr.reset(0)
+
+
+def test_gemma_shaped_long_context(gemma):
+    """32768 context rows ingested at once, then 16 draft steps (0 and 15 checked)."""
+    cfg, W, Wd, dr = gemma
+    wl = syn.WORKLOADS["gemma_L32768_ingest"]
+    X = syn.make_feats(cfg, wl.ctx_len, seed=0)
+    gdr = make_gpu_drafter(cfg, Wd, max_ctx=wl.ctx_len)
+    gdr.ingest_context(to_torch(X))
+    anchors = syn.anchors(wl)[:, 0]
+    outs = {}
+    for s in range(wl.steps):
+        o = _draft(gdr, cfg, int(anchors[s]), want_logits=s in (0, 15))
+        if s in (0, 15):
+            outs[s] = o
+    assert gdr.check() == 0
+    dr.reset(0)
+    dr.ingest(X)
+    rows = np.unique(np.concatenate([[0, 32767], syn.uniform_int(9, 10, (30,), 0, 32767)]))
+    check_cache(dr, gdr, cfg, 0, rows, label="long cache")
+    for s, (tok, conf, lg) in outs.items():
+        check_block(dr, 0, int(anchors[s]), tok, conf, lg, label=f"long step {s}")
+    dr.reset(0)
+
+
+def test_gemma_shaped_batched_serving(gemma):
+    """64 sequences with ragged contexts (512-8192 rows), 128 steps of 1-6 new
+    rows per sequence and one block per sequence; four sequences are checked at
+    steps 0 and 127."""
+    cfg, W, Wd, dr = gemma
+    wl = syn.WORKLOADS["gemma_batched64"]
+    n = wl.n_seqs
+    lens = syn.ctx_lengths(wl)
+    counts = syn.step_counts(wl)
+    anchors = syn.anchors(wl)
+    max_ctx = int(lens.max() + counts.sum(axis=0).max()) + 8
+    gdr = make_gpu_drafter(cfg, Wd, max_ctx=max_ctx, max_seqs=n)
+    ids = torch.arange(n, dtype=torch.int32, device="cuda")
+
+    def ingest(step, cnts):
+        feats = [syn.make_feats(cfg, int(c), seed=0, step=step, seq=i) for i, c in enumerate(cnts)]
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(cnts)]), dtype=torch.int32, device="cuda")
+        gdr.ingest_context_batched(ids, cu, to_torch(np.concatenate(feats, axis=0)))
+        return feats
+
+    first = ingest(-1, lens)
+    sample = [0, 17, int(np.argmax(lens)), int(np.argmin(lens))]
+    kept = {i: [first[i]] for i in sample}
+    del first
+    tok = torch.empty(n, cfg.gamma, dtype=torch.int32, device="cuda")
+    conf = torch.empty(n, cfg.gamma, dtype=torch.float32, device="cuda")
+    lg = torch.empty(n, cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda")
+    results = {}
+    for s in range(wl.steps):
+        feats = ingest(s, counts[s])
+        for i in sample:
+            kept[i].append(feats[i])
+        want = s in (0, wl.steps - 1)
+        gdr.draft_batched(ids, to_torch(anchors[s]), tok, conf, lg if want else None)
+        if want:
+            torch.cuda.synchronize()
+            results[s] = {i: (tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
+                              len(kept[i])) for i in sample}
+    assert gdr.check() == 0
+    for i in sample:
+        assert gdr.context_length(i) == int(lens[i] + counts[:, i].sum())
+    for s, per in results.items():
+        for i, (t, c, l, nparts) in per.items():
+            dr.reset(0)
+            for part in kept[i][:nparts]:
+                dr.ingest(part)
+            check_block(dr, 0, int(anchors[s, i]), t, c, l, label=f"batched step {s} seq {i}")
+    dr.reset(0)
