@@ -23,7 +23,7 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_ingest_context_batched", "dspark_draft_batched", "dspark_ingest_context_host",
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
-            "dspark_profile_read"]
+            "dspark_profile_read", "dspark_linear"]
 
 
 class DsparkError(RuntimeError):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_launch_count": ([vp], i64),
         "dspark_version": ([], ctypes.c_char_p),
         "dspark_profile": ([vp, i32], i32),
+        "dspark_linear": ([i32, vp, i64, vp, i32, i32, i32, vp, i64, i32, vp], i32),
         "dspark_profile_read": ([vp, i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
     }
@@ -107,6 +108,22 @@ def _stream(stream) -> int:
     if stream is None:
         return int(torch.cuda.current_stream().cuda_stream)
     return int(getattr(stream, "cuda_stream", stream))
+
+
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_STREAM, KERNEL_TC = 0, 1, 2, 3
+
+
+def linear(A, W, out, kernel: int = KERNEL_AUTO, stream=None):
+    """out[m, n] = sum_k A[m, k] W[n, k] on the GPU (A, W bf16 or float32 CUDA tensors, out float32)."""
+    import torch
+    lib = load()
+    dt = BF16 if A.dtype == torch.bfloat16 else FP32
+    M, K = A.shape
+    N = W.shape[0]
+    st = lib.dspark_linear(dt, _ptr(A), A.stride(0), _ptr(W), M, N, K, _ptr(out), out.stride(0), int(kernel),
+                           _stream(stream))
+    if st != OK:
+        raise DsparkError(st, lib.dspark_last_error(None).decode())
 
 
 class _CudaArray:

@@ -153,7 +153,7 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     if (M <= 16 && skinny_ok(M, K))
         return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
     if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_gemm_ok(M, N, K))
-        return tc_gemm((const char*)A + (size_t)a_row0 * lda * 2, lda, *tcw, M, N, K, ep, h->num_sms, st);
+        return tc_gemm((const char*)A + (size_t)a_row0 * lda * 2, lda, *tcw, M, N, K, ep, h->num_sms, h->d_err, st);
     const char* a = (const char*)A;
     if (!a_rows) a += (size_t)a_row0 * lda * (a_dtype == DT_BF16 ? 2 : 4);
     return gemm_simt(a_dtype, a, lda, a_rows, h->dt, W, M, N, K, ep, st);
@@ -450,6 +450,43 @@ int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_ho
         if (launches_host) launches_host[c] = nl[c];
     }
     return CAT_COUNT;
+}
+
+dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
+                            int32_t K, float* out_dev, int64_t ldo, int32_t kernel, void* stream) {
+    if (!A_dev || !W_dev || !out_dev) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "a pointer is NULL");
+    if (M < 0 || N < 0 || K <= 0 || lda < K || ldo < N) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "bad shape");
+    if (dtype != DSPARK_BF16 && dtype != DSPARK_FP32) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "unknown dtype");
+    if (M == 0 || N == 0) return DSPARK_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int dt = dtype == DSPARK_BF16 ? DT_BF16 : DT_F32;
+    EpiParams ep;
+    ep.kind = EPI_STORE_F32;
+    ep.out_f32 = out_dev;
+    ep.ldo = ldo;
+    static int* err_word = nullptr;
+    int num_sms = 148, dev = 0;
+    CUDA_TRY(nullptr, cudaGetDevice(&dev));
+    CUDA_TRY(nullptr, cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+    if (kernel == 0) kernel = (M <= 16 && skinny_ok(M, K)) ? 2 : (dt == DT_BF16 && tc_available() && tc_gemm_ok(M, N, K) ? 3 : 1);
+    if (kernel == 1) {
+        CUDA_TRY(nullptr, gemm_simt(dt, A_dev, lda, nullptr, dt, W_dev, M, N, K, ep, st));
+    } else if (kernel == 2) {
+        if (!skinny_ok(M, K) || lda % 8 != 0) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "shape not for weight streaming");
+        CUDA_TRY(nullptr, gemm_skinny(dt, A_dev, lda, nullptr, 0, dt, W_dev, M, N, K, ep, nullptr, 0, num_sms, st));
+    } else if (kernel == 3) {
+        if (dt != DT_BF16 || !tc_available() || !tc_gemm_ok(M, N, K) || lda % 8 != 0 || ((uintptr_t)A_dev & 15) ||
+            ((uintptr_t)W_dev & 15))
+            return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "shape not for the tensor-core GEMM");
+        if (!err_word) CUDA_TRY(nullptr, cudaMalloc((void**)&err_word, sizeof(int)));
+        TcWeight w;
+        CUDA_TRY(nullptr, tc_prepare(w, W_dev, N, K));
+        if (!w.ready) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "tensor map rejected");
+        CUDA_TRY(nullptr, tc_gemm(A_dev, lda, w, M, N, K, ep, num_sms, err_word, st));
+    } else {
+        return fail(nullptr, DSPARK_ERR_INVALID_ARG, "unknown kernel");
+    }
+    return DSPARK_OK;
 }
 
 const char* dspark_version(void) { return "dspark-gb300 0.1"; }

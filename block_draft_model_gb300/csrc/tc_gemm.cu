@@ -1,20 +1,385 @@
-// Tensor-core GEMM: not enabled yet (the SIMT kernels serve every shape).
+// Tensor-core GEMM for sm_100-family GPUs (tcgen05 + TMA + TMEM), bf16 in, fp32 accumulate:
+//   acc[m, n] = sum_k A[m, k] W[n, k]     A: [M, K] bf16, W: [N, K] bf16 (K contiguous)
+// and the GEMM epilogues of epilogue.cuh.
+//
+// Persistent, warp-specialised CTA (one per SM, 192 threads):
+//   warp 0     TMA producer: 128x64 A and 256x64 W tiles (128-byte swizzle) into a
+//              STAGES-deep shared-memory ring, one mbarrier (with transaction
+//              bytes) per stage;
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and one
+//              elected lane issues tcgen05.mma (M 128, N 256, K 16) per 16-wide
+//              K slice; tcgen05.commit frees a stage when its MMAs retire and
+//              signals the epilogue when a tile's accumulator is complete;
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows), then
+//              the epilogue functor, while the MMA warp fills the other
+//              accumulator.
+// Every mbarrier wait is bounded (about one second of %globaltimer); on a
+// timeout the kernel records DSPARK_DEVERR_TIMEOUT, stops every role, drains
+// its own MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdio.h>
+
+#include "epilogue.cuh"
 #include "tc_gemm.cuh"
 
 namespace dspark {
 
-bool tc_available() { return false; }
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int TMEM_COLS = 2 * BN;     // two accumulators
+constexpr int NTHREADS = 192;
+constexpr uint64_t TIMEOUT_NS = 1000000000ull;
+constexpr int DEVERR_TIMEOUT = 16;
+
+constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + 256; }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of `parity`; false on timeout (which raises the
+// CTA's abort flag) or when another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > TIMEOUT_NS) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart (stride offset),
+// descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TileMap {
+    int nM, nN;
+    bool n_fast;
+    __device__ __forceinline__ void at(int t, int& m0, int& n0) const {
+        int mi, ni;
+        if (n_fast) {
+            mi = t / nN;
+            ni = t - mi * nN;
+        } else {
+            ni = t / nM;
+            mi = t - ni * nM;
+        }
+        m0 = mi * BM;
+        n0 = ni * BN;
+    }
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
+              TileMap tm, EpiParams ep, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES));
+    uint64_t* full = bars;                      // [STAGES]
+    uint64_t* empty = bars + STAGES;            // [STAGES]
+    uint64_t* acc_full = bars + 2 * STAGES;     // [2]
+    uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = tm.nM * tm.nN;
+    const int nkb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                int m0, n0;
+                tm.at(t, m0, n0);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+                    tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
+                    tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id = idesc(BM, BN);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = sdesc(sA + stage * A_BYTES);
+                    const uint64_t db = sdesc(sB + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)  // +32 bytes per 16-wide K slice inside the swizzled row
+                        umma(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb | k) ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+                if (++buf == 2) {
+                    buf = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // drain: every MMA issued by this thread has retired once `drain` completes
+            umma_commit(drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+            }
+        }
+    } else {
+        // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31
+        const int q = warp & 3;
+        int buf = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            int m0, n0;
+            tm.at(t, m0, n0);
+            if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(base + c * 32, r);
+                const int nb = n0 + c * 32;
+                if (row < M && nb < N) {
+                    if (ep.kind == EPI_SWIGLU) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2)
+                            if (nb + j + 1 < N) epi_pair(ep, row, nb + j, __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (nb + j < N) epi_one(ep, row, nb + j, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (++buf == 2) {
+                buf = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(err, DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_state = -1;  // -1 unknown, 0 unavailable, 1 available
+
+bool init_encode() {
+    if (g_state >= 0) return g_state == 1;
+    g_state = 0;
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (major != 10) return false;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    if (cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
+        return false;
+    g_state = 1;
+    return true;
+}
+
+// 2-D bf16 tensor map: rows x cols (cols contiguous, row stride ld elements), box box_rows x 64.
+bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_available() { return init_encode(); }
+
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K) {
     w.ready = false;
     w.ptr = ptr;
     w.N = N;
     w.K = K;
+    if (!init_encode()) return cudaSuccess;
+    if (K % 8 != 0 || ((uintptr_t)ptr & 15) != 0) return cudaSuccess;
+    if (!encode(reinterpret_cast<CUtensorMap*>(w.tmap), ptr, N, K, K, BN)) return cudaSuccess;
+    w.ready = true;
     return cudaSuccess;
 }
+
 void tc_release(TcWeight& w) { w.ready = false; }
-bool tc_gemm_ok(int, int, int) { return false; }
-cudaError_t tc_gemm(const void*, int64_t, const TcWeight&, int, int, int, const EpiParams&, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+
+bool tc_gemm_ok(int M, int N, int K) { return g_state == 1 && M >= 1 && N >= 1 && K >= BK && K % 8 == 0; }
+
+cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
+                    int num_sms, int* err, cudaStream_t st) {
+    if (!w.ready || !tc_gemm_ok(M, N, K) || N > w.N || K != w.K) return cudaErrorInvalidValue;
+    if (lda % 8 != 0 || ((uintptr_t)A & 15) != 0) return cudaErrorInvalidValue;
+    CUtensorMap tmA;
+    if (!encode(&tmA, A, M, K, lda, BM)) return cudaErrorInvalidValue;
+    TileMap tm;
+    tm.nM = (M + BM - 1) / BM;
+    tm.nN = (N + BN - 1) / BN;
+    tm.n_fast = tm.nN <= tm.nM;
+    const int tiles = tm.nM * tm.nN;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    k_tc_gemm<<<grid, NTHREADS, smem_bytes(), st>>>(tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm,
+                                                     ep, err);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace dspark

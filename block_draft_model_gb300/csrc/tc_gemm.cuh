@@ -21,7 +21,9 @@ bool tc_available();
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K);
 void tc_release(TcWeight& w);
 bool tc_gemm_ok(int M, int N, int K);
+// A: [M, K] bf16 with row stride lda (16-byte aligned).  A bounded device wait
+// that gives up sets bit 16 of *err (the handle's device error word).
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
-                    int num_sms, cudaStream_t st);
+                    int num_sms, int* err, cudaStream_t st);
 
 }  // namespace dspark

@@ -178,6 +178,7 @@ dspark_status dspark_context_length(dspark_handle* h, int32_t seq_id, int32_t* o
 #define DSPARK_DEVERR_SEQ_RANGE 2     /* a batched sequence id outside [0, max_seqs)  */
 #define DSPARK_DEVERR_CAPACITY 4      /* a batched ingest would exceed max_ctx        */
 #define DSPARK_DEVERR_NONFINITE 8     /* a logit row had no finite maximum            */
+#define DSPARK_DEVERR_TIMEOUT 16      /* a bounded wait inside a kernel gave up       */
 dspark_status dspark_check(dspark_handle* h, int32_t* word_host);
 
 /* Device pointers to the library-owned cache of (seq_id, layer): K and V rows
@@ -202,6 +203,18 @@ const char* dspark_last_error(const dspark_handle* h);
 dspark_status dspark_profile(dspark_handle* h, int32_t class_mask);
 int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_host, double* ms_host,
                             int64_t* ranges_host, int64_t* launches_host);
+
+/* The contraction inside every projection of the step ("module-dflash.ts":
+ * the ops.matmul calls of #buildContext, #buildBlock, #layer, #baseLogits),
+ * as a standalone call: out[m, n] = sum_k A[m, k] W[n, k], fp32 result.
+ * A_dev [M, K] (row stride lda elements) and W_dev [N, K] are both bf16
+ * (dtype DSPARK_BF16) or both float32 (DSPARK_FP32); out_dev [M, N] float32
+ * with row stride ldo.  `kernel` selects the implementation: 0 the one the step
+ * would use for this shape, 1 SIMT tiles, 2 weight streaming (M <= 16, K % 8 == 0),
+ * 3 tcgen05 tensor cores (bf16, K >= 64, K % 8 == 0, 16-byte aligned rows).
+ * DSPARK_ERR_UNSUPPORTED if the chosen kernel cannot take the shape. */
+dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
+                            int32_t K, float* out_dev, int64_t ldo, int32_t kernel, void* stream);
 
 /* Number of kernel launches issued by this handle since creation (all calls). */
 int64_t dspark_launch_count(const dspark_handle* h);

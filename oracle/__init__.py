@@ -15,6 +15,7 @@ from .dspark_oracle import (  # noqa: F401
     context_kv,
     ffn,
     gelu_tanh,
+    linear,
     markov_logits,
     rmsnorm,
     sigmoid,

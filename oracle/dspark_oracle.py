@@ -54,6 +54,12 @@ def to_f64(a: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------- primitives
 
+def linear(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """The contraction of every projection (MLX ``ops.matmul(x, W)`` with W stored
+    [out, in] here): x W^T in float64."""
+    return to_f64(x) @ to_f64(W).T
+
+
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     """MLX ``rmsNorm(x, w, eps)`` as used by ``#buildContext`` and ``#layer``:
     each row divided by the root of (its mean square + eps), times w (R3)."""

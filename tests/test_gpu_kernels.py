@@ -1,0 +1,59 @@
+"""Kernel-level parity of the contraction behind every projection
+(dspark_linear: out = A W^T) for each GEMM implementation, against the
+oracle's float64 definition, on shapes that span several tiles and ragged
+tails.  bf16 inputs, fp32 accumulation: max|d| <= 1e-4 * max|ref|."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from helpers import to_torch
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_draft_model_gb300 as bdm
+    bdm.build()
+    bdm.load()
+
+
+SHAPES = [(1, 64, 64), (5, 1000, 1024), (8, 4096, 2048), (16, 3072, 1024), (17, 300, 136),
+          (128, 256, 64), (129, 257, 192), (320, 1000, 1024), (1024, 1024, 10240), (777, 2048, 1024)]
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_linear_kernels(kernel, shape):
+    import block_draft_model_gb300 as bdm
+    M, N, K = shape
+    if kernel == 2 and M > 16:
+        pytest.skip("weight streaming takes M <= 16")
+    if kernel == 3 and K < 64:
+        pytest.skip("tensor-core path takes K >= 64")
+    A = syn.normal_bf16(7, 1, (M, K))
+    W = syn.normal_bf16(7, 2, (N, K), 0.05)
+    ref = oracle.linear(A, W)
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    bdm.linear(to_torch(A), to_torch(W), out, kernel=kernel)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.max(np.abs(got - ref))
+    assert err <= 1e-4 * np.max(np.abs(ref)), (kernel, shape, err)
+
+
+def test_linear_fp32_simt_and_streaming():
+    import block_draft_model_gb300 as bdm
+    for kernel, (M, N, K) in ((1, (70, 130, 200)), (2, (4, 1024, 256))):
+        A = syn.normal_f32(8, 1, (M, K))
+        W = syn.normal_f32(8, 2, (N, K), 0.05)
+        out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        bdm.linear(to_torch(A), to_torch(W), out, kernel=kernel)
+        torch.cuda.synchronize()
+        ref = oracle.linear(A, W)
+        assert np.max(np.abs(out.double().cpu().numpy() - ref)) <= 1e-5 * np.max(np.abs(ref))

@@ -407,3 +407,13 @@ def test_argmax_ties_take_the_lowest_index():
 def test_bad_config_is_rejected():
     with pytest.raises(ValueError):
         oracle.Drafter(tiny_cfg(d_draft=9, n_heads=2), {})
+
+
+def test_linear_against_loops():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(3, 5)).astype(np.float32)
+    W = rng.normal(size=(4, 5)).astype(np.float32)
+    out = oracle.linear(x, W)
+    for m in range(3):
+        for n in range(4):
+            assert abs(out[m, n] - sum(float(x[m, k]) * float(W[n, k]) for k in range(5))) < 1e-12
