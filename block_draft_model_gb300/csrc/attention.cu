@@ -183,23 +183,24 @@ size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head
     return (size_t)B * n_heads * n_chunks * gamma * (head_dim + 2);
 }
 
+cudaError_t attention_init() {
+    const int sm = (int)Smem::bytes(GMAX, HMAX);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_partial<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_attn_partial<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+}
+
 cudaError_t attention(const AttnParams& p, cudaStream_t st) {
     const int hd = p.d / p.n_heads;
     if (p.gamma > GMAX || hd > HMAX || hd % 8 != 0) return cudaErrorInvalidValue;
     const size_t sm = Smem::bytes(p.gamma, hd);
     dim3 g1(p.n_chunks, p.n_heads, p.B);
-    cudaError_t e;
-    if (p.cache_dtype == DT_BF16) {
-        e = cudaFuncSetAttribute(k_attn_partial<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
+    if (p.cache_dtype == DT_BF16)
         k_attn_partial<bf16><<<g1, NT, sm, st>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(k_attn_partial<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
+    else
         k_attn_partial<float><<<g1, NT, sm, st>>>(p);
-    }
     note_launch();
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g2(p.n_heads, p.B);
     if (p.out_dtype == DT_BF16)

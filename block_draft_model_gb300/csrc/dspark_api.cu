@@ -2,6 +2,7 @@
 // and the ingest / draft step orchestration (see include/dspark.h).
 #include <cuda_runtime.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -36,6 +37,23 @@ struct ProfRange {
     int cat;
     cudaEvent_t a, b;
     long long launches;
+    cudaGraphNode_t na = nullptr, nb = nullptr;  // event-record nodes when captured in a graph
+};
+
+// A captured draft step, replayed while its inputs and outputs stay the same.
+struct DraftGraph {
+    int B = 0;
+    const int* seq_ids = nullptr;
+    const int* anchors = nullptr;
+    int* tokens = nullptr;
+    float* conf = nullptr;
+    float* logits = nullptr;
+    uint32_t mask = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<ProfRange> ranges;
+    long long kernels = 0;
+    uint64_t last_use = 0;
 };
 
 }  // namespace
@@ -63,9 +81,14 @@ struct dspark_handle {
     void* w1 = nullptr;
     void* w2 = nullptr;
     float* conf_wb = nullptr;                // [d + r + 1]
-    TcWeight tc_wc, tc_out_proj;             // tensor-core views (bf16 only)
+    TcWeight tc_wc, tc_out_proj;             // tensor-core views (bf16 only), rows >= 17
     std::vector<TcWeight> tc_kv, tc_qkv, tc_wo, tc_wgu, tc_wd;
-    TcWeight tc_tok_proj;
+    TcWeightStream ts_wc, ts_out_proj;       // weight-streaming tensor-core views, rows <= 16
+    std::vector<TcWeightStream> ts_kv, ts_qkv, ts_wo, ts_wgu, ts_wd;
+    float* ts_part = nullptr;                // split-K partials of the streaming GEMM
+    size_t ts_part_floats = 0;
+    unsigned int* ts_tickets = nullptr;
+    size_t ts_n_tickets = 0;
     // caches: [layer][seq][K|V][rows][d]
     void* cache = nullptr;
     int64_t rows = 0, seq_stride = 0, kv_off = 0, layer_stride = 0;
@@ -96,6 +119,13 @@ struct dspark_handle {
 
     std::string err = "no error";
     long long launches_at_create = 0;
+    // CUDA graphs of the draft step
+    bool use_graphs = true;
+    cudaStream_t cap_stream = nullptr;
+    std::vector<DraftGraph> graphs;
+    uint64_t graph_clock = 0;
+    std::vector<ProfRange>* cap_ranges = nullptr;  // set while capturing
+    int* anchor_dev = nullptr;                     // [1] anchor of the non-batched draft
     // profiling
     bool prof_on = false;
     uint32_t prof_mask = 0;
@@ -146,10 +176,29 @@ int attn_chunks(const dspark_handle* h, int B, int max_keys) {
     return std::max(1, std::min(want, by_keys));
 }
 
-// acc = A . W^T with the best kernel for the shape.
+// A weight and its tensor-core views.
+struct WView {
+    const void* W;
+    const TcWeight* tc;
+    const TcWeightStream* ts;
+};
+template <typename V>
+const V* at_or_null(const std::vector<V>& v, int i) {
+    return v.empty() ? nullptr : &v[i];
+}
+
+// acc = A . W^T with the best kernel for the shape:
+//   rows <= 16, bf16: weight-streaming tcgen05 (swap-AB) kernel;
+//   rows <= 16 otherwise (fp32 drafter, gathered rows): SIMT weight streaming;
+//   rows >= 17, bf16: persistent tcgen05 GEMM;  anything else: SIMT tiles.
 cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, const int* a_rows, int a_row0,
-                 const void* W, const TcWeight* tcw, int M, int N, int K, const EpiParams& ep, cudaStream_t st) {
+                 const WView& wv, int M, int N, int K, const EpiParams& ep, cudaStream_t st) {
     if (M <= 0 || N <= 0) return cudaSuccess;
+    const void* W = wv.W;
+    const TcWeight* tcw = wv.tc;
+    if (M <= 16 && wv.ts && wv.ts->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_stream_ok(M, N, K))
+        return tc_stream((const char*)A + (size_t)a_row0 * lda * 2, lda, *wv.ts, M, N, K, ep, h->ts_part,
+                         h->ts_part_floats, h->ts_tickets, h->ts_n_tickets, h->num_sms, h->d_err, st);
     if (M <= 16 && skinny_ok(M, K))
         return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
     if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_gemm_ok(M, N, K))
@@ -159,33 +208,48 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     return gemm_simt(a_dtype, a, lda, a_rows, h->dt, W, M, N, K, ep, st);
 }
 
+// Next event of the handle's reusable timing-event pool (nullptr if none can be made).
+cudaEvent_t pool_event(dspark_handle* h) {
+    if (h->prof_next >= h->prof_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        h->prof_pool.push_back(e);
+    }
+    return h->prof_pool[h->prof_next++];
+}
+
 // Records an event pair around one class of launches when profiling is on.
 struct Prof {
     dspark_handle* h;
     cudaStream_t st;
     int idx = -1;
     long long l0 = 0;
-    cudaEvent_t ev() {
-        if (h->prof_next >= h->prof_pool.size()) {
-            cudaEvent_t e;
-            if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
-            h->prof_pool.push_back(e);
-        }
-        return h->prof_pool[h->prof_next++];
+    cudaEvent_t ev() { return pool_event(h); }
+    std::vector<ProfRange>& list() { return h->cap_ranges ? *h->cap_ranges : h->prof_ranges; }
+    void record(cudaEvent_t e) {
+        if (h->cap_ranges) cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+        else cudaEventRecord(e, st);
     }
     Prof(dspark_handle* h_, int cat, cudaStream_t st_) : h(h_), st(st_) {
         if (!h->prof_on || !(h->prof_mask & (1u << cat))) return;
-        cudaEvent_t a = ev(), b = ev();
-        if (!a || !b) return;
-        cudaEventRecord(a, st);
-        h->prof_ranges.push_back({cat, a, b, 0});
-        idx = (int)h->prof_ranges.size() - 1;
+        cudaEvent_t a, b;
+        if (h->cap_ranges) {  // placeholders: every replay gets fresh events
+            if (cudaEventCreate(&a) != cudaSuccess) return;
+            if (cudaEventCreate(&b) != cudaSuccess) return;
+        } else {
+            a = ev();
+            b = ev();
+            if (!a || !b) return;
+        }
+        record(a);
+        list().push_back({cat, a, b, 0});
+        idx = (int)list().size() - 1;
         l0 = launch_count();
     }
     void end() {
         if (idx < 0) return;
-        cudaEventRecord(h->prof_ranges[idx].b, st);
-        h->prof_ranges[idx].launches = launch_count() - l0;
+        record(list()[idx].b);
+        list()[idx].launches = launch_count() - l0;
         idx = -1;
     }
     ~Prof() { end(); }
@@ -251,7 +315,7 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
         ep.ldo = d;
         {
             Prof pr(h, CAT_INGEST_PROJ, st);
-            CUDA_TRY(h, gemm(h, h->dt, X, h->mH, nullptr, 0, h->W_c, &h->tc_wc, n, d, h->mH, ep, st));
+            CUDA_TRY(h, gemm(h, h->dt, X, h->mH, nullptr, 0, WView{h->W_c, &h->tc_wc, &h->ts_wc}, n, d, h->mH, ep, st));
         }
         const int lp = h->dt;  // normalised rows in the storage type (bf16 feeds the tensor cores)
         {
@@ -270,8 +334,8 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
             // otherwise slot 0 at len[0] + m: the device length advances after every chunk
             const void* Ni = (const char*)h->Nbuf + (size_t)i * h->ingest_rows * d * h->esz;
             const void* Wkv = (const char*)h->wqkv[i] + (size_t)d * d * h->esz;  // rows [d, 3d) = [W_k; W_v]
-            CUDA_TRY(h, gemm(h, lp, Ni, d, nullptr, 0, Wkv, h->tc_kv.empty() ? nullptr : &h->tc_kv[i], n, 2 * d, d,
-                             kv, st));
+            CUDA_TRY(h, gemm(h, lp, Ni, d, nullptr, 0, WView{Wkv, at_or_null(h->tc_kv, i), at_or_null(h->ts_kv, i)}, n,
+                             2 * d, d, kv, st));
         }
         if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
     }
@@ -290,10 +354,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ep.kind = EPI_ADD_F32;
         ep.out_f32 = h->x;
         ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
-        CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor, h->tok_proj, nullptr, B,
-                         d, c.hidden, ep, st));
+        CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
+                         WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
     }
-    const bool lowp = (h->dt == DT_BF16) && R > 16;  // tensor-core path takes bf16 A operands
+    const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
     void* actA = lowp ? h->act_lp : (void*)h->act;
     const int adt = lowp ? DT_BF16 : DT_F32;
     for (int i = 0; i < c.n_layers; ++i) {
@@ -310,8 +374,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         qkv.seq_ids = seq_ids;
         {
             Prof pr(h, CAT_QKV, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wqkv[i], h->tc_qkv.empty() ? nullptr : &h->tc_qkv[i], R,
-                             3 * d, d, qkv, st));
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
+                             WView{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)}, R, 3 * d, d, qkv,
+                             st));
         }
         AttnParams ap;
         ap.q = h->q;
@@ -341,8 +406,8 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         res.ldo = d;
         {
             Prof pr(h, CAT_O, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wo[i], h->tc_wo.empty() ? nullptr : &h->tc_wo[i], R, d,
-                             d, res, st));
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
+                             WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
         }
         {
             Prof pr(h, CAT_NORM, st);
@@ -356,13 +421,14 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         sw.act = c.act;
         {
             Prof pr(h, CAT_GATE_UP, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0, h->wgu[i], h->tc_wgu.empty() ? nullptr : &h->tc_wgu[i], R,
-                             2 * F, d, sw, st));
+            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
+                             WView{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)}, R, 2 * F, d, sw,
+                             st));
         }
         {
             Prof pr(h, CAT_DOWN, st);
-            CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0, h->wd[i], h->tc_wd.empty() ? nullptr : &h->tc_wd[i], R,
-                             d, F, res, st));
+            CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
+                             WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F, res, st));
         }
     }
     {
@@ -382,7 +448,8 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             A = h->act_lp;
             adt2 = DT_BF16;
         }
-        CUDA_TRY(h, gemm(h, adt2, A, d, nullptr, 0, h->out_proj, &h->tc_out_proj, R, V, d, ep, st));
+        CUDA_TRY(h, gemm(h, adt2, A, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V, d, ep,
+                         st));
     }
     MarkovParams mp;
     mp.U = h->U;
@@ -411,6 +478,97 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         mp.k = k;
         CUDA_TRY(h, markov_step(mp, st));
     }
+    return DSPARK_OK;
+}
+
+void destroy_graph(DraftGraph& g) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+    for (auto& r : g.ranges) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g = DraftGraph();
+}
+
+// The draft step through a cached CUDA graph: captured on the handle's own
+// stream the first time (inputs, outputs, B and the profiling mask form the
+// key), then replayed on `st`.  Kernels read every per-call value (context
+// lengths, anchors, previous tokens) from device memory, so a replay needs no
+// parameter updates.
+dspark_status draft_graphed(dspark_handle* h, int B, const int* seq_ids, const int* anchors, int max_keys,
+                            int* tokens, float* conf, float* logits, cudaStream_t st) {
+    const uint32_t mask = h->prof_on ? h->prof_mask : 0u;
+    DraftGraph* g = nullptr;
+    for (auto& c : h->graphs)
+        if (c.exec && c.B == B && c.seq_ids == seq_ids && c.anchors == anchors && c.tokens == tokens &&
+            c.conf == conf && c.logits == logits && c.mask == mask)
+            g = &c;
+    if (!g) {
+        if (h->graphs.size() >= 8) {
+            auto old = std::min_element(h->graphs.begin(), h->graphs.end(),
+                                        [](const DraftGraph& a, const DraftGraph& b) { return a.last_use < b.last_use; });
+            destroy_graph(*old);
+            h->graphs.erase(old);
+        }
+        DraftGraph ng;
+        ng.B = B;
+        ng.seq_ids = seq_ids;
+        ng.anchors = anchors;
+        ng.tokens = tokens;
+        ng.conf = conf;
+        ng.logits = logits;
+        ng.mask = mask;
+        const long long l0 = launch_count();
+        CUDA_TRY(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed));
+        h->cap_ranges = &ng.ranges;
+        dspark_status s = draft_rows(h, B, seq_ids, anchors, 0, max_keys, tokens, conf, logits, h->cap_stream);
+        h->cap_ranges = nullptr;
+        cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &ng.graph);
+        ng.kernels = launch_count() - l0;
+        note_launch(-(int)ng.kernels);  // capturing is not launching
+        if (s != DSPARK_OK || ce != cudaSuccess) {
+            destroy_graph(ng);
+            if (s != DSPARK_OK) return s;
+            return fail(h, DSPARK_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(ce));
+        }
+        cudaError_t ie = cudaGraphInstantiate(&ng.exec, ng.graph, 0);
+        if (ie != cudaSuccess) {
+            destroy_graph(ng);
+            return fail(h, DSPARK_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+        }
+        if (!ng.ranges.empty()) {
+            size_t n = 0;
+            cudaGraphGetNodes(ng.graph, nullptr, &n);
+            std::vector<cudaGraphNode_t> nodes(n);
+            cudaGraphGetNodes(ng.graph, nodes.data(), &n);
+            for (auto node : nodes) {
+                cudaGraphNodeType t;
+                if (cudaGraphNodeGetType(node, &t) != cudaSuccess || t != cudaGraphNodeTypeEventRecord) continue;
+                cudaEvent_t e;
+                if (cudaGraphEventRecordNodeGetEvent(node, &e) != cudaSuccess) continue;
+                for (auto& r : ng.ranges) {
+                    if (r.a == e) r.na = node;
+                    if (r.b == e) r.nb = node;
+                }
+            }
+        }
+        h->graphs.push_back(std::move(ng));
+        g = &h->graphs.back();
+    }
+    g->last_use = ++h->graph_clock;
+    if (mask) {
+        for (auto& r : g->ranges) {
+            if (!r.na || !r.nb) continue;
+            cudaEvent_t a = pool_event(h), b = pool_event(h);
+            if (!a || !b) break;
+            CUDA_TRY(h, cudaGraphExecEventRecordNodeSetEvent(g->exec, r.na, a));
+            CUDA_TRY(h, cudaGraphExecEventRecordNodeSetEvent(g->exec, r.nb, b));
+            h->prof_ranges.push_back({r.cat, a, b, r.launches});
+        }
+    }
+    CUDA_TRY(h, cudaGraphLaunch(g->exec, st));
+    note_launch((int)g->kernels);
     return DSPARK_OK;
 }
 
@@ -468,7 +626,11 @@ dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const
     int num_sms = 148, dev = 0;
     CUDA_TRY(nullptr, cudaGetDevice(&dev));
     CUDA_TRY(nullptr, cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
-    if (kernel == 0) kernel = (M <= 16 && skinny_ok(M, K)) ? 2 : (dt == DT_BF16 && tc_available() && tc_gemm_ok(M, N, K) ? 3 : 1);
+    if (kernel == 0) {
+        if (M <= 16 && dt == DT_BF16 && tc_stream_ok(M, N, K)) kernel = 4;
+        else if (M <= 16 && skinny_ok(M, K)) kernel = 2;
+        else kernel = (dt == DT_BF16 && tc_available() && tc_gemm_ok(M, N, K)) ? 3 : 1;
+    }
     if (kernel == 1) {
         CUDA_TRY(nullptr, gemm_simt(dt, A_dev, lda, nullptr, dt, W_dev, M, N, K, ep, st));
     } else if (kernel == 2) {
@@ -483,6 +645,38 @@ dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const
         CUDA_TRY(nullptr, tc_prepare(w, W_dev, N, K));
         if (!w.ready) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "tensor map rejected");
         CUDA_TRY(nullptr, tc_gemm(A_dev, lda, w, M, N, K, ep, num_sms, err_word, st));
+    } else if (kernel == 4) {
+        if (dt != DT_BF16 || !tc_stream_ok(M, N, K) || lda % 8 != 0 || ((uintptr_t)A_dev & 15) ||
+            ((uintptr_t)W_dev & 15))
+            return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "shape not for the streaming tensor-core GEMM");
+        // process-wide scratch for this standalone call (grow-only; counters stay zeroed between launches)
+        static float* part = nullptr;
+        static size_t part_floats = 0;
+        static unsigned int* tickets = nullptr;
+        static size_t n_tickets = 0;
+        if (!err_word) CUDA_TRY(nullptr, cudaMalloc((void**)&err_word, sizeof(int)));
+        const size_t need = tc_stream_scratch_floats(N, K, num_sms), tiles = (size_t)(N + 127) / 128;
+        if (need > part_floats) {
+            CUDA_TRY(nullptr, cudaDeviceSynchronize());
+            if (part) cudaFree(part);
+            part = nullptr;
+            part_floats = 0;
+            CUDA_TRY(nullptr, cudaMalloc((void**)&part, need * 4));
+            part_floats = need;
+        }
+        if (tiles > n_tickets) {
+            CUDA_TRY(nullptr, cudaDeviceSynchronize());
+            if (tickets) cudaFree(tickets);
+            tickets = nullptr;
+            n_tickets = 0;
+            CUDA_TRY(nullptr, cudaMalloc((void**)&tickets, tiles * sizeof(unsigned int)));
+            CUDA_TRY(nullptr, cudaMemset(tickets, 0, tiles * sizeof(unsigned int)));
+            n_tickets = tiles;
+        }
+        TcWeightStream w;
+        CUDA_TRY(nullptr, tc_stream_prepare(w, W_dev, N, K));
+        if (!w.ready) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "tensor map rejected");
+        CUDA_TRY(nullptr, tc_stream(A_dev, lda, w, M, N, K, ep, part, part_floats, tickets, n_tickets, num_sms, err_word, st));
     } else {
         return fail(nullptr, DSPARK_ERR_INVALID_ARG, "unknown kernel");
     }
@@ -504,10 +698,11 @@ void dspark_destroy(dspark_handle* h) {
     if (h->rowmap.p) cudaFree(h->rowmap.p);
     if (h->stage_in.p) cudaFree(h->stage_in.p);
     if (h->stage_out.p) cudaFree(h->stage_out.p);
+    for (auto& g : h->graphs) destroy_graph(g);
+    if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
     for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
     tc_release(h->tc_wc);
     tc_release(h->tc_out_proj);
-    tc_release(h->tc_tok_proj);
     for (auto* v : {&h->tc_kv, &h->tc_qkv, &h->tc_wo, &h->tc_wgu, &h->tc_wd})
         for (auto& w : *v) tc_release(w);
     delete h;
@@ -645,6 +840,10 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, (void**)&h->mk_i, (size_t)cfg->max_seqs * h->mk_ctas * 4));
     CTRY(dalloc(h, (void**)&h->mk_cnt, (size_t)cfg->max_seqs * 4));
     CTRY(dalloc(h, (void**)&h->safe_ids, (size_t)cfg->max_seqs * 4));
+    CTRY(dalloc(h, (void**)&h->anchor_dev, sizeof(int)));
+    CTRY(attention_init());
+    CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+    if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));
     CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
     h->ws_floats = (size_t)4 << 20;
@@ -670,6 +869,33 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));
             CTRY(tc_prepare(h->tc_wd[i], h->wd[i], d, F));
         }
+    }
+    if (h->dt == DT_BF16 && tc_stream_ok(1, 1, 64)) {
+        size_t part = 0, tiles = 0;
+        auto prep = [&](TcWeightStream& v, const void* p, int N, int K) -> cudaError_t {
+            part = std::max(part, tc_stream_scratch_floats(N, K, h->num_sms));
+            tiles = std::max(tiles, (size_t)(N + 127) / 128);
+            return tc_stream_prepare(v, p, N, K);
+        };
+        CTRY(prep(h->ts_wc, h->W_c, d, h->mH));
+        CTRY(prep(h->ts_out_proj, h->out_proj, V, d));
+        h->ts_kv.resize(nL);
+        h->ts_qkv.resize(nL);
+        h->ts_wo.resize(nL);
+        h->ts_wgu.resize(nL);
+        h->ts_wd.resize(nL);
+        for (int i = 0; i < nL; ++i) {
+            CTRY(prep(h->ts_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * d, d));
+            CTRY(prep(h->ts_qkv[i], h->wqkv[i], 3 * d, d));
+            CTRY(prep(h->ts_wo[i], h->wo[i], d, d));
+            CTRY(prep(h->ts_wgu[i], h->wgu[i], 2 * F, d));
+            CTRY(prep(h->ts_wd[i], h->wd[i], d, F));
+        }
+        h->ts_part_floats = part;
+        h->ts_n_tickets = tiles;
+        CTRY(dalloc(h, (void**)&h->ts_part, std::max<size_t>(part, 4) * 4));
+        CTRY(dalloc(h, (void**)&h->ts_tickets, tiles * sizeof(unsigned int)));
+        CTRY(cudaMemsetAsync(h->ts_tickets, 0, tiles * sizeof(unsigned int), st));
     }
     CTRY(cudaStreamSynchronize(st));
 #undef CTRY
@@ -699,10 +925,16 @@ dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens
     if (!tokens_dev || !conf_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "tokens or conf is NULL");
     if (last_token < 0 || last_token >= h->cfg.vocab)
         return fail(h, DSPARK_ERR_INVALID_ARG, "last_token " + std::to_string(last_token) + " outside [0, vocab)");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (h->use_graphs) {
+        CUDA_TRY(h, set_len(h->anchor_dev, 0, last_token, st));
+        return draft_graphed(h, 1, nullptr, h->anchor_dev, h->cfg.max_ctx + h->cfg.gamma, tokens_dev, conf_dev,
+                             logits_dev, st);
+    }
     dspark_status s = sync_len(h, 0);
     if (s != DSPARK_OK) return s;
     return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
-                      logits_dev, (cudaStream_t)stream);
+                      logits_dev, st);
 }
 
 dspark_status dspark_ingest_context_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,
@@ -738,6 +970,9 @@ dspark_status dspark_draft_batched(dspark_handle* h, int32_t n_seqs, const int32
     cudaStream_t st = (cudaStream_t)stream;
     CUDA_TRY(h, check_draft_inputs(seq_ids_dev, last_tokens_dev, n_seqs, h->cfg.max_seqs, h->cfg.vocab, h->d_err,
                                    h->safe_ids, h->safe_anchors, st));
+    if (h->use_graphs)
+        return draft_graphed(h, n_seqs, h->safe_ids, h->safe_anchors, h->cfg.max_ctx + h->cfg.gamma, tokens_dev,
+                             conf_dev, logits_dev, st);
     return draft_rows(h, n_seqs, h->safe_ids, h->safe_anchors, 0, h->cfg.max_ctx + h->cfg.gamma, tokens_dev, conf_dev,
                       logits_dev, st);
 }

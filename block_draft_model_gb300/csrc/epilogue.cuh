@@ -61,4 +61,119 @@ __device__ __forceinline__ void epi_pair(const EpiParams& ep, int m, int n_even,
         reinterpret_cast<float*>(ep.out_act)[off] = h;
 }
 
+// 32 consecutive columns [n, n + 32) of row m (n a multiple of 32), with
+// 16-byte vector stores where the layout allows; falls back to one element at
+// a time at the right edge or for unaligned leading dimensions.
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 p = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&p);
+        }
+        d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+__device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+__device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int pos, int c, const float* v) {
+    if (pos < 0 || pos >= ep.max_rows) return;
+    const int64_t off = (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) + (int64_t)pos * ep.d + (c % ep.d);
+    if (ep.cache_dtype == DT_BF16) store_bf16x32(reinterpret_cast<bf16*>(ep.cache) + off, v);
+    else store_f32x32(reinterpret_cast<float*>(ep.cache) + off, v);
+}
+
+__device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v) {
+    const bool full = n + 32 <= N;
+    switch (ep.kind) {
+        case EPI_STORE_F32:
+        case EPI_ADD_F32:
+            if (full && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0) {
+                float* dst = ep.out_f32 + (int64_t)m * ep.ldo + n;
+                if (ep.kind == EPI_ADD_F32) {
+                    float t[32];
+                    const float4* s4 = reinterpret_cast<const float4*>(dst);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 a = s4[q];
+                        t[4 * q] = a.x + v[4 * q];
+                        t[4 * q + 1] = a.y + v[4 * q + 1];
+                        t[4 * q + 2] = a.z + v[4 * q + 2];
+                        t[4 * q + 3] = a.w + v[4 * q + 3];
+                    }
+                    store_f32x32(dst, t);
+                } else {
+                    store_f32x32(dst, v);
+                }
+                return;
+            }
+            break;
+        case EPI_KV_CACHE:
+            if (full && (ep.d & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
+                const int slot = ep.row_seq ? ep.row_seq[m] : 0;
+                const int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
+                cache_store32(ep, slot, pos, n, v);
+                return;
+            }
+            break;
+        case EPI_QKV:
+            if (full && (ep.d & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
+                if (n < ep.d) {
+                    if ((ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0) {
+                        store_f32x32(ep.out_f32 + (int64_t)m * ep.ldo + n, v);
+                        return;
+                    }
+                    break;
+                }
+                const int b = m / ep.gamma, j = m - b * ep.gamma;
+                const int slot = ep.seq_ids ? ep.seq_ids[b] : b;
+                if (slot >= 0) cache_store32(ep, slot, ep.seq_len[slot] + j, n - ep.d, v);
+                return;
+            }
+            break;
+        case EPI_SWIGLU:
+            if (full && (ep.ld_act & 15) == 0 && ((uintptr_t)ep.out_act & 15) == 0) {
+                float h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[i] = act_fn(ep.act, v[2 * i]) * v[2 * i + 1];
+                const int64_t off = (int64_t)m * ep.ld_act + (n >> 1);
+                if (ep.act_dtype == DT_BF16) {
+                    uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(ep.out_act) + off);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 p = __floats2bfloat162_rn(h[8 * q + 2 * i], h[8 * q + 2 * i + 1]);
+                            w[i] = *reinterpret_cast<uint32_t*>(&p);
+                        }
+                        d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(ep.out_act) + off);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                }
+                return;
+            }
+            break;
+        default:
+            return;
+    }
+    if (ep.kind == EPI_SWIGLU) {
+        for (int j = 0; j < 32; j += 2)
+            if (n + j + 1 < N) epi_pair(ep, m, n + j, v[j], v[j + 1]);
+    } else {
+        for (int j = 0; j < 32; ++j)
+            if (n + j < N) epi_one(ep, m, n + j, v[j]);
+    }
+}
+
 }  // namespace dspark

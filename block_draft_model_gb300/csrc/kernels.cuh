@@ -96,6 +96,7 @@ struct AttnParams {
     int out_dtype;
 };
 size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim);
+cudaError_t attention_init();  // once per process/device, before any launch or capture
 cudaError_t attention(const AttnParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ Markov chain, argmax, confidence

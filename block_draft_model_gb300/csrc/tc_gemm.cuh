@@ -26,4 +26,21 @@ bool tc_gemm_ok(int M, int N, int K);
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
                     int num_sms, int* err, cudaStream_t st);
 
+// Weight-streaming variant for M <= 16 activation rows (tc_stream.cu): the
+// weights are the MMA's 128-row side.  `part`/`tickets` are scratch for the
+// split-K partials (tc_stream_scratch_floats floats; one zeroed counter per
+// 128-row tile, left zeroed after every launch).
+struct TcWeightStream {
+    bool ready = false;
+    const void* ptr = nullptr;
+    int N = 0, K = 0;
+    alignas(64) unsigned char tmap[128];
+};
+bool tc_stream_ok(int M, int N, int K);
+size_t tc_stream_scratch_floats(int N, int K, int num_sms);
+cudaError_t tc_stream_prepare(TcWeightStream& w, const void* ptr, int N, int K);
+cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M, int N, int K, const EpiParams& ep,
+                      float* part, size_t part_floats, unsigned int* tickets, size_t n_tickets, int num_sms, int* err,
+                      cudaStream_t st);
+
 }  // namespace dspark

@@ -1,0 +1,280 @@
+// Weight-streaming tensor-core GEMM for a handful of activation rows (the
+// batch-1 draft step: M = gamma <= 16), "swap-AB" on tcgen05:
+//   acc[m, n] = sum_k X[m, k] W[n, k]       W: [N, K] bf16, X: [M <= 16, K] bf16
+// W supplies the MMA's M side (128 weight rows per tile, streamed once from
+// HBM by TMA with the 128-byte swizzle) and X the N side (16 columns; TMA fills
+// the rows beyond M with zeros).  Each tcgen05.mma is 128x16x16; the fp32
+// accumulator is 16 TMEM columns.
+//
+// The work is HBM-bound, so the layout serves bytes in flight: a CTA owns one
+// (128-row tile, K slice) unit, keeps STAGES 18 KB stages in flight, and two
+// CTAs fit on an SM.  When the weight rows alone cannot fill the GPU, K is split
+// over CTAs; each CTA writes its 128x16 partial to scratch and the last CTA of
+// the tile (ticket counter, no spinning) adds the partials in split order and
+// applies the epilogue, so results do not depend on scheduling.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "epilogue.cuh"
+#include "tc_common.cuh"
+#include "tc_gemm.cuh"
+
+namespace dspark {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 16, BK = 64, STAGES = 6;
+constexpr int W_BYTES = BM * BK * 2;  // 16 KB
+constexpr int X_BYTES = BN * BK * 2;  // 2 KB
+constexpr int TMEM_COLS = 32;
+constexpr int NTHREADS = 192;
+
+constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (W_BYTES + X_BYTES) + 256; }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// grid: n_tiles * splits CTAs; CTA b handles tile b / splits, K blocks
+// [s * kb_per, min(nkb, (s + 1) * kb_per)) with s = b % splits.
+__global__ void __launch_bounds__(NTHREADS, 2)
+    k_tc_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
+                int splits, int kb_per, EpiParams ep, float* __restrict__ part, unsigned int* __restrict__ tickets,
+                int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sW = smem_u32(smem);
+    const uint32_t sX = sW + STAGES * W_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (W_BYTES + X_BYTES));
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* acc_full = bars + 2 * STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* is_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / splits, split = blockIdx.x - tile * splits;
+    const int nkb = (K + BK - 1) / BK;
+    const int kb0 = split * kb_per, kb1 = min(nkb, kb0 + kb_per);
+    const int n0 = tile * BM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) break;
+                mbar_arrive_expect_tx(&full[stage], W_BYTES + X_BYTES);
+                tma_load_2d(sW + stage * W_BYTES, &tmW, &full[stage], kb * BK, n0);
+                tma_load_2d(sX + stage * X_BYTES, &tmX, &full[stage], kb * BK, 0);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id = idesc(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dw = sdesc(sW + stage * W_BYTES);
+                const uint64_t dx = sdesc(sX + stage * X_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma(tmem, dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), id, (kb > kb0 || k > 0) ? 1u : 0u);
+                umma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            umma_commit(acc_full);  // also drains: completes once every MMA above has retired
+            if (ok) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(acc_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                }
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;  // weight row within the tile
+        const int n = n0 + row;
+        float v[BN];
+        bool have = mbar_wait(acc_full, 0, abort_flag) && !*abort_flag;
+        if (have) {
+            tc_fence_after();
+            uint32_t r[BN];
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16), r);
+#pragma unroll
+            for (int m = 0; m < BN; ++m) v[m] = __uint_as_float(r[m]);
+        } else {
+#pragma unroll
+            for (int m = 0; m < BN; ++m) v[m] = 0.f;
+        }
+        bool final_ = (splits == 1);
+        if (splits > 1) {
+            float4* dst = reinterpret_cast<float4*>(part + (((int64_t)tile * splits + split) * BM + row) * BN);
+#pragma unroll
+            for (int c = 0; c < BN / 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            __threadfence();
+            epi_bar();
+            if (threadIdx.x == 64) {
+                const unsigned int t = atomicAdd(&tickets[tile], 1u);
+                *is_last = (t == (unsigned int)splits - 1);
+            }
+            epi_bar();
+            if (*is_last) {
+                __threadfence();
+#pragma unroll
+                for (int m = 0; m < BN; ++m) v[m] = 0.f;
+                for (int s = 0; s < splits; ++s) {
+                    const float4* src = reinterpret_cast<const float4*>(part + (((int64_t)tile * splits + s) * BM + row) * BN);
+#pragma unroll
+                    for (int c = 0; c < BN / 4; ++c) {
+                        const float4 t = __ldcg(src + c);
+                        v[4 * c] += t.x;
+                        v[4 * c + 1] += t.y;
+                        v[4 * c + 2] += t.z;
+                        v[4 * c + 3] += t.w;
+                    }
+                }
+                if (threadIdx.x == 64) tickets[tile] = 0u;
+                final_ = true;
+            }
+        }
+        if (final_ && have) {
+            if (ep.kind == EPI_SWIGLU) {
+                // (gate, up) rows are adjacent lanes: even lanes take their odd neighbour's value
+#pragma unroll
+                for (int m = 0; m < BN; ++m) {
+                    const float up = __shfl_down_sync(0xffffffffu, v[m], 1);
+                    if (m < M && !(lane & 1) && n + 1 < N) epi_pair(ep, m, n, v[m], up);
+                }
+            } else if (n < N) {
+#pragma unroll
+                for (int m = 0; m < BN; ++m)
+                    if (m < M) epi_one(ep, m, n, v[m]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(err, DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+bool g_ready = false;
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+
+bool ready() {
+    if (g_ready) return true;
+    if (!tc_available()) return false;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    if (cudaFuncSetAttribute(k_tc_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
+        return false;
+    g_ready = true;
+    return true;
+}
+
+bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && N >= 1 && K >= BK && K % 8 == 0; }
+
+size_t tc_stream_scratch_floats(int N, int K, int num_sms) {
+    const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
+    int splits = (2 * num_sms + nT - 1) / nT;
+    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 16 ? 16 : splits));
+    return splits > 1 ? (size_t)nT * splits * BM * BN : 0;
+}
+
+cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M, int N, int K, const EpiParams& ep,
+                      float* part, size_t part_floats, unsigned int* tickets, size_t n_tickets, int num_sms, int* err,
+                      cudaStream_t st) {
+    if (!w.ready || !tc_stream_ok(M, N, K) || N != w.N || K != w.K) return cudaErrorInvalidValue;
+    if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
+    const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
+    int splits = (2 * num_sms + nT - 1) / nT;
+    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 16 ? 16 : splits));
+    while (splits > 1 && ((size_t)nT * splits * BM * BN > part_floats || (size_t)nT > n_tickets)) --splits;
+    int kb_per = (nkb + splits - 1) / splits;
+    splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
+    CUtensorMap tmX;
+    if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
+    k_tc_stream<<<nT * splits, NTHREADS, smem_bytes(), st>>>(*reinterpret_cast<const CUtensorMap*>(w.tmap), tmX, M, N,
+                                                              K, splits, kb_per, ep, part, tickets, err);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t tc_stream_prepare(TcWeightStream& w, const void* ptr, int N, int K) {
+    w.ready = false;
+    w.ptr = ptr;
+    w.N = N;
+    w.K = K;
+    if (!ready()) return cudaSuccess;
+    if (K % 8 != 0 || ((uintptr_t)ptr & 15) != 0) return cudaSuccess;
+    if (!encode(reinterpret_cast<CUtensorMap*>(w.tmap), ptr, N, K, K, BM)) return cudaSuccess;
+    w.ready = true;
+    return cudaSuccess;
+}
+
+}  // namespace dspark

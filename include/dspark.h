@@ -211,7 +211,8 @@ int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_ho
  * (dtype DSPARK_BF16) or both float32 (DSPARK_FP32); out_dev [M, N] float32
  * with row stride ldo.  `kernel` selects the implementation: 0 the one the step
  * would use for this shape, 1 SIMT tiles, 2 weight streaming (M <= 16, K % 8 == 0),
- * 3 tcgen05 tensor cores (bf16, K >= 64, K % 8 == 0, 16-byte aligned rows).
+ * 3 tcgen05 tensor cores (bf16, K >= 64, K % 8 == 0, 16-byte aligned rows),
+ * 4 tcgen05 weight streaming (as 3, and M <= 16).
  * DSPARK_ERR_UNSUPPORTED if the chosen kernel cannot take the shape. */
 dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
                             int32_t K, float* out_dev, int64_t ldo, int32_t kernel, void* stream);

@@ -22,18 +22,19 @@ def _lib():
     bdm.load()
 
 
-SHAPES = [(1, 64, 64), (5, 1000, 1024), (8, 4096, 2048), (16, 3072, 1024), (17, 300, 136),
+SHAPES = [(1, 64, 64), (5, 1000, 1024), (8, 4096, 2048), (16, 3072, 1024), (17, 300, 136), (3, 73448, 2048),
+          (8, 2048, 10240), (2, 130, 200),
           (128, 256, 64), (129, 257, 192), (320, 1000, 1024), (1024, 1024, 10240), (777, 2048, 1024)]
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_linear_kernels(kernel, shape):
     import block_draft_model_gb300 as bdm
     M, N, K = shape
-    if kernel == 2 and M > 16:
+    if kernel in (2, 4) and M > 16:
         pytest.skip("weight streaming takes M <= 16")
-    if kernel == 3 and K < 64:
+    if kernel in (3, 4) and K < 64:
         pytest.skip("tensor-core path takes K >= 64")
     A = syn.normal_bf16(7, 1, (M, K))
     W = syn.normal_bf16(7, 2, (N, K), 0.05)
