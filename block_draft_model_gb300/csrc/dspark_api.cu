@@ -102,6 +102,7 @@ struct dspark_handle {
     void* h_lp = nullptr;
     float* attn_part = nullptr;
     size_t attn_part_floats = 0;
+    unsigned int* attn_tickets = nullptr;    // [max_seqs * n_heads]
     float* mk_v = nullptr;
     int* mk_i = nullptr;
     unsigned int* mk_cnt = nullptr;
@@ -169,11 +170,11 @@ cudaError_t grow(DevBuf& b, size_t bytes) {
 }
 
 int attn_chunks(const dspark_handle* h, int B, int max_keys) {
-    // enough CTAs for two per SM, but at least 32 keys per chunk
+    // enough CTAs for two per SM, but at least 256 keys (four tiles) per range
     const int nh = h->cfg.n_heads;
     int want = (2 * h->num_sms + nh * B - 1) / (nh * B);
-    int by_keys = (max_keys + 31) / 32;
-    return std::max(1, std::min(want, by_keys));
+    int by_keys = (max_keys + 255) / 256;
+    return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks()));
 }
 
 // A weight and its tensor-core views.
@@ -284,6 +285,8 @@ dspark_status check_cfg(const dspark_config* c, std::string& why) {
     const int hd = c->d_draft / c->n_heads;
     if (c->gamma > 16) { why = "gamma > 16"; return DSPARK_ERR_UNSUPPORTED; }
     if (hd > 256 || hd % 8 != 0) { why = "head_dim must be a multiple of 8 and <= 256"; return DSPARK_ERR_UNSUPPORTED; }
+    if (256 % (hd / 8) != 0 || c->gamma > 256 / (hd / 8)) { why = "gamma * head_dim must be <= 2048 with head_dim / 8 dividing 256"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->dtype == DSPARK_FP32 && hd > 128) { why = "fp32 drafters take head_dim <= 128"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->d_draft % 64 != 0) { why = "d_draft must be a multiple of 64"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->markov_rank % 8 != 0 || c->markov_rank > 1024) { why = "markov_rank must be a multiple of 8, <= 1024"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
@@ -392,6 +395,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ap.n_heads = c.n_heads;
         ap.n_chunks = attn_chunks(h, B, max_keys);
         ap.part = h->attn_part;
+        ap.tickets = h->attn_tickets;
         ap.out = actA;
         ap.out_dtype = adt;
         if (attn_scratch_floats(B, c.n_heads, ap.n_chunks, c.gamma, h->hd) > h->attn_part_floats)
@@ -834,6 +838,9 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         }
         h->attn_part_floats = worst;
         CTRY(dalloc(h, (void**)&h->attn_part, worst * 4));
+        const size_t nt = (size_t)cfg->max_seqs * cfg->n_heads;
+        CTRY(dalloc(h, (void**)&h->attn_tickets, nt * sizeof(unsigned int)));
+        CTRY(cudaMemsetAsync(h->attn_tickets, 0, nt * sizeof(unsigned int), st));
     }
     h->mk_ctas = markov_ctas(V);
     CTRY(dalloc(h, (void**)&h->mk_v, (size_t)cfg->max_seqs * h->mk_ctas * 4));

@@ -90,12 +90,14 @@ struct AttnParams {
     const int* seq_len;      // context length per slot (block rows sit at len .. len+gamma-1)
     const int* seq_ids;      // slot of sequence b (nullptr: b)
     int B, gamma, d, n_heads;
-    int n_chunks;            // split of the (len + gamma) keys of one sequence
+    int n_chunks;            // split of the (len + gamma) keys of one sequence, 1 .. attn_max_chunks()
     float* part;             // scratch: B * n_heads * n_chunks * gamma * (head_dim + 2) floats
+    unsigned int* tickets;   // scratch: B * n_heads counters, zero before and after every launch
     void* out;               // [B*gamma, d] attention output, out_dtype
     int out_dtype;
 };
 size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim);
+int attn_max_chunks();
 cudaError_t attention_init();  // once per process/device, before any launch or capture
 cudaError_t attention(const AttnParams& p, cudaStream_t st);
 

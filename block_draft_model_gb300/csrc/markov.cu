@@ -7,8 +7,10 @@
 //   conf_k  = sigmoid(conf_w . [y_k ; e] + conf_b)
 // One fused launch per position: every CTA streams a slice of w2, adds the
 // base logits, keeps its best (value, index); the last CTA to finish (ticket
-// counter, no spinning) reduces the CTA results in a fixed order, writes the
-// token and the confidence, and re-arms the counter.  The token stays on the
+// counter, no spinning) reduces the CTA results, writes the token and the
+// confidence, and re-arms the counter.  Four lanes share a vocabulary row (128
+// bytes each for r = 256), so every load is a full 32-byte sector and a row
+// needs a two-step shuffle; two rows per lane group are in flight at once.  The token stays on the
 // device, where the next position's launch reads it.
 #include <climits>
 #include <math.h>
@@ -21,7 +23,8 @@ namespace dspark {
 namespace {
 
 constexpr int NT = 256;
-constexpr int RW = 4;          // rows per warp in flight
+constexpr int LPR = 4;         // lanes per vocabulary row
+constexpr int RPW = 32 / LPR;  // rows per warp pass
 constexpr int RMAX = 1024;     // largest Markov rank
 
 template <typename TW>
@@ -44,40 +47,60 @@ __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
     const int rows = (V + gridDim.x - 1) / gridDim.x;
     const int v_begin = blockIdx.x * rows, v_end = min(V, v_begin + rows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane & (LPR - 1), rw = lane / LPR;
     const int64_t urow = (int64_t)(b * p.gamma + k) * V;
     const int nvec = r / VE;
 
     ArgBest best{-INFINITY, INT_MAX};
-    for (int v0 = v_begin + warp * RW; v0 < v_end; v0 += (NT / 32) * RW) {
-        float acc[RW];
+    // each pass: 8 rows per warp, 4 lanes per row, two passes in flight
+    for (int v0 = v_begin + warp * (2 * RPW); v0 < v_end; v0 += (NT / 32) * (2 * RPW)) {
+        const int va = v0 + rw, vb = v0 + RPW + rw;
+        const TW* ra = w2 + (int64_t)min(va, v_end - 1) * r;
+        const TW* rb = w2 + (int64_t)min(vb, v_end - 1) * r;
+        float aa = 0.f, ab = 0.f;
+        for (int vi = sub; vi < nvec; vi += 4 * LPR) {
+            uint4 ua[4], ub[4];
 #pragma unroll
-        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
-        for (int vi = lane; vi < nvec; vi += 32) {
-            uint4 u[RW];
-#pragma unroll
-            for (int i = 0; i < RW; ++i) {
-                const int v = min(v0 + i, v_end - 1);
-                u[i] = ld_stream16(w2 + (int64_t)v * r + vi * VE);
+            for (int q = 0; q < 4; ++q) {
+                const int x = vi + q * LPR;
+                ua[q] = x < nvec ? __ldg(reinterpret_cast<const uint4*>(ra + x * VE)) : make_uint4(0, 0, 0, 0);
+                ub[q] = x < nvec ? __ldg(reinterpret_cast<const uint4*>(rb + x * VE)) : make_uint4(0, 0, 0, 0);
             }
-            const float* ep = e + vi * VE;
 #pragma unroll
-            for (int i = 0; i < RW; ++i) {
-                float f[VE];
-                Vec16<TW>::unpack(u[i], f);
+            for (int q = 0; q < 4; ++q) {
+                const int x = vi + q * LPR;
+                if (x >= nvec) break;
+                float fa[VE], fb[VE];
+                Vec16<TW>::unpack(ua[q], fa);
+                Vec16<TW>::unpack(ub[q], fb);
+                const float* ep = e + x * VE;
 #pragma unroll
-                for (int q = 0; q < VE; ++q) acc[i] = fmaf(f[q], ep[q], acc[i]);
+                for (int t = 0; t < VE; ++t) {
+                    aa = fmaf(fa[t], ep[t], aa);
+                    ab = fmaf(fb[t], ep[t], ab);
+                }
             }
         }
 #pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            const float bias = warp_sum(acc[i]);
-            const int v = v0 + i;
-            if (v < v_end) {
-                const float l = p.U[urow + v] + bias;
-                if (p.logits && lane == 0) p.logits[urow + v] = l;
-                if (better(l, v, best.v, best.i)) {
+        for (int o = 1; o < LPR; o <<= 1) {
+            aa += __shfl_xor_sync(0xffffffffu, aa, o);
+            ab += __shfl_xor_sync(0xffffffffu, ab, o);
+        }
+        if (sub == 0) {
+            if (va < v_end) {
+                const float l = p.U[urow + va] + aa;
+                if (p.logits) p.logits[urow + va] = l;
+                if (better(l, va, best.v, best.i)) {
                     best.v = l;
-                    best.i = v;
+                    best.i = va;
+                }
+            }
+            if (vb < v_end) {
+                const float l = p.U[urow + vb] + ab;
+                if (p.logits) p.logits[urow + vb] = l;
+                if (better(l, vb, best.v, best.i)) {
+                    best.v = l;
+                    best.i = vb;
                 }
             }
         }
@@ -104,7 +127,8 @@ __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // last CTA of this sequence: fixed-order reduction of the CTA results
+    // last CTA of this sequence: reduction of the CTA results (the key is a total order, so the
+    // result does not depend on the order of arrival)
     ArgBest fb{-INFINITY, INT_MAX};
     for (int c = threadIdx.x; c < (int)gridDim.x; c += NT) {
         const float v = __ldcg(p.part_v + b * gridDim.x + c);
@@ -146,8 +170,8 @@ __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
 }  // namespace
 
 int markov_ctas(int V) {
-    int c = (V + 511) / 512;
-    return c < 1 ? 1 : (c > 1024 ? 1024 : c);
+    int c = (V + 255) / 256;  // 256 vocabulary rows per CTA
+    return c < 1 ? 1 : (c > 2048 ? 2048 : c);
 }
 
 cudaError_t markov_step(const MarkovParams& p, cudaStream_t st) {

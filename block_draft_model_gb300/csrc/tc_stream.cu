@@ -168,7 +168,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 __threadfence();
 #pragma unroll
                 for (int m = 0; m < BN; ++m) v[m] = 0.f;
-                for (int s = 0; s < splits; ++s) {
+                // splits added in order; four splits' loads in flight at a time
+                int s = 0;
+                for (; s + 4 <= splits; s += 4) {
+                    float4 t[4][BN / 4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4* src =
+                            reinterpret_cast<const float4*>(part + (((int64_t)tile * splits + s + u) * BM + row) * BN);
+#pragma unroll
+                        for (int c = 0; c < BN / 4; ++c) t[u][c] = __ldcg(src + c);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int c = 0; c < BN / 4; ++c) {
+                            v[4 * c] += t[u][c].x;
+                            v[4 * c + 1] += t[u][c].y;
+                            v[4 * c + 2] += t[u][c].z;
+                            v[4 * c + 3] += t[u][c].w;
+                        }
+                }
+                for (; s < splits; ++s) {
                     const float4* src = reinterpret_cast<const float4*>(part + (((int64_t)tile * splits + s) * BM + row) * BN);
 #pragma unroll
                     for (int c = 0; c < BN / 4; ++c) {
@@ -242,7 +263,7 @@ bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && 
 size_t tc_stream_scratch_floats(int N, int K, int num_sms) {
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
     int splits = (2 * num_sms + nT - 1) / nT;
-    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 16 ? 16 : splits));
+    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 8 ? 8 : splits));
     return splits > 1 ? (size_t)nT * splits * BM * BN : 0;
 }
 
@@ -253,7 +274,7 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
     int splits = (2 * num_sms + nT - 1) / nT;
-    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 16 ? 16 : splits));
+    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 8 ? 8 : splits));
     while (splits > 1 && ((size_t)nT * splits * BM * BN > part_floats || (size_t)nT > n_tickets)) --splits;
     int kb_per = (nkb + splits - 1) / splits;
     splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
