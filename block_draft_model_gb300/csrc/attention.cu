@@ -296,13 +296,21 @@ __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
     if (tid == 0) p.tickets[bh] = 0u;
 }
 
-constexpr int SMEM_LIMIT = 227 * 1024;
+int g_smem_limit = 0;  // largest dynamic shared memory the kernels may request on this device
 
 template <typename TC, typename TO>
 cudaError_t set_attr() {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_attention<TC, TO>);
+    if (e != cudaSuccess) return e;
+    int dev = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    const int limit = optin - (int)fa.sharedSizeBytes;
+    g_smem_limit = limit;
     const int sm = Layout<TC>(HMAX, GMAX).bytes();
     return cudaFuncSetAttribute(k_attention<TC, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                sm < SMEM_LIMIT ? sm : SMEM_LIMIT);
+                                sm < limit ? sm : limit);
 }
 
 }  // namespace
@@ -326,7 +334,8 @@ cudaError_t attention(const AttnParams& p, cudaStream_t st) {
     if (p.gamma > GMAX || hd > HMAX || hd % 8 != 0 || p.n_chunks < 1 || p.n_chunks > CMAX || NT % (hd / 8) != 0 ||
         p.gamma > NT / (hd / 8))
         return cudaErrorInvalidValue;
-    if (p.cache_dtype != DT_BF16 && Layout<float>(hd, p.gamma).bytes() > SMEM_LIMIT) return cudaErrorInvalidValue;
+    const int need = p.cache_dtype == DT_BF16 ? Layout<bf16>(hd, p.gamma).bytes() : Layout<float>(hd, p.gamma).bytes();
+    if (need > g_smem_limit) return cudaErrorInvalidValue;
     dim3 grid(p.n_chunks, p.n_heads, p.B);
     if (p.cache_dtype == DT_BF16) {
         const size_t sm = Layout<bf16>(hd, p.gamma).bytes();
