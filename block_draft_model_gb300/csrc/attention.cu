@@ -83,6 +83,8 @@ __device__ __forceinline__ void unpack8(const uint8_t* p, float* f) {
 
 template <typename TC, typename TO>
 __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t sm[];
     const int gamma = p.gamma, d = p.d, hd = d / p.n_heads;
     const Layout<TC> L(hd, gamma);
@@ -339,12 +341,12 @@ cudaError_t attention(const AttnParams& p, cudaStream_t st) {
     dim3 grid(p.n_chunks, p.n_heads, p.B);
     if (p.cache_dtype == DT_BF16) {
         const size_t sm = Layout<bf16>(hd, p.gamma).bytes();
-        if (p.out_dtype == DT_BF16) k_attention<bf16, bf16><<<grid, NT, sm, st>>>(p);
-        else k_attention<bf16, float><<<grid, NT, sm, st>>>(p);
+        if (p.out_dtype == DT_BF16) launch(k_attention<bf16, bf16>, grid, NT, sm, st, p);
+        else launch(k_attention<bf16, float>, grid, NT, sm, st, p);
     } else {
         const size_t sm = Layout<float>(hd, p.gamma).bytes();
-        if (p.out_dtype == DT_BF16) k_attention<float, bf16><<<grid, NT, sm, st>>>(p);
-        else k_attention<float, float><<<grid, NT, sm, st>>>(p);
+        if (p.out_dtype == DT_BF16) launch(k_attention<float, bf16>, grid, NT, sm, st, p);
+        else launch(k_attention<float, float>, grid, NT, sm, st, p);
     }
     note_launch();
     return cudaGetLastError();

@@ -11,6 +11,36 @@ namespace dspark {
 
 typedef __nv_bfloat16 bf16;
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the step is launched with programmatic stream serialization:
+// it may start while its predecessor is still running.  pdl_trigger() lets the
+// next kernel start launching; pdl_wait() blocks until every predecessor grid
+// has completed and its memory is visible.  Each kernel calls pdl_wait() before
+// it touches memory that an earlier kernel writes or reads, and before it
+// exits, so completion stays transitive along the stream.  Both are no-ops for
+// a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with programmatic stream serialization (when enabled).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- element access
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }

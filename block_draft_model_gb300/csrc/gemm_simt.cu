@@ -19,6 +19,8 @@ __device__ __forceinline__ void load8(const T* row, int64_t k, int K, float* f) 
 template <typename TA, typename TW>
 __global__ void __launch_bounds__(NT) k_gemm_simt(const TA* __restrict__ A, int64_t lda, const int* __restrict__ a_rows,
                                                   const TW* __restrict__ W, int M, int N, int K, EpiParams ep) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float As[BK][BM + 4];
     __shared__ float Ws[BK][BN + 4];
     const int tid = threadIdx.x;
@@ -91,13 +93,13 @@ cudaError_t gemm_simt(int a_dtype, const void* A, int64_t lda, const int* a_rows
     if (M <= 0 || N <= 0) return cudaSuccess;
     dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
     if (a_dtype == DT_F32 && w_dtype == DT_F32)
-        k_gemm_simt<float, float><<<grid, NT, 0, st>>>((const float*)A, lda, a_rows, (const float*)W, M, N, K, ep);
+        launch(k_gemm_simt<float, float>, grid, NT, 0, st, (const float*)A, lda, a_rows, (const float*)W, M, N, K, ep);
     else if (a_dtype == DT_BF16 && w_dtype == DT_BF16)
-        k_gemm_simt<bf16, bf16><<<grid, NT, 0, st>>>((const bf16*)A, lda, a_rows, (const bf16*)W, M, N, K, ep);
+        launch(k_gemm_simt<bf16, bf16>, grid, NT, 0, st, (const bf16*)A, lda, a_rows, (const bf16*)W, M, N, K, ep);
     else if (a_dtype == DT_F32 && w_dtype == DT_BF16)
-        k_gemm_simt<float, bf16><<<grid, NT, 0, st>>>((const float*)A, lda, a_rows, (const bf16*)W, M, N, K, ep);
+        launch(k_gemm_simt<float, bf16>, grid, NT, 0, st, (const float*)A, lda, a_rows, (const bf16*)W, M, N, K, ep);
     else
-        k_gemm_simt<bf16, float><<<grid, NT, 0, st>>>((const bf16*)A, lda, a_rows, (const float*)W, M, N, K, ep);
+        launch(k_gemm_simt<bf16, float>, grid, NT, 0, st, (const bf16*)A, lda, a_rows, (const float*)W, M, N, K, ep);
     note_launch();
     return cudaGetLastError();
 }

@@ -24,6 +24,8 @@ template <typename TW, typename TA, int MR>
 __global__ void __launch_bounds__(NT) k_skinny(const TA* __restrict__ A, int64_t lda, const int* __restrict__ a_rows,
                                                int a_row0, const TW* __restrict__ W, int M, int N, int K,
                                                int k_per_split, EpiParams ep, float* __restrict__ ws) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int VE = Vec16<TW>::N;         // weight elements per 16-byte vector
     constexpr int KC = SMEM_FLOATS / MR;     // activation chunk (columns)
     __shared__ __align__(16) float As[MR * KC];
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(NT) k_skinny(const TA* __restrict__ A, int64_t
 
 // Fixed-order sum of the split-K partials, then the epilogue.
 __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M, int N, EpiParams ep) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t total = (int64_t)M * N;
     const bool pairs = ep.kind == EPI_SWIGLU;
     const int64_t items = pairs ? total / 2 : total;
@@ -161,13 +165,13 @@ cudaError_t launch(const void* A, int64_t lda, const int* a_rows, int a_row0, co
     kps = (kps + 7) / 8 * 8;
     splits = (K + kps - 1) / kps;
     dim3 grid(row_ctas, splits);
-    k_skinny<TW, TA, MR><<<grid, NT, 0, st>>>((const TA*)A, lda, a_rows, a_row0, (const TW*)W, M, N, K, kps, ep, ws);
+    launch(k_skinny<TW, TA, MR>, grid, NT, 0, st, (const TA*)A, lda, a_rows, a_row0, (const TW*)W, M, N, K, kps, ep, ws);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || splits == 1) return e;
     int64_t items = (int64_t)M * N;
     int blocks = (int)std::min<int64_t>((items + 255) / 256, 8 * num_sms);
-    k_splitk_reduce<<<blocks, 256, 0, st>>>(ws, splits, M, N, ep);
+    launch(k_splitk_reduce, blocks, 256, 0, st, ws, splits, M, N, ep);
     note_launch();
     return cudaGetLastError();
 }

@@ -29,6 +29,8 @@ constexpr int RMAX = 1024;     // largest Markov rank
 
 template <typename TW>
 __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int VE = Vec16<TW>::N;
     __shared__ __align__(16) float e[RMAX];
     __shared__ float red_v[NT / 32];
@@ -178,9 +180,9 @@ cudaError_t markov_step(const MarkovParams& p, cudaStream_t st) {
     if (p.r > RMAX || p.r % 8 != 0) return cudaErrorInvalidValue;
     dim3 grid(p.ctas, p.B);
     if (p.w_dtype == DT_BF16)
-        k_markov<bf16><<<grid, NT, 0, st>>>(p);
+        launch(k_markov<bf16>, grid, NT, 0, st, p);
     else
-        k_markov<float><<<grid, NT, 0, st>>>(p);
+        launch(k_markov<float>, grid, NT, 0, st, p);
     note_launch();
     return cudaGetLastError();
 }

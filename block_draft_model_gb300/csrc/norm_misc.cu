@@ -1,4 +1,6 @@
 // Row normalisations, block set-up and per-sequence bookkeeping kernels.
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -14,6 +16,8 @@ template <typename TO>
 __global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x, int64_t ldx,
                                                      const float* __restrict__ w, int n, float eps, TO* out,
                                                      int64_t ldo) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[32];
     const float* xr = x + (int64_t)blockIdx.x * ldx;
     float ss = 0.f;
@@ -34,6 +38,8 @@ __global__ void __launch_bounds__(NT) k_ingest_norm(const float* __restrict__ P,
                                                     const float* __restrict__ ctx_norm,
                                                     const float* const* __restrict__ attn_norm, int n_layers, TO* out,
                                                     int64_t layer_stride) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float h[];
     __shared__ float red[32];
     const float* pr = P + (int64_t)blockIdx.x * d;
@@ -60,6 +66,8 @@ __global__ void __launch_bounds__(NT) k_ingest_norm(const float* __restrict__ P,
 }
 
 __global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc, int B, int gamma, int d) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t total = (int64_t)B * gamma * d, per = (int64_t)gamma * d;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
         x[i] = bc[i % per];
@@ -68,6 +76,8 @@ __global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc
 __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int total,
                                 const int* __restrict__ seq_len, int max_seqs, int max_ctx, int* row_seq, int* row_pos,
                                 int* err) {
+    pdl_trigger();
+    pdl_wait();
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
         // sequence i with cu[i] <= t < cu[i+1] (binary search over the prefix sums)
         int lo = 0, hi = n_seqs - 1;
@@ -97,6 +107,8 @@ __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __re
 
 __global__ void k_ingest_commit(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int* seq_len,
                                 int max_seqs, int max_ctx) {
+    pdl_trigger();
+    pdl_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seqs; i += gridDim.x * blockDim.x) {
         const int sid = seq_ids[i];
         if (sid < 0 || sid >= max_seqs) continue;
@@ -105,11 +117,17 @@ __global__ void k_ingest_commit(const int* __restrict__ seq_ids, const int* __re
     }
 }
 
-__global__ void k_add_len(int* seq_len, int slot, int delta) { seq_len[slot] += delta; }
-__global__ void k_set_len(int* seq_len, int slot, int value) { seq_len[slot] = value; }
+__global__ void k_add_len(int* seq_len, int slot, int delta) {
+    pdl_trigger();
+    pdl_wait(); seq_len[slot] += delta; }
+__global__ void k_set_len(int* seq_len, int slot, int value) {
+    pdl_trigger();
+    pdl_wait(); seq_len[slot] = value; }
 
 __global__ void k_check_draft(const int* __restrict__ seq_ids, const int* __restrict__ anchors, int n, int max_seqs,
                               int V, int* err, int* safe_ids, int* safe_anchors) {
+    pdl_trigger();
+    pdl_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const int sid = seq_ids[i];
         const bool bad_id = sid < 0 || sid >= max_seqs;
@@ -124,6 +142,8 @@ __global__ void k_check_draft(const int* __restrict__ seq_ids, const int* __rest
 template <typename T>
 __global__ void k_block_const(const T* __restrict__ mask_emb, const T* __restrict__ block_pos, int gamma, int d,
                               float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < gamma * d; i += gridDim.x * blockDim.x) {
         const int j = i / d;
         float v = to_f32(block_pos[i]);
@@ -134,11 +154,22 @@ __global__ void k_block_const(const T* __restrict__ mask_emb, const T* __restric
 
 template <typename T>
 __global__ void k_to_float(const T* __restrict__ in, int64_t n, float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = to_f32(in[i]);
 }
 
 }  // namespace
+
+static int g_pdl = -1;
+bool pdl_enabled() {
+    if (g_pdl < 0) {
+        const char* e = getenv("DSPARK_NO_PDL");
+        g_pdl = (e && e[0] == '1') ? 0 : 1;
+    }
+    return g_pdl == 1;
+}
 
 static long long g_launches = 0;
 long long launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
@@ -148,9 +179,9 @@ cudaError_t block_const_init(int dtype, const void* mask_emb, const void* block_
                              cudaStream_t st) {
     const int blocks = std::max(1, std::min((gamma * d + 255) / 256, 1024));
     if (dtype == DT_BF16)
-        k_block_const<bf16><<<blocks, 256, 0, st>>>((const bf16*)mask_emb, (const bf16*)block_pos, gamma, d, out);
+        launch(k_block_const<bf16>, blocks, 256, 0, st, (const bf16*)mask_emb, (const bf16*)block_pos, gamma, d, out);
     else
-        k_block_const<float><<<blocks, 256, 0, st>>>((const float*)mask_emb, (const float*)block_pos, gamma, d, out);
+        launch(k_block_const<float>, blocks, 256, 0, st, (const float*)mask_emb, (const float*)block_pos, gamma, d, out);
     note_launch();
     return cudaGetLastError();
 }
@@ -159,9 +190,9 @@ cudaError_t to_float(int dtype, const void* in, int64_t n, float* out, cudaStrea
     if (n <= 0) return cudaSuccess;
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024));
     if (dtype == DT_BF16)
-        k_to_float<bf16><<<blocks, 256, 0, st>>>((const bf16*)in, n, out);
+        launch(k_to_float<bf16>, blocks, 256, 0, st, (const bf16*)in, n, out);
     else
-        k_to_float<float><<<blocks, 256, 0, st>>>((const float*)in, n, out);
+        launch(k_to_float<float>, blocks, 256, 0, st, (const float*)in, n, out);
     note_launch();
     return cudaGetLastError();
 }
@@ -170,9 +201,9 @@ cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, 
                          void* out, int64_t ldo, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     if (out_dtype == DT_BF16)
-        k_rmsnorm_rows<bf16><<<rows, NT, 0, st>>>(x, ldx, w, n, eps, (bf16*)out, ldo);
+        launch(k_rmsnorm_rows<bf16>, rows, NT, 0, st, x, ldx, w, n, eps, (bf16*)out, ldo);
     else
-        k_rmsnorm_rows<float><<<rows, NT, 0, st>>>(x, ldx, w, n, eps, (float*)out, ldo);
+        launch(k_rmsnorm_rows<float>, rows, NT, 0, st, x, ldx, w, n, eps, (float*)out, ldo);
     note_launch();
     return cudaGetLastError();
 }
@@ -183,11 +214,9 @@ cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float*
     if (rows <= 0) return cudaSuccess;
     size_t sm = (size_t)d * sizeof(float);
     if (out_dtype == DT_BF16)
-        k_ingest_norm<bf16><<<rows, NT, sm, st>>>(P, d, eps, ctx_norm, attn_norm_dev, n_layers, (bf16*)out,
-                                                  layer_stride);
+        launch(k_ingest_norm<bf16>, rows, NT, sm, st, P, d, eps, ctx_norm, attn_norm_dev, n_layers, (bf16*)out, layer_stride);
     else
-        k_ingest_norm<float><<<rows, NT, sm, st>>>(P, d, eps, ctx_norm, attn_norm_dev, n_layers, (float*)out,
-                                                   layer_stride);
+        launch(k_ingest_norm<float>, rows, NT, sm, st, P, d, eps, ctx_norm, attn_norm_dev, n_layers, (float*)out, layer_stride);
     note_launch();
     return cudaGetLastError();
 }
@@ -195,7 +224,7 @@ cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float*
 cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st) {
     int64_t total = (int64_t)B * gamma * d;
     int blocks = (int)std::min<int64_t>((total + 255) / 256, 1024);
-    k_block_init<<<blocks, 256, 0, st>>>(x, block_const, B, gamma, d);
+    launch(k_block_init, blocks, 256, 0, st, x, block_const, B, gamma, d);
     note_launch();
     return cudaGetLastError();
 }
@@ -204,8 +233,7 @@ cudaError_t ingest_rowmap(const int* seq_ids, const int* cu, int n_seqs, int tot
                           int max_ctx, int* row_seq, int* row_pos, int* err, cudaStream_t st) {
     if (total <= 0) return cudaSuccess;
     int blocks = std::min((total + 255) / 256, 1024);
-    k_ingest_rowmap<<<blocks, 256, 0, st>>>(seq_ids, cu, n_seqs, total, seq_len, max_seqs, max_ctx, row_seq, row_pos,
-                                            err);
+    launch(k_ingest_rowmap, blocks, 256, 0, st, seq_ids, cu, n_seqs, total, seq_len, max_seqs, max_ctx, row_seq, row_pos, err);
     note_launch();
     return cudaGetLastError();
 }
@@ -213,19 +241,19 @@ cudaError_t ingest_rowmap(const int* seq_ids, const int* cu, int n_seqs, int tot
 cudaError_t ingest_commit(const int* seq_ids, const int* cu, int n_seqs, int* seq_len, int max_seqs, int max_ctx,
                           cudaStream_t st) {
     if (n_seqs <= 0) return cudaSuccess;
-    k_ingest_commit<<<(n_seqs + 255) / 256, 256, 0, st>>>(seq_ids, cu, n_seqs, seq_len, max_seqs, max_ctx);
+    launch(k_ingest_commit, (n_seqs + 255) / 256, 256, 0, st, seq_ids, cu, n_seqs, seq_len, max_seqs, max_ctx);
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t add_len(int* seq_len, int slot, int delta, cudaStream_t st) {
-    k_add_len<<<1, 1, 0, st>>>(seq_len, slot, delta);
+    launch(k_add_len, 1, 1, 0, st, seq_len, slot, delta);
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t set_len(int* seq_len, int slot, int value, cudaStream_t st) {
-    k_set_len<<<1, 1, 0, st>>>(seq_len, slot, value);
+    launch(k_set_len, 1, 1, 0, st, seq_len, slot, value);
     note_launch();
     return cudaGetLastError();
 }
@@ -233,7 +261,7 @@ cudaError_t set_len(int* seq_len, int slot, int value, cudaStream_t st) {
 cudaError_t check_draft_inputs(const int* seq_ids, const int* anchors, int n, int max_seqs, int V, int* err,
                                int* safe_ids, int* safe_anchors, cudaStream_t st) {
     if (n <= 0) return cudaSuccess;
-    k_check_draft<<<(n + 255) / 256, 256, 0, st>>>(seq_ids, anchors, n, max_seqs, V, err, safe_ids, safe_anchors);
+    launch(k_check_draft, (n + 255) / 256, 256, 0, st, seq_ids, anchors, n, max_seqs, V, err, safe_ids, safe_anchors);
     note_launch();
     return cudaGetLastError();
 }

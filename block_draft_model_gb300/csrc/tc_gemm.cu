@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();  // operands and outputs are shared with earlier kernels of the stream
 
     if (warp == 0) {
         if (lane == 0) {
@@ -272,8 +274,7 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.n_fast = tm.nN <= tm.nM;
     const int tiles = tm.nM * tm.nN;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    k_tc_gemm<<<grid, NTHREADS, smem_bytes(), st>>>(tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm,
-                                                     ep, err);
+    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
     note_launch();
     return cudaGetLastError();
 }

@@ -90,12 +90,23 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    pdl_trigger();
     if (warp == 0) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+            // The weights are never written by the step: the first ring of weight tiles
+            // is requested before waiting for the kernels that produce X.
+            const int pre = min(STAGES, kb1 - kb0);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], W_BYTES + X_BYTES);
+                tma_load_2d(sW + i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * X_BYTES, &tmX, &full[i], (kb0 + i) * BK, 0);
+            int stage = pre % STAGES;
+            uint32_t phase = pre == STAGES ? 1u : 0u;
+            for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) break;
                 mbar_arrive_expect_tx(&full[stage], W_BYTES + X_BYTES);
                 tma_load_2d(sW + stage * W_BYTES, &tmW, &full[stage], kb * BK, n0);
@@ -105,8 +116,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     phase ^= 1u;
                 }
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
+        pdl_wait();
         if (lane == 0) {
             const uint32_t id = idesc(BM, BN);
             int stage = 0;
@@ -137,6 +151,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         }
     } else {
+        pdl_wait();  // the epilogue reads and writes buffers shared with earlier kernels
         const int q = warp & 3;
         const int row = q * 32 + lane;  // weight row within the tile
         const int n = n0 + row;
@@ -280,8 +295,7 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
     CUtensorMap tmX;
     if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
-    k_tc_stream<<<nT * splits, NTHREADS, smem_bytes(), st>>>(*reinterpret_cast<const CUtensorMap*>(w.tmap), tmX, M, N,
-                                                              K, splits, kb_per, ep, part, tickets, err);
+    launch(k_tc_stream, nT * splits, NTHREADS, smem_bytes(), st, *reinterpret_cast<const CUtensorMap*>(w.tmap), tmX, M, N, K, splits, kb_per, ep, part, tickets, err);
     note_launch();
     return cudaGetLastError();
 }
