@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
+        __syncwarp();  // lane 0 rejoins its warp before the CTA-wide barrier
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t id = idesc(BM, BN);
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
             }
         }
+        __syncwarp();
     } else {
         // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31
         const int q = warp & 3;

@@ -14,6 +14,7 @@
 // applies the epilogue, so results do not depend on scheduling.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "epilogue.cuh"
 #include "tc_common.cuh"
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         } else {
             pdl_wait();
         }
+        __syncwarp();  // lane 0 rejoins its warp before the CTA-wide barrier
     } else if (warp == 1) {
         pdl_wait();
         if (lane == 0) {
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 }
             }
         }
+        __syncwarp();
     } else {
         pdl_wait();  // the epilogue reads and writes buffers shared with earlier kernels
         const int q = warp & 3;
@@ -275,10 +278,27 @@ bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64
 
 bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && N >= 1 && K >= BK && K % 8 == 0; }
 
+// Largest split of K (environment DSPARK_STREAM_MAX_SPLITS, default 8).
+int max_splits() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("DSPARK_STREAM_MAX_SPLITS");
+        v = e ? atoi(e) : 8;
+        if (v < 1) v = 1;
+        if (v > 16) v = 16;
+    }
+    return v;
+}
+
+int choose_splits(int nT, int nkb, int num_sms) {
+    int splits = (2 * num_sms + nT - 1) / nT;
+    const int mx = max_splits();
+    return splits < 1 ? 1 : (splits > nkb ? nkb : (splits > mx ? mx : splits));
+}
+
 size_t tc_stream_scratch_floats(int N, int K, int num_sms) {
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
-    int splits = (2 * num_sms + nT - 1) / nT;
-    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 8 ? 8 : splits));
+    const int splits = choose_splits(nT, nkb, num_sms);
     return splits > 1 ? (size_t)nT * splits * BM * BN : 0;
 }
 
@@ -288,8 +308,7 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     if (!w.ready || !tc_stream_ok(M, N, K) || N != w.N || K != w.K) return cudaErrorInvalidValue;
     if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
-    int splits = (2 * num_sms + nT - 1) / nT;
-    splits = splits < 1 ? 1 : (splits > nkb ? nkb : (splits > 8 ? 8 : splits));
+    int splits = choose_splits(nT, nkb, num_sms);
     while (splits > 1 && ((size_t)nT * splits * BM * BN > part_floats || (size_t)nT > n_tickets)) --splits;
     int kb_per = (nkb + splits - 1) / splits;
     splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
