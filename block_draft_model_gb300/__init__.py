@@ -23,7 +23,7 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_ingest_context_batched", "dspark_draft_batched", "dspark_ingest_context_host",
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
-            "dspark_profile_read", "dspark_linear"]
+            "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error"]
 
 
 class DsparkError(RuntimeError):
@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_version": ([], ctypes.c_char_p),
         "dspark_profile": ([vp, i32], i32),
         "dspark_linear": ([i32, vp, i64, vp, i32, i32, i32, vp, i64, i32, vp], i32),
+        "dspark_linear_stream_noalloc": ([vp, i64, vp, i32, i32, i32, vp, i64, vp], i32),
+        "dspark_noalloc_last_error": ([], ctypes.c_char_p),
         "dspark_profile_read": ([vp, i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
     }
@@ -124,6 +126,18 @@ def linear(A, W, out, kernel: int = KERNEL_AUTO, stream=None):
                            _stream(stream))
     if st != OK:
         raise DsparkError(st, lib.dspark_last_error(None).decode())
+
+
+def linear_stream_noalloc(A, W, out, stream=None):
+    """out = A W^T (bf16 A [M <= 16, K], W [N, K]; float out) through the entry point that allocates
+    no device memory (its scratch is a static device array of the library)."""
+    lib = load()
+    M, K = A.shape
+    N = W.shape[0]
+    st = lib.dspark_linear_stream_noalloc(_ptr(A), A.stride(0), _ptr(W), M, N, K, _ptr(out), out.stride(0),
+                                          _stream(stream))
+    if st != OK:
+        raise DsparkError(st, lib.dspark_noalloc_last_error().decode())
 
 
 class _CudaArray:

@@ -217,6 +217,28 @@ int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_ho
 dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
                             int32_t K, float* out_dev, int64_t ldo, int32_t kernel, void* stream);
 
+/* out = A W^T with the weight-streaming tensor-core kernel (dspark_linear's
+ * kernel 4), for callers that cannot allocate device memory: code living in
+ * another runtime's memory pool, allocator-free serving loops, contexts whose
+ * allocations are frozen after start-up.  The pages have no counterpart of
+ * this call; it is an interface of this library.  It allocates nothing: the
+ * kernel's split-K scratch is a static device array of
+ * DSPARK_NOALLOC_SCRATCH_FLOATS floats plus DSPARK_NOALLOC_MAX_TILES tickets,
+ * held by every GPU that loads the library until the process exits.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current, so make that first call before any stream
+ * capture.  Every call shares the array: the tickets are cleared on each call,
+ * and calls whose work overlaps on the GPU race.
+ * Shapes: bf16 A_dev [M, K] (row stride lda), bf16 W_dev [N, K], float out_dev
+ * [M, N] (row stride ldo); 1 <= M <= 16, K >= 64, K % 8 == 0, lda % 8 == 0,
+ * 16-byte aligned A and W, N <= 128 * DSPARK_NOALLOC_MAX_TILES
+ * (DSPARK_ERR_CAPACITY beyond).  dspark_noalloc_last_error() describes a failure. */
+#define DSPARK_NOALLOC_SCRATCH_FLOATS 4194304
+#define DSPARK_NOALLOC_MAX_TILES 4096
+dspark_status dspark_linear_stream_noalloc(const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
+                                           int32_t K, float* out_dev, int64_t ldo, void* stream);
+const char* dspark_noalloc_last_error(void);
+
 /* Number of kernel launches issued by this handle since creation (all calls). */
 int64_t dspark_launch_count(const dspark_handle* h);
 
