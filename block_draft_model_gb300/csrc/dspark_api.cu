@@ -107,6 +107,8 @@ struct dspark_handle {
     int* mk_i = nullptr;
     unsigned int* mk_cnt = nullptr;
     int mk_ctas = 1;
+    int mk_chain_max = 0;                    // largest co-resident grid of the one-launch Markov chain
+    unsigned int* mk_bar = nullptr;          // [2] grid-barrier words
     float* ws = nullptr;
     size_t ws_floats = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
@@ -170,10 +172,10 @@ cudaError_t grow(DevBuf& b, size_t bytes) {
 }
 
 int attn_chunks(const dspark_handle* h, int B, int max_keys) {
-    // enough CTAs for two per SM, but at least 256 keys (four tiles) per range
+    // enough CTAs for two per SM, but at least 64 keys (one tile) per range
     const int nh = h->cfg.n_heads;
     int want = (2 * h->num_sms + nh * B - 1) / (nh * B);
-    int by_keys = (max_keys + 255) / 256;
+    int by_keys = (max_keys + 63) / 64;
     return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks()));
 }
 
@@ -287,7 +289,7 @@ dspark_status check_cfg(const dspark_config* c, std::string& why) {
     if (hd > 256 || hd % 8 != 0) { why = "head_dim must be a multiple of 8 and <= 256"; return DSPARK_ERR_UNSUPPORTED; }
     if (256 % (hd / 8) != 0 || c->gamma > 256 / (hd / 8)) { why = "gamma * head_dim must be <= 2048 with head_dim / 8 dividing 256"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->dtype == DSPARK_FP32 && hd > 128) { why = "fp32 drafters take head_dim <= 128"; return DSPARK_ERR_UNSUPPORTED; }
-    if (c->d_draft % 64 != 0) { why = "d_draft must be a multiple of 64"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->d_draft % 64 != 0 || c->d_draft > 4096) { why = "d_draft must be a multiple of 64, <= 4096"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->markov_rank % 8 != 0 || c->markov_rank > 1024) { why = "markov_rank must be a multiple of 8, <= 1024"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
     if ((int64_t)c->max_ctx + c->gamma > (1 << 30)) { why = "max_ctx too large"; return DSPARK_ERR_UNSUPPORTED; }
@@ -478,6 +480,13 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.err = h->d_err;
     mp.ctas = h->mk_ctas;
     Prof pr(h, CAT_MARKOV, st);
+    // one cooperative launch when B sequences x ctas fit co-resident, else one launch per position
+    const int chain_ctas = std::min(h->mk_ctas, h->mk_chain_max / std::max(B, 1));
+    if (chain_ctas >= 8 || chain_ctas >= h->mk_ctas) {
+        mp.ctas = chain_ctas;
+        CUDA_TRY(h, markov_chain(mp, h->mk_bar, h->mk_bar + 1, st));
+        return DSPARK_OK;
+    }
     for (int k = 0; k < c.gamma; ++k) {
         mp.k = k;
         CUDA_TRY(h, markov_step(mp, st));
@@ -843,8 +852,11 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         CTRY(cudaMemsetAsync(h->attn_tickets, 0, nt * sizeof(unsigned int), st));
     }
     h->mk_ctas = markov_ctas(V);
-    CTRY(dalloc(h, (void**)&h->mk_v, (size_t)cfg->max_seqs * h->mk_ctas * 4));
-    CTRY(dalloc(h, (void**)&h->mk_i, (size_t)cfg->max_seqs * h->mk_ctas * 4));
+    h->mk_chain_max = markov_chain_max_ctas(h->dt);
+    CTRY(dalloc(h, (void**)&h->mk_v, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
+    CTRY(dalloc(h, (void**)&h->mk_i, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
+    CTRY(dalloc(h, (void**)&h->mk_bar, 2 * sizeof(unsigned int)));
+    CTRY(cudaMemsetAsync(h->mk_bar, 0, 2 * sizeof(unsigned int), st));
     CTRY(dalloc(h, (void**)&h->mk_cnt, (size_t)cfg->max_seqs * 4));
     CTRY(dalloc(h, (void**)&h->safe_ids, (size_t)cfg->max_seqs * 4));
     CTRY(dalloc(h, (void**)&h->anchor_dev, sizeof(int)));

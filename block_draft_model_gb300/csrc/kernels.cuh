@@ -124,6 +124,12 @@ struct MarkovParams {
 };
 int markov_ctas(int V);
 cudaError_t markov_step(const MarkovParams& p, cudaStream_t st);
+// All gamma positions in one cooperative launch (p.ctas CTAs per sequence, one
+// bounded grid barrier per position; part_v/part_i hold 2 * B * ctas entries;
+// bar_count/bar_gen: zeroed words, left reusable).  markov_chain_max_ctas is the
+// largest co-resident grid.
+int markov_chain_max_ctas(int w_dtype);
+cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st);
 
 // ------------------------------------------------------------------ bookkeeping kernels
 // For a batched ingest: per feature row t, its slot and cache position

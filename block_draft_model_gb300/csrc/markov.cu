@@ -13,6 +13,7 @@
 // needs a two-step shuffle; two rows per lane group are in flight at once.  The token stays on the
 // device, where the next position's launch reads it.
 #include <climits>
+#include <stdint.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -169,11 +170,222 @@ __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
     }
 }
 
+// Bounded grid-wide barrier for a cooperative launch: `count` and `gen` are
+// zero-initialised device words shared by all CTAs.  Gives up after about a
+// second (sets DSPARK_DEVERR_TIMEOUT in *err and returns false).
+__device__ __forceinline__ bool grid_sync(unsigned int* count, unsigned int* gen, unsigned int n_ctas, int* err) {
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ok = 1;
+        const unsigned int g = *(volatile unsigned int*)gen;
+        __threadfence();
+        if (atomicAdd(count, 1u) == n_ctas - 1) {
+            *(volatile unsigned int*)count = 0u;
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            uint64_t t0, t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+            while (*(volatile unsigned int*)gen == g) {
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+                if (t - t0 > 1000000000ull) {
+                    atomicOr(err, 16);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+// The whole chain in one cooperative launch: grid = ctas * B CTAs, CTA c of
+// sequence b = blockIdx.x / ctas streams its slice of w2 at every position;
+// after one grid barrier per position every CTA of the sequence reduces the
+// CTA winners itself (the key is a total order, so all agree), and CTA 0 of the
+// sequence writes the token and the confidence.  Partials are double-buffered
+// by position parity: a buffer is rewritten two positions later, after a
+// barrier every CTA passed only once done reading it.
+template <typename TW>
+__global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned int* bar_count, unsigned int* bar_gen) {
+    constexpr int VE = Vec16<TW>::N;
+    __shared__ __align__(16) float e[RMAX];
+    __shared__ float red_v[NT / 32];
+    __shared__ int red_i[NT / 32];
+    __shared__ float redf[32];
+    __shared__ int prev_s;
+
+    const int ctas = p.ctas;
+    const int b = blockIdx.x / ctas, cta = blockIdx.x - b * ctas;
+    const int r = p.r, V = p.V;
+    const TW* w1 = reinterpret_cast<const TW*>(p.w1);
+    const TW* w2 = reinterpret_cast<const TW*>(p.w2);
+    const int rows = (V + ctas - 1) / ctas;
+    const int v_begin = cta * rows, v_end = min(V, v_begin + rows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane & (LPR - 1), rw = lane / LPR;
+    const int nvec = r / VE;
+    if (threadIdx.x == 0) prev_s = min(max(p.anchors ? p.anchors[b] : p.anchor, 0), V - 1);
+    __syncthreads();
+
+    for (int k = 0; k < p.gamma; ++k) {
+        const int prev = prev_s;
+        for (int c = threadIdx.x; c < r; c += NT) e[c] = to_f32(w1[(int64_t)prev * r + c]);
+        __syncthreads();
+        const int64_t urow = (int64_t)(b * p.gamma + k) * V;
+        ArgBest best{-INFINITY, INT_MAX};
+        for (int v0 = v_begin + warp * (2 * RPW); v0 < v_end; v0 += (NT / 32) * (2 * RPW)) {
+            const int va = v0 + rw, vb = v0 + RPW + rw;
+            const TW* ra = w2 + (int64_t)min(va, v_end - 1) * r;
+            const TW* rb = w2 + (int64_t)min(vb, v_end - 1) * r;
+            float aa = 0.f, ab = 0.f;
+            for (int vi = sub; vi < nvec; vi += 4 * LPR) {
+                uint4 ua[4], ub[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int x = vi + q * LPR;
+                    ua[q] = x < nvec ? __ldg(reinterpret_cast<const uint4*>(ra + x * VE)) : make_uint4(0, 0, 0, 0);
+                    ub[q] = x < nvec ? __ldg(reinterpret_cast<const uint4*>(rb + x * VE)) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int x = vi + q * LPR;
+                    if (x >= nvec) break;
+                    float fa[VE], fb[VE];
+                    Vec16<TW>::unpack(ua[q], fa);
+                    Vec16<TW>::unpack(ub[q], fb);
+                    const float* ep = e + x * VE;
+#pragma unroll
+                    for (int t = 0; t < VE; ++t) {
+                        aa = fmaf(fa[t], ep[t], aa);
+                        ab = fmaf(fb[t], ep[t], ab);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < LPR; o <<= 1) {
+                aa += __shfl_xor_sync(0xffffffffu, aa, o);
+                ab += __shfl_xor_sync(0xffffffffu, ab, o);
+            }
+            if (sub == 0) {
+                if (va < v_end) {
+                    const float l = p.U[urow + va] + aa;
+                    if (p.logits) p.logits[urow + va] = l;
+                    if (better(l, va, best.v, best.i)) {
+                        best.v = l;
+                        best.i = va;
+                    }
+                }
+                if (vb < v_end) {
+                    const float l = p.U[urow + vb] + ab;
+                    if (p.logits) p.logits[urow + vb] = l;
+                    if (better(l, vb, best.v, best.i)) {
+                        best.v = l;
+                        best.i = vb;
+                    }
+                }
+            }
+        }
+        best = warp_argbest(best);
+        if (lane == 0) {
+            red_v[warp] = best.v;
+            red_i[warp] = best.i;
+        }
+        __syncthreads();
+        const int64_t pb = (int64_t)(k & 1) * p.B * ctas + (int64_t)b * ctas;
+        if (threadIdx.x == 0) {
+            ArgBest cb{-INFINITY, INT_MAX};
+            for (int w = 0; w < NT / 32; ++w)
+                if (better(red_v[w], red_i[w], cb.v, cb.i)) {
+                    cb.v = red_v[w];
+                    cb.i = red_i[w];
+                }
+            p.part_v[pb + cta] = cb.v;
+            p.part_i[pb + cta] = cb.i;
+        }
+        grid_sync(bar_count, bar_gen, gridDim.x, p.err);
+        // every CTA of the sequence: the winner over the CTA results
+        ArgBest fb{-INFINITY, INT_MAX};
+        for (int c = threadIdx.x; c < ctas; c += NT) {
+            const float v = __ldcg(p.part_v + pb + c);
+            const int i = __ldcg(p.part_i + pb + c);
+            if (better(v, i, fb.v, fb.i)) {
+                fb.v = v;
+                fb.i = i;
+            }
+        }
+        fb = warp_argbest(fb);
+        __syncthreads();  // red_v/red_i reuse
+        if (lane == 0) {
+            red_v[warp] = fb.v;
+            red_i[warp] = fb.i;
+        }
+        float z = 0.f;
+        if (cta == 0) {
+            const float* yr = p.y + (int64_t)(b * p.gamma + k) * p.d;
+            for (int c = threadIdx.x; c < p.d; c += NT) z = fmaf(yr[c], p.conf_w[c], z);
+            for (int c = threadIdx.x; c < r; c += NT) z = fmaf(e[c], p.conf_w[p.d + c], z);
+        }
+        z = block_sum(z, redf);  // contains __syncthreads: red_v/red_i are complete
+        if (threadIdx.x == 0) {
+            ArgBest tb{-INFINITY, INT_MAX};
+            for (int w = 0; w < NT / 32; ++w)
+                if (better(red_v[w], red_i[w], tb.v, tb.i)) {
+                    tb.v = red_v[w];
+                    tb.i = red_i[w];
+                }
+            int tok = tb.i;
+            if (tok == INT_MAX || !(tb.v > -INFINITY)) {
+                if (cta == 0) atomicOr(p.err, 8);
+                tok = 0;
+            }
+            prev_s = tok;
+            if (cta == 0) {
+                p.tokens[b * p.gamma + k] = tok;
+                p.conf[b * p.gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + r])));
+            }
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 int markov_ctas(int V) {
     int c = (V + 255) / 256;  // 256 vocabulary rows per CTA
     return c < 1 ? 1 : (c > 2048 ? 2048 : c);
+}
+
+int markov_chain_max_ctas(int w_dtype) {
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cudaError_t e = w_dtype == DT_BF16
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_markov_chain<bf16>, NT, 0)
+                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_markov_chain<float>, NT, 0);
+    if (e != cudaSuccess) return 0;
+    return per_sm * sms;
+}
+
+cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st) {
+    if (p.r > RMAX || p.r % 8 != 0) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas * p.B);
+    cfg.blockDim = dim3(NT);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = p.w_dtype == DT_BF16 ? cudaLaunchKernelEx(&cfg, k_markov_chain<bf16>, p, bar_count, bar_gen)
+                                         : cudaLaunchKernelEx(&cfg, k_markov_chain<float>, p, bar_count, bar_gen);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t markov_step(const MarkovParams& p, cudaStream_t st) {

@@ -31,37 +31,62 @@ __global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x
     for (int c = threadIdx.x; c < n; c += NT) o[c] = from_f32<TO>(xr[c] * s * w[c]);
 }
 
-// One CTA per context row: H = RMSNorm(P) * ctx_norm (kept in shared memory),
-// then every layer's normalised copy RMSNorm(H) * attn_norm_i.
+// One warp per context row: H = RMSNorm(P) * ctx_norm kept in registers, then
+// every layer's normalised copy RMSNorm(H) * attn_norm_i (16-byte stores).
+constexpr int INW = 8;  // rows (warps) per CTA
+
 template <typename TO>
-__global__ void __launch_bounds__(NT) k_ingest_norm(const float* __restrict__ P, int d, float eps,
-                                                    const float* __restrict__ ctx_norm,
-                                                    const float* const* __restrict__ attn_norm, int n_layers, TO* out,
-                                                    int64_t layer_stride) {
+__global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int rows, int d, float eps,
+                                                         const float* __restrict__ ctx_norm,
+                                                         const float* const* __restrict__ attn_norm, int n_layers,
+                                                         TO* out, int64_t layer_stride) {
     pdl_trigger();
     pdl_wait();
-    extern __shared__ float h[];
-    __shared__ float red[32];
-    const float* pr = P + (int64_t)blockIdx.x * d;
+    constexpr int MAXV = 32;  // float4 per lane: d <= 32 * 4 * 32 = 4096
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * INW + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const float4* pr = reinterpret_cast<const float4*>(P + (int64_t)row * d);
+    const int nv = d / 4;
+    float4 h[MAXV];
     float ss = 0.f;
-    for (int c = threadIdx.x; c < d; c += NT) {
-        float v = pr[c];
-        ss = fmaf(v, v, ss);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) {
+            h[i] = pr[v];
+            ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
+        }
     }
-    ss = block_sum(ss, red);
+    ss = warp_sum(ss);
     const float s1 = rsqrtf(ss / (float)d + eps);
+    const float4* cn = reinterpret_cast<const float4*>(ctx_norm);
     float ss2 = 0.f;
-    for (int c = threadIdx.x; c < d; c += NT) {
-        float v = pr[c] * s1 * ctx_norm[c];
-        h[c] = v;
-        ss2 = fmaf(v, v, ss2);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) {
+            const float4 w = cn[v];
+            h[i] = make_float4(h[i].x * s1 * w.x, h[i].y * s1 * w.y, h[i].z * s1 * w.z, h[i].w * s1 * w.w);
+            ss2 += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
+        }
     }
-    ss2 = block_sum(ss2, red);
+    ss2 = warp_sum(ss2);
     const float s2 = rsqrtf(ss2 / (float)d + eps);
-    for (int i = 0; i < n_layers; ++i) {
-        const float* an = attn_norm[i];
-        TO* o = out + i * layer_stride + (int64_t)blockIdx.x * d;
-        for (int c = threadIdx.x; c < d; c += NT) o[c] = from_f32<TO>(h[c] * s2 * an[c]);
+    for (int l = 0; l < n_layers; ++l) {
+        const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
+        TO* o = out + l * layer_stride + (int64_t)row * d;
+#pragma unroll
+        for (int i = 0; i < MAXV; ++i) {
+            const int v = lane + 32 * i;
+            if (v < nv) {
+                const float4 w = an[v];
+                o[4 * v] = from_f32<TO>(h[i].x * s2 * w.x);
+                o[4 * v + 1] = from_f32<TO>(h[i].y * s2 * w.y);
+                o[4 * v + 2] = from_f32<TO>(h[i].z * s2 * w.z);
+                o[4 * v + 3] = from_f32<TO>(h[i].w * s2 * w.w);
+            }
+        }
     }
 }
 
@@ -212,11 +237,14 @@ cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float*
                         const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
                         int64_t layer_stride, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    size_t sm = (size_t)d * sizeof(float);
+    if (d % 4 != 0 || d > 4096) return cudaErrorInvalidValue;
+    const int blocks = (rows + INW - 1) / INW;
     if (out_dtype == DT_BF16)
-        launch(k_ingest_norm<bf16>, rows, NT, sm, st, P, d, eps, ctx_norm, attn_norm_dev, n_layers, (bf16*)out, layer_stride);
+        launch(k_ingest_norm<bf16>, blocks, INW * 32, 0, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
+               (bf16*)out, layer_stride);
     else
-        launch(k_ingest_norm<float>, rows, NT, sm, st, P, d, eps, ctx_norm, attn_norm_dev, n_layers, (float*)out, layer_stride);
+        launch(k_ingest_norm<float>, blocks, INW * 32, 0, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
+               (float*)out, layer_stride);
     note_launch();
     return cudaGetLastError();
 }
