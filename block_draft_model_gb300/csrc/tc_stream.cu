@@ -50,8 +50,8 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 // [s * kb_per, min(nkb, (s + 1) * kb_per)) with s = b % splits.
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_tc_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
-                int splits, int kb_per, EpiParams ep, float* __restrict__ part, unsigned int* __restrict__ tickets,
-                int* err) {
+                int splits, int kb_per, int cluster_reduce, EpiParams ep, float* __restrict__ part,
+                unsigned int* __restrict__ tickets, int* err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -171,7 +171,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int m = 0; m < BN; ++m) v[m] = 0.f;
         }
         bool final_ = (splits == 1);
-        if (splits > 1) {
+        if (splits > 1 && cluster_reduce) {
+            // partial tile [128 rows][16] into this CTA's (now idle) first weight stage; the cluster
+            // reduction below reads it through distributed shared memory
+            float4* red = reinterpret_cast<float4*>(smem) + row * (BN / 4);
+#pragma unroll
+            for (int c = 0; c < BN / 4; ++c) red[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        } else if (splits > 1) {
             float4* dst = reinterpret_cast<float4*>(part + (((int64_t)tile * splits + split) * BM + row) * BN);
 #pragma unroll
             for (int c = 0; c < BN / 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
@@ -237,6 +243,53 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         }
     }
+    if (splits > 1 && cluster_reduce) {
+        // Split-K reduction inside the cluster (the tile's `splits` CTAs): after the first cluster
+        // barrier every partial is in its CTA's shared memory; CTA s reduces rows
+        // [s * 128 / splits, (s + 1) * 128 / splits) over all CTAs in split order and applies the
+        // epilogue; the second barrier keeps every CTA's shared memory alive until all reads are done.
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+        if (warp >= 2) {
+            const int t = threadIdx.x - 64;  // 0..127
+            const int rps = BM / splits;
+            const bool mine = t < rps;
+            const int row = split * rps + (mine ? t : 0);
+            float v[BN];
+#pragma unroll
+            for (int m = 0; m < BN; ++m) v[m] = 0.f;
+            const uint32_t laddr = smem_u32(smem) + (uint32_t)(row * BN * 4);
+            for (int s2 = 0; s2 < splits; ++s2) {
+                uint32_t raddr;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(s2));
+#pragma unroll
+                for (int c = 0; c < BN / 4; ++c) {
+                    float a, b2, c2, d2;
+                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(a), "=f"(b2), "=f"(c2), "=f"(d2)
+                                 : "r"(raddr + c * 16)
+                                 : "memory");
+                    v[4 * c] += a;
+                    v[4 * c + 1] += b2;
+                    v[4 * c + 2] += c2;
+                    v[4 * c + 3] += d2;
+                }
+            }
+            const int n = n0 + row;
+            const bool ok = mine && !*abort_flag;
+            if (ep.kind == EPI_SWIGLU) {
+#pragma unroll
+                for (int m = 0; m < BN; ++m) {
+                    const float up = __shfl_down_sync(0xffffffffu, v[m], 1);
+                    if (ok && m < M && !(row & 1) && n + 1 < N) epi_pair(ep, m, n, v[m], up);
+                }
+            } else if (ok && n < N) {
+#pragma unroll
+                for (int m = 0; m < BN; ++m)
+                    if (m < M) epi_one(ep, m, n, v[m]);
+            }
+        }
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) atomicOr(err, DEVERR_TIMEOUT);
@@ -290,6 +343,17 @@ int max_splits() {
     return v;
 }
 
+// Split-K reduction through distributed shared memory (environment
+// DSPARK_STREAM_CLUSTER=0 selects the scratch-and-ticket reduction instead).
+bool cluster_splits_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("DSPARK_STREAM_CLUSTER");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 int choose_splits(int nT, int nkb, int num_sms) {
     int splits = (2 * num_sms + nT - 1) / nT;
     const int mx = max_splits();
@@ -310,11 +374,42 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
     int splits = choose_splits(nT, nkb, num_sms);
     while (splits > 1 && ((size_t)nT * splits * BM * BN > part_floats || (size_t)nT > n_tickets)) --splits;
-    int kb_per = (nkb + splits - 1) / splits;
-    splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
     CUtensorMap tmX;
     if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
-    launch(k_tc_stream, nT * splits, NTHREADS, smem_bytes(), st, *reinterpret_cast<const CUtensorMap*>(w.tmap), tmX, M, N, K, splits, kb_per, ep, part, tickets, err);
+    const CUtensorMap& tmW = *reinterpret_cast<const CUtensorMap*>(w.tmap);
+    if (cluster_splits_enabled() && part_floats != 0) {
+        // cluster reduction: splits is a power of two (cluster size <= 8) and every split non-empty
+        int cs = 1;
+        while (cs * 2 <= choose_splits(nT, nkb, num_sms) && cs * 2 <= 8 && cs * 2 <= nkb) cs *= 2;
+        if (cs > 1) {
+            const int kbp = (nkb + cs - 1) / cs;
+            if ((cs - 1) * kbp < nkb) {
+                cudaLaunchAttribute attr[2];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = cs;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[1].val.programmaticStreamSerializationAllowed = 1;
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(nT * cs);
+                cfg.blockDim = dim3(NTHREADS);
+                cfg.dynamicSmemBytes = smem_bytes();
+                cfg.stream = st;
+                cfg.attrs = attr;
+                cfg.numAttrs = pdl_enabled() ? 2 : 1;
+                cudaError_t e = cudaLaunchKernelEx(&cfg, k_tc_stream, tmW, tmX, M, N, K, cs, kbp, 1, ep, part, tickets,
+                                                   err);
+                note_launch();
+                if (e != cudaSuccess) return e;
+                return cudaGetLastError();
+            }
+        }
+    }
+    int kb_per = (nkb + splits - 1) / splits;
+    splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
+    launch(k_tc_stream, nT * splits, NTHREADS, smem_bytes(), st, tmW, tmX, M, N, K, splits, kb_per, 0, ep, part,
+           tickets, err);
     note_launch();
     return cudaGetLastError();
 }
