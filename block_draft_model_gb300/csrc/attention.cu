@@ -98,8 +98,6 @@ __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
 
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0)
-        l2_prefetch_share(p.pf.ptr, p.pf.bytes, (b * gridDim.y + h) * gridDim.x + c, gridDim.x * gridDim.y * gridDim.z);
     const int slot = p.seq_ids ? p.seq_ids[b] : b;
     const int n_keys = slot < 0 ? 0 : p.seq_len[slot] + gamma;  // a rejected sequence has no keys
     const int chunk = (n_keys + p.n_chunks - 1) / p.n_chunks;

@@ -24,20 +24,6 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 bool pdl_enabled();
 
-// Ask the L2 to fetch this CTA's share of [ptr, ptr + bytes) (64 KB bulk
-// prefetches; no data comes to the SM).  Called by one thread.
-__device__ __forceinline__ void l2_prefetch_share(const void* ptr, size_t bytes, unsigned int cta, unsigned int ctas) {
-    if (!ptr || bytes == 0) return;
-    const size_t per = ((bytes + ctas - 1) / ctas + 15) & ~(size_t)15;
-    size_t lo = (size_t)cta * per, hi = lo + per;
-    if (hi > bytes) hi = bytes & ~(size_t)15;
-    for (size_t o = lo; o < hi; o += 65536) {
-        const size_t n = (hi - o < 65536) ? (hi - o) : 65536;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const char*)ptr + o), "r"((unsigned int)n)
-                     : "memory");
-    }
-}
-
 // cudaLaunchKernelEx with programmatic stream serialization (when enabled).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -365,20 +365,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
     void* actA = lowp ? h->act_lp : (void*)h->act;
     const int adt = lowp ? DT_BF16 : DT_F32;
-    // L2 prefetch plan: each kernel asks for the weights the kernel after next will stream
-    const size_t es = h->esz, kPfMax = (size_t)48 << 20;
-    auto pf = [&](const void* ptr, size_t bytes) {
-        L2Prefetch x;
-        if (ptr && bytes <= kPfMax) {
-            x.ptr = ptr;
-            x.bytes = bytes;
-        }
-        return x;
-    };
-    const size_t b_qkv = (size_t)3 * d * d * es, b_o = (size_t)d * d * es, b_gu = (size_t)2 * F * d * es,
-                 b_dn = (size_t)d * F * es;
     for (int i = 0; i < c.n_layers; ++i) {
-        const bool last = i + 1 == c.n_layers;
         if (i == 0) pr_block.end();
         {
             Prof pr(h, CAT_NORM, st);
@@ -390,7 +377,6 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         qkv.ldo = d;
         qkv.gamma = c.gamma;
         qkv.seq_ids = seq_ids;
-        qkv.pf = pf(h->wo[i], b_o);
         {
             Prof pr(h, CAT_QKV, st);
             CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
@@ -414,7 +400,6 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ap.tickets = h->attn_tickets;
         ap.out = actA;
         ap.out_dtype = adt;
-        ap.pf = pf(h->wgu[i], b_gu);
         if (attn_scratch_floats(B, c.n_heads, ap.n_chunks, c.gamma, h->hd) > h->attn_part_floats)
             return fail(h, DSPARK_ERR_CAPACITY, "attention scratch too small");
         {
@@ -427,10 +412,8 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         res.ldo = d;
         {
             Prof pr(h, CAT_O, st);
-            EpiParams r_o = res;
-            r_o.pf = pf(h->wd[i], b_dn);
             CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
-                             WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, r_o, st));
+                             WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
         }
         {
             Prof pr(h, CAT_NORM, st);
@@ -442,7 +425,6 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         sw.act_dtype = adt;
         sw.ld_act = F;
         sw.act = c.act;
-        sw.pf = last ? pf(h->out_proj, std::min(kPfMax, (size_t)c.vocab * d * es)) : pf(h->wqkv[i + 1], b_qkv);
         {
             Prof pr(h, CAT_GATE_UP, st);
             CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,

@@ -20,16 +20,8 @@ enum EpiKind {
     EPI_QKV = 4,        // columns [0, d) -> out_f32 (Q), [d, 2d) -> K cache, [2d, 3d) -> V cache
 };
 
-// A byte range of read-only data (weights, caches) that a kernel asks the L2 to
-// fetch ahead of a later kernel of the step; split evenly over the kernel's CTAs.
-struct L2Prefetch {
-    const void* ptr = nullptr;
-    size_t bytes = 0;
-};
-
 struct EpiParams {
     int kind = EPI_STORE_F32;
-    L2Prefetch pf;               // prefetch issued by the GEMM kernels at their start
     float* out_f32 = nullptr;
     int64_t ldo = 0;
     void* out_act = nullptr;     // EPI_SWIGLU output, element type act_dtype
@@ -103,7 +95,6 @@ struct AttnParams {
     unsigned int* tickets;   // scratch: B * n_heads counters, zero before and after every launch
     void* out;               // [B*gamma, d] attention output, out_dtype
     int out_dtype;
-    L2Prefetch pf;           // issued at the kernel's start
 };
 size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim);
 int attn_max_chunks();

@@ -71,7 +71,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int kb0 = split * kb_per, kb1 = min(nkb, kb0 + kb_per);
     const int n0 = tile * BM;
 
-    if (threadIdx.x == 32) l2_prefetch_share(ep.pf.ptr, ep.pf.bytes, blockIdx.x, gridDim.x);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
