@@ -31,6 +31,18 @@ __global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x
     for (int c = threadIdx.x; c < n; c += NT) o[c] = from_f32<TO>(xr[c] * s * w[c]);
 }
 
+// Four consecutive outputs with one 8-byte (bf16) or 16-byte (fp32) store.
+__device__ __forceinline__ void store4(bf16* o, float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(o) = u;
+}
+__device__ __forceinline__ void store4(float* o, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(o) = make_float4(a, b, c, d);
+}
+
 // One warp per context row: H = RMSNorm(P) * ctx_norm kept in registers, then
 // every layer's normalised copy RMSNorm(H) * attn_norm_i (16-byte stores).
 constexpr int INW = 8;  // rows (warps) per CTA
@@ -81,10 +93,7 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
             const int v = lane + 32 * i;
             if (v < nv) {
                 const float4 w = an[v];
-                o[4 * v] = from_f32<TO>(h[i].x * s2 * w.x);
-                o[4 * v + 1] = from_f32<TO>(h[i].y * s2 * w.y);
-                o[4 * v + 2] = from_f32<TO>(h[i].z * s2 * w.z);
-                o[4 * v + 3] = from_f32<TO>(h[i].w * s2 * w.w);
+                store4(o + 4 * v, h[i].x * s2 * w.x, h[i].y * s2 * w.y, h[i].z * s2 * w.z, h[i].w * s2 * w.w);
             }
         }
     }
