@@ -250,45 +250,57 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         // epilogue; the second barrier keeps every CTA's shared memory alive until all reads are done.
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
         if (warp >= 2) {
+            // item = (row of my share, group of 4 activation columns); all splits' float4s of an
+            // item are requested together, then added in split order
             const int t = threadIdx.x - 64;  // 0..127
             const int rps = BM / splits;
-            const bool mine = t < rps;
-            const int row = split * rps + (mine ? t : 0);
-            float v[BN];
+            const bool swiglu = ep.kind == EPI_SWIGLU;
+            for (int it0 = 0; it0 < rps * 4; it0 += 128) {
+                const int it = it0 + t;
+                const bool mine = it < rps * 4;
+                const int r = mine ? it >> 2 : 0, cg = it & 3;
+                const int row = split * rps + r;
+                const uint32_t laddr = smem_u32(smem) + (uint32_t)(row * BN * 4 + cg * 16);
+                float4 part4[8];
 #pragma unroll
-            for (int m = 0; m < BN; ++m) v[m] = 0.f;
-            const uint32_t laddr = smem_u32(smem) + (uint32_t)(row * BN * 4);
-            for (int s2 = 0; s2 < splits; ++s2) {
-                uint32_t raddr;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(s2));
-#pragma unroll
-                for (int c = 0; c < BN / 4; ++c) {
-                    float a, b2, c2, d2;
-                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                 : "=f"(a), "=f"(b2), "=f"(c2), "=f"(d2)
-                                 : "r"(raddr + c * 16)
-                                 : "memory");
-                    v[4 * c] += a;
-                    v[4 * c + 1] += b2;
-                    v[4 * c + 2] += c2;
-                    v[4 * c + 3] += d2;
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    part4[s2] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (s2 < splits) {
+                        uint32_t raddr;
+                        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(s2));
+                        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(part4[s2].x), "=f"(part4[s2].y), "=f"(part4[s2].z), "=f"(part4[s2].w)
+                                     : "r"(raddr)
+                                     : "memory");
+                    }
                 }
-            }
-            const int n = n0 + row;
-            const bool ok = mine && !*abort_flag;
-            if (ep.kind == EPI_SWIGLU) {
+                float v4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < BN; ++m) {
-                    const float up = __shfl_down_sync(0xffffffffu, v[m], 1);
-                    if (ok && m < M && !(row & 1) && n + 1 < N) epi_pair(ep, m, n, v[m], up);
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    v4[0] += part4[s2].x;
+                    v4[1] += part4[s2].y;
+                    v4[2] += part4[s2].z;
+                    v4[3] += part4[s2].w;
                 }
-            } else if (ok && n < N) {
+                const int n = n0 + row;
+                const bool ok = mine && !*abort_flag;
+                if (swiglu) {
+                    // (gate, up) rows 2j, 2j+1 are items four apart in the same warp
 #pragma unroll
-                for (int m = 0; m < BN; ++m)
-                    if (m < M) epi_one(ep, m, n, v[m]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float up = __shfl_down_sync(0xffffffffu, v4[q], 4);
+                        const int m = 4 * cg + q;
+                        if (ok && m < M && !(row & 1) && n + 1 < N) epi_pair(ep, m, n, v4[q], up);
+                    }
+                } else if (ok && n < N) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (4 * cg + q < M) epi_one(ep, 4 * cg + q, n, v4[q]);
+                }
             }
         }
-        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+        // only the shared-memory reads above must be done before any CTA of the cluster exits
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
