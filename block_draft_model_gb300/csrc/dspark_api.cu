@@ -293,6 +293,7 @@ dspark_status check_cfg(const dspark_config* c, std::string& why) {
     if (c->markov_rank % 8 != 0 || c->markov_rank > 1024) { why = "markov_rank must be a multiple of 8, <= 1024"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
     if ((int64_t)c->max_ctx + c->gamma > (1 << 30)) { why = "max_ctx too large"; return DSPARK_ERR_UNSUPPORTED; }
+    if ((size_t)(c->n_layers + 1) * c->d_draft * 4 > 200 * 1024) { why = "(n_layers + 1) * d_draft * 4 bytes must fit 200 KB of shared memory"; return DSPARK_ERR_UNSUPPORTED; }
     return DSPARK_OK;
 }
 
@@ -481,7 +482,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.ctas = h->mk_ctas;
     Prof pr(h, CAT_MARKOV, st);
     // one cooperative launch when B sequences x ctas fit co-resident, else one launch per position
-    const int chain_ctas = std::min(h->mk_ctas, h->mk_chain_max / std::max(B, 1));
+    const int chain_ctas = std::min(std::min(h->mk_ctas, h->num_sms), h->mk_chain_max / std::max(B, 1));
     if (chain_ctas >= 8 || chain_ctas >= h->mk_ctas) {
         mp.ctas = chain_ctas;
         CUDA_TRY(h, markov_chain(mp, h->mk_bar, h->mk_bar + 1, st));

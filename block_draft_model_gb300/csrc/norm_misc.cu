@@ -43,57 +43,67 @@ __device__ __forceinline__ void store4(float* o, float a, float b, float c, floa
     *reinterpret_cast<float4*>(o) = make_float4(a, b, c, d);
 }
 
-// One warp per context row: H = RMSNorm(P) * ctx_norm kept in registers, then
-// every layer's normalised copy RMSNorm(H) * attn_norm_i (16-byte stores).
-constexpr int INW = 8;  // rows (warps) per CTA
+// Ingest normalisation, one warp per context row (rows_per_warp rows in turn):
+// H = RMSNorm(P) * ctx_norm in registers, then every layer's normalised copy
+// RMSNorm(H) * attn_norm_i with 8/16-byte stores.  The norm vectors are staged
+// once per CTA in shared memory ((n_layers + 1) * d floats).
+constexpr int INW = 8;  // warps per CTA
 
-template <typename TO>
+template <typename TO, int MAXV>
 __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int rows, int d, float eps,
                                                          const float* __restrict__ ctx_norm,
                                                          const float* const* __restrict__ attn_norm, int n_layers,
-                                                         TO* out, int64_t layer_stride) {
+                                                         TO* out, int64_t layer_stride, int rows_per_warp) {
+    extern __shared__ __align__(16) float wsm[];  // [n_layers + 1][d]
     pdl_trigger();
     pdl_wait();
-    constexpr int MAXV = 32;  // float4 per lane: d <= 32 * 4 * 32 = 4096
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * INW + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const float4* pr = reinterpret_cast<const float4*>(P + (int64_t)row * d);
     const int nv = d / 4;
-    float4 h[MAXV];
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-        const int v = lane + 32 * i;
-        if (v < nv) {
-            h[i] = pr[v];
-            ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
-        }
-    }
-    ss = warp_sum(ss);
-    const float s1 = rsqrtf(ss / (float)d + eps);
-    const float4* cn = reinterpret_cast<const float4*>(ctx_norm);
-    float ss2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-        const int v = lane + 32 * i;
-        if (v < nv) {
-            const float4 w = cn[v];
-            h[i] = make_float4(h[i].x * s1 * w.x, h[i].y * s1 * w.y, h[i].z * s1 * w.z, h[i].w * s1 * w.w);
-            ss2 += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
-        }
-    }
-    ss2 = warp_sum(ss2);
-    const float s2 = rsqrtf(ss2 / (float)d + eps);
+    for (int i = threadIdx.x; i < nv; i += INW * 32)
+        reinterpret_cast<float4*>(wsm)[i] = reinterpret_cast<const float4*>(ctx_norm)[i];
     for (int l = 0; l < n_layers; ++l) {
         const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
-        TO* o = out + l * layer_stride + (int64_t)row * d;
+        for (int i = threadIdx.x; i < nv; i += INW * 32) reinterpret_cast<float4*>(wsm + (l + 1) * d)[i] = an[i];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * INW + (threadIdx.x >> 5)) * rows_per_warp;
+    for (int rr = 0; rr < rows_per_warp; ++rr) {
+        const int row = row0 + rr;
+        if (row >= rows) break;
+        const float4* pr = reinterpret_cast<const float4*>(P + (int64_t)row * d);
+        float4 h[MAXV];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < MAXV; ++i) {
+            const int v = lane + 32 * i;
+            h[i] = v < nv ? pr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
+        }
+        ss = warp_sum(ss);
+        const float s1 = rsqrtf(ss / (float)d + eps);
+        const float4* cn = reinterpret_cast<const float4*>(wsm);
+        float ss2 = 0.f;
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
             const int v = lane + 32 * i;
             if (v < nv) {
-                const float4 w = an[v];
-                store4(o + 4 * v, h[i].x * s2 * w.x, h[i].y * s2 * w.y, h[i].z * s2 * w.z, h[i].w * s2 * w.w);
+                const float4 w = cn[v];
+                h[i] = make_float4(h[i].x * s1 * w.x, h[i].y * s1 * w.y, h[i].z * s1 * w.z, h[i].w * s1 * w.w);
+                ss2 += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
+            }
+        }
+        ss2 = warp_sum(ss2);
+        const float s2 = rsqrtf(ss2 / (float)d + eps);
+        for (int l = 0; l < n_layers; ++l) {
+            const float4* an = reinterpret_cast<const float4*>(wsm + (l + 1) * d);
+            TO* o = out + l * layer_stride + (int64_t)row * d;
+#pragma unroll
+            for (int i = 0; i < MAXV; ++i) {
+                const int v = lane + 32 * i;
+                if (v < nv) {
+                    const float4 w = an[v];
+                    store4(o + 4 * v, h[i].x * s2 * w.x, h[i].y * s2 * w.y, h[i].z * s2 * w.z, h[i].w * s2 * w.w);
+                }
             }
         }
     }
@@ -242,20 +252,50 @@ cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, 
     return cudaGetLastError();
 }
 
+template <typename TO, int MAXV>
+cudaError_t launch_ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
+                               const float* const* attn_norm_dev, int n_layers, void* out, int64_t layer_stride,
+                               cudaStream_t st) {
+    const size_t sm = (size_t)(n_layers + 1) * d * sizeof(float);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_ingest_norm<TO, MAXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    // about two CTAs per SM; each CTA stages the norm vectors once
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int rpw = std::max(1, (rows + INW * 2 * sms - 1) / (INW * 2 * sms));
+    const int blocks = (rows + INW * rpw - 1) / (INW * rpw);
+    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, sm, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
+           (TO*)out, layer_stride, rpw);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <typename TO>
+cudaError_t ingest_norm_t(const float* P, int rows, int d, float eps, const float* ctx_norm,
+                          const float* const* attn_norm_dev, int n_layers, void* out, int64_t layer_stride,
+                          cudaStream_t st) {
+    const int per_lane = (d / 4 + 31) / 32;
+    if (per_lane <= 2) return launch_ingest_norm<TO, 2>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 4) return launch_ingest_norm<TO, 4>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 8) return launch_ingest_norm<TO, 8>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 16) return launch_ingest_norm<TO, 16>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    return launch_ingest_norm<TO, 32>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+}
+
 cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
                         const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
                         int64_t layer_stride, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    if (d % 4 != 0 || d > 4096) return cudaErrorInvalidValue;
-    const int blocks = (rows + INW - 1) / INW;
+    if (d % 4 != 0 || d > 4096 || (size_t)(n_layers + 1) * d * sizeof(float) > 200 * 1024) return cudaErrorInvalidValue;
     if (out_dtype == DT_BF16)
-        launch(k_ingest_norm<bf16>, blocks, INW * 32, 0, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
-               (bf16*)out, layer_stride);
-    else
-        launch(k_ingest_norm<float>, blocks, INW * 32, 0, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
-               (float*)out, layer_stride);
-    note_launch();
-    return cudaGetLastError();
+        return ingest_norm_t<bf16>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    return ingest_norm_t<float>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
 }
 
 cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st) {
