@@ -482,7 +482,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.ctas = h->mk_ctas;
     Prof pr(h, CAT_MARKOV, st);
     // one cooperative launch when B sequences x ctas fit co-resident, else one launch per position
-    const int chain_ctas = std::min(std::min(h->mk_ctas, h->num_sms), h->mk_chain_max / std::max(B, 1));
+    const int chain_ctas = std::min(h->mk_ctas, h->mk_chain_max / std::max(B, 1));
     if (chain_ctas >= 8 || chain_ctas >= h->mk_ctas) {
         mp.ctas = chain_ctas;
         CUDA_TRY(h, markov_chain(mp, h->mk_bar, h->mk_bar + 1, st));

@@ -355,8 +355,8 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
 }  // namespace
 
 int markov_ctas(int V) {
-    int c = (V + 255) / 256;  // 256 vocabulary rows per CTA
-    return c < 1 ? 1 : (c > 2048 ? 2048 : c);
+    int c = (V + 127) / 128;  // 128 vocabulary rows per CTA
+    return c < 1 ? 1 : (c > 4096 ? 4096 : c);
 }
 
 int markov_chain_max_ctas(int w_dtype) {
