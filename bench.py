@@ -1,14 +1,20 @@
 #!/usr/bin/env python
 """Benchmark of the DSpark/DFlash drafter step on one GB300 (or N replicas).
 
-Workload (default): the MiniCPM-shaped drafter in bf16 (H 2048, m 5 taps,
-d 2048, 16 heads of 128, 5 layers, F 4096, gamma 8, V 73448, Markov rank 256),
-batch 1.  One step = a fresh sequence ingests L = 1024 context rows of
-features [1024, 10240] (Eq 2 + Eq 3 into the per-layer K/V caches) and drafts
-one block of 8 tokens over that context.  Inputs are seeded synthetic draws
-(weights N(0, 0.02), norms 1, features and embedding N(0, 1)); 16 distinct
-feature batches (21 MB each) are cycled, so every step streams > 1 GB of
-weights, caches and features: far more than the 129 MB L2.
+Workload (default, --workload minicpm_L1024): the MiniCPM-shaped drafter in
+bf16 (H 2048, m 5 taps, d 2048, 16 heads of 128, 5 layers, F 4096, gamma 8,
+V 73448, Markov rank 256), batch 1.  One step = a fresh sequence ingests
+L = 1024 context rows of features [1024, 10240] (Eq 2 + Eq 3 into the
+per-layer K/V caches) and drafts one block of 8 tokens over that context.
+Inputs are seeded synthetic draws (weights N(0, 0.02), norms 1, features and
+embedding N(0, 1)); 16 distinct feature batches (21 MB each) are cycled, so
+every step streams > 1 GB of weights, caches and features: far more than the
+129 MB L2.
+
+Other workloads (same JSON line): gemma_L32768_ingest (a fresh 32768-row
+context and 16 blocks per step), gemma_L4096_stream (1-6 new rows and one
+block per step over a 4096-row context), gemma_batched64 (64 ragged sequences,
+1-6 new rows and one block each per step).
 
 Prints one JSON line: draft blocks/s (= steps/s) over the whole job, context
 tokens/s, the per-phase rates, the roofline of the dominant kernel class
@@ -131,42 +137,50 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- work accounting
 
-def class_work(cls: str, cfg, T: int, L: int):
+def class_work(cls: str, cfg, T: int, L_total: int, B: int):
     """Algorithmic bytes and flops of one timed range of a kernel class, and its bound.
 
-    T: context rows ingested per step; L: context length at draft time.
-    bf16 weights/caches (2 B), fp32 activations/logits (4 B)."""
+    T: context rows in one ingest range; L_total: context rows summed over the
+    B sequences of one draft; B: sequences per draft.  bf16 weights, features
+    and caches (2 B), fp32 logits (4 B).  A projection over <= 16 activation
+    rows streams its weights once (HBM-bound); more rows make it a dense
+    contraction (tensor-bound)."""
     d, F, H, V, r, g, nL, mH = (cfg.d_draft, cfg.ff, cfg.hidden, cfg.vocab, cfg.markov_rank, cfg.gamma,
                                 cfg.n_layers, cfg.feat_dim)
+    rows = B * g
+    gemm_bound = "hbm" if rows <= 16 else "tensor"
     if cls == "ingest_proj":
-        return dict(bytes=T * mH * 2 + d * mH * 2 + T * d * 4, flops=2 * T * mH * d, bound="tensor")
+        return dict(bytes=T * mH * 2 + d * mH * 2 + T * d * 4, flops=2 * T * mH * d,
+                    bound="tensor" if T > 16 else "hbm")
     if cls == "ingest_kv":
-        return dict(bytes=nL * (T * d * 2 + 2 * d * d * 2 + T * 2 * d * 2), flops=nL * 2 * T * d * 2 * d, bound="tensor")
+        return dict(bytes=nL * (T * d * 2 + 2 * d * d * 2 + T * 2 * d * 2), flops=nL * 2 * T * d * 2 * d,
+                    bound="tensor" if T > 16 else "hbm")
     if cls == "out_proj":
-        return dict(bytes=V * d * 2 + g * V * 4, flops=2 * g * V * d, bound="hbm")
+        return dict(bytes=V * d * 2 + rows * V * 4, flops=2 * rows * V * d, bound=gemm_bound)
     if cls == "attention":
-        return dict(bytes=2 * (L + g) * d * 2, flops=4 * g * (L + g) * d, bound="hbm")
+        return dict(bytes=2 * (L_total + rows) * d * 2, flops=4 * g * (L_total + rows) * d, bound="hbm")
     if cls == "markov_argmax":
-        return dict(bytes=V * r * 2 + g * V * 4, flops=2 * g * V * r, bound="hbm")
+        return dict(bytes=V * r * 2 + rows * V * 4, flops=2 * rows * V * r, bound="hbm")
     if cls == "qkv_proj":
-        return dict(bytes=3 * d * d * 2, flops=2 * g * 3 * d * d, bound="hbm")
+        return dict(bytes=3 * d * d * 2, flops=2 * rows * 3 * d * d, bound=gemm_bound)
     if cls == "o_proj":
-        return dict(bytes=d * d * 2, flops=2 * g * d * d, bound="hbm")
+        return dict(bytes=d * d * 2, flops=2 * rows * d * d, bound=gemm_bound)
     if cls == "gate_up_proj":
-        return dict(bytes=2 * F * d * 2, flops=2 * g * 2 * F * d, bound="hbm")
+        return dict(bytes=2 * F * d * 2, flops=2 * rows * 2 * F * d, bound=gemm_bound)
     if cls == "down_proj":
-        return dict(bytes=F * d * 2, flops=2 * g * F * d, bound="hbm")
+        return dict(bytes=F * d * 2, flops=2 * rows * F * d, bound=gemm_bound)
     if cls == "block_build":
-        return dict(bytes=d * H * 2, flops=2 * d * H, bound="hbm")
+        return dict(bytes=d * H * 2, flops=2 * B * d * H, bound="hbm")
     return dict(bytes=0, flops=0, bound="hbm")
 
 
-def draft_bytes_min(cfg, L):
-    """Algorithmic bytes of one batch-1 draft block: every weight once (w2 once),
-    the caches of all layers, the embedding row."""
+def draft_bytes_min(cfg, L_total, B=1):
+    """Algorithmic bytes of one draft call: every weight once (w2 once), the
+    caches of all layers for every sequence, the embedding rows."""
     d, F, H, V, r, nL = cfg.d_draft, cfg.ff, cfg.hidden, cfg.vocab, cfg.markov_rank, cfg.n_layers
     layers = nL * (4 * d * d + 3 * F * d) * 2
-    return layers + d * H * 2 + V * d * 2 + V * r * 2 + cfg.gamma * r * 2 + nL * 2 * (L + cfg.gamma) * d * 2 + H * 2
+    return (layers + d * H * 2 + V * d * 2 + V * r * 2 + B * cfg.gamma * r * 2
+            + nL * 2 * (L_total + B * cfg.gamma) * d * 2 + B * H * 2)
 
 
 def ingest_flops(cfg, T):
@@ -205,24 +219,6 @@ def load_traffic(kernel_class: str, workload: str):
     return ent["bytes_per_range"] if digest == ent.get("source_sha") else None
 
 
-# --------------------------------------------------------------------------- CPU oracle timing
-
-def time_oracle(wl, W, feats_pool, anchors, seconds: float, max_steps: int):
-    import oracle
-    cfg = wl.cfg
-    dr = oracle.Drafter(cfg, W)
-    n, t0 = 0, time.perf_counter()
-    while n < max_steps:
-        dr.reset(0)
-        dr.ingest(feats_pool[n % len(feats_pool)])
-        dr.draft(int(anchors[n % len(anchors)]))
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return n, dt
-
-
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -230,38 +226,292 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def bf16_dev(a, dev):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    return t.view(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Runner:
+    """One workload: its step (one pass of the whole hot path), its units, and its oracle sample."""
+    metric = ""
+    unit = "blocks/s"
+    blocks_per_step = 1
+
+    def __init__(self, wl, dev, seed=0):
+        self.wl, self.cfg, self.dev, self.seed = wl, wl.cfg, dev, seed
+
+    # GPU side
+    def make_drafter(self, W, max_ctx, max_seqs=1):
+        import torch
+
+        import block_draft_model_gb300 as bdm
+        cfg = self.cfg
+        self.Wd = {k: (bf16_dev(v, self.dev) if v.dtype == np.uint16 else torch.from_numpy(v).to(self.dev))
+                   for k, v in W.items()}
+        return bdm.Drafter(hidden=cfg.hidden, n_taps=cfg.n_taps, d_draft=cfg.d_draft, n_heads=cfg.n_heads,
+                           n_layers=cfg.n_layers, ff_mult=cfg.ff_mult, gamma=cfg.gamma, vocab=cfg.vocab,
+                           markov_rank=cfg.markov_rank, eps=cfg.eps, dtype=bdm.BF16, max_ctx=max_ctx,
+                           max_seqs=max_seqs, weights=self.Wd)
+
+
+class FreshContextRunner(Runner):
+    """Batch 1: every step ingests a fresh context of L rows, then drafts `drafts` blocks."""
+
+    def __init__(self, wl, dev, drafts=1, pool=POOL, seed=0):
+        super().__init__(wl, dev, seed)
+        self.T, self.drafts, self.npool = wl.ctx_len, drafts, pool
+        self.blocks_per_step = drafts
+        self.metric = (f"draft blocks/s (batch 1, fresh context of {self.T} rows ingested per step, "
+                       f"{drafts} block{'s' if drafts > 1 else ''} per step)")
+        self.ctx_tokens_per_step = self.T
+        self.L_total = self.T
+
+    def setup(self):
+        import torch
+        cfg = self.cfg
+        self.W = syn.make_weights(cfg, seed=self.seed)
+        self.g = self.make_drafter(self.W, max_ctx=self.T)
+        self.pool_np = [syn.make_feats(cfg, self.T, seed=self.seed, step=i) for i in range(self.npool)]
+        self.pool = [bf16_dev(x, self.dev) for x in self.pool_np]
+        self.anchors = syn.uniform_int(self.seed, syn.STREAM_ANCHORS, (max(self.npool, 16) * self.drafts,), 0,
+                                       cfg.vocab - 1)
+        self.tok = torch.empty(cfg.gamma, dtype=torch.int32, device=self.dev)
+        self.conf = torch.empty(cfg.gamma, dtype=torch.float32, device=self.dev)
+        self.host_pool = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in self.pool_np[:2]]
+        self.tok_h = torch.empty(cfg.gamma, dtype=torch.int32).pin_memory()
+        self.conf_h = torch.empty(cfg.gamma, dtype=torch.float32).pin_memory()
+        self.h2d = self.T * cfg.feat_dim * 2
+        self.d2h = self.drafts * cfg.gamma * 8
+
+    def step(self, i):
+        g = self.g
+        g.reset(0)
+        g.ingest_context(self.pool[i % self.npool])
+        for j in range(self.drafts):
+            g.draft(int(self.anchors[(i * self.drafts + j) % len(self.anchors)]), self.tok, self.conf)
+
+    def host_step(self, i):
+        g = self.g
+        g.reset(0)
+        g.ingest_context_host(self.host_pool[i % len(self.host_pool)])
+        for j in range(self.drafts):
+            g.draft_host(int(self.anchors[(i * self.drafts + j) % len(self.anchors)]), self.tok_h, self.conf_h)
+
+    def phases(self, timed):
+        g, T = self.g, self.T
+        ms_ingest = timed(lambda i: (g.reset(0), g.ingest_context(self.pool[i % self.npool])))
+        g.reset(0)
+        g.ingest_context(self.pool[0])
+        ms_draft = timed(lambda i: g.draft(int(self.anchors[i % len(self.anchors)]), self.tok, self.conf))
+        bm = draft_bytes_min(self.cfg, T)
+        return {"ingest_ms": ms_ingest, "ingest_ctx_tokens_per_s": T / (ms_ingest / 1e3),
+                "ingest_tflops": ingest_flops(self.cfg, T) / (ms_ingest / 1e3) / 1e12,
+                "draft_ms": ms_draft, "draft_blocks_per_s": 1e3 / ms_draft, "draft_bytes_min": bm,
+                "draft_gbs_of_bytes_min": bm / (ms_draft / 1e3) / 1e9}
+
+    def oracle_baseline(self, seconds, max_steps):
+        """The CPU oracle on a bounded sample of this workload, scaled to blocks/s of the full step:
+        ingest of up to 4096 rows and one draft are timed separately, the step time is
+        T / rows * t_ingest + drafts * t_draft."""
+        import oracle
+        dr = oracle.Drafter(self.cfg, self.W)
+        rows = min(self.T, 4096)
+        n, t_in, t_dr, t0 = 0, 0.0, 0.0, time.perf_counter()
+        while n < max_steps:
+            dr.reset(0)
+            a = time.perf_counter()
+            dr.ingest(self.pool_np[n % self.npool][:rows])
+            b = time.perf_counter()
+            dr.draft(int(self.anchors[n % len(self.anchors)]))
+            c = time.perf_counter()
+            t_in += b - a
+            t_dr += c - b
+            n += 1
+            if c - t0 >= seconds:
+                break
+        step_s = (t_in / n) * self.T / rows + (t_dr / n) * self.drafts
+        sample = (f"{n} x (ingest {rows} rows + 1 block) of the same drafter, fp64"
+                  + ("" if rows == self.T and self.drafts == 1 else
+                     f"; scaled to a step of {self.T} rows + {self.drafts} blocks"))
+        return self.drafts / step_s, sample
+
+
+class StreamRunner(Runner):
+    """Batch 1: a context of L rows is ingested once; every step ingests 1-6 new rows and drafts one block."""
+
+    def __init__(self, wl, dev, seed=0):
+        super().__init__(wl, dev, seed)
+        self.metric = f"draft blocks/s (batch 1, context {wl.ctx_len} rows growing by 1-6 rows per step)"
+
+    def setup(self):
+        import torch
+        cfg, wl = self.cfg, self.wl
+        self.W = syn.make_weights(cfg, seed=self.seed)
+        self.max_ctx = wl.ctx_len + 6 * 4096
+        self.g = self.make_drafter(self.W, max_ctx=self.max_ctx)
+        self.g.ingest_context(bf16_dev(syn.make_feats(cfg, wl.ctx_len, seed=self.seed), self.dev))
+        counts = syn.uniform_int(self.seed, syn.STREAM_COUNTS, (256,), 1, 6)
+        new_np = [syn.make_feats(cfg, int(c), seed=self.seed, step=i) for i, c in enumerate(counts)]
+        self.new = [bf16_dev(x, self.dev) for x in new_np]
+        self.new_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in new_np[:32]]
+        self.length = wl.ctx_len
+        self.tok_h = torch.empty(cfg.gamma, dtype=torch.int32).pin_memory()
+        self.conf_h = torch.empty(cfg.gamma, dtype=torch.float32).pin_memory()
+        self.anchors = syn.uniform_int(self.seed, syn.STREAM_ANCHORS, (256,), 0, cfg.vocab - 1)
+        self.tok = torch.empty(cfg.gamma, dtype=torch.int32, device=self.dev)
+        self.conf = torch.empty(cfg.gamma, dtype=torch.float32, device=self.dev)
+        self.ctx_tokens_per_step = float(counts.mean())
+        self.L_total = wl.ctx_len
+        self.h2d = int(self.ctx_tokens_per_step * cfg.feat_dim * 2)
+        self.d2h = cfg.gamma * 8
+
+    def step(self, i):
+        x = self.new[i % len(self.new)]
+        self.length += x.shape[0]
+        if self.length > self.max_ctx:
+            raise RuntimeError("context capacity exhausted; lower --steps")
+        self.g.ingest_context(x)
+        self.g.draft(int(self.anchors[i % len(self.anchors)]), self.tok, self.conf)
+
+    def host_step(self, i):
+        x = self.new_h[i % len(self.new_h)]
+        self.length += x.shape[0]
+        if self.length > self.max_ctx:
+            raise RuntimeError("context capacity exhausted; lower --steps")
+        self.g.ingest_context_host(x)
+        self.g.draft_host(int(self.anchors[i % len(self.anchors)]), self.tok_h, self.conf_h)
+
+    def phases(self, timed):
+        return {}
+
+
+class BatchedRunner(Runner):
+    """64 sequences with ragged contexts; every step ingests 1-6 rows per sequence and drafts one block each."""
+
+    def __init__(self, wl, dev, seed=0):
+        super().__init__(wl, dev, seed)
+        self.blocks_per_step = wl.n_seqs
+        self.metric = (f"draft blocks/s ({wl.n_seqs} sequences per step, ragged contexts "
+                       f"{wl.ctx_len_range[0]}-{wl.ctx_len_range[1]} rows, 1-6 new rows per sequence per step)")
+
+    def setup(self):
+        import torch
+        cfg, wl = self.cfg, self.wl
+        n = wl.n_seqs
+        self.W = syn.make_weights(cfg, seed=self.seed)
+        lens = syn.ctx_lengths(wl, seed=self.seed)
+        self.max_ctx = int(lens.max()) + 6 * 2048
+        self.g = self.make_drafter(self.W, max_ctx=self.max_ctx, max_seqs=n)
+        self.ids = torch.arange(n, dtype=torch.int32, device=self.dev)
+        for i in range(n):  # one-shot contexts, one sequence at a time to bound host memory
+            feats = bf16_dev(syn.make_feats(cfg, int(lens[i]), seed=self.seed, seq=i), self.dev)
+            cu = torch.tensor([0, int(lens[i])], dtype=torch.int32, device=self.dev)
+            self.g.ingest_context_batched(self.ids[i:i + 1], cu, feats)
+        self.L_total = int(lens.sum())
+        counts = syn.uniform_int(self.seed, syn.STREAM_COUNTS, (64, n), 1, 6)
+        self.steps_in = []
+        for s in range(counts.shape[0]):
+            feats = np.concatenate([syn.make_feats(cfg, int(c), seed=self.seed, step=s, seq=i)
+                                    for i, c in enumerate(counts[s])])
+            cu = np.concatenate([[0], np.cumsum(counts[s])]).astype(np.int32)
+            self.steps_in.append((bf16_dev(feats, self.dev), torch.from_numpy(cu).to(self.dev),
+                                  torch.from_numpy(feats.view(np.int16)).pin_memory(), torch.from_numpy(cu).pin_memory()))
+        anchors = syn.uniform_int(self.seed, syn.STREAM_ANCHORS, (64, n), 0, cfg.vocab - 1)
+        self.anchors = [torch.from_numpy(a.copy()).to(self.dev) for a in anchors]
+        self.anchors_h = [torch.from_numpy(a.copy()).pin_memory() for a in anchors]
+        self.tok = torch.empty(n, cfg.gamma, dtype=torch.int32, device=self.dev)
+        self.conf = torch.empty(n, cfg.gamma, dtype=torch.float32, device=self.dev)
+        self.tok_h = torch.empty(n, cfg.gamma, dtype=torch.int32).pin_memory()
+        self.conf_h = torch.empty(n, cfg.gamma, dtype=torch.float32).pin_memory()
+        self.ctx_tokens_per_step = float(counts.sum(axis=1).mean())
+        self.h2d = int(self.ctx_tokens_per_step * cfg.feat_dim * 2 + (n + 1) * 4 + n * 4)
+        self.d2h = n * cfg.gamma * 8
+
+    def step(self, i):
+        feats, cu, _, _ = self.steps_in[i % len(self.steps_in)]
+        self.g.ingest_context_batched(self.ids, cu, feats)
+        self.g.draft_batched(self.ids, self.anchors[i % len(self.anchors)], self.tok, self.conf)
+
+    def host_step(self, i):
+        _, _, feats_h, cu_h = self.steps_in[i % len(self.steps_in)]
+        feats = feats_h.to(self.dev, non_blocking=True).view(__import__("torch").bfloat16)
+        cu = cu_h.to(self.dev, non_blocking=True)
+        anchors = self.anchors_h[i % len(self.anchors_h)].to(self.dev, non_blocking=True)
+        self.g.ingest_context_batched(self.ids, cu, feats)
+        self.g.draft_batched(self.ids, anchors, self.tok, self.conf)
+        self.tok_h.copy_(self.tok)
+        self.conf_h.copy_(self.conf)
+
+    def phases(self, timed):
+        return {}
+
+
+def make_runner(name, dev):
+    wl = syn.WORKLOADS[name]
+    if name == "minicpm_L1024":
+        return FreshContextRunner(wl, dev)
+    if name == "gemma_L32768_ingest":
+        return FreshContextRunner(wl, dev, drafts=wl.steps, pool=2)
+    if name == "gemma_L4096_stream":
+        return StreamRunner(wl, dev)
+    if name == "gemma_batched64":
+        return BatchedRunner(wl, dev)
+    raise SystemExit(f"unknown workload {name}")
+
+
 # --------------------------------------------------------------------------- main
+
+def reference_arm(args):
+    """The CPU oracle on the default workload, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = syn.WORKLOADS[args.workload]
+    cfg = wl.cfg
+    T = wl.ctx_len or 1024
+    W = syn.make_weights(cfg, seed=0)
+    pool = [syn.make_feats(cfg, min(T, 4096), seed=0, step=i) for i in range(2)]
+    anchors = syn.uniform_int(0, syn.STREAM_ANCHORS, (64,), 0, cfg.vocab - 1)
+    import oracle
+    dr = oracle.Drafter(cfg, W)
+
+    def one(i):
+        dr.reset(0)
+        dr.ingest(pool[i % 2])
+        dr.draft(int(anchors[i % 64]))
+
+    n_w = max(1, args.warmup)
+    for i in range(n_w):
+        one(i)
+    t0 = time.perf_counter()
+    n = 0
+    while n < args.steps:
+        one(n)
+        n += 1
+        if time.perf_counter() - t0 > 240:
+            break
+    dt = time.perf_counter() - t0
+    v = n / dt
+    sample = f"{n} steps of ingest {min(T, 4096)} rows + 1 block (fp64 numpy, {cpu_cores()} threads)"
+    line = {"impl": "reference", "metric": f"draft blocks/s ({wl.name}, CPU oracle)", "value": v,
+            "unit": "blocks/s", "n_gpus": args.gpus, "steps": n, "warmup": n_w, "ms_per_step": 1e3 * dt / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "ctx_len": T, "gamma": cfg.gamma, "batch": 1},
+            "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
 
 def main():
     args = parse()
-    wl = syn.WORKLOADS[args.workload]
-    cfg = wl.cfg
-    assert wl.n_seqs == 1 and cfg.dtype == "bf16", "the bench drives batch-1 bf16 workloads"
-    rank, world, local = dist_setup(args.gpus)
-    T = wl.ctx_len
-    metric = "draft blocks/s (batch 1, fresh context of 1024 rows ingested per block)"
-
-    anchors = syn.anchors(syn.Workload(wl.name, cfg, steps=POOL))[:, 0]
     if args.impl == "reference":
-        if rank != 0:
-            return
-        W = syn.make_weights(cfg, seed=0)
-        pool = [syn.make_feats(cfg, T, seed=0, step=i) for i in range(min(POOL, 4))]
-        import oracle  # noqa: F401
-        n_w = max(1, args.warmup)
-        time_oracle(wl, W, pool, anchors, 1e9, n_w)
-        n, dt = time_oracle(wl, W, pool, anchors, 1e9, args.steps)
-        v = n / dt
-        line = {"impl": "reference", "metric": metric, "value": v, "unit": "blocks/s", "n_gpus": args.gpus,
-                "steps": n, "warmup": n_w, "ms_per_step": 1e3 * dt / n, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl.name, "ctx_len": T, "gamma": cfg.gamma, "batch": 1},
-                "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
-                                 "sample": f"{n} full steps (ingest {T} rows + 1 block), fp64 numpy"},
-                "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
+        reference_arm(args)
         return
-
+    rank, world, local = dist_setup(args.gpus)
     import torch
 
     import block_draft_model_gb300 as bdm
@@ -269,32 +519,21 @@ def main():
     dev = torch.device("cuda", local)
     bdm.build()
     bdm.load()
-    W = syn.make_weights(cfg, seed=0)
-    Wd = {}
-    for k, v in W.items():
-        t = torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
-        Wd[k] = t.view(torch.bfloat16) if v.dtype == np.uint16 else t
-    pool_np = [syn.make_feats(cfg, T, seed=0, step=i) for i in range(POOL)]
-    pool = [torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in pool_np]
-    g = bdm.Drafter(hidden=cfg.hidden, n_taps=cfg.n_taps, d_draft=cfg.d_draft, n_heads=cfg.n_heads,
-                    n_layers=cfg.n_layers, ff_mult=cfg.ff_mult, gamma=cfg.gamma, vocab=cfg.vocab,
-                    markov_rank=cfg.markov_rank, eps=cfg.eps, dtype=bdm.BF16, max_ctx=T, weights=Wd)
+    run = make_runner(args.workload, dev)
+    run.setup()
+    cfg, g = run.cfg, run.g
     stream = torch.cuda.current_stream(dev)
-    tok = torch.empty(cfg.gamma, dtype=torch.int32, device=dev)
-    conf = torch.empty(cfg.gamma, dtype=torch.float32, device=dev)
-
-    def step(i):
-        g.reset(0)
-        g.ingest_context(pool[i % POOL])
-        g.draft(int(anchors[i % POOL]), tok, conf)
+    B = run.wl.n_seqs
 
     # warm-up, with a profile of every kernel class to find the dominant one
-    for i in range(max(3, args.warmup)):
-        step(i)
+    nw = max(3, args.warmup)
+    for i in range(nw):
+        run.step(i)
     torch.cuda.synchronize()
     g.profile(-1)
-    for i in range(4):
-        step(i)
+    nprof = 2
+    for i in range(nprof):
+        run.step(nw + i)
     torch.cuda.synchronize()
     prof_all = g.profile_read()
     g.profile(0)
@@ -309,9 +548,10 @@ def main():
     g.profile(1 << prof_all[dominant][3])
     l0 = g.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    base = nw + nprof
     ev0.record(stream)
     for i in range(args.steps):
-        step(i)
+        run.step(base + i)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -322,27 +562,25 @@ def main():
     ms_max = reduce_max(ms, world, dev)
     clk = clocks.stop() if rank == 0 else None
 
-    # the dominant kernel's live timing (ranges recorded on the launching stream in the timed region)
+    # the dominant kernel class, timed live (event pairs on the launching stream inside the timed region)
     dms, dranges, dlaunch, _ = prof[dominant]
     peaks = load_peaks()
-    work = class_work(dominant, cfg, T, T)
+    T_range = getattr(run, "T", int(round(run.ctx_tokens_per_step)))
+    work = class_work(dominant, cfg, T_range, run.L_total, B)
     per_range_s = dms / 1e3 / max(dranges, 1)
     if work["bound"] == "tensor":
         ach = work["flops"] / per_range_s / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
     else:
         ach = work["bytes"] / per_range_s / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
+        peak, unit = peaks["hbm_gbs"], "GB/s"
     roofline = {"kernel": dominant, "bound": work["bound"], "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "peak_src": peaks["src"], "traffic": load_traffic(dominant, wl.name),
+                "frac": ach / peak, "peak_src": peaks["src"], "traffic": load_traffic(dominant, run.wl.name),
                 "algorithmic_per_launch": work["bytes"] if work["bound"] == "hbm" else work["flops"],
                 "avg_range_us": per_range_s * 1e6, "launches_per_range": dlaunch / max(dranges, 1),
                 "share_of_step": prof_all[dominant][0] / sum(v[0] for v in prof_all.values())}
 
-    # phases (outside the timed region): ingest-only and draft-only rates
-    def timed(fn, n):
+    def timed(fn, n=max(10, min(args.steps, 50))):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         a.record(stream)
@@ -352,54 +590,42 @@ def main():
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n
 
-    nph = max(10, min(args.steps, 50))
-    ms_ingest = timed(lambda i: (g.reset(0), g.ingest_context(pool[i % POOL])), nph)
-    g.reset(0)
-    g.ingest_context(pool[0])
-    ms_draft = timed(lambda i: g.draft(int(anchors[i % POOL]), tok, conf), nph)
-    per_class = {k: round(v[0] / 4, 4) for k, v in prof_all.items() if v[1]}
+    phases = run.phases(timed) if hasattr(run, "phases") else {}
+    phases["per_class_ms_per_step"] = {k: round(v[0] / nprof, 4) for k, v in prof_all.items() if v[1]}
+    phases["note"] = ("per-class times come from a separate profiled pass whose event pairs break the "
+                      "launch overlap; they rank the kernels, the step time is the timed region's")
 
-    # end to end through the host-buffer C-ABI calls (pinned host memory)
-    host_pool = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in pool_np[:4]]
-    tok_h = torch.empty(cfg.gamma, dtype=torch.int32).pin_memory()
-    conf_h = torch.empty(cfg.gamma, dtype=torch.float32).pin_memory()
-    ne2e = max(5, min(args.steps, 50))
-    for i in range(2):
-        g.reset(0)
-        g.ingest_context_host(host_pool[i % 4])
-        g.draft_host(int(anchors[i % POOL]), tok_h, conf_h)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(ne2e):
-        g.reset(0)
-        g.ingest_context_host(host_pool[i % 4])
-        g.draft_host(int(anchors[i % POOL]), tok_h, conf_h)
-    e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+    # end to end through the public API with host buffers (pinned): copies inside the timed region
+    e2e = None
+    if getattr(run, "host_step", None):
+        ne = max(5, min(args.steps, 30))
+        for i in range(2):
+            run.host_step(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(ne):
+            run.host_step(i)
+        torch.cuda.synchronize()
+        e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * ne * run.blocks_per_step / e2e_s, "unit": "blocks/s",
+               "h2d_bytes_per_step": int(run.h2d), "d2h_bytes_per_step": int(run.d2h)}
     assert g.check() == 0
 
-    value = world * args.steps / (ms_max / 1e3)
-    line = {"metric": metric, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "ctx_len": T, "gamma": cfg.gamma, "batch": 1, "d_draft": cfg.d_draft,
-                       "vocab": cfg.vocab, "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (>1 GB streamed per step; 16 feature batches cycled)"},
-            "ctx_tokens_per_s": value * T,
-            "phases": {"ingest_ms": ms_ingest, "ingest_ctx_tokens_per_s": T / (ms_ingest / 1e3),
-                       "ingest_tflops": ingest_flops(cfg, T) / (ms_ingest / 1e3) / 1e12,
-                       "draft_ms": ms_draft, "draft_blocks_per_s": 1e3 / ms_draft,
-                       "draft_bytes_min": draft_bytes_min(cfg, T),
-                       "draft_gbs_of_bytes_min": draft_bytes_min(cfg, T) / (ms_draft / 1e3) / 1e9,
-                       "per_class_ms": per_class},
-            "roofline": roofline,
-            "clocks": clk,
-            "gpu_launches": launches,
-            "e2e": {"value": world * ne2e / e2e_s, "unit": "blocks/s",
-                    "h2d_bytes_per_step": int(T * cfg.feat_dim * 2), "d2h_bytes_per_step": int(cfg.gamma * 8)}}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, dt = time_oracle(wl, W, pool_np[:4], anchors, args.cpu_seconds, 50)
-        line["cpu_baseline"] = {"value": n / dt, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": f"{n} full steps (ingest {T} rows + 1 block) of the same workload, fp64"}
+    value = world * args.steps * run.blocks_per_step / (ms_max / 1e3)
+    line = {"metric": run.metric, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+            "warmup": nw, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": run.wl.name, "ctx_len": run.wl.ctx_len, "sequences": B, "gamma": cfg.gamma,
+                       "d_draft": cfg.d_draft, "vocab": cfg.vocab,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (weights, caches and features stream > 1 GB per step)"},
+            "ctx_tokens_per_s": world * args.steps * run.ctx_tokens_per_step / (ms_max / 1e3),
+            "phases": phases, "roofline": roofline, "clocks": clk, "gpu_launches": launches, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(run, FreshContextRunner):
+        v, sample = run.oracle_baseline(args.cpu_seconds, 50)
+        line["cpu_baseline"] = {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     g.close()
