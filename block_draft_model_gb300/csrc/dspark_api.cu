@@ -108,6 +108,12 @@ struct dspark_handle {
     unsigned int* mk_cnt = nullptr;
     int mk_ctas = 1;
     int mk_chain_max = 0;                    // largest co-resident grid of the one-launch Markov chain
+    TcWeight tc_w2;                          // w2 [V, r] for the many-sequence Markov GEMM
+    TcWeight tc_tok_proj;                    // tok_proj [d, H] for the many-sequence block build
+    void* emb_rows = nullptr;                // [max_seqs, H] gathered anchor embeddings (bf16)
+    void* mk_E = nullptr;                    // [max_seqs, r] gathered w1 rows (bf16)
+    float* mk_pv = nullptr;                  // [max_seqs, ceil(V/32)] chunk partials
+    int* mk_pi = nullptr;
     unsigned int* mk_bar = nullptr;          // [2] grid-barrier words
     float* ws = nullptr;
     size_t ws_floats = 0;
@@ -360,8 +366,14 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ep.kind = EPI_ADD_F32;
         ep.out_f32 = h->x;
         ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
-        CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
-                         WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
+        if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
+            // many sequences: gather the anchor embeddings, then one tensor-core GEMM
+            CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
+            CUDA_TRY(h, tc_gemm(h->emb_rows, c.hidden, h->tc_tok_proj, B, d, c.hidden, ep, h->num_sms, h->d_err, st));
+        } else {
+            CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
+                             WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
+        }
     }
     const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
     void* actA = lowp ? h->act_lp : (void*)h->act;
@@ -481,6 +493,26 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.err = h->d_err;
     mp.ctas = h->mk_ctas;
     Prof pr(h, CAT_MARKOV, st);
+    if (B >= 8 && h->tc_w2.ready && h->mk_E && tc_gemm_ok(B, V, c.markov_rank) && anchors_dev) {
+        // many sequences: per position a [B, r] x [V, r]^T tensor-core GEMM reads w2 once for all of them
+        const int nch = (V + 31) / 32;
+        for (int k = 0; k < c.gamma; ++k) {
+            CUDA_TRY(h, markov_gather(h->w1, c.markov_rank, V, anchors_dev, tokens, c.gamma, k, B, h->mk_E, st));
+            EpiParams ep;
+            ep.kind = EPI_MARKOV;
+            ep.ldo = V;
+            ep.gamma = c.gamma;
+            ep.mk_U = h->U;
+            ep.mk_logits = logits;
+            ep.mk_part_v = h->mk_pv;
+            ep.mk_part_i = h->mk_pi;
+            ep.mk_k = k;
+            CUDA_TRY(h, tc_gemm(h->mk_E, c.markov_rank, h->tc_w2, B, V, c.markov_rank, ep, h->num_sms, h->d_err, st));
+            CUDA_TRY(h, markov_finish(h->mk_pv, h->mk_pi, nch, h->w1, h->dt, h->y, h->conf_wb, anchors_dev, tokens, conf,
+                                      B, c.gamma, k, d, c.markov_rank, V, h->d_err, st));
+        }
+        return DSPARK_OK;
+    }
     // one cooperative launch when B sequences x ctas fit co-resident, else one launch per position
     const int chain_ctas = std::min(h->mk_ctas, h->mk_chain_max / std::max(B, 1));
     if (chain_ctas >= 8 || chain_ctas >= h->mk_ctas) {
@@ -717,6 +749,8 @@ void dspark_destroy(dspark_handle* h) {
     for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
     tc_release(h->tc_wc);
     tc_release(h->tc_out_proj);
+    tc_release(h->tc_w2);
+    tc_release(h->tc_tok_proj);
     for (auto* v : {&h->tc_kv, &h->tc_qkv, &h->tc_wo, &h->tc_wgu, &h->tc_wd})
         for (auto& w : *v) tc_release(w);
     delete h;
@@ -889,6 +923,15 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));
             CTRY(tc_prepare(h->tc_wd[i], h->wd[i], d, F));
         }
+    }
+    if (h->dt == DT_BF16 && tc_available() && cfg->max_seqs >= 8) {
+        CTRY(tc_prepare(h->tc_w2, h->w2, V, r));
+        CTRY(tc_prepare(h->tc_tok_proj, h->tok_proj, d, H));
+        CTRY(dalloc(h, &h->emb_rows, (size_t)cfg->max_seqs * H * 2));
+        CTRY(dalloc(h, &h->mk_E, (size_t)cfg->max_seqs * r * 2));
+        const size_t nch = (size_t)(V + 31) / 32;
+        CTRY(dalloc(h, (void**)&h->mk_pv, (size_t)cfg->max_seqs * nch * 4));
+        CTRY(dalloc(h, (void**)&h->mk_pi, (size_t)cfg->max_seqs * nch * 4));
     }
     if (h->dt == DT_BF16 && tc_stream_ok(1, 1, 64)) {
         size_t part = 0, tiles = 0;

@@ -4,6 +4,8 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+#include <climits>
+
 namespace dspark {
 
 __device__ __forceinline__ float act_fn(int act, float g) {
@@ -92,6 +94,25 @@ __device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int
 
 __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v) {
     const bool full = n + 32 <= N;
+    if (ep.kind == EPI_MARKOV) {
+        const int64_t row = (int64_t)m * ep.gamma + ep.mk_k;
+        const float* u = ep.mk_U + row * ep.ldo + n;
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int j = 0; j < 32; ++j) {
+            if (n + j >= N) break;
+            const float l = v[j] + u[j];
+            if (ep.mk_logits) ep.mk_logits[row * ep.ldo + n + j] = l;
+            if (better(l, n + j, bv, bi)) {
+                bv = l;
+                bi = n + j;
+            }
+        }
+        const int nch = (N + 31) / 32;
+        ep.mk_part_v[(int64_t)m * nch + (n >> 5)] = bv;
+        ep.mk_part_i[(int64_t)m * nch + (n >> 5)] = bi;
+        return;
+    }
     switch (ep.kind) {
         case EPI_STORE_F32:
         case EPI_ADD_F32:

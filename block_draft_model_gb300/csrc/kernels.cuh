@@ -18,6 +18,7 @@ enum EpiKind {
     EPI_SWIGLU = 2,     // columns come in (gate, up) pairs: out_act[m * ld_act + n/2] = act(gate) * up
     EPI_KV_CACHE = 3,   // columns [0, d) -> K cache, [d, 2d) -> V cache, row -> (seq, position)
     EPI_QKV = 4,        // columns [0, d) -> out_f32 (Q), [d, 2d) -> K cache, [2d, 3d) -> V cache
+    EPI_MARKOV = 5,     // l = acc + U[m*gamma + k][n]; logits (optional); argmax partial per 32 columns
 };
 
 struct EpiParams {
@@ -40,6 +41,12 @@ struct EpiParams {
     const int* seq_len = nullptr;  // device context lengths per slot
     int gamma = 1;                 // EPI_QKV: GEMM row m is block row m % gamma of sequence m / gamma
     const int* seq_ids = nullptr;  // EPI_QKV: slot of sequence b (nullptr: slot b)
+    // EPI_MARKOV (row m = sequence, column n = vocabulary entry, position mk)
+    const float* mk_U = nullptr;   // [B*gamma, ldo] base logits
+    float* mk_logits = nullptr;    // [B*gamma, ldo] or nullptr
+    float* mk_part_v = nullptr;    // [B, ceil(N/32)] best value of each 32-column chunk
+    int* mk_part_i = nullptr;      // [B, ceil(N/32)] its index
+    int mk_k = 0;
 };
 
 // Generic tiled SIMT GEMM (fp32 FMA), any M, N, K.  A rows may be gathered:
@@ -129,6 +136,14 @@ cudaError_t markov_step(const MarkovParams& p, cudaStream_t st);
 // bar_count/bar_gen: zeroed words, left reusable).  markov_chain_max_ctas is the
 // largest co-resident grid.
 int markov_chain_max_ctas(int w_dtype);
+// Many-sequence form: per position k, gather E[b] = w1[prev_b] (bf16, [B, r]),
+// a tensor-core GEMM with the EPI_MARKOV epilogue, then markov_finish reduces
+// the chunk partials of every sequence to its token and confidence.
+cudaError_t markov_gather(const void* w1, int r, int V, const int* anchors, const int* tokens, int gamma, int k, int B,
+                          void* E, cudaStream_t st);
+cudaError_t markov_finish(const float* part_v, const int* part_i, int nchunks, const void* w1, int w_dtype,
+                          const float* y, const float* conf_w, const int* anchors, int* tokens, float* conf, int B,
+                          int gamma, int k, int d, int r, int V, int* err, cudaStream_t st);
 cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st);
 
 // ------------------------------------------------------------------ bookkeeping kernels

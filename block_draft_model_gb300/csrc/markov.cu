@@ -352,7 +352,90 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
     }
 }
 
+// E[b][:] = w1[prev_b] for the many-sequence form (prev_b = anchor at k = 0, else token k-1).
+template <typename TW>
+__global__ void k_markov_gather(const TW* __restrict__ w1, int r, int V, const int* __restrict__ anchors,
+                                const int* __restrict__ tokens, int gamma, int k, TW* __restrict__ E) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x;
+    int prev = k == 0 ? anchors[b] : tokens[b * gamma + k - 1];
+    prev = min(max(prev, 0), V - 1);
+    for (int c = threadIdx.x; c < r; c += blockDim.x) E[(int64_t)b * r + c] = w1[(int64_t)prev * r + c];
+}
+
+// Per sequence: the best of the 32-column chunk partials, then token and confidence.
+template <typename TW>
+__global__ void __launch_bounds__(NT) k_markov_finish(const float* __restrict__ part_v, const int* __restrict__ part_i,
+                                                      int nchunks, const TW* __restrict__ w1,
+                                                      const float* __restrict__ y, const float* __restrict__ conf_w,
+                                                      const int* __restrict__ anchors, int* tokens, float* conf,
+                                                      int gamma, int k, int d, int r, int V, int* err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red_v[NT / 32];
+    __shared__ int red_i[NT / 32];
+    __shared__ float redf[32];
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ArgBest best{-INFINITY, INT_MAX};
+    for (int c = threadIdx.x; c < nchunks; c += NT) {
+        const float v = part_v[(int64_t)b * nchunks + c];
+        const int i = part_i[(int64_t)b * nchunks + c];
+        if (better(v, i, best.v, best.i)) {
+            best.v = v;
+            best.i = i;
+        }
+    }
+    best = warp_argbest(best);
+    if (lane == 0) {
+        red_v[warp] = best.v;
+        red_i[warp] = best.i;
+    }
+    int prev = k == 0 ? anchors[b] : tokens[b * gamma + k - 1];
+    prev = min(max(prev, 0), V - 1);
+    const float* yr = y + (int64_t)(b * gamma + k) * d;
+    float z = 0.f;
+    for (int c = threadIdx.x; c < d; c += NT) z = fmaf(yr[c], conf_w[c], z);
+    for (int c = threadIdx.x; c < r; c += NT) z = fmaf(to_f32(w1[(int64_t)prev * r + c]), conf_w[d + c], z);
+    z = block_sum(z, redf);
+    if (threadIdx.x == 0) {
+        ArgBest tb{-INFINITY, INT_MAX};
+        for (int w = 0; w < NT / 32; ++w)
+            if (better(red_v[w], red_i[w], tb.v, tb.i)) {
+                tb.v = red_v[w];
+                tb.i = red_i[w];
+            }
+        int tok = tb.i;
+        if (tok == INT_MAX || !(tb.v > -INFINITY)) {
+            atomicOr(err, 8);
+            tok = 0;
+        }
+        tokens[b * gamma + k] = tok;
+        conf[b * gamma + k] = 1.f / (1.f + expf(-(z + conf_w[d + r])));
+    }
+}
+
 }  // namespace
+
+cudaError_t markov_gather(const void* w1, int r, int V, const int* anchors, const int* tokens, int gamma, int k, int B,
+                          void* E, cudaStream_t st) {
+    launch(k_markov_gather<bf16>, B, 128, 0, st, (const bf16*)w1, r, V, anchors, tokens, gamma, k, (bf16*)E);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t markov_finish(const float* part_v, const int* part_i, int nchunks, const void* w1, int w_dtype,
+                          const float* y, const float* conf_w, const int* anchors, int* tokens, float* conf, int B,
+                          int gamma, int k, int d, int r, int V, int* err, cudaStream_t st) {
+    if (w_dtype == DT_BF16)
+        launch(k_markov_finish<bf16>, B, NT, 0, st, part_v, part_i, nchunks, (const bf16*)w1, y, conf_w, anchors,
+               tokens, conf, gamma, k, d, r, V, err);
+    else
+        launch(k_markov_finish<float>, B, NT, 0, st, part_v, part_i, nchunks, (const float*)w1, y, conf_w, anchors,
+               tokens, conf, gamma, k, d, r, V, err);
+    note_launch();
+    return cudaGetLastError();
+}
 
 int markov_ctas(int V) {
     int c = (V + 127) / 128;  // 128 vocabulary rows per CTA
