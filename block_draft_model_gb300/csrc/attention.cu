@@ -318,13 +318,17 @@ cudaError_t set_attr() {
 }  // namespace
 
 size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim) {
-    return (size_t)B * n_heads * n_chunks * gamma * (head_dim + 2);
+    // partial rows of head_dim + 2 floats (SIMT kernel) or head_dim + 4 (tensor-core kernel)
+    return (size_t)B * n_heads * n_chunks * gamma * (head_dim + 4);
 }
 
-int attn_max_chunks() { return CMAX; }
+int attn_max_chunks(int cache_dtype, int head_dim, int gamma) {
+    return attention_tc_ok(cache_dtype, head_dim, gamma) ? attention_tc_max_chunks() : CMAX;
+}
 
 cudaError_t attention_init() {
     cudaError_t e;
+    if ((e = attention_tc_init()) != cudaSuccess) return e;
     if ((e = set_attr<bf16, bf16>()) != cudaSuccess) return e;
     if ((e = set_attr<bf16, float>()) != cudaSuccess) return e;
     if ((e = set_attr<float, bf16>()) != cudaSuccess) return e;
@@ -333,6 +337,7 @@ cudaError_t attention_init() {
 
 cudaError_t attention(const AttnParams& p, cudaStream_t st) {
     const int hd = p.d / p.n_heads;
+    if (attention_tc_ok(p.cache_dtype, hd, p.gamma)) return attention_tc(p, st);
     if (p.gamma > GMAX || hd > HMAX || hd % 8 != 0 || p.n_chunks < 1 || p.n_chunks > CMAX || NT % (hd / 8) != 0 ||
         p.gamma > NT / (hd / 8))
         return cudaErrorInvalidValue;

@@ -1,0 +1,450 @@
+// Block attention of a draft layer on the tensor cores, for a bf16 K/V cache
+// ("module-dflash.ts", #layer: the gamma block queries attend bidirectionally
+// over [context ++ block], scale head_dim^-1/2, no mask; the block's own K/V
+// rows sit in the cache right after the context, so every key is a cache row).
+//
+// Same split-K flash-decoding structure as the SIMT kernel ("attention" and
+// "combine" passes of "src/dspark-runtime.js", propose): the keys of one
+// (sequence, head) are cut into ranges, one CTA each, and the last CTA of the
+// (sequence, head), found with a ticket counter, merges the ranges in a fixed
+// order.  Ranges are whole 64-key tiles, sized on the device from the actual
+// length; CTAs past the last range exit at once.
+//
+// Inside a CTA (4 warps) the keys stream through a 3-stage cp.async ring of
+// 64-key K and V tiles (rows padded by 16 bytes, so ldmatrix is conflict-free).
+// Each warp owns 16 keys of every tile and keeps its own running softmax state:
+//   S   = Q K^T  mma.m16n8k16 bf16, the (<= 16) queries as the M dimension,
+//                Q (pre-scaled by head_dim^-1/2 log2 e, rounded to bf16) held in
+//                registers as A fragments, K fragments from ldmatrix;
+//   P   = 2^(S - m)   in registers; the S accumulator layout is the A fragment
+//                layout of the next product, P rounded to bf16;
+//   O  += P V    mma.m16n8k16, V fragments from ldmatrix.trans.
+// The row sums add the bf16-rounded P, so every range's output is a convex
+// combination of V rows.  At the end the four warps merge through shared
+// memory into the range's (m, l, o) partial (log2 domain, rows of head_dim + 4
+// floats so that the last CTA can stage them with 16-byte cp.async copies).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int TK = 64;      // keys per tile
+constexpr int NW = 4;       // warps per CTA, 16 keys of each tile per warp
+constexpr int NT = NW * 32;
+constexpr int NSTAGE = 3;   // cp.async ring depth
+constexpr int GMAX = 16;    // queries per block (the M of the MMA)
+constexpr int CMAX = 128;   // largest number of key ranges per (sequence, head)
+
+template <int HD>
+struct TLayout {
+    static constexpr int RB = HD * 2 + 16;  // padded bytes of one K or V row
+    static constexpr int TILE = TK * RB;
+    static constexpr int STAGE = 2 * TILE;  // K tile, then V tile
+    static constexpr int BYTES = NSTAGE * STAGE;
+    // after the key loop the ring is reused:
+    //   this CTA's four warps: their outputs and (m, l)
+    static constexpr int OWS = HD + 8;                      // padded row of a warp's output, floats
+    static constexpr int OW = 0;                            // [NW][GMAX][OWS] fp32
+    static constexpr int ML = OW + NW * GMAX * OWS * 4;     // [NW][GMAX] m, then [NW][GMAX] l
+    static_assert(ML + 2 * NW * GMAX * 4 <= BYTES, "warp merge buffers must fit in the tile ring");
+    //   the last CTA's merge of the ranges: weights, l, then partials staged piece by piece
+    static constexpr int PW = HD + 4;                       // partial row: m, l, 2 unused, o[HD] (16-byte rows)
+    static constexpr int WM = 0;                            // [GMAX][CMAX] m, then the range weights
+    static constexpr int LM = WM + GMAX * CMAX * 4;         // [GMAX][CMAX] l
+    static constexpr int STG = LM + GMAX * CMAX * 4;        // staged partials
+    static_assert(STG + GMAX * PW * 4 <= BYTES, "one range of partials must fit beside the weights");
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+// c[16x8] += a[16x16] . b[16x8], bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 2^x (hardware approximation; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// (lo, hi) -> bf16x2 with lo in the low half; the rounded values are returned through lo/hi
+__device__ __forceinline__ uint32_t pack_round(float& lo, float& hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    lo = __low2float(v);
+    hi = __high2float(v);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename TO>
+__device__ __forceinline__ void store4(TO* dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* dst, float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// Copies of keys [t0, t0 + TK) into one ring stage; keys at or past `end` are zero-filled.
+template <int HD>
+__device__ __forceinline__ void load_kv(uint32_t dst, const bf16* Kb, const bf16* Vb, int64_t stride, int t0,
+                                        int end) {
+    using L = TLayout<HD>;
+    constexpr int VPR = HD * 2 / 16;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < TK * VPR; i += NT) {
+        const int r = i / VPR, v = i - r * VPR;
+        const int key = t0 + r;
+        const bool ok = key < end;
+        const int64_t off = (int64_t)(ok ? key : t0) * stride + v * 8;
+        const uint32_t so = r * L::RB + v * 16;
+        cp_async16(dst + so, Kb + off, ok ? 16 : 0);
+        cp_async16(dst + L::TILE + so, Vb + off, ok ? 16 : 0);
+    }
+}
+
+template <int HD, typename TO>
+__global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
+    using L = TLayout<HD>;
+    constexpr int KS = HD / 16;  // 16-wide k steps of Q K^T; pairs of 8-wide output tiles of P V
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ int is_last;
+
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gamma = p.gamma, d = p.d;
+    const int slot = p.seq_ids ? p.seq_ids[b] : b;
+    const int n_keys = slot < 0 ? 0 : p.seq_len[slot] + gamma;  // a rejected sequence has no keys
+    TO* out = reinterpret_cast<TO*>(p.out) + (int64_t)b * gamma * d + h * HD;
+    if (n_keys == 0) {
+        if (c == 0)
+            for (int i = tid; i < gamma * (HD / 4); i += NT)
+                store4<TO>(out + (int64_t)(i / (HD / 4)) * d + (i % (HD / 4)) * 4, 0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int per = (n_keys + p.n_chunks - 1) / p.n_chunks;
+    const int chunk = (per + TK - 1) / TK * TK;
+    const int n_real = (n_keys + chunk - 1) / chunk;
+    if (c >= n_real) return;
+    const int start = c * chunk, end = min(n_keys, start + chunk);
+    const int n_tiles = (end - start + TK - 1) / TK;
+
+    const bf16* Kb = reinterpret_cast<const bf16*>(p.cache) + (int64_t)slot * p.seq_stride + h * HD;
+    const bf16* Vb = Kb + p.kv_off;
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(sm);
+#pragma unroll
+    for (int s = 0; s < NSTAGE - 1; ++s) {
+        if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, d, start + s * TK, end);
+        cp_async_commit();
+    }
+
+    // Q as A fragments: rows g and g+8, columns (lane % 4) * 2 (+8) of every 16-wide k step
+    const int g = lane >> 2, cq = (lane & 3) * 2;
+    uint32_t qf[KS][4];
+    {
+        const float qs = rsqrtf((float)HD) * 1.4426950408889634f;
+        const float* q0 = p.q + (int64_t)(b * gamma + g) * d + h * HD;
+        const float* q1 = q0 + (int64_t)8 * d;
+        const bool v0 = g < gamma, v1 = g + 8 < gamma;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int col = ks * 16 + cq;
+            float2 a = v0 ? *reinterpret_cast<const float2*>(q0 + col) : make_float2(0.f, 0.f);
+            float2 bq = v1 ? *reinterpret_cast<const float2*>(q1 + col) : make_float2(0.f, 0.f);
+            float2 cc = v0 ? *reinterpret_cast<const float2*>(q0 + col + 8) : make_float2(0.f, 0.f);
+            float2 dd = v1 ? *reinterpret_cast<const float2*>(q1 + col + 8) : make_float2(0.f, 0.f);
+            float x0 = a.x * qs, x1 = a.y * qs, y0 = bq.x * qs, y1 = bq.y * qs;
+            float z0 = cc.x * qs, z1 = cc.y * qs, w0 = dd.x * qs, w1 = dd.y * qs;
+            qf[ks][0] = pack_round(x0, x1);
+            qf[ks][1] = pack_round(y0, y1);
+            qf[ks][2] = pack_round(z0, z1);
+            qf[ks][3] = pack_round(w0, w1);
+        }
+    }
+
+    float o[2 * KS][4];
+#pragma unroll
+    for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g, g+8 (l: this thread's columns)
+
+    // ldmatrix row addresses: lane -> matrix lane/8, row lane%8
+    const int lr = lane & 7, lm = lane >> 3, kw = warp * 16;
+    const uint32_t k_lane = (uint32_t)((kw + (lm >> 1) * 8 + lr) * L::RB + (lm & 1) * 16);
+    const uint32_t v_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * L::RB + (lm >> 1) * 16);
+
+    for (int t = 0; t < n_tiles; ++t) {
+        cp_async_wait<NSTAGE - 2>();
+        __syncthreads();  // tile t is visible; every warp is done with tile t-1, whose stage is refilled next
+        {
+            const int tn = t + NSTAGE - 1;
+            if (tn < n_tiles) load_kv<HD>(ring + (tn % NSTAGE) * L::STAGE, Kb, Vb, d, start + tn * TK, end);
+            cp_async_commit();
+        }
+        const int nk = min(TK, end - (start + t * TK));
+        if (kw >= nk) continue;
+        const uint32_t kbase = ring + (t % NSTAGE) * L::STAGE;
+        const uint32_t vbase = kbase + L::TILE;
+
+        float s[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + k_lane + ks * 32, b0, b1, b2, b3);
+            mma16816(s[0], qf[ks], b0, b1);
+            mma16816(s[1], qf[ks], b2, b3);
+        }
+        if (kw + 16 > nk) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (kw + n * 8 + cq + e >= nk) s[n][e] = s[n][2 + e] = -INFINITY;
+        }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = ex2(m0 - ms0), a1 = ex2(m1 - ms1);
+        m0 = mn0;
+        m1 = mn1;
+        float p00 = ex2(s[0][0] - ms0), p01 = ex2(s[0][1] - ms0), p02 = ex2(s[0][2] - ms1), p03 = ex2(s[0][3] - ms1);
+        float p10 = ex2(s[1][0] - ms0), p11 = ex2(s[1][1] - ms0), p12 = ex2(s[1][2] - ms1), p13 = ex2(s[1][3] - ms1);
+        uint32_t pf[4];
+        pf[0] = pack_round(p00, p01);  // row g,   keys cq, cq+1
+        pf[1] = pack_round(p02, p03);  // row g+8, keys cq, cq+1
+        pf[2] = pack_round(p10, p11);  // row g,   keys 8+cq, 9+cq
+        pf[3] = pack_round(p12, p13);  // row g+8, keys 8+cq, 9+cq
+        l0 = l0 * a0 + ((p00 + p01) + (p10 + p11));
+        l1 = l1 * a1 + ((p02 + p03) + (p12 + p13));
+#pragma unroll
+        for (int n = 0; n < 2 * KS; ++n) {
+            o[n][0] *= a0;
+            o[n][1] *= a0;
+            o[n][2] *= a1;
+            o[n][3] *= a1;
+        }
+#pragma unroll
+        for (int n2 = 0; n2 < KS; ++n2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vbase + v_lane + n2 * 32, b0, b1, b2, b3);
+            mma16816(o[2 * n2], pf, b0, b1);
+            mma16816(o[2 * n2 + 1], pf, b2, b3);
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is free for the merge buffers
+
+    // ---- merge the four warps into this range's partial
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    float* Ow = reinterpret_cast<float*>(sm + L::OW);
+    float* Mw = reinterpret_cast<float*>(sm + L::ML);
+    float* Lw = Mw + NW * GMAX;
+#pragma unroll
+    for (int n = 0; n < 2 * KS; ++n) {
+        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g) * L::OWS + n * 8 + cq) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g + 8) * L::OWS + n * 8 + cq) = make_float2(o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+        Mw[warp * GMAX + g] = m0;
+        Mw[warp * GMAX + g + 8] = m1;
+        Lw[warp * GMAX + g] = l0;
+        Lw[warp * GMAX + g + 8] = l1;
+    }
+    __syncthreads();
+
+    constexpr int w = L::PW;
+    const int64_t bh = (int64_t)b * p.n_heads + h;
+    float* part = p.part + (bh * p.n_chunks + c) * gamma * w;
+    for (int i = tid; i < gamma * (HD / 4); i += NT) {
+        const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < NW; ++v) M = fmaxf(M, Mw[v * GMAX + j]);
+        float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int v = 0; v < NW; ++v) {
+            const float mv = Mw[v * GMAX + j];
+            const float wt = mv == -INFINITY ? 0.f : ex2(mv - M);
+            l += wt * Lw[v * GMAX + j];
+            const float4 ov = *reinterpret_cast<const float4*>(Ow + (v * GMAX + j) * L::OWS + e);
+            acc[0] += wt * ov.x;
+            acc[1] += wt * ov.y;
+            acc[2] += wt * ov.z;
+            acc[3] += wt * ov.w;
+        }
+        if (n_real == 1) {
+            const float inv = 1.f / l;  // the range holds at least one key, so l >= 1
+            store4<TO>(out + (int64_t)j * d + e, acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        } else {
+            *reinterpret_cast<float4*>(part + j * w + 4 + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (e == 0) *reinterpret_cast<float2*>(part + j * w) = make_float2(M, l);
+        }
+    }
+    if (n_real == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = (atomicAdd(&p.tickets[bh], 1u) == (unsigned int)n_real - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // ---- last CTA of (b, h): merge the n_real ranges in order.  The (m, l) of
+    // every (range, query) come in one parallel pass; the partial outputs are
+    // staged into shared memory with cp.async, as many ranges at a time as fit.
+    const float* all = p.part + bh * p.n_chunks * gamma * w;  // range cc, query j at (cc * gamma + j) * w
+    float* Wm = reinterpret_cast<float*>(sm + L::WM);
+    float* Lm = reinterpret_cast<float*>(sm + L::LM);
+    const int npairs = gamma * n_real;
+#pragma unroll 4
+    for (int q = tid; q < npairs; q += NT) {
+        const int cc = q / gamma, j = q - cc * gamma;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(all + (int64_t)q * w));
+        Wm[j * CMAX + cc] = ml.x;
+        Lm[j * CMAX + cc] = ml.y;
+    }
+    __syncthreads();
+    for (int j = warp; j < gamma; j += NW) {
+        float* wj = Wm + j * CMAX;
+        float M = -INFINITY;
+        for (int cc = lane; cc < n_real; cc += 32) M = fmaxf(M, wj[cc]);
+        M = warp_max(M);
+        float lsum = 0.f;
+        for (int cc = lane; cc < n_real; cc += 32) {
+            const float m = wj[cc];
+            const float wt = m == -INFINITY ? 0.f : ex2(m - M);
+            wj[cc] = wt;
+            lsum += wt * Lm[j * CMAX + cc];
+        }
+        lsum = warp_sum(lsum);
+        const float inv = 1.f / lsum;
+        for (int cc = lane; cc < n_real; cc += 32) wj[cc] *= inv;
+    }
+    constexpr int ITEMS = (GMAX * (HD / 4) + NT - 1) / NT;  // (query, 4 columns) items per thread
+    float acc[ITEMS][4];
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
+    const int rbytes = gamma * w * 4;
+    const int fit = (L::BYTES - L::STG) / rbytes;
+    const uint32_t stg = ring + L::STG;
+    const float* S = reinterpret_cast<const float*>(sm + L::STG);
+    for (int c0 = 0; c0 < n_real; c0 += fit) {
+        const int nr = min(fit, n_real - c0);
+        __syncthreads();  // weights are final; the previous piece has been consumed
+        const char* src = reinterpret_cast<const char*>(all + (int64_t)c0 * gamma * w);
+        for (int i = tid; i < nr * rbytes / 16; i += NT) cp_async16(stg + i * 16, src + i * 16, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const int i = tid + k * NT;
+            if (i < gamma * (HD / 4)) {
+                const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+                const float* wj = Wm + j * CMAX + c0;
+                for (int cc = 0; cc < nr; ++cc) {
+                    const float wt = wj[cc];
+                    const float4 x = *reinterpret_cast<const float4*>(S + (cc * gamma + j) * w + 4 + e);
+                    acc[k][0] = fmaf(wt, x.x, acc[k][0]);
+                    acc[k][1] = fmaf(wt, x.y, acc[k][1]);
+                    acc[k][2] = fmaf(wt, x.z, acc[k][2]);
+                    acc[k][3] = fmaf(wt, x.w, acc[k][3]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+        const int i = tid + k * NT;
+        if (i < gamma * (HD / 4)) {
+            const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+            store4<TO>(out + (int64_t)j * d + e, acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+        }
+    }
+    if (tid == 0) p.tickets[bh] = 0u;
+}
+
+template <int HD, typename TO>
+cudaError_t set_attr_tc() {
+    return cudaFuncSetAttribute(k_attention_tc<HD, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TLayout<HD>::BYTES);
+}
+
+}  // namespace
+
+bool attention_tc_ok(int cache_dtype, int head_dim, int gamma) {
+    return cache_dtype == DT_BF16 && (head_dim == 64 || head_dim == 128) && gamma >= 1 && gamma <= GMAX;
+}
+
+int attention_tc_max_chunks() { return CMAX; }
+
+cudaError_t attention_tc_init() {
+    cudaError_t e;
+    if ((e = set_attr_tc<64, bf16>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<64, float>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<128, bf16>()) != cudaSuccess) return e;
+    return set_attr_tc<128, float>();
+}
+
+cudaError_t attention_tc(const AttnParams& p, cudaStream_t st) {
+    const int hd = p.d / p.n_heads;
+    if (!attention_tc_ok(p.cache_dtype, hd, p.gamma) || p.n_chunks < 1 || p.n_chunks > CMAX ||
+        (p.out_dtype != DT_BF16 && p.out_dtype != DT_F32))
+        return cudaErrorInvalidValue;
+    dim3 grid(p.n_chunks, p.n_heads, p.B);
+    const bool o16 = p.out_dtype == DT_BF16;
+    if (hd == 64) {
+        const size_t sm = TLayout<64>::BYTES;
+        if (o16) launch(k_attention_tc<64, bf16>, grid, NT, sm, st, p);
+        else launch(k_attention_tc<64, float>, grid, NT, sm, st, p);
+    } else {
+        const size_t sm = TLayout<128>::BYTES;
+        if (o16) launch(k_attention_tc<128, bf16>, grid, NT, sm, st, p);
+        else launch(k_attention_tc<128, float>, grid, NT, sm, st, p);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

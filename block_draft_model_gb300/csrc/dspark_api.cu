@@ -108,7 +108,7 @@ struct dspark_handle {
     unsigned int* mk_cnt = nullptr;
     int mk_ctas = 1;
     int mk_chain_max = 0;                    // largest co-resident grid of the one-launch Markov chain
-    TcWeight tc_w2;                          // w2 [V, r] for the many-sequence Markov GEMM
+    TcWeight tc_mk_E;                        // mk_E as the N operand of the many-sequence Markov GEMM
     TcWeight tc_tok_proj;                    // tok_proj [d, H] for the many-sequence block build
     void* emb_rows = nullptr;                // [max_seqs, H] gathered anchor embeddings (bf16)
     void* mk_E = nullptr;                    // [max_seqs, r] gathered w1 rows (bf16)
@@ -178,11 +178,15 @@ cudaError_t grow(DevBuf& b, size_t bytes) {
 }
 
 int attn_chunks(const dspark_handle* h, int B, int max_keys) {
-    // enough CTAs for two per SM, but at least 64 keys (one tile) per range
+    // Few (sequence, head) pairs: one wave of two CTAs per SM, so that each range
+    // is long and the last CTA merges few partials.  Many pairs: about a dozen
+    // CTAs per SM over the launch, so that sequences of unequal length balance.
+    // At least 64 keys (one tile) per range either way.
     const int nh = h->cfg.n_heads;
-    int want = (2 * h->num_sms + nh * B - 1) / (nh * B);
+    const int pairs = nh * B;
+    int want = pairs < 2 * h->num_sms ? (2 * h->num_sms + pairs - 1) / pairs : (12 * h->num_sms + pairs - 1) / pairs;
     int by_keys = (max_keys + 63) / 64;
-    return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks()));
+    return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks(h->dt, h->hd, h->cfg.gamma)));
 }
 
 // A weight and its tensor-core views.
@@ -493,21 +497,23 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.err = h->d_err;
     mp.ctas = h->mk_ctas;
     Prof pr(h, CAT_MARKOV, st);
-    if (B >= 8 && h->tc_w2.ready && h->mk_E && tc_gemm_ok(B, V, c.markov_rank) && anchors_dev) {
-        // many sequences: per position a [B, r] x [V, r]^T tensor-core GEMM reads w2 once for all of them
+    if (B >= 8 && h->tc_mk_E.ready && tc_gemm_ok(V, B, c.markov_rank) && anchors_dev) {
+        // many sequences: per position a [V, r] x [B, r]^T tensor-core GEMM reads w2 once for all of
+        // them; vocabulary entries are the rows, so the base logits are read along their rows
         const int nch = (V + 31) / 32;
         for (int k = 0; k < c.gamma; ++k) {
             CUDA_TRY(h, markov_gather(h->w1, c.markov_rank, V, anchors_dev, tokens, c.gamma, k, B, h->mk_E, st));
             EpiParams ep;
-            ep.kind = EPI_MARKOV;
+            ep.kind = EPI_MARKOV_T;
             ep.ldo = V;
+            ep.mk_nch = nch;
             ep.gamma = c.gamma;
             ep.mk_U = h->U;
             ep.mk_logits = logits;
             ep.mk_part_v = h->mk_pv;
             ep.mk_part_i = h->mk_pi;
             ep.mk_k = k;
-            CUDA_TRY(h, tc_gemm(h->mk_E, c.markov_rank, h->tc_w2, B, V, c.markov_rank, ep, h->num_sms, h->d_err, st));
+            CUDA_TRY(h, tc_gemm(h->w2, c.markov_rank, h->tc_mk_E, V, B, c.markov_rank, ep, h->num_sms, h->d_err, st));
             CUDA_TRY(h, markov_finish(h->mk_pv, h->mk_pi, nch, h->w1, h->dt, h->y, h->conf_wb, anchors_dev, tokens, conf,
                                       B, c.gamma, k, d, c.markov_rank, V, h->d_err, st));
         }
@@ -749,7 +755,7 @@ void dspark_destroy(dspark_handle* h) {
     for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
     tc_release(h->tc_wc);
     tc_release(h->tc_out_proj);
-    tc_release(h->tc_w2);
+    tc_release(h->tc_mk_E);
     tc_release(h->tc_tok_proj);
     for (auto* v : {&h->tc_kv, &h->tc_qkv, &h->tc_wo, &h->tc_wgu, &h->tc_wd})
         for (auto& w : *v) tc_release(w);
@@ -876,7 +882,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, &h->h_lp, (size_t)R * F * 2));
     {
         size_t worst = 0;
-        for (int B : {1, cfg->max_seqs}) {
+        for (int B = 1; B <= cfg->max_seqs; ++B) {
             int ch = attn_chunks(h, B, cfg->max_ctx + cfg->gamma);
             worst = std::max(worst, attn_scratch_floats(B, cfg->n_heads, ch, cfg->gamma, h->hd));
         }
@@ -925,10 +931,10 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         }
     }
     if (h->dt == DT_BF16 && tc_available() && cfg->max_seqs >= 8) {
-        CTRY(tc_prepare(h->tc_w2, h->w2, V, r));
         CTRY(tc_prepare(h->tc_tok_proj, h->tok_proj, d, H));
         CTRY(dalloc(h, &h->emb_rows, (size_t)cfg->max_seqs * H * 2));
         CTRY(dalloc(h, &h->mk_E, (size_t)cfg->max_seqs * r * 2));
+        CTRY(tc_prepare(h->tc_mk_E, h->mk_E, cfg->max_seqs, r));
         const size_t nch = (size_t)(V + 31) / 32;
         CTRY(dalloc(h, (void**)&h->mk_pv, (size_t)cfg->max_seqs * nch * 4));
         CTRY(dalloc(h, (void**)&h->mk_pi, (size_t)cfg->max_seqs * nch * 4));

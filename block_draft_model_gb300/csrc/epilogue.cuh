@@ -92,27 +92,59 @@ __device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int
     else store_f32x32(reinterpret_cast<float*>(ep.cache) + off, v);
 }
 
+// EPI_MARKOV_T for one warp: lane l holds the accumulators of vocabulary row
+// `vrow` (valid: vrow < V) for sequences nb .. nb+31 (those >= N are absent).
+// Adds the base logits (consecutive lanes read consecutive entries of a U row),
+// stores the logits if asked, then a reduce-scatter over the lanes (5 exchange
+// steps, halving the columns each time) leaves in lane l the best of the
+// warp's 32 rows for sequence nb + l: larger value, then lower index.  Called
+// by all 32 lanes; vrow - lane is the warp's first row, a multiple of 32.
+__device__ __forceinline__ void markov_t32(const EpiParams& ep, int vrow, bool valid, int nb, int N, const float* acc) {
+    const int lane = threadIdx.x & 31;
+    float val[32];
+    int idx[32];
+    // all 32 loads first: a logits store between them would have to wait for
+    // the load before it (the compiler cannot rule out that the buffers overlap)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const bool ok = valid && nb + j < N;
+        const int64_t row = (int64_t)(nb + j) * ep.gamma + ep.mk_k;
+        val[j] = ok ? acc[j] + __ldcs(ep.mk_U + row * ep.ldo + vrow) : -INFINITY;
+        idx[j] = ok ? vrow : INT_MAX;
+    }
+    if (ep.mk_logits) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (valid && nb + j < N) ep.mk_logits[((int64_t)(nb + j) * ep.gamma + ep.mk_k) * ep.ldo + vrow] = val[j];
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;  // keep columns [w, 2w), else [0, w)
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float sv = upper ? val[i] : val[i + w];
+            const int si = upper ? idx[i] : idx[i + w];
+            float kv = upper ? val[i + w] : val[i];
+            int ki = upper ? idx[i + w] : idx[i];
+            const float ov = __shfl_xor_sync(0xffffffffu, sv, w);
+            const int oi = __shfl_xor_sync(0xffffffffu, si, w);
+            if (better(ov, oi, kv, ki)) {
+                kv = ov;
+                ki = oi;
+            }
+            val[i] = kv;
+            idx[i] = ki;
+        }
+    }
+    if (nb + lane < N) {
+        const int64_t o = (int64_t)(nb + lane) * ep.mk_nch + ((vrow - lane) >> 5);
+        ep.mk_part_v[o] = val[0];
+        ep.mk_part_i[o] = idx[0];
+    }
+}
+
 __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v) {
     const bool full = n + 32 <= N;
-    if (ep.kind == EPI_MARKOV) {
-        const int64_t row = (int64_t)m * ep.gamma + ep.mk_k;
-        const float* u = ep.mk_U + row * ep.ldo + n;
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int j = 0; j < 32; ++j) {
-            if (n + j >= N) break;
-            const float l = v[j] + u[j];
-            if (ep.mk_logits) ep.mk_logits[row * ep.ldo + n + j] = l;
-            if (better(l, n + j, bv, bi)) {
-                bv = l;
-                bi = n + j;
-            }
-        }
-        const int nch = (N + 31) / 32;
-        ep.mk_part_v[(int64_t)m * nch + (n >> 5)] = bv;
-        ep.mk_part_i[(int64_t)m * nch + (n >> 5)] = bi;
-        return;
-    }
     switch (ep.kind) {
         case EPI_STORE_F32:
         case EPI_ADD_F32:
@@ -188,10 +220,13 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
         default:
             return;
     }
+    // unrolled so that v stays in registers
     if (ep.kind == EPI_SWIGLU) {
+#pragma unroll
         for (int j = 0; j < 32; j += 2)
             if (n + j + 1 < N) epi_pair(ep, m, n + j, v[j], v[j + 1]);
     } else {
+#pragma unroll
         for (int j = 0; j < 32; ++j)
             if (n + j < N) epi_one(ep, m, n + j, v[j]);
     }

@@ -18,7 +18,8 @@ enum EpiKind {
     EPI_SWIGLU = 2,     // columns come in (gate, up) pairs: out_act[m * ld_act + n/2] = act(gate) * up
     EPI_KV_CACHE = 3,   // columns [0, d) -> K cache, [d, 2d) -> V cache, row -> (seq, position)
     EPI_QKV = 4,        // columns [0, d) -> out_f32 (Q), [d, 2d) -> K cache, [2d, 3d) -> V cache
-    EPI_MARKOV = 5,     // l = acc + U[m*gamma + k][n]; logits (optional); argmax partial per 32 columns
+    EPI_MARKOV_T = 5,   // row m = vocabulary entry, column n = sequence: l = acc + U[n*gamma + k][m];
+                        // logits (optional); argmax partial per sequence and 32 rows (tensor-core GEMM only)
 };
 
 struct EpiParams {
@@ -41,11 +42,12 @@ struct EpiParams {
     const int* seq_len = nullptr;  // device context lengths per slot
     int gamma = 1;                 // EPI_QKV: GEMM row m is block row m % gamma of sequence m / gamma
     const int* seq_ids = nullptr;  // EPI_QKV: slot of sequence b (nullptr: slot b)
-    // EPI_MARKOV (row m = sequence, column n = vocabulary entry, position mk)
+    // EPI_MARKOV_T (row m = vocabulary entry, column n = sequence, block position mk_k)
     const float* mk_U = nullptr;   // [B*gamma, ldo] base logits
     float* mk_logits = nullptr;    // [B*gamma, ldo] or nullptr
-    float* mk_part_v = nullptr;    // [B, ceil(N/32)] best value of each 32-column chunk
-    int* mk_part_i = nullptr;      // [B, ceil(N/32)] its index
+    float* mk_part_v = nullptr;    // [B, mk_nch] best value of each 32-entry vocabulary chunk
+    int* mk_part_i = nullptr;      // [B, mk_nch] its index
+    int mk_nch = 0;                // ceil(V / 32)
     int mk_k = 0;
 };
 
@@ -104,9 +106,15 @@ struct AttnParams {
     int out_dtype;
 };
 size_t attn_scratch_floats(int B, int n_heads, int n_chunks, int gamma, int head_dim);
-int attn_max_chunks();
+int attn_max_chunks(int cache_dtype, int head_dim, int gamma);
 cudaError_t attention_init();  // once per process/device, before any launch or capture
+// bf16 caches with head_dim 64 or 128 run on the tensor cores (mma.sync, key
+// ranges of whole 64-key tiles, empty ranges exit); the rest on the SIMT kernel.
 cudaError_t attention(const AttnParams& p, cudaStream_t st);
+bool attention_tc_ok(int cache_dtype, int head_dim, int gamma);
+int attention_tc_max_chunks();
+cudaError_t attention_tc_init();
+cudaError_t attention_tc(const AttnParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ Markov chain, argmax, confidence
 struct MarkovParams {
@@ -137,8 +145,9 @@ cudaError_t markov_step(const MarkovParams& p, cudaStream_t st);
 // largest co-resident grid.
 int markov_chain_max_ctas(int w_dtype);
 // Many-sequence form: per position k, gather E[b] = w1[prev_b] (bf16, [B, r]),
-// a tensor-core GEMM with the EPI_MARKOV epilogue, then markov_finish reduces
-// the chunk partials of every sequence to its token and confidence.
+// a tensor-core GEMM w2 . E^T ([V, B]) with the EPI_MARKOV_T epilogue, then
+// markov_finish reduces the chunk partials of every sequence to its token and
+// confidence.
 cudaError_t markov_gather(const void* w1, int r, int V, const int* anchors, const int* tokens, int gamma, int k, int B,
                           void* E, cudaStream_t st);
 cudaError_t markov_finish(const float* part_v, const int* part_i, int nchunks, const void* w1, int w_dtype,

@@ -129,13 +129,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();  // lane 0 rejoins its warp before the CTA-wide barrier
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t id = idesc(BM, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
+                int m0, n0;
+                tm.at(t, m0, n0);
+                // a narrow last (or only) column tile multiplies only its 16-aligned width
+                const int n_rem = N - n0;
+                const uint32_t id = idesc(BM, n_rem >= BN ? BN : (n_rem + 15) & ~15);
                 const uint32_t d_tmem = tmem + buf * BN;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -182,10 +186,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
+                const int nb = n0 + c * 32;
+                if (nb >= N) break;  // columns past N were not multiplied
                 uint32_t r[32];
                 tmem_ld32(base + c * 32, r);
-                const int nb = n0 + c * 32;
-                if (row < M && nb < N) {
+                if (ep.kind == EPI_MARKOV_T) {  // warp-wide: every lane takes part
+                    if (m0 + q * 32 < M) {
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        markov_t32(ep, row, row < M, nb, N, v);
+                    }
+                } else if (row < M) {
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);

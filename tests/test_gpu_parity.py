@@ -173,6 +173,45 @@ def test_batched_equals_per_sequence():
             assert np.max(np.abs(tensor_to_f64(gv) - V)) <= 2e-2 * np.max(np.abs(V))
 
 
+def test_batched_many_sequences_ragged_vocab():
+    """Eleven sequences (the many-sequence paths: gathered anchor embeddings and
+    the Markov bias as one GEMM per position over all sequences), ragged
+    context lengths including 0 and tile edges, V 1000 (not a multiple of the
+    32-entry argmax chunks or the 128-row GEMM tiles), r 64, head_dim 64."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=128, n_heads=2, n_layers=2, ff_mult=2, gamma=4,
+                            vocab=1000, markov_rank=64)
+    W = syn.make_weights(cfg, seed=11, norm_std=0.1)
+    lens = [0, 1, 5, 63, 64, 65, 130, 7, 200, 33, 90]
+    n = len(lens)
+    feats = [syn.make_feats(cfg, L, seed=11, seq=i) for i, L in enumerate(lens)]
+    gb = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=208, max_seqs=12)
+    ids = torch.arange(n, dtype=torch.int32, device="cuda")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    gb.ingest_context_batched(ids, cu, to_torch(np.concatenate(feats, axis=0)))
+    anchors = torch.tensor([0, 999, 31, 32, 500, 998, 1, 640, 2, 333, 768], dtype=torch.int32, device="cuda")
+    tok = torch.empty(n, cfg.gamma, dtype=torch.int32, device="cuda")
+    conf = torch.empty(n, cfg.gamma, dtype=torch.float32, device="cuda")
+    lg = torch.empty(n, cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda")
+    gb.draft_batched(ids, anchors, tok, conf, lg)
+    torch.cuda.synchronize()
+    assert gb.check() == 0
+    dr = oracle.Drafter(cfg, W)
+    for i, L in enumerate(lens):
+        if L:
+            dr.ingest(feats[i], seq=i)
+    for i in range(n):
+        check_block(dr, i, int(anchors[i]), tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
+                    label=f"seq {i} (L {lens[i]})")
+
+
+def test_bf16_attention_many_key_ranges():
+    """head_dim 128, 1500 context rows: the keys of each head are split over
+    many CTAs (64-key tiles, a ragged last tile) and merged by the last one."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=7,
+                            vocab=1000, markov_rank=64)
+    _small(cfg, 1500, seed=12, chunks=[700], anchors=[4, 998], max_ctx=1600)
+
+
 def test_host_checked_errors():
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=2,
