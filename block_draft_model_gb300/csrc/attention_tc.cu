@@ -35,28 +35,30 @@ namespace {
 constexpr int TK = 64;      // keys per tile
 constexpr int NW = 4;       // warps per CTA, 16 keys of each tile per warp
 constexpr int NT = NW * 32;
-constexpr int NSTAGE = 3;   // cp.async ring depth
 constexpr int GMAX = 16;    // queries per block (the M of the MMA)
 constexpr int CMAX = 128;   // largest number of key ranges per (sequence, head)
+static_assert(NT == GMAX * 8, "the merge gives each query eight threads");
 
-template <int HD>
+// NS: cp.async ring depth; 3 when two CTAs share an SM, 6 when one CTA has it alone
+template <int HD, int NS>
 struct TLayout {
     static constexpr int RB = HD * 2 + 16;  // padded bytes of one K or V row
     static constexpr int TILE = TK * RB;
     static constexpr int STAGE = 2 * TILE;  // K tile, then V tile
-    static constexpr int BYTES = NSTAGE * STAGE;
+    static constexpr int BYTES = NS * STAGE;
     // after the key loop the ring is reused:
     //   this CTA's four warps: their outputs and (m, l)
     static constexpr int OWS = HD + 8;                      // padded row of a warp's output, floats
     static constexpr int OW = 0;                            // [NW][GMAX][OWS] fp32
     static constexpr int ML = OW + NW * GMAX * OWS * 4;     // [NW][GMAX] m, then [NW][GMAX] l
     static_assert(ML + 2 * NW * GMAX * 4 <= BYTES, "warp merge buffers must fit in the tile ring");
-    //   the last CTA's merge of the ranges: weights, l, then partials staged piece by piece
+    //   the last CTA's merge of the ranges, staged piece by piece: per query the
+    //   piece's range weights, the running (max, sum, rescale), then the partials
     static constexpr int PW = HD + 4;                       // partial row: m, l, 2 unused, o[HD] (16-byte rows)
-    static constexpr int WM = 0;                            // [GMAX][CMAX] m, then the range weights
-    static constexpr int LM = WM + GMAX * CMAX * 4;         // [GMAX][CMAX] l
-    static constexpr int STG = LM + GMAX * CMAX * 4;        // staged partials
-    static_assert(STG + GMAX * PW * 4 <= BYTES, "one range of partials must fit beside the weights");
+    static constexpr int WM = 0;                            // [GMAX][CMAX] range weights of the piece
+    static constexpr int MJ = WM + GMAX * CMAX * 4;         // [GMAX] running max, [GMAX] sum, [GMAX] rescale
+    static constexpr int STG = MJ + 4 * GMAX * 4;           // staged partials (16-byte aligned)
+    static_assert(STG + GMAX * PW * 4 <= BYTES, "one range of partials must fit beside the merge state");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
@@ -120,7 +122,7 @@ __device__ __forceinline__ void store4<bf16>(bf16* dst, float a, float b, float 
 template <int HD>
 __device__ __forceinline__ void load_kv(uint32_t dst, const bf16* Kb, const bf16* Vb, int64_t stride, int t0,
                                         int end) {
-    using L = TLayout<HD>;
+    constexpr int RB = HD * 2 + 16, TILE = TK * RB;  // as in TLayout
     constexpr int VPR = HD * 2 / 16;
 #pragma unroll 4
     for (int i = threadIdx.x; i < TK * VPR; i += NT) {
@@ -128,15 +130,15 @@ __device__ __forceinline__ void load_kv(uint32_t dst, const bf16* Kb, const bf16
         const int key = t0 + r;
         const bool ok = key < end;
         const int64_t off = (int64_t)(ok ? key : t0) * stride + v * 8;
-        const uint32_t so = r * L::RB + v * 16;
+        const uint32_t so = r * RB + v * 16;
         cp_async16(dst + so, Kb + off, ok ? 16 : 0);
-        cp_async16(dst + L::TILE + so, Vb + off, ok ? 16 : 0);
+        cp_async16(dst + TILE + so, Vb + off, ok ? 16 : 0);
     }
 }
 
-template <int HD, typename TO>
+template <int HD, typename TO, int NS>
 __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
-    using L = TLayout<HD>;
+    using L = TLayout<HD, NS>;
     constexpr int KS = HD / 16;  // 16-wide k steps of Q K^T; pairs of 8-wide output tiles of P V
     pdl_trigger();
     pdl_wait();
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const bf16* Vb = Kb + p.kv_off;
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(sm);
 #pragma unroll
-    for (int s = 0; s < NSTAGE - 1; ++s) {
+    for (int s = 0; s < NS - 1; ++s) {
         if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, d, start + s * TK, end);
         cp_async_commit();
     }
@@ -206,16 +208,16 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const uint32_t v_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * L::RB + (lm >> 1) * 16);
 
     for (int t = 0; t < n_tiles; ++t) {
-        cp_async_wait<NSTAGE - 2>();
+        cp_async_wait<NS - 2>();
         __syncthreads();  // tile t is visible; every warp is done with tile t-1, whose stage is refilled next
         {
-            const int tn = t + NSTAGE - 1;
-            if (tn < n_tiles) load_kv<HD>(ring + (tn % NSTAGE) * L::STAGE, Kb, Vb, d, start + tn * TK, end);
+            const int tn = t + NS - 1;
+            if (tn < n_tiles) load_kv<HD>(ring + (tn % NS) * L::STAGE, Kb, Vb, d, start + tn * TK, end);
             cp_async_commit();
         }
         const int nk = min(TK, end - (start + t * TK));
         if (kw >= nk) continue;
-        const uint32_t kbase = ring + (t % NSTAGE) * L::STAGE;
+        const uint32_t kbase = ring + (t % NS) * L::STAGE;
         const uint32_t vbase = kbase + L::TILE;
 
         float s[2][4];
@@ -323,74 +325,115 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         }
     }
     if (n_real == 1) return;
-    __threadfence();
+    // Ticket: after the barrier, one acquire-release atomic publishes this CTA's
+    // partial (release, cumulative over the barrier) and, in the last CTA, makes
+    // every other CTA's partial visible (acquire, passed on by the next barrier).
     __syncthreads();
-    if (tid == 0) is_last = (atomicAdd(&p.tickets[bh], 1u) == (unsigned int)n_real - 1);
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-
-    // ---- last CTA of (b, h): merge the n_real ranges in order.  The (m, l) of
-    // every (range, query) come in one parallel pass; the partial outputs are
-    // staged into shared memory with cp.async, as many ranges at a time as fit.
-    const float* all = p.part + bh * p.n_chunks * gamma * w;  // range cc, query j at (cc * gamma + j) * w
-    float* Wm = reinterpret_cast<float*>(sm + L::WM);
-    float* Lm = reinterpret_cast<float*>(sm + L::LM);
-    const int npairs = gamma * n_real;
-#pragma unroll 4
-    for (int q = tid; q < npairs; q += NT) {
-        const int cc = q / gamma, j = q - cc * gamma;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(all + (int64_t)q * w));
-        Wm[j * CMAX + cc] = ml.x;
-        Lm[j * CMAX + cc] = ml.y;
+    if (tid == 0) {
+        unsigned int prev;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(prev) : "l"(p.tickets + bh) : "memory");
+        is_last = prev == (unsigned int)n_real - 1;
     }
     __syncthreads();
-    for (int j = warp; j < gamma; j += NW) {
-        float* wj = Wm + j * CMAX;
-        float M = -INFINITY;
-        for (int cc = lane; cc < n_real; cc += 32) M = fmaxf(M, wj[cc]);
-        M = warp_max(M);
-        float lsum = 0.f;
-        for (int cc = lane; cc < n_real; cc += 32) {
-            const float m = wj[cc];
-            const float wt = m == -INFINITY ? 0.f : ex2(m - M);
-            wj[cc] = wt;
-            lsum += wt * Lm[j * CMAX + cc];
-        }
-        lsum = warp_sum(lsum);
-        const float inv = 1.f / lsum;
-        for (int cc = lane; cc < n_real; cc += 32) wj[cc] *= inv;
+    if (!is_last) return;
+
+    // ---- last CTA of (b, h): merge the n_real ranges in order.  The partials
+    // (m, l and o of every query) are staged into shared memory with cp.async,
+    // as many ranges as fit per piece (usually all: one round trip), and merged
+    // piece by piece with a running max, sum and rescale per query.
+    const float* all = p.part + bh * p.n_chunks * gamma * w;  // range cc, query j at (cc * gamma + j) * w
+    float* Wm = reinterpret_cast<float*>(sm + L::WM);
+    float* Mj = reinterpret_cast<float*>(sm + L::MJ);
+    float* Lj = Mj + GMAX;
+    float* Sc = Lj + GMAX;
+    if (tid < GMAX) {
+        Mj[tid] = -INFINITY;
+        Lj[tid] = 0.f;
     }
     constexpr int ITEMS = (GMAX * (HD / 4) + NT - 1) / NT;  // (query, 4 columns) items per thread
     float acc[ITEMS][4];
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
     const int rbytes = gamma * w * 4;
-    const int fit = (L::BYTES - L::STG) / rbytes;
+    const int fit = min((L::BYTES - L::STG) / rbytes, CMAX);
     const uint32_t stg = ring + L::STG;
     const float* S = reinterpret_cast<const float*>(sm + L::STG);
     for (int c0 = 0; c0 < n_real; c0 += fit) {
         const int nr = min(fit, n_real - c0);
-        __syncthreads();  // weights are final; the previous piece has been consumed
+        __syncthreads();  // the previous piece has been consumed
         const char* src = reinterpret_cast<const char*>(all + (int64_t)c0 * gamma * w);
         for (int i = tid; i < nr * rbytes / 16; i += NT) cp_async16(stg + i * 16, src + i * 16, 16);
         cp_async_commit();
         cp_async_wait<0>();
+        __syncthreads();
+        {
+            // per query j: eight threads (one per range residue mod 8) find the piece's max and sum
+            const int j = tid >> 3, sub = tid & 7;
+            const bool qv = j < gamma;
+            float pm = -INFINITY;
+            if (qv)
+                for (int cc = sub; cc < nr; cc += 8) pm = fmaxf(pm, S[(cc * gamma + j) * w]);
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+            const float m_old = qv ? Mj[j] : -INFINITY, m_new = fmaxf(m_old, pm);
+            const float ms = m_new == -INFINITY ? 0.f : m_new;
+            float lsum = 0.f;
+            if (qv)
+                for (int cc = sub; cc < nr; cc += 8) {
+                    const float2 ml = *reinterpret_cast<const float2*>(S + (cc * gamma + j) * w);
+                    const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - ms);
+                    Wm[j * CMAX + cc] = wt;
+                    lsum += wt * ml.y;
+                }
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+            if (qv && sub == 0) {
+                const float sc = m_old == -INFINITY ? 0.f : ex2(m_old - ms);
+                Sc[j] = sc;
+                Lj[j] = Lj[j] * sc + lsum;
+                Mj[j] = m_new;
+            }
+        }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
             const int i = tid + k * NT;
             if (i < gamma * (HD / 4)) {
                 const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
-                const float* wj = Wm + j * CMAX + c0;
-                for (int cc = 0; cc < nr; ++cc) {
-                    const float wt = wj[cc];
-                    const float4 x = *reinterpret_cast<const float4*>(S + (cc * gamma + j) * w + 4 + e);
-                    acc[k][0] = fmaf(wt, x.x, acc[k][0]);
-                    acc[k][1] = fmaf(wt, x.y, acc[k][1]);
-                    acc[k][2] = fmaf(wt, x.z, acc[k][2]);
-                    acc[k][3] = fmaf(wt, x.w, acc[k][3]);
+                const float sc = Sc[j];
+                float a0 = acc[k][0] * sc, a1 = acc[k][1] * sc, a2 = acc[k][2] * sc, a3 = acc[k][3] * sc;
+                const float* wj = Wm + j * CMAX;
+                const float* sj = S + j * w + 4 + e;  // range cc at sj + cc * gamma * w
+                const int cs = gamma * w;
+                float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;  // second accumulator set: two chains
+                int cc = 0;
+                for (; cc + 2 <= nr; cc += 2) {
+                    const float w0 = wj[cc], w1 = wj[cc + 1];
+                    const float4 x = *reinterpret_cast<const float4*>(sj + cc * cs);
+                    const float4 y = *reinterpret_cast<const float4*>(sj + (cc + 1) * cs);
+                    a0 = fmaf(w0, x.x, a0);
+                    a1 = fmaf(w0, x.y, a1);
+                    a2 = fmaf(w0, x.z, a2);
+                    a3 = fmaf(w0, x.w, a3);
+                    b0 = fmaf(w1, y.x, b0);
+                    b1 = fmaf(w1, y.y, b1);
+                    b2 = fmaf(w1, y.z, b2);
+                    b3 = fmaf(w1, y.w, b3);
                 }
+                if (cc < nr) {
+                    const float w0 = wj[cc];
+                    const float4 x = *reinterpret_cast<const float4*>(sj + cc * cs);
+                    a0 = fmaf(w0, x.x, a0);
+                    a1 = fmaf(w0, x.y, a1);
+                    a2 = fmaf(w0, x.z, a2);
+                    a3 = fmaf(w0, x.w, a3);
+                }
+                acc[k][0] = a0 + b0;
+                acc[k][1] = a1 + b1;
+                acc[k][2] = a2 + b2;
+                acc[k][3] = a3 + b3;
             }
         }
     }
@@ -399,16 +442,28 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         const int i = tid + k * NT;
         if (i < gamma * (HD / 4)) {
             const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
-            store4<TO>(out + (int64_t)j * d + e, acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+            const float inv = 1.f / Lj[j];  // every range holds at least one key, so the sum is >= 1
+            store4<TO>(out + (int64_t)j * d + e, acc[k][0] * inv, acc[k][1] * inv, acc[k][2] * inv, acc[k][3] * inv);
         }
     }
     if (tid == 0) p.tickets[bh] = 0u;
 }
 
-template <int HD, typename TO>
+template <int HD, typename TO, int NS>
 cudaError_t set_attr_tc() {
-    return cudaFuncSetAttribute(k_attention_tc<HD, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TLayout<HD>::BYTES);
+    return cudaFuncSetAttribute(k_attention_tc<HD, TO, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TLayout<HD, NS>::BYTES);
+}
+
+int g_num_sms = 0;
+
+template <int HD, typename TO>
+void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
+    // a grid that fits one CTA per SM gives each CTA the SM's whole shared memory: a deeper ring
+    if ((int)(grid.x * grid.y * grid.z) <= g_num_sms)
+        launch(k_attention_tc<HD, TO, 6>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
+    else
+        launch(k_attention_tc<HD, TO, 3>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);
 }
 
 }  // namespace
@@ -421,10 +476,17 @@ int attention_tc_max_chunks() { return CMAX; }
 
 cudaError_t attention_tc_init() {
     cudaError_t e;
-    if ((e = set_attr_tc<64, bf16>()) != cudaSuccess) return e;
-    if ((e = set_attr_tc<64, float>()) != cudaSuccess) return e;
-    if ((e = set_attr_tc<128, bf16>()) != cudaSuccess) return e;
-    return set_attr_tc<128, float>();
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = set_attr_tc<64, bf16, 3>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<64, float, 3>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<128, bf16, 3>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<128, float, 3>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<64, bf16, 6>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<64, float, 6>()) != cudaSuccess) return e;
+    if ((e = set_attr_tc<128, bf16, 6>()) != cudaSuccess) return e;
+    return set_attr_tc<128, float, 6>();
 }
 
 cudaError_t attention_tc(const AttnParams& p, cudaStream_t st) {
@@ -435,13 +497,11 @@ cudaError_t attention_tc(const AttnParams& p, cudaStream_t st) {
     dim3 grid(p.n_chunks, p.n_heads, p.B);
     const bool o16 = p.out_dtype == DT_BF16;
     if (hd == 64) {
-        const size_t sm = TLayout<64>::BYTES;
-        if (o16) launch(k_attention_tc<64, bf16>, grid, NT, sm, st, p);
-        else launch(k_attention_tc<64, float>, grid, NT, sm, st, p);
+        if (o16) launch_tc<64, bf16>(p, grid, st);
+        else launch_tc<64, float>(p, grid, st);
     } else {
-        const size_t sm = TLayout<128>::BYTES;
-        if (o16) launch(k_attention_tc<128, bf16>, grid, NT, sm, st, p);
-        else launch(k_attention_tc<128, float>, grid, NT, sm, st, p);
+        if (o16) launch_tc<128, bf16>(p, grid, st);
+        else launch_tc<128, float>(p, grid, st);
     }
     note_launch();
     return cudaGetLastError();

@@ -178,13 +178,14 @@ cudaError_t grow(DevBuf& b, size_t bytes) {
 }
 
 int attn_chunks(const dspark_handle* h, int B, int max_keys) {
-    // Few (sequence, head) pairs: one wave of two CTAs per SM, so that each range
-    // is long and the last CTA merges few partials.  Many pairs: about a dozen
-    // CTAs per SM over the launch, so that sequences of unequal length balance.
-    // At least 64 keys (one tile) per range either way.
+    // Few (sequence, head) pairs: at most one CTA per SM (the tensor-core kernel
+    // then runs a deeper cp.async ring), so that each range is long and the last
+    // CTA merges few partials.  Many pairs: about a dozen CTAs per SM over the
+    // launch, so that sequences of unequal length balance.  At least 64 keys
+    // (one tile) per range either way.
     const int nh = h->cfg.n_heads;
     const int pairs = nh * B;
-    int want = pairs < 2 * h->num_sms ? (2 * h->num_sms + pairs - 1) / pairs : (12 * h->num_sms + pairs - 1) / pairs;
+    int want = pairs <= h->num_sms ? h->num_sms / pairs : (12 * h->num_sms + pairs - 1) / pairs;
     int by_keys = (max_keys + 63) / 64;
     return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks(h->dt, h->hd, h->cfg.gamma)));
 }
