@@ -114,7 +114,8 @@ struct dspark_handle {
     void* mk_E = nullptr;                    // [max_seqs, r] gathered w1 rows (bf16)
     float* mk_pv = nullptr;                  // [max_seqs, ceil(V/32)] chunk partials
     int* mk_pi = nullptr;
-    unsigned int* mk_bar = nullptr;          // [2] grid-barrier words
+    unsigned int* mk_bar = nullptr;          // [2] grid-barrier words, then the chain's launch epoch
+    unsigned long long* mk_keys = nullptr;   // [2, max_seqs, 16] argmax words of the Markov chain, then 2 counters
     float* ws = nullptr;
     size_t ws_floats = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
@@ -497,6 +498,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.counters = h->mk_cnt;
     mp.err = h->d_err;
     mp.ctas = h->mk_ctas;
+    mp.keys = h->mk_keys;
+    mp.keys_stride = 16 * h->cfg.max_seqs;
+    mp.epoch = h->mk_bar + 2;
+    mp.bar = h->mk_keys + 2 * (size_t)h->cfg.max_seqs * 16;
     Prof pr(h, CAT_MARKOV, st);
     if (B >= 8 && h->tc_mk_E.ready && tc_gemm_ok(V, B, c.markov_rank) && anchors_dev) {
         // many sequences: per position a [V, r] x [B, r]^T tensor-core GEMM reads w2 once for all of
@@ -518,6 +523,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             CUDA_TRY(h, markov_finish(h->mk_pv, h->mk_pi, nch, h->w1, h->dt, h->y, h->conf_wb, anchors_dev, tokens, conf,
                                       B, c.gamma, k, d, c.markov_rank, V, h->d_err, st));
         }
+        return DSPARK_OK;
+    }
+    if (markov_chain_resident_ok(mp)) {
+        CUDA_TRY(h, markov_chain_resident(mp, h->num_sms, st));
         return DSPARK_OK;
     }
     // one cooperative launch when B sequences x ctas fit co-resident, else one launch per position
@@ -897,12 +906,15 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->mk_chain_max = markov_chain_max_ctas(h->dt);
     CTRY(dalloc(h, (void**)&h->mk_v, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
     CTRY(dalloc(h, (void**)&h->mk_i, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
-    CTRY(dalloc(h, (void**)&h->mk_bar, 2 * sizeof(unsigned int)));
-    CTRY(cudaMemsetAsync(h->mk_bar, 0, 2 * sizeof(unsigned int), st));
+    CTRY(dalloc(h, (void**)&h->mk_bar, 3 * sizeof(unsigned int)));
+    CTRY(cudaMemsetAsync(h->mk_bar, 0, 3 * sizeof(unsigned int), st));
+    CTRY(dalloc(h, (void**)&h->mk_keys, (2 * (size_t)cfg->max_seqs * 16 + 2) * sizeof(unsigned long long)));
+    CTRY(cudaMemsetAsync(h->mk_keys, 0, (2 * (size_t)cfg->max_seqs * 16 + 2) * sizeof(unsigned long long), st));
     CTRY(dalloc(h, (void**)&h->mk_cnt, (size_t)cfg->max_seqs * 4));
     CTRY(dalloc(h, (void**)&h->safe_ids, (size_t)cfg->max_seqs * 4));
     CTRY(dalloc(h, (void**)&h->anchor_dev, sizeof(int)));
     CTRY(attention_init());
+    CTRY(markov_chain_resident_init());
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));

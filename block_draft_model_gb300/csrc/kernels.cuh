@@ -136,12 +136,17 @@ struct MarkovParams {
     unsigned int* counters;  // scratch: B counters, zero between launches
     int* err;                // device error word
     int ctas;                // CTAs per sequence over V
+    unsigned long long* keys = nullptr;  // markov_chain: 2 sets of keys_stride argmax words (sequence b, position k
+                                         // at b * 16 + k), zero before the first launch
+    int keys_stride = 0;                 // >= 16 * B
+    unsigned int* epoch = nullptr;       // markov_chain: launch counter (selects the word set), zero-initialised
+    unsigned long long* bar = nullptr;   // markov_chain_resident: 2 arrival counters, zero-initialised
 };
 int markov_ctas(int V);
 cudaError_t markov_step(const MarkovParams& p, cudaStream_t st);
 // All gamma positions in one cooperative launch (p.ctas CTAs per sequence, one
-// bounded grid barrier per position; part_v/part_i hold 2 * B * ctas entries;
-// bar_count/bar_gen: zeroed words, left reusable).  markov_chain_max_ctas is the
+// bounded grid barrier per position, the argmax through 64-bit atomic max words
+// p.keys; bar_count/bar_gen: zeroed words, left reusable).  markov_chain_max_ctas is the
 // largest co-resident grid.
 int markov_chain_max_ctas(int w_dtype);
 // Many-sequence form: per position k, gather E[b] = w1[prev_b] (bf16, [B, r]),
@@ -154,6 +159,12 @@ cudaError_t markov_finish(const float* part_v, const int* part_i, int nchunks, c
                           const float* y, const float* conf_w, const int* anchors, int* tokens, float* conf, int B,
                           int gamma, int k, int d, int r, int V, int* err, cudaStream_t st);
 cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st);
+// Up to 8 sequences with bf16 weights and r in {64, 128, 256}: one cooperative CTA
+// per SM keeps its slice of w2 in shared memory for the whole chain and runs the
+// dot products on the tensor cores.
+cudaError_t markov_chain_resident_init();  // once per process/device
+bool markov_chain_resident_ok(const MarkovParams& p);
+cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream_t st);
 
 // ------------------------------------------------------------------ bookkeeping kernels
 // For a batched ingest: per feature row t, its slot and cache position

@@ -12,6 +12,7 @@
 // bytes each for r = 256), so every load is a full 32-byte sector and a row
 // needs a two-step shuffle; two rows per lane group are in flight at once.  The token stays on the
 // device, where the next position's launch reads it.
+#include <algorithm>
 #include <climits>
 #include <stdint.h>
 #include <math.h>
@@ -27,6 +28,7 @@ constexpr int NT = 256;
 constexpr int LPR = 4;         // lanes per vocabulary row
 constexpr int RPW = 32 / LPR;  // rows per warp pass
 constexpr int RMAX = 1024;     // largest Markov rank
+constexpr int GMAX_CHAIN = 16; // largest block size (key words per sequence)
 
 template <typename TW>
 __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
@@ -202,13 +204,27 @@ __device__ __forceinline__ bool grid_sync(unsigned int* count, unsigned int* gen
     return ok != 0;
 }
 
+// (value, index) -> one 64-bit key whose unsigned order is the argmax order:
+// larger value first, then lower index.  Key 0 is below every candidate.
+__device__ __forceinline__ unsigned long long arg_key(float v, int i) {
+    unsigned int u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(~(unsigned int)i);
+}
+__device__ __forceinline__ float key_value(unsigned long long key) {
+    unsigned int u = (unsigned int)(key >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7fffffffu) : ~u;
+    return __uint_as_float(u);
+}
+
 // The whole chain in one cooperative launch: grid = ctas * B CTAs, CTA c of
-// sequence b = blockIdx.x / ctas streams its slice of w2 at every position;
-// after one grid barrier per position every CTA of the sequence reduces the
-// CTA winners itself (the key is a total order, so all agree), and CTA 0 of the
-// sequence writes the token and the confidence.  Partials are double-buffered
-// by position parity: a buffer is rewritten two positions later, after a
-// barrier every CTA passed only once done reading it.
+// sequence b = blockIdx.x / ctas streams its slice of w2 at every position and
+// folds its best (value, index) into one 64-bit word per (sequence, position)
+// with an atomic max; after one grid barrier per position every CTA reads the
+// token from that word.  The confidences need only the tokens, so CTA 0 of
+// each sequence computes them after the last position.  The words alternate
+// between two sets by launch parity (a device epoch counter): a launch clears
+// the other set, which the next launch uses.
 template <typename TW>
 __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned int* bar_count, unsigned int* bar_gen) {
     constexpr int VE = Vec16<TW>::N;
@@ -216,7 +232,7 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
     __shared__ float red_v[NT / 32];
     __shared__ int red_i[NT / 32];
     __shared__ float redf[32];
-    __shared__ int prev_s;
+    __shared__ int toks[GMAX_CHAIN + 1];
 
     const int ctas = p.ctas;
     const int b = blockIdx.x / ctas, cta = blockIdx.x - b * ctas;
@@ -228,11 +244,18 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane & (LPR - 1), rw = lane / LPR;
     const int nvec = r / VE;
-    if (threadIdx.x == 0) prev_s = min(max(p.anchors ? p.anchors[b] : p.anchor, 0), V - 1);
+    const unsigned int par = *(volatile unsigned int*)p.epoch & 1u;
+    unsigned long long* keys = p.keys + (size_t)par * p.keys_stride + (size_t)b * GMAX_CHAIN;
+    if (blockIdx.x == 0) {
+        unsigned long long* other = p.keys + (size_t)(par ^ 1u) * p.keys_stride;
+        for (int i = threadIdx.x; i < p.keys_stride; i += NT) other[i] = 0ull;
+        if (p.bar && threadIdx.x == 0) p.bar[par ^ 1u] = 0ull;  // shared with the resident form
+    }
+    if (threadIdx.x == 0) toks[0] = min(max(p.anchors ? p.anchors[b] : p.anchor, 0), V - 1);
     __syncthreads();
 
     for (int k = 0; k < p.gamma; ++k) {
-        const int prev = prev_s;
+        const int prev = toks[k];
         for (int c = threadIdx.x; c < r; c += NT) e[c] = to_f32(w1[(int64_t)prev * r + c]);
         __syncthreads();
         const int64_t urow = (int64_t)(b * p.gamma + k) * V;
@@ -295,7 +318,6 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
             red_i[warp] = best.i;
         }
         __syncthreads();
-        const int64_t pb = (int64_t)(k & 1) * p.B * ctas + (int64_t)b * ctas;
         if (threadIdx.x == 0) {
             ArgBest cb{-INFINITY, INT_MAX};
             for (int w = 0; w < NT / 32; ++w)
@@ -303,53 +325,269 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
                     cb.v = red_v[w];
                     cb.i = red_i[w];
                 }
-            p.part_v[pb + cta] = cb.v;
-            p.part_i[pb + cta] = cb.i;
+            if (cb.i != INT_MAX) atomicMax(keys + k, arg_key(cb.v, cb.i));
         }
-        grid_sync(bar_count, bar_gen, gridDim.x, p.err);
-        // every CTA of the sequence: the winner over the CTA results
-        ArgBest fb{-INFINITY, INT_MAX};
-        for (int c = threadIdx.x; c < ctas; c += NT) {
-            const float v = __ldcg(p.part_v + pb + c);
-            const int i = __ldcg(p.part_i + pb + c);
-            if (better(v, i, fb.v, fb.i)) {
-                fb.v = v;
-                fb.i = i;
-            }
-        }
-        fb = warp_argbest(fb);
-        __syncthreads();  // red_v/red_i reuse
-        if (lane == 0) {
-            red_v[warp] = fb.v;
-            red_i[warp] = fb.i;
-        }
-        float z = 0.f;
-        if (cta == 0) {
-            const float* yr = p.y + (int64_t)(b * p.gamma + k) * p.d;
-            for (int c = threadIdx.x; c < p.d; c += NT) z = fmaf(yr[c], p.conf_w[c], z);
-            for (int c = threadIdx.x; c < r; c += NT) z = fmaf(e[c], p.conf_w[p.d + c], z);
-        }
-        z = block_sum(z, redf);  // contains __syncthreads: red_v/red_i are complete
+        grid_sync(bar_count, bar_gen, gridDim.x, p.err);  // orders the atomic before the arrival
         if (threadIdx.x == 0) {
-            ArgBest tb{-INFINITY, INT_MAX};
-            for (int w = 0; w < NT / 32; ++w)
-                if (better(red_v[w], red_i[w], tb.v, tb.i)) {
-                    tb.v = red_v[w];
-                    tb.i = red_i[w];
-                }
-            int tok = tb.i;
-            if (tok == INT_MAX || !(tb.v > -INFINITY)) {
+            const unsigned long long key = __ldcg(keys + k);
+            int tok = (int)(~(unsigned int)key);
+            if (key == 0ull || !(key_value(key) > -INFINITY) || tok < 0 || tok >= V) {
                 if (cta == 0) atomicOr(p.err, 8);
                 tok = 0;
             }
-            prev_s = tok;
-            if (cta == 0) {
-                p.tokens[b * p.gamma + k] = tok;
-                p.conf[b * p.gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + r])));
-            }
+            toks[k + 1] = tok;
+            if (cta == 0) p.tokens[b * p.gamma + k] = tok;
         }
         __syncthreads();
     }
+    // confidences of every position: sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b)
+    if (cta == 0) {
+        for (int k = 0; k < p.gamma; ++k) {
+            const float* yr = p.y + (int64_t)(b * p.gamma + k) * p.d;
+            const TW* er = w1 + (int64_t)toks[k] * r;
+            float z = 0.f;
+            for (int c = threadIdx.x; c < p.d; c += NT) z = fmaf(yr[c], p.conf_w[c], z);
+            for (int c = threadIdx.x; c < r; c += NT) z = fmaf(to_f32(er[c]), p.conf_w[p.d + c], z);
+            z = block_sum(z, redf);
+            if (threadIdx.x == 0) p.conf[b * p.gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + r])));
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(p.epoch, 1u);  // every CTA read it before the first barrier
+}
+
+// ---- resident form: up to 8 sequences, bf16 weights, r = 64, 128 or 256 ------------
+// One CTA per SM for the whole chain.  CTA c owns vocabulary rows
+// [c * rows, (c + 1) * rows) for every sequence and keeps as many of its w2
+// rows as fit in shared memory for all gamma positions (the rest are read
+// from global memory each position), so w2 crosses the memory system once
+// per chain instead of once per position.  The dot products w2 . e_b run on
+// the tensor cores: mma.m16n8k16 with 16 vocabulary rows as M, the (up to 8)
+// sequences' e = w1[prev] as the N columns, r as K.  Inside each 32-wide slice
+// of r the K order is permuted so that a lane's A fragments for two k-steps
+// are one 16-byte chunk of a row and its B fragments one 16-byte chunk of its
+// sequence's e (the same permutation on both sides leaves every dot product
+// unchanged).  Resident rows are stored with their 16-byte chunks XOR-swizzled
+// by row, so the fragment loads are free of bank conflicts.  Per position:
+// base logits (prefetched into shared memory during the previous barrier), a
+// (value, index) atomic max per sequence, then one grid barrier on a 64-bit
+// arrival counter (release add, acquire poll; it counts up through the launch,
+// barrier k opens at (k + 1) * gridDim.x).  Counters and argmax words
+// alternate between two sets by launch parity.
+constexpr int NT_RES = 512;
+constexpr int NB_RES = 8;  // sequences: the N of the MMA
+
+__device__ __forceinline__ void cp_async16_res(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// c[16x8] += a[16x16] . b[16x8], bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// the two k-steps held by one 16-byte chunk of rows g, g+8 (lo, hi) and of e
+__device__ __forceinline__ void mma_chunk(float* c, const uint4& lo, const uint4& hi, const uint4& ev) {
+    mma_bf16_16816(c, lo.x, hi.x, lo.y, hi.y, ev.x, ev.y);
+    mma_bf16_16816(c, lo.z, hi.z, lo.w, hi.w, ev.z, ev.w);
+}
+
+// Bounded barrier of the resident chain: true when every CTA has arrived.
+__device__ __forceinline__ bool res_barrier(unsigned long long* bar, unsigned long long target, int* err) {
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ok = 1;
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+        uint64_t t0, t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+        while (true) {
+            unsigned long long cur;
+            asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(bar) : "memory");
+            if (cur >= target) break;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 > 1000000000ull) {
+                atomicOr(err, 16);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+template <int KD>  // r = 32 * KD
+__global__ void __launch_bounds__(NT_RES, 1) k_markov_chain_res(MarkovParams p, int n_cache) {
+    constexpr int R = KD * 32;
+    constexpr int ROWB = R * 2;   // bytes of one w2 row
+    constexpr int CPR = ROWB / 16;  // 16-byte chunks per row (a multiple of 8)
+    // dynamic shared memory: [n_cache][ROWB] resident w2 rows (swizzled chunks),
+    // then the base logits of the next position, [2 buffers][B][rows] fp32
+    extern __shared__ __align__(128) uint8_t w2s[];
+    __shared__ float red_v[NB_RES][NT_RES / 32];
+    __shared__ int red_i[NB_RES][NT_RES / 32];
+    __shared__ float redf[32];
+    __shared__ int toks[NB_RES][GMAX_CHAIN + 1];
+
+    const int V = p.V, gamma = p.gamma, NB = p.B;
+    const bf16* __restrict__ w1 = reinterpret_cast<const bf16*>(p.w1);
+    const bf16* __restrict__ w2 = reinterpret_cast<const bf16*>(p.w2);
+    float* __restrict__ lg = p.logits;
+    const int rows = (V + gridDim.x - 1) / gridDim.x;
+    const int v_begin = blockIdx.x * rows;
+    const int nrows = max(0, min(V, v_begin + rows) - v_begin);
+    const int nc = min(n_cache, nrows);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float* ubuf = reinterpret_cast<float*>(w2s + (size_t)n_cache * ROWB);  // [2][NB][rows]
+    const uint32_t ubuf_s = (uint32_t)__cvta_generic_to_shared(ubuf);
+    const uint32_t w2s_s = (uint32_t)__cvta_generic_to_shared(w2s);
+
+    {  // the resident rows: chunk c of row li at chunk c ^ (li & 7)
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(w2 + (int64_t)v_begin * R);
+        for (int i = tid; i < nc * CPR; i += NT_RES) {
+            const int li = i / CPR, c = i - li * CPR;
+            cp_async16_res(w2s_s + li * ROWB + ((c ^ (li & 7)) * 16), src + (size_t)i * 16);
+        }
+    }
+    auto load_u = [&](int k) {  // base logits of position k for this CTA's rows, into buffer k & 1
+        for (int i = tid; i < NB * nrows; i += NT_RES) {
+            const int b = i / nrows, li = i - b * nrows;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                             ubuf_s + (uint32_t)((((k & 1) * NB + b) * rows + li) * 4)),
+                         "l"(p.U + (int64_t)(b * gamma + k) * V + v_begin + li)
+                         : "memory");
+        }
+    };
+    load_u(0);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const unsigned int par = *(volatile unsigned int*)p.epoch & 1u;
+    unsigned long long* keys = p.keys + (size_t)par * p.keys_stride;
+    unsigned long long* bar = p.bar + par;
+    if (blockIdx.x == 0) {
+        unsigned long long* other = p.keys + (size_t)(par ^ 1u) * p.keys_stride;
+        for (int i = tid; i < p.keys_stride; i += NT_RES) other[i] = 0ull;
+        if (tid == 0) p.bar[par ^ 1u] = 0ull;
+    }
+    if (tid < NB) toks[tid][0] = min(max(p.anchors ? p.anchors[tid] : p.anchor, 0), V - 1);
+
+    const int tiles = (nrows + 15) / 16;
+    for (int k = 0; k < gamma; ++k) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");  // resident rows (k = 0) and this position's U
+        __syncthreads();
+        const float* uk = ubuf + (k & 1) * NB * rows;
+        // B fragments: lane (g, t) supplies sequence g's e = w1[prev_g], chunk 4j + t of every slice j
+        uint4 ev[KD];
+#pragma unroll
+        for (int j = 0; j < KD; ++j)
+            ev[j] = g < NB ? __ldg(reinterpret_cast<const uint4*>(w1 + (int64_t)toks[g][k] * R + (4 * j + t) * 8))
+                           : make_uint4(0, 0, 0, 0);
+        ArgBest best[2] = {{-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}};  // sequences 2t, 2t+1
+        // the highest tiles (rows read from global memory) first: their loads overlap the load of e
+        for (int tile = warp + (tiles - 1 - warp) / 16 * 16; tile >= 0 && warp < tiles; tile -= 16) {
+            const int la = tile * 16 + g, lb = la + 8;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            if (tile * 16 + 16 <= nc) {
+#pragma unroll
+                for (int j = 0; j < KD; ++j) {
+                    const int ch = 4 * j + t;
+                    const uint4 lo = *reinterpret_cast<const uint4*>(w2s + la * ROWB + ((ch ^ (la & 7)) * 16));
+                    const uint4 hi = *reinterpret_cast<const uint4*>(w2s + lb * ROWB + ((ch ^ (lb & 7)) * 16));
+                    mma_chunk(c, lo, hi, ev[j]);
+                }
+            } else {
+                uint4 lo[KD], hi[KD];
+#pragma unroll
+                for (int j = 0; j < KD; ++j) {
+                    const int ch = 4 * j + t;
+                    lo[j] = la < nc ? *reinterpret_cast<const uint4*>(w2s + la * ROWB + ((ch ^ (la & 7)) * 16))
+                            : la < nrows ? __ldg(reinterpret_cast<const uint4*>(w2 + (int64_t)(v_begin + la) * R + ch * 8))
+                                         : make_uint4(0, 0, 0, 0);
+                    hi[j] = lb < nc ? *reinterpret_cast<const uint4*>(w2s + lb * ROWB + ((ch ^ (lb & 7)) * 16))
+                            : lb < nrows ? __ldg(reinterpret_cast<const uint4*>(w2 + (int64_t)(v_begin + lb) * R + ch * 8))
+                                         : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int j = 0; j < KD; ++j) mma_chunk(c, lo[j], hi[j], ev[j]);
+            }
+            // c[0], c[1]: row la, sequences 2t, 2t+1; c[2], c[3]: row lb
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int li = q < 2 ? la : lb, n = 2 * t + (q & 1);
+                if (li < nrows && n < NB) {
+                    const int v = v_begin + li;
+                    const float l = c[q] + uk[n * rows + li];
+                    if (lg) lg[(int64_t)(n * gamma + k) * V + v] = l;
+                    if (better(l, v, best[q & 1].v, best[q & 1].i)) {
+                        best[q & 1].v = l;
+                        best[q & 1].i = v;
+                    }
+                }
+            }
+        }
+        // over the 8 row groups of the warp (lanes with equal t hold the same sequences)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, best[h].v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, best[h].i, o);
+                if (better(ov, oi, best[h].v, best[h].i)) {
+                    best[h].v = ov;
+                    best[h].i = oi;
+                }
+            }
+            if (g == 0 && 2 * t + h < NB) {
+                red_v[2 * t + h][warp] = best[h].v;
+                red_i[2 * t + h][warp] = best[h].i;
+            }
+        }
+        __syncthreads();
+        if (warp < NB) {  // warp b reduces sequence b's 16 warp results
+            ArgBest cb{lane < NT_RES / 32 ? red_v[warp][lane] : -INFINITY,
+                       lane < NT_RES / 32 ? red_i[warp][lane] : INT_MAX};
+            cb = warp_argbest(cb);
+            if (lane == 0 && cb.i != INT_MAX) atomicMax(keys + warp * GMAX_CHAIN + k, arg_key(cb.v, cb.i));
+        }
+        if (k + 1 < gamma) load_u(k + 1);  // its buffer was last read two positions ago
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        res_barrier(bar, (unsigned long long)(k + 1) * gridDim.x, p.err);
+        if (tid < NB) {
+            const unsigned long long key = __ldcg(keys + tid * GMAX_CHAIN + k);
+            int tok = (int)(~(unsigned int)key);
+            if (key == 0ull || !(key_value(key) > -INFINITY) || tok < 0 || tok >= V) {
+                if (blockIdx.x == 0) atomicOr(p.err, 8);
+                tok = 0;
+            }
+            toks[tid][k + 1] = tok;
+            if (blockIdx.x == 0) p.tokens[tid * gamma + k] = tok;
+        }
+    }
+    __syncthreads();
+    // confidences: sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b), by CTA 0
+    if (blockIdx.x == 0) {
+        for (int b = 0; b < NB; ++b)
+            for (int k = 0; k < gamma; ++k) {
+                const float* yr = p.y + (int64_t)(b * gamma + k) * p.d;
+                const bf16* er = w1 + (int64_t)toks[b][k] * R;
+                float z = 0.f;
+                for (int c = tid; c < p.d; c += NT_RES) z = fmaf(yr[c], p.conf_w[c], z);
+                for (int c = tid; c < R; c += NT_RES) z = fmaf(to_f32(er[c]), p.conf_w[p.d + c], z);
+                z = block_sum(z, redf);
+                if (tid == 0) p.conf[b * gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + R])));
+            }
+        if (tid == 0) atomicAdd(p.epoch, 1u);  // every CTA read it before the first barrier
+    }
+}
+
+int g_res_ok[3] = {0, 0, 0};  // the resident chain's kernels for r = 64, 128, 256
+int g_res_budget = 0;         // its dynamic shared memory
+
+template <int KD>
+cudaError_t res_attr(int bytes) {
+    return cudaFuncSetAttribute(k_markov_chain_res<KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // E[b][:] = w1[prev_b] for the many-sequence form (prev_b = anchor at k = 0, else token k-1).
@@ -454,7 +692,8 @@ int markov_chain_max_ctas(int w_dtype) {
 }
 
 cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st) {
-    if (p.r > RMAX || p.r % 8 != 0) return cudaErrorInvalidValue;
+    if (p.r > RMAX || p.r % 8 != 0 || p.gamma > GMAX_CHAIN || !p.keys || !p.epoch || p.keys_stride < 16 * p.B)
+        return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
@@ -479,6 +718,54 @@ cudaError_t markov_step(const MarkovParams& p, cudaStream_t st) {
     else
         launch(k_markov<float>, grid, NT, 0, st, p);
     note_launch();
+    return cudaGetLastError();
+}
+
+bool markov_chain_resident_ok(const MarkovParams& p) {
+    const int kd = p.r / 32;
+    return p.w_dtype == DT_BF16 && p.B >= 1 && p.B <= NB_RES && p.r % 32 == 0 && (kd == 2 || kd == 4 || kd == 8) &&
+           p.gamma >= 1 && p.gamma <= GMAX_CHAIN && p.keys && p.epoch && p.bar && p.keys_stride >= 16 * p.B &&
+           g_res_ok[kd == 8 ? 2 : kd / 2 - 1];
+}
+
+cudaError_t markov_chain_resident_init() {
+    int dev = 0, optin = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    g_res_budget = (optin - 4096) / 16 * 16;  // static shared memory and headroom
+    g_res_ok[0] = res_attr<2>(g_res_budget) == cudaSuccess;
+    g_res_ok[1] = res_attr<4>(g_res_budget) == cudaSuccess;
+    g_res_ok[2] = res_attr<8>(g_res_budget) == cudaSuccess;
+    (void)cudaGetLastError();
+    return cudaSuccess;
+}
+
+cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream_t st) {
+    if (!markov_chain_resident_ok(p)) return cudaErrorInvalidValue;
+    const int kd = p.r / 32;
+    // what the base-logit buffers leave of the budget holds resident rows
+    const int rows = (p.V + num_sms - 1) / num_sms;
+    const int ubytes = (2 * p.B * rows * 4 + 15) / 16 * 16;
+    const int n_cache = std::max(0, std::min(rows, (g_res_budget - ubytes) / (p.r * 2)));
+    const size_t smem = (size_t)n_cache * p.r * 2 + ubytes;
+    if ((int)smem > g_res_budget) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(NT_RES);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (kd == 2) e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<2>, p, n_cache);
+    else if (kd == 4) e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<4>, p, n_cache);
+    else e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<8>, p, n_cache);
+    note_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -204,6 +204,36 @@ def test_batched_many_sequences_ragged_vocab():
                     label=f"seq {i} (L {lens[i]})")
 
 
+@pytest.mark.parametrize("n_seq,rank,vocab", [(3, 64, 1000), (1, 128, 5003), (7, 256, 2048)])
+def test_markov_chain_few_sequences(n_seq, rank, vocab):
+    """1 to 7 sequences with r in {64, 128, 256}: the whole Markov chain in one
+    cooperative launch with the vocabulary slices resident on the SMs and the
+    dot products on the tensor cores; vocabularies that leave ragged slices."""
+    cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=6,
+                            vocab=vocab, markov_rank=rank)
+    W = syn.make_weights(cfg, seed=13, norm_std=0.1)
+    lens = [17 + 5 * i for i in range(n_seq)]
+    feats = [syn.make_feats(cfg, L, seed=13, seq=i) for i, L in enumerate(lens)]
+    gb = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=64, max_seqs=n_seq)
+    ids = torch.arange(n_seq, dtype=torch.int32, device="cuda")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    gb.ingest_context_batched(ids, cu, to_torch(np.concatenate(feats, axis=0)))
+    anchors = torch.tensor([(37 * i + 5) % vocab for i in range(n_seq)], dtype=torch.int32, device="cuda")
+    tok = torch.empty(n_seq, cfg.gamma, dtype=torch.int32, device="cuda")
+    conf = torch.empty(n_seq, cfg.gamma, dtype=torch.float32, device="cuda")
+    lg = torch.empty(n_seq, cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda")
+    dr = oracle.Drafter(cfg, W)
+    for i, L in enumerate(lens):
+        dr.ingest(feats[i], seq=i)
+    for rep in range(3):  # repeated launches alternate the argmax word sets
+        gb.draft_batched(ids, anchors, tok, conf, lg)
+        torch.cuda.synchronize()
+        assert gb.check() == 0
+        for i in range(n_seq):
+            check_block(dr, i, int(anchors[i]), tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
+                        label=f"launch {rep} seq {i}")
+
+
 def test_bf16_attention_many_key_ranges():
     """head_dim 128, 1500 context rows: the keys of each head are split over
     many CTAs (64-key tiles, a ragged last tile) and merged by the last one."""
