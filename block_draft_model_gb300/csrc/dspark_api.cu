@@ -122,6 +122,7 @@ struct dspark_handle {
     int* safe_anchors = nullptr;             // [max_seqs] batched anchors clamped into [0, V)
     // ingest workspaces
     int ingest_rows = 0;
+    int P_rows = 0;                          // rows of P: room for the K ranges of a split projection
     float* P = nullptr;
     void* Nbuf = nullptr;
     DevBuf rowmap;                           // row_seq, row_pos (grow-only)
@@ -331,15 +332,28 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
         ep.kind = EPI_STORE_F32;
         ep.out_f32 = h->P;
         ep.ldo = d;
+        // Too few output tiles for the SMs: cut K into ranges (separate work units
+        // whose partial products the normalisation sums).
+        int ks = 1;
+        if (n > 16 && h->tc_wc.ready && tc_gemm_ok(n, d, h->mH)) {
+            const int tiles = ((n + 127) / 128) * ((d + 255) / 256);
+            ks = std::max(1, std::min({h->num_sms / tiles, 4, h->P_rows / n, h->mH / (64 * 8)}));
+        }
         {
             Prof pr(h, CAT_INGEST_PROJ, st);
-            CUDA_TRY(h, gemm(h, h->dt, X, h->mH, nullptr, 0, WView{h->W_c, &h->tc_wc, &h->ts_wc}, n, d, h->mH, ep, st));
+            if (ks > 1) {
+                ep.split_rows = n;
+                CUDA_TRY(h, tc_gemm(X, h->mH, h->tc_wc, n, d, h->mH, ep, h->num_sms, h->d_err, st, ks));
+            } else {
+                CUDA_TRY(h, gemm(h, h->dt, X, h->mH, nullptr, 0, WView{h->W_c, &h->tc_wc, &h->ts_wc}, n, d, h->mH, ep,
+                                 st));
+            }
         }
         const int lp = h->dt;  // normalised rows in the storage type (bf16 feeds the tensor cores)
         {
             Prof pr(h, CAT_INGEST_NORM, st);
-            CUDA_TRY(h, ingest_norm(h->P, n, d, h->cfg.eps, h->ctx_norm, h->attn_norm_dev, nL, lp, h->Nbuf,
-                                    (int64_t)h->ingest_rows * d, st));
+            CUDA_TRY(h, ingest_norm(h->P, ks, (int64_t)n * d, n, d, h->cfg.eps, h->ctx_norm, h->attn_norm_dev, nL, lp,
+                                    h->Nbuf, (int64_t)h->ingest_rows * d, st));
         }
         Prof pr_kv(h, CAT_INGEST_KV, st);
         for (int i = 0; i < nL; ++i) {
@@ -923,7 +937,8 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, (void**)&h->ws, h->ws_floats * 4));
     // ingest workspaces
     h->ingest_rows = std::max(1, std::min(std::max(cfg->max_ctx, 16), 16384));
-    CTRY(dalloc(h, (void**)&h->P, (size_t)h->ingest_rows * d * 4));
+    h->P_rows = h->ingest_rows * (h->ingest_rows <= 4096 ? 4 : 1);
+    CTRY(dalloc(h, (void**)&h->P, (size_t)h->P_rows * d * 4));
     CTRY(dalloc(h, &h->Nbuf, (size_t)nL * h->ingest_rows * d * es));
 
     // tensor-core views of the big weights (bf16 only)

@@ -26,6 +26,7 @@ struct EpiParams {
     int kind = EPI_STORE_F32;
     float* out_f32 = nullptr;
     int64_t ldo = 0;
+    int split_rows = 0;          // EPI_STORE_F32 of a K-split tensor-core GEMM: rows between the ranges' outputs
     void* out_act = nullptr;     // EPI_SWIGLU output, element type act_dtype
     int act_dtype = DT_F32;
     int64_t ld_act = 0;
@@ -74,9 +75,10 @@ cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, 
 
 // Ingest normalisation: H = RMSNorm(P) * ctx_norm, then for each layer i
 // N_i = RMSNorm(H) * attn_norm_i, written to out + i * layer_stride (out_dtype).
-cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
-                        const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
-                        int64_t layer_stride, cudaStream_t st);
+// P holds nsplit partial products (K ranges) at P + s * split_stride; they are summed first.
+cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int rows, int d, float eps,
+                        const float* ctx_norm, const float* const* attn_norm_dev, int n_layers, int out_dtype,
+                        void* out, int64_t layer_stride, cudaStream_t st);
 
 // x[b * gamma + j] = block_const[j] for b < B, j < gamma (fp32).
 cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st);

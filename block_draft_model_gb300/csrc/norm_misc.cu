@@ -50,7 +50,8 @@ __device__ __forceinline__ void store4(float* o, float a, float b, float c, floa
 constexpr int INW = 8;  // warps per CTA
 
 template <typename TO, int MAXV>
-__global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int rows, int d, float eps,
+__global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int nsplit, int64_t split_stride,
+                                                         int rows, int d, float eps,
                                                          const float* __restrict__ ctx_norm,
                                                          const float* const* __restrict__ attn_norm, int n_layers,
                                                          TO* out, int64_t layer_stride, int rows_per_warp) {
@@ -77,8 +78,20 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
         for (int i = 0; i < MAXV; ++i) {
             const int v = lane + 32 * i;
             h[i] = v < nv ? pr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
-            ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
         }
+        for (int sp = 1; sp < nsplit; ++sp) {  // partial products of the other K ranges
+            const float4* ps = reinterpret_cast<const float4*>(P + sp * split_stride + (int64_t)row * d);
+#pragma unroll
+            for (int i = 0; i < MAXV; ++i) {
+                const int v = lane + 32 * i;
+                if (v < nv) {
+                    const float4 a = ps[v];
+                    h[i] = make_float4(h[i].x + a.x, h[i].y + a.y, h[i].z + a.z, h[i].w + a.w);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < MAXV; ++i) ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
         ss = warp_sum(ss);
         const float s1 = rsqrtf(ss / (float)d + eps);
         const float4* cn = reinterpret_cast<const float4*>(wsm);
@@ -253,7 +266,8 @@ cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, 
 }
 
 template <typename TO, int MAXV>
-cudaError_t launch_ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
+cudaError_t launch_ingest_norm(const float* P, int nsplit, int64_t split_stride, int rows, int d, float eps,
+                               const float* ctx_norm,
                                const float* const* attn_norm_dev, int n_layers, void* out, int64_t layer_stride,
                                cudaStream_t st) {
     const size_t sm = (size_t)(n_layers + 1) * d * sizeof(float);
@@ -270,32 +284,36 @@ cudaError_t launch_ingest_norm(const float* P, int rows, int d, float eps, const
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int rpw = std::max(1, (rows + INW * 2 * sms - 1) / (INW * 2 * sms));
     const int blocks = (rows + INW * rpw - 1) / (INW * rpw);
-    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, sm, st, P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers,
-           (TO*)out, layer_stride, rpw);
+    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, sm, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
+           attn_norm_dev, n_layers, (TO*)out, layer_stride, rpw);
     note_launch();
     return cudaGetLastError();
 }
 
 template <typename TO>
-cudaError_t ingest_norm_t(const float* P, int rows, int d, float eps, const float* ctx_norm,
+cudaError_t ingest_norm_t(const float* P, int nsplit, int64_t split_stride, int rows, int d, float eps,
+                          const float* ctx_norm,
                           const float* const* attn_norm_dev, int n_layers, void* out, int64_t layer_stride,
                           cudaStream_t st) {
     const int per_lane = (d / 4 + 31) / 32;
-    if (per_lane <= 2) return launch_ingest_norm<TO, 2>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
-    if (per_lane <= 4) return launch_ingest_norm<TO, 4>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
-    if (per_lane <= 8) return launch_ingest_norm<TO, 8>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
-    if (per_lane <= 16) return launch_ingest_norm<TO, 16>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
-    return launch_ingest_norm<TO, 32>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 2) return launch_ingest_norm<TO, 2>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 4) return launch_ingest_norm<TO, 4>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 8) return launch_ingest_norm<TO, 8>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    if (per_lane <= 16) return launch_ingest_norm<TO, 16>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+    return launch_ingest_norm<TO, 32>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
 }
 
-cudaError_t ingest_norm(const float* P, int rows, int d, float eps, const float* ctx_norm,
-                        const float* const* attn_norm_dev, int n_layers, int out_dtype, void* out,
-                        int64_t layer_stride, cudaStream_t st) {
+cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int rows, int d, float eps,
+                        const float* ctx_norm, const float* const* attn_norm_dev, int n_layers, int out_dtype,
+                        void* out, int64_t layer_stride, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
+    if (nsplit < 1 || (nsplit > 1 && split_stride < (int64_t)rows * d)) return cudaErrorInvalidValue;
     if (d % 4 != 0 || d > 4096 || (size_t)(n_layers + 1) * d * sizeof(float) > 200 * 1024) return cudaErrorInvalidValue;
     if (out_dtype == DT_BF16)
-        return ingest_norm_t<bf16>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
-    return ingest_norm_t<float>(P, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out, layer_stride, st);
+        return ingest_norm_t<bf16>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out,
+                                   layer_stride, st);
+    return ingest_norm_t<float>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out,
+                                layer_stride, st);
 }
 
 cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st) {

@@ -40,7 +40,10 @@ constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTE
 struct TileMap {
     int nM, nN;
     bool n_fast;
-    __device__ __forceinline__ void at(int t, int& m0, int& n0) const {
+    int ks;  // K ranges per output tile (consecutive work units)
+    __device__ __forceinline__ void at(int t, int& m0, int& n0, int& s) const {
+        s = t % ks;
+        t /= ks;
         int mi, ni;
         if (n_fast) {
             mi = t / nN;
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = tm.nM * tm.nN;
+    const int tiles = tm.nM * tm.nN * tm.ks;
     const int nkb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -109,9 +112,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                int m0, n0;
-                tm.at(t, m0, n0);
-                for (int kb = 0; kb < nkb; ++kb) {
+                int m0, n0, s;
+                tm.at(t, m0, n0, s);
+                const int kb1 = (s + 1) * nkb / tm.ks;
+                for (int kb = s * nkb / tm.ks; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -135,13 +139,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                int m0, n0;
-                tm.at(t, m0, n0);
+                int m0, n0, s;
+                tm.at(t, m0, n0, s);
+                const int kb0 = s * nkb / tm.ks, kb1 = (s + 1) * nkb / tm.ks;
                 // a narrow last (or only) column tile multiplies only its 16-aligned width
                 const int n_rem = N - n0;
                 const uint32_t id = idesc(BM, n_rem >= BN ? BN : (n_rem + 15) & ~15);
                 const uint32_t d_tmem = tmem + buf * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint64_t db = sdesc(sB + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)  // +32 bytes per 16-wide K slice inside the swizzled row
-                        umma(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb | k) ? 1u : 0u);
+                        umma(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > kb0 || k) ? 1u : 0u);
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -178,11 +183,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int buf = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-            int m0, n0;
-            tm.at(t, m0, n0);
+            int m0, n0, s;
+            tm.at(t, m0, n0, s);
             if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) break;
             tc_fence_after();
             const int row = m0 + q * 32 + lane;
+            const int orow = row + s * ep.split_rows;  // output row (K range s of a split product)
             const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi_row32(ep, row, nb, N, v);
+                    epi_row32(ep, orow, nb, N, v);
                 }
             }
             tc_fence_before();
@@ -277,8 +283,10 @@ void tc_release(TcWeight& w) { w.ready = false; }
 bool tc_gemm_ok(int M, int N, int K) { return g_state == 1 && M >= 1 && N >= 1 && K >= BK && K % 8 == 0; }
 
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
-                    int num_sms, int* err, cudaStream_t st) {
+                    int num_sms, int* err, cudaStream_t st, int ksplit) {
     if (!w.ready || !tc_gemm_ok(M, N, K) || N > w.N || K != w.K) return cudaErrorInvalidValue;
+    if (ksplit < 1 || (ksplit > 1 && (ep.kind != EPI_STORE_F32 || ep.split_rows < M || ksplit > (K + BK - 1) / BK)))
+        return cudaErrorInvalidValue;
     if (lda % 8 != 0 || ((uintptr_t)A & 15) != 0) return cudaErrorInvalidValue;
     CUtensorMap tmA;
     if (!encode(&tmA, A, M, K, lda, BM)) return cudaErrorInvalidValue;
@@ -286,7 +294,8 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.nM = (M + BM - 1) / BM;
     tm.nN = (N + BN - 1) / BN;
     tm.n_fast = tm.nN <= tm.nM;
-    const int tiles = tm.nM * tm.nN;
+    tm.ks = ksplit;
+    const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
     launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
     note_launch();

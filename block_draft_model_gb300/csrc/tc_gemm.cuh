@@ -23,8 +23,11 @@ void tc_release(TcWeight& w);
 bool tc_gemm_ok(int M, int N, int K);
 // A: [M, K] bf16 with row stride lda (16-byte aligned).  A bounded device wait
 // that gives up sets bit 16 of *err (the handle's device error word).
+// ksplit > 1 (EPI_STORE_F32 only) cuts K into ksplit ranges, each a separate
+// work unit: range s stores its partial product at rows s * ep.split_rows + m
+// of ep.out_f32, and the consumer sums the ranges.
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
-                    int num_sms, int* err, cudaStream_t st);
+                    int num_sms, int* err, cudaStream_t st, int ksplit = 1);
 
 // Weight-streaming variant for M <= 16 activation rows (tc_stream.cu): the
 // weights are the MMA's 128-row side.  `part`/`tickets` are scratch for the

@@ -204,6 +204,15 @@ def test_batched_many_sequences_ragged_vocab():
                     label=f"seq {i} (L {lens[i]})")
 
 
+def test_ingest_projection_split_over_k():
+    """A context projection with few output tiles (300 rows, d 256) and a long
+    K (4 taps x 512): the tensor-core GEMM cuts K into ranges whose partial
+    products the normalisation sums."""
+    cfg = syn.DrafterConfig(hidden=512, n_taps=4, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=4,
+                            vocab=600, markov_rank=32)
+    _small(cfg, 300, seed=14, chunks=[], anchors=[3, 599])
+
+
 @pytest.mark.parametrize("n_seq,rank,vocab", [(3, 64, 1000), (1, 128, 5003), (7, 256, 2048)])
 def test_markov_chain_few_sequences(n_seq, rank, vocab):
     """1 to 7 sequences with r in {64, 128, 256}: the whole Markov chain in one
