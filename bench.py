@@ -169,6 +169,9 @@ def class_work(cls: str, cfg, T: int, L_total: int, B: int):
         return dict(bytes=2 * F * d * 2, flops=2 * rows * 2 * F * d, bound=gemm_bound)
     if cls == "down_proj":
         return dict(bytes=F * d * 2, flops=2 * rows * F * d, bound=gemm_bound)
+    if cls == "draft_layers":  # every layer of a batch-1 draft in one launch
+        return dict(bytes=nL * ((4 * d * d + 3 * F * d) * 2 + 2 * (L_total + rows) * d * 2),
+                    flops=nL * (2 * rows * (4 * d * d + 3 * F * d) + 4 * g * (L_total + rows) * d), bound="hbm")
     if cls == "block_build":
         return dict(bytes=d * H * 2, flops=2 * B * d * H, bound="hbm")
     return dict(bytes=0, flops=0, bound="hbm")

@@ -27,11 +27,11 @@ struct DevBuf {
 // Kernel classes of the step, timed by dspark_profile.
 enum Cat {
     CAT_INGEST_PROJ, CAT_INGEST_NORM, CAT_INGEST_KV, CAT_BLOCK, CAT_NORM, CAT_QKV, CAT_ATTN, CAT_O, CAT_GATE_UP,
-    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_COUNT
+    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_LAYERS, CAT_COUNT
 };
 const char* const kCatNames[CAT_COUNT] = {"ingest_proj", "ingest_norm", "ingest_kv", "block_build", "rmsnorm",
                                           "qkv_proj", "attention", "o_proj", "gate_up_proj", "down_proj",
-                                          "out_proj", "markov_argmax"};
+                                          "out_proj", "markov_argmax", "draft_layers"};
 
 struct ProfRange {
     int cat;
@@ -116,6 +116,10 @@ struct dspark_handle {
     int* mk_pi = nullptr;
     unsigned int* mk_bar = nullptr;          // [2] grid-barrier words, then the chain's launch epoch
     unsigned long long* mk_keys = nullptr;   // [2, max_seqs, 16] argmax words of the Markov chain, then 2 counters
+    unsigned long long* pk_bar = nullptr;    // persistent draft layers: 2 barrier counters, then the launch epoch
+    void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
+    int pk_map3d = 0;
+    bool use_persistent = true;
     float* ws = nullptr;
     size_t ws_floats = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
@@ -398,7 +402,53 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
     void* actA = lowp ? h->act_lp : (void*)h->act;
     const int adt = lowp ? DT_BF16 : DT_F32;
-    for (int i = 0; i < c.n_layers; ++i) {
+    bool layers_done = false;
+    // One persistent launch for every layer pays off while a layer's weights are
+    // a few slices per SM (its projections run on the legacy warp MMA); larger
+    // layers stream faster through the per-kernel tcgen05 path.
+    const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
+    const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
+    if (B == 1 && !seq_ids && lowp && h->use_persistent && persistent_fits) {
+        // every layer in one persistent launch
+        DraftPersistArgs a{};
+        a.x = h->x;
+        a.q = h->q;
+        a.act = h->act_lp;
+        a.hact = h->h_lp;
+        a.part = h->attn_part;
+        a.cache = h->cache;
+        a.layer_stride = h->layer_stride;
+        a.kv_off = h->kv_off;
+        a.max_rows = (int)h->rows;
+        a.seq_len = h->d_len;
+        a.wqkv = h->wqkv.data();
+        a.wo = h->wo.data();
+        a.wgu = h->wgu.data();
+        a.wd = h->wd.data();
+        a.attn_norm = h->attn_norm.data();
+        a.ff_norm = h->ff_norm.data();
+        a.d = d;
+        a.F = F;
+        a.nh = c.n_heads;
+        a.nL = c.n_layers;
+        a.gamma = c.gamma;
+        a.act_kind = c.act;
+        a.nchunks = std::max(1, std::min({32, h->num_sms / c.n_heads, (max_keys + 63) / 64}));
+        a.eps = c.eps;
+        a.maps = h->pk_maps;
+        a.map3d = h->pk_map3d;
+        a.bar = h->pk_bar;
+        a.epoch = reinterpret_cast<unsigned int*>(h->pk_bar + 2);
+        a.err = h->d_err;
+        if (draft_persistent_ok(a) &&
+            attn_scratch_floats(1, c.n_heads, a.nchunks, c.gamma, h->hd) <= h->attn_part_floats) {
+            pr_block.end();
+            Prof pr(h, CAT_LAYERS, st);
+            CUDA_TRY(h, draft_persistent(a, h->num_sms, st));
+            layers_done = true;
+        }
+    }
+    for (int i = 0; i < c.n_layers && !layers_done; ++i) {
         if (i == 0) pr_block.end();
         {
             Prof pr(h, CAT_NORM, st);
@@ -929,6 +979,31 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, (void**)&h->anchor_dev, sizeof(int)));
     CTRY(attention_init());
     CTRY(markov_chain_resident_init());
+    CTRY(draft_persistent_init());
+    CTRY(dalloc(h, (void**)&h->pk_bar, 3 * sizeof(unsigned long long)));
+    CTRY(cudaMemsetAsync(h->pk_bar, 0, 3 * sizeof(unsigned long long), st));
+    if (h->dt == DT_BF16 && d % 512 == 0 && F % 512 == 0 && tc_available()) {
+        // weight-slice tensor maps of the persistent draft layers (3-D if the driver takes it)
+        struct alignas(64) Map128 {
+            unsigned char b[128];
+        };
+        std::vector<Map128> maps((size_t)4 * nL);
+        for (int three = 1; three >= 0 && !h->pk_maps; --three) {
+            bool ok = true;
+            for (int i = 0; i < nL && ok; ++i) {
+                ok = tc_encode_slot_map(&maps[4 * i + 0], h->wqkv[i], 3 * (int64_t)d, d, three) &&
+                     tc_encode_slot_map(&maps[4 * i + 1], h->wo[i], d, d, three) &&
+                     tc_encode_slot_map(&maps[4 * i + 2], h->wgu[i], 2 * (int64_t)F, d, three) &&
+                     tc_encode_slot_map(&maps[4 * i + 3], h->wd[i], d, F, three);
+            }
+            if (!ok) continue;
+            CTRY(dalloc(h, &h->pk_maps, maps.size() * sizeof(Map128)));
+            CTRY(cudaMemcpyAsync(h->pk_maps, maps.data(), maps.size() * sizeof(Map128), cudaMemcpyHostToDevice, st));
+            CTRY(cudaStreamSynchronize(st));  // the host array goes out of scope
+            h->pk_map3d = three;
+        }
+    }
+    if (const char* env = getenv("DSPARK_NO_PERSISTENT")) h->use_persistent = env[0] == '0';
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));

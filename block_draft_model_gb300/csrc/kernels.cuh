@@ -118,6 +118,39 @@ int attention_tc_max_chunks();
 cudaError_t attention_tc_init();
 cudaError_t attention_tc(const AttnParams& p, cudaStream_t st);
 
+// ------------------------------------------------------------------ persistent draft layers
+// Every draft layer of sequence slot 0 (batch 1, bf16) in one cooperative launch,
+// one CTA per SM: x (the block rows after the block build) -> x after the last
+// layer; Q, the block's K/V cache rows, the attention output and the SwiGLU
+// output pass through q, the cache, act and hact.  Host arrays of layer pointers.
+struct DraftPersistArgs {
+    float* x;
+    float* q;
+    void* act;                  // [gamma, d] bf16
+    void* hact;                 // [gamma, F] bf16
+    float* part;                // n_heads * nchunks * gamma * (head_dim + 4) floats
+    void* cache;                // layer 0 base (bf16), slot 0
+    int64_t layer_stride, kv_off;
+    int max_rows;
+    const int* seq_len;         // device; entry 0
+    const void* const* wqkv;    // [n_layers] of [3d, d]
+    const void* const* wo;      // [n_layers] of [d, d]
+    const void* const* wgu;     // [n_layers] of [2F, d], rows (gate f, up f) interleaved
+    const void* const* wd;      // [n_layers] of [d, F]
+    const float* const* attn_norm;
+    const float* const* ff_norm;
+    int d, F, nh, nL, gamma, act_kind, nchunks;
+    float eps;
+    const void* maps;           // device [n_layers][4] slot tensor maps (tc_encode_slot_map) of wqkv, wo, wgu, wd
+    int map3d;                  // the maps are 3-D
+    unsigned long long* bar;    // 2 zero-initialised words
+    unsigned int* epoch;        // zero-initialised
+    int* err;
+};
+cudaError_t draft_persistent_init();  // once per process/device
+bool draft_persistent_ok(const DraftPersistArgs& a);
+cudaError_t draft_persistent(const DraftPersistArgs& a, int num_sms, cudaStream_t st);
+
 // ------------------------------------------------------------------ Markov chain, argmax, confidence
 struct MarkovParams {
     const float* U;          // [B*gamma, V] base logits

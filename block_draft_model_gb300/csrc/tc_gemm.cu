@@ -266,6 +266,30 @@ bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64
 
 bool tc_available() { return init_encode(); }
 
+bool tc_encode_slot_map(void* map, const void* W, int64_t rows, int64_t K, bool three_d) {
+    if (!init_encode() || K % 512 != 0 || ((uintptr_t)W & 15) != 0) return false;
+    CUresult r;
+    if (three_d) {
+        // (64 elements of a 128-byte column block, row, column block): one box = 16 rows x 512
+        cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)(K * 2), 128};
+        cuuint32_t box[3] = {64, 16, 8};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = g_encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+        cuuint32_t box[2] = {64, 16};
+        cuuint32_t estr[2] = {1, 1};
+        r = g_encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K) {
     w.ready = false;
     w.ptr = ptr;

@@ -18,6 +18,11 @@ struct TcWeight {
 };
 
 bool tc_available();
+// Tensor map (128 bytes at `map`, host memory) over a bf16 weight [rows, K] whose
+// one box is a 16-row x 512-column slice laid out as 8 column blocks of
+// [16 rows][64] with the 128-byte swizzle: a 3-D map (one copy per slice) or,
+// with three_d false, a 2-D map with [16][64] boxes (eight copies per slice).
+bool tc_encode_slot_map(void* map, const void* W, int64_t rows, int64_t K, bool three_d);
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K);
 void tc_release(TcWeight& w);
 bool tc_gemm_ok(int M, int N, int K);

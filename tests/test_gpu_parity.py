@@ -204,6 +204,21 @@ def test_batched_many_sequences_ragged_vocab():
                     label=f"seq {i} (L {lens[i]})")
 
 
+@pytest.mark.parametrize("n_heads,gamma,L", [(4, 5, 300), (8, 12, 50), (4, 8, 1500)])
+def test_persistent_draft_layers(n_heads, gamma, L):
+    """Shapes the one-launch draft layers take (d and F multiples of 512, head
+    dim 64 or 128): one or two 8-row block tiles, one key range (no merge) and
+    many key ranges (merged), three draws in a row on the same handle."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=512, n_heads=n_heads, n_layers=2, ff_mult=2, gamma=gamma,
+                            vocab=1000, markov_rank=32)
+    dr, gdr, _ = _small(cfg, L, seed=15, chunks=[L // 2], anchors=[1, 998, 500], max_ctx=L + 16)
+    X = syn.make_feats(cfg, 3, seed=16)
+    dr.ingest(X)
+    gdr.ingest_context(to_torch(X))
+    tok, conf, lg = _draft(gdr, cfg, 77)
+    check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
+
+
 def test_ingest_projection_split_over_k():
     """A context projection with few output tiles (300 rows, d 256) and a long
     K (4 taps x 512): the tensor-core GEMM cuts K into ranges whose partial
