@@ -203,23 +203,26 @@ def load_peaks():
 
 
 def load_traffic(kernel_class: str, workload: str):
-    """DRAM bytes per range from a committed ncu summary, if it still matches the kernel source."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
-        with open(p) as f:
-            table = json.load(f)
-    except (OSError, ValueError):
-        return None
-    ent = table.get(f"{workload}/{kernel_class}")
-    if not ent:
-        return None
+    """DRAM bytes per range from the committed ncu traffic table (profiles/traffic.md),
+    if its row still matches the kernel source."""
     import hashlib
-    src = os.path.join(ROOT, ent["source"])
+    p = os.path.join(ROOT, "profiles", "traffic.md")
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        lines = open(p).read().splitlines()
     except OSError:
         return None
-    return ent["bytes_per_range"] if digest == ent.get("source_sha") else None
+    for ln in lines:
+        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+        if len(cells) != 7 or cells[0] != workload or cells[1] != kernel_class:
+            continue
+        try:
+            digest = hashlib.sha256(open(os.path.join(ROOT, cells[2]), "rb").read()).hexdigest()[:16]
+            if digest != cells[3]:
+                return None
+            return int(cells[4]) * int(cells[5])
+        except (OSError, ValueError):
+            return None
+    return None
 
 
 def cpu_cores():
