@@ -83,6 +83,7 @@ struct dspark_handle {
     float* conf_wb = nullptr;                // [d + r + 1]
     TcWeight tc_wc, tc_out_proj;             // tensor-core views (bf16 only), rows >= 17
     std::vector<TcWeight> tc_kv, tc_qkv, tc_wo, tc_wgu, tc_wd;
+    TcWeight tc_kv_a, tc_kv_w;               // every layer's ingest K/V product as one grouped GEMM (A: Nbuf)
     TcWeightStream ts_wc, ts_out_proj;       // weight-streaming tensor-core views, rows <= 16
     std::vector<TcWeightStream> ts_kv, ts_qkv, ts_wo, ts_wgu, ts_wd;
     float* ts_part = nullptr;                // split-K partials of the streaming GEMM
@@ -360,6 +361,19 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
                                     h->Nbuf, (int64_t)h->ingest_rows * d, st));
         }
         Prof pr_kv(h, CAT_INGEST_KV, st);
+        if (n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * d, d)) {
+            // all layers in one launch: [nL x row tiles x column tiles] work units
+            EpiParams kv = cache_epi(h, 0);
+            kv.kind = EPI_KV_CACHE;
+            kv.group_stride = h->layer_stride;
+            if (row_seq) {
+                kv.row_seq = row_seq + t0;
+                kv.row_pos = row_pos + t0;
+            }
+            CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * d, d, kv, h->num_sms, h->d_err, st));
+            if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
+            continue;
+        }
         for (int i = 0; i < nL; ++i) {
             EpiParams kv = cache_epi(h, i);
             kv.kind = EPI_KV_CACHE;
@@ -908,7 +922,8 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->ff_norm.resize(nL);
     for (int i = 0; i < nL; ++i) {
         const size_t dd = (size_t)d * d;
-        CTRY(dalloc(h, &h->wqkv[i], 3 * dd * es));
+        if (i == 0) CTRY(dalloc(h, &h->wqkv[0], (size_t)nL * 3 * dd * es));  // layers back to back
+        else h->wqkv[i] = (char*)h->wqkv[0] + (size_t)i * 3 * dd * es;
         CTRY(cudaMemcpyAsync(h->wqkv[i], w->wq[i], dd * es, cudaMemcpyDeviceToDevice, st));
         CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + dd * es, w->wk[i], dd * es, cudaMemcpyDeviceToDevice, st));
         CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + 2 * dd * es, w->wv[i], dd * es, cudaMemcpyDeviceToDevice, st));
@@ -1027,6 +1042,11 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         h->tc_wd.resize(nL);
         for (int i = 0; i < nL; ++i) {
             CTRY(tc_prepare(h->tc_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * d, d));
+            if (i == 0) {
+                tc_prepare_grouped(h->tc_kv_a, h->Nbuf, nL, (int64_t)h->ingest_rows * d, h->ingest_rows, d, true);
+                tc_prepare_grouped(h->tc_kv_w, (char*)h->wqkv[0] + (size_t)d * d * es, nL, 3 * (int64_t)d * d, 2 * d, d,
+                                   false);
+            }
             CTRY(tc_prepare(h->tc_qkv[i], h->wqkv[i], 3 * d, d));
             CTRY(tc_prepare(h->tc_wo[i], h->wo[i], d, d));
             CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));

@@ -14,9 +14,10 @@ __device__ __forceinline__ float act_fn(int act, float g) {
     return 0.5f * g * (1.f + tanhf(c * (g + 0.044715f * g * g * g)));
 }
 
-__device__ __forceinline__ void cache_store(const EpiParams& ep, int slot, int pos, int c, float v) {
+__device__ __forceinline__ void cache_store(const EpiParams& ep, int slot, int pos, int c, float v, int grp = 0) {
     if (pos < 0 || pos >= ep.max_rows) return;
-    int64_t off = (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) + (int64_t)pos * ep.d + (c % ep.d);
+    int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) +
+                  (int64_t)pos * ep.d + (c % ep.d);
     if (ep.cache_dtype == DT_BF16)
         reinterpret_cast<bf16*>(ep.cache)[off] = __float2bfloat16_rn(v);
     else
@@ -24,7 +25,7 @@ __device__ __forceinline__ void cache_store(const EpiParams& ep, int slot, int p
 }
 
 // One output element (every kind except EPI_SWIGLU).
-__device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float v) {
+__device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float v, int grp = 0) {
     switch (ep.kind) {
         case EPI_STORE_F32:
             ep.out_f32[(int64_t)m * ep.ldo + n] = v;
@@ -35,7 +36,7 @@ __device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float
         case EPI_KV_CACHE: {
             int slot = ep.row_seq ? ep.row_seq[m] : 0;
             int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
-            cache_store(ep, slot, pos, n, v);
+            cache_store(ep, slot, pos, n, v, grp);
             break;
         }
         case EPI_QKV: {
@@ -85,9 +86,11 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-__device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int pos, int c, const float* v) {
+__device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int pos, int c, const float* v,
+                                              int grp = 0) {
     if (pos < 0 || pos >= ep.max_rows) return;
-    const int64_t off = (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) + (int64_t)pos * ep.d + (c % ep.d);
+    const int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) +
+                        (int64_t)pos * ep.d + (c % ep.d);
     if (ep.cache_dtype == DT_BF16) store_bf16x32(reinterpret_cast<bf16*>(ep.cache) + off, v);
     else store_f32x32(reinterpret_cast<float*>(ep.cache) + off, v);
 }
@@ -143,7 +146,7 @@ __device__ __forceinline__ void markov_t32(const EpiParams& ep, int vrow, bool v
     }
 }
 
-__device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v) {
+__device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v, int grp = 0) {
     const bool full = n + 32 <= N;
     switch (ep.kind) {
         case EPI_STORE_F32:
@@ -172,7 +175,7 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
             if (full && (ep.d & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
                 const int slot = ep.row_seq ? ep.row_seq[m] : 0;
                 const int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
-                cache_store32(ep, slot, pos, n, v);
+                cache_store32(ep, slot, pos, n, v, grp);
                 return;
             }
             break;
@@ -228,7 +231,7 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (n + j < N) epi_one(ep, m, n + j, v[j]);
+            if (n + j < N) epi_one(ep, m, n + j, v[j], grp);
     }
 }
 

@@ -27,6 +27,7 @@ struct EpiParams {
     float* out_f32 = nullptr;
     int64_t ldo = 0;
     int split_rows = 0;          // EPI_STORE_F32 of a K-split tensor-core GEMM: rows between the ranges' outputs
+    int64_t group_stride = 0;    // EPI_KV_CACHE of a grouped tensor-core GEMM: cache elements between groups
     void* out_act = nullptr;     // EPI_SWIGLU output, element type act_dtype
     int act_dtype = DT_F32;
     int64_t ld_act = 0;

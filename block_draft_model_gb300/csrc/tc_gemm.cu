@@ -40,8 +40,13 @@ constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTE
 struct TileMap {
     int nM, nN;
     bool n_fast;
-    int ks;  // K ranges per output tile (consecutive work units)
-    __device__ __forceinline__ void at(int t, int& m0, int& n0, int& s) const {
+    int ks;      // K ranges per output tile (consecutive work units)
+    int groups;  // independent problems of the same shape (third map coordinate = group)
+    int map3d;   // the tensor maps are 3-D (grouped launches, also with one group)
+    __device__ __forceinline__ void at(int t, int& m0, int& n0, int& s, int& g) const {
+        const int per = nM * nN * ks;
+        g = t / per;
+        t -= g * per;
         s = t % ks;
         t /= ks;
         int mi, ni;
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = tm.nM * tm.nN * tm.ks;
+    const int tiles = tm.nM * tm.nN * tm.ks * tm.groups;
     const int nkb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -112,8 +117,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                int m0, n0, s;
-                tm.at(t, m0, n0, s);
+                int m0, n0, s, g;
+                tm.at(t, m0, n0, s, g);
                 const int kb1 = (s + 1) * nkb / tm.ks;
                 for (int kb = s * nkb / tm.ks; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -121,8 +126,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    if (tm.map3d) {
+                        tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0, g);
+                        tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0, g);
+                    } else {
+                        tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
+                        tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -139,8 +149,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                int m0, n0, s;
-                tm.at(t, m0, n0, s);
+                int m0, n0, s, g;
+                tm.at(t, m0, n0, s, g);
                 const int kb0 = s * nkb / tm.ks, kb1 = (s + 1) * nkb / tm.ks;
                 // a narrow last (or only) column tile multiplies only its 16-aligned width
                 const int n_rem = N - n0;
@@ -183,8 +193,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int buf = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-            int m0, n0, s;
-            tm.at(t, m0, n0, s);
+            int m0, n0, s, g;
+            tm.at(t, m0, n0, s, g);
             if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) break;
             tc_fence_after();
             const int row = m0 + q * 32 + lane;
@@ -207,7 +217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi_row32(ep, orow, nb, N, v);
+                    epi_row32(ep, orow, nb, N, v, g);
                 }
             }
             tc_fence_before();
@@ -266,6 +276,42 @@ bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64
 
 bool tc_available() { return init_encode(); }
 
+bool tc_prepare_grouped(TcWeight& w, const void* ptr, int groups, int64_t group_stride, int rows, int K, bool a_side) {
+    w.ready = false;
+    w.ptr = ptr;
+    w.N = rows;
+    w.K = K;
+    if (!init_encode() || groups < 1 || K % 8 != 0 || ((uintptr_t)ptr & 15) != 0 || group_stride % 8 != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)groups};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)group_stride * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)(a_side ? BM : BN), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(w.tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    w.ready = r == CUDA_SUCCESS;
+    return w.ready;
+}
+
+cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, int M, int N, int K, const EpiParams& ep,
+                            int num_sms, int* err, cudaStream_t st) {
+    if (!a.ready || !w.ready || groups < 1 || !tc_gemm_ok(M, N, K) || M > a.N || N > w.N || K != w.K || K != a.K)
+        return cudaErrorInvalidValue;
+    TileMap tm;
+    tm.nM = (M + BM - 1) / BM;
+    tm.nN = (N + BN - 1) / BN;
+    tm.n_fast = tm.nN <= tm.nM;
+    tm.ks = 1;
+    tm.groups = groups;
+    tm.map3d = 1;
+    const int tiles = tm.nM * tm.nN * groups;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, *reinterpret_cast<const CUtensorMap*>(a.tmap),
+           *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
+    note_launch();
+    return cudaGetLastError();
+}
+
 bool tc_encode_slot_map(void* map, const void* W, int64_t rows, int64_t K, bool three_d) {
     if (!init_encode() || K % 512 != 0 || ((uintptr_t)W & 15) != 0) return false;
     CUresult r;
@@ -319,6 +365,8 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.nN = (N + BN - 1) / BN;
     tm.n_fast = tm.nN <= tm.nM;
     tm.ks = ksplit;
+    tm.groups = 1;
+    tm.map3d = 0;
     const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
     launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);

@@ -26,6 +26,13 @@ bool tc_encode_slot_map(void* map, const void* W, int64_t rows, int64_t K, bool 
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K);
 void tc_release(TcWeight& w);
 bool tc_gemm_ok(int M, int N, int K);
+// `groups` problems of one shape in one launch: acc_g = A_g . W_g^T.  Both sides are
+// 3-D views (bf16 rows of K, group g at ptr + g * group_stride elements) made by
+// tc_prepare_grouped (a_side: 128-row boxes of A, else 256-row boxes of W); the
+// EPI_KV_CACHE epilogue of group g writes at ep.cache + g * ep.group_stride.
+bool tc_prepare_grouped(TcWeight& w, const void* ptr, int groups, int64_t group_stride, int rows, int K, bool a_side);
+cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, int M, int N, int K, const EpiParams& ep,
+                            int num_sms, int* err, cudaStream_t st);
 // A: [M, K] bf16 with row stride lda (16-byte aligned).  A bounded device wait
 // that gives up sets bit 16 of *err (the handle's device error word).
 // ksplit > 1 (EPI_STORE_F32 only) cuts K into ksplit ranges, each a separate
