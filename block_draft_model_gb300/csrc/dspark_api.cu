@@ -121,6 +121,7 @@ struct dspark_handle {
     void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
     int pk_map3d = 0;
     bool use_persistent = true;
+    bool fuse_norm = false;                  // RMSNorm folded into the weight-streaming projections
     float* ws = nullptr;
     size_t ws_floats = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
@@ -229,6 +230,14 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     return gemm_simt(a_dtype, a, lda, a_rows, h->dt, W, M, N, K, ep, st);
 }
 
+// RMSNorm(x) * w for the R block rows, then (that) . W^T.  Where the weight-streaming
+// tensor-core kernel runs the product, the normalisation is folded into it (the
+// operand is x * w, the row scale multiplies the accumulator); otherwise a
+// normalisation kernel writes the operand to actA first.
+cudaError_t norm_gemm(dspark_handle* h, const float* w, int R, const WView& wv, int N, int K, const EpiParams& ep,
+                      void* actA, int adt, cudaStream_t st, int norm_cat);
+
+
 // Next event of the handle's reusable timing-event pool (nullptr if none can be made).
 cudaEvent_t pool_event(dspark_handle* h) {
     if (h->prof_next >= h->prof_pool.size()) {
@@ -275,6 +284,28 @@ struct Prof {
     }
     ~Prof() { end(); }
 };
+
+cudaError_t norm_gemm(dspark_handle* h, const float* w, int R, const WView& wv, int N, int K, const EpiParams& ep,
+                      void* actA, int adt, cudaStream_t st, int norm_cat) {
+    const int d = h->d;
+    // Opt-in: every CTA then rebuilds the normalised rows and their scales from the whole row of
+    // x before its first MMA, which measured slower than the separate normalisation launch on
+    // both the draft layers and the vocabulary projection.
+    if (h->fuse_norm && adt == DT_BF16 && R <= 16 && wv.ts && wv.ts->ready && tc_stream_ok(R, N, K) &&
+        K % 64 == 0 && K == d) {
+        Prof pr(h, norm_cat, st);
+        const StreamNorm sn{h->x, w, (int64_t)d, h->cfg.eps};
+        return tc_stream(nullptr, 0, *wv.ts, R, N, K, ep, h->ts_part, h->ts_part_floats, h->ts_tickets,
+                         h->ts_n_tickets, h->num_sms, h->d_err, st, &sn);
+    }
+    {
+        Prof pr(h, CAT_NORM, st);
+        cudaError_t e = rmsnorm_rows(h->x, d, w, R, d, h->cfg.eps, adt, actA, d, st);
+        if (e != cudaSuccess) return e;
+    }
+    Prof pr(h, norm_cat, st);
+    return gemm(h, adt, actA, d, nullptr, 0, wv, R, N, K, ep, st);
+}
 
 EpiParams cache_epi(const dspark_handle* h, int layer) {
     EpiParams ep;
@@ -464,22 +495,15 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     }
     for (int i = 0; i < c.n_layers && !layers_done; ++i) {
         if (i == 0) pr_block.end();
-        {
-            Prof pr(h, CAT_NORM, st);
-            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->attn_norm[i], R, d, c.eps, adt, actA, d, st));
-        }
         EpiParams qkv = cache_epi(h, i);
         qkv.kind = EPI_QKV;
         qkv.out_f32 = h->q;
         qkv.ldo = d;
         qkv.gamma = c.gamma;
         qkv.seq_ids = seq_ids;
-        {
-            Prof pr(h, CAT_QKV, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
-                             WView{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)}, R, 3 * d, d, qkv,
-                             st));
-        }
+        CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R,
+                              WView{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)}, 3 * d, d, qkv,
+                              actA, adt, st, CAT_QKV));
         AttnParams ap;
         ap.q = h->q;
         ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
@@ -512,22 +536,15 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
                              WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
         }
-        {
-            Prof pr(h, CAT_NORM, st);
-            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->ff_norm[i], R, d, c.eps, adt, actA, d, st));
-        }
         EpiParams sw;
         sw.kind = EPI_SWIGLU;
         sw.out_act = lowp ? h->h_lp : (void*)h->hbuf;
         sw.act_dtype = adt;
         sw.ld_act = F;
         sw.act = c.act;
-        {
-            Prof pr(h, CAT_GATE_UP, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
-                             WView{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)}, R, 2 * F, d, sw,
-                             st));
-        }
+        CUDA_TRY(h, norm_gemm(h, h->ff_norm[i], R,
+                              WView{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)}, 2 * F, d, sw, actA,
+                              adt, st, CAT_GATE_UP));
         {
             Prof pr(h, CAT_DOWN, st);
             CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
@@ -544,15 +561,13 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ep.kind = EPI_STORE_F32;
         ep.out_f32 = h->U;
         ep.ldo = V;
-        const void* A = h->y;
-        int adt2 = DT_F32;
         if (lowp) {
-            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_BF16, h->act_lp, d, st));
-            A = h->act_lp;
-            adt2 = DT_BF16;
+            CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
+                                  h->act_lp, DT_BF16, st, CAT_OUT_PROJ));
+        } else {
+            CUDA_TRY(h, gemm(h, DT_F32, h->y, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V,
+                             d, ep, st));
         }
-        CUDA_TRY(h, gemm(h, adt2, A, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V, d, ep,
-                         st));
     }
     MarkovParams mp;
     mp.U = h->U;
@@ -1019,6 +1034,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         }
     }
     if (const char* env = getenv("DSPARK_NO_PERSISTENT")) h->use_persistent = env[0] == '0';
+    if (const char* env = getenv("DSPARK_NORM_FUSION")) h->fuse_norm = env[0] == '1';
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));

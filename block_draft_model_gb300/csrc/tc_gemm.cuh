@@ -54,8 +54,17 @@ struct TcWeightStream {
 bool tc_stream_ok(int M, int N, int K);
 size_t tc_stream_scratch_floats(int N, int K, int num_sms);
 cudaError_t tc_stream_prepare(TcWeightStream& w, const void* ptr, int N, int K);
+// Pre-norm operand of tc_stream: the X side is x * g (x fp32 [M, ldx], g fp32 [K])
+// and the accumulator row m is scaled by 1 / sqrt(mean_k(x[m][k]^2) + eps): the
+// product with RMSNorm(x) * g without a separate normalisation kernel.
+struct StreamNorm {
+    const float* x;
+    const float* g;
+    int64_t ldx;
+    float eps;
+};
 cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M, int N, int K, const EpiParams& ep,
                       float* part, size_t part_floats, unsigned int* tickets, size_t n_tickets, int num_sms, int* err,
-                      cudaStream_t st);
+                      cudaStream_t st, const StreamNorm* norm = nullptr);
 
 }  // namespace dspark

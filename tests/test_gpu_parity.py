@@ -219,6 +219,20 @@ def test_persistent_draft_layers(n_heads, gamma, L):
     check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
 
 
+@pytest.mark.parametrize("gamma", [4, 16])
+def test_normalisation_folded_into_weight_streaming(monkeypatch, gamma):
+    """The opt-in mode where the weight-streaming projections (QKV, gate/up,
+    vocabulary) normalise their own input rows: each CTA rebuilds RMSNorm(x)
+    in shared memory and scales its accumulators by the rows' inverse RMS.
+    The one-launch layers are switched off so that every projection takes it;
+    d 768 gives 12 K-blocks, the vocabulary a ragged last weight tile."""
+    monkeypatch.setenv("DSPARK_NORM_FUSION", "1")
+    monkeypatch.setenv("DSPARK_NO_PERSISTENT", "1")
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=768, n_heads=6, n_layers=2, ff_mult=2, gamma=gamma,
+                            vocab=1100, markov_rank=32)
+    _small(cfg, 200, seed=17, chunks=[90], anchors=[5, 1099], norm_std=0.3)
+
+
 def test_ingest_projection_split_over_k():
     """A context projection with few output tiles (300 rows, d 256) and a long
     K (4 taps x 512): the tensor-core GEMM cuts K into ranges whose partial
