@@ -115,12 +115,15 @@ struct dspark_handle {
     void* mk_E = nullptr;                    // [max_seqs, r] gathered w1 rows (bf16)
     float* mk_pv = nullptr;                  // [max_seqs, ceil(V/32)] chunk partials
     int* mk_pi = nullptr;
-    unsigned int* mk_bar = nullptr;          // [2] grid-barrier words, then the chain's launch epoch
+    unsigned int* mk_bar = nullptr;          // [2] grid-barrier words, the chain's launch epoch, the FMA chain's
+    unsigned long long* mk_slots = nullptr;  // [2, 16 * 2 * (num_sms + 1)] exchange words and counters, FMA chain
+    bool mk_fma = true;                      // one or two sequences: the FMA chain
     unsigned long long* mk_keys = nullptr;   // [2, max_seqs, 16] argmax words of the Markov chain, then 2 counters
     unsigned long long* pk_bar = nullptr;    // persistent draft layers: 2 barrier counters, then the launch epoch
     void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
     int pk_map3d = 0;
     bool use_persistent = true;
+    bool force_persistent = false;           // one-launch layers whatever their size
     bool fuse_norm = false;                  // RMSNorm folded into the weight-streaming projections
     float* ws = nullptr;
     size_t ws_floats = 0;
@@ -453,7 +456,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     // layers stream faster through the per-kernel tcgen05 path.
     const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
     const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
-    if (B == 1 && !seq_ids && lowp && h->use_persistent && persistent_fits) {
+    if (B == 1 && !seq_ids && lowp && h->use_persistent && (persistent_fits || h->force_persistent)) {
         // every layer in one persistent launch
         DraftPersistArgs a{};
         a.x = h->x;
@@ -556,15 +559,16 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
     }
     {
-        Prof pr(h, CAT_OUT_PROJ, st);
         EpiParams ep;
         ep.kind = EPI_STORE_F32;
         ep.out_f32 = h->U;
         ep.ldo = V;
         if (lowp) {
+            // norm_gemm opens its own normalisation and projection ranges
             CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
                                   h->act_lp, DT_BF16, st, CAT_OUT_PROJ));
         } else {
+            Prof pr(h, CAT_OUT_PROJ, st);
             CUDA_TRY(h, gemm(h, DT_F32, h->y, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V,
                              d, ep, st));
         }
@@ -617,6 +621,17 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
                                       B, c.gamma, k, d, c.markov_rank, V, h->d_err, st));
         }
         return DSPARK_OK;
+    }
+    if (h->mk_fma && h->mk_slots) {
+        MarkovParams fp = mp;
+        fp.keys = h->mk_slots;
+        fp.keys_stride = 16 * 2 * (h->num_sms + 1);
+        fp.epoch = h->mk_bar + 3;
+        fp.bar = nullptr;
+        if (markov_chain_fma_ok(fp, h->num_sms)) {
+            CUDA_TRY(h, markov_chain_fma(fp, h->num_sms, st));
+            return DSPARK_OK;
+        }
     }
     if (markov_chain_resident_ok(mp)) {
         CUDA_TRY(h, markov_chain_resident(mp, h->num_sms, st));
@@ -1000,8 +1015,13 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->mk_chain_max = markov_chain_max_ctas(h->dt);
     CTRY(dalloc(h, (void**)&h->mk_v, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
     CTRY(dalloc(h, (void**)&h->mk_i, 2 * (size_t)cfg->max_seqs * h->mk_ctas * 4));
-    CTRY(dalloc(h, (void**)&h->mk_bar, 3 * sizeof(unsigned int)));
-    CTRY(cudaMemsetAsync(h->mk_bar, 0, 3 * sizeof(unsigned int), st));
+    CTRY(dalloc(h, (void**)&h->mk_bar, 4 * sizeof(unsigned int)));
+    CTRY(cudaMemsetAsync(h->mk_bar, 0, 4 * sizeof(unsigned int), st));
+    {
+        const size_t n_slots = 2 * (size_t)16 * 2 * (h->num_sms + 1);
+        CTRY(dalloc(h, (void**)&h->mk_slots, n_slots * sizeof(unsigned long long)));
+        CTRY(cudaMemsetAsync(h->mk_slots, 0, n_slots * sizeof(unsigned long long), st));
+    }
     CTRY(dalloc(h, (void**)&h->mk_keys, (2 * (size_t)cfg->max_seqs * 16 + 2) * sizeof(unsigned long long)));
     CTRY(cudaMemsetAsync(h->mk_keys, 0, (2 * (size_t)cfg->max_seqs * 16 + 2) * sizeof(unsigned long long), st));
     CTRY(dalloc(h, (void**)&h->mk_cnt, (size_t)cfg->max_seqs * 4));
@@ -1034,6 +1054,8 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         }
     }
     if (const char* env = getenv("DSPARK_NO_PERSISTENT")) h->use_persistent = env[0] == '0';
+    if (const char* env = getenv("DSPARK_MARKOV_MMA")) h->mk_fma = env[0] != '1';
+    if (const char* env = getenv("DSPARK_PERSISTENT")) h->force_persistent = env[0] == '1';
     if (const char* env = getenv("DSPARK_NORM_FUSION")) h->fuse_norm = env[0] == '1';
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';

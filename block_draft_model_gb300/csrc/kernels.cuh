@@ -201,6 +201,12 @@ cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigne
 cudaError_t markov_chain_resident_init();  // once per process/device
 bool markov_chain_resident_ok(const MarkovParams& p);
 cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream_t st);
+// One or two sequences (bf16, r = 64, 128 or 256): the resident slice with FMA dot
+// products; p.keys holds 2 sets of p.keys_stride >= 16 * B * (num_sms + 1) exchange
+// words and arrival counters (zero before the first launch), selected by the parity
+// of p.epoch, which the launch advances.  They must not be shared with the other chains.
+bool markov_chain_fma_ok(const MarkovParams& p, int num_sms);
+cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st);
 
 // ------------------------------------------------------------------ bookkeeping kernels
 // For a batched ingest: per feature row t, its slot and cache position

@@ -582,8 +582,260 @@ __global__ void __launch_bounds__(NT_RES, 1) k_markov_chain_res(MarkovParams p, 
     }
 }
 
+// One or two sequences: the same resident w2 slice, but the dot products run on
+// the FMA pipes (bf16 x bf16 + fp32, one rounding each), since a warp MMA would
+// spend 7 of its 8 columns on nothing.  An 8-lane group takes 8 rows of a
+// 512-row pass, strided by 64 so that the rows read from global memory (past
+// the resident ones) spread over every group; lane s holds the 16-byte chunks
+// s, s + 8, ... of each row and of e = w1[prev], and a butterfly over the group
+// leaves lane s with the whole dot product of the group's row s.  The
+// position's argmax goes through one 64-bit word per CTA and an arrival
+// counter (word stored, then a release add); one lane per CTA polls the
+// counter with a bound and its warp then reads every word once, which keeps
+// the polling off the words' cache lines.  Before publishing, each CTA pulls
+// the w1 row of its own best into L2, which holds the next position's e
+// wherever the winner came from.
+constexpr int NT_FMA = 512;
+constexpr int NB_FMA = 2;  // sequences the FMA chain serves
+
+__device__ __forceinline__ uint64_t chain_clock() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// acc += sum over the 8 bf16 pairs of w and e, in order
+__device__ __forceinline__ float fma_chunk(const uint4& w, const uint4& e, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\tmov.b32 {a2, a3}, %2;\n\tmov.b32 {a4, a5}, %3;\n\tmov.b32 {a6, a7}, %4;\n\t"
+        "mov.b32 {b0, b1}, %5;\n\tmov.b32 {b2, b3}, %6;\n\tmov.b32 {b4, b5}, %7;\n\tmov.b32 {b6, b7}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %0, a1, b1, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a2, b2, %0;\n\tfma.rn.f32.bf16 %0, a3, b3, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a4, b4, %0;\n\tfma.rn.f32.bf16 %0, a5, b5, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a6, b6, %0;\n\tfma.rn.f32.bf16 %0, a7, b7, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(e.x), "r"(e.y), "r"(e.z), "r"(e.w));
+    return acc;
+}
+
+// 8 row partials per lane of an 8-lane group -> lane s holds the group sum of row s
+__device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int s) {
+    float h[4], q[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float give = (s & 4) ? a[i] : a[i + 4];
+        h[i] = ((s & 4) ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, give, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float give = (s & 2) ? h[i] : h[i + 2];
+        q[i] = ((s & 2) ? h[i + 2] : h[i]) + __shfl_xor_sync(0xffffffffu, give, 2);
+    }
+    const float give = (s & 1) ? q[0] : q[1];
+    return ((s & 1) ? q[1] : q[0]) + __shfl_xor_sync(0xffffffffu, give, 1);
+}
+
+template <int KD, int NF>  // r = 32 * KD, NF sequences
+__global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, int n_cache) {
+    constexpr int R = KD * 32;
+    constexpr int ROWB = R * 2;
+    constexpr int CPR = ROWB / 16;  // 16-byte chunks per row
+    constexpr int CPL = CPR / 8;    // chunks per lane
+    constexpr int GROUPS = NT_FMA / 8;
+    constexpr int PASS = GROUPS * 8;  // rows per pass
+    extern __shared__ __align__(128) uint8_t w2s[];
+    __shared__ float red_v[NF][NT_FMA / 32];
+    __shared__ int red_i[NF][NT_FMA / 32];
+    __shared__ float redf[32];
+    __shared__ int toks[NF][GMAX_CHAIN + 1];
+
+    const int V = p.V, gamma = p.gamma, G = gridDim.x;
+    const bf16* __restrict__ w1 = reinterpret_cast<const bf16*>(p.w1);
+    const bf16* __restrict__ w2 = reinterpret_cast<const bf16*>(p.w2);
+    float* __restrict__ lg = p.logits;
+    const int rows = (V + G - 1) / G;
+    const int v_begin = blockIdx.x * rows;
+    const int nrows = max(0, min(V, v_begin + rows) - v_begin);
+    const int nc = min(n_cache, nrows);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, s = lane & 7, grp = tid >> 3;
+    float* ubuf = reinterpret_cast<float*>(w2s + (size_t)n_cache * ROWB);  // [2][NF][rows]
+    const uint32_t ubuf_s = (uint32_t)__cvta_generic_to_shared(ubuf);
+    const uint32_t w2s_s = (uint32_t)__cvta_generic_to_shared(w2s);
+    const uint4* __restrict__ w2g = reinterpret_cast<const uint4*>(w2 + (int64_t)v_begin * R);
+
+    {  // the resident rows: chunk c of row li at chunk c ^ (li & 7)
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(w2 + (int64_t)v_begin * R);
+        for (int i = tid; i < nc * CPR; i += NT_FMA) {
+            const int li = i / CPR, c = i - li * CPR;
+            cp_async16_res(w2s_s + li * ROWB + ((c ^ (li & 7)) * 16), src + (size_t)i * 16);
+        }
+    }
+    auto load_u = [&](int k) {
+        for (int i = tid; i < NF * nrows; i += NT_FMA) {
+            const int b = i / nrows, li = i - b * nrows;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                             ubuf_s + (uint32_t)((((k & 1) * NF + b) * rows + li) * 4)),
+                         "l"(p.U + (int64_t)(b * gamma + k) * V + v_begin + li)
+                         : "memory");
+        }
+    };
+    load_u(0);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const unsigned int par = *(volatile unsigned int*)p.epoch & 1u;
+    unsigned long long* slots = p.keys + (size_t)par * p.keys_stride;  // [16][NF][G] words
+    unsigned long long* arrived = slots + (size_t)GMAX_CHAIN * NF * G;   // [16][NF] arrival counters
+    if (blockIdx.x == 0) {
+        unsigned long long* other = p.keys + (size_t)(par ^ 1u) * p.keys_stride;
+        for (int i = tid; i < p.keys_stride; i += NT_FMA) other[i] = 0ull;
+    }
+    if (tid < NF) toks[tid][0] = min(max(p.anchors ? p.anchors[tid] : p.anchor, 0), V - 1);
+
+    for (int k = 0; k < gamma; ++k) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const float* uk = ubuf + (k & 1) * NF * rows;
+        uint4 ev[NF][CPL];
+#pragma unroll
+        for (int n = 0; n < NF; ++n)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+                ev[n][j] = __ldg(reinterpret_cast<const uint4*>(w1 + (int64_t)toks[n][k] * R) + s + 8 * j);
+        ArgBest best[NF];
+#pragma unroll
+        for (int n = 0; n < NF; ++n) best[n] = {-INFINITY, INT_MAX};
+        for (int base = 0; base < nrows; base += PASS) {
+            float acc[NF][8];
+            // the highest rows (read from global memory) first: their loads overlap the load of e
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                const int li = base + grp + GROUPS * i;
+                uint4 w[CPL];
+                if (li < nc) {
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j)
+                        w[j] = *reinterpret_cast<const uint4*>(w2s + li * ROWB + (((s + 8 * j) ^ (li & 7)) * 16));
+                } else if (li < nrows) {
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) w[j] = __ldg(w2g + (int64_t)li * CPR + s + 8 * j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) w[j] = make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int n = 0; n < NF; ++n) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) a = fma_chunk(w[j], ev[n][j], a);
+                    acc[n][i] = a;
+                }
+            }
+            const int li = base + grp + GROUPS * s;
+#pragma unroll
+            for (int n = 0; n < NF; ++n) {
+                const float dot = reduce_scatter8(acc[n], s);
+                if (li < nrows) {
+                    const int v = v_begin + li;
+                    const float l = dot + uk[n * rows + li];
+                    if (lg) lg[(int64_t)(n * gamma + k) * V + v] = l;
+                    if (better(l, v, best[n].v, best[n].i)) {
+                        best[n].v = l;
+                        best[n].i = v;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NF; ++n) {
+            const ArgBest wb = warp_argbest(best[n]);
+            if (lane == 0) {
+                red_v[n][warp] = wb.v;
+                red_i[n][warp] = wb.i;
+            }
+        }
+        __syncthreads();
+        if (k + 1 < gamma) load_u(k + 1);  // its buffer was last read two positions ago
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (warp < NF) {
+            const int n = warp;
+            unsigned long long* sl = slots + (size_t)(k * NF + n) * G;
+            ArgBest cb{lane < NT_FMA / 32 ? red_v[n][lane] : -INFINITY, lane < NT_FMA / 32 ? red_i[n][lane] : INT_MAX};
+            cb = warp_argbest(cb);
+            if (lane == 0) {
+                // a CTA without rows still arrives, with a word below every real one
+                const unsigned long long key = cb.i != INT_MAX ? arg_key(cb.v, cb.i) : 1ull;
+                if (cb.i != INT_MAX) {
+                    const char* row = reinterpret_cast<const char*>(w1 + (int64_t)cb.i * R);
+#pragma unroll
+                    for (int o = 0; o < ROWB; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + o));
+                }
+                asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(sl + blockIdx.x), "l"(key) : "memory");
+                asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(arrived + k * NF + n) : "memory");
+            }
+            // lane 0 waits (bounded) for every CTA's arrival, then the warp reads the words once
+            bool timed_out = false;
+            if (lane == 0) {
+                const uint64_t t0 = chain_clock();
+                while (true) {
+                    unsigned long long cur;
+                    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(arrived + k * NF + n) : "memory");
+                    if (cur >= (unsigned long long)G) break;
+                    if (chain_clock() - t0 > 1000000000ull) {
+                        timed_out = true;
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+            unsigned long long m = 0ull;
+            for (int c = lane; c < G; c += 32) {
+                unsigned long long w;
+                asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(sl + c) : "memory");
+                m = w > m ? w : m;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long om = __shfl_xor_sync(0xffffffffu, m, o);
+                m = om > m ? om : m;
+            }
+            if (lane == 0) {
+                int tok = (int)(~(unsigned int)m);
+                if (timed_out) atomicOr(p.err, 16);
+                if (m <= 1ull || !(key_value(m) > -INFINITY) || tok < 0 || tok >= V) {
+                    if (blockIdx.x == 0) atomicOr(p.err, 8);
+                    tok = 0;
+                }
+                toks[n][k + 1] = tok;
+                if (blockIdx.x == 0) p.tokens[n * gamma + k] = tok;
+            }
+        }
+    }
+    __syncthreads();
+    // confidences: sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b), by CTA 0
+    if (blockIdx.x == 0) {
+        for (int b = 0; b < NF; ++b)
+            for (int k = 0; k < gamma; ++k) {
+                const float* yr = p.y + (int64_t)(b * gamma + k) * p.d;
+                const bf16* er = w1 + (int64_t)toks[b][k] * R;
+                float z = 0.f;
+                for (int c = tid; c < p.d; c += NT_FMA) z = fmaf(yr[c], p.conf_w[c], z);
+                for (int c = tid; c < R; c += NT_FMA) z = fmaf(to_f32(er[c]), p.conf_w[p.d + c], z);
+                z = block_sum(z, redf);
+                if (tid == 0) p.conf[b * gamma + k] = 1.f / (1.f + expf(-(z + p.conf_w[p.d + R])));
+            }
+        // every CTA read the parity before its first release add; CTA 0's last acquire follows them all
+        if (tid == 0) atomicAdd(p.epoch, 1u);
+    }
+}
+
 int g_res_ok[3] = {0, 0, 0};  // the resident chain's kernels for r = 64, 128, 256
 int g_res_budget = 0;         // its dynamic shared memory
+
+bool g_fma_ok = false;         // the FMA chain's kernels
+
+template <int KD, int NF>
+cudaError_t fma_attr(int bytes) {
+    return cudaFuncSetAttribute(k_markov_chain_fma<KD, NF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
 
 template <int KD>
 cudaError_t res_attr(int bytes) {
@@ -737,6 +989,9 @@ cudaError_t markov_chain_resident_init() {
     g_res_ok[0] = res_attr<2>(g_res_budget) == cudaSuccess;
     g_res_ok[1] = res_attr<4>(g_res_budget) == cudaSuccess;
     g_res_ok[2] = res_attr<8>(g_res_budget) == cudaSuccess;
+    g_fma_ok = fma_attr<2, 1>(g_res_budget) == cudaSuccess && fma_attr<2, 2>(g_res_budget) == cudaSuccess &&
+               fma_attr<4, 1>(g_res_budget) == cudaSuccess && fma_attr<4, 2>(g_res_budget) == cudaSuccess &&
+               fma_attr<8, 1>(g_res_budget) == cudaSuccess && fma_attr<8, 2>(g_res_budget) == cudaSuccess;
     (void)cudaGetLastError();
     return cudaSuccess;
 }
@@ -764,6 +1019,44 @@ cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream
     if (kd == 2) e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<2>, p, n_cache);
     else if (kd == 4) e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<4>, p, n_cache);
     else e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<8>, p, n_cache);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+bool markov_chain_fma_ok(const MarkovParams& p, int num_sms) {
+    const int kd = p.r / 32;
+    return g_fma_ok && p.w_dtype == DT_BF16 && p.B >= 1 && p.B <= NB_FMA && p.r % 32 == 0 &&
+           (kd == 2 || kd == 4 || kd == 8) && p.gamma >= 1 && p.gamma <= GMAX_CHAIN && p.keys && p.epoch &&
+           (int64_t)p.keys_stride >= (int64_t)GMAX_CHAIN * p.B * (num_sms + 1);
+}
+
+cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st) {
+    if (!markov_chain_fma_ok(p, num_sms)) return cudaErrorInvalidValue;
+    const int kd = p.r / 32;
+    const int rows = (p.V + num_sms - 1) / num_sms;
+    const int ubytes = (2 * p.B * rows * 4 + 15) / 16 * 16;
+    const int n_cache = std::max(0, std::min(rows, (g_res_budget - ubytes) / (p.r * 2)));
+    const size_t smem = (size_t)n_cache * p.r * 2 + ubytes;
+    if ((int)smem > g_res_budget) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA polls the others' words
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(NT_FMA);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    const bool one = p.B == 1;
+    if (kd == 2) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 1>, p, n_cache)
+                         : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 2>, p, n_cache);
+    else if (kd == 4) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 1>, p, n_cache)
+                              : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 2>, p, n_cache);
+    else e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 1>, p, n_cache)
+                 : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 2>, p, n_cache);
     note_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

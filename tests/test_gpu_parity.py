@@ -242,11 +242,20 @@ def test_ingest_projection_split_over_k():
     _small(cfg, 300, seed=14, chunks=[], anchors=[3, 599])
 
 
-@pytest.mark.parametrize("n_seq,rank,vocab", [(3, 64, 1000), (1, 128, 5003), (7, 256, 2048)])
-def test_markov_chain_few_sequences(n_seq, rank, vocab):
+@pytest.mark.parametrize("n_seq,rank,vocab,form", [
+    (3, 64, 1000, "mma"), (1, 128, 5003, "mma"), (7, 256, 2048, "mma"),
+    (3, 64, 1000, "fma"), (2, 128, 5003, "fma"), (1, 256, 73448, "fma"), (2, 256, 100003, "fma"),
+])
+def test_markov_chain_few_sequences(monkeypatch, n_seq, rank, vocab, form):
     """1 to 7 sequences with r in {64, 128, 256}: the whole Markov chain in one
-    cooperative launch with the vocabulary slices resident on the SMs and the
-    dot products on the tensor cores; vocabularies that leave ragged slices."""
+    cooperative launch with the vocabulary slices resident on the SMs; the dot
+    products on the tensor cores ("mma") or, for one or two sequences, on the
+    FMA pipes with the argmax exchanged through per-CTA words ("fma").
+    Vocabularies that leave ragged slices, CTAs without rows (V 1000), rows
+    past the resident ones (V 73448) and several 512-row passes (V 100003);
+    three sequences then one on the same handle switch between the forms."""
+    if form == "mma":
+        monkeypatch.setenv("DSPARK_MARKOV_MMA", "1")
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=6,
                             vocab=vocab, markov_rank=rank)
     W = syn.make_weights(cfg, seed=13, norm_std=0.1)
@@ -270,6 +279,13 @@ def test_markov_chain_few_sequences(n_seq, rank, vocab):
         for i in range(n_seq):
             check_block(dr, i, int(anchors[i]), tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
                         label=f"launch {rep} seq {i}")
+    if n_seq > 1:  # fewer sequences on the same handle: the other form's words and epoch stay consistent
+        for rep in range(2):
+            gb.draft_batched(ids[:1], anchors[:1], tok[:1], conf[:1], lg[:1])
+            torch.cuda.synchronize()
+            assert gb.check() == 0
+            check_block(dr, 0, int(anchors[0]), tok[0].cpu().numpy(), conf[0].cpu().numpy(), lg[0].cpu().numpy(),
+                        label=f"one sequence, launch {rep}")
 
 
 def test_bf16_attention_many_key_ranges():
