@@ -101,6 +101,9 @@ struct dspark_handle {
     float *x = nullptr, *act = nullptr, *hbuf = nullptr, *q = nullptr, *y = nullptr, *U = nullptr;
     void* act_lp = nullptr;                  // bf16 copies of A operands for the tensor-core path
     void* h_lp = nullptr;
+    void* xb = nullptr;                      // [16, d] bf16 operand x * g written by the residual epilogues
+    float* ssp = nullptr;                    // [d / 8, 16] their 8-column sums of x^2
+    bool chain_norm = true;                  // batch-1 layers: norms through the residual epilogues
     float* attn_part = nullptr;
     size_t attn_part_floats = 0;
     unsigned int* attn_tickets = nullptr;    // [max_seqs * n_heads]
@@ -224,6 +227,7 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     if (M <= 16 && wv.ts && wv.ts->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_stream_ok(M, N, K))
         return tc_stream((const char*)A + (size_t)a_row0 * lda * 2, lda, *wv.ts, M, N, K, ep, h->ts_part,
                          h->ts_part_floats, h->ts_tickets, h->ts_n_tickets, h->num_sms, h->d_err, st);
+    if (ep.ssp) return cudaErrorInvalidValue;  // only the weight-streaming epilogue hands over the next operand
     if (M <= 16 && skinny_ok(M, K))
         return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
     if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_gemm_ok(M, N, K))
@@ -308,6 +312,33 @@ cudaError_t norm_gemm(dspark_handle* h, const float* w, int R, const WView& wv, 
     }
     Prof pr(h, norm_cat, st);
     return gemm(h, adt, actA, d, nullptr, 0, wv, R, N, K, ep, st);
+}
+
+// A projection whose RMSNorm comes through the previous residual epilogue: X = h->xb holds
+// bf16(x * g) and h->ssp the 8-column sums of x^2, from which the kernel forms the row scales.
+cudaError_t chained_gemm(dspark_handle* h, int R, const WView& wv, int N, int K, const EpiParams& ep, cudaStream_t st,
+                         int cat) {
+    Prof pr(h, cat, st);
+    StreamNorm sn;
+    sn.ssp = h->ssp;
+    sn.eps = h->cfg.eps;
+    return tc_stream(h->xb, K, *wv.ts, R, N, K, ep, h->ts_part, h->ts_part_floats, h->ts_tickets, h->ts_n_tickets,
+                     h->num_sms, h->d_err, st, &sn);
+}
+
+// Every batch-1 projection streams (so the residual epilogues can hand over the next norm's operand).
+bool norm_chain_ok(const dspark_handle* h, int R, bool lowp) {
+    if (!h->chain_norm || !lowp || R > 16 || !h->ts_out_proj.ready || !tc_stream_ok(R, h->cfg.vocab, h->d) ||
+        h->d % 64 != 0)
+        return false;
+    const int d = h->d, F = h->F;
+    for (int i = 0; i < h->cfg.n_layers; ++i) {
+        const TcWeightStream* v[4] = {at_or_null(h->ts_qkv, i), at_or_null(h->ts_wo, i), at_or_null(h->ts_wgu, i),
+                                      at_or_null(h->ts_wd, i)};
+        for (const TcWeightStream* w : v)
+            if (!w || !w->ready) return false;
+    }
+    return tc_stream_ok(R, 3 * d, d) && tc_stream_ok(R, d, d) && tc_stream_ok(R, 2 * F, d) && tc_stream_ok(R, d, F);
 }
 
 EpiParams cache_epi(const dspark_handle* h, int layer) {
@@ -496,6 +527,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             layers_done = true;
         }
     }
+    // Batch 1: the residual epilogues of W_o and W_down also write the next projection's operand
+    // bf16(x * g) and the row sums of x^2, so no normalisation launch sits between the layers.
+    const bool chain = !layers_done && norm_chain_ok(h, R, lowp);
     for (int i = 0; i < c.n_layers && !layers_done; ++i) {
         if (i == 0) pr_block.end();
         EpiParams qkv = cache_epi(h, i);
@@ -504,9 +538,11 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         qkv.ldo = d;
         qkv.gamma = c.gamma;
         qkv.seq_ids = seq_ids;
-        CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R,
-                              WView{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)}, 3 * d, d, qkv,
-                              actA, adt, st, CAT_QKV));
+        const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
+        if (chain && i > 0)
+            CUDA_TRY(h, chained_gemm(h, R, wqkv, 3 * d, d, qkv, st, CAT_QKV));
+        else
+            CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, 3 * d, d, qkv, actA, adt, st, CAT_QKV));
         AttnParams ap;
         ap.q = h->q;
         ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
@@ -534,6 +570,12 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         res.kind = EPI_ADD_F32;
         res.out_f32 = h->x;
         res.ldo = d;
+        if (chain) {
+            res.xb = h->xb;
+            res.ld_xb = d;
+            res.ssp = h->ssp;
+            res.xb_g = h->ff_norm[i];
+        }
         {
             Prof pr(h, CAT_O, st);
             CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
@@ -545,9 +587,12 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         sw.act_dtype = adt;
         sw.ld_act = F;
         sw.act = c.act;
-        CUDA_TRY(h, norm_gemm(h, h->ff_norm[i], R,
-                              WView{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)}, 2 * F, d, sw, actA,
-                              adt, st, CAT_GATE_UP));
+        const WView wgu{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)};
+        if (chain)
+            CUDA_TRY(h, chained_gemm(h, R, wgu, 2 * F, d, sw, st, CAT_GATE_UP));
+        else
+            CUDA_TRY(h, norm_gemm(h, h->ff_norm[i], R, wgu, 2 * F, d, sw, actA, adt, st, CAT_GATE_UP));
+        if (chain) res.xb_g = i + 1 < c.n_layers ? h->attn_norm[i + 1] : h->out_norm;
         {
             Prof pr(h, CAT_DOWN, st);
             CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
@@ -563,7 +608,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ep.kind = EPI_STORE_F32;
         ep.out_f32 = h->U;
         ep.ldo = V;
-        if (lowp) {
+        if (chain) {
+            CUDA_TRY(h, chained_gemm(h, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep, st,
+                                     CAT_OUT_PROJ));
+        } else if (lowp) {
             // norm_gemm opens its own normalisation and projection ranges
             CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
                                   h->act_lp, DT_BF16, st, CAT_OUT_PROJ));
@@ -999,6 +1047,9 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, (void**)&h->U, (size_t)R * V * 4));
     CTRY(dalloc(h, &h->act_lp, (size_t)R * wide * 2));
     CTRY(dalloc(h, &h->h_lp, (size_t)R * F * 2));
+    CTRY(dalloc(h, &h->xb, (size_t)16 * d * 2));
+    CTRY(dalloc(h, (void**)&h->ssp, (size_t)(d / 8 + 1) * 16 * sizeof(float)));
+    CTRY(cudaMemsetAsync(h->ssp, 0, (size_t)(d / 8 + 1) * 16 * sizeof(float), st));
     {
         size_t worst = 0;
         for (int B = 1; B <= cfg->max_seqs; ++B) {
@@ -1056,6 +1107,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     if (const char* env = getenv("DSPARK_NO_PERSISTENT")) h->use_persistent = env[0] == '0';
     if (const char* env = getenv("DSPARK_MARKOV_MMA")) h->mk_fma = env[0] != '1';
     if (const char* env = getenv("DSPARK_PERSISTENT")) h->force_persistent = env[0] == '1';
+    if (const char* env = getenv("DSPARK_NO_NORM_CHAIN")) h->chain_norm = env[0] == '0';
     if (const char* env = getenv("DSPARK_NORM_FUSION")) h->fuse_norm = env[0] == '1';
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';

@@ -51,6 +51,13 @@ struct EpiParams {
     int* mk_part_i = nullptr;      // [B, mk_nch] its index
     int mk_nch = 0;                // ceil(V / 32)
     int mk_k = 0;
+    // EPI_ADD_F32 of the weight-streaming GEMM, when ssp is set: besides x += acc, the next
+    // projection's operand xb[m * ld_xb + n] = bf16(x * xb_g[n]) and the row sums of x^2 over each
+    // 8 columns, ssp[(n / 8) * 16 + m] (what that projection's row-sum form reads)
+    void* xb = nullptr;
+    int64_t ld_xb = 0;
+    const float* xb_g = nullptr;
+    float* ssp = nullptr;
 };
 
 // Generic tiled SIMT GEMM (fp32 FMA), any M, N, K.  A rows may be gathered:

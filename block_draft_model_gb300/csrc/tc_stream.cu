@@ -32,7 +32,8 @@ constexpr int X_BYTES = BN * BK * 2;  // 2 KB
 constexpr int TMEM_COLS = 32;
 constexpr int NTHREADS = 192;
 
-constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (W_BYTES + X_BYTES) + 256; }
+// tail after the ring: barriers and flags (256 B), then the row-scale partials [8][16] (512 B)
+constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (W_BYTES + X_BYTES) + 768; }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -45,6 +46,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Row-sum form: rsc[m] = 1 / sqrt(mean(x[m]^2) + eps) from the producer's 8-column sums
+// (K / 8 of them per row), added by the four epilogue warps in a fixed order.
+__device__ __forceinline__ void build_rowscale(const StreamNorm& sn, int K, float* red, float* rsc) {
+    const int t = threadIdx.x - 64;  // 0..127
+    const int m = t & 15, part = t >> 4;
+    const int nP = K >> 3;
+    float s = 0.f;
+#pragma unroll 8
+    for (int j = part; j < nP; j += 8) s += __ldcg(sn.ssp + j * 16 + m);
+    red[part * 16 + m] = s;
+    epi_bar();
+    if (t < 16) {
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a += red[q * 16 + t];
+        rsc[t] = rsqrtf(a / (float)K + sn.eps);
+    }
+    epi_bar();
+}
+
+// EPI_ADD_F32 with the next projection's operand: x += v, xb = bf16(x * g[n]); returns x^2.
+__device__ __forceinline__ float epi_add_xb(const EpiParams& ep, int m, int n, float v) {
+    float* p = ep.out_f32 + (int64_t)m * ep.ldo + n;
+    const float x = *p + v;
+    *p = x;
+    reinterpret_cast<bf16*>(ep.xb)[(int64_t)m * ep.ld_xb + n] = __float2bfloat16(x * ep.xb_g[n]);
+    return x * x;
+}
 
 // Pre-norm operand, built by the four epilogue warps while the weights stream:
 // the MMA's X side for K block kb is bf16(x[m][kb*64 + j] * g[kb*64 + j]) (rows
@@ -154,7 +184,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     volatile int* is_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
     float* rsc = reinterpret_cast<float*>(bars + 16);  // pre-norm row scales [BN]
     volatile int* bfail = reinterpret_cast<volatile int*>(bars + 24);  // pre-norm builder gave up
+    float* rs_red = reinterpret_cast<float*>(bars + 32);               // row-sum form partials [8][16]
     const bool prenorm = sn.x != nullptr;
+    const bool rowscale = !prenorm && sn.ssp != nullptr;
+    const bool xbm = ep.ssp != nullptr;  // EPI_ADD_F32 that also writes the next operand and row sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / splits, split = blockIdx.x - tile * splits;
@@ -250,6 +283,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     } else {
         pdl_wait();  // the epilogue reads and writes buffers shared with earlier kernels
         if (prenorm) build_prenorm(sn, M, K, kb0, kb1, sX, full, empty, rsc, abort_flag, bfail);
+        if (rowscale) build_rowscale(sn, K, rs_red, rsc);
         const int q = warp & 3;
         const int row = q * 32 + lane;  // weight row within the tile
         const int n = n0 + row;
@@ -260,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             uint32_t r[BN];
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16), r);
 #pragma unroll
-            for (int m = 0; m < BN; ++m) v[m] = __uint_as_float(r[m]) * (prenorm ? rsc[m] : 1.f);
+            for (int m = 0; m < BN; ++m) v[m] = __uint_as_float(r[m]) * ((prenorm || rowscale) ? rsc[m] : 1.f);
         } else {
 #pragma unroll
             for (int m = 0; m < BN; ++m) v[m] = 0.f;
@@ -334,7 +368,21 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             } else if (n < N) {
 #pragma unroll
                 for (int m = 0; m < BN; ++m)
-                    if (m < M) epi_one(ep, m, n, v[m]);
+                    if (m < M) {
+                        if (xbm) v[m] = epi_add_xb(ep, m, n, v[m]);
+                        else epi_one(ep, m, n, v[m]);
+                    }
+            }
+        }
+        if (xbm && final_) {
+            // 8-column sums of x^2: lanes are consecutive columns
+#pragma unroll
+            for (int m = 0; m < BN; ++m) {
+                float a = (have && n < N && m < M) ? v[m] : 0.f;
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                a += __shfl_xor_sync(0xffffffffu, a, 4);
+                if ((lane & 7) == 0 && n < N && m < M) ep.ssp[(n >> 3) * 16 + m] = a;
             }
         }
     }
@@ -387,10 +435,30 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         const int m = 4 * cg + q;
                         if (ok && m < M && !(row & 1) && n + 1 < N) epi_pair(ep, m, n, v4[q], up);
                     }
-                } else if (ok && n < N) {
+                } else {
+                    float x2[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (ok && n < N) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (4 * cg + q < M) epi_one(ep, 4 * cg + q, n, v4[q]);
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * cg + q < M) {
+                                if (xbm) x2[q] = epi_add_xb(ep, 4 * cg + q, n, v4[q]);
+                                else epi_one(ep, 4 * cg + q, n, v4[q]);
+                            }
+                    }
+                    if (xbm) {
+                        // 8-column sums of x^2: the 8 lanes of an activation-row group hold 8 consecutive
+                        // columns (lane bits 2..4); their first lane writes the group's four rows
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            x2[q] += __shfl_xor_sync(0xffffffffu, x2[q], 4);
+                            x2[q] += __shfl_xor_sync(0xffffffffu, x2[q], 8);
+                            x2[q] += __shfl_xor_sync(0xffffffffu, x2[q], 16);
+                        }
+                        if ((lane >> 2) == 0 && mine && n < N)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (4 * cg + q < M) ep.ssp[(n >> 3) * 16 + 4 * cg + q] = x2[q];
+                    }
                 }
             }
         }
@@ -479,13 +547,20 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     if (!w.ready || !tc_stream_ok(M, N, K) || N != w.N || K != w.K) return cudaErrorInvalidValue;
     StreamNorm sn{};
     CUtensorMap tmX;
-    if (norm) {
-        if (!norm->x || !norm->g || K % BK != 0 || norm->ldx < K || norm->ldx % 4 != 0 ||
-            ((uintptr_t)norm->x & 15) != 0 || ((uintptr_t)norm->g & 15) != 0)
+    if (ep.ssp && (ep.kind != EPI_ADD_F32 || !ep.xb || !ep.xb_g || N % 8 != 0)) return cudaErrorInvalidValue;
+    if (norm && norm->x) {
+        if (!norm->g || K % BK != 0 || norm->ldx < K || norm->ldx % 4 != 0 || ((uintptr_t)norm->x & 15) != 0 ||
+            ((uintptr_t)norm->g & 15) != 0)
             return cudaErrorInvalidValue;
         sn = *norm;
+        sn.ssp = nullptr;
         tmX = *reinterpret_cast<const CUtensorMap*>(w.tmap);  // unused in the pre-norm mode
     } else {
+        if (norm) {
+            if (!norm->ssp || K % 8 != 0) return cudaErrorInvalidValue;
+            sn.ssp = norm->ssp;
+            sn.eps = norm->eps;
+        }
         if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
         if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
     }

@@ -228,9 +228,32 @@ def test_normalisation_folded_into_weight_streaming(monkeypatch, gamma):
     d 768 gives 12 K-blocks, the vocabulary a ragged last weight tile."""
     monkeypatch.setenv("DSPARK_NORM_FUSION", "1")
     monkeypatch.setenv("DSPARK_NO_PERSISTENT", "1")
+    monkeypatch.setenv("DSPARK_NO_NORM_CHAIN", "1")
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=768, n_heads=6, n_layers=2, ff_mult=2, gamma=gamma,
                             vocab=1100, markov_rank=32)
     _small(cfg, 200, seed=17, chunks=[90], anchors=[5, 1099], norm_std=0.3)
+
+
+@pytest.mark.parametrize("d,n_heads,gamma,L,vocab", [(512, 4, 8, 300, 1000), (64, 1, 16, 100, 777),
+                                                     (768, 6, 5, 257, 1100)])
+def test_norm_chain_through_residual_epilogues(monkeypatch, d, n_heads, gamma, L, vocab):
+    """Batch-1 layers without normalisation launches: the W_o and W_down
+    epilogues write x, the next projection's operand bf16(x * g) and the
+    8-column sums of x^2; QKV, gate/up and the vocabulary projection scale
+    their accumulators by 1 / rms from those sums.  d 512 and 768 reduce
+    split-K through clusters; d 64 runs W_o unsplit (the per-column epilogue);
+    gamma 16 fills all 16 operand rows.  The one-launch layers are off so the
+    small shapes take the per-kernel path."""
+    monkeypatch.setenv("DSPARK_NO_PERSISTENT", "1")
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=d, n_heads=n_heads, n_layers=3, ff_mult=2, gamma=gamma,
+                            vocab=vocab, markov_rank=32)
+    dr, gdr, _ = _small(cfg, L, seed=18, chunks=[L // 3], anchors=[2, vocab - 1, vocab // 2], norm_std=0.3,
+                        max_ctx=L + 8)
+    X = syn.make_feats(cfg, 2, seed=19)
+    dr.ingest(X)
+    gdr.ingest_context(to_torch(X))
+    tok, conf, lg = _draft(gdr, cfg, 11)
+    check_block(dr, 0, 11, tok, conf, lg, label="after 2 more rows")
 
 
 def test_ingest_projection_split_over_k():
