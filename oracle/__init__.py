@@ -18,6 +18,10 @@ from .dspark_oracle import (  # noqa: F401
     linear,
     markov_logits,
     rmsnorm,
+    sample_candidates,
+    sample_token,
+    sample_uniform,
+    splitmix64,
     sigmoid,
     silu,
     softmax,

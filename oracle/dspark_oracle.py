@@ -31,6 +31,17 @@ reason, in the design notes of the repository):
      later positions use the previously drafted token (greedy).
   R8 argmax ties resolve to the lowest index.
   R9 conf_k = sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b), y_k after out_norm.
+  R10 sampling instead of argmax (both pages name a temperature, a top-k and a
+     seeded key stream, "module-dflash.ts" ``forwardInfer`` / "src/dspark-
+     runtime.js" ``propose``, but define none of them): with temperature t > 0
+     the candidates are the top_k largest logits (ties to the lower index; all
+     V when top_k = 0), and the token is drawn from softmax(logits / t) over
+     them by the Gumbel-max rule, argmax_v (l_v / t + g_v), g_v = -ln(-ln u_v).
+     u_v comes from the counter-based SplitMix64 generator (Steele, Lea and
+     Flood, 2014): the (c + 1)-th output of the stream seeded with `seed`, for
+     the counter c = slot * 2^48 + draw * 2^24 + v, top 24 bits, centred:
+     u = (floor(z / 2^40) + 0.5) / 2^24.  `draw` numbers the tokens drawn for
+     one sequence slot since the sampler was set (gamma per draft call).
 """
 from __future__ import annotations
 
@@ -132,6 +143,49 @@ def ffn(n2: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, act: str
     u = n2 @ Wu.T
     a = silu(g) if act == "silu" else gelu_tanh(g)
     return (a * u) @ Wd.T
+
+
+# --------------------------------------------------------------------------- sampling (R10)
+
+SPLITMIX_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+
+
+def splitmix64(counter: np.ndarray, seed: int) -> np.ndarray:
+    """Output number counter + 1 of the SplitMix64 stream that starts at `seed`
+    (state advanced by the golden-ratio increment, then the two xor-shift-
+    multiply rounds and a final xor-shift), for an array of counters."""
+    c = np.asarray(counter, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + (c + np.uint64(1)) * SPLITMIX_GAMMA
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+    return z ^ (z >> np.uint64(31))
+
+
+def sample_uniform(seed: int, slot: int, draw: int, v: np.ndarray) -> np.ndarray:
+    """u in (0, 1) for vocabulary entries v of draw `draw` of sequence `slot` (R10)."""
+    c = (np.uint64(slot) << np.uint64(48)) | (np.uint64(draw) << np.uint64(24)) | np.asarray(v, dtype=np.uint64)
+    return ((splitmix64(c, seed) >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+
+
+def sample_candidates(logits: np.ndarray, top_k: int) -> np.ndarray:
+    """Indices of the top_k largest logits, larger first, ties to the lower index; all when top_k = 0."""
+    V = logits.shape[0]
+    if top_k <= 0 or top_k >= V:
+        return np.arange(V)
+    order = np.lexsort((np.arange(V), -logits))
+    return order[:top_k]
+
+
+def sample_token(logits: np.ndarray, temperature: float, top_k: int, seed: int, slot: int, draw: int,
+                 keys_out: list | None = None) -> int:
+    """R10: argmax over the candidates of logits / t + Gumbel noise (ties to the lower index)."""
+    cand = np.sort(sample_candidates(logits, top_k))
+    g = -np.log(-np.log(sample_uniform(seed, slot, draw, cand)))
+    z = logits[cand] / temperature + g
+    if keys_out is not None:
+        keys_out.append((cand, z))
+    return int(cand[int(np.argmax(z))])
 
 
 def markov_logits(U_k: np.ndarray, w1: np.ndarray, w2: np.ndarray, prev: int):
@@ -254,10 +308,12 @@ class Drafter:
     def confidence(self, y_k: np.ndarray, e: np.ndarray) -> float:
         return confidence(y_k, e, self.w["conf.w"], self.w["conf.b"][0])
 
-    def draft(self, anchor: int, seq: int = 0):
-        """``forwardInfer`` with greedy selection: the parallel backbone once, then
-        the sequential Markov chain.  Returns (tokens [gamma] int64,
-        conf [gamma], logits [gamma, V], y [gamma, d], U [gamma, V])."""
+    def draft(self, anchor: int, seq: int = 0, sample: tuple | None = None):
+        """``forwardInfer``: the parallel backbone once, then the sequential Markov
+        chain, greedy (R8) or, with sample = (temperature, top_k, seed, draw0),
+        drawn by R10 with draw number draw0 + k at position k for slot `seq`.
+        Returns (tokens [gamma] int64, conf [gamma], logits [gamma, V],
+        y [gamma, d], U [gamma, V])."""
         cfg = self.cfg
         y = self.backbone(anchor, seq)
         U = self.base_logits(y)
@@ -267,7 +323,11 @@ class Drafter:
         prev = int(anchor)
         for k in range(cfg.gamma):
             lk, e = self.markov_step(U[k], prev)
-            tok = int(np.argmax(lk))           # R8: first maximum
+            if sample is not None and sample[0] > 0:
+                t, top_k, seed, draw0 = sample
+                tok = sample_token(lk, t, top_k, seed, seq, draw0 + k)
+            else:
+                tok = int(np.argmax(lk))       # R8: first maximum
             logits[k] = lk
             conf[k] = self.confidence(y[k], e)
             tokens[k] = tok
