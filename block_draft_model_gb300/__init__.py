@@ -23,7 +23,8 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_ingest_context_batched", "dspark_draft_batched", "dspark_ingest_context_host",
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
-            "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error"]
+            "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error",
+            "dspark_set_sampling"]
 
 
 class DsparkError(RuntimeError):
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_ingest_context_host": ([vp, vp, i32, vp], i32),
         "dspark_draft_host": ([vp, i32, vp, vp, vp, vp], i32),
         "dspark_reset": ([vp, i32, vp], i32),
+        "dspark_set_sampling": ([vp, ctypes.c_float, i32, ctypes.c_uint64, vp], i32),
         "dspark_context_length": ([vp, i32, ctypes.POINTER(i32)], i32),
         "dspark_check": ([vp, ctypes.POINTER(i32)], i32),
         "dspark_get_cache": ([vp, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)], i32),
@@ -227,6 +229,11 @@ class Drafter:
     def draft_host(self, last_token: int, tokens_host, conf_host, logits_host=None, stream=None):
         self._check(self.lib.dspark_draft_host(self._h, int(last_token), _ptr(tokens_host), _ptr(conf_host),
                                                _ptr(logits_host), _stream(stream)))
+
+    def set_sampling(self, temperature: float, top_k: int = 0, seed: int = 0, stream=None):
+        """temperature > 0: draw the Markov chain's tokens (top_k candidates, 0 = all) instead of argmax."""
+        self._check(self.lib.dspark_set_sampling(self._h, float(temperature), int(top_k), int(seed) & (2**64 - 1),
+                                                 _stream(stream)))
 
     def reset(self, seq_id: int = 0, stream=None):
         self._check(self.lib.dspark_reset(self._h, int(seq_id), _stream(stream)))

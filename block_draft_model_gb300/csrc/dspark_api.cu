@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <string>
 #include <vector>
 
@@ -104,6 +105,12 @@ struct dspark_handle {
     void* xb = nullptr;                      // [16, d] bf16 operand x * g written by the residual epilogues
     float* ssp = nullptr;                    // [d / 8, 16] their 8-column sums of x^2
     bool chain_norm = true;                  // batch-1 layers: norms through the residual epilogues
+    // sampling instead of argmax (temperature > 0)
+    float samp_t = 0.f;
+    int samp_k = 0;
+    unsigned long long samp_seed = 0;
+    unsigned int* samp_draws = nullptr;      // [max_seqs] draw counters
+    unsigned long long* samp_cand = nullptr; // [max_seqs, sample_ctas, 64] candidate words
     float* attn_part = nullptr;
     size_t attn_part_floats = 0;
     unsigned int* attn_tickets = nullptr;    // [max_seqs * n_heads]
@@ -648,6 +655,39 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     mp.epoch = h->mk_bar + 2;
     mp.bar = h->mk_keys + 2 * (size_t)h->cfg.max_seqs * 16;
     Prof pr(h, CAT_MARKOV, st);
+    if (h->samp_t > 0.f) {
+        SampleParams sp;
+        sp.U = h->U;
+        sp.w1 = h->w1;
+        sp.w2 = h->w2;
+        sp.w_dtype = h->dt;
+        sp.y = h->y;
+        sp.conf_w = h->conf_wb;
+        sp.B = B;
+        sp.gamma = c.gamma;
+        sp.V = V;
+        sp.r = c.markov_rank;
+        sp.d = d;
+        sp.anchors = anchors_dev;
+        sp.anchor = anchor;
+        sp.seq_ids = seq_ids;
+        sp.n_slots = c.max_seqs;
+        sp.tokens = tokens;
+        sp.conf = conf;
+        sp.logits = logits;
+        sp.temperature = h->samp_t;
+        sp.top_k = h->samp_k;
+        sp.seed = h->samp_seed;
+        sp.draws = h->samp_draws;
+        sp.cand = h->samp_cand;
+        sp.cand_stride = 64;
+        sp.err = h->d_err;
+        for (int k = 0; k < c.gamma; ++k) {
+            sp.k = k;
+            CUDA_TRY(h, markov_sample_step(sp, h->num_sms, st));
+        }
+        return DSPARK_OK;
+    }
     if (B >= 8 && h->tc_mk_E.ready && tc_gemm_ok(V, B, c.markov_rank) && anchors_dev) {
         // many sequences: per position a [V, r] x [B, r]^T tensor-core GEMM reads w2 once for all of
         // them; vocabulary entries are the rows, so the base logits are read along their rows
@@ -1080,6 +1120,11 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(dalloc(h, (void**)&h->anchor_dev, sizeof(int)));
     CTRY(attention_init());
     CTRY(markov_chain_resident_init());
+    CTRY(sample_init());
+    CTRY(dalloc(h, (void**)&h->samp_draws, (size_t)cfg->max_seqs * sizeof(unsigned int)));
+    CTRY(cudaMemsetAsync(h->samp_draws, 0, (size_t)cfg->max_seqs * sizeof(unsigned int), st));
+    CTRY(dalloc(h, (void**)&h->samp_cand,
+                (size_t)cfg->max_seqs * sample_ctas(cfg->vocab, h->num_sms) * 64 * sizeof(unsigned long long)));
     CTRY(draft_persistent_init());
     CTRY(dalloc(h, (void**)&h->pk_bar, 3 * sizeof(unsigned long long)));
     CTRY(cudaMemsetAsync(h->pk_bar, 0, 3 * sizeof(unsigned long long), st));
@@ -1300,6 +1345,23 @@ dspark_status dspark_reset(dspark_handle* h, int32_t seq_id, void* stream) {
     CUDA_TRY(h, set_len(h->d_len, seq_id, 0, (cudaStream_t)stream));
     h->len_host[seq_id] = 0;
     h->len_known[seq_id] = 1;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_set_sampling(dspark_handle* h, float temperature, int32_t top_k, uint64_t seed, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (!(temperature >= 0.f) || !std::isfinite(temperature))
+        return fail(h, DSPARK_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+    if (top_k < 0 || top_k > 64) return fail(h, DSPARK_ERR_INVALID_ARG, "top_k must be in [0, 64]");
+    if (temperature > 0.f && !sample_ok(h->cfg.vocab, h->cfg.markov_rank, top_k, h->num_sms))
+        return fail(h, DSPARK_ERR_UNSUPPORTED, "sampling is not available for this vocabulary and rank");
+    CUDA_TRY(h, cudaMemsetAsync(h->samp_draws, 0, (size_t)h->cfg.max_seqs * sizeof(unsigned int),
+                                (cudaStream_t)stream));
+    h->samp_t = temperature;
+    h->samp_k = top_k;
+    h->samp_seed = seed;
+    for (auto& g : h->graphs) destroy_graph(g);  // the captured steps carry the old settings
+    h->graphs.clear();
     return DSPARK_OK;
 }
 

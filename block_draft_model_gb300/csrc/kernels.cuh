@@ -212,6 +212,39 @@ cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream
 // products; p.keys holds 2 sets of p.keys_stride >= 16 * B * (num_sms + 1) exchange
 // words and arrival counters (zero before the first launch), selected by the parity
 // of p.epoch, which the launch advances.  They must not be shared with the other chains.
+// Sampling form of the chain (temperature > 0): per block position k, CTAs over the
+// vocabulary compute the logits and publish candidate words, then one CTA per sequence
+// draws the token (Gumbel-max over the top_k candidates, SplitMix64 uniforms keyed by
+// slot, draw counter + k and vocabulary entry) and its confidence; the last position
+// advances draws[slot] by gamma.
+struct SampleParams {
+    const float* U = nullptr;          // [B*gamma, V] base logits
+    const void* w1 = nullptr;          // [V, r], w_dtype
+    const void* w2 = nullptr;
+    int w_dtype = DT_BF16;
+    const float* y = nullptr;          // [B*gamma, d] out-normed block rows
+    const float* conf_w = nullptr;     // [d + r + 1]
+    int B = 0, gamma = 0, V = 0, r = 0, d = 0, k = 0;
+    const int* anchors = nullptr;      // [B] device, or nullptr: `anchor`
+    int anchor = 0;
+    const int* seq_ids = nullptr;      // [B] slots, or nullptr: slot b
+    int n_slots = 0;                   // slots with a draw counter
+    int* tokens = nullptr;             // [B, gamma]
+    float* conf = nullptr;
+    float* logits = nullptr;           // [B, gamma, V] or nullptr
+    float temperature = 0.f;
+    int top_k = 0;                     // 0: the whole vocabulary; else 1..64
+    unsigned long long seed = 0;
+    unsigned int* draws = nullptr;     // [n_slots] draw counters
+    unsigned long long* cand = nullptr;  // [B, ctas, cand_stride] candidate words
+    int cand_stride = 0;
+    int* err = nullptr;
+};
+int sample_ctas(int V, int num_sms);
+bool sample_ok(int V, int r, int top_k, int num_sms);
+cudaError_t sample_init();
+cudaError_t markov_sample_step(const SampleParams& p, int num_sms, cudaStream_t st);
+
 bool markov_chain_fma_ok(const MarkovParams& p, int num_sms);
 cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st);
 

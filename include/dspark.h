@@ -165,6 +165,21 @@ dspark_status dspark_ingest_context_host(dspark_handle* h, const void* feats_hos
 dspark_status dspark_draft_host(dspark_handle* h, int32_t last_token, int32_t* tokens_host, float* conf_host,
                                 float* logits_host, void* stream);
 
+/* Token choice of the Markov chain ("module-dflash.ts", forwardInfer: processLogits +
+ * sampleToken with a seeded KeyStream; "src/dspark-runtime.js", propose: the
+ * temperature > 0 branch).  temperature = 0 (the default): argmax, lowest index on ties.
+ * temperature > 0: the token of block position k is drawn from softmax(l / temperature)
+ * over the top_k largest logits (ties to the lower index; top_k = 0: the whole
+ * vocabulary), as argmax of l_v / temperature - ln(-ln u_v), where u_v is built from the
+ * SplitMix64 output number c + 1 of the stream seeded with `seed`,
+ * c = slot * 2^48 + (draw mod 2^24) * 2^24 + v, u = (top 24 bits + 0.5) / 2^24, and draw =
+ * the slot's draw counter + k; every draft call advances the counters of its sequences by
+ * gamma.  This call resets every counter to 0 (stream-ordered on `stream`) and applies to
+ * the following draft calls.  Errors: INVALID_ARG (temperature negative or not finite,
+ * top_k outside [0, 64]), UNSUPPORTED (vocabulary above 256 x 2048 entries or rank above
+ * 1024 with sampling on). */
+dspark_status dspark_set_sampling(dspark_handle* h, float temperature, int32_t top_k, uint64_t seed, void* stream);
+
 /* Set the context length of seq_id to 0 (stream-ordered on `stream`). */
 dspark_status dspark_reset(dspark_handle* h, int32_t seq_id, void* stream);
 

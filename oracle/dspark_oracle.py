@@ -41,7 +41,8 @@ reason, in the design notes of the repository):
      Flood, 2014): the (c + 1)-th output of the stream seeded with `seed`, for
      the counter c = slot * 2^48 + draw * 2^24 + v, top 24 bits, centred:
      u = (floor(z / 2^40) + 0.5) / 2^24.  `draw` numbers the tokens drawn for
-     one sequence slot since the sampler was set (gamma per draft call).
+     one sequence slot since the sampler was set (gamma per draft call), taken
+     modulo 2^24 so that the three fields of c never overlap (v < 2^24).
 """
 from __future__ import annotations
 
@@ -164,7 +165,8 @@ def splitmix64(counter: np.ndarray, seed: int) -> np.ndarray:
 
 def sample_uniform(seed: int, slot: int, draw: int, v: np.ndarray) -> np.ndarray:
     """u in (0, 1) for vocabulary entries v of draw `draw` of sequence `slot` (R10)."""
-    c = (np.uint64(slot) << np.uint64(48)) | (np.uint64(draw) << np.uint64(24)) | np.asarray(v, dtype=np.uint64)
+    c = ((np.uint64(slot) << np.uint64(48)) | (np.uint64(draw % (1 << 24)) << np.uint64(24))
+         | np.asarray(v, dtype=np.uint64))
     return ((splitmix64(c, seed) >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
 
 
