@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--workload", default="minicpm_L1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="> 0: the Markov chain draws its tokens (top-k candidates) instead of the argmax")
+    ap.add_argument("--top-k", type=int, default=0)
     return ap.parse_args()
 
 
@@ -527,6 +530,8 @@ def main():
     bdm.load()
     run = make_runner(args.workload, dev)
     run.setup()
+    if args.temperature > 0:
+        run.g.set_sampling(args.temperature, args.top_k, 2024)
     cfg, g = run.cfg, run.g
     stream = torch.cuda.current_stream(dev)
     B = run.wl.n_seqs
@@ -631,6 +636,8 @@ def main():
             "config": {"workload": run.wl.name, "ctx_len": run.wl.ctx_len, "sequences": B, "gamma": cfg.gamma,
                        "d_draft": cfg.d_draft, "vocab": cfg.vocab,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "token_choice": (f"sampled (temperature {args.temperature}, top-k {args.top_k})"
+                                        if args.temperature > 0 else "argmax"),
                        "l2": "inputs larger than L2 (weights, caches and features stream > 1 GB per step)"},
             "ctx_tokens_per_s": world * args.steps * run.ctx_tokens_per_step / (ms_max / 1e3),
             "phases": phases, "roofline": roofline, "clocks": clk, "gpu_launches": launches, "e2e": e2e}

@@ -13,7 +13,8 @@
 // Two launches per block position:
 //   k_sample_logits: CTAs over the vocabulary compute l = U_k + w2 . w1[prev], write the
 //     logits, and publish either their best Gumbel key (top_k = 0) or their own top_k
-//     logits as sorted 64-bit words (order-preserving float bits << 32 | ~index);
+//     logits as 64-bit words (order-preserving float bits << 32 | ~index), found by the
+//     same radix select;
 //   k_sample_pick: one CTA per sequence gathers the words, finds the top_k-th largest by
 //     an 8-pass radix select (the union of the CTAs' lists holds the global top_k), draws
 //     among the words at or above it, and writes the token and the confidence.
@@ -28,12 +29,12 @@ namespace dspark {
 
 namespace {
 
-constexpr int NT_L = 256;        // k_sample_logits threads
+constexpr int NT_L = 512;        // k_sample_logits threads
 constexpr int NT_P = 1024;       // k_sample_pick threads
 constexpr int LPR_S = 4;         // lanes per vocabulary row
 constexpr int RPW_S = 32 / LPR_S;
 constexpr int RMAX_S = 1024;     // largest Markov rank
-constexpr int ROWS_MAX = 2048;   // vocabulary rows per CTA (the local sort's size)
+constexpr int ROWS_MAX = 2048;   // vocabulary rows per CTA (the local selection's size)
 constexpr int TOPK_MAX = 64;
 constexpr int MAX_CTAS = 256;
 
@@ -80,6 +81,91 @@ __device__ __forceinline__ unsigned long long block_max64(unsigned long long w, 
     return warp_max64(t);
 }
 
+struct KthShared {
+    unsigned int hist[256];
+    unsigned long long prefix;
+    unsigned int rem;
+    int count;
+    int done;
+};
+
+// The K-th largest of the nonzero words w[0, n) (they are distinct), for the whole block;
+// 1 when there are no more than K of them.  MSB-first radix select on 8-bit digits; it
+// stops once every word under the chosen prefix is wanted.
+__device__ unsigned long long block_kth_word(const unsigned long long* w, int n, int K, KthShared& ks) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        ks.prefix = 0ull;
+        ks.rem = (unsigned int)K;
+        ks.count = 0;
+        ks.done = 0;
+    }
+    __syncthreads();
+    int nz = 0;
+    for (int i = tid; i < n; i += nt) nz += w[i] != 0ull;
+    nz = __reduce_add_sync(0xffffffffu, nz);
+    if (lane == 0 && nz) atomicAdd(&ks.count, nz);
+    __syncthreads();
+    if (ks.count <= K) return 1ull;
+    unsigned long long mask = 0ull;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += nt) ks.hist[i] = 0u;
+        __syncthreads();
+        const unsigned long long prefix = ks.prefix;
+        // block-uniform trip count, so that every lane takes part in the match; the lanes of a
+        // warp that fall in the same bin add once (the high digits crowd into few bins)
+        for (int i0 = 0; i0 < n; i0 += nt) {
+            const int i = i0 + tid;
+            const unsigned long long x = i < n ? w[i] : 0ull;
+            const bool in = x != 0ull && (x & mask) == prefix;
+            const uint32_t bin = in ? ((uint32_t)(x >> shift) & 255u) : 256u;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (in && lane == __ffs(peers) - 1) atomicAdd(&ks.hist[bin], (unsigned int)__popc(peers));
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds digits 255 - 8l down to 248 - 8l; find where the count from the top
+            // reaches the rank still wanted
+            unsigned int h8[8], loc = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                h8[q] = ks.hist[255 - 8 * lane - q];
+                loc += h8[q];
+            }
+            unsigned int incl = loc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const unsigned int rem = ks.rem, excl = incl - loc;
+            const unsigned int hit = __ballot_sync(0xffffffffu, excl < rem && rem <= incl);
+            if (hit != 0u && lane == __ffs(hit) - 1) {
+                unsigned int cum = excl, hq = 0;
+                int qs = 7;
+                bool found = false;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (!found && cum + h8[q] >= rem) {
+                        qs = q;
+                        hq = h8[q];
+                        found = true;
+                    } else if (!found) {
+                        cum += h8[q];
+                    }
+                }
+                ks.prefix = prefix | ((unsigned long long)(255 - 8 * lane - qs) << shift);
+                ks.rem = rem - cum;
+                ks.done = (hq == rem - cum);  // every word under the new prefix is wanted
+            }
+        }
+        mask |= 0xffull << shift;
+        __syncthreads();
+        if (ks.done) break;
+    }
+    return ks.prefix;
+}
+
 __device__ __forceinline__ int sample_prev(const SampleParams& p, int b) {
     const int prev = p.k == 0 ? (p.anchors ? p.anchors[b] : p.anchor) : p.tokens[b * p.gamma + p.k - 1];
     return min(max(prev, 0), p.V - 1);
@@ -103,6 +189,8 @@ __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
     __shared__ __align__(16) float e[RMAX_S];
     __shared__ unsigned long long keys[ROWS_MAX];
     __shared__ unsigned long long red[32];
+    __shared__ KthShared ks;
+    __shared__ int n_out;
 
     const int b = blockIdx.y, k = p.k, r = p.r, V = p.V, K = p.top_k;
     const int prev = sample_prev(p, b);
@@ -115,10 +203,6 @@ __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
     const int rows = (V + gridDim.x - 1) / gridDim.x;
     const int v_begin = blockIdx.x * rows, v_end = min(V, v_begin + rows);
     const int nrows = max(0, v_end - v_begin);
-    int np2 = 1;
-    while (np2 < nrows) np2 <<= 1;
-    if (K > 0)
-        for (int i = threadIdx.x; i < np2; i += NT_L) keys[i] = 0ull;
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -126,27 +210,51 @@ __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
     const int64_t urow = (int64_t)(b * p.gamma + k) * V;
     const int nvec = r / VE;
     unsigned long long zbest = 0ull;
-    for (int v0 = v_begin + warp * RPW_S; v0 < v_end; v0 += (NT_L / 32) * RPW_S) {
-        const int v = v0 + rw;
-        const TW* row = w2 + (int64_t)min(v, v_end - 1) * r;
-        float acc = 0.f;
-        for (int x = sub; x < nvec; x += LPR_S) {
-            float f[VE];
-            Vec16<TW>::unpack(__ldg(reinterpret_cast<const uint4*>(row + x * VE)), f);
-            const float* ep = e + x * VE;
+    // two rows per lane group per pass, eight 16-byte chunks of each requested before any is used
+    constexpr int QL = 8;
+    for (int v0 = v_begin + warp * (2 * RPW_S); v0 < v_end; v0 += (NT_L / 32) * (2 * RPW_S)) {
+        int vr[2] = {v0 + rw, v0 + RPW_S + rw};
+        float acc[2] = {0.f, 0.f};
+        for (int x0 = sub; x0 < nvec; x0 += QL * LPR_S) {
+            uint4 u[2][QL];
 #pragma unroll
-            for (int t = 0; t < VE; ++t) acc = fmaf(f[t], ep[t], acc);
+            for (int h = 0; h < 2; ++h) {
+                const TW* row = w2 + (int64_t)min(vr[h], v_end - 1) * r;
+#pragma unroll
+                for (int q = 0; q < QL; ++q) {
+                    const int x = x0 + q * LPR_S;
+                    u[h][q] = x < nvec ? __ldg(reinterpret_cast<const uint4*>(row + x * VE)) : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < QL; ++q) {
+                const int x = x0 + q * LPR_S;
+                if (x < nvec) {
+                    const float* ep = e + x * VE;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float f[VE];
+                        Vec16<TW>::unpack(u[h][q], f);
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) acc[h] = fmaf(f[t], ep[t], acc[h]);
+                    }
+                }
+            }
         }
 #pragma unroll
-        for (int o = 1; o < LPR_S; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (sub == 0 && v < v_end) {
-            const float l = p.U[urow + v] + acc;
-            if (p.logits) p.logits[urow + v] = l;
-            if (K > 0) {
-                keys[v - v_begin] = word_of(l, v);
-            } else {
-                const unsigned long long zw = word_of(l / p.temperature + gumbel_noise(p.seed, slot, draw, v), v);
-                zbest = zw > zbest ? zw : zbest;
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int o = 1; o < LPR_S; o <<= 1) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
+            const int v = vr[h];
+            if (sub == 0 && v < v_end) {
+                const float l = p.U[urow + v] + acc[h];
+                if (p.logits) p.logits[urow + v] = l;
+                if (K > 0) {
+                    keys[v - v_begin] = word_of(l, v);
+                } else {
+                    const unsigned long long zw = word_of(l / p.temperature + gumbel_noise(p.seed, slot, draw, v), v);
+                    zbest = zw > zbest ? zw : zbest;
+                }
             }
         }
     }
@@ -157,22 +265,16 @@ __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
         return;
     }
     __syncthreads();
-    // bitonic sort of the CTA's words, largest first
-    for (int size = 2; size <= np2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < (np2 >> 1); i += NT_L) {
-                const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-                const unsigned long long a = keys[lo], c = keys[hi];
-                const bool desc = (lo & size) == 0;
-                if (desc ? (a < c) : (a > c)) {
-                    keys[lo] = c;
-                    keys[hi] = a;
-                }
-            }
-            __syncthreads();
-        }
+    // this CTA's top_k words (unordered): the ones at or above its top_k-th largest
+    const unsigned long long thr = block_kth_word(keys, nrows, K, ks);
+    if (threadIdx.x == 0) n_out = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nrows; i += NT_L) {
+        const unsigned long long w = keys[i];
+        if (w != 0ull && w >= thr) out[atomicAdd(&n_out, 1)] = w;
     }
-    for (int j = threadIdx.x; j < K; j += NT_L) out[j] = j < nrows ? keys[j] : 0ull;
+    __syncthreads();
+    for (int j = n_out + threadIdx.x; j < K; j += NT_L) out[j] = 0ull;
 }
 
 template <typename TW>
@@ -180,11 +282,9 @@ __global__ void __launch_bounds__(NT_P) k_sample_pick(SampleParams p, int ctas) 
     pdl_trigger();
     pdl_wait();
     extern __shared__ unsigned long long words[];  // [ctas * cand_stride]
-    __shared__ unsigned int hist[256];
+    __shared__ KthShared ks;
     __shared__ unsigned long long red[32];
     __shared__ float redf[32];
-    __shared__ unsigned long long s_prefix;
-    __shared__ unsigned int s_rem;
 
     const int b = blockIdx.x, k = p.k, r = p.r, V = p.V;
     const int K = p.top_k;
@@ -193,77 +293,18 @@ __global__ void __launch_bounds__(NT_P) k_sample_pick(SampleParams p, int ctas) 
     const uint32_t slot = sample_slot(p, b);
     const uint32_t draw = p.draws[slot] + (uint32_t)k;
     const unsigned long long* src = p.cand + (size_t)b * ctas * p.cand_stride;
-    int nz = 0;
     for (int i = threadIdx.x; i < n; i += NT_P) {
         const int c = i / per, j = i - c * per;
-        const unsigned long long w = __ldcg(src + (size_t)c * p.cand_stride + j);
-        words[i] = w;
-        nz += w != 0ull;
+        words[i] = __ldcg(src + (size_t)c * p.cand_stride + j);
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
     unsigned long long pick = 0ull;
     if (K == 0) {
         unsigned long long m = 0ull;
         for (int i = threadIdx.x; i < n; i += NT_P) m = words[i] > m ? words[i] : m;
         pick = block_max64(m, red);
     } else {
-        const int total = (int)block_sum((float)nz, redf);
-        // the top_k-th largest word (all of them when there are no more than top_k)
-        unsigned long long thr = 1ull;
-        if (total > K) {
-            if (threadIdx.x == 0) {
-                s_prefix = 0ull;
-                s_rem = (unsigned int)K;
-            }
-            unsigned long long mask = 0ull;
-            for (int shift = 56; shift >= 0; shift -= 8) {
-                if (threadIdx.x < 256) hist[threadIdx.x] = 0u;
-                __syncthreads();
-                const unsigned long long prefix = s_prefix;
-                for (int i = threadIdx.x; i < n; i += NT_P) {
-                    const unsigned long long w = words[i];
-                    if (w != 0ull && (w & mask) == prefix) atomicAdd(&hist[(uint32_t)(w >> shift) & 255u], 1u);
-                }
-                __syncthreads();
-                if (warp == 0) {
-                    // lane l holds digits 255 - 8l down to 248 - 8l; find where the count from the
-                    // top reaches the rank still wanted
-                    unsigned int h8[8], loc = 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        h8[q] = hist[255 - 8 * lane - q];
-                        loc += h8[q];
-                    }
-                    unsigned int incl = loc;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += t;
-                    }
-                    const unsigned int rem = s_rem, excl = incl - loc;
-                    const unsigned int hit = __ballot_sync(0xffffffffu, excl < rem && rem <= incl);
-                    if (hit != 0u && lane == __ffs(hit) - 1) {
-                        unsigned int cum = excl;
-                        int qs = 7;
-                        bool found = false;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            if (!found && cum + h8[q] >= rem) {
-                                qs = q;
-                                found = true;
-                            } else if (!found) {
-                                cum += h8[q];
-                            }
-                        }
-                        s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - qs) << shift);
-                        s_rem = rem - cum;
-                    }
-                }
-                mask |= 0xffull << shift;
-                __syncthreads();
-            }
-            thr = s_prefix;
-        }
+        const unsigned long long thr = block_kth_word(words, n, K, ks);
         unsigned long long m = 0ull;
         for (int i = threadIdx.x; i < n; i += NT_P) {
             const unsigned long long w = words[i];
