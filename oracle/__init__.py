@@ -15,9 +15,11 @@ from .dspark_oracle import (  # noqa: F401
     context_kv,
     ffn,
     gelu_tanh,
+    head_rmsnorm,
     linear,
     markov_logits,
     rmsnorm,
+    rope,
     sample_candidates,
     sample_token,
     sample_uniform,

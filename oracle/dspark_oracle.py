@@ -43,6 +43,16 @@ reason, in the design notes of the repository):
      u = (floor(z / 2^40) + 0.5) / 2^24.  `draw` numbers the tokens drawn for
      one sequence slot since the sampler was set (gamma per draft call), taken
      modulo 2^24 so that the three fields of c never overlap (v < 2^24).
+  R11 the variant of "src/dspark-runtime.js" (kernels ``noiseNormRope`` for the
+     block rows and ``contextNormRope`` for the context rows, ``qNorm`` /
+     ``kNorm`` bindings, K/V widths KV != H): grouped-query attention with
+     n_kv_heads K/V heads, query head h reading K/V head h // (n_heads /
+     n_kv_heads); optional per-head RMSNorm of Q and K (weight [head_dim]
+     shared by the heads, the same eps) followed by rotary embedding in the
+     rotate-half layout, entries e and e + hd/2 turned by pos * theta^(-2e/hd);
+     V is neither normalised nor rotated.  Positions: context row t of a
+     sequence at t, block row j at L + j (L = context length), so the block
+     continues the context.
 """
 from __future__ import annotations
 
@@ -121,21 +131,46 @@ def context_kv(H_ctx: np.ndarray, attn_norm: np.ndarray, Wk: np.ndarray, Wv: np.
     return n @ Wk.T, n @ Wv.T
 
 
-def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, n_heads: int, probs_out: list | None = None):
+def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, n_heads: int, probs_out: list | None = None,
+              n_kv_heads: int = 0):
     """Scaled dot-product attention of ``#layer``: per head, softmax(Q K^T / sqrt(hd)) V
-    over every key row (no mask, R6).  Q: [g, d]; K, V: [n, d] (context first,
-    then block).  Returns O [g, d] with heads concatenated."""
+    over every key row (no mask, R6).  Q: [g, d]; K, V: [n, d_kv] (context first,
+    then block); query head h reads K/V head h // (n_heads / n_kv_heads) (R11;
+    n_kv_heads = 0: one K/V head per query head).  Returns O [g, d] with heads
+    concatenated."""
     g, d = Q.shape
     hd = d // n_heads
+    group = n_heads // (n_kv_heads or n_heads)
     O = np.empty((g, d), dtype=np.float64)
     for h in range(n_heads):
         sl = slice(h * hd, (h + 1) * hd)
-        S = (Q[:, sl] @ K[:, sl].T) * (hd ** -0.5)
+        kv = slice((h // group) * hd, (h // group + 1) * hd)
+        S = (Q[:, sl] @ K[:, kv].T) * (hd ** -0.5)
         P = softmax(S)
         if probs_out is not None:
             probs_out.append(P)
-        O[:, sl] = P @ V[:, sl]
+        O[:, sl] = P @ V[:, kv]
     return O
+
+
+def head_rmsnorm(x: np.ndarray, w: np.ndarray, n_heads: int, eps: float) -> np.ndarray:
+    """R11: RMSNorm of every head's slice of the rows of x, weight w [head_dim]."""
+    rows, width = x.shape
+    hd = width // n_heads
+    return rmsnorm(x.reshape(rows, n_heads, hd), w, eps).reshape(rows, width)
+
+
+def rope(x: np.ndarray, positions: np.ndarray, n_heads: int, theta: float) -> np.ndarray:
+    """R11: rotary embedding, rotate-half layout: in every head, entries e and
+    e + hd/2 (e < hd/2) are turned by the angle pos * theta^(-2e/hd)."""
+    rows, width = x.shape
+    hd = width // n_heads
+    half = hd // 2
+    ang = np.asarray(positions, np.float64)[:, None] * theta ** (-2.0 * np.arange(half) / hd)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    xh = x.reshape(rows, n_heads, hd)
+    a, b = xh[..., :half], xh[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1).reshape(rows, width)
 
 
 def ffn(n2: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, act: str = "silu") -> np.ndarray:
@@ -218,6 +253,10 @@ class Drafter:
         d = cfg.d_draft
         if d % cfg.n_heads != 0:
             raise ValueError(f"d_draft {d} not divisible by n_heads {cfg.n_heads}")
+        if cfg.n_heads % cfg.kv_heads != 0:
+            raise ValueError(f"n_heads {cfg.n_heads} not a multiple of n_kv_heads {cfg.kv_heads}")
+        if cfg.rope_theta > 0 and cfg.head_dim % 2 != 0:
+            raise ValueError("rotary embedding needs an even head_dim")
         self.raw = weights
         w = {}
         for name, arr in weights.items():
@@ -226,12 +265,14 @@ class Drafter:
             w[name] = to_f64(arr)
         self.w = w
         self.seqs: dict[int, list] = {}      # seq -> [ [K_i], [V_i] ] per layer, lists of row blocks
+        self.pos_offset = 0                  # added to every position of R11 (a pin shifts it)
 
     # ------------------------------------------------------------------ ingest
     def _cache(self, seq: int):
         if seq not in self.seqs:
-            self.seqs[seq] = [[np.zeros((0, self.cfg.d_draft)) for _ in range(self.cfg.n_layers)],
-                              [np.zeros((0, self.cfg.d_draft)) for _ in range(self.cfg.n_layers)]]
+            dkv = self.cfg.d_kv
+            self.seqs[seq] = [[np.zeros((0, dkv)) for _ in range(self.cfg.n_layers)],
+                              [np.zeros((0, dkv)) for _ in range(self.cfg.n_layers)]]
         return self.seqs[seq]
 
     def reset(self, seq: int = 0):
@@ -244,6 +285,7 @@ class Drafter:
     def ingest(self, X: np.ndarray, seq: int = 0, chunk: int = 2048):
         """Eq 2 then Eq 3 for T new context rows, appended to the caches of ``seq``."""
         cfg, w = self.cfg, self.w
+        L0 = self.context_length(seq)
         Ks, Vs = self._cache(seq)
         T = X.shape[0]
         newK = [[] for _ in range(cfg.n_layers)]
@@ -251,13 +293,25 @@ class Drafter:
         for t0 in range(0, T, chunk):
             Xc = to_f64(X[t0:t0 + chunk])
             Hc = context_features(Xc, w["W_c"], w["ctx_norm"], cfg.eps)
+            pos = L0 + t0 + np.arange(Hc.shape[0])
             for i in range(cfg.n_layers):
                 k, v = context_kv(Hc, w[f"bb.{i}.attn_norm"], w[f"bb.{i}.k"], w[f"bb.{i}.v"], cfg.eps)
+                k = self.qk_transform(k, i, "k", pos, cfg.kv_heads)
                 newK[i].append(k)
                 newV[i].append(v)
         for i in range(cfg.n_layers):
             Ks[i] = np.concatenate([Ks[i]] + newK[i], axis=0)
             Vs[i] = np.concatenate([Vs[i]] + newV[i], axis=0)
+
+    def qk_transform(self, x: np.ndarray, layer: int, which: str, positions: np.ndarray, n_heads: int):
+        """R11 on Q or K rows: per-head RMSNorm (if configured), then rotary
+        embedding at `positions` (if configured); identity otherwise."""
+        cfg = self.cfg
+        if cfg.qk_norm:
+            x = head_rmsnorm(x, self.w[f"bb.{layer}.{which}_norm"], n_heads, cfg.eps)
+        if cfg.rope_theta > 0:
+            x = rope(x, np.asarray(positions) + self.pos_offset, n_heads, cfg.rope_theta)
+        return x
 
     def cache(self, seq: int, layer: int):
         Ks, Vs = self._cache(seq)
@@ -283,9 +337,12 @@ class Drafter:
         Q = n @ w[f"bb.{i}.q"].T
         Kb = n @ w[f"bb.{i}.k"].T
         Vb = n @ w[f"bb.{i}.v"].T
+        pos = Kc.shape[0] + np.arange(cfg.gamma)      # R11: the block continues the context
+        Q = self.qk_transform(Q, i, "q", pos, cfg.n_heads)
+        Kb = self.qk_transform(Kb, i, "k", pos, cfg.kv_heads)
         K = np.concatenate([Kc, Kb], axis=0)
         V = np.concatenate([Vc, Vb], axis=0)
-        O = attention(Q, K, V, cfg.n_heads, probs_out)
+        O = attention(Q, K, V, cfg.n_heads, probs_out, cfg.kv_heads)
         x = x + O @ w[f"bb.{i}.o"].T
         n2 = rmsnorm(x, w[f"bb.{i}.ff_norm"], cfg.eps)
         return x + ffn(n2, w[f"bb.{i}.gate"], w[f"bb.{i}.up"], w[f"bb.{i}.down"], cfg.act)

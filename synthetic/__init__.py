@@ -107,10 +107,21 @@ class DrafterConfig:
     eps: float = 1e-6
     dtype: str = "bf16"  # "bf16" or "fp32": storage type of weights, features and caches
     act: str = "silu"    # "silu" or "gelu_tanh"
+    n_kv_heads: int = 0       # K/V heads; 0 = n_heads (fewer: grouped-query attention)
+    qk_norm: bool = False     # per-head RMSNorm of Q and K (weights q_norm, k_norm [head_dim] per layer)
+    rope_theta: float = 0.0   # > 0: rotary position embedding of Q and K with this base
 
     @property
     def head_dim(self) -> int:
         return self.d_draft // self.n_heads
+
+    @property
+    def kv_heads(self) -> int:
+        return self.n_kv_heads or self.n_heads
+
+    @property
+    def d_kv(self) -> int:
+        return self.kv_heads * self.head_dim
 
     @property
     def ff(self) -> int:
@@ -128,6 +139,9 @@ def param_names(cfg: DrafterConfig) -> list[str]:
         names += [f"bb.{i}.{n}" for n in ("attn_norm", "q", "k", "v", "o", "ff_norm", "gate", "up", "down")]
     names += ["W_c", "ctx_norm", "tok_proj", "mask_emb", "block_pos", "out_norm", "out_proj",
               "markov.w1", "markov.w2", "conf.w", "conf.b"]
+    if cfg.qk_norm:  # after the rest, so that the other parameters keep their streams
+        for i in range(cfg.n_layers):
+            names += [f"bb.{i}.q_norm", f"bb.{i}.k_norm"]
     return names
 
 
@@ -135,8 +149,9 @@ def param_shape(cfg: DrafterConfig, name: str) -> tuple:
     d, F, H, V, r, g = cfg.d_draft, cfg.ff, cfg.hidden, cfg.vocab, cfg.markov_rank, cfg.gamma
     if name.startswith("bb."):
         leaf = name.split(".")[2]
-        return {"attn_norm": (d,), "ff_norm": (d,), "q": (d, d), "k": (d, d), "v": (d, d), "o": (d, d),
-                "gate": (F, d), "up": (F, d), "down": (d, F)}[leaf]
+        dkv, hd = cfg.d_kv, cfg.head_dim
+        return {"attn_norm": (d,), "ff_norm": (d,), "q": (d, d), "k": (dkv, d), "v": (dkv, d), "o": (d, d),
+                "gate": (F, d), "up": (F, d), "down": (d, F), "q_norm": (hd,), "k_norm": (hd,)}[leaf]
     return {"W_c": (d, cfg.feat_dim), "ctx_norm": (d,), "tok_proj": (d, H), "mask_emb": (g - 1, d),
             "block_pos": (g, d), "out_norm": (d,), "out_proj": (V, d), "markov.w1": (V, r),
             "markov.w2": (V, r), "conf.w": (d + r,), "conf.b": (1,), "embed": (V, H)}[name]

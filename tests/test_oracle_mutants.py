@@ -11,7 +11,7 @@ import synthetic as syn
 from test_oracle_pins import brute_force_draft, tiny_cfg
 
 
-def _no_scale_attention(Q, K, V, n_heads, probs_out=None):
+def _no_scale_attention(Q, K, V, n_heads, probs_out=None, n_kv_heads=0):
     g, d = Q.shape
     hd = d // n_heads
     O = np.empty((g, d))
