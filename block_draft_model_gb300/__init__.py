@@ -38,7 +38,8 @@ class Config(ctypes.Structure):
                 ("n_heads", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("ff_mult", ctypes.c_int32),
                 ("gamma", ctypes.c_int32), ("vocab", ctypes.c_int32), ("markov_rank", ctypes.c_int32),
                 ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("max_ctx", ctypes.c_int32), ("max_seqs", ctypes.c_int32)]
+                ("max_ctx", ctypes.c_int32), ("max_seqs", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("qk_norm", ctypes.c_int32), ("rope_theta", ctypes.c_float)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -50,7 +51,7 @@ class Weights(ctypes.Structure):
                 ("attn_norm", _PP), ("wq", _PP), ("wk", _PP), ("wv", _PP), ("wo", _PP), ("ff_norm", _PP),
                 ("w_gate", _PP), ("w_up", _PP), ("w_down", _PP), ("out_norm", ctypes.c_void_p),
                 ("out_proj", ctypes.c_void_p), ("markov_w1", ctypes.c_void_p), ("markov_w2", ctypes.c_void_p),
-                ("conf_w", ctypes.c_void_p), ("conf_b", ctypes.c_void_p)]
+                ("conf_w", ctypes.c_void_p), ("conf_b", ctypes.c_void_p), ("q_norm", _PP), ("k_norm", _PP)]
 
 
 _lib = None
@@ -156,10 +157,12 @@ class Drafter:
     in bf16 (or float32 for ``dtype=FP32``), norm vectors float32."""
 
     def __init__(self, *, hidden, n_taps, d_draft, n_heads, n_layers, ff_mult, gamma, vocab, markov_rank,
-                 eps=1e-6, dtype=BF16, act=ACT_SILU, max_ctx=4096, max_seqs=1, weights=None, stream=None):
+                 eps=1e-6, dtype=BF16, act=ACT_SILU, max_ctx=4096, max_seqs=1, weights=None, stream=None,
+                 n_kv_heads=0, qk_norm=False, rope_theta=0.0):
         self.lib = load()
         self.cfg = Config(hidden, n_taps, d_draft, n_heads, n_layers, ff_mult, gamma, vocab, markov_rank, eps,
-                          dtype, act, max_ctx, max_seqs)
+                          dtype, act, max_ctx, max_seqs, n_kv_heads, int(bool(qk_norm)), rope_theta)
+        self.d_kv = (n_kv_heads or n_heads) * (d_draft // n_heads)
         self.gamma, self.vocab = gamma, vocab
         self._h = ctypes.c_void_p(0)
         w = weights or {}
@@ -173,7 +176,8 @@ class Drafter:
         fields = {}
         for key, fmt in (("attn_norm", "bb.{}.attn_norm"), ("wq", "bb.{}.q"), ("wk", "bb.{}.k"), ("wv", "bb.{}.v"),
                          ("wo", "bb.{}.o"), ("ff_norm", "bb.{}.ff_norm"), ("w_gate", "bb.{}.gate"),
-                         ("w_up", "bb.{}.up"), ("w_down", "bb.{}.down")):
+                         ("w_up", "bb.{}.up"), ("w_down", "bb.{}.down"), ("q_norm", "bb.{}.q_norm"),
+                         ("k_norm", "bb.{}.k_norm")):
             p, a = arr(fmt)
             fields[key] = p
             self._keep.append(a)
@@ -182,7 +186,7 @@ class Drafter:
                          fields["wk"], fields["wv"], fields["wo"], fields["ff_norm"], fields["w_gate"],
                          fields["w_up"], fields["w_down"], _ptr(w.get("out_norm")), _ptr(w.get("out_proj")),
                          _ptr(w.get("markov.w1")), _ptr(w.get("markov.w2")), _ptr(w.get("conf.w")),
-                         _ptr(w.get("conf.b")))
+                         _ptr(w.get("conf.b")), fields["q_norm"], fields["k_norm"])
         self._embed = w.get("embed")   # borrowed by the library: keep it alive
         st = self.lib.dspark_create(ctypes.byref(self.cfg), ctypes.byref(self.w), _stream(stream),
                                     ctypes.byref(self._h))
@@ -252,11 +256,11 @@ class Drafter:
         return out.value
 
     def cache(self, seq_id: int, layer: int, rows: int):
-        """(K, V) views [rows, d] of the library-owned cache of (seq_id, layer)."""
+        """(K, V) views [rows, d_kv] of the library-owned cache of (seq_id, layer)."""
         import torch
         k, v = ctypes.c_void_p(0), ctypes.c_void_p(0)
         self._check(self.lib.dspark_get_cache(self._h, int(seq_id), int(layer), ctypes.byref(k), ctypes.byref(v)))
-        d = self.cfg.d_draft
+        d = self.d_kv
         if self.cfg.dtype == FP32:
             mk = lambda p: torch.as_tensor(_CudaArray(p, (rows, d), "<f4"), device="cuda")
         else:

@@ -103,9 +103,12 @@ __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
     const int chunk = (n_keys + p.n_chunks - 1) / p.n_chunks;
     const int start = min(n_keys, c * chunk), end = min(n_keys, start + chunk);
 
-    const TC* Kb = reinterpret_cast<const TC*>(p.cache) + (int64_t)max(slot, 0) * p.seq_stride + h * hd;
+    // K/V head of query head h and the cache row width (grouped-query attention)
+    const int dkv = p.d_kv ? p.d_kv : d;
+    const int kvh = p.n_kv_heads ? h / (p.n_heads / p.n_kv_heads) : h;
+    const TC* Kb = reinterpret_cast<const TC*>(p.cache) + (int64_t)max(slot, 0) * p.seq_stride + kvh * hd;
     const TC* Vb = Kb + p.kv_off;
-    if (start < end) load_tile<TC>(sm, sm + L.tile_bytes(), Kb, Vb, d, start, end, L);
+    if (start < end) load_tile<TC>(sm, sm + L.tile_bytes(), Kb, Vb, dkv, start, end, L);
     cp_async_commit();
 
     const float scale = rsqrtf((float)hd);
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
         const int nk = min(TK, end - t0);
         if (t0 + TK < end) {
             uint8_t* nxt = sm + (buf ^ 1) * 2 * L.tile_bytes();
-            load_tile<TC>(nxt, nxt + L.tile_bytes(), Kb, Vb, d, t0 + TK, end, L);
+            load_tile<TC>(nxt, nxt + L.tile_bytes(), Kb, Vb, dkv, t0 + TK, end, L);
         }
         cp_async_commit();
         cp_async_wait_1();

@@ -165,12 +165,16 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const int start = c * chunk, end = min(n_keys, start + chunk);
     const int n_tiles = (end - start + TK - 1) / TK;
 
-    const bf16* Kb = reinterpret_cast<const bf16*>(p.cache) + (int64_t)slot * p.seq_stride + h * HD;
+    // K/V head of query head h, and the cache row width (grouped-query attention shares one K/V head
+    // between n_heads / n_kv_heads query heads)
+    const int dkv = p.d_kv ? p.d_kv : d;
+    const int kvh = p.n_kv_heads ? h / (p.n_heads / p.n_kv_heads) : h;
+    const bf16* Kb = reinterpret_cast<const bf16*>(p.cache) + (int64_t)slot * p.seq_stride + kvh * HD;
     const bf16* Vb = Kb + p.kv_off;
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(sm);
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
-        if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, d, start + s * TK, end);
+        if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, dkv, start + s * TK, end);
         cp_async_commit();
     }
 
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         __syncthreads();  // tile t is visible; every warp is done with tile t-1, whose stage is refilled next
         {
             const int tn = t + NS - 1;
-            if (tn < n_tiles) load_kv<HD>(ring + (tn % NS) * L::STAGE, Kb, Vb, d, start + tn * TK, end);
+            if (tn < n_tiles) load_kv<HD>(ring + (tn % NS) * L::STAGE, Kb, Vb, dkv, start + tn * TK, end);
             cp_async_commit();
         }
         const int nk = min(TK, end - (start + t * TK));

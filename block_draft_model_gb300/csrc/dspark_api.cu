@@ -76,6 +76,10 @@ struct dspark_handle {
     float* block_const = nullptr;            // [gamma, d]
     std::vector<void*> wqkv, wo, wgu, wd;    // wqkv [3d, d]; wgu [2F, d] rows (gate f, up f) interleaved
     std::vector<float*> attn_norm, ff_norm;
+    std::vector<float*> q_norm, k_norm;      // [head_dim] per layer (qk_norm)
+    float** k_norm_dev = nullptr;            // device array of the k_norm pointers
+    int nkv = 0, dkv = 0;                    // K/V heads and K/V width
+    bool qk_rope = false;                    // per-head norm and/or rotation of Q and K
     float** attn_norm_dev = nullptr;         // device array of the attn_norm pointers
     float* out_norm = nullptr;
     void* out_proj = nullptr;
@@ -345,7 +349,40 @@ bool norm_chain_ok(const dspark_handle* h, int R, bool lowp) {
         for (const TcWeightStream* w : v)
             if (!w || !w->ready) return false;
     }
-    return tc_stream_ok(R, 3 * d, d) && tc_stream_ok(R, d, d) && tc_stream_ok(R, 2 * F, d) && tc_stream_ok(R, d, F);
+    return tc_stream_ok(R, d + 2 * h->dkv, d) && tc_stream_ok(R, d, d) && tc_stream_ok(R, 2 * F, d) &&
+           tc_stream_ok(R, d, F);
+}
+
+// Per-head norm / rotation arguments shared by the block and ingest forms (layer `layer`).
+QkRope qk_rope_args(const dspark_handle* h, int layer) {
+    QkRope a;
+    a.cache = (char*)h->cache + (size_t)layer * h->layer_stride * h->esz;
+    a.cache_dtype = h->dt;
+    a.layer_stride = h->layer_stride;
+    a.seq_stride = h->seq_stride;
+    a.d_kv = h->dkv;
+    a.max_rows = (int)h->rows;
+    a.seq_len = h->d_len;
+    a.k_norm = h->cfg.qk_norm ? h->k_norm[layer] : nullptr;
+    a.n_heads = h->cfg.n_heads;
+    a.n_kv_heads = h->nkv;
+    a.head_dim = h->hd;
+    a.eps = h->cfg.eps;
+    a.theta = h->cfg.rope_theta;
+    return a;
+}
+
+// The context rows just projected: per-head K norm / rotation in every layer's cache, at the
+// rows' positions (slot 0 at len + m, or the batched row_seq / row_pos), before the length moves.
+cudaError_t ingest_qk(dspark_handle* h, int n, const int* row_seq, const int* row_pos, cudaStream_t st) {
+    if (!h->qk_rope || n <= 0) return cudaSuccess;
+    QkRope a = qk_rope_args(h, 0);
+    a.k_norm_layers = h->cfg.qk_norm ? h->k_norm_dev : nullptr;
+    a.n_layers = h->cfg.n_layers;
+    a.rows = n;
+    a.row_seq = row_seq;
+    a.row_pos = row_pos;
+    return qk_rope_ingest(a, st);
 }
 
 EpiParams cache_epi(const dspark_handle* h, int layer) {
@@ -355,6 +392,7 @@ EpiParams cache_epi(const dspark_handle* h, int layer) {
     ep.seq_stride = h->seq_stride;
     ep.kv_off = h->kv_off;
     ep.d = h->d;
+    ep.d_kv = h->dkv;
     ep.max_rows = (int)h->rows;
     ep.seq_len = h->d_len;
     return ep;
@@ -384,6 +422,12 @@ dspark_status check_cfg(const dspark_config* c, std::string& why) {
     if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
     if ((int64_t)c->max_ctx + c->gamma > (1 << 30)) { why = "max_ctx too large"; return DSPARK_ERR_UNSUPPORTED; }
     if ((size_t)(c->n_layers + 1) * c->d_draft * 4 > 200 * 1024) { why = "(n_layers + 1) * d_draft * 4 bytes must fit 200 KB of shared memory"; return DSPARK_ERR_UNSUPPORTED; }
+    if (c->n_kv_heads < 0 || c->n_heads % (c->n_kv_heads ? c->n_kv_heads : c->n_heads) != 0) {
+        why = "n_heads must be a multiple of n_kv_heads";
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (c->qk_norm != 0 && c->qk_norm != 1) { why = "qk_norm must be 0 or 1"; return DSPARK_ERR_INVALID_ARG; }
+    if (!(c->rope_theta >= 0.f) || !std::isfinite(c->rope_theta)) { why = "rope_theta must be finite and >= 0"; return DSPARK_ERR_INVALID_ARG; }
     return DSPARK_OK;
 }
 
@@ -433,7 +477,7 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
                                     h->Nbuf, (int64_t)h->ingest_rows * d, st));
         }
         Prof pr_kv(h, CAT_INGEST_KV, st);
-        if (n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * d, d)) {
+        if (n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * h->dkv, d)) {
             // all layers in one launch: [nL x row tiles x column tiles] work units
             EpiParams kv = cache_epi(h, 0);
             kv.kind = EPI_KV_CACHE;
@@ -442,7 +486,8 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
                 kv.row_seq = row_seq + t0;
                 kv.row_pos = row_pos + t0;
             }
-            CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * d, d, kv, h->num_sms, h->d_err, st));
+            CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * h->dkv, d, kv, h->num_sms, h->d_err, st));
+            CUDA_TRY(h, ingest_qk(h, n, row_seq ? row_seq + t0 : nullptr, row_seq ? row_pos + t0 : nullptr, st));
             if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
             continue;
         }
@@ -455,10 +500,11 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
             }
             // otherwise slot 0 at len[0] + m: the device length advances after every chunk
             const void* Ni = (const char*)h->Nbuf + (size_t)i * h->ingest_rows * d * h->esz;
-            const void* Wkv = (const char*)h->wqkv[i] + (size_t)d * d * h->esz;  // rows [d, 3d) = [W_k; W_v]
+            const void* Wkv = (const char*)h->wqkv[i] + (size_t)d * d * h->esz;  // rows [d, d + 2 d_kv) = [W_k; W_v]
             CUDA_TRY(h, gemm(h, lp, Ni, d, nullptr, 0, WView{Wkv, at_or_null(h->tc_kv, i), at_or_null(h->ts_kv, i)}, n,
-                             2 * d, d, kv, st));
+                             2 * h->dkv, d, kv, st));
         }
+        CUDA_TRY(h, ingest_qk(h, n, row_seq ? row_seq + t0 : nullptr, row_seq ? row_pos + t0 : nullptr, st));
         if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
     }
     return DSPARK_OK;
@@ -494,7 +540,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     // layers stream faster through the per-kernel tcgen05 path.
     const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
     const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
-    if (B == 1 && !seq_ids && lowp && h->use_persistent && (persistent_fits || h->force_persistent)) {
+    // (the one-launch layers keep one K/V head per query head and no per-head transform)
+    if (B == 1 && !seq_ids && lowp && h->use_persistent && (persistent_fits || h->force_persistent) && !h->qk_rope &&
+        h->nkv == c.n_heads) {
         // every layer in one persistent launch
         DraftPersistArgs a{};
         a.x = h->x;
@@ -547,9 +595,20 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         qkv.seq_ids = seq_ids;
         const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
         if (chain && i > 0)
-            CUDA_TRY(h, chained_gemm(h, R, wqkv, 3 * d, d, qkv, st, CAT_QKV));
+            CUDA_TRY(h, chained_gemm(h, R, wqkv, d + 2 * h->dkv, d, qkv, st, CAT_QKV));
         else
-            CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, 3 * d, d, qkv, actA, adt, st, CAT_QKV));
+            CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, d + 2 * h->dkv, d, qkv, actA, adt, st, CAT_QKV));
+        if (h->qk_rope) {
+            Prof pq(h, CAT_QKV, st);
+            QkRope qr = qk_rope_args(h, i);
+            qr.q = h->q;
+            qr.ldq = d;
+            qr.q_norm = h->cfg.qk_norm ? h->q_norm[i] : nullptr;
+            qr.B = B;
+            qr.gamma = c.gamma;
+            qr.seq_ids = seq_ids;
+            CUDA_TRY(h, qk_rope_block(qr, st));
+        }
         AttnParams ap;
         ap.q = h->q;
         ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
@@ -562,6 +621,8 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         ap.gamma = c.gamma;
         ap.d = d;
         ap.n_heads = c.n_heads;
+        ap.d_kv = h->dkv;
+        ap.n_kv_heads = h->nkv;
         ap.n_chunks = attn_chunks(h, B, max_keys);
         ap.part = h->attn_part;
         ap.tickets = h->attn_tickets;
@@ -984,6 +1045,12 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         if (!w->attn_norm[i] || !w->wq[i] || !w->wk[i] || !w->wv[i] || !w->wo[i] || !w->ff_norm[i] ||
             !w->w_gate[i] || !w->w_up[i] || !w->w_down[i])
             return fail(nullptr, DSPARK_ERR_INVALID_ARG, "layer " + std::to_string(i) + " has a NULL weight");
+    if (cfg->qk_norm) {
+        if (!w->q_norm || !w->k_norm) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "q_norm / k_norm are NULL");
+        for (int i = 0; i < nL; ++i)
+            if (!w->q_norm[i] || !w->k_norm[i])
+                return fail(nullptr, DSPARK_ERR_INVALID_ARG, "layer " + std::to_string(i) + " has a NULL q/k norm");
+    }
 
     dspark_handle* h = new dspark_handle();
     h->cfg = *cfg;
@@ -1011,6 +1078,9 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->d = d;
     h->F = F;
     h->hd = d / cfg->n_heads;
+    h->nkv = cfg->n_kv_heads ? cfg->n_kv_heads : cfg->n_heads;
+    h->dkv = h->nkv * h->hd;
+    h->qk_rope = cfg->qk_norm != 0 || cfg->rope_theta > 0.f;
     h->mH = cfg->n_taps * H;
     h->R = cfg->max_seqs * cfg->gamma;
     const int R = h->R;
@@ -1038,13 +1108,22 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->wd.resize(nL);
     h->attn_norm.resize(nL);
     h->ff_norm.resize(nL);
+    const int dkv = h->dkv;
+    if (cfg->qk_norm) {
+        h->q_norm.resize(nL);
+        h->k_norm.resize(nL);
+    }
     for (int i = 0; i < nL; ++i) {
-        const size_t dd = (size_t)d * d;
-        if (i == 0) CTRY(dalloc(h, &h->wqkv[0], (size_t)nL * 3 * dd * es));  // layers back to back
-        else h->wqkv[i] = (char*)h->wqkv[0] + (size_t)i * 3 * dd * es;
+        const size_t dd = (size_t)d * d, kd = (size_t)dkv * d, qkv = dd + 2 * kd;
+        if (i == 0) CTRY(dalloc(h, &h->wqkv[0], (size_t)nL * qkv * es));  // layers back to back
+        else h->wqkv[i] = (char*)h->wqkv[0] + (size_t)i * qkv * es;
         CTRY(cudaMemcpyAsync(h->wqkv[i], w->wq[i], dd * es, cudaMemcpyDeviceToDevice, st));
-        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + dd * es, w->wk[i], dd * es, cudaMemcpyDeviceToDevice, st));
-        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + 2 * dd * es, w->wv[i], dd * es, cudaMemcpyDeviceToDevice, st));
+        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + dd * es, w->wk[i], kd * es, cudaMemcpyDeviceToDevice, st));
+        CTRY(cudaMemcpyAsync((char*)h->wqkv[i] + (dd + kd) * es, w->wv[i], kd * es, cudaMemcpyDeviceToDevice, st));
+        if (cfg->qk_norm) {
+            CTRY(copy_f32(&h->q_norm[i], w->q_norm[i], h->hd));
+            CTRY(copy_f32(&h->k_norm[i], w->k_norm[i], h->hd));
+        }
         CTRY(copy_mat(&h->wo[i], w->wo[i], dd));
         CTRY(dalloc(h, &h->wgu[i], 2 * (size_t)F * d * es));
         CTRY(cudaMemcpy2DAsync(h->wgu[i], 2 * d * es, w->w_gate[i], d * es, d * es, F, cudaMemcpyDeviceToDevice, st));
@@ -1053,6 +1132,10 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         CTRY(copy_mat(&h->wd[i], w->w_down[i], (size_t)d * F));
         CTRY(copy_f32(&h->attn_norm[i], w->attn_norm[i], d));
         CTRY(copy_f32(&h->ff_norm[i], w->ff_norm[i], d));
+    }
+    if (cfg->qk_norm) {
+        CTRY(dalloc(h, (void**)&h->k_norm_dev, sizeof(float*) * nL));
+        CTRY(cudaMemcpyAsync(h->k_norm_dev, h->k_norm.data(), sizeof(float*) * nL, cudaMemcpyHostToDevice, st));
     }
     CTRY(dalloc(h, (void**)&h->attn_norm_dev, sizeof(float*) * nL));
     CTRY(cudaMemcpyAsync(h->attn_norm_dev, h->attn_norm.data(), sizeof(float*) * nL, cudaMemcpyHostToDevice, st));
@@ -1066,7 +1149,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
 
     // caches
     h->rows = (int64_t)cfg->max_ctx + cfg->gamma;
-    h->kv_off = h->rows * d;
+    h->kv_off = h->rows * dkv;
     h->seq_stride = 2 * h->kv_off;
     h->layer_stride = h->seq_stride * cfg->max_seqs;
     CTRY(dalloc(h, &h->cache, (size_t)h->layer_stride * nL * es));
@@ -1176,13 +1259,13 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         h->tc_wgu.resize(nL);
         h->tc_wd.resize(nL);
         for (int i = 0; i < nL; ++i) {
-            CTRY(tc_prepare(h->tc_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * d, d));
+            CTRY(tc_prepare(h->tc_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * dkv, d));
             if (i == 0) {
                 tc_prepare_grouped(h->tc_kv_a, h->Nbuf, nL, (int64_t)h->ingest_rows * d, h->ingest_rows, d, true);
-                tc_prepare_grouped(h->tc_kv_w, (char*)h->wqkv[0] + (size_t)d * d * es, nL, 3 * (int64_t)d * d, 2 * d, d,
-                                   false);
+                tc_prepare_grouped(h->tc_kv_w, (char*)h->wqkv[0] + (size_t)d * d * es, nL,
+                                   (int64_t)(d + 2 * dkv) * d, 2 * dkv, d, false);
             }
-            CTRY(tc_prepare(h->tc_qkv[i], h->wqkv[i], 3 * d, d));
+            CTRY(tc_prepare(h->tc_qkv[i], h->wqkv[i], d + 2 * dkv, d));
             CTRY(tc_prepare(h->tc_wo[i], h->wo[i], d, d));
             CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));
             CTRY(tc_prepare(h->tc_wd[i], h->wd[i], d, F));
@@ -1212,8 +1295,8 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         h->ts_wgu.resize(nL);
         h->ts_wd.resize(nL);
         for (int i = 0; i < nL; ++i) {
-            CTRY(prep(h->ts_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * d, d));
-            CTRY(prep(h->ts_qkv[i], h->wqkv[i], 3 * d, d));
+            CTRY(prep(h->ts_kv[i], (char*)h->wqkv[i] + (size_t)d * d * es, 2 * dkv, d));
+            CTRY(prep(h->ts_qkv[i], h->wqkv[i], d + 2 * dkv, d));
             CTRY(prep(h->ts_wo[i], h->wo[i], d, d));
             CTRY(prep(h->ts_wgu[i], h->wgu[i], 2 * F, d));
             CTRY(prep(h->ts_wd[i], h->wd[i], d, F));

@@ -14,10 +14,12 @@ __device__ __forceinline__ float act_fn(int act, float g) {
     return 0.5f * g * (1.f + tanhf(c * (g + 0.044715f * g * g * g)));
 }
 
+// Column c of a K/V product ([0, w): K, [w, 2w): V, w = the cache row width) of (slot, pos).
 __device__ __forceinline__ void cache_store(const EpiParams& ep, int slot, int pos, int c, float v, int grp = 0) {
     if (pos < 0 || pos >= ep.max_rows) return;
-    int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) +
-                  (int64_t)pos * ep.d + (c % ep.d);
+    const int w = ep.d_kv ? ep.d_kv : ep.d;
+    int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= w ? ep.kv_off : 0) +
+                  (int64_t)pos * w + (c >= w ? c - w : c);
     if (ep.cache_dtype == DT_BF16)
         reinterpret_cast<bf16*>(ep.cache)[off] = __float2bfloat16_rn(v);
     else
@@ -89,8 +91,9 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
 __device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int pos, int c, const float* v,
                                               int grp = 0) {
     if (pos < 0 || pos >= ep.max_rows) return;
-    const int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= ep.d ? ep.kv_off : 0) +
-                        (int64_t)pos * ep.d + (c % ep.d);
+    const int w = ep.d_kv ? ep.d_kv : ep.d;
+    const int64_t off = grp * ep.group_stride + (int64_t)slot * ep.seq_stride + (c >= w ? ep.kv_off : 0) +
+                        (int64_t)pos * w + (c >= w ? c - w : c);
     if (ep.cache_dtype == DT_BF16) store_bf16x32(reinterpret_cast<bf16*>(ep.cache) + off, v);
     else store_f32x32(reinterpret_cast<float*>(ep.cache) + off, v);
 }
@@ -172,7 +175,8 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
             }
             break;
         case EPI_KV_CACHE:
-            if (full && (ep.d & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
+            // 32 columns never straddle K and V when the cache row width is a multiple of 32
+            if (full && (ep.d & 31) == 0 && ((ep.d_kv ? ep.d_kv : ep.d) & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
                 const int slot = ep.row_seq ? ep.row_seq[m] : 0;
                 const int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
                 cache_store32(ep, slot, pos, n, v, grp);
@@ -180,7 +184,7 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
             }
             break;
         case EPI_QKV:
-            if (full && (ep.d & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
+            if (full && (ep.d & 31) == 0 && ((ep.d_kv ? ep.d_kv : ep.d) & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
                 if (n < ep.d) {
                     if ((ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0) {
                         store_f32x32(ep.out_f32 + (int64_t)m * ep.ldo + n, v);

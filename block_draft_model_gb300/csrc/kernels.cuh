@@ -38,6 +38,7 @@ struct EpiParams {
     int64_t seq_stride = 0;      // elements between sequences
     int64_t kv_off = 0;          // elements from K to V of one sequence
     int d = 0;
+    int d_kv = 0;                // cache row width (0: d); EPI_QKV: Q is columns [0, d), K and V d_kv each
     int max_rows = 0;            // rows per sequence cache (positions must be < max_rows)
     const int* row_seq = nullptr;  // EPI_KV_CACHE: sequence slot per GEMM row (nullptr: slot 0)
     const int* row_pos = nullptr;  // EPI_KV_CACHE: position per GEMM row, -1 = drop (nullptr: len[slot] + m)
@@ -109,6 +110,8 @@ struct AttnParams {
     const int* seq_len;      // context length per slot (block rows sit at len .. len+gamma-1)
     const int* seq_ids;      // slot of sequence b (nullptr: b)
     int B, gamma, d, n_heads;
+    int d_kv = 0, n_kv_heads = 0;  // cache row width and K/V heads (0: d, n_heads); head h reads K/V head
+                                   // h / (n_heads / n_kv_heads)
     int n_chunks;            // split of the (len + gamma) keys of one sequence, 1 .. attn_max_chunks()
     float* part;             // scratch: B * n_heads * n_chunks * gamma * (head_dim + 2) floats
     unsigned int* tickets;   // scratch: B * n_heads counters, zero before and after every launch
@@ -125,6 +128,33 @@ bool attention_tc_ok(int cache_dtype, int head_dim, int gamma);
 int attention_tc_max_chunks();
 cudaError_t attention_tc_init();
 cudaError_t attention_tc(const AttnParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ per-head Q/K norm and rotation
+// The variant of "src/dspark-runtime.js" (noiseNormRope, contextNormRope): every head of a Q
+// or K row is RMS-normalised with a [head_dim] weight (when given) and then turned by the
+// rotary embedding (when theta > 0), rotate-half layout: entries e and e + hd/2 by the angle
+// pos * theta^(-2e/hd).  In place: Q rows in fp32, K rows in the cache (dtype).
+struct QkRope {
+    float* q = nullptr;                  // block form: Q rows [B*gamma, ldq] (row b*gamma + j)
+    int64_t ldq = 0;
+    const float* q_norm = nullptr;       // [head_dim] or nullptr (no norm)
+    const float* k_norm = nullptr;       // block form: this layer's [head_dim] or nullptr
+    const float* const* k_norm_layers = nullptr;  // ingest form: device array of n_layers pointers, or nullptr
+    void* cache = nullptr;               // layer base (block form) / layer 0 base (ingest form)
+    int cache_dtype = DT_BF16;
+    int64_t layer_stride = 0, seq_stride = 0;
+    int d_kv = 0, max_rows = 0;
+    const int* seq_len = nullptr;        // device context length per slot
+    int n_heads = 0, n_kv_heads = 0, head_dim = 0, n_layers = 1;
+    float eps = 0.f, theta = 0.f;
+    int B = 0, gamma = 0;                // block form: rows b*gamma + j at position len[slot] + j
+    const int* seq_ids = nullptr;        // block form: slot of sequence b (nullptr: b)
+    int rows = 0;                        // ingest form: context rows just written
+    const int* row_seq = nullptr;        // ingest form: slot per row (nullptr: slot 0)
+    const int* row_pos = nullptr;        // ingest form: position per row, -1 = dropped (nullptr: len[slot] + m)
+};
+cudaError_t qk_rope_block(const QkRope& a, cudaStream_t st);   // the block's Q rows and K rows of one layer
+cudaError_t qk_rope_ingest(const QkRope& a, cudaStream_t st);  // K rows of new context rows, every layer
 
 // ------------------------------------------------------------------ persistent draft layers
 // Every draft layer of sequence slot 0 (batch 1, bf16) in one cooperative launch,

@@ -74,6 +74,16 @@ typedef struct dspark_config {
     int32_t act;          /* dspark_act                                                 */
     int32_t max_ctx;      /* context capacity per sequence (tokens)                     */
     int32_t max_seqs;     /* number of sequences with their own caches (>= 1)           */
+    /* The variant of "src/dspark-runtime.js" (noiseNormRope / contextNormRope, K/V
+     * width below H).  All zero: multi-head attention without either transform.   */
+    int32_t n_kv_heads;   /* K/V heads (0: n_heads); n_heads % n_kv_heads == 0; query   */
+                          /* head h reads K/V head h / (n_heads / n_kv_heads)           */
+    int32_t qk_norm;      /* 1: RMSNorm of every head of Q and K (weights q_norm,       */
+                          /* k_norm [head_dim] per layer, the same eps)                 */
+    float rope_theta;     /* > 0: rotary embedding of Q and K after the norm, rotate-   */
+                          /* half layout: entries e, e + hd/2 turned by                 */
+                          /* pos * theta^(-2e/hd); context row t at pos t, block row j  */
+                          /* at pos L + j (L = context length)                          */
 } dspark_config;
 
 /* Weights, as device pointers in cfg.dtype unless noted (norm vectors float32).
@@ -88,8 +98,8 @@ typedef struct dspark_weights {
     const void* block_pos;    /* [gamma, d]                                              */
     const float* const* attn_norm;  /* host array of n_layers device pointers, each [d]  */
     const void* const* wq;          /* ... each [d, d]                                   */
-    const void* const* wk;          /* ... each [d, d]                                   */
-    const void* const* wv;          /* ... each [d, d]                                   */
+    const void* const* wk;          /* ... each [d_kv, d], d_kv = n_kv_heads * head_dim   */
+    const void* const* wv;          /* ... each [d_kv, d]                                */
     const void* const* wo;          /* ... each [d, d]                                   */
     const float* const* ff_norm;    /* ... each [d]                                      */
     const void* const* w_gate;      /* ... each [F, d]                                   */
@@ -101,6 +111,8 @@ typedef struct dspark_weights {
     const void* markov_w2;    /* [V, r]        vocab factor (bias = w2 . w1[prev])       */
     const void* conf_w;       /* [d + r]       confidence head weight                    */
     const void* conf_b;       /* [1]           confidence head bias                      */
+    const float* const* q_norm;     /* host array of n_layers device pointers, each       */
+    const float* const* k_norm;     /* [head_dim] (read only when cfg.qk_norm)            */
 } dspark_weights;
 
 typedef struct dspark_handle dspark_handle;
@@ -108,7 +120,7 @@ typedef struct dspark_handle dspark_handle;
 /* Create a drafter on the current CUDA device.  Copies and repacks every weight
  * except `embed` into library-owned device memory (the caller may free them
  * once this returns, after synchronising `stream`), and allocates the context
- * caches: n_layers x max_seqs x 2 x (max_ctx + gamma) x d elements of dtype.
+ * caches: n_layers x max_seqs x 2 x (max_ctx + gamma) x d_kv elements of dtype.
  * Source: initFromDims / DflashDrafter constructor ("module-dflash.ts"), which
  * also rejects d % n_heads != 0.  Returns DSPARK_ERR_INVALID_ARG for a bad
  * config or NULL weight, DSPARK_ERR_UNSUPPORTED for shapes outside the limits

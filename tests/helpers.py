@@ -40,7 +40,8 @@ def make_gpu_drafter(cfg, Wd: dict, max_ctx: int, max_seqs: int = 1):
                        n_layers=cfg.n_layers, ff_mult=cfg.ff_mult, gamma=cfg.gamma, vocab=cfg.vocab,
                        markov_rank=cfg.markov_rank, eps=cfg.eps, dtype=bdm.FP32 if cfg.dtype == "fp32" else bdm.BF16,
                        act=bdm.ACT_GELU_TANH if cfg.act == "gelu_tanh" else bdm.ACT_SILU, max_ctx=max_ctx,
-                       max_seqs=max_seqs, weights=Wd)
+                       max_seqs=max_seqs, weights=Wd, n_kv_heads=cfg.n_kv_heads, qk_norm=cfg.qk_norm,
+                       rope_theta=cfg.rope_theta)
 
 
 def tensor_to_f64(t) -> np.ndarray:
