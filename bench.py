@@ -29,6 +29,7 @@ touches the data path (replicas only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -58,6 +59,10 @@ def parse():
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="> 0: the Markov chain draws its tokens (top-k candidates) instead of the argmax")
     ap.add_argument("--top-k", type=int, default=0)
+    ap.add_argument("--n-kv-heads", type=int, default=0,
+                    help="grouped-query variant: K/V heads of the drafter (0: one per query head)")
+    ap.add_argument("--qk-norm", action="store_true", help="variant: per-head RMSNorm of Q and K")
+    ap.add_argument("--rope-theta", type=float, default=0.0, help="variant: rotary embedding base (0: none)")
     return ap.parse_args()
 
 
@@ -150,22 +155,23 @@ def class_work(cls: str, cfg, T: int, L_total: int, B: int):
     contraction (tensor-bound)."""
     d, F, H, V, r, g, nL, mH = (cfg.d_draft, cfg.ff, cfg.hidden, cfg.vocab, cfg.markov_rank, cfg.gamma,
                                 cfg.n_layers, cfg.feat_dim)
+    dkv = cfg.d_kv  # K/V width (d without grouped-query attention)
     rows = B * g
     gemm_bound = "hbm" if rows <= 16 else "tensor"
     if cls == "ingest_proj":
         return dict(bytes=T * mH * 2 + d * mH * 2 + T * d * 4, flops=2 * T * mH * d,
                     bound="tensor" if T > 16 else "hbm")
     if cls == "ingest_kv":
-        return dict(bytes=nL * (T * d * 2 + 2 * d * d * 2 + T * 2 * d * 2), flops=nL * 2 * T * d * 2 * d,
+        return dict(bytes=nL * (T * d * 2 + 2 * dkv * d * 2 + T * 2 * dkv * 2), flops=nL * 2 * T * d * 2 * dkv,
                     bound="tensor" if T > 16 else "hbm")
     if cls == "out_proj":
         return dict(bytes=V * d * 2 + rows * V * 4, flops=2 * rows * V * d, bound=gemm_bound)
     if cls == "attention":
-        return dict(bytes=2 * (L_total + rows) * d * 2, flops=4 * g * (L_total + rows) * d, bound="hbm")
+        return dict(bytes=2 * (L_total + rows) * dkv * 2, flops=4 * g * (L_total + rows) * d, bound="hbm")
     if cls == "markov_argmax":
         return dict(bytes=V * r * 2 + rows * V * 4, flops=2 * rows * V * r, bound="hbm")
     if cls == "qkv_proj":
-        return dict(bytes=3 * d * d * 2, flops=2 * rows * 3 * d * d, bound=gemm_bound)
+        return dict(bytes=(d + 2 * dkv) * d * 2, flops=2 * rows * (d + 2 * dkv) * d, bound=gemm_bound)
     if cls == "o_proj":
         return dict(bytes=d * d * 2, flops=2 * rows * d * d, bound=gemm_bound)
     if cls == "gate_up_proj":
@@ -173,8 +179,9 @@ def class_work(cls: str, cfg, T: int, L_total: int, B: int):
     if cls == "down_proj":
         return dict(bytes=F * d * 2, flops=2 * rows * F * d, bound=gemm_bound)
     if cls == "draft_layers":  # every layer of a batch-1 draft in one launch
-        return dict(bytes=nL * ((4 * d * d + 3 * F * d) * 2 + 2 * (L_total + rows) * d * 2),
-                    flops=nL * (2 * rows * (4 * d * d + 3 * F * d) + 4 * g * (L_total + rows) * d), bound="hbm")
+        return dict(bytes=nL * ((2 * d * d + 2 * dkv * d + 3 * F * d) * 2 + 2 * (L_total + rows) * dkv * 2),
+                    flops=nL * (2 * rows * (2 * d * d + 2 * dkv * d + 3 * F * d) + 4 * g * (L_total + rows) * d),
+                    bound="hbm")
     if cls == "block_build":
         return dict(bytes=d * H * 2, flops=2 * B * d * H, bound="hbm")
     return dict(bytes=0, flops=0, bound="hbm")
@@ -184,14 +191,15 @@ def draft_bytes_min(cfg, L_total, B=1):
     """Algorithmic bytes of one draft call: every weight once (w2 once), the
     caches of all layers for every sequence, the embedding rows."""
     d, F, H, V, r, nL = cfg.d_draft, cfg.ff, cfg.hidden, cfg.vocab, cfg.markov_rank, cfg.n_layers
-    layers = nL * (4 * d * d + 3 * F * d) * 2
+    dkv = cfg.d_kv
+    layers = nL * (2 * d * d + 2 * dkv * d + 3 * F * d) * 2
     return (layers + d * H * 2 + V * d * 2 + V * r * 2 + B * cfg.gamma * r * 2
-            + nL * 2 * (L_total + B * cfg.gamma) * d * 2 + B * H * 2)
+            + nL * 2 * (L_total + B * cfg.gamma) * dkv * 2 + B * H * 2)
 
 
 def ingest_flops(cfg, T):
     d, mH, nL = cfg.d_draft, cfg.feat_dim, cfg.n_layers
-    return 2 * T * mH * d + nL * 2 * T * d * 2 * d
+    return 2 * T * mH * d + nL * 2 * T * d * 2 * cfg.d_kv
 
 
 def load_peaks():
@@ -263,7 +271,8 @@ class Runner:
         return bdm.Drafter(hidden=cfg.hidden, n_taps=cfg.n_taps, d_draft=cfg.d_draft, n_heads=cfg.n_heads,
                            n_layers=cfg.n_layers, ff_mult=cfg.ff_mult, gamma=cfg.gamma, vocab=cfg.vocab,
                            markov_rank=cfg.markov_rank, eps=cfg.eps, dtype=bdm.BF16, max_ctx=max_ctx,
-                           max_seqs=max_seqs, weights=self.Wd)
+                           max_seqs=max_seqs, weights=self.Wd, n_kv_heads=cfg.n_kv_heads, qk_norm=cfg.qk_norm,
+                           rope_theta=cfg.rope_theta)
 
 
 class FreshContextRunner(Runner):
@@ -458,8 +467,10 @@ class BatchedRunner(Runner):
         return {}
 
 
-def make_runner(name, dev):
+def make_runner(name, dev, variant=None):
     wl = syn.WORKLOADS[name]
+    if variant:  # the same workload on the grouped-query / QK-norm / rotary drafter
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, **variant))
     if name == "minicpm_L1024":
         return FreshContextRunner(wl, dev)
     if name == "gemma_L32768_ingest":
@@ -528,7 +539,9 @@ def main():
     dev = torch.device("cuda", local)
     bdm.build()
     bdm.load()
-    run = make_runner(args.workload, dev)
+    variant = {k: v for k, v in (("n_kv_heads", args.n_kv_heads), ("qk_norm", args.qk_norm),
+                                 ("rope_theta", args.rope_theta)) if v}
+    run = make_runner(args.workload, dev, variant)
     run.setup()
     if args.temperature > 0:
         run.g.set_sampling(args.temperature, args.top_k, 2024)
@@ -638,6 +651,7 @@ def main():
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "token_choice": (f"sampled (temperature {args.temperature}, top-k {args.top_k})"
                                         if args.temperature > 0 else "argmax"),
+                       **({"variant": variant} if variant else {}),
                        "l2": "inputs larger than L2 (weights, caches and features stream > 1 GB per step)"},
             "ctx_tokens_per_s": world * args.steps * run.ctx_tokens_per_step / (ms_max / 1e3),
             "phases": phases, "roofline": roofline, "clocks": clk, "gpu_launches": launches, "e2e": e2e}

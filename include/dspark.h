@@ -135,7 +135,8 @@ void dspark_destroy(dspark_handle* h);
  * updateContext): for T new context rows feats_dev [T, m*H] (dtype, taps
  * concatenated on the feature axis), compute H_ctx = RMSNorm(W_c x) * ctx_norm
  * and, for every layer i, append W_k,i n and W_v,i n with
- * n = RMSNorm(H_ctx) * attn_norm_i to the layer's cache.  T = 0 is a no-op.
+ * n = RMSNorm(H_ctx) * attn_norm_i to the layer's cache (with the variant fields of the
+ * config, the K heads normalised and turned at their positions first).  T = 0 is a no-op.
  * DSPARK_ERR_CAPACITY if the context would exceed max_ctx (nothing launched). */
 dspark_status dspark_ingest_context(dspark_handle* h, const void* feats_dev, int32_t T, void* stream);
 
@@ -144,8 +145,10 @@ dspark_status dspark_ingest_context(dspark_handle* h, const void* feats_dev, int
  * mask_emb[j-1] + block_pos[j]), n_layers of #layer attending over
  * [context ++ block] with no mask, out_norm, base logits U = out_proj y, then
  * for k = 0..gamma-1: logits_k = U_k + w2 w1[prev_k] (prev_0 = last_token,
- * prev_k = token_{k-1}), token_k = argmax (lowest index on ties),
- * conf_k = sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b).
+ * prev_k = token_{k-1}), token_k = argmax (lowest index on ties; a draw instead
+ * when dspark_set_sampling set a temperature), conf_k = sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b).
+ * With the variant fields of the config, the heads of Q and of the block's K rows are
+ * normalised and turned at positions L + j before the attention.
  * Outputs: tokens_dev [gamma] int32, conf_dev [gamma] float, and, if not NULL,
  * logits_dev [gamma, V] float.  The context is not modified. */
 dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens_dev, float* conf_dev,
