@@ -80,6 +80,7 @@ struct dspark_handle {
     float** k_norm_dev = nullptr;            // device array of the k_norm pointers
     int nkv = 0, dkv = 0;                    // K/V heads and K/V width
     bool qk_rope = false;                    // per-head norm and/or rotation of Q and K
+    double* rope_freq = nullptr;             // [head_dim / 2] rotation frequencies (rope_theta > 0)
     float** attn_norm_dev = nullptr;         // device array of the attn_norm pointers
     float* out_norm = nullptr;
     void* out_proj = nullptr;
@@ -369,6 +370,7 @@ QkRope qk_rope_args(const dspark_handle* h, int layer) {
     a.head_dim = h->hd;
     a.eps = h->cfg.eps;
     a.theta = h->cfg.rope_theta;
+    a.freq = h->rope_freq;
     return a;
 }
 
@@ -1132,6 +1134,10 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         CTRY(copy_mat(&h->wd[i], w->w_down[i], (size_t)d * F));
         CTRY(copy_f32(&h->attn_norm[i], w->attn_norm[i], d));
         CTRY(copy_f32(&h->ff_norm[i], w->ff_norm[i], d));
+    }
+    if (cfg->rope_theta > 0.f) {
+        CTRY(dalloc(h, (void**)&h->rope_freq, (size_t)(h->hd / 2) * sizeof(double)));
+        CTRY(qk_rope_freq_fill(cfg->rope_theta, h->hd, h->rope_freq, st));
     }
     if (cfg->qk_norm) {
         CTRY(dalloc(h, (void**)&h->k_norm_dev, sizeof(float*) * nL));

@@ -147,12 +147,15 @@ struct QkRope {
     const int* seq_len = nullptr;        // device context length per slot
     int n_heads = 0, n_kv_heads = 0, head_dim = 0, n_layers = 1;
     float eps = 0.f, theta = 0.f;
+    const double* freq = nullptr;        // [head_dim / 2] theta^(-2e/hd), e < hd/2 (required when theta > 0)
     int B = 0, gamma = 0;                // block form: rows b*gamma + j at position len[slot] + j
     const int* seq_ids = nullptr;        // block form: slot of sequence b (nullptr: b)
     int rows = 0;                        // ingest form: context rows just written
     const int* row_seq = nullptr;        // ingest form: slot per row (nullptr: slot 0)
     const int* row_pos = nullptr;        // ingest form: position per row, -1 = dropped (nullptr: len[slot] + m)
 };
+// Fill dev[0, head_dim / 2) with theta^(-2e/hd), computed on the host in double (theta > 0).
+cudaError_t qk_rope_freq_fill(float theta, int head_dim, double* dev, cudaStream_t st);
 cudaError_t qk_rope_block(const QkRope& a, cudaStream_t st);   // the block's Q rows and K rows of one layer
 cudaError_t qk_rope_ingest(const QkRope& a, cudaStream_t st);  // K rows of new context rows, every layer
 

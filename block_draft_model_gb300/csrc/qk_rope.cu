@@ -5,9 +5,12 @@
 // e = l, l + 32, ... (hd <= 256), the RMS over the head comes from a warp sum,
 // and the angle pos * theta^(-2e/hd) is formed and reduced modulo 2 pi in
 // double precision before the single-precision sine and cosine (a float angle
-// would be off by about 2e-3 rad at position 32768).
+// would be off by about 2e-3 rad at position 32768); the frequencies come from a
+// table built once on the host, so each pair costs a few double operations.
 #include <math.h>
 #include <stdint.h>
+
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -25,7 +28,7 @@ __device__ __forceinline__ void st_elem(bf16* p, float v) { *p = __float2bfloat1
 
 // One head vector v[0, hd) in place: optional RMSNorm with weight w, then optional rotation at pos.
 template <typename T>
-__device__ __forceinline__ void head_norm_rope(T* v, int hd, const float* w, float eps, float theta, int pos) {
+__device__ __forceinline__ void head_norm_rope(T* v, int hd, const float* w, float eps, const double* freq, int pos) {
     const int lane = threadIdx.x & 31, half = hd >> 1;
     float a[MAXP], b[MAXP];
     float ss = 0.f;
@@ -48,14 +51,14 @@ __device__ __forceinline__ void head_norm_rope(T* v, int hd, const float* w, flo
             }
         }
     }
-    if (theta > 0.f) {
+    if (freq) {
         const double two_pi = 6.283185307179586476925286766559;
 #pragma unroll
         for (int i = 0; i < MAXP; ++i) {
             const int e = lane + 32 * i;
             if (e < half) {
-                double ang = (double)pos * pow((double)theta, -2.0 * (double)e / (double)hd);
-                ang -= two_pi * rint(ang / two_pi);
+                double ang = (double)pos * freq[e];
+                ang -= two_pi * rint(ang * (1.0 / two_pi));
                 float sn, cs;
                 sincosf((float)ang, &sn, &cs);
                 const float na = a[i] * cs - b[i] * sn, nb = b[i] * cs + a[i] * sn;
@@ -86,13 +89,12 @@ __global__ void __launch_bounds__(32) k_qk_block(QkRope a) {
     if (slot < 0) return;
     const int pos = a.seq_len[slot] + j;
     if (head < a.n_heads) {
-        head_norm_rope(a.q + (int64_t)m * a.ldq + (int64_t)head * a.head_dim, a.head_dim, a.q_norm, a.eps, a.theta,
-                       pos);
+        head_norm_rope(a.q + (int64_t)m * a.ldq + (int64_t)head * a.head_dim, a.head_dim, a.q_norm, a.eps, a.freq, pos);
     } else {
         if (pos < 0 || pos >= a.max_rows) return;
         TC* k = reinterpret_cast<TC*>(a.cache) + (int64_t)slot * a.seq_stride + (int64_t)pos * a.d_kv +
                 (int64_t)(head - a.n_heads) * a.head_dim;
-        head_norm_rope(k, a.head_dim, a.k_norm, a.eps, a.theta, pos);
+        head_norm_rope(k, a.head_dim, a.k_norm, a.eps, a.freq, pos);
     }
 }
 
@@ -109,15 +111,24 @@ __global__ void __launch_bounds__(32) k_qk_ingest(QkRope a) {
     if (pos < 0 || pos >= a.max_rows) return;
     TC* k = reinterpret_cast<TC*>(a.cache) + (int64_t)layer * a.layer_stride + (int64_t)slot * a.seq_stride +
             (int64_t)pos * a.d_kv + (int64_t)kvh * a.head_dim;
-    head_norm_rope(k, a.head_dim, a.k_norm_layers ? a.k_norm_layers[layer] : nullptr, a.eps, a.theta, pos);
+    head_norm_rope(k, a.head_dim, a.k_norm_layers ? a.k_norm_layers[layer] : nullptr, a.eps, a.freq, pos);
 }
 
 bool args_ok(const QkRope& a) {
     return a.cache && a.seq_len && a.head_dim >= 2 && a.head_dim <= 2 * 32 * MAXP && a.head_dim % 2 == 0 &&
-           a.n_kv_heads >= 1 && a.d_kv == a.n_kv_heads * a.head_dim;
+           a.n_kv_heads >= 1 && a.d_kv == a.n_kv_heads * a.head_dim && (a.theta <= 0.f || a.freq);
 }
 
 }  // namespace
+
+cudaError_t qk_rope_freq_fill(float theta, int head_dim, double* dev, cudaStream_t st) {
+    if (!(theta > 0.f) || head_dim < 2 || !dev) return cudaErrorInvalidValue;
+    std::vector<double> f(head_dim / 2);
+    for (int e = 0; e < head_dim / 2; ++e) f[e] = pow((double)theta, -2.0 * (double)e / (double)head_dim);
+    cudaError_t err = cudaMemcpyAsync(dev, f.data(), f.size() * sizeof(double), cudaMemcpyHostToDevice, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);  // the host table goes out of scope
+    return err;
+}
 
 cudaError_t qk_rope_block(const QkRope& a, cudaStream_t st) {
     if (!args_ok(a) || !a.q || a.n_heads < 1 || a.B < 1 || a.gamma < 1) return cudaErrorInvalidValue;
