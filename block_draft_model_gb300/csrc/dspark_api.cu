@@ -423,7 +423,6 @@ dspark_status check_cfg(const dspark_config* c, std::string& why) {
     if (c->markov_rank % 8 != 0 || c->markov_rank > 1024) { why = "markov_rank must be a multiple of 8, <= 1024"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->hidden % 8 != 0) { why = "hidden must be a multiple of 8"; return DSPARK_ERR_UNSUPPORTED; }
     if ((int64_t)c->max_ctx + c->gamma > (1 << 30)) { why = "max_ctx too large"; return DSPARK_ERR_UNSUPPORTED; }
-    if ((size_t)(c->n_layers + 1) * c->d_draft * 4 > 200 * 1024) { why = "(n_layers + 1) * d_draft * 4 bytes must fit 200 KB of shared memory"; return DSPARK_ERR_UNSUPPORTED; }
     if (c->n_kv_heads < 0 || c->n_heads % (c->n_kv_heads ? c->n_kv_heads : c->n_heads) != 0) {
         why = "n_heads must be a multiple of n_kv_heads";
         return DSPARK_ERR_INVALID_ARG;

@@ -45,9 +45,10 @@ __device__ __forceinline__ void store4(float* o, float a, float b, float c, floa
 
 // Ingest normalisation, one warp per context row (rows_per_warp rows in turn):
 // H = RMSNorm(P) * ctx_norm in registers, then every layer's normalised copy
-// RMSNorm(H) * attn_norm_i with 8/16-byte stores.  The norm vectors are staged
-// once per CTA in shared memory ((n_layers + 1) * d floats).
-constexpr int INW = 8;  // warps per CTA
+// RMSNorm(H) * attn_norm_i with 8/16-byte stores.  The norm vectors are read
+// where they are used (they stay in L1/L2), so the CTAs carry no shared memory
+// and many of them are resident at once.
+constexpr int INW = 4;  // warps per CTA
 
 template <typename TO, int MAXV>
 __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int nsplit, int64_t split_stride,
@@ -55,17 +56,9 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
                                                          const float* __restrict__ ctx_norm,
                                                          const float* const* __restrict__ attn_norm, int n_layers,
                                                          TO* out, int64_t layer_stride, int rows_per_warp) {
-    extern __shared__ __align__(16) float wsm[];  // [n_layers + 1][d]
     pdl_trigger();
     pdl_wait();
     const int nv = d / 4;
-    for (int i = threadIdx.x; i < nv; i += INW * 32)
-        reinterpret_cast<float4*>(wsm)[i] = reinterpret_cast<const float4*>(ctx_norm)[i];
-    for (int l = 0; l < n_layers; ++l) {
-        const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
-        for (int i = threadIdx.x; i < nv; i += INW * 32) reinterpret_cast<float4*>(wsm + (l + 1) * d)[i] = an[i];
-    }
-    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int row0 = (blockIdx.x * INW + (threadIdx.x >> 5)) * rows_per_warp;
     for (int rr = 0; rr < rows_per_warp; ++rr) {
@@ -94,13 +87,13 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
         for (int i = 0; i < MAXV; ++i) ss += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
         ss = warp_sum(ss);
         const float s1 = rsqrtf(ss / (float)d + eps);
-        const float4* cn = reinterpret_cast<const float4*>(wsm);
+        const float4* cn = reinterpret_cast<const float4*>(ctx_norm);
         float ss2 = 0.f;
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
             const int v = lane + 32 * i;
             if (v < nv) {
-                const float4 w = cn[v];
+                const float4 w = __ldg(cn + v);
                 h[i] = make_float4(h[i].x * s1 * w.x, h[i].y * s1 * w.y, h[i].z * s1 * w.z, h[i].w * s1 * w.w);
                 ss2 += h[i].x * h[i].x + h[i].y * h[i].y + h[i].z * h[i].z + h[i].w * h[i].w;
             }
@@ -108,13 +101,13 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
         ss2 = warp_sum(ss2);
         const float s2 = rsqrtf(ss2 / (float)d + eps);
         for (int l = 0; l < n_layers; ++l) {
-            const float4* an = reinterpret_cast<const float4*>(wsm + (l + 1) * d);
+            const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
             TO* o = out + l * layer_stride + (int64_t)row * d;
 #pragma unroll
             for (int i = 0; i < MAXV; ++i) {
                 const int v = lane + 32 * i;
                 if (v < nv) {
-                    const float4 w = an[v];
+                    const float4 w = __ldg(an + v);
                     store4(o + 4 * v, h[i].x * s2 * w.x, h[i].y * s2 * w.y, h[i].z * s2 * w.z, h[i].w * s2 * w.w);
                 }
             }
@@ -270,21 +263,13 @@ cudaError_t launch_ingest_norm(const float* P, int nsplit, int64_t split_stride,
                                const float* ctx_norm,
                                const float* const* attn_norm_dev, int n_layers, void* out, int64_t layer_stride,
                                cudaStream_t st) {
-    const size_t sm = (size_t)(n_layers + 1) * d * sizeof(float);
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_ingest_norm<TO, MAXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
-    // about two CTAs per SM; each CTA stages the norm vectors once
+    // up to four CTAs per SM before a warp takes more than one row
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int rpw = std::max(1, (rows + INW * 2 * sms - 1) / (INW * 2 * sms));
+    const int rpw = std::max(1, (rows + INW * 4 * sms - 1) / (INW * 4 * sms));
     const int blocks = (rows + INW * rpw - 1) / (INW * rpw);
-    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, sm, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
+    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, 0, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
            attn_norm_dev, n_layers, (TO*)out, layer_stride, rpw);
     note_launch();
     return cudaGetLastError();
@@ -308,7 +293,7 @@ cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int ro
                         void* out, int64_t layer_stride, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     if (nsplit < 1 || (nsplit > 1 && split_stride < (int64_t)rows * d)) return cudaErrorInvalidValue;
-    if (d % 4 != 0 || d > 4096 || (size_t)(n_layers + 1) * d * sizeof(float) > 200 * 1024) return cudaErrorInvalidValue;
+    if (d % 4 != 0 || d > 4096) return cudaErrorInvalidValue;
     if (out_dtype == DT_BF16)
         return ingest_norm_t<bf16>(P, nsplit, split_stride, rows, d, eps, ctx_norm, attn_norm_dev, n_layers, out,
                                    layer_stride, st);
