@@ -14,7 +14,7 @@ import numpy as np
 import oracle
 import synthetic as syn
 
-# spec tolerances: max|dlogit| <= REL * max|logit|
+# parity tolerances: max|dlogit| <= REL * max|logit| (bf16 weights and caches; fp32 drafter)
 REL_BF16 = 2e-2
 REL_FP32 = 1e-4
 
