@@ -151,6 +151,7 @@ struct dspark_handle {
     void* Nbuf = nullptr;
     DevBuf rowmap;                           // row_seq, row_pos (grow-only)
     DevBuf stage_in, stage_out;              // host-call staging (grow-only)
+    cudaEvent_t in_copied = nullptr;         // the host features are in stage_in
 
     std::string err = "no error";
     long long launches_at_create = 0;
@@ -1017,6 +1018,7 @@ void dspark_destroy(dspark_handle* h) {
     for (void* p : h->allocs) cudaFree(p);
     if (h->rowmap.p) cudaFree(h->rowmap.p);
     if (h->stage_in.p) cudaFree(h->stage_in.p);
+    if (h->in_copied) cudaEventDestroy(h->in_copied);
     if (h->stage_out.p) cudaFree(h->stage_out.p);
     for (auto& g : h->graphs) destroy_graph(g);
     if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
@@ -1400,10 +1402,14 @@ dspark_status dspark_ingest_context_host(dspark_handle* h, const void* feats_hos
     cudaStream_t st = (cudaStream_t)stream;
     const size_t bytes = (size_t)T * h->mH * h->esz;
     CUDA_TRY(h, grow(h->stage_in, bytes));
+    if (!h->in_copied) CUDA_TRY(h, cudaEventCreateWithFlags(&h->in_copied, cudaEventDisableTiming));
     CUDA_TRY(h, cudaMemcpyAsync(h->stage_in.p, feats_host, bytes, cudaMemcpyHostToDevice, st));
+    CUDA_TRY(h, cudaEventRecord(h->in_copied, st));
     dspark_status s = dspark_ingest_context(h, h->stage_in.p, T, stream);
     if (s != DSPARK_OK) return s;
-    CUDA_TRY(h, cudaStreamSynchronize(st));
+    // the caller may reuse feats_host once it has been read; the ingest itself finishes in stream
+    // order, so a draft submitted next queues behind it without an idle gap on the device
+    CUDA_TRY(h, cudaEventSynchronize(h->in_copied));
     return DSPARK_OK;
 }
 

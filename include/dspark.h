@@ -172,10 +172,13 @@ dspark_status dspark_draft_batched(dspark_handle* h, int32_t n_seqs, const int32
                                    const int32_t* last_tokens_dev, int32_t* tokens_dev, float* conf_dev,
                                    float* logits_dev, void* stream);
 
-/* Host-buffer forms of ingest and draft for sequence 0: the library copies
- * feats_host [T, m*H] in, runs the step, copies tokens/conf (and logits, if
- * logits_host is not NULL) out, and synchronises `stream`.  Same arithmetic
- * as the device-pointer calls. */
+/* Host-buffer forms of ingest and draft for sequence 0, same arithmetic as the
+ * device-pointer calls.  dspark_ingest_context_host copies feats_host [T, m*H] in
+ * (through a library staging buffer, on `stream`), enqueues the ingest and returns
+ * once feats_host has been read; the ingest completes in stream order.
+ * dspark_draft_host runs the draft, copies tokens/conf (and logits, if logits_host
+ * is not NULL) out and synchronises `stream`.  Consecutive host-buffer calls of one
+ * handle go on one stream (the staging buffers are reused). */
 dspark_status dspark_ingest_context_host(dspark_handle* h, const void* feats_host, int32_t T, void* stream);
 dspark_status dspark_draft_host(dspark_handle* h, int32_t last_token, int32_t* tokens_host, float* conf_host,
                                 float* logits_host, void* stream);

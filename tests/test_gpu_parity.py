@@ -127,6 +127,7 @@ def test_host_buffer_calls_match_device_calls():
     b = make_gpu_drafter(cfg, Wd, max_ctx=32)
     Xh = torch.from_numpy(X.view(np.int16)).pin_memory()
     b.ingest_context_host(Xh)
+    Xh.zero_()  # the call returns once the features have been read: reusing the buffer changes nothing
     tb = torch.empty(cfg.gamma, dtype=torch.int32).pin_memory()
     cb = torch.empty(cfg.gamma, dtype=torch.float32).pin_memory()
     lb = torch.empty(cfg.gamma, cfg.vocab, dtype=torch.float32).pin_memory()
