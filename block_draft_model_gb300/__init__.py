@@ -24,7 +24,7 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
             "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error",
-            "dspark_set_sampling"]
+            "dspark_set_sampling", "dspark_selftest_wait"]
 
 
 class DsparkError(RuntimeError):
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_draft_host": ([vp, i32, vp, vp, vp, vp], i32),
         "dspark_reset": ([vp, i32, vp], i32),
         "dspark_set_sampling": ([vp, ctypes.c_float, i32, ctypes.c_uint64, vp], i32),
+        "dspark_selftest_wait": ([i32, ctypes.POINTER(i32)], i32),
         "dspark_context_length": ([vp, i32, ctypes.POINTER(i32)], i32),
         "dspark_check": ([vp, ctypes.POINTER(i32)], i32),
         "dspark_get_cache": ([vp, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp)], i32),
@@ -149,6 +150,20 @@ class _CudaArray:
     def __init__(self, ptr: int, shape, typestr: str):
         self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
                                          "version": 3, "strides": None}
+
+
+def selftest_wait(which: int) -> int:
+    """Run one of the library's bounded device waits on words that nothing completes;
+    returns the error word it recorded (DEVERR_TIMEOUT when the wait gave up)."""
+    lib = load()
+    w = ctypes.c_int32(0)
+    st = lib.dspark_selftest_wait(int(which), ctypes.byref(w))
+    if st != OK:
+        raise DsparkError(st, lib.dspark_last_error(None).decode())
+    return int(w.value)
+
+
+DEVERR_TIMEOUT = 16
 
 
 class Drafter:

@@ -731,6 +731,23 @@ bool draft_persistent_ok(const DraftPersistArgs& a) {
     return nslot >= 4 && a.maps;
 }
 
+namespace {
+// The layers' grid barrier with one CTA where two are expected: it gives up after its limit.
+__global__ void __launch_bounds__(NCW * 32) k_barrier_selftest(unsigned long long* bar, int* err) {
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    grid_barrier(bar, 2ull, err, &abort_flag);
+}
+}  // namespace
+
+cudaError_t persistent_wait_selftest(void* scratch, int* err, cudaStream_t st) {
+    if (!scratch || !err) return cudaErrorInvalidValue;
+    k_barrier_selftest<<<1, NCW * 32, 0, st>>>(reinterpret_cast<unsigned long long*>(scratch), err);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t draft_persistent(const DraftPersistArgs& a, int num_sms, cudaStream_t st) {
     if (!draft_persistent_ok(a)) return cudaErrorInvalidValue;
     PersistParams p{};

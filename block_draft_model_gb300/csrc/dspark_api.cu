@@ -1459,6 +1459,35 @@ dspark_status dspark_set_sampling(dspark_handle* h, float temperature, int32_t t
     return DSPARK_OK;
 }
 
+dspark_status dspark_selftest_wait(int32_t which, int32_t* word_host) {
+    if (which < 0 || which > 4) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "which must be in [0, 4]");
+    void* scratch = nullptr;
+    int* err = nullptr;
+    cudaStream_t st = nullptr;
+    auto done = [&](dspark_status s, const std::string& why) {
+        if (st) cudaStreamDestroy(st);
+        if (scratch) cudaFree(scratch);
+        if (err) cudaFree(err);
+        return s == DSPARK_OK ? s : fail(nullptr, s, why);
+    };
+    cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaMalloc(&scratch, 64);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, 64, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int), st);
+    if (e == cudaSuccess) {
+        if (which <= 2) e = markov_wait_selftest(which, scratch, err, st);
+        else if (which == 3) e = persistent_wait_selftest(scratch, err, st);
+        else e = mbar_wait_selftest(err, st);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    int v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return done(DSPARK_ERR_CUDA, std::string("self-test: ") + cudaGetErrorString(e));
+    if (word_host) *word_host = v;
+    return done(DSPARK_OK, "");
+}
+
 dspark_status dspark_check(dspark_handle* h, int32_t* word_host) {
     if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
     int v = 0;

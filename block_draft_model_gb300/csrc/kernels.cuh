@@ -278,6 +278,14 @@ bool sample_ok(int V, int r, int top_k, int num_sms);
 cudaError_t sample_init();
 cudaError_t markov_sample_step(const SampleParams& p, int num_sms, cudaStream_t st);
 
+// Self-tests of the bounded device waits (each on words that nothing completes; every one gives
+// up after about a second and ORs DEVERR_TIMEOUT into *err): which = 0 the FMA chain's arrival
+// count, 1 the resident chain's barrier, 2 the cooperative chain's barrier (scratch: 64 zeroed
+// bytes); the persistent layers' grid barrier; the tensor-core kernels' mbarrier wait.
+cudaError_t markov_wait_selftest(int which, void* scratch, int* err, cudaStream_t st);
+cudaError_t persistent_wait_selftest(void* scratch, int* err, cudaStream_t st);
+cudaError_t mbar_wait_selftest(int* err, cudaStream_t st);
+
 bool markov_chain_fma_ok(const MarkovParams& p, int num_sms);
 cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st);
 

@@ -604,6 +604,17 @@ __device__ __forceinline__ uint64_t chain_clock() {
     return t;
 }
 
+// One thread waits (bounded, about a second) until *counter >= target; true when it gave up.
+__device__ __forceinline__ bool wait_arrivals(const unsigned long long* counter, unsigned long long target) {
+    const uint64_t t0 = chain_clock();
+    while (true) {
+        unsigned long long cur;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(counter) : "memory");
+        if (cur >= target) return false;
+        if (chain_clock() - t0 > 1000000000ull) return true;
+    }
+}
+
 // acc += sum over the 8 bf16 pairs of w and e, in order
 __device__ __forceinline__ float fma_chunk(const uint4& w, const uint4& e, float acc) {
     asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
@@ -773,18 +784,7 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
             }
             // lane 0 waits (bounded) for every CTA's arrival, then the warp reads the words once
             bool timed_out = false;
-            if (lane == 0) {
-                const uint64_t t0 = chain_clock();
-                while (true) {
-                    unsigned long long cur;
-                    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(arrived + k * NF + n) : "memory");
-                    if (cur >= (unsigned long long)G) break;
-                    if (chain_clock() - t0 > 1000000000ull) {
-                        timed_out = true;
-                        break;
-                    }
-                }
-            }
+            if (lane == 0) timed_out = wait_arrivals(arrived + k * NF + n, (unsigned long long)G);
             __syncwarp();
             unsigned long long m = 0ull;
             for (int c = lane; c < G; c += 32) {
@@ -831,6 +831,19 @@ int g_res_ok[3] = {0, 0, 0};  // the resident chain's kernels for r = 64, 128, 2
 int g_res_budget = 0;         // its dynamic shared memory
 
 bool g_fma_ok = false;         // the FMA chain's kernels
+
+// Each bounded wait of the chains on words that nothing completes: one CTA, so the FMA chain's
+// arrival count (target 1, nobody arrives), the resident chain's barrier and the cooperative
+// chain's barrier (two CTAs expected) all give up after their limit and record the timeout.
+__global__ void k_wait_selftest(int which, unsigned long long* w64, unsigned int* w32, int* err) {
+    if (which == 0) {
+        if (threadIdx.x == 0 && wait_arrivals(w64, 1ull)) atomicOr(err, 16);
+    } else if (which == 1) {
+        res_barrier(w64, 2ull, err);
+    } else {
+        grid_sync(w32, w32 + 1, 2u, err);
+    }
+}
 
 template <int KD, int NF>
 cudaError_t fma_attr(int bytes) {
@@ -1021,6 +1034,14 @@ cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream
     else e = cudaLaunchKernelEx(&cfg, k_markov_chain_res<8>, p, n_cache);
     note_launch();
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t markov_wait_selftest(int which, void* scratch, int* err, cudaStream_t st) {
+    if (which < 0 || which > 2 || !scratch || !err) return cudaErrorInvalidValue;
+    k_wait_selftest<<<1, 64, 0, st>>>(which, reinterpret_cast<unsigned long long*>(scratch),
+                                       reinterpret_cast<unsigned int*>(scratch) + 4, err);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -502,7 +502,28 @@ bool encode(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tensor-core kernels' mbarrier wait on a barrier that nothing arrives at: it gives up after
+// its limit, as a stalled copy or MMA would make it.
+__global__ void k_mbar_selftest(int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag)) atomicOr(err, DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t mbar_wait_selftest(int* err, cudaStream_t st) {
+    if (!err) return cudaErrorInvalidValue;
+    k_mbar_selftest<<<1, 32, 0, st>>>(err);
+    note_launch();
+    return cudaGetLastError();
+}
 
 bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && N >= 1 && K >= BK && K % 8 == 0; }
 

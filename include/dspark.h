@@ -205,6 +205,17 @@ dspark_status dspark_reset(dspark_handle* h, int32_t seq_id, void* stream);
  * returns DSPARK_ERR_DEVICE if the device error word is set. */
 dspark_status dspark_context_length(dspark_handle* h, int32_t seq_id, int32_t* out_host);
 
+/* Self-test of the bounded device waits (failure detection without a fault): runs
+ * one of the library's waits on device words that nothing completes, in a small
+ * kernel of its own on a private stream: which = 0 the single-sequence Markov
+ * chain's arrival count, 1 the resident chain's barrier, 2 the cooperative
+ * chain's barrier, 3 the one-launch layers' grid barrier, 4 the tensor-core
+ * kernels' mbarrier wait.  The wait gives up after its limit (about one second)
+ * and the kernel returns normally; *word_host (may be NULL) receives the error
+ * word it recorded, DSPARK_DEVERR_TIMEOUT when the wait gave up.  The device
+ * stays usable.  Synchronises that stream; INVALID_ARG for another `which`. */
+dspark_status dspark_selftest_wait(int32_t which, int32_t* word_host);
+
 /* Read and clear the device error word (synchronises the device).  *word_host
  * (may be NULL) receives it: 0 = none, otherwise a DSPARK_DEVERR_* bit set. */
 #define DSPARK_DEVERR_TOKEN_RANGE 1   /* a batched anchor token outside [0, V)        */
