@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const bool prenorm = sn.x != nullptr;
     const bool rowscale = !prenorm && sn.ssp != nullptr;
     const bool xbm = ep.ssp != nullptr;  // EPI_ADD_F32 that also writes the next operand and row sums
+    // EPI_ADD_F32 reduced in the cluster: the residual entries this thread will own in the final
+    // epilogue (at most two items of four activation rows), loaded while the weights stream; no other
+    // thread of the kernel touches them
+    const bool xpre_on = splits > 1 && cluster_reduce && ep.kind == EPI_ADD_F32;
+    float xpre[2][4];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / splits, split = blockIdx.x - tile * splits;
@@ -282,6 +287,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
     } else {
         pdl_wait();  // the epilogue reads and writes buffers shared with earlier kernels
+        if (xpre_on) {
+            const int t = threadIdx.x - 64, rps = BM / splits;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int it = h * 128 + t;
+                const int nn = n0 + split * rps + (it >> 2), cg = it & 3;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    xpre[h][qq] = (it < rps * 4 && nn < N && 4 * cg + qq < M)
+                                      ? __ldcg(ep.out_f32 + (int64_t)(4 * cg + qq) * ep.ldo + nn)
+                                      : 0.f;
+            }
+        }
         if (prenorm) build_prenorm(sn, M, K, kb0, kb1, sX, full, empty, rsc, abort_flag, bfail);
         if (rowscale) build_rowscale(sn, K, rs_red, rsc);
         const int q = warp & 3;
@@ -438,11 +456,23 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 } else {
                     float x2[4] = {0.f, 0.f, 0.f, 0.f};
                     if (ok && n < N) {
+                        const int h = it0 >> 7;  // 0 or 1: the prefetched residual of this item
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             if (4 * cg + q < M) {
-                                if (xbm) x2[q] = epi_add_xb(ep, 4 * cg + q, n, v4[q]);
-                                else epi_one(ep, 4 * cg + q, n, v4[q]);
+                                if (xpre_on) {
+                                    const float xn = (h ? xpre[1][q] : xpre[0][q]) + v4[q];
+                                    ep.out_f32[(int64_t)(4 * cg + q) * ep.ldo + n] = xn;
+                                    if (xbm) {
+                                        reinterpret_cast<bf16*>(ep.xb)[(int64_t)(4 * cg + q) * ep.ld_xb + n] =
+                                            __float2bfloat16(xn * ep.xb_g[n]);
+                                        x2[q] = xn * xn;
+                                    }
+                                } else if (xbm) {
+                                    x2[q] = epi_add_xb(ep, 4 * cg + q, n, v4[q]);
+                                } else {
+                                    epi_one(ep, 4 * cg + q, n, v4[q]);
+                                }
                             }
                     }
                     if (xbm) {
