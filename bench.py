@@ -484,12 +484,33 @@ def make_runner(name, dev, variant=None):
 
 # --------------------------------------------------------------------------- main
 
+def variant_of(args):
+    """The grouped-query / QK-norm / rotary options given on the command line."""
+    return {k: v for k, v in (("n_kv_heads", args.n_kv_heads), ("qk_norm", args.qk_norm),
+                              ("rope_theta", args.rope_theta)) if v}
+
+
+def arm_config(wl, world, args, variant=None):
+    """The `config` object both arms print for a workload."""
+    cfg = wl.cfg
+    return {"workload": wl.name, "ctx_len": wl.ctx_len, "sequences": wl.n_seqs, "gamma": cfg.gamma,
+            "d_draft": cfg.d_draft, "vocab": cfg.vocab,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "token_choice": (f"sampled (temperature {args.temperature}, top-k {args.top_k})"
+                             if args.temperature > 0 else "argmax"),
+            **({"variant": variant} if variant else {}),
+            "l2": "inputs larger than L2 (weights, caches and features stream > 1 GB per step)"}
+
+
 def reference_arm(args):
     """The CPU oracle on the default workload, timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    variant = variant_of(args)
     wl = syn.WORKLOADS[args.workload]
+    if variant:
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, **variant))
     cfg = wl.cfg
     T = wl.ctx_len or 1024
     W = syn.make_weights(cfg, seed=0)
@@ -498,10 +519,12 @@ def reference_arm(args):
     import oracle
     dr = oracle.Drafter(cfg, W)
 
+    sample = (args.temperature, args.top_k, 2024, 0) if args.temperature > 0 else None
+
     def one(i):
         dr.reset(0)
         dr.ingest(pool[i % 2])
-        dr.draft(int(anchors[i % 64]))
+        dr.draft(int(anchors[i % 64]), sample=sample)
 
     n_w = max(1, args.warmup)
     for i in range(n_w):
@@ -516,10 +539,11 @@ def reference_arm(args):
     dt = time.perf_counter() - t0
     v = n / dt
     sample = f"{n} steps of ingest {min(T, 4096)} rows + 1 block (fp64 numpy, {cpu_cores()} threads)"
-    line = {"impl": "reference", "metric": f"draft blocks/s ({wl.name}, CPU oracle)", "value": v,
+    # the same metric, unit, direction and config as this workload's GPU line
+    line = {"impl": "reference", "metric": make_runner(args.workload, None, variant).metric, "value": v,
             "unit": "blocks/s", "n_gpus": args.gpus, "steps": n, "warmup": n_w, "ms_per_step": 1e3 * dt / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "ctx_len": T, "gamma": cfg.gamma, "batch": 1},
+            "config": arm_config(wl, 1, args, variant),
             "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -539,8 +563,7 @@ def main():
     dev = torch.device("cuda", local)
     bdm.build()
     bdm.load()
-    variant = {k: v for k, v in (("n_kv_heads", args.n_kv_heads), ("qk_norm", args.qk_norm),
-                                 ("rope_theta", args.rope_theta)) if v}
+    variant = variant_of(args)
     run = make_runner(args.workload, dev, variant)
     run.setup()
     if args.temperature > 0:
@@ -646,13 +669,7 @@ def main():
     line = {"metric": run.metric, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
             "warmup": nw, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": run.wl.name, "ctx_len": run.wl.ctx_len, "sequences": B, "gamma": cfg.gamma,
-                       "d_draft": cfg.d_draft, "vocab": cfg.vocab,
-                       "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "token_choice": (f"sampled (temperature {args.temperature}, top-k {args.top_k})"
-                                        if args.temperature > 0 else "argmax"),
-                       **({"variant": variant} if variant else {}),
-                       "l2": "inputs larger than L2 (weights, caches and features stream > 1 GB per step)"},
+            "config": arm_config(run.wl, world, args, variant),
             "ctx_tokens_per_s": world * args.steps * run.ctx_tokens_per_step / (ms_max / 1e3),
             "phases": phases, "roofline": roofline, "clocks": clk, "gpu_launches": launches, "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(run, FreshContextRunner):
