@@ -66,3 +66,30 @@ def test_host_side_errors_without_gpu(lib):
     assert lib.dspark_ingest_context(None, None, 4, None) == bdm.ERR_INVALID_ARG
     assert lib.dspark_draft(None, 0, None, None, None, None) == bdm.ERR_INVALID_ARG
     lib.dspark_destroy(None)
+
+
+def test_variant_and_sampling_arguments_without_gpu(lib):
+    """The grouped-query / QK-norm / rotary config fields, the sampler and the wait
+    self-test reject bad arguments before any device work."""
+    import block_draft_model_gb300 as bdm
+    h = ctypes.c_void_p(0)
+
+    def create(**kw):
+        cfg = bdm.Config(256, 3, 128, 4, 2, 2, 4, 1024, 32, 1e-6, 0, 0, 64, 1)
+        for k, v in kw.items():
+            setattr(cfg, k, v)
+        return lib.dspark_create(ctypes.byref(cfg), None, None, ctypes.byref(h))
+
+    assert create(n_kv_heads=3) == bdm.ERR_INVALID_ARG
+    assert b"multiple of n_kv_heads" in lib.dspark_last_error(None)
+    assert create(n_kv_heads=-1) == bdm.ERR_INVALID_ARG
+    assert create(qk_norm=2) == bdm.ERR_INVALID_ARG
+    assert create(rope_theta=-1.0) == bdm.ERR_INVALID_ARG
+    assert create(rope_theta=float("inf")) == bdm.ERR_INVALID_ARG
+    # a valid variant config gets past the config check to the weight check
+    assert create(n_kv_heads=2, qk_norm=1, rope_theta=10000.0) == bdm.ERR_INVALID_ARG
+    assert b"weights are NULL" in lib.dspark_last_error(None)
+    assert not h.value
+    assert lib.dspark_set_sampling(None, ctypes.c_float(1.0), 0, 0, None) == bdm.ERR_INVALID_ARG
+    for which in (-1, 5, 100):
+        assert lib.dspark_selftest_wait(which, None) == bdm.ERR_INVALID_ARG
