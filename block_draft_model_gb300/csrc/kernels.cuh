@@ -237,7 +237,8 @@ cudaError_t markov_finish(const float* part_v, const int* part_i, int nchunks, c
 cudaError_t markov_chain(const MarkovParams& p, unsigned int* bar_count, unsigned int* bar_gen, cudaStream_t st);
 // Up to 8 sequences with bf16 weights and r in {64, 128, 256}: one cooperative CTA
 // per SM keeps its slice of w2 in shared memory for the whole chain and runs the
-// dot products on the tensor cores.
+// dot products on the warp MMA (the sequences are its N columns).  The draft step
+// takes it for 3 to 8 sequences; one or two take the FMA form below.
 cudaError_t markov_chain_resident_init();  // once per process/device
 bool markov_chain_resident_ok(const MarkovParams& p);
 cudaError_t markov_chain_resident(const MarkovParams& p, int num_sms, cudaStream_t st);

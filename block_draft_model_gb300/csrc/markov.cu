@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(NT) k_markov_chain(MarkovParams p, unsigned in
 }
 
 // ---- resident form: up to 8 sequences, bf16 weights, r = 64, 128 or 256 ------------
+// (the draft step uses it for 3 to 8 sequences; one or two take the FMA form further down)
 // One CTA per SM for the whole chain.  CTA c owns vocabulary rows
 // [c * rows, (c + 1) * rows) for every sequence and keeps as many of its w2
 // rows as fit in shared memory for all gamma positions (the rest are read
