@@ -101,3 +101,48 @@ def test_brute_force_pin_catches_transposed_query(monkeypatch):
     logits = dr.draft(4)[2]
     blogits = brute_force_draft(cfg, W, oracle.to_f64(X).tolist(), 4)[2]
     assert np.max(np.abs(logits - np.array(blogits))) > 1e-6
+
+
+def _layer_norm(x, w, eps):
+    c = x - np.mean(x, axis=-1, keepdims=True)
+    return c / np.sqrt(np.mean(c * c, axis=-1, keepdims=True) + eps) * w
+
+
+def _confidence_without_e(self, y_k, e):
+    return od.confidence(y_k, np.zeros_like(e), self.w["conf.w"], self.w["conf.b"][0])
+
+
+def _block_without_positions(self, anchor):
+    cfg, w = self.cfg, self.w
+    x = np.empty((cfg.gamma, cfg.d_draft))
+    x[0] = w["tok_proj"] @ od.to_f64(self.raw["embed"][anchor])
+    for j in range(1, cfg.gamma):
+        x[j] = w["mask_emb"][j - 1]
+    return x
+
+
+def _backbone_without_out_norm(self, anchor, seq=0, probs_out=None):
+    Ks, Vs = self._cache(seq)
+    x = self.block_input(anchor)
+    for i in range(self.cfg.n_layers):
+        x = self.layer(i, x, Ks[i], Vs[i], probs_out)
+    return x
+
+
+MORE_MUTANTS = {
+    "LayerNorm (mean subtracted) instead of RMSNorm": (od, "rmsnorm", _layer_norm),
+    "confidence without the previous token's w1 row": (od.Drafter, "confidence", _confidence_without_e),
+    "block position rows dropped": (od.Drafter, "block_input", _block_without_positions),
+    "out_norm skipped": (od.Drafter, "backbone", _backbone_without_out_norm),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MORE_MUTANTS))
+def test_brute_force_pin_catches_more_mistakes(monkeypatch, name):
+    cfg = tiny_cfg(gamma=3)
+    W = syn.make_weights(cfg, seed=24, norm_std=0.3, std=0.3)
+    X = syn.make_feats(cfg, 5, seed=24)
+    assert _max_diff(cfg, W, X, 4) < 1e-12
+    owner, attr, fn = MORE_MUTANTS[name]
+    monkeypatch.setattr(owner, attr, fn)
+    assert _max_diff(cfg, W, X, 4) > 1e-6, name
