@@ -17,7 +17,6 @@ from .dspark_oracle import (  # noqa: F401
     gelu_tanh,
     head_rmsnorm,
     linear,
-    markov_logits,
     rmsnorm,
     rope,
     sample_candidates,

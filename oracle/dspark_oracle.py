@@ -225,13 +225,6 @@ def sample_token(logits: np.ndarray, temperature: float, top_k: int, seed: int, 
     return int(cand[int(np.argmax(z))])
 
 
-def markov_logits(U_k: np.ndarray, w1: np.ndarray, w2: np.ndarray, prev: int):
-    """``#markov`` for one position: e = w1[prev] (row gather, [r]); bias = w2 e
-    (w2 stored [V, r]); logits = U_k + bias.  Returns (logits [V], e [r])."""
-    e = to_f64(w1[prev])
-    return U_k + to_f64(w2) @ e, e
-
-
 def confidence(y_k: np.ndarray, e: np.ndarray, conf_w: np.ndarray, conf_b: float) -> float:
     """``#confidence``: sigmoid([y_k ; e] . conf_w + conf_b) (R9)."""
     z = float(np.concatenate([y_k, e]) @ conf_w) + float(conf_b)

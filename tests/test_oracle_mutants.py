@@ -8,7 +8,7 @@ import oracle
 import oracle.dspark_oracle as od
 import synthetic as syn
 
-from test_oracle_pins import brute_force_draft, tiny_cfg
+from test_oracle_pins import brute_force_draft, check_gelu_tanh, tiny_cfg
 
 
 def _no_scale_attention(Q, K, V, n_heads, probs_out=None, n_kv_heads=0):
@@ -146,3 +146,18 @@ def test_brute_force_pin_catches_more_mistakes(monkeypatch, name):
     owner, attr, fn = MORE_MUTANTS[name]
     monkeypatch.setattr(owner, attr, fn)
     assert _max_diff(cfg, W, X, 4) > 1e-6, name
+
+
+def _gelu_erf(g):
+    """The exact (erf) GELU, a plausible stand-in for the tanh form."""
+    import scipy.special
+    return 0.5 * g * (1.0 + scipy.special.erf(g / np.sqrt(2.0)))
+
+
+def test_gelu_pin_catches_erf_for_tanh(monkeypatch):
+    """The brute force restates the tanh formula, so it cannot tell the two GELU forms
+    apart; the library-routine pin must."""
+    check_gelu_tanh(od.gelu_tanh)
+    monkeypatch.setattr(od, "gelu_tanh", _gelu_erf)
+    with pytest.raises(AssertionError):
+        check_gelu_tanh(od.gelu_tanh)

@@ -354,6 +354,16 @@ def test_hand_worked_two_dimensional_drafter():
 
 # --------------------------------------------------------------------------- scalar pieces
 
+def check_gelu_tanh(fn):
+    """The tanh form of GELU that MLX calls ``geluApprox`` (``#layer`` of "module-dflash.ts")
+    against PyTorch's own tanh-approximate GELU in float64.  The erf form differs from it by
+    up to ~5e-4 on [-8, 8], far above this tolerance, so substituting one for the other fails."""
+    torch = pytest.importorskip("torch")
+    z = np.concatenate([np.linspace(-8, 8, 1601), [-30.0, -1e-3, 1e-3, 30.0]])
+    ref = torch.nn.functional.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    np.testing.assert_allclose(fn(z), ref, rtol=1e-12, atol=1e-12)
+
+
 def test_scalar_functions_against_library_routines():
     z = np.linspace(-30, 30, 601)
     np.testing.assert_allclose(oracle.sigmoid(z), scipy.special.expit(z), rtol=1e-14, atol=1e-300)
@@ -362,6 +372,7 @@ def test_scalar_functions_against_library_routines():
     exact = 0.5 * z * (1 + scipy.special.erf(z / math.sqrt(2)))
     assert np.max(np.abs(oracle.gelu_tanh(z) - exact)) < 1e-3
     assert oracle.gelu_tanh(np.array([0.0]))[0] == 0.0
+    check_gelu_tanh(oracle.gelu_tanh)
     np.testing.assert_allclose(oracle.softmax(np.array([[0.0, math.log(3.0)]])), [[0.25, 0.75]], atol=1e-15)
     x = np.array([[3.0, 4.0]])
     np.testing.assert_allclose(oracle.rmsnorm(x, np.array([1.0, 2.0]), 0.0),
