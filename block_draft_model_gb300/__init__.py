@@ -24,6 +24,7 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
             "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error",
+            "dspark_noalloc_check",
             "dspark_set_sampling", "dspark_selftest_wait"]
 
 
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_linear": ([i32, vp, i64, vp, i32, i32, i32, vp, i64, i32, vp], i32),
         "dspark_linear_stream_noalloc": ([vp, i64, vp, i32, i32, i32, vp, i64, vp], i32),
         "dspark_noalloc_last_error": ([], ctypes.c_char_p),
+        "dspark_noalloc_check": ([ctypes.POINTER(i32)], i32),
         "dspark_profile_read": ([vp, i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
     }
@@ -135,13 +137,30 @@ def linear(A, W, out, kernel: int = KERNEL_AUTO, stream=None):
 def linear_stream_noalloc(A, W, out, stream=None):
     """out = A W^T (bf16 A [M <= 16, K], W [N, K]; float out) through the entry point that allocates
     no device memory (its scratch is a static device array of the library)."""
+    import torch
     lib = load()
     M, K = A.shape
     N = W.shape[0]
+    if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or out.dtype != torch.float32:
+        raise DsparkError(ERR_INVALID_ARG, "A and W must be bfloat16 and out float32")
+    if (W.shape[1] != K or tuple(out.shape) != (M, N) or W.stride(1) != 1 or W.stride(0) != K
+            or A.stride(1) != 1 or out.stride(1) != 1):
+        raise DsparkError(ERR_INVALID_ARG, "W must be a contiguous [N, K] matrix, A and out row-major [M, K], [M, N]")
     st = lib.dspark_linear_stream_noalloc(_ptr(A), A.stride(0), _ptr(W), M, N, K, _ptr(out), out.stride(0),
                                           _stream(stream))
     if st != OK:
         raise DsparkError(st, lib.dspark_noalloc_last_error().decode())
+
+
+def noalloc_check() -> int:
+    """Read and clear the error word of the allocation-free entry point on the current device
+    (synchronous); returns it, 0 when no bounded wait gave up since the last check."""
+    lib = load()
+    w = ctypes.c_int32(0)
+    st = lib.dspark_noalloc_check(ctypes.byref(w))
+    if st not in (OK, ERR_DEVICE):
+        raise DsparkError(st, lib.dspark_noalloc_last_error().decode())
+    return int(w.value)
 
 
 class _CudaArray:

@@ -14,7 +14,9 @@
 // device, with that device current, on the first call made on it.  That
 // first call should therefore come before any stream capture.  All calls share
 // the arrays: the tickets are cleared on every call, and two calls whose work
-// overlaps on the GPU race on the scratch.
+// overlaps on the GPU race on the scratch.  A kernel that gives up on a bounded
+// wait records DSPARK_DEVERR_TIMEOUT in the shared error word, which
+// dspark_noalloc_check reads and clears.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -122,6 +124,30 @@ dspark_status dspark_linear_stream_noalloc(const void* A_dev, int64_t lda, const
         return DSPARK_ERR_CUDA;
     }
     return DSPARK_OK;
+}
+
+dspark_status dspark_noalloc_check(int32_t* word_host) {
+    if (!word_host) {
+        g_msg = "word_host is NULL";
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    *word_host = 0;
+    // the symbol copies go through the current device's copy of g_err and allocate nothing;
+    // they wait for the device's earlier work, so every call before this one is covered
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err, sizeof(int)) != cudaSuccess) {
+        g_msg = "reading the error word failed";
+        return DSPARK_ERR_CUDA;
+    }
+    *word_host = v;
+    if (v == 0) return DSPARK_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_err, &zero, sizeof(int)) != cudaSuccess) {
+        g_msg = "clearing the error word failed";
+        return DSPARK_ERR_CUDA;
+    }
+    g_msg = "a bounded device wait gave up (DSPARK_DEVERR_TIMEOUT); the output of that call is incomplete";
+    return DSPARK_ERR_DEVICE;
 }
 
 const char* dspark_noalloc_last_error(void) { return g_msg; }

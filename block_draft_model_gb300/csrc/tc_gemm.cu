@@ -239,24 +239,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_state = -1;  // -1 unknown, 0 unavailable, 1 available
+// Per device (the shared-memory attribute belongs to the device's context):
+// -1 unknown, 0 unavailable, 1 available.
+constexpr int kMaxDev = 64;
+int g_state[kMaxDev] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1,
+                        -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1,
+                        -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 bool init_encode() {
-    if (g_state >= 0) return g_state == 1;
-    g_state = 0;
     int dev = 0, major = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    if (g_state[dev] >= 0) return g_state[dev] == 1;
+    g_state[dev] = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
     if (major != 10) return false;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
     if (cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
         return false;
-    g_state = 1;
+    g_state[dev] = 1;
     return true;
 }
 
@@ -350,7 +358,7 @@ cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K) {
 
 void tc_release(TcWeight& w) { w.ready = false; }
 
-bool tc_gemm_ok(int M, int N, int K) { return g_state == 1 && M >= 1 && N >= 1 && K >= BK && K % 8 == 0; }
+bool tc_gemm_ok(int M, int N, int K) { return init_encode() && M >= 1 && N >= 1 && K >= BK && K % 8 == 0; }
 
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
                     int num_sms, int* err, cudaStream_t st, int ksplit) {

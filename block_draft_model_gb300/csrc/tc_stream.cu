@@ -504,21 +504,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
-bool g_ready = false;
+// Per device: the raised shared-memory limit is an attribute of the device's context.
+constexpr int kMaxDev = 64;
+bool g_ready[kMaxDev] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
 
 bool ready() {
-    if (g_ready) return true;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    if (g_ready[dev]) return true;
     if (!tc_available()) return false;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-    g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    if (!g_enc) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
     if (cudaFuncSetAttribute(k_tc_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
         return false;
-    g_ready = true;
+    g_ready[dev] = true;
     return true;
 }
 

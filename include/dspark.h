@@ -281,6 +281,14 @@ dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const
 #define DSPARK_NOALLOC_MAX_TILES 4096
 dspark_status dspark_linear_stream_noalloc(const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
                                            int32_t K, float* out_dev, int64_t ldo, void* stream);
+/* Read and clear the error word that dspark_linear_stream_noalloc's kernels
+ * share on the current device (a static device int, like their scratch).  The
+ * kernel records DSPARK_DEVERR_TIMEOUT there when one of its bounded waits gives
+ * up; the call that launched it has already returned DSPARK_OK, and its output
+ * is incomplete.  Synchronous: waits for the device's earlier work, copies the
+ * word into *word_host and, if it was set, clears it and returns
+ * DSPARK_ERR_DEVICE (DSPARK_OK when it was 0).  Allocates nothing. */
+dspark_status dspark_noalloc_check(int32_t* word_host);
 const char* dspark_noalloc_last_error(void);
 
 /* Number of kernel launches issued by this handle since creation (all calls). */
