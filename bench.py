@@ -182,6 +182,10 @@ def class_work(cls: str, cfg, T: int, L_total: int, B: int):
         return dict(bytes=nL * ((2 * d * d + 2 * dkv * d + 3 * F * d) * 2 + 2 * (L_total + rows) * dkv * 2),
                     flops=nL * (2 * rows * (2 * d * d + 2 * dkv * d + 3 * F * d) + 4 * g * (L_total + rows) * d),
                     bound="hbm")
+    if cls == "draft_step":  # block build, every layer, out_norm and out_proj of a batch-1 draft in one launch
+        layers = class_work("draft_layers", cfg, T, L_total, B)
+        return dict(bytes=layers["bytes"] + d * H * 2 + V * d * 2 + rows * V * 4,
+                    flops=layers["flops"] + 2 * B * d * H + 2 * rows * V * d, bound="hbm")
     if cls == "block_build":
         return dict(bytes=d * H * 2, flops=2 * B * d * H, bound="hbm")
     return dict(bytes=0, flops=0, bound="hbm")

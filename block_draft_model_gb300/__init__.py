@@ -24,7 +24,7 @@ EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
             "dspark_profile_read", "dspark_linear", "dspark_linear_stream_noalloc", "dspark_noalloc_last_error",
-            "dspark_noalloc_check",
+            "dspark_noalloc_check", "dspark_set_path",
             "dspark_set_sampling", "dspark_selftest_wait"]
 
 
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_draft_host": ([vp, i32, vp, vp, vp, vp], i32),
         "dspark_reset": ([vp, i32, vp], i32),
         "dspark_set_sampling": ([vp, ctypes.c_float, i32, ctypes.c_uint64, vp], i32),
+        "dspark_set_path": ([vp, i32, i32], i32),
         "dspark_selftest_wait": ([i32, ctypes.POINTER(i32)], i32),
         "dspark_context_length": ([vp, i32, ctypes.POINTER(i32)], i32),
         "dspark_check": ([vp, ctypes.POINTER(i32)], i32),
@@ -183,6 +184,8 @@ def selftest_wait(which: int) -> int:
 
 
 DEVERR_TIMEOUT = 16
+PATH_LAYERS, PATH_MARKOV, PATH_NORM_CHAIN, PATH_GRAPHS = range(4)
+LAYERS_AUTO, LAYERS_PER_KERNEL, LAYERS_PERSISTENT_MMA, LAYERS_STEP_TC = range(4)
 
 
 class Drafter:
@@ -272,6 +275,10 @@ class Drafter:
         """temperature > 0: draw the Markov chain's tokens (top_k candidates, 0 = all) instead of argmax."""
         self._check(self.lib.dspark_set_sampling(self._h, float(temperature), int(top_k), int(seed) & (2**64 - 1),
                                                  _stream(stream)))
+
+    def set_path(self, what: int, value: int):
+        """Force one form of a computation (PATH_* / LAYERS_*; 0 = the library's choice)."""
+        self._check(self.lib.dspark_set_path(self._h, int(what), int(value)))
 
     def reset(self, seq_id: int = 0, stream=None):
         self._check(self.lib.dspark_reset(self._h, int(seq_id), _stream(stream)))

@@ -465,11 +465,7 @@ int g_num_sms = 0;
 template <int HD, typename TO>
 void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
     // a grid that fits one CTA per SM gives each CTA the SM's whole shared memory: a deeper ring
-    static const int ring = [] {  // DSPARK_ATTN_RING=3 keeps the shallow ring (two CTAs' room per SM) always
-        const char* e = getenv("DSPARK_ATTN_RING");
-        return e ? atoi(e) : 0;
-    }();
-    if (ring != 3 && (int)(grid.x * grid.y * grid.z) <= g_num_sms)
+    if ((int)(grid.x * grid.y * grid.z) <= g_num_sms)
         launch(k_attention_tc<HD, TO, 6>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
     else
         launch(k_attention_tc<HD, TO, 3>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);

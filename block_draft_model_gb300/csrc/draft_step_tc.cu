@@ -1,0 +1,991 @@
+// One persistent launch for a batch-1 draft step up to the base logits, with
+// every projection on the tcgen05 tensor cores:
+//   "module-dflash.ts" #buildBlock   x_0 = E[a] tok_proj^T + block_pos[0], x_j = mask_emb[j-1] + block_pos[j]
+//   "module-dflash.ts" #layer        pre-norm bidirectional attention over [context ++ block] and a
+//                                    SwiGLU FFN, each with a residual add (every draft layer)
+//   "module-dflash.ts" #baseLogits   y = RMSNorm(x) * out_norm, U = y out_proj^T
+// ("src/dspark-runtime.js", propose: the same chain, kept on the device).
+//
+// Phases, separated by bounded grid barriers (one cooperative CTA per SM):
+//   TOK   x = E[a] tok_proj^T (row 0 only) + block rows
+//   per layer:  QKV (Q rows to q, block K/V rows into the cache after the context)
+//               ATT (attention items (head, key range), merged by the last range of a head)
+//               WO  (x += O W_o^T)   GU (h = act(gate) * up)   DOWN (x += h W_down^T)
+//   OUT   U = RMSNorm(x) * out_norm . out_proj^T (and y)
+//
+// Every projection phase is a weight stream with at most 16 activation rows:
+// the weights are the MMA's M side (128-row tiles, 64-wide K blocks of 16 KB
+// moved by TMA with the 128-byte swizzle) and the block rows its N = 16 side,
+// one tcgen05.mma of 128 x 16 x 16 per 16-wide K slice, fp32 accumulators in
+// TMEM (16 columns each).  A phase's K blocks, taken tile by tile, are cut
+// into one contiguous range per CTA, so every CTA streams the same number of
+// bytes; a tile shared by several CTAs is reduced by the last of them to
+// finish (partials in global memory, a ticket per tile, sums in CTA order,
+// so the result does not depend on timing).
+//
+// Roles: warp 0 (one lane) streams every weight K block of every phase into a
+// ring of shared-memory stages in the order the CTA consumes them and never
+// waits for a grid barrier, so the next phases' weights arrive while the CTA
+// waits for the others.  Warp 1 owns TMEM and one lane issues the MMAs.
+// Warps 2-9 build each phase's MMA operand (the normalised rows, RMSNorm
+// applied before rounding to bf16), read the accumulators back, run the
+// epilogues and the attention, and take part in the grid barriers.
+//
+// Every wait is bounded (about one second); a timeout sets DSPARK_DEVERR_TIMEOUT
+// in the error word, every role stops, in-flight copies and MMAs are waited
+// for, TMEM is freed and the kernel returns.
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.cuh"
+#include "tc_common.cuh"
+
+namespace dspark {
+
+namespace {
+
+using namespace tc;
+
+constexpr int NCW = 8;                    // consumer warps (warps 2..9)
+constexpr int NCT = NCW * 32;             // consumer threads
+constexpr int NTHR = (NCW + 2) * 32;      // plus the producer and MMA warps
+constexpr int TM = 128;                   // weight rows per tile (MMA M)
+constexpr int KB = 64;                    // K elements per ring stage
+constexpr int STAGE_BYTES = TM * KB * 2;  // 16 KB
+constexpr int BSLOT_BYTES = 16 * KB * 2;  // one K block of the 16-row operand: 2 KB
+constexpr int NACC = 16;                  // TMEM accumulators of 16 fp32 columns
+constexpr int TMEM_COLS = NACC * 16;
+constexpr int TKA = 64;                   // attention keys per tile
+constexpr int MAXL = 16;                  // layers
+constexpr int GMAX = 16;                  // block rows
+
+enum Kind { K_TOK = 0, K_QKV = 1, K_WO = 2, K_GU = 3, K_DOWN = 4, K_OUT = 5 };
+
+struct StepParams {
+    float* x;          // [gamma, d] residual stream
+    float* q;          // [gamma, d] queries
+    bf16* act;         // [gamma, d] attention output
+    bf16* hact;        // [gamma, F] act(gate) * up
+    float* y;          // [gamma, d] out-normed rows
+    float* U;          // [gamma, V] logits before the Markov bias
+    float* ssq;        // [d / 128][16] per column tile: sums of x^2 of each block row
+    float* part;       // projection partials [(tiles + G)][gamma][128]
+    float* apart;      // attention partials [nh][nchunks][gamma][hd + 4]
+    unsigned int* tickets;   // [max tiles] zero between phases
+    unsigned int* atickets;  // [nh] zero between layers
+    bf16* cache;       // layer 0, slot 0: K rows at + pos * d, V rows at + kv_off + pos * d
+    int64_t layer_stride, kv_off;
+    int max_rows;
+    const int* seq_len;       // [0]: context length
+    const bf16* embed;        // [V, H]
+    const int* anchor_dev;    // [0]: anchor token, or nullptr (then `anchor`)
+    int anchor;
+    const float* block_const; // [gamma, d]: mask_emb + block_pos (row 0: block_pos[0])
+    const float* attn_norm[MAXL];
+    const float* ff_norm[MAXL];
+    const float* out_norm;
+    const CUtensorMap* maps;  // [2 + 4 * nL]: tok_proj, per layer (qkv, wo, gate/up, down), out_proj
+    int d, F, H, V, nh, nL, gamma, act_kind, nchunks;
+    float eps;
+    int nstage;               // ring stages
+    int ubytes;               // operand / attention staging area
+    unsigned long long* bar;  // 2 arrival counters (launch parity)
+    unsigned int* epoch;
+    int* err;
+};
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cons_sync() { named_sync(1, NCT); }
+// Consumer barrier that also returns the OR of `v` over the consumer threads: a decision every
+// consumer takes alike (the abort flag can be raised by the other roles at any time).
+__device__ __forceinline__ bool cons_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(NCT)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void attn_sync() { named_sync(2, 128); }
+
+__device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_round(float& lo, float& hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    lo = __low2float(v);
+    hi = __high2float(v);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- the schedule
+// Phase s: 0 TOK; 1 + 4 i + k: layer i, k = 0 QKV, 1 WO, 2 GU, 3 DOWN; 1 + 4 nL: OUT.
+struct Shape {
+    int kind, layer, N, K, nT, nkb;
+};
+__device__ __forceinline__ Shape phase_shape(const StepParams& p, int s) {
+    Shape sh;
+    if (s == 0) {
+        sh.kind = K_TOK;
+        sh.layer = 0;
+        sh.N = p.d;
+        sh.K = p.H;
+    } else if (s == 1 + 4 * p.nL) {
+        sh.kind = K_OUT;
+        sh.layer = 0;
+        sh.N = p.V;
+        sh.K = p.d;
+    } else {
+        const int k = (s - 1) & 3;
+        sh.layer = (s - 1) >> 2;
+        sh.kind = K_QKV + k;
+        sh.N = k == 0 ? 3 * p.d : (k == 1 ? p.d : (k == 2 ? 2 * p.F : p.d));
+        sh.K = k == 3 ? p.F : p.d;
+    }
+    sh.nT = (sh.N + TM - 1) / TM;
+    sh.nkb = (sh.K + KB - 1) / KB;
+    return sh;
+}
+
+// The phase's K blocks (tile-major) cut into contiguous ranges over the first
+// min(G, T) CTAs: CTA c owns [c T / g, (c + 1) T / g).
+__device__ __forceinline__ void my_range(const Shape& sh, int c, int G, int& lo, int& hi) {
+    const int T = sh.nT * sh.nkb;
+    const int g = min(G, T);
+    if (c >= g) {
+        lo = hi = 0;
+        return;
+    }
+    lo = (int)((int64_t)c * T / g);
+    hi = (int)((int64_t)(c + 1) * T / g);
+}
+// The CTA that owns K block j of the phase.
+__device__ __forceinline__ int owner(const Shape& sh, int G, int j) {
+    const int64_t T = (int64_t)sh.nT * sh.nkb;
+    const int64_t g = min((int64_t)G, T);
+    return (int)(((int64_t)(j + 1) * g + T - 1) / T - 1);
+}
+
+// ---------------------------------------------------------------- grid barrier
+// Arrival counter counting up through the launch: barrier n opens at n * G.  Returns true
+// (on every consumer thread alike) when the CTA has to stop.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long target, int* err,
+                                             volatile int* abort_flag) {
+    cons_sync();
+    if (threadIdx.x == 64) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+        const uint64_t t0 = globaltimer();
+        while (true) {
+            unsigned long long cur;
+            asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(bar) : "memory");
+            if (cur >= target || *abort_flag) break;
+            if (globaltimer() - t0 > TIMEOUT_NS) {
+                atomicOr(err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+        }
+    }
+    return cons_sync_or(*abort_flag != 0);
+}
+
+// ---------------------------------------------------------------- operand staging
+// The phase's operand for the CTA's K blocks: slot i holds K block (kb_first + i) mod nkb
+// as [16 rows][64] bf16, row n at n * 128 bytes, 16-byte chunk c at (c ^ (n & 7)) * 16 (the
+// layout a 128-byte-swizzled TMA copy gives).  Rows past the block rows are zero.
+__device__ __forceinline__ void stage_operand(const StepParams& p, const Shape& sh, int kb_first, int nslots,
+                                              uint8_t* ub, const float* rs, int anchor) {
+    const int t = threadIdx.x - 64;
+    const int K = sh.K, gamma = p.gamma;
+    const float* g = sh.kind == K_QKV ? p.attn_norm[sh.layer] : (sh.kind == K_GU ? p.ff_norm[sh.layer] : p.out_norm);
+    constexpr int BATCH = 4;  // chunks per thread whose loads are in flight together
+    const int total = nslots * 128;
+    for (int i0 = t; i0 < total; i0 += BATCH * NCT) {
+        uint4 v[BATCH];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b * NCT;
+            const int slot = i >> 7, n = (i >> 3) & 15, ch = i & 7;
+            const int k0 = ((kb_first + slot) % sh.nkb) * KB + ch * 8;
+            v[b] = make_uint4(0, 0, 0, 0);
+            if (i < total && k0 < K) {
+                if (sh.kind == K_TOK) {
+                    if (n == 0) v[b] = __ldg(reinterpret_cast<const uint4*>(p.embed + (int64_t)anchor * p.H + k0));
+                } else if (n < gamma) {
+                    if (sh.kind == K_WO) {
+                        v[b] = __ldcg(reinterpret_cast<const uint4*>(p.act + (int64_t)n * p.d + k0));
+                    } else if (sh.kind == K_DOWN) {
+                        v[b] = __ldcg(reinterpret_cast<const uint4*>(p.hact + (int64_t)n * p.F + k0));
+                    } else {
+                        const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)n * p.d + k0);
+                        const float4* gr = reinterpret_cast<const float4*>(g + k0);
+                        const float4 x0 = __ldcg(xr), x1 = __ldcg(xr + 1), g0 = __ldg(gr), g1 = __ldg(gr + 1);
+                        const float r = rs[n];
+                        v[b] = make_uint4(pack2(x0.x * r * g0.x, x0.y * r * g0.y),
+                                          pack2(x0.z * r * g0.z, x0.w * r * g0.w),
+                                          pack2(x1.x * r * g1.x, x1.y * r * g1.y),
+                                          pack2(x1.z * r * g1.z, x1.w * r * g1.w));
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b * NCT;
+            if (i < total) {
+                const int slot = i >> 7, n = (i >> 3) & 15, ch = i & 7;
+                *reinterpret_cast<uint4*>(ub + slot * BSLOT_BYTES + n * 128 + ((ch ^ (n & 7)) * 16)) = v[b];
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+}
+
+// ---------------------------------------------------------------- epilogues
+// Thread (row r of the tile, column group cg) holds v[i] = acc[r][cg * 8 + i].
+// x += v (or, for the block build, x = v + block rows) and the tile's sums of x^2 per block row.
+__device__ __forceinline__ void fin_residual(const StepParams& p, int kind, int t, int r, int cg, const float* v,
+                                             float* red) {
+    const int n = t * TM + r, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float s2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int j = cg * 8 + i;
+        s2[i] = 0.f;
+        if (j < p.gamma) {
+            float* xp = p.x + (int64_t)j * p.d + n;
+            const float base = kind == K_TOK ? __ldg(p.block_const + (int64_t)j * p.d + n) : __ldcg(xp);
+            const float xv = base + v[i];
+            *xp = xv;
+            s2[i] = xv * xv;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s2[i] = warp_sum(s2[i]);
+    // red[warp - 2][8]: the warp's 32 rows; warps w and w + 4 share the column group
+    if (lane == 0)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red[(warp - 2) * 8 + i] = s2[i];
+    cons_sync();
+    const int tt = threadIdx.x - 64;
+    if (tt < 16 && tt < p.gamma) {
+        const int g2 = tt >> 3, i = tt & 7;  // column group, entry: the four warps of that group in lane order
+        float a = 0.f;
+        for (int q4 = 0; q4 < 4; ++q4) {
+            // warps 2..9 -> index 0..7; group g2 holds indices 4 g2 .. 4 g2 + 3, their lane quarters 2, 3, 0, 1
+            a += red[(g2 * 4 + q4) * 8 + i];
+        }
+        p.ssq[t * 16 + tt] = a;
+    }
+    cons_sync();
+}
+
+__device__ __forceinline__ void finalize(const StepParams& p, const Shape& sh, int t, int r, int cg, float* v,
+                                         float* red, int L) {
+    const int n = t * TM + r, lane = threadIdx.x & 31;
+    const int gamma = p.gamma, d = p.d;
+    switch (sh.kind) {
+        case K_TOK:
+        case K_WO:
+        case K_DOWN:
+            fin_residual(p, sh.kind, t, r, cg, v, red);
+            break;
+        case K_QKV: {
+            bf16* cache = p.cache + (int64_t)sh.layer * p.layer_stride;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = cg * 8 + i;
+                if (j >= gamma) continue;
+                if (n < d) {
+                    p.q[(int64_t)j * d + n] = v[i];
+                } else if (L + j < p.max_rows) {
+                    const int64_t off = (int64_t)(L + j) * d + (n < 2 * d ? n - d : n - 2 * d);
+                    cache[(n < 2 * d ? 0 : p.kv_off) + off] = __float2bfloat16_rn(v[i]);
+                }
+            }
+            break;
+        }
+        case K_GU: {
+            // (gate f, up f) are rows 2f, 2f + 1: adjacent lanes
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float up = __shfl_down_sync(0xffffffffu, v[i], 1);
+                const int j = cg * 8 + i;
+                if (j < gamma && !(lane & 1) && n + 1 < sh.N)
+                    p.hact[(int64_t)j * p.F + (n >> 1)] = __float2bfloat16_rn(act_fn(p.act_kind, v[i]) * up);
+            }
+            break;
+        }
+        default: {  // K_OUT
+            if (n < p.V)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = cg * 8 + i;
+                    if (j < gamma) p.U[(int64_t)j * p.V + n] = v[i];
+                }
+            break;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- attention
+// One (head, key range) item on warps 2-5: flash decoding over 64-key tiles of a two-stage
+// cp.async ring in `ab`; scores in the log2 domain.  The partial (m, l, o) goes to apart,
+// or, with a single range, the normalised output straight to act.
+template <int HD>
+__device__ void attn_item(const StepParams& p, int layer, int h, int start, int end, int n_real, int rg,
+                          uint8_t* ab) {
+    constexpr int RB = HD * 2 + 16, TILE = TKA * RB, STAGE = 2 * TILE, KS = HD / 16;
+    const int tid = threadIdx.x - 64, warp = tid >> 5, lane = tid & 31;
+    const int gamma = p.gamma, d = p.d;
+    const bf16* Kb = p.cache + (int64_t)layer * p.layer_stride + h * HD;
+    const bf16* Vb = Kb + p.kv_off;
+    const uint32_t ring = smem_u32(ab);
+    const int n_tiles = (end - start + TKA - 1) / TKA;
+    auto load = [&](int st, int t0) {
+        constexpr int VPR = HD * 2 / 16;
+        for (int i = tid; i < TKA * VPR; i += 128) {
+            const int r = i / VPR, v = i - r * VPR;
+            const int key = t0 + r;
+            const bool ok = key < end;
+            const int64_t off = (int64_t)(ok ? key : t0) * d + v * 8;
+            const uint32_t so = ring + st * STAGE + r * RB + v * 16;
+            cp_async16z(so, Kb + off, ok ? 16 : 0);
+            cp_async16z(so + TILE, Vb + off, ok ? 16 : 0);
+        }
+        cp_commit();
+    };
+    load(0, start);
+    const int g = lane >> 2, cq = (lane & 3) * 2;
+    uint32_t qf[KS][4];
+    {
+        const float qs = rsqrtf((float)HD) * 1.4426950408889634f;
+        const float* q0 = p.q + (int64_t)g * d + h * HD;
+        const float* q1 = q0 + (int64_t)8 * d;
+        const bool v0 = g < gamma, v1 = g + 8 < gamma;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int col = ks * 16 + cq;
+            const float2 a = v0 ? __ldcg(reinterpret_cast<const float2*>(q0 + col)) : make_float2(0.f, 0.f);
+            const float2 b = v1 ? __ldcg(reinterpret_cast<const float2*>(q1 + col)) : make_float2(0.f, 0.f);
+            const float2 c = v0 ? __ldcg(reinterpret_cast<const float2*>(q0 + col + 8)) : make_float2(0.f, 0.f);
+            const float2 e = v1 ? __ldcg(reinterpret_cast<const float2*>(q1 + col + 8)) : make_float2(0.f, 0.f);
+            float x0 = a.x * qs, x1 = a.y * qs, y0 = b.x * qs, y1 = b.y * qs;
+            float z0 = c.x * qs, z1 = c.y * qs, w0 = e.x * qs, w1 = e.y * qs;
+            qf[ks][0] = pack_round(x0, x1);
+            qf[ks][1] = pack_round(y0, y1);
+            qf[ks][2] = pack_round(z0, z1);
+            qf[ks][3] = pack_round(w0, w1);
+        }
+    }
+    float o[2 * KS][4];
+#pragma unroll
+    for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int lr = lane & 7, lm = lane >> 3, kw = warp * 16;
+    const uint32_t k_lane = (uint32_t)((kw + (lm >> 1) * 8 + lr) * RB + (lm & 1) * 16);
+    const uint32_t v_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * RB + (lm >> 1) * 16);
+    for (int t = 0; t < n_tiles; ++t) {
+        if (t + 1 < n_tiles) load((t + 1) & 1, start + (t + 1) * TKA);
+        else cp_commit();
+        cp_wait<1>();
+        attn_sync();
+        const int nk = min(TKA, end - (start + t * TKA));
+        if (kw < nk) {
+            const uint32_t kbase = ring + (t & 1) * STAGE, vbase = kbase + TILE;
+            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + k_lane + ks * 32, b0, b1, b2, b3);
+                mma16816(s[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+                mma16816(s[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+            }
+            if (kw + 16 > nk) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (kw + n * 8 + cq + e >= nk) s[n][e] = s[n][2 + e] = -INFINITY;
+            }
+            float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+            float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float a0 = ex2(m0 - ms0), a1 = ex2(m1 - ms1);
+            m0 = mn0;
+            m1 = mn1;
+            float p00 = ex2(s[0][0] - ms0), p01 = ex2(s[0][1] - ms0), p02 = ex2(s[0][2] - ms1), p03 = ex2(s[0][3] - ms1);
+            float p10 = ex2(s[1][0] - ms0), p11 = ex2(s[1][1] - ms0), p12 = ex2(s[1][2] - ms1), p13 = ex2(s[1][3] - ms1);
+            const uint32_t pf0 = pack_round(p00, p01), pf1 = pack_round(p02, p03);
+            const uint32_t pf2 = pack_round(p10, p11), pf3 = pack_round(p12, p13);
+            l0 = l0 * a0 + ((p00 + p01) + (p10 + p11));
+            l1 = l1 * a1 + ((p02 + p03) + (p12 + p13));
+#pragma unroll
+            for (int n = 0; n < 2 * KS; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+#pragma unroll
+            for (int n2 = 0; n2 < KS; ++n2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vbase + v_lane + n2 * 32, b0, b1, b2, b3);
+                mma16816(o[2 * n2], pf0, pf1, pf2, pf3, b0, b1);
+                mma16816(o[2 * n2 + 1], pf0, pf1, pf2, pf3, b2, b3);
+            }
+        }
+        attn_sync();  // every warp is done with this stage before it is refilled
+    }
+    cp_wait<0>();
+    attn_sync();
+    // the four warps' key slices merged through shared memory, then this range's partial (or the output)
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    constexpr int OWS = HD + 8;
+    float* Ow = reinterpret_cast<float*>(ab);
+    float* Mw = Ow + 4 * GMAX * OWS;
+    float* Lw = Mw + 4 * GMAX;
+#pragma unroll
+    for (int n = 0; n < 2 * KS; ++n) {
+        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g) * OWS + n * 8 + cq) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g + 8) * OWS + n * 8 + cq) = make_float2(o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+        Mw[warp * GMAX + g] = m0;
+        Mw[warp * GMAX + g + 8] = m1;
+        Lw[warp * GMAX + g] = l0;
+        Lw[warp * GMAX + g + 8] = l1;
+    }
+    attn_sync();
+    constexpr int PW = HD + 4;
+    for (int i = tid; i < gamma * (HD / 4); i += 128) {
+        const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) M = fmaxf(M, Mw[v * GMAX + j]);
+        float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const float mv = Mw[v * GMAX + j];
+            const float wt = mv == -INFINITY ? 0.f : ex2(mv - M);
+            l += wt * Lw[v * GMAX + j];
+            const float4 ov = *reinterpret_cast<const float4*>(Ow + (v * GMAX + j) * OWS + e);
+            acc[0] += wt * ov.x;
+            acc[1] += wt * ov.y;
+            acc[2] += wt * ov.z;
+            acc[3] += wt * ov.w;
+        }
+        if (n_real == 1) {
+            const float inv = 1.f / l;
+            *reinterpret_cast<uint2*>(p.act + (int64_t)j * d + h * HD + e) =
+                make_uint2(pack2(acc[0] * inv, acc[1] * inv), pack2(acc[2] * inv, acc[3] * inv));
+        } else {
+            float* pr = p.apart + ((int64_t)(h * p.nchunks + rg) * gamma + j) * PW;
+            *reinterpret_cast<float4*>(pr + 4 + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (e == 0) *reinterpret_cast<float2*>(pr) = make_float2(M, l);
+        }
+    }
+}
+
+// The last key range of head h to finish merges all n_real ranges' partials (in range order).
+template <int HD>
+__device__ void attn_merge(const StepParams& p, int h, int n_real) {
+    constexpr int PW = HD + 4;
+    const int tid = threadIdx.x - 64;
+    const int gamma = p.gamma;
+    for (int i = tid; i < gamma * (HD / 4); i += 128) {
+        const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+        const float* base = p.apart + ((int64_t)h * p.nchunks * gamma + j) * PW;
+        const int64_t cs = (int64_t)gamma * PW;
+        float M = -INFINITY;
+        for (int c = 0; c < n_real; ++c) M = fmaxf(M, __ldcg(base + c * cs));
+        float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int c = 0; c < n_real; ++c) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + c * cs));
+            const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+            l += wt * ml.y;
+            const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + c * cs + 4 + e));
+            a0 = fmaf(wt, ov.x, a0);
+            a1 = fmaf(wt, ov.y, a1);
+            a2 = fmaf(wt, ov.z, a2);
+            a3 = fmaf(wt, ov.w, a3);
+        }
+        const float inv = 1.f / l;
+        *reinterpret_cast<uint2*>(p.act + (int64_t)j * p.d + h * HD + e) =
+            make_uint2(pack2(a0 * inv, a1 * inv), pack2(a2 * inv, a3 * inv));
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int HD>
+__global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant__ StepParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 128-byte swizzle: 1024-byte aligned
+    uint8_t* ring = smem;
+    uint8_t* ub = ring + (size_t)p.nstage * STAGE_BYTES;           // operand slots / attention staging
+    uint64_t* full = reinterpret_cast<uint64_t*>(ub + p.ubytes);
+    uint64_t* empty = full + p.nstage;
+    uint64_t* acc_full = empty + p.nstage;
+    uint64_t* acc_empty = acc_full + NACC;
+    uint64_t* b_full = acc_empty + NACC;
+    uint64_t* b_taken = b_full + 1;  // the MMA warp has seen the phase's b_full
+    uint64_t* drain = b_taken + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* flag = abort_flag + 1;                  // ticket outcome, broadcast to the consumers
+    float* rs = reinterpret_cast<float*>(tmem_slot + 4);   // [16] row scales
+    float* red = rs + 16;                                  // [8][8] row-sum partials
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int nph = 2 + 4 * p.nL;
+    const int S = p.nstage;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 1);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_taken, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    const unsigned int par = *(volatile unsigned int*)p.epoch & 1u;
+    unsigned long long* bar = p.bar + par;
+    if (c == 0 && threadIdx.x == 0) p.bar[par ^ 1u] = 0ull;  // the next launch's counter
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---- producer: every K block of every phase, in consumption order
+        if (lane == 0) {
+            uint32_t idx = 0;
+            bool ok = true;
+            for (int s = 0; s < nph && ok; ++s) {
+                const Shape sh = phase_shape(p, s);
+                const CUtensorMap* map = p.maps + s;
+                asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+                int lo, hi;
+                my_range(sh, c, G, lo, hi);
+                for (int j = lo; j < hi; ++j, ++idx) {
+                    const int st = (int)(idx % (uint32_t)S);
+                    if (!mbar_wait(&empty[st], ((idx / (uint32_t)S) & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int t = j / sh.nkb, kb = j - t * sh.nkb;
+                    mbar_arrive_expect_tx(&full[st], STAGE_BYTES);  // rows / columns past the matrix arrive as zeros
+                    tma_load_2d(smem_u32(ring + (size_t)st * STAGE_BYTES), map, &full[st], kb * KB, t * TM);
+                }
+            }
+            // no copy may still be in flight when the CTA exits (only possible after an abort)
+            volatile int never = 0;
+            for (uint32_t i = idx > (uint32_t)S ? idx - (uint32_t)S : 0u; i < idx; ++i)
+                mbar_wait(&full[i % (uint32_t)S], (i / (uint32_t)S) & 1u, &never);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            const uint32_t id = idesc(TM, 16);
+            uint32_t idx = 0, u = 0, bph = 0;
+            bool ok = true;
+            for (int s = 0; s < nph && ok; ++s) {
+                const Shape sh = phase_shape(p, s);
+                int lo, hi;
+                my_range(sh, c, G, lo, hi);
+                if (!mbar_wait(b_full, bph & 1u, abort_flag)) break;  // the phase's operand is staged
+                ++bph;
+                mbar_arrive(b_taken);
+                tc_fence_after();
+                const int kb_first = lo % sh.nkb;
+                const uint32_t ub_s = smem_u32(ub);
+                for (int j = lo; j < hi && ok;) {
+                    const int t = j / sh.nkb, kb0 = j - t * sh.nkb, kb1 = min(sh.nkb, kb0 + (hi - j));
+                    const int a = (int)(u % NACC);
+                    if (!mbar_wait(&acc_empty[a], ((u / NACC) & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (uint32_t)(a * 16);
+                    for (int kb = kb0; kb < kb1; ++kb, ++idx) {
+                        const int st = (int)(idx % (uint32_t)S);
+                        if (!mbar_wait(&full[st], (idx / (uint32_t)S) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int slot = (kb - kb_first + sh.nkb) % sh.nkb;
+                        const uint64_t dw = sdesc(smem_u32(ring + (size_t)st * STAGE_BYTES));
+                        const uint64_t dx = sdesc(ub_s + (uint32_t)(slot * BSLOT_BYTES));
+#pragma unroll
+                        for (int k = 0; k < KB / 16; ++k)
+                            umma(d_tmem, dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), id, (kb > kb0 || k > 0) ? 1u : 0u);
+                        umma_commit(&empty[st]);
+                    }
+                    if (!ok) break;
+                    umma_commit(&acc_full[a]);
+                    ++u;
+                    j += kb1 - kb0;
+                }
+            }
+            // every MMA issued above has retired before TMEM is freed
+            umma_commit(drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- consumers: operands, epilogues, attention, grid barriers
+        const int tt = threadIdx.x - 64;
+        const int q4 = warp & 3, cg = (warp - 2) >> 2;  // TMEM lane quarter, column group
+        const int r = q4 * 32 + lane;                    // row of the tile
+        const int L = __ldcg(p.seq_len);
+        const int anchor = p.anchor_dev ? __ldcg(p.anchor_dev) : p.anchor;
+        const int n_keys = L + p.gamma;
+        const int per = (n_keys + p.nchunks - 1) / p.nchunks;
+        const int chunk = (per + TKA - 1) / TKA * TKA;
+        const int n_real = (n_keys + chunk - 1) / chunk;
+        unsigned long long nbar = 0;
+        uint32_t u = 0;
+        bool live = true;
+        for (int s = 0; s < nph && live; ++s) {
+            const Shape sh = phase_shape(p, s);
+            int lo, hi;
+            my_range(sh, c, G, lo, hi);
+            // row scales of the normalised operands, from the column tiles' sums of x^2
+            if (sh.kind == K_QKV || sh.kind == K_GU || sh.kind == K_OUT) {
+                if (tt < p.gamma) {
+                    float a = 0.f;
+                    for (int t2 = 0; t2 < p.d / TM; ++t2) a += __ldcg(p.ssq + t2 * 16 + tt);
+                    rs[tt] = rsqrtf(a / (float)p.d + p.eps);
+                }
+                cons_sync();
+            }
+            if (sh.kind == K_OUT) {
+                // y = RMSNorm(x) * out_norm in fp32 (the confidence head's input): a column range per CTA
+                const int c0 = (int)((int64_t)c * p.d / G), c1 = (int)((int64_t)(c + 1) * p.d / G);
+                for (int i = tt; i < p.gamma * (c1 - c0); i += NCT) {
+                    const int j = i / (c1 - c0), k = c0 + i % (c1 - c0);
+                    p.y[(int64_t)j * p.d + k] = __ldcg(p.x + (int64_t)j * p.d + k) * rs[j] * __ldg(p.out_norm + k);
+                }
+            }
+            const int nslots = min(sh.nkb, hi - lo);
+            stage_operand(p, sh, hi > lo ? lo % sh.nkb : 0, nslots, ub, rs, anchor);
+            cons_sync();
+            if (tt == 0) {
+                // b_full completes once per phase: the MMA warp must have seen the previous one
+                if (s == 0 || mbar_wait(b_taken, (uint32_t)(s - 1) & 1u, abort_flag)) mbar_arrive(b_full);
+                else *abort_flag = 1;
+            }
+            // epilogues of the CTA's tiles, in MMA order
+            for (int j = lo; j < hi;) {
+                const int t = j / sh.nkb, kb0 = j - t * sh.nkb, kb1 = min(sh.nkb, kb0 + (hi - j));
+                j += kb1 - kb0;
+                const int a = (int)(u % NACC);
+                if (!mbar_wait(&acc_full[a], (u / NACC) & 1u, abort_flag)) *abort_flag = 1;
+                ++u;
+                tc_fence_after();
+                float v[8];
+                // tcgen05.ld is warp-wide: the whole warp takes the same branch
+                const bool ld_ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+                if (ld_ok && cg * 8 < p.gamma) {
+                    uint32_t rr[8];
+                    tmem_ld8(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(a * 16 + cg * 8), rr);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(rr[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                }
+                tc_fence_before();
+                const bool stop = cons_sync_or(*abort_flag != 0);
+                if (tt == 0) mbar_arrive(&acc_empty[a]);  // TMEM columns free for the MMA warp
+                if (stop) {
+                    live = false;
+                    break;
+                }
+                const int cf = owner(sh, G, t * sh.nkb), cl = owner(sh, G, t * sh.nkb + sh.nkb - 1);
+                if (cf == cl) {
+                    finalize(p, sh, t, r, cg, v, red, L);
+                    continue;
+                }
+                // shared tile: this CTA's partial, then the last CTA of the tile adds them in CTA order
+                float* pp = p.part + (int64_t)(c + t) * p.gamma * TM;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (cg * 8 + i < p.gamma) __stcg(pp + (cg * 8 + i) * TM + r, v[i]);
+                __threadfence();
+                cons_sync();
+                if (tt == 0) *flag = atomicAdd(&p.tickets[t], 1u) == (unsigned int)(cl - cf);
+                cons_sync();
+                if (*flag) {
+                    __threadfence();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                    for (int c2 = cf; c2 <= cl; ++c2) {
+                        const float* src = p.part + (int64_t)(c2 + t) * p.gamma * TM;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (cg * 8 + i < p.gamma) v[i] += __ldcg(src + (cg * 8 + i) * TM + r);
+                    }
+                    finalize(p, sh, t, r, cg, v, red, L);
+                    if (tt == 0) p.tickets[t] = 0u;
+                }
+                cons_sync();  // `flag` is rewritten by the next shared tile
+            }
+            if (!live || s == nph - 1) break;
+            if (grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;
+            if (sh.kind == K_QKV) {
+                // ---- attention of layer sh.layer: item c = (head, key range) on warps 2-5
+                const int h = c / p.nchunks, rg = c - h * p.nchunks;
+                if (c < p.nh * p.nchunks && rg < n_real && warp < 6) {
+                    const int start = rg * chunk, end = min(n_keys, start + chunk);
+                    attn_item<HD>(p, sh.layer, h, start, end, n_real, rg, ub);
+                    if (n_real > 1) {
+                        __threadfence();
+                        attn_sync();
+                        if (tt == 0) *flag = atomicAdd(&p.atickets[h], 1u) == (unsigned int)(n_real - 1);
+                        attn_sync();
+                        if (*flag) {
+                            __threadfence();
+                            attn_merge<HD>(p, h, n_real);
+                            if (tt == 0) p.atickets[h] = 0u;
+                        }
+                        attn_sync();
+                    }
+                }
+                if (grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err, DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+    if (c == 0 && threadIdx.x == 0) atomicAdd(p.epoch, 1u);  // every CTA read it before the first barrier
+}
+
+// The step's grid barrier with one CTA where two are expected: it gives up after its limit and
+// every consumer thread sees the same outcome.
+__global__ void __launch_bounds__(NTHR, 1) k_step_barrier_selftest(unsigned long long* bar, int* err) {
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    if (threadIdx.x >= 64) {
+        const bool stop = grid_barrier(bar, 2ull, err, &abort_flag);
+        if (threadIdx.x == 64 && !stop) atomicOr(err, 1);  // not expected: the barrier cannot open
+    }
+}
+
+int g_budget = 0;  // dynamic shared memory the kernel may take (0: unavailable)
+
+// Staging area: the operand slots of the widest phase, or the attention's two-stage ring and its
+// merge scratch, whichever is larger.
+int ubytes_for(const DraftStepArgs& a, int G) {
+    const int hd = a.d / a.nh;
+    auto slots = [&](int N, int K) {
+        const int nT = (N + TM - 1) / TM, nkb = (K + KB - 1) / KB;
+        const int64_t T = (int64_t)nT * nkb;
+        const int g = (int)std::min<int64_t>(G, T);
+        const int mx = (int)((T + g - 1) / g) + 1;  // a range can straddle one more K block than the mean
+        return std::min(nkb, mx);
+    };
+    int ns = std::max({slots(a.d, a.H), slots(3 * a.d, a.d), slots(a.d, a.d), slots(2 * a.F, a.d), slots(a.d, a.F),
+                       slots(a.V, a.d)});
+    const int attn = 2 * 2 * TKA * (hd * 2 + 16);
+    const int merge = (4 * GMAX * (hd + 8) + 8 * GMAX) * 4;
+    return std::max({ns * BSLOT_BYTES, attn, merge});
+}
+
+}  // namespace
+
+cudaError_t step_wait_selftest(void* scratch, int* err, cudaStream_t st) {
+    if (!scratch || !err) return cudaErrorInvalidValue;
+    k_step_barrier_selftest<<<1, NTHR, 0, st>>>(reinterpret_cast<unsigned long long*>(scratch), err);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t draft_step_tc_init() {
+    int dev = 0, optin = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    const int budget = (optin - 1024) / 1024 * 1024;
+    const bool ok =
+        cudaFuncSetAttribute(k_draft_step_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget) == cudaSuccess &&
+        cudaFuncSetAttribute(k_draft_step_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget) == cudaSuccess;
+    (void)cudaGetLastError();
+    g_budget = ok ? budget : 0;
+    return cudaSuccess;
+}
+
+// Bytes after the ring and staging area: barriers, TMEM slot, flags, row scales and sums.
+static constexpr int kTail = 1024;
+
+static int stages_for(const DraftStepArgs& a, int G) {
+    const int s = (g_budget - 1024 - ubytes_for(a, G) - kTail) / STAGE_BYTES;
+    // the tail holds 2 s + 2 NACC + 3 mbarriers, the TMEM slot and flags (16 B), rs[16] and red[64]
+    return (2 * s + 2 * NACC + 3) * 8 + 16 + 80 * 4 <= kTail ? s : 0;
+}
+
+bool draft_step_tc_ok(const DraftStepArgs& a, int G) {
+    if (g_budget == 0 || !a.maps) return false;
+    const int hd = a.nh > 0 ? a.d / a.nh : 0;
+    if (a.gamma < 1 || a.gamma > GMAX || a.nL < 1 || a.nL > MAXL || (hd != 64 && hd != 128) || a.d % TM != 0 ||
+        a.F % KB != 0 || a.H % 8 != 0 || a.d % a.nh != 0 || a.V < 1 || a.nchunks < 1)
+        return false;
+    if (a.nh * a.nchunks > G) return false;  // one attention item per CTA
+    return stages_for(a, G) >= 4;
+}
+
+size_t draft_step_tc_part_floats(const DraftStepArgs& a, int G) {
+    const int maxN = std::max({3 * a.d, 2 * a.F, a.V});
+    return ((size_t)(maxN + TM - 1) / TM + G) * a.gamma * TM;
+}
+
+cudaError_t draft_step_tc(const DraftStepArgs& a, int G, cudaStream_t st) {
+    if (!draft_step_tc_ok(a, G)) return cudaErrorInvalidValue;
+    StepParams p{};
+    p.x = a.x;
+    p.q = a.q;
+    p.act = reinterpret_cast<bf16*>(a.act);
+    p.hact = reinterpret_cast<bf16*>(a.hact);
+    p.y = a.y;
+    p.U = a.U;
+    p.ssq = a.ssq;
+    p.part = a.part;
+    p.apart = a.apart;
+    p.tickets = a.tickets;
+    p.atickets = a.atickets;
+    p.cache = reinterpret_cast<bf16*>(a.cache);
+    p.layer_stride = a.layer_stride;
+    p.kv_off = a.kv_off;
+    p.max_rows = a.max_rows;
+    p.seq_len = a.seq_len;
+    p.embed = reinterpret_cast<const bf16*>(a.embed);
+    p.anchor_dev = a.anchor_dev;
+    p.anchor = a.anchor;
+    p.block_const = a.block_const;
+    for (int i = 0; i < a.nL; ++i) {
+        p.attn_norm[i] = a.attn_norm[i];
+        p.ff_norm[i] = a.ff_norm[i];
+    }
+    p.out_norm = a.out_norm;
+    p.maps = reinterpret_cast<const CUtensorMap*>(a.maps);
+    p.d = a.d;
+    p.F = a.F;
+    p.H = a.H;
+    p.V = a.V;
+    p.nh = a.nh;
+    p.nL = a.nL;
+    p.gamma = a.gamma;
+    p.act_kind = a.act_kind;
+    p.nchunks = a.nchunks;
+    p.eps = a.eps;
+    p.ubytes = ubytes_for(a, G);
+    p.nstage = stages_for(a, G);
+    p.bar = a.bar;
+    p.epoch = a.epoch;
+    p.err = a.err;
+    const size_t smem = 1024 + (size_t)p.nstage * STAGE_BYTES + p.ubytes + kTail;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(NTHR);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int hd = a.d / a.nh;
+    cudaError_t e = hd == 64 ? cudaLaunchKernelEx(&cfg, k_draft_step_tc<64>, p)
+                             : cudaLaunchKernelEx(&cfg, k_draft_step_tc<128>, p);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -20,6 +20,9 @@ namespace {
 
 thread_local std::string g_create_error = "no error";
 
+// Forms of the batch-1 draft layers (dspark_set_path, DSPARK_PATH_LAYERS).
+enum { LAYERS_AUTO = 0, LAYERS_PER_KERNEL = 1, LAYERS_PERSISTENT_MMA = 2, LAYERS_STEP_TC = 3 };
+
 struct DevBuf {
     void* p = nullptr;
     size_t bytes = 0;
@@ -28,11 +31,11 @@ struct DevBuf {
 // Kernel classes of the step, timed by dspark_profile.
 enum Cat {
     CAT_INGEST_PROJ, CAT_INGEST_NORM, CAT_INGEST_KV, CAT_BLOCK, CAT_NORM, CAT_QKV, CAT_ATTN, CAT_O, CAT_GATE_UP,
-    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_LAYERS, CAT_COUNT
+    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_LAYERS, CAT_STEP, CAT_COUNT
 };
 const char* const kCatNames[CAT_COUNT] = {"ingest_proj", "ingest_norm", "ingest_kv", "block_build", "rmsnorm",
                                           "qkv_proj", "attention", "o_proj", "gate_up_proj", "down_proj",
-                                          "out_proj", "markov_argmax", "draft_layers"};
+                                          "out_proj", "markov_argmax", "draft_layers", "draft_step"};
 
 struct ProfRange {
     int cat;
@@ -135,11 +138,19 @@ struct dspark_handle {
     bool mk_fma = true;                      // one or two sequences: the FMA chain
     unsigned long long* mk_keys = nullptr;   // [2, max_seqs, 16] argmax words of the Markov chain, then 2 counters
     unsigned long long* pk_bar = nullptr;    // persistent draft layers: 2 barrier counters, then the launch epoch
+    TcWeightStream ts_tok_proj;              // tok_proj [d, H] as a 128-row weight stream
+    void* ds_maps = nullptr;                 // one-launch tcgen05 step: [2 + 4 n_layers] weight tensor maps
+    float* ds_ssq = nullptr;                 // [d / 128, 16] column-tile sums of x^2
+    float* ds_part = nullptr;                // projection partials
+    size_t ds_part_floats = 0;
+    unsigned int* ds_tickets = nullptr;      // per weight tile
+    float* ds_apart = nullptr;               // attention partials
+    size_t ds_apart_floats = 0;
+    unsigned int* ds_atickets = nullptr;     // per head
+    unsigned long long* ds_bar = nullptr;    // 2 barrier counters, then the launch epoch
     void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
     int pk_map3d = 0;
-    bool use_persistent = true;
-    bool force_persistent = false;           // one-launch layers whatever their size
-    bool fuse_norm = false;                  // RMSNorm folded into the weight-streaming projections
+    int layers_path = 0;                     // DSPARK_PATH_LAYERS: 0 auto, else the forced form
     float* ws = nullptr;
     size_t ws_floats = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
@@ -308,16 +319,6 @@ struct Prof {
 cudaError_t norm_gemm(dspark_handle* h, const float* w, int R, const WView& wv, int N, int K, const EpiParams& ep,
                       void* actA, int adt, cudaStream_t st, int norm_cat) {
     const int d = h->d;
-    // Opt-in: every CTA then rebuilds the normalised rows and their scales from the whole row of
-    // x before its first MMA, which measured slower than the separate normalisation launch on
-    // both the draft layers and the vocabulary projection.
-    if (h->fuse_norm && adt == DT_BF16 && R <= 16 && wv.ts && wv.ts->ready && tc_stream_ok(R, N, K) &&
-        K % 64 == 0 && K == d) {
-        Prof pr(h, norm_cat, st);
-        const StreamNorm sn{h->x, w, (int64_t)d, h->cfg.eps};
-        return tc_stream(nullptr, 0, *wv.ts, R, N, K, ep, h->ts_part, h->ts_part_floats, h->ts_tickets,
-                         h->ts_n_tickets, h->num_sms, h->d_err, st, &sn);
-    }
     {
         Prof pr(h, CAT_NORM, st);
         cudaError_t e = rmsnorm_rows(h->x, d, w, R, d, h->cfg.eps, adt, actA, d, st);
@@ -513,182 +514,242 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
 }
 
 // The draft step for B sequences (slots seq_ids[b], or slot b when NULL).
+// The one-launch tcgen05 step (block build, every layer, out_norm, out_proj) for a batch-1 draft
+// of a bf16 multi-head drafter without the per-head Q/K transforms; false if it does not apply.
+bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
+                     DraftStepArgs& a) {
+    const dspark_config& c = h->cfg;
+    if (B != 1 || seq_ids || h->dt != DT_BF16 || !h->ds_maps || h->qk_rope || h->nkv != c.n_heads) return false;
+    a = DraftStepArgs{};
+    a.x = h->x;
+    a.q = h->q;
+    a.act = h->act_lp;
+    a.hact = h->h_lp;
+    a.y = h->y;
+    a.U = h->U;
+    a.ssq = h->ds_ssq;
+    a.part = h->ds_part;
+    a.apart = h->ds_apart;
+    a.tickets = h->ds_tickets;
+    a.atickets = h->ds_atickets;
+    a.cache = h->cache;
+    a.layer_stride = h->layer_stride;
+    a.kv_off = h->kv_off;
+    a.max_rows = (int)h->rows;
+    a.seq_len = h->d_len;
+    a.embed = h->embed;
+    a.anchor_dev = anchors_dev;
+    a.anchor = anchor;
+    a.block_const = h->block_const;
+    a.attn_norm = h->attn_norm.data();
+    a.ff_norm = h->ff_norm.data();
+    a.out_norm = h->out_norm;
+    a.maps = h->ds_maps;
+    a.d = h->d;
+    a.F = h->F;
+    a.H = c.hidden;
+    a.V = c.vocab;
+    a.nh = c.n_heads;
+    a.nL = c.n_layers;
+    a.gamma = c.gamma;
+    a.act_kind = c.act;
+    // one attention item (head, key range) per CTA, at least one 64-key tile per range
+    a.nchunks = std::max(1, std::min(h->num_sms / c.n_heads, (max_keys + 63) / 64));
+    a.eps = c.eps;
+    a.bar = h->ds_bar;
+    a.epoch = reinterpret_cast<unsigned int*>(h->ds_bar + 2);
+    a.err = h->d_err;
+    return draft_step_tc_ok(a, h->num_sms) && draft_step_tc_part_floats(a, h->num_sms) <= h->ds_part_floats &&
+           (size_t)c.n_heads * a.nchunks * c.gamma * (h->hd + 4) <= h->ds_apart_floats;
+}
+
 dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
                          int* tokens, float* conf, float* logits, cudaStream_t st) {
     const dspark_config& c = h->cfg;
     const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
-    Prof pr_block(h, CAT_BLOCK, st);
-    CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st));
-    {
-        EpiParams ep;
-        ep.kind = EPI_ADD_F32;
-        ep.out_f32 = h->x;
-        ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
-        if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
-            // many sequences: gather the anchor embeddings, then one tensor-core GEMM
-            CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
-            CUDA_TRY(h, tc_gemm(h->emb_rows, c.hidden, h->tc_tok_proj, B, d, c.hidden, ep, h->num_sms, h->d_err, st));
-        } else {
-            CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
-                             WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
-        }
+    DraftStepArgs dsa;
+    const bool one_launch = h->layers_path == LAYERS_STEP_TC &&
+                            draft_step_args(h, B, seq_ids, anchors_dev, anchor, max_keys, dsa);
+    if (one_launch) {
+        Prof pr(h, CAT_STEP, st);
+        CUDA_TRY(h, draft_step_tc(dsa, h->num_sms, st));
     }
-    const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
-    void* actA = lowp ? h->act_lp : (void*)h->act;
-    const int adt = lowp ? DT_BF16 : DT_F32;
-    bool layers_done = false;
-    // One persistent launch for every layer pays off while a layer's weights are
-    // a few slices per SM (its projections run on the legacy warp MMA); larger
-    // layers stream faster through the per-kernel tcgen05 path.
-    const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
-    const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
-    // (the one-launch layers keep one K/V head per query head and no per-head transform)
-    if (B == 1 && !seq_ids && lowp && h->use_persistent && (persistent_fits || h->force_persistent) && !h->qk_rope &&
-        h->nkv == c.n_heads) {
-        // every layer in one persistent launch
-        DraftPersistArgs a{};
-        a.x = h->x;
-        a.q = h->q;
-        a.act = h->act_lp;
-        a.hact = h->h_lp;
-        a.part = h->attn_part;
-        a.cache = h->cache;
-        a.layer_stride = h->layer_stride;
-        a.kv_off = h->kv_off;
-        a.max_rows = (int)h->rows;
-        a.seq_len = h->d_len;
-        a.wqkv = h->wqkv.data();
-        a.wo = h->wo.data();
-        a.wgu = h->wgu.data();
-        a.wd = h->wd.data();
-        a.attn_norm = h->attn_norm.data();
-        a.ff_norm = h->ff_norm.data();
-        a.d = d;
-        a.F = F;
-        a.nh = c.n_heads;
-        a.nL = c.n_layers;
-        a.gamma = c.gamma;
-        a.act_kind = c.act;
-        a.nchunks = std::max(1, std::min({32, h->num_sms / c.n_heads, (max_keys + 63) / 64}));
-        a.eps = c.eps;
-        a.maps = h->pk_maps;
-        a.map3d = h->pk_map3d;
-        a.bar = h->pk_bar;
-        a.epoch = reinterpret_cast<unsigned int*>(h->pk_bar + 2);
-        a.err = h->d_err;
-        if (draft_persistent_ok(a) &&
-            attn_scratch_floats(1, c.n_heads, a.nchunks, c.gamma, h->hd) <= h->attn_part_floats) {
-            pr_block.end();
-            Prof pr(h, CAT_LAYERS, st);
-            CUDA_TRY(h, draft_persistent(a, h->num_sms, st));
-            layers_done = true;
-        }
-    }
-    // Batch 1: the residual epilogues of W_o and W_down also write the next projection's operand
-    // bf16(x * g) and the row sums of x^2, so no normalisation launch sits between the layers.
-    const bool chain = !layers_done && norm_chain_ok(h, R, lowp);
-    for (int i = 0; i < c.n_layers && !layers_done; ++i) {
-        if (i == 0) pr_block.end();
-        EpiParams qkv = cache_epi(h, i);
-        qkv.kind = EPI_QKV;
-        qkv.out_f32 = h->q;
-        qkv.ldo = d;
-        qkv.gamma = c.gamma;
-        qkv.seq_ids = seq_ids;
-        const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
-        if (chain && i > 0)
-            CUDA_TRY(h, chained_gemm(h, R, wqkv, d + 2 * h->dkv, d, qkv, st, CAT_QKV));
-        else
-            CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, d + 2 * h->dkv, d, qkv, actA, adt, st, CAT_QKV));
-        if (h->qk_rope) {
-            Prof pq(h, CAT_QKV, st);
-            QkRope qr = qk_rope_args(h, i);
-            qr.q = h->q;
-            qr.ldq = d;
-            qr.q_norm = h->cfg.qk_norm ? h->q_norm[i] : nullptr;
-            qr.B = B;
-            qr.gamma = c.gamma;
-            qr.seq_ids = seq_ids;
-            CUDA_TRY(h, qk_rope_block(qr, st));
-        }
-        AttnParams ap;
-        ap.q = h->q;
-        ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
-        ap.cache_dtype = h->dt;
-        ap.seq_stride = h->seq_stride;
-        ap.kv_off = h->kv_off;
-        ap.seq_len = h->d_len;
-        ap.seq_ids = seq_ids;
-        ap.B = B;
-        ap.gamma = c.gamma;
-        ap.d = d;
-        ap.n_heads = c.n_heads;
-        ap.d_kv = h->dkv;
-        ap.n_kv_heads = h->nkv;
-        ap.n_chunks = attn_chunks(h, B, max_keys);
-        ap.part = h->attn_part;
-        ap.tickets = h->attn_tickets;
-        ap.out = actA;
-        ap.out_dtype = adt;
-        if (attn_scratch_floats(B, c.n_heads, ap.n_chunks, c.gamma, h->hd) > h->attn_part_floats)
-            return fail(h, DSPARK_ERR_CAPACITY, "attention scratch too small");
+    if (!one_launch) {
+        Prof pr_block(h, CAT_BLOCK, st);
+        CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st));
         {
-            Prof pr(h, CAT_ATTN, st);
-            CUDA_TRY(h, attention(ap, st));
+            EpiParams ep;
+            ep.kind = EPI_ADD_F32;
+            ep.out_f32 = h->x;
+            ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
+            if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
+                // many sequences: gather the anchor embeddings, then one tensor-core GEMM
+                CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
+                CUDA_TRY(h, tc_gemm(h->emb_rows, c.hidden, h->tc_tok_proj, B, d, c.hidden, ep, h->num_sms, h->d_err, st));
+            } else {
+                CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
+                                 WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
+            }
         }
-        EpiParams res;
-        res.kind = EPI_ADD_F32;
-        res.out_f32 = h->x;
-        res.ldo = d;
-        if (chain) {
-            res.xb = h->xb;
-            res.ld_xb = d;
-            res.ssp = h->ssp;
-            res.xb_g = h->ff_norm[i];
+        const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
+        void* actA = lowp ? h->act_lp : (void*)h->act;
+        const int adt = lowp ? DT_BF16 : DT_F32;
+        bool layers_done = false;
+        // One persistent launch for every layer pays off while a layer's weights are
+        // a few slices per SM (its projections run on the legacy warp MMA); larger
+        // layers stream faster through the per-kernel tcgen05 path.
+        const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
+        const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
+        // (the one-launch layers keep one K/V head per query head and no per-head transform)
+        if (B == 1 && !seq_ids && lowp &&
+            (h->layers_path == LAYERS_PERSISTENT_MMA || (h->layers_path == LAYERS_AUTO && persistent_fits)) &&
+            !h->qk_rope &&
+            h->nkv == c.n_heads) {
+            // every layer in one persistent launch
+            DraftPersistArgs a{};
+            a.x = h->x;
+            a.q = h->q;
+            a.act = h->act_lp;
+            a.hact = h->h_lp;
+            a.part = h->attn_part;
+            a.cache = h->cache;
+            a.layer_stride = h->layer_stride;
+            a.kv_off = h->kv_off;
+            a.max_rows = (int)h->rows;
+            a.seq_len = h->d_len;
+            a.wqkv = h->wqkv.data();
+            a.wo = h->wo.data();
+            a.wgu = h->wgu.data();
+            a.wd = h->wd.data();
+            a.attn_norm = h->attn_norm.data();
+            a.ff_norm = h->ff_norm.data();
+            a.d = d;
+            a.F = F;
+            a.nh = c.n_heads;
+            a.nL = c.n_layers;
+            a.gamma = c.gamma;
+            a.act_kind = c.act;
+            a.nchunks = std::max(1, std::min({32, h->num_sms / c.n_heads, (max_keys + 63) / 64}));
+            a.eps = c.eps;
+            a.maps = h->pk_maps;
+            a.map3d = h->pk_map3d;
+            a.bar = h->pk_bar;
+            a.epoch = reinterpret_cast<unsigned int*>(h->pk_bar + 2);
+            a.err = h->d_err;
+            if (draft_persistent_ok(a) &&
+                attn_scratch_floats(1, c.n_heads, a.nchunks, c.gamma, h->hd) <= h->attn_part_floats) {
+                pr_block.end();
+                Prof pr(h, CAT_LAYERS, st);
+                CUDA_TRY(h, draft_persistent(a, h->num_sms, st));
+                layers_done = true;
+            }
+        }
+        // Batch 1: the residual epilogues of W_o and W_down also write the next projection's operand
+        // bf16(x * g) and the row sums of x^2, so no normalisation launch sits between the layers.
+        const bool chain = !layers_done && norm_chain_ok(h, R, lowp);
+        for (int i = 0; i < c.n_layers && !layers_done; ++i) {
+            if (i == 0) pr_block.end();
+            EpiParams qkv = cache_epi(h, i);
+            qkv.kind = EPI_QKV;
+            qkv.out_f32 = h->q;
+            qkv.ldo = d;
+            qkv.gamma = c.gamma;
+            qkv.seq_ids = seq_ids;
+            const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
+            if (chain && i > 0)
+                CUDA_TRY(h, chained_gemm(h, R, wqkv, d + 2 * h->dkv, d, qkv, st, CAT_QKV));
+            else
+                CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, d + 2 * h->dkv, d, qkv, actA, adt, st, CAT_QKV));
+            if (h->qk_rope) {
+                Prof pq(h, CAT_QKV, st);
+                QkRope qr = qk_rope_args(h, i);
+                qr.q = h->q;
+                qr.ldq = d;
+                qr.q_norm = h->cfg.qk_norm ? h->q_norm[i] : nullptr;
+                qr.B = B;
+                qr.gamma = c.gamma;
+                qr.seq_ids = seq_ids;
+                CUDA_TRY(h, qk_rope_block(qr, st));
+            }
+            AttnParams ap;
+            ap.q = h->q;
+            ap.cache = (char*)h->cache + (size_t)i * h->layer_stride * h->esz;
+            ap.cache_dtype = h->dt;
+            ap.seq_stride = h->seq_stride;
+            ap.kv_off = h->kv_off;
+            ap.seq_len = h->d_len;
+            ap.seq_ids = seq_ids;
+            ap.B = B;
+            ap.gamma = c.gamma;
+            ap.d = d;
+            ap.n_heads = c.n_heads;
+            ap.d_kv = h->dkv;
+            ap.n_kv_heads = h->nkv;
+            ap.n_chunks = attn_chunks(h, B, max_keys);
+            ap.part = h->attn_part;
+            ap.tickets = h->attn_tickets;
+            ap.out = actA;
+            ap.out_dtype = adt;
+            if (attn_scratch_floats(B, c.n_heads, ap.n_chunks, c.gamma, h->hd) > h->attn_part_floats)
+                return fail(h, DSPARK_ERR_CAPACITY, "attention scratch too small");
+            {
+                Prof pr(h, CAT_ATTN, st);
+                CUDA_TRY(h, attention(ap, st));
+            }
+            EpiParams res;
+            res.kind = EPI_ADD_F32;
+            res.out_f32 = h->x;
+            res.ldo = d;
+            if (chain) {
+                res.xb = h->xb;
+                res.ld_xb = d;
+                res.ssp = h->ssp;
+                res.xb_g = h->ff_norm[i];
+            }
+            {
+                Prof pr(h, CAT_O, st);
+                CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
+                                 WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
+            }
+            EpiParams sw;
+            sw.kind = EPI_SWIGLU;
+            sw.out_act = lowp ? h->h_lp : (void*)h->hbuf;
+            sw.act_dtype = adt;
+            sw.ld_act = F;
+            sw.act = c.act;
+            const WView wgu{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)};
+            if (chain)
+                CUDA_TRY(h, chained_gemm(h, R, wgu, 2 * F, d, sw, st, CAT_GATE_UP));
+            else
+                CUDA_TRY(h, norm_gemm(h, h->ff_norm[i], R, wgu, 2 * F, d, sw, actA, adt, st, CAT_GATE_UP));
+            if (chain) res.xb_g = i + 1 < c.n_layers ? h->attn_norm[i + 1] : h->out_norm;
+            {
+                Prof pr(h, CAT_DOWN, st);
+                CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
+                                 WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F, res, st));
+            }
         }
         {
-            Prof pr(h, CAT_O, st);
-            CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
-                             WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
+            Prof pr(h, CAT_NORM, st);
+            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
         }
-        EpiParams sw;
-        sw.kind = EPI_SWIGLU;
-        sw.out_act = lowp ? h->h_lp : (void*)h->hbuf;
-        sw.act_dtype = adt;
-        sw.ld_act = F;
-        sw.act = c.act;
-        const WView wgu{h->wgu[i], at_or_null(h->tc_wgu, i), at_or_null(h->ts_wgu, i)};
-        if (chain)
-            CUDA_TRY(h, chained_gemm(h, R, wgu, 2 * F, d, sw, st, CAT_GATE_UP));
-        else
-            CUDA_TRY(h, norm_gemm(h, h->ff_norm[i], R, wgu, 2 * F, d, sw, actA, adt, st, CAT_GATE_UP));
-        if (chain) res.xb_g = i + 1 < c.n_layers ? h->attn_norm[i + 1] : h->out_norm;
         {
-            Prof pr(h, CAT_DOWN, st);
-            CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
-                             WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F, res, st));
-        }
-    }
-    {
-        Prof pr(h, CAT_NORM, st);
-        CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
-    }
-    {
-        EpiParams ep;
-        ep.kind = EPI_STORE_F32;
-        ep.out_f32 = h->U;
-        ep.ldo = V;
-        if (chain) {
-            CUDA_TRY(h, chained_gemm(h, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep, st,
-                                     CAT_OUT_PROJ));
-        } else if (lowp) {
-            // norm_gemm opens its own normalisation and projection ranges
-            CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
-                                  h->act_lp, DT_BF16, st, CAT_OUT_PROJ));
-        } else {
-            Prof pr(h, CAT_OUT_PROJ, st);
-            CUDA_TRY(h, gemm(h, DT_F32, h->y, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V,
-                             d, ep, st));
+            EpiParams ep;
+            ep.kind = EPI_STORE_F32;
+            ep.out_f32 = h->U;
+            ep.ldo = V;
+            if (chain) {
+                CUDA_TRY(h, chained_gemm(h, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep, st,
+                                         CAT_OUT_PROJ));
+            } else if (lowp) {
+                // norm_gemm opens its own normalisation and projection ranges
+                CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
+                                      h->act_lp, DT_BF16, st, CAT_OUT_PROJ));
+            } else {
+                Prof pr(h, CAT_OUT_PROJ, st);
+                CUDA_TRY(h, gemm(h, DT_F32, h->y, d, nullptr, 0, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, R, V,
+                                 d, ep, st));
+            }
         }
     }
     MarkovParams mp;
@@ -1239,13 +1300,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             h->pk_map3d = three;
         }
     }
-    if (const char* env = getenv("DSPARK_NO_PERSISTENT")) h->use_persistent = env[0] == '0';
-    if (const char* env = getenv("DSPARK_MARKOV_MMA")) h->mk_fma = env[0] != '1';
-    if (const char* env = getenv("DSPARK_PERSISTENT")) h->force_persistent = env[0] == '1';
-    if (const char* env = getenv("DSPARK_NO_NORM_CHAIN")) h->chain_norm = env[0] == '0';
-    if (const char* env = getenv("DSPARK_NORM_FUSION")) h->fuse_norm = env[0] == '1';
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
-    if (const char* env = getenv("DSPARK_NO_GRAPHS")) h->use_graphs = env[0] == '0';
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));
     CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
     h->ws_floats = (size_t)4 << 20;
@@ -1313,6 +1368,43 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         CTRY(dalloc(h, (void**)&h->ts_part, std::max<size_t>(part, 4) * 4));
         CTRY(dalloc(h, (void**)&h->ts_tickets, tiles * sizeof(unsigned int)));
         CTRY(cudaMemsetAsync(h->ts_tickets, 0, tiles * sizeof(unsigned int), st));
+        // the one-launch tcgen05 draft step: its weight maps in launch order, and its scratch
+        CTRY(tc_stream_prepare(h->ts_tok_proj, h->tok_proj, d, H));
+        CTRY(draft_step_tc_init());
+        bool maps_ok = h->ts_tok_proj.ready && h->ts_out_proj.ready;
+        for (int i = 0; i < nL; ++i)
+            maps_ok = maps_ok && h->ts_qkv[i].ready && h->ts_wo[i].ready && h->ts_wgu[i].ready && h->ts_wd[i].ready;
+        if (maps_ok && dkv == d && d % 128 == 0) {
+            struct alignas(64) Map128 {
+                unsigned char b[128];
+            };
+            std::vector<Map128> maps((size_t)2 + 4 * nL);
+            auto put = [&](size_t k, const TcWeightStream& w) { memcpy(maps[k].b, w.tmap, 128); };
+            put(0, h->ts_tok_proj);
+            for (int i = 0; i < nL; ++i) {
+                put(1 + 4 * i, h->ts_qkv[i]);
+                put(2 + 4 * i, h->ts_wo[i]);
+                put(3 + 4 * i, h->ts_wgu[i]);
+                put(4 + 4 * i, h->ts_wd[i]);
+            }
+            put(1 + 4 * (size_t)nL, h->ts_out_proj);
+            CTRY(dalloc(h, &h->ds_maps, maps.size() * sizeof(Map128)));
+            CTRY(cudaMemcpyAsync(h->ds_maps, maps.data(), maps.size() * sizeof(Map128), cudaMemcpyHostToDevice, st));
+            CTRY(cudaStreamSynchronize(st));  // the host array goes out of scope
+            const int G = h->num_sms;
+            const size_t max_tiles = (size_t)(std::max({3 * d, 2 * F, V}) + 127) / 128;
+            h->ds_part_floats = (max_tiles + G) * cfg->gamma * 128;
+            CTRY(dalloc(h, (void**)&h->ds_part, h->ds_part_floats * 4));
+            CTRY(dalloc(h, (void**)&h->ds_tickets, max_tiles * sizeof(unsigned int)));
+            CTRY(cudaMemsetAsync(h->ds_tickets, 0, max_tiles * sizeof(unsigned int), st));
+            CTRY(dalloc(h, (void**)&h->ds_ssq, (size_t)(d / 128) * 16 * sizeof(float)));
+            h->ds_apart_floats = (size_t)G * cfg->gamma * (h->hd + 4);
+            CTRY(dalloc(h, (void**)&h->ds_apart, h->ds_apart_floats * 4));
+            CTRY(dalloc(h, (void**)&h->ds_atickets, (size_t)cfg->n_heads * sizeof(unsigned int)));
+            CTRY(cudaMemsetAsync(h->ds_atickets, 0, (size_t)cfg->n_heads * sizeof(unsigned int), st));
+            CTRY(dalloc(h, (void**)&h->ds_bar, 3 * sizeof(unsigned long long)));
+            CTRY(cudaMemsetAsync(h->ds_bar, 0, 3 * sizeof(unsigned long long), st));
+        }
     }
     CTRY(cudaStreamSynchronize(st));
 #undef CTRY
@@ -1459,8 +1551,36 @@ dspark_status dspark_set_sampling(dspark_handle* h, float temperature, int32_t t
     return DSPARK_OK;
 }
 
+dspark_status dspark_set_path(dspark_handle* h, int32_t what, int32_t value) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    switch (what) {
+        case DSPARK_PATH_LAYERS:
+            if (value < 0 || value > 3) return fail(h, DSPARK_ERR_INVALID_ARG, "layers path must be in [0, 3]");
+            h->layers_path = value;
+            break;
+        case DSPARK_PATH_MARKOV:
+            if (value < 0 || value > 1) return fail(h, DSPARK_ERR_INVALID_ARG, "Markov path must be 0 or 1");
+            h->mk_fma = value == 0;
+            break;
+        case DSPARK_PATH_NORM_CHAIN:
+            if (value < 0 || value > 1) return fail(h, DSPARK_ERR_INVALID_ARG, "norm-chain path must be 0 or 1");
+            h->chain_norm = value == 0;
+            break;
+        case DSPARK_PATH_GRAPHS:
+            if (value < 0 || value > 1) return fail(h, DSPARK_ERR_INVALID_ARG, "graphs path must be 0 or 1");
+            h->use_graphs = value == 0;
+            break;
+        default:
+            return fail(h, DSPARK_ERR_INVALID_ARG, "unknown path");
+    }
+    // captured draft steps were recorded with the old choice
+    for (auto& g : h->graphs) destroy_graph(g);
+    h->graphs.clear();
+    return DSPARK_OK;
+}
+
 dspark_status dspark_selftest_wait(int32_t which, int32_t* word_host) {
-    if (which < 0 || which > 4) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "which must be in [0, 4]");
+    if (which < 0 || which > 5) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "which must be in [0, 5]");
     void* scratch = nullptr;
     int* err = nullptr;
     cudaStream_t st = nullptr;
@@ -1478,7 +1598,8 @@ dspark_status dspark_selftest_wait(int32_t which, int32_t* word_host) {
     if (e == cudaSuccess) {
         if (which <= 2) e = markov_wait_selftest(which, scratch, err, st);
         else if (which == 3) e = persistent_wait_selftest(scratch, err, st);
-        else e = mbar_wait_selftest(err, st);
+        else if (which == 4) e = mbar_wait_selftest(err, st);
+        else e = step_wait_selftest(scratch, err, st);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     int v = 0;

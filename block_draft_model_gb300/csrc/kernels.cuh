@@ -192,6 +192,43 @@ cudaError_t draft_persistent_init();  // once per process/device
 bool draft_persistent_ok(const DraftPersistArgs& a);
 cudaError_t draft_persistent(const DraftPersistArgs& a, int num_sms, cudaStream_t st);
 
+// Batch-1 draft step up to the logits in one cooperative launch with tcgen05 projections
+// (draft_step_tc.cu): block build, every layer, out_norm and out_proj.
+struct DraftStepArgs {
+    float* x;                   // [gamma, d]
+    float* q;                   // [gamma, d]
+    void* act;                  // [gamma, d] bf16
+    void* hact;                 // [gamma, F] bf16
+    float* y;                   // [gamma, d]
+    float* U;                   // [gamma, V]
+    float* ssq;                 // [d / 128, 16]
+    float* part;                // draft_step_tc_part_floats floats
+    float* apart;               // n_heads * nchunks * gamma * (head_dim + 4) floats
+    unsigned int* tickets;      // [max(3d, 2F, V) / 128] zero-initialised
+    unsigned int* atickets;     // [n_heads] zero-initialised
+    void* cache;                // layer 0 base (bf16), slot 0
+    int64_t layer_stride, kv_off;
+    int max_rows;
+    const int* seq_len;         // device; entry 0
+    const void* embed;          // [V, H] bf16
+    const int* anchor_dev;      // device [1] or nullptr
+    int anchor;
+    const float* block_const;   // [gamma, d]
+    const float* const* attn_norm;
+    const float* const* ff_norm;
+    const float* out_norm;
+    const void* maps;           // device [2 + 4 n_layers] weight tensor maps (box 64 x 128, 128-byte swizzle)
+    int d, F, H, V, nh, nL, gamma, act_kind, nchunks;
+    float eps;
+    unsigned long long* bar;    // 2 zero-initialised words
+    unsigned int* epoch;        // zero-initialised
+    int* err;
+};
+cudaError_t draft_step_tc_init();  // per device
+bool draft_step_tc_ok(const DraftStepArgs& a, int num_sms);
+size_t draft_step_tc_part_floats(const DraftStepArgs& a, int num_sms);
+cudaError_t draft_step_tc(const DraftStepArgs& a, int num_sms, cudaStream_t st);
+
 // ------------------------------------------------------------------ Markov chain, argmax, confidence
 struct MarkovParams {
     const float* U;          // [B*gamma, V] base logits
@@ -286,6 +323,7 @@ cudaError_t markov_sample_step(const SampleParams& p, int num_sms, cudaStream_t 
 cudaError_t markov_wait_selftest(int which, void* scratch, int* err, cudaStream_t st);
 cudaError_t persistent_wait_selftest(void* scratch, int* err, cudaStream_t st);
 cudaError_t mbar_wait_selftest(int* err, cudaStream_t st);
+cudaError_t step_wait_selftest(void* scratch, int* err, cudaStream_t st);
 
 bool markov_chain_fma_ok(const MarkovParams& p, int num_sms);
 cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st);

@@ -212,14 +212,8 @@ __global__ void k_to_float(const T* __restrict__ in, int64_t n, float* __restric
 
 }  // namespace
 
-static int g_pdl = -1;
-bool pdl_enabled() {
-    if (g_pdl < 0) {
-        const char* e = getenv("DSPARK_NO_PDL");
-        g_pdl = (e && e[0] == '1') ? 0 : 1;
-    }
-    return g_pdl == 1;
-}
+// Every launch of the step uses programmatic dependent launch.
+bool pdl_enabled() { return true; }
 
 static long long g_launches = 0;
 long long launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }

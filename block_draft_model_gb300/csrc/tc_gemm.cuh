@@ -54,16 +54,12 @@ struct TcWeightStream {
 bool tc_stream_ok(int M, int N, int K);
 size_t tc_stream_scratch_floats(int N, int K, int num_sms);
 cudaError_t tc_stream_prepare(TcWeightStream& w, const void* ptr, int N, int K);
-// Pre-norm operand of tc_stream: the X side is x * g (x fp32 [M, ldx], g fp32 [K])
-// and the accumulator row m is scaled by 1 / sqrt(mean_k(x[m][k]^2) + eps): the
-// product with RMSNorm(x) * g without a separate normalisation kernel.
+// Row scales of tc_stream: X is bf16(x * g) already, and the accumulator row m is scaled by
+// 1 / sqrt(mean_k(x[m][k]^2) + eps) from the 8-column sums of x^2 written by the epilogue that
+// produced x: the product with RMSNorm(x) * g without a separate normalisation kernel.
 struct StreamNorm {
-    const float* x = nullptr;    // pre-norm form: the fp32 rows and the norm weight g
-    const float* g = nullptr;
-    int64_t ldx = 0;
+    const float* ssp = nullptr;  // ssp[(k / 8) * 16 + m] = sum of x[m]^2 over columns [k, k + 8)
     float eps = 0.f;
-    const float* ssp = nullptr;  // row-sum form: X is bf16(x * g) already; ssp[(k / 8) * 16 + m] = sum of x[m]^2
-                                 // over columns [k, k + 8), written by the epilogue that produced x
 };
 cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M, int N, int K, const EpiParams& ep,
                       float* part, size_t part_floats, unsigned int* tickets, size_t n_tickets, int num_sms, int* err,

@@ -76,94 +76,6 @@ __device__ __forceinline__ float epi_add_xb(const EpiParams& ep, int m, int n, f
     return x * x;
 }
 
-// Pre-norm operand, built by the four epilogue warps while the weights stream:
-// the MMA's X side for K block kb is bf16(x[m][kb*64 + j] * g[kb*64 + j]) (rows
-// m >= M zero), written into the ring's X slot in the 128-byte-swizzled layout
-// a TMA copy would give (row m at m * 128, 16-byte chunk c at c ^ (m & 7)); the
-// RMSNorm row scale 1 / sqrt(mean(x[m]^2) + eps) over the whole row is applied to
-// the accumulator, so the product is W . (RMSNorm(x) * g) up to the rounding of
-// the operand.  Each stage's full barrier counts the builder's arrival too.
-// x * g of one 16-byte operand chunk (rows m >= M: zero).
-__device__ __forceinline__ uint4 prenorm_chunk(const StreamNorm& sn, int M, int m, int k) {
-    if (m >= M) return make_uint4(0, 0, 0, 0);
-    const float4* xr = reinterpret_cast<const float4*>(sn.x + (int64_t)m * sn.ldx + k);
-    const float4* gr = reinterpret_cast<const float4*>(sn.g + k);
-    const float4 x0 = __ldcg(xr), x1 = __ldcg(xr + 1), g0 = __ldg(gr), g1 = __ldg(gr + 1);
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(x0.x * g0.x, x0.y * g0.y);
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(x0.z * g0.z, x0.w * g0.w);
-    __nv_bfloat162 p2 = __floats2bfloat162_rn(x1.x * g1.x, x1.y * g1.y);
-    __nv_bfloat162 p3 = __floats2bfloat162_rn(x1.z * g1.z, x1.w * g1.w);
-    return make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                      *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
-}
-
-__device__ __forceinline__ void build_prenorm(const StreamNorm& sn, int M, int K, int kb0, int kb1, uint32_t sX,
-                                              uint64_t* full, uint64_t* empty, float* rsc, volatile int* abort_flag,
-                                              volatile int* bfail) {
-    constexpr int GRP = 4;  // K blocks whose operand loads are in flight together
-    const int t = threadIdx.x - 64;  // 0..127
-    const int m = t >> 3, c = t & 7;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    uint4 cur[GRP];
-#pragma unroll
-    for (int u = 0; u < GRP; ++u) cur[u] = kb0 + u < kb1 ? prenorm_chunk(sn, M, m, (kb0 + u) * BK + c * 8) : make_uint4(0, 0, 0, 0);
-    for (int g0 = kb0; g0 < kb1 && ok; g0 += GRP) {
-        uint4 nxt[GRP];  // the next group's loads go out before this group is stored
-#pragma unroll
-        for (int u = 0; u < GRP; ++u) {
-            const int kb = g0 + GRP + u;
-            nxt[u] = kb < kb1 ? prenorm_chunk(sn, M, m, kb * BK + c * 8) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < GRP; ++u) {
-            if (g0 + u >= kb1) break;
-            // every builder thread passes the same barriers: a failed wait is published in
-            // the builder's own flag before the barrier and read by all after it
-            if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-                const uint32_t dst = sX + stage * X_BYTES + m * 128 + ((c ^ (m & 7)) * 16);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(cur[u].x), "r"(cur[u].y),
-                             "r"(cur[u].z), "r"(cur[u].w)
-                             : "memory");
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
-            } else {
-                *bfail = 1;
-            }
-            epi_bar();
-            if (*bfail) {
-                ok = false;
-                break;
-            }
-            if (t == 0) mbar_arrive(&full[stage]);
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < GRP; ++u) cur[u] = nxt[u];
-    }
-    // row scales over the whole row (needed only by the epilogue); eight loads in flight per thread
-    float ss = 0.f;
-    if (m < M) {
-        const float4* xr = reinterpret_cast<const float4*>(sn.x + (int64_t)m * sn.ldx);
-        const int n4 = K / 4;
-        for (int k0 = c; k0 < n4; k0 += 64) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = k0 + 8 * u < n4 ? __ldcg(xr + k0 + 8 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
-        }
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-    if (c == 0) rsc[m] = rsqrtf(ss / (float)K + sn.eps);
-    epi_bar();
-}
-
 // grid: n_tiles * splits CTAs; CTA b handles tile b / splits, K blocks
 // [s * kb_per, min(nkb, (s + 1) * kb_per)) with s = b % splits.
 __global__ void __launch_bounds__(NTHREADS, 2)
@@ -182,11 +94,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* is_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    float* rsc = reinterpret_cast<float*>(bars + 16);  // pre-norm row scales [BN]
-    volatile int* bfail = reinterpret_cast<volatile int*>(bars + 24);  // pre-norm builder gave up
-    float* rs_red = reinterpret_cast<float*>(bars + 32);               // row-sum form partials [8][16]
-    const bool prenorm = sn.x != nullptr;
-    const bool rowscale = !prenorm && sn.ssp != nullptr;
+    float* rsc = reinterpret_cast<float*>(bars + 16);    // row scales [BN]
+    float* rs_red = reinterpret_cast<float*>(bars + 32);  // row-sum partials [8][16]
+    const bool rowscale = sn.ssp != nullptr;
     const bool xbm = ep.ssp != nullptr;  // EPI_ADD_F32 that also writes the next operand and row sums
     // EPI_ADD_F32 reduced in the cluster: the residual entries this thread will own in the final
     // epilogue (at most two items of four activation rows), loaded while the weights stream; no other
@@ -202,12 +112,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], prenorm ? 2 : 1);  // pre-norm: the weight copy and the X builder
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
-        *bfail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -225,8 +134,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     if (warp == 0) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
-            if (!prenorm) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
-            const uint32_t stage_tx = prenorm ? W_BYTES : W_BYTES + X_BYTES;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+            const uint32_t stage_tx = W_BYTES + X_BYTES;
             // The weights are never written by the step: the first ring of weight tiles
             // is requested before waiting for the kernels that produce X.
             const int pre = min(STAGES, kb1 - kb0);
@@ -235,15 +144,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 tma_load_2d(sW + i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0);
             }
             pdl_wait();
-            if (!prenorm)
-                for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * X_BYTES, &tmX, &full[i], (kb0 + i) * BK, 0);
+            for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * X_BYTES, &tmX, &full[i], (kb0 + i) * BK, 0);
             int stage = pre % STAGES;
             uint32_t phase = pre == STAGES ? 1u : 0u;
             for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) break;
                 mbar_arrive_expect_tx(&full[stage], stage_tx);
                 tma_load_2d(sW + stage * W_BYTES, &tmW, &full[stage], kb * BK, n0);
-                if (!prenorm) tma_load_2d(sX + stage * X_BYTES, &tmX, &full[stage], kb * BK, 0);
+                tma_load_2d(sX + stage * X_BYTES, &tmX, &full[stage], kb * BK, 0);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -300,7 +208,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                                       : 0.f;
             }
         }
-        if (prenorm) build_prenorm(sn, M, K, kb0, kb1, sX, full, empty, rsc, abort_flag, bfail);
         if (rowscale) build_rowscale(sn, K, rs_red, rsc);
         const int q = warp & 3;
         const int row = q * 32 + lane;  // weight row within the tile
@@ -312,7 +219,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             uint32_t r[BN];
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16), r);
 #pragma unroll
-            for (int m = 0; m < BN; ++m) v[m] = __uint_as_float(r[m]) * ((prenorm || rowscale) ? rsc[m] : 1.f);
+            for (int m = 0; m < BN; ++m) v[m] = __uint_as_float(r[m]) * (rowscale ? rsc[m] : 1.f);
         } else {
 #pragma unroll
             for (int m = 0; m < BN; ++m) v[m] = 0.f;
@@ -564,33 +471,13 @@ cudaError_t mbar_wait_selftest(int* err, cudaStream_t st) {
 
 bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && N >= 1 && K >= BK && K % 8 == 0; }
 
-// Largest split of K (environment DSPARK_STREAM_MAX_SPLITS, default 8).
-int max_splits() {
-    static int v = -1;
-    if (v < 0) {
-        const char* e = getenv("DSPARK_STREAM_MAX_SPLITS");
-        v = e ? atoi(e) : 8;
-        if (v < 1) v = 1;
-        if (v > 16) v = 16;
-    }
-    return v;
-}
-
-// Split-K reduction through distributed shared memory (environment
-// DSPARK_STREAM_CLUSTER=0 selects the scratch-and-ticket reduction instead).
-bool cluster_splits_enabled() {
-    static int v = -1;
-    if (v < 0) {
-        const char* e = getenv("DSPARK_STREAM_CLUSTER");
-        v = (e && e[0] == '0') ? 0 : 1;
-    }
-    return v == 1;
-}
+// Largest split of K; split-K partial sums are reduced inside a thread-block cluster through
+// distributed shared memory where the split allows, else through scratch and tile tickets.
+constexpr int kMaxSplits = 8;
 
 int choose_splits(int nT, int nkb, int num_sms) {
     int splits = (2 * num_sms + nT - 1) / nT;
-    const int mx = max_splits();
-    return splits < 1 ? 1 : (splits > nkb ? nkb : (splits > mx ? mx : splits));
+    return splits < 1 ? 1 : (splits > nkb ? nkb : (splits > kMaxSplits ? kMaxSplits : splits));
 }
 
 size_t tc_stream_scratch_floats(int N, int K, int num_sms) {
@@ -606,27 +493,18 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     StreamNorm sn{};
     CUtensorMap tmX;
     if (ep.ssp && (ep.kind != EPI_ADD_F32 || !ep.xb || !ep.xb_g || N % 8 != 0)) return cudaErrorInvalidValue;
-    if (norm && norm->x) {
-        if (!norm->g || K % BK != 0 || norm->ldx < K || norm->ldx % 4 != 0 || ((uintptr_t)norm->x & 15) != 0 ||
-            ((uintptr_t)norm->g & 15) != 0)
-            return cudaErrorInvalidValue;
-        sn = *norm;
-        sn.ssp = nullptr;
-        tmX = *reinterpret_cast<const CUtensorMap*>(w.tmap);  // unused in the pre-norm mode
-    } else {
-        if (norm) {
-            if (!norm->ssp || K % 8 != 0) return cudaErrorInvalidValue;
-            sn.ssp = norm->ssp;
-            sn.eps = norm->eps;
-        }
-        if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
-        if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
+    if (norm) {
+        if (!norm->ssp || K % 8 != 0) return cudaErrorInvalidValue;
+        sn.ssp = norm->ssp;
+        sn.eps = norm->eps;
     }
+    if (ldx % 8 != 0 || ((uintptr_t)X & 15) != 0) return cudaErrorInvalidValue;
+    if (!encode(&tmX, X, M, K, ldx, BN)) return cudaErrorInvalidValue;
     const int nT = (N + BM - 1) / BM, nkb = (K + BK - 1) / BK;
     int splits = choose_splits(nT, nkb, num_sms);
     while (splits > 1 && ((size_t)nT * splits * BM * BN > part_floats || (size_t)nT > n_tickets)) --splits;
     const CUtensorMap& tmW = *reinterpret_cast<const CUtensorMap*>(w.tmap);
-    if (cluster_splits_enabled() && part_floats != 0) {
+    if (part_floats != 0) {
         // cluster reduction: splits is a power of two (cluster size <= 8) and every split non-empty
         int cs = 1;
         while (cs * 2 <= choose_splits(nT, nkb, num_sms) && cs * 2 <= 8 && cs * 2 <= nkb) cs *= 2;

@@ -210,7 +210,8 @@ dspark_status dspark_context_length(dspark_handle* h, int32_t seq_id, int32_t* o
  * kernel of its own on a private stream: which = 0 the single-sequence Markov
  * chain's arrival count, 1 the resident chain's barrier, 2 the cooperative
  * chain's barrier, 3 the one-launch layers' grid barrier, 4 the tensor-core
- * kernels' mbarrier wait.  The wait gives up after its limit (about one second)
+ * kernels' mbarrier wait, 5 the one-launch step's grid barrier (whose outcome
+ * every thread of the CTA takes alike).  The wait gives up after its limit (about one second)
  * and the kernel returns normally; *word_host (may be NULL) receives the error
  * word it recorded, DSPARK_DEVERR_TIMEOUT when the wait gave up.  The device
  * stays usable.  Synchronises that stream; INVALID_ARG for another `which`. */
@@ -290,6 +291,28 @@ dspark_status dspark_linear_stream_noalloc(const void* A_dev, int64_t lda, const
  * DSPARK_ERR_DEVICE (DSPARK_OK when it was 0).  Allocates nothing. */
 dspark_status dspark_noalloc_check(int32_t* word_host);
 const char* dspark_noalloc_last_error(void);
+
+/* Choose between forms of the same computation, per handle (the library picks
+ * by shape when a choice is 0, its default).  The forms compute the same
+ * function up to floating-point rounding order; the choice exists so that each
+ * form can be exercised and measured.  Captured draft graphs are dropped.
+ *   DSPARK_PATH_LAYERS      batch-1 draft layers: 0 auto, 1 one kernel per
+ *                           projection, 2 every layer in one launch on warp
+ *                           MMAs, 3 the whole step up to the logits in one
+ *                           launch on tcgen05 (block build, layers, out_proj)
+ *   DSPARK_PATH_MARKOV      Markov chain of 1-2 sequences: 0 FMA-pipe chain,
+ *                           1 the warp-MMA chain
+ *   DSPARK_PATH_NORM_CHAIN  batch-1 per-kernel layers: 0 RMSNorm through the
+ *                           residual epilogues, 1 separate normalisation launches
+ *   DSPARK_PATH_GRAPHS      draft steps: 0 captured and replayed as CUDA graphs,
+ *                           1 launched directly
+ * DSPARK_ERR_INVALID_ARG for an unknown choice or value.  A forced form that
+ * does not apply to the drafter or batch falls back to the default. */
+#define DSPARK_PATH_LAYERS 0
+#define DSPARK_PATH_MARKOV 1
+#define DSPARK_PATH_NORM_CHAIN 2
+#define DSPARK_PATH_GRAPHS 3
+dspark_status dspark_set_path(dspark_handle* h, int32_t what, int32_t value);
 
 /* Number of kernel launches issued by this handle since creation (all calls). */
 int64_t dspark_launch_count(const dspark_handle* h);

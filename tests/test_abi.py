@@ -91,5 +91,12 @@ def test_variant_and_sampling_arguments_without_gpu(lib):
     assert b"weights are NULL" in lib.dspark_last_error(None)
     assert not h.value
     assert lib.dspark_set_sampling(None, ctypes.c_float(1.0), 0, 0, None) == bdm.ERR_INVALID_ARG
-    for which in (-1, 5, 100):
+    for which in (-1, 6, 100):
         assert lib.dspark_selftest_wait(which, None) == bdm.ERR_INVALID_ARG
+
+
+def test_set_path_rejects_bad_choices_without_gpu(lib):
+    """dspark_set_path checks the handle before anything else."""
+    import block_draft_model_gb300 as bdm
+    assert lib.dspark_set_path(None, bdm.PATH_LAYERS, 0) == bdm.ERR_INVALID_ARG
+    assert b"NULL" in lib.dspark_last_error(None)

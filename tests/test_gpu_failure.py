@@ -27,8 +27,8 @@ def _gpu():
 
 # 0: the single-sequence Markov chain's arrival count, 1: the resident chain's barrier,
 # 2: the cooperative chain's barrier, 3: the one-launch layers' grid barrier,
-# 4: the tensor-core kernels' mbarrier wait
-@pytest.mark.parametrize("which", range(5))
+# 4: the tensor-core kernels' mbarrier wait, 5: the one-launch step's grid barrier
+@pytest.mark.parametrize("which", range(6))
 def test_bounded_wait_gives_up_and_reports(which):
     import block_draft_model_gb300 as bdm
     word = bdm.selftest_wait(which)
@@ -38,7 +38,7 @@ def test_bounded_wait_gives_up_and_reports(which):
 def test_selftest_rejects_unknown_wait():
     import block_draft_model_gb300 as bdm
     with pytest.raises(bdm.DsparkError):
-        bdm.selftest_wait(5)
+        bdm.selftest_wait(6)
 
 
 def test_device_usable_after_the_timeouts():

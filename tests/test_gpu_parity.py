@@ -40,12 +40,16 @@ def _draft(gdr, cfg, anchor, want_logits=True):
     return tok.cpu().numpy(), conf.cpu().numpy(), (lg.cpu().numpy() if want_logits else None)
 
 
-def _small(cfg, L, seed, chunks, anchors, norm_std=0.1, max_ctx=None):
+def _small(cfg, L, seed, chunks, anchors, norm_std=0.1, max_ctx=None, paths=()):
+    """Ingest L rows in `chunks`, compare every cache row, then draft each anchor and compare.
+    paths: (what, value) pairs given to set_path first (which form of the computation runs)."""
     W = syn.make_weights(cfg, seed=seed, norm_std=norm_std)
     X = syn.make_feats(cfg, L, seed=seed)
     dr = oracle.Drafter(cfg, W)
     dr.ingest(X)
     gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=max_ctx or L + 8)
+    for what, value in paths:
+        gdr.set_path(what, value)
     Xd = to_torch(X)
     lo = 0
     for hi in chunks + [L]:
@@ -53,7 +57,8 @@ def _small(cfg, L, seed, chunks, anchors, norm_std=0.1, max_ctx=None):
         lo = hi
     assert gdr.context_length() == L
     rel = rel_tol(cfg)
-    check_cache(dr, gdr, cfg, 0, np.arange(L), rel, label="cache")
+    if L:
+        check_cache(dr, gdr, cfg, 0, np.arange(L), rel, label="cache")
     for a in anchors:
         tok, conf, lg = _draft(gdr, cfg, a)
         check_block(dr, 0, a, tok, conf, lg, rel=rel, label=f"anchor {a}")
@@ -207,12 +212,14 @@ def test_batched_many_sequences_ragged_vocab():
 
 @pytest.mark.parametrize("n_heads,gamma,L", [(4, 5, 300), (8, 12, 50), (4, 8, 1500)])
 def test_persistent_draft_layers(n_heads, gamma, L):
-    """Shapes the one-launch draft layers take (d and F multiples of 512, head
-    dim 64 or 128): one or two 8-row block tiles, one key range (no merge) and
-    many key ranges (merged), three draws in a row on the same handle."""
+    """Every draft layer in one launch on warp MMAs (d and F multiples of 512,
+    head dim 64 or 128): one or two 8-row block tiles, one key range (no merge)
+    and many key ranges (merged), three draws in a row on the same handle."""
+    import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=512, n_heads=n_heads, n_layers=2, ff_mult=2, gamma=gamma,
                             vocab=1000, markov_rank=32)
-    dr, gdr, _ = _small(cfg, L, seed=15, chunks=[L // 2], anchors=[1, 998, 500], max_ctx=L + 16)
+    dr, gdr, _ = _small(cfg, L, seed=15, chunks=[L // 2], anchors=[1, 998, 500], max_ctx=L + 16,
+                        paths=[(bdm.PATH_LAYERS, bdm.LAYERS_PERSISTENT_MMA)])
     X = syn.make_feats(cfg, 3, seed=16)
     dr.ingest(X)
     gdr.ingest_context(to_torch(X))
@@ -220,36 +227,73 @@ def test_persistent_draft_layers(n_heads, gamma, L):
     check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
 
 
+# d, heads, gamma, L, vocab, hidden, layers
+STEP_SHAPES = [
+    (256, 2, 8, 300, 1000, 256, 2),     # head_dim 128, one key range per head over 2 x 76 CTAs
+    (128, 2, 16, 97, 777, 192, 2),      # head_dim 64, all 16 block rows (both TMEM column groups), H % 64 != 0
+    (384, 3, 5, 1500, 2053, 320, 3),    # three heads of 128, many key ranges merged, ragged vocabulary tile
+    (512, 8, 1, 40, 4096, 256, 1),      # gamma 1 (no mask rows), eight heads of 64
+    (256, 4, 7, 0, 1100, 256, 2),       # empty context: the block attends to itself only
+]
+
+
+@pytest.mark.parametrize("d,n_heads,gamma,L,vocab,hidden,n_layers", STEP_SHAPES)
+def test_one_launch_step_tc(d, n_heads, gamma, L, vocab, hidden, n_layers):
+    """The whole batch-1 step up to the logits in one launch with tcgen05 projections:
+    K blocks split over the CTAs with tiles shared by several CTAs (partials reduced by the
+    last one), key ranges of one head merged by the last range, ragged weight tiles,
+    three draws in a row on the same handle, then more context and another draw."""
+    import block_draft_model_gb300 as bdm
+    cfg = syn.DrafterConfig(hidden=hidden, n_taps=2, d_draft=d, n_heads=n_heads, n_layers=n_layers, ff_mult=2,
+                            gamma=gamma, vocab=vocab, markov_rank=32)
+    dr, gdr, _ = _small(cfg, L, seed=31, chunks=[L // 2] if L else [], anchors=[1, vocab - 1, vocab // 3],
+                        max_ctx=L + 16, norm_std=0.3, paths=[(bdm.PATH_LAYERS, bdm.LAYERS_STEP_TC)])
+    X = syn.make_feats(cfg, 3, seed=32)
+    dr.ingest(X)
+    gdr.ingest_context(to_torch(X))
+    tok, conf, lg = _draft(gdr, cfg, 77)
+    check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
+    assert gdr.check() == 0
+
+
+@pytest.mark.parametrize("layers", ["per_kernel", "step_tc"])
+def test_layer_forms_agree_without_graphs(layers):
+    """The per-kernel and the one-launch forms, launched directly (no CUDA graph) with the
+    anchor passed by value."""
+    import block_draft_model_gb300 as bdm
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=6,
+                            vocab=900, markov_rank=32)
+    form = bdm.LAYERS_PER_KERNEL if layers == "per_kernel" else bdm.LAYERS_STEP_TC
+    _small(cfg, 130, seed=33, chunks=[60], anchors=[3, 899, 450], norm_std=0.3,
+           paths=[(bdm.PATH_GRAPHS, 1), (bdm.PATH_LAYERS, form)])
+
+
 @pytest.mark.parametrize("gamma", [4, 16])
-def test_normalisation_folded_into_weight_streaming(monkeypatch, gamma):
-    """The opt-in mode where the weight-streaming projections (QKV, gate/up,
-    vocabulary) normalise their own input rows: each CTA rebuilds RMSNorm(x)
-    in shared memory and scales its accumulators by the rows' inverse RMS.
-    The one-launch layers are switched off so that every projection takes it;
-    d 768 gives 12 K-blocks, the vocabulary a ragged last weight tile."""
-    monkeypatch.setenv("DSPARK_NORM_FUSION", "1")
-    monkeypatch.setenv("DSPARK_NO_PERSISTENT", "1")
-    monkeypatch.setenv("DSPARK_NO_NORM_CHAIN", "1")
+def test_separate_normalisation_launches(gamma):
+    """Batch-1 layers one kernel per projection with a normalisation launch before each
+    normalised projection; d 768 gives 12 K-blocks, the vocabulary a ragged last weight tile."""
+    import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=768, n_heads=6, n_layers=2, ff_mult=2, gamma=gamma,
                             vocab=1100, markov_rank=32)
-    _small(cfg, 200, seed=17, chunks=[90], anchors=[5, 1099], norm_std=0.3)
+    _small(cfg, 200, seed=17, chunks=[90], anchors=[5, 1099], norm_std=0.3,
+           paths=[(bdm.PATH_LAYERS, bdm.LAYERS_PER_KERNEL), (bdm.PATH_NORM_CHAIN, 1)])
 
 
 @pytest.mark.parametrize("d,n_heads,gamma,L,vocab", [(512, 4, 8, 300, 1000), (64, 1, 16, 100, 777),
                                                      (768, 6, 5, 257, 1100)])
-def test_norm_chain_through_residual_epilogues(monkeypatch, d, n_heads, gamma, L, vocab):
+def test_norm_chain_through_residual_epilogues(d, n_heads, gamma, L, vocab):
     """Batch-1 layers without normalisation launches: the W_o and W_down
     epilogues write x, the next projection's operand bf16(x * g) and the
     8-column sums of x^2; QKV, gate/up and the vocabulary projection scale
     their accumulators by 1 / rms from those sums.  d 512 and 768 reduce
     split-K through clusters; d 64 runs W_o unsplit (the per-column epilogue);
-    gamma 16 fills all 16 operand rows.  The one-launch layers are off so the
-    small shapes take the per-kernel path."""
-    monkeypatch.setenv("DSPARK_NO_PERSISTENT", "1")
+    gamma 16 fills all 16 operand rows.  The per-kernel form is forced so the
+    small shapes take it."""
+    import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=d, n_heads=n_heads, n_layers=3, ff_mult=2, gamma=gamma,
                             vocab=vocab, markov_rank=32)
     dr, gdr, _ = _small(cfg, L, seed=18, chunks=[L // 3], anchors=[2, vocab - 1, vocab // 2], norm_std=0.3,
-                        max_ctx=L + 8)
+                        max_ctx=L + 8, paths=[(bdm.PATH_LAYERS, bdm.LAYERS_PER_KERNEL)])
     X = syn.make_feats(cfg, 2, seed=19)
     dr.ingest(X)
     gdr.ingest_context(to_torch(X))
@@ -270,7 +314,7 @@ def test_ingest_projection_split_over_k():
     (3, 64, 1000, "mma"), (1, 128, 5003, "mma"), (7, 256, 2048, "mma"),
     (3, 64, 1000, "fma"), (2, 128, 5003, "fma"), (1, 256, 73448, "fma"), (2, 256, 100003, "fma"),
 ])
-def test_markov_chain_few_sequences(monkeypatch, n_seq, rank, vocab, form):
+def test_markov_chain_few_sequences(n_seq, rank, vocab, form):
     """1 to 7 sequences with r in {64, 128, 256}: the whole Markov chain in one
     cooperative launch with the vocabulary slices resident on the SMs; the dot
     products on the tensor cores ("mma") or, for one or two sequences, on the
@@ -278,14 +322,15 @@ def test_markov_chain_few_sequences(monkeypatch, n_seq, rank, vocab, form):
     Vocabularies that leave ragged slices, CTAs without rows (V 1000), rows
     past the resident ones (V 73448) and several 512-row passes (V 100003);
     three sequences then one on the same handle switch between the forms."""
-    if form == "mma":
-        monkeypatch.setenv("DSPARK_MARKOV_MMA", "1")
+    import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=6,
                             vocab=vocab, markov_rank=rank)
     W = syn.make_weights(cfg, seed=13, norm_std=0.1)
     lens = [17 + 5 * i for i in range(n_seq)]
     feats = [syn.make_feats(cfg, L, seed=13, seq=i) for i, L in enumerate(lens)]
     gb = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=64, max_seqs=n_seq)
+    if form == "mma":
+        gb.set_path(bdm.PATH_MARKOV, 1)
     ids = torch.arange(n_seq, dtype=torch.int32, device="cuda")
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
     gb.ingest_context_batched(ids, cu, to_torch(np.concatenate(feats, axis=0)))
@@ -360,22 +405,33 @@ def test_host_checked_errors():
 def test_minicpm_shaped_full_size():
     """MiniCPM-shaped drafter (H 2048, m 5, d 2048, 16 heads, 5 layers, gamma 8,
     V 73448, r 256), 1024 context rows, then draft; every cache row of sampled
-    rows and every logit of two blocks are compared."""
+    rows and every logit of two blocks are compared, for the default one-launch
+    step and for the per-kernel form on a second handle."""
+    import block_draft_model_gb300 as bdm
     wl = syn.WORKLOADS["minicpm_L1024"]
     cfg = wl.cfg
     W = syn.make_weights(cfg, seed=0)
     X = syn.make_feats(cfg, wl.ctx_len, seed=0)
-    gdr = make_gpu_drafter(cfg, weights_to_device(W), max_ctx=wl.ctx_len + 64)
-    gdr.ingest_context(to_torch(X))
+    Wd = weights_to_device(W)
     anchors = syn.anchors(wl)[:, 0]
-    outs = [_draft(gdr, cfg, int(a)) for a in (anchors[0], 12345)]
-    assert gdr.check() == 0
+    outs = {}
+    for form in (bdm.LAYERS_STEP_TC, bdm.LAYERS_PER_KERNEL):
+        gdr = make_gpu_drafter(cfg, Wd, max_ctx=wl.ctx_len + 64)
+        gdr.set_path(bdm.PATH_LAYERS, form)
+        gdr.ingest_context(to_torch(X))
+        outs[form] = [_draft(gdr, cfg, int(a)) for a in (anchors[0], 12345)]
+        assert gdr.check() == 0
+        if form == bdm.LAYERS_STEP_TC:
+            keep = gdr
+        else:
+            gdr.close()
     dr = oracle.Drafter(cfg, W)
     dr.ingest(X)
     rows = np.unique(np.concatenate([[0, 1, 511, 1023], syn.uniform_int(9, 9, (28,), 0, 1023)]))
-    check_cache(dr, gdr, cfg, 0, rows, label="minicpm cache")
-    for a, (tok, conf, lg) in zip((anchors[0], 12345), outs):
-        check_block(dr, 0, int(a), tok, conf, lg, label=f"minicpm anchor {a}")
+    check_cache(dr, keep, cfg, 0, rows, label="minicpm cache")
+    for form, blocks in outs.items():
+        for a, (tok, conf, lg) in zip((anchors[0], 12345), blocks):
+            check_block(dr, 0, int(a), tok, conf, lg, label=f"minicpm form {form} anchor {a}")
 
 
 @pytest.fixture(scope="module")
