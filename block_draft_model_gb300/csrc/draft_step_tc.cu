@@ -8,28 +8,36 @@
 //
 // Phases, separated by bounded grid barriers (one cooperative CTA per SM):
 //   TOK   x = E[a] tok_proj^T (row 0 only) + block rows
-//   per layer:  QKV (Q rows to q, block K/V rows into the cache after the context)
-//               ATT (attention items (head, key range), merged by the last range of a head)
-//               WO  (x += O W_o^T)   GU (h = act(gate) * up)   DOWN (x += h W_down^T)
+//   per layer:  QKV  [q | k | v] = RMSNorm(x) * attn_norm . W_qkv^T
+//               ATT  attention items (head, key range): partial (max, sum, output) per range,
+//                    then the head's ranges merge them into O
+//               WO   x += O W_o^T
+//               GU   [gate | up] = RMSNorm(x) * ff_norm . W_gu^T
+//               DOWN x += (act(gate) * up) W_down^T
 //   OUT   U = RMSNorm(x) * out_norm . out_proj^T (and y)
 //
 // Every projection phase is a weight stream with at most 16 activation rows:
 // the weights are the MMA's M side (128-row tiles, 64-wide K blocks of 16 KB
-// moved by TMA with the 128-byte swizzle) and the block rows its N = 16 side,
-// one tcgen05.mma of 128 x 16 x 16 per 16-wide K slice, fp32 accumulators in
-// TMEM (16 columns each).  A phase's K blocks, taken tile by tile, are cut
-// into one contiguous range per CTA, so every CTA streams the same number of
-// bytes; a tile shared by several CTAs is reduced by the last of them to
-// finish (partials in global memory, a ticket per tile, sums in CTA order,
-// so the result does not depend on timing).
+// moved by TMA with the 128-byte swizzle) and the block rows its N = 16 side.
+// A phase's K blocks, taken tile by tile, are cut into one contiguous range
+// per CTA, so every CTA streams the same number of bytes.  The four 16-wide
+// K slices of a K block go to four accumulators (16 TMEM columns each), so
+// consecutive MMAs do not wait for one another; the epilogue adds them.
+// RMSNorm is split: the operand is bf16(x * g) and each accumulator row is
+// scaled by 1 / sqrt(mean(x^2) + eps) of its block row, computed while the
+// MMAs run.  Every phase adds its partial products into fp32 buffers with
+// fire-and-forget atomic adds (x itself for the block build, W_o and W_down;
+// U for out_proj), so a tile shared by several CTAs needs no second pass;
+// the buffers are zeroed (x set to the block rows) in earlier phases.  The
+// key ranges of one attention head merge their partials cooperatively once
+// all of them have arrived (a per-head count), so the W_o operand is a copy.
 //
 // Roles: warp 0 (one lane) streams every weight K block of every phase into a
 // ring of shared-memory stages in the order the CTA consumes them and never
 // waits for a grid barrier, so the next phases' weights arrive while the CTA
 // waits for the others.  Warp 1 owns TMEM and one lane issues the MMAs.
-// Warps 2-9 build each phase's MMA operand (the normalised rows, RMSNorm
-// applied before rounding to bf16), read the accumulators back, run the
-// epilogues and the attention, and take part in the grid barriers.
+// Warps 2-9 build the operands, read the accumulators back, run the epilogues
+// and the attention, and take part in the grid barriers.
 //
 // Every wait is bounded (about one second); a timeout sets DSPARK_DEVERR_TIMEOUT
 // in the error word, every role stops, in-flight copies and MMAs are waited
@@ -57,8 +65,10 @@ constexpr int TM = 128;                   // weight rows per tile (MMA M)
 constexpr int KB = 64;                    // K elements per ring stage
 constexpr int STAGE_BYTES = TM * KB * 2;  // 16 KB
 constexpr int BSLOT_BYTES = 16 * KB * 2;  // one K block of the 16-row operand: 2 KB
-constexpr int NACC = 16;                  // TMEM accumulators of 16 fp32 columns
-constexpr int TMEM_COLS = NACC * 16;
+constexpr int CH = 4;                     // independent accumulator chains per tile (the K slices of a K block)
+constexpr int UCOLS = CH * 16;            // TMEM columns of one tile's accumulators
+constexpr int NACC = 8;                   // tiles whose accumulators are in TMEM at once
+constexpr int TMEM_COLS = NACC * UCOLS;   // 512: the whole TMEM of the SM
 constexpr int TKA = 64;                   // attention keys per tile
 constexpr int MAXL = 16;                  // layers
 constexpr int GMAX = 16;                  // block rows
@@ -67,16 +77,13 @@ enum Kind { K_TOK = 0, K_QKV = 1, K_WO = 2, K_GU = 3, K_DOWN = 4, K_OUT = 5 };
 
 struct StepParams {
     float* x;          // [gamma, d] residual stream
-    float* q;          // [gamma, d] queries
-    bf16* act;         // [gamma, d] attention output
-    bf16* hact;        // [gamma, F] act(gate) * up
+    float* qkv;        // [gamma, 3d] QKV products (added into; zero before the phase)
+    float* gu;         // [gamma, 2F] gate/up products, rows (gate f, up f) interleaved (idem)
     float* y;          // [gamma, d] out-normed rows
     float* U;          // [gamma, V] logits before the Markov bias
-    float* ssq;        // [d / 128][16] per column tile: sums of x^2 of each block row
-    float* part;       // projection partials [(tiles + G)][gamma][128]
-    float* apart;      // attention partials [nh][nchunks][gamma][hd + 4]
-    unsigned int* tickets;   // [max tiles] zero between phases
-    unsigned int* atickets;  // [nh] zero between layers
+    bf16* act;         // [gamma, d] attention output O
+    float* apart;      // attention partials [nh][nchunks][gamma][hd + 4]: max, sum, -, -, output
+    unsigned int* hcnt;      // [2][nh] arrivals of a head's key ranges, counting up through the launch
     bf16* cache;       // layer 0, slot 0: K rows at + pos * d, V rows at + kv_off + pos * d
     int64_t layer_stride, kv_off;
     int max_rows;
@@ -216,6 +223,22 @@ __device__ __forceinline__ int owner(const Shape& sh, int G, int j) {
     return (int)(((int64_t)(j + 1) * g + T - 1) / T - 1);
 }
 
+// Bounded mbarrier wait for a thread that may wait long (the epilogue warps): backs off with
+// short sleeps so that it does not compete with the MMA thread for the barrier unit.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > TIMEOUT_NS) {
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- grid barrier
 // Arrival counter counting up through the launch: barrier n opens at n * G.  Returns true
 // (on every consumer thread alike) when the CTA has to stop.
@@ -243,155 +266,184 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned l
 // ---------------------------------------------------------------- operand staging
 // The phase's operand for the CTA's K blocks: slot i holds K block (kb_first + i) mod nkb
 // as [16 rows][64] bf16, row n at n * 128 bytes, 16-byte chunk c at (c ^ (n & 7)) * 16 (the
-// layout a 128-byte-swizzled TMA copy gives).  Rows past the block rows are zero.
+// layout a 128-byte-swizzled TMA copy gives).  Only the block rows are written: a row n past
+// them feeds accumulator column n alone, which no epilogue reads (the block build uses row 0).
+//   TOK: the anchor's embedding row;  QKV / GU / OUT: x * g (the row scale comes later);
+//   WO: the attention output O;  DOWN: act(gate) * up.
+// Every thread takes an equal share of the (slot, row, chunk) items and issues all of its
+// loads before any of the arithmetic, so the staging costs one round trip to L2.
+__device__ __forceinline__ void st_chunk(uint8_t* ub, int slot, int n, int ch, const float* f) {
+    *reinterpret_cast<uint4*>(ub + slot * BSLOT_BYTES + n * 128 + ((ch ^ (n & 7)) * 16)) =
+        make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
 __device__ __forceinline__ void stage_operand(const StepParams& p, const Shape& sh, int kb_first, int nslots,
-                                              uint8_t* ub, const float* rs, int anchor) {
+                                              uint8_t* ub, int anchor) {
     const int t = threadIdx.x - 64;
     const int K = sh.K, gamma = p.gamma;
-    const float* g = sh.kind == K_QKV ? p.attn_norm[sh.layer] : (sh.kind == K_GU ? p.ff_norm[sh.layer] : p.out_norm);
-    constexpr int BATCH = 4;  // chunks per thread whose loads are in flight together
-    const int total = nslots * 128;
-    for (int i0 = t; i0 < total; i0 += BATCH * NCT) {
-        uint4 v[BATCH];
+    const int rows = sh.kind == K_TOK ? 1 : gamma;
+    const int total = nslots * rows * 8;
+    // item i: slot i / (rows * 8), row (i / 8) % rows, chunk i % 8
+    auto decode = [&](int i, int& slot, int& n, int& ch, int& k0) {
+        slot = i / (rows * 8);
+        const int rem = i - slot * rows * 8;
+        n = rem >> 3;
+        ch = rem & 7;
+        k0 = ((kb_first + slot) % sh.nkb) * KB + ch * 8;
+    };
+    {
+        constexpr int BATCH = 4;  // items per thread whose loads are in flight together
+        const float* g =
+            sh.kind == K_QKV ? p.attn_norm[sh.layer] : (sh.kind == K_GU ? p.ff_norm[sh.layer] : p.out_norm);
+        for (int i0 = t; i0 < total; i0 += BATCH * NCT) {
+            float4 a[BATCH][4];
+            // loads
 #pragma unroll
-        for (int b = 0; b < BATCH; ++b) {
-            const int i = i0 + b * NCT;
-            const int slot = i >> 7, n = (i >> 3) & 15, ch = i & 7;
-            const int k0 = ((kb_first + slot) % sh.nkb) * KB + ch * 8;
-            v[b] = make_uint4(0, 0, 0, 0);
-            if (i < total && k0 < K) {
+            for (int b = 0; b < BATCH; ++b) {
+                const int i = i0 + b * NCT;
+                int slot, n, ch, k0;
+                decode(i, slot, n, ch, k0);
+                const bool ok = i < total && k0 < K;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[b][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!ok) continue;
                 if (sh.kind == K_TOK) {
-                    if (n == 0) v[b] = __ldg(reinterpret_cast<const uint4*>(p.embed + (int64_t)anchor * p.H + k0));
-                } else if (n < gamma) {
-                    if (sh.kind == K_WO) {
-                        v[b] = __ldcg(reinterpret_cast<const uint4*>(p.act + (int64_t)n * p.d + k0));
-                    } else if (sh.kind == K_DOWN) {
-                        v[b] = __ldcg(reinterpret_cast<const uint4*>(p.hact + (int64_t)n * p.F + k0));
-                    } else {
-                        const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)n * p.d + k0);
-                        const float4* gr = reinterpret_cast<const float4*>(g + k0);
-                        const float4 x0 = __ldcg(xr), x1 = __ldcg(xr + 1), g0 = __ldg(gr), g1 = __ldg(gr + 1);
-                        const float r = rs[n];
-                        v[b] = make_uint4(pack2(x0.x * r * g0.x, x0.y * r * g0.y),
-                                          pack2(x0.z * r * g0.z, x0.w * r * g0.w),
-                                          pack2(x1.x * r * g1.x, x1.y * r * g1.y),
-                                          pack2(x1.z * r * g1.z, x1.w * r * g1.w));
-                    }
+                    a[b][0] = __ldg(reinterpret_cast<const float4*>(p.embed + (int64_t)anchor * p.H + k0));
+                } else if (sh.kind == K_WO) {
+                    a[b][0] = __ldcg(reinterpret_cast<const float4*>(p.act + (int64_t)n * p.d + k0));
+                } else if (sh.kind == K_DOWN) {
+                    // columns k0 .. k0 + 7 of act(gate) * up are the (gate, up) pairs 2 k0 .. 2 k0 + 15 of gu
+                    const float4* gr = reinterpret_cast<const float4*>(p.gu + (int64_t)n * 2 * p.F + 2 * k0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) a[b][q] = __ldcg(gr + q);
+                } else {
+                    const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)n * p.d + k0);
+                    const float4* gr = reinterpret_cast<const float4*>(g + k0);
+                    a[b][0] = __ldcg(xr);
+                    a[b][1] = __ldcg(xr + 1);
+                    a[b][2] = __ldg(gr);
+                    a[b][3] = __ldg(gr + 1);
                 }
             }
-        }
+            // arithmetic and stores
 #pragma unroll
-        for (int b = 0; b < BATCH; ++b) {
-            const int i = i0 + b * NCT;
-            if (i < total) {
-                const int slot = i >> 7, n = (i >> 3) & 15, ch = i & 7;
-                *reinterpret_cast<uint4*>(ub + slot * BSLOT_BYTES + n * 128 + ((ch ^ (n & 7)) * 16)) = v[b];
+            for (int b = 0; b < BATCH; ++b) {
+                const int i = i0 + b * NCT;
+                if (i >= total) continue;
+                int slot, n, ch, k0;
+                decode(i, slot, n, ch, k0);
+                if (sh.kind == K_TOK || sh.kind == K_WO) {
+                    // bf16 already (the embedding row; the attention output): the chunk as is
+                    *reinterpret_cast<float4*>(ub + slot * BSLOT_BYTES + n * 128 + ((ch ^ (n & 7)) * 16)) = a[b][0];
+                    continue;
+                }
+                float f[8];
+                if (sh.kind == K_DOWN) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        f[2 * q] = act_fn(p.act_kind, a[b][q].x) * a[b][q].y;
+                        f[2 * q + 1] = act_fn(p.act_kind, a[b][q].z) * a[b][q].w;
+                    }
+                } else {
+                    f[0] = a[b][0].x * a[b][2].x;
+                    f[1] = a[b][0].y * a[b][2].y;
+                    f[2] = a[b][0].z * a[b][2].z;
+                    f[3] = a[b][0].w * a[b][2].w;
+                    f[4] = a[b][1].x * a[b][3].x;
+                    f[5] = a[b][1].y * a[b][3].y;
+                    f[6] = a[b][1].z * a[b][3].z;
+                    f[7] = a[b][1].w * a[b][3].w;
+                }
+                st_chunk(ub, slot, n, ch, f);
             }
         }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
 }
 
+// rs[j] = 1 / sqrt(mean(x[j]^2) + eps) over the whole row, a warp per block row.
+__device__ __forceinline__ void row_scales(const StepParams& p, float* rs) {
+    const int w = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31;
+    for (int j = w; j < p.gamma; j += NCW) {
+        const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)j * p.d);
+        float a = 0.f;
+        for (int k4 = lane; k4 < p.d / 4; k4 += 32) {
+            const float4 v = __ldcg(xr + k4);
+            a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        a = warp_sum(a);
+        if (lane == 0) rs[j] = rsqrtf(a / (float)p.d + p.eps);
+    }
+}
+
+// Zero a CTA's share of a buffer of n floats (16-byte aligned): float4 shares, and the last
+// CTA also takes the n % 4 trailing floats.
+__device__ __forceinline__ void zero_share(float* buf, int64_t n, int c, int G) {
+    const int64_t n4 = n / 4;
+    const int64_t a = n4 * c / G, b = n4 * (c + 1) / G;
+    float4* b4 = reinterpret_cast<float4*>(buf);
+    for (int64_t i = a + (threadIdx.x - 64); i < b; i += NCT) b4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c == G - 1 && threadIdx.x - 64 < (int)(n - 4 * n4)) buf[4 * n4 + (threadIdx.x - 64)] = 0.f;
+}
+
 // ---------------------------------------------------------------- epilogues
-// Thread (row r of the tile, column group cg) holds v[i] = acc[r][cg * 8 + i].
-// x += v (or, for the block build, x = v + block rows) and the tile's sums of x^2 per block row.
-__device__ __forceinline__ void fin_residual(const StepParams& p, int kind, int t, int r, int cg, const float* v,
-                                             float* red) {
-    const int n = t * TM + r, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float s2[8];
+// Thread (row r of the tile, column group cg) holds v[i] = acc[r][cg * 8 + i], scaled.  Every
+// phase adds into its output; nothing else touches those entries during the phase.
+__device__ __forceinline__ void epi_add(const StepParams& p, const Shape& sh, int t, int r, int cg, const float* v) {
+    const int n = t * TM + r;
+    if (n >= sh.N) return;
+    float* dst;
+    int64_t ld;
+    int rows = p.gamma;
+    if (sh.kind == K_QKV) {
+        dst = p.qkv;
+        ld = 3 * (int64_t)p.d;
+    } else if (sh.kind == K_GU) {
+        dst = p.gu;
+        ld = 2 * (int64_t)p.F;
+    } else if (sh.kind == K_OUT) {
+        dst = p.U;
+        ld = p.V;
+    } else {
+        dst = p.x;
+        ld = p.d;
+        if (sh.kind == K_TOK) rows = 1;  // only operand row 0 (the anchor) is staged
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int j = cg * 8 + i;
-        s2[i] = 0.f;
-        if (j < p.gamma) {
-            float* xp = p.x + (int64_t)j * p.d + n;
-            const float base = kind == K_TOK ? __ldg(p.block_const + (int64_t)j * p.d + n) : __ldcg(xp);
-            const float xv = base + v[i];
-            *xp = xv;
-            s2[i] = xv * xv;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s2[i] = warp_sum(s2[i]);
-    // red[warp - 2][8]: the warp's 32 rows; warps w and w + 4 share the column group
-    if (lane == 0)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) red[(warp - 2) * 8 + i] = s2[i];
-    cons_sync();
-    const int tt = threadIdx.x - 64;
-    if (tt < 16 && tt < p.gamma) {
-        const int g2 = tt >> 3, i = tt & 7;  // column group, entry: the four warps of that group in lane order
-        float a = 0.f;
-        for (int q4 = 0; q4 < 4; ++q4) {
-            // warps 2..9 -> index 0..7; group g2 holds indices 4 g2 .. 4 g2 + 3, their lane quarters 2, 3, 0, 1
-            a += red[(g2 * 4 + q4) * 8 + i];
-        }
-        p.ssq[t * 16 + tt] = a;
-    }
-    cons_sync();
-}
-
-__device__ __forceinline__ void finalize(const StepParams& p, const Shape& sh, int t, int r, int cg, float* v,
-                                         float* red, int L) {
-    const int n = t * TM + r, lane = threadIdx.x & 31;
-    const int gamma = p.gamma, d = p.d;
-    switch (sh.kind) {
-        case K_TOK:
-        case K_WO:
-        case K_DOWN:
-            fin_residual(p, sh.kind, t, r, cg, v, red);
-            break;
-        case K_QKV: {
-            bf16* cache = p.cache + (int64_t)sh.layer * p.layer_stride;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = cg * 8 + i;
-                if (j >= gamma) continue;
-                if (n < d) {
-                    p.q[(int64_t)j * d + n] = v[i];
-                } else if (L + j < p.max_rows) {
-                    const int64_t off = (int64_t)(L + j) * d + (n < 2 * d ? n - d : n - 2 * d);
-                    cache[(n < 2 * d ? 0 : p.kv_off) + off] = __float2bfloat16_rn(v[i]);
-                }
-            }
-            break;
-        }
-        case K_GU: {
-            // (gate f, up f) are rows 2f, 2f + 1: adjacent lanes
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float up = __shfl_down_sync(0xffffffffu, v[i], 1);
-                const int j = cg * 8 + i;
-                if (j < gamma && !(lane & 1) && n + 1 < sh.N)
-                    p.hact[(int64_t)j * p.F + (n >> 1)] = __float2bfloat16_rn(act_fn(p.act_kind, v[i]) * up);
-            }
-            break;
-        }
-        default: {  // K_OUT
-            if (n < p.V)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = cg * 8 + i;
-                    if (j < gamma) p.U[(int64_t)j * p.V + n] = v[i];
-                }
-            break;
-        }
+        if (j < rows) atomicAdd(dst + j * ld + n, v[i]);  // result unused: a fire-and-forget reduction
     }
 }
 
 // ---------------------------------------------------------------- attention
 // One (head, key range) item on warps 2-5: flash decoding over 64-key tiles of a two-stage
-// cp.async ring in `ab`; scores in the log2 domain.  The partial (m, l, o) goes to apart,
-// or, with a single range, the normalised output straight to act.
+// cp.async ring in `ab`; scores in the log2 domain; the range's partial (max, sum, output)
+// goes to apart.  The range that holds the block's own keys (rows L .. L + gamma - 1) first
+// writes the head's block K/V rows into the cache, in the cache's bf16 format.
 template <int HD>
-__device__ void attn_item(const StepParams& p, int layer, int h, int start, int end, int n_real, int rg,
-                          uint8_t* ab) {
+__device__ void attn_item(const StepParams& p, int layer, int h, int start, int end, int L, int rg, uint8_t* ab) {
     constexpr int RB = HD * 2 + 16, TILE = TKA * RB, STAGE = 2 * TILE, KS = HD / 16;
     const int tid = threadIdx.x - 64, warp = tid >> 5, lane = tid & 31;
     const int gamma = p.gamma, d = p.d;
-    const bf16* Kb = p.cache + (int64_t)layer * p.layer_stride + h * HD;
+    bf16* Kw = p.cache + (int64_t)layer * p.layer_stride + h * HD;
+    const bf16* Kb = Kw;
     const bf16* Vb = Kb + p.kv_off;
     const uint32_t ring = smem_u32(ab);
+    if (end > L) {
+        for (int i = tid; i < gamma * HD / 4; i += 128) {
+            const int j = i / (HD / 4), e = (i - j * (HD / 4)) * 4;
+            if (L + j >= p.max_rows) continue;
+            const float* src = p.qkv + (int64_t)j * 3 * d + h * HD + e;
+            const float4 kv = __ldcg(reinterpret_cast<const float4*>(src + d));
+            const float4 vv = __ldcg(reinterpret_cast<const float4*>(src + 2 * d));
+            bf16* kd = Kw + (int64_t)(L + j) * d + e;
+            *reinterpret_cast<uint2*>(kd) = make_uint2(pack2(kv.x, kv.y), pack2(kv.z, kv.w));
+            *reinterpret_cast<uint2*>(kd + p.kv_off) = make_uint2(pack2(vv.x, vv.y), pack2(vv.z, vv.w));
+        }
+        __threadfence();
+        attn_sync();  // the rows are in global memory before any copy of this CTA reads them
+    }
     const int n_tiles = (end - start + TKA - 1) / TKA;
     auto load = [&](int st, int t0) {
         constexpr int VPR = HD * 2 / 16;
@@ -411,8 +463,8 @@ __device__ void attn_item(const StepParams& p, int layer, int h, int start, int 
     uint32_t qf[KS][4];
     {
         const float qs = rsqrtf((float)HD) * 1.4426950408889634f;
-        const float* q0 = p.q + (int64_t)g * d + h * HD;
-        const float* q1 = q0 + (int64_t)8 * d;
+        const float* q0 = p.qkv + (int64_t)g * 3 * d + h * HD;
+        const float* q1 = q0 + (int64_t)8 * 3 * d;
         const bool v0 = g < gamma, v1 = g + 8 < gamma;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -534,40 +586,75 @@ __device__ void attn_item(const StepParams& p, int layer, int h, int start, int 
             acc[2] += wt * ov.z;
             acc[3] += wt * ov.w;
         }
-        if (n_real == 1) {
-            const float inv = 1.f / l;
-            *reinterpret_cast<uint2*>(p.act + (int64_t)j * d + h * HD + e) =
-                make_uint2(pack2(acc[0] * inv, acc[1] * inv), pack2(acc[2] * inv, acc[3] * inv));
-        } else {
-            float* pr = p.apart + ((int64_t)(h * p.nchunks + rg) * gamma + j) * PW;
-            *reinterpret_cast<float4*>(pr + 4 + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            if (e == 0) *reinterpret_cast<float2*>(pr) = make_float2(M, l);
-        }
+        float* pr = p.apart + ((int64_t)(h * p.nchunks + rg) * gamma + j) * PW;
+        *reinterpret_cast<float4*>(pr + 4 + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        if (e == 0) *reinterpret_cast<float2*>(pr) = make_float2(M, l);
     }
 }
 
-// The last key range of head h to finish merges all n_real ranges' partials (in range order).
+// After every key range of head h has written its partial (the head's arrival count reached
+// `target`), range rg merges its share of the head's gamma x HD outputs:
+// O = sum_r exp2(m_r - M) o_r / sum_r exp2(m_r - M) l_r, M = max_r m_r, ranges in order.
 template <int HD>
-__device__ void attn_merge(const StepParams& p, int h, int n_real) {
+__device__ void attn_merge(const StepParams& p, unsigned int* cnt, unsigned int target, int h, int rg, int n_real,
+                           volatile int* abort_flag) {
     constexpr int PW = HD + 4;
     const int tid = threadIdx.x - 64;
-    const int gamma = p.gamma;
-    for (int i = tid; i < gamma * (HD / 4); i += 128) {
-        const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+    __threadfence();
+    attn_sync();
+    if (tid == 0) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+        const uint64_t t0 = globaltimer();
+        while (true) {
+            unsigned int cur;
+            asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(cnt) : "memory");
+            if (cur >= target || *abort_flag) break;
+            if (globaltimer() - t0 > TIMEOUT_NS) {
+                atomicOr(p.err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    attn_sync();
+    const int gamma = p.gamma, groups = gamma * (HD / 4);
+    const int g0 = (int)((int64_t)rg * groups / n_real), g1 = (int)((int64_t)(rg + 1) * groups / n_real);
+    for (int gi = g0 + tid; gi < g1; gi += 128) {
+        const int j = gi / (HD / 4), e = (gi - j * (HD / 4)) * 4;
         const float* base = p.apart + ((int64_t)h * p.nchunks * gamma + j) * PW;
         const int64_t cs = (int64_t)gamma * PW;
-        float M = -INFINITY;
-        for (int c = 0; c < n_real; ++c) M = fmaxf(M, __ldcg(base + c * cs));
-        float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        for (int c = 0; c < n_real; ++c) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + c * cs));
-            const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-            l += wt * ml.y;
-            const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + c * cs + 4 + e));
-            a0 = fmaf(wt, ov.x, a0);
-            a1 = fmaf(wt, ov.y, a1);
-            a2 = fmaf(wt, ov.z, a2);
-            a3 = fmaf(wt, ov.w, a3);
+        constexpr int RB = 16;  // ranges whose loads are in flight together
+        float M = -INFINITY, l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int r0 = 0; r0 < n_real; r0 += RB) {
+            float2 ml[RB];
+            float4 ov[RB];
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+                const int r = min(r0 + u, n_real - 1);
+                ml[u] = __ldcg(reinterpret_cast<const float2*>(base + r * cs));
+                ov[u] = __ldcg(reinterpret_cast<const float4*>(base + r * cs + 4 + e));
+            }
+            float Mn = M;
+#pragma unroll
+            for (int u = 0; u < RB; ++u)
+                if (r0 + u < n_real) Mn = fmaxf(Mn, ml[u].x);
+            const float sc = M == -INFINITY ? 0.f : ex2(M - Mn);
+            l *= sc;
+            a0 *= sc;
+            a1 *= sc;
+            a2 *= sc;
+            a3 *= sc;
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+                const float wt = (r0 + u < n_real && ml[u].x != -INFINITY) ? ex2(ml[u].x - Mn) : 0.f;
+                l = fmaf(wt, ml[u].y, l);
+                a0 = fmaf(wt, ov[u].x, a0);
+                a1 = fmaf(wt, ov[u].y, a1);
+                a2 = fmaf(wt, ov[u].z, a2);
+                a3 = fmaf(wt, ov[u].w, a3);
+            }
+            M = Mn;
         }
         const float inv = 1.f / l;
         *reinterpret_cast<uint2*>(p.act + (int64_t)j * p.d + h * HD + e) =
@@ -592,9 +679,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
     uint64_t* drain = b_taken + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* flag = abort_flag + 1;                  // ticket outcome, broadcast to the consumers
     float* rs = reinterpret_cast<float*>(tmem_slot + 4);   // [16] row scales
-    float* red = rs + 16;                                  // [8][8] row-sum partials
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, G = gridDim.x;
@@ -608,13 +693,12 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 1);
+            mbar_init(&acc_empty[a], NCW);  // every consumer warp has read the accumulators
         }
         mbar_init(b_full, 1);
         mbar_init(b_taken, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
-        *flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -625,16 +709,18 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
     }
     const unsigned int par = *(volatile unsigned int*)p.epoch & 1u;
     unsigned long long* bar = p.bar + par;
-    if (c == 0 && threadIdx.x == 0) p.bar[par ^ 1u] = 0ull;  // the next launch's counter
+    if (c == 0 && threadIdx.x == 0) p.bar[par ^ 1u] = 0ull;  // the next launch's counters
+    if (c == 0 && threadIdx.x < p.nh) p.hcnt[(par ^ 1u) * p.nh + threadIdx.x] = 0u;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- producer: every K block of every phase, in consumption order
+        // ---- producer: every K block of every phase, in consumption order (ring position
+        // st / phase bit ph and the K block coordinates advance incrementally)
         if (lane == 0) {
-            uint32_t idx = 0;
+            uint32_t st = 0, ph = 0, issued = 0;
             bool ok = true;
             for (int s = 0; s < nph && ok; ++s) {
                 const Shape sh = phase_shape(p, s);
@@ -642,66 +728,87 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
                 asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
                 int lo, hi;
                 my_range(sh, c, G, lo, hi);
-                for (int j = lo; j < hi; ++j, ++idx) {
-                    const int st = (int)(idx % (uint32_t)S);
-                    if (!mbar_wait(&empty[st], ((idx / (uint32_t)S) & 1u) ^ 1u, abort_flag)) {
+                int t = lo / sh.nkb, kb = lo - t * sh.nkb;
+                for (int j = lo; j < hi; ++j) {
+                    if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const int t = j / sh.nkb, kb = j - t * sh.nkb;
                     mbar_arrive_expect_tx(&full[st], STAGE_BYTES);  // rows / columns past the matrix arrive as zeros
                     tma_load_2d(smem_u32(ring + (size_t)st * STAGE_BYTES), map, &full[st], kb * KB, t * TM);
+                    ++issued;
+                    if (++kb == sh.nkb) {
+                        kb = 0;
+                        ++t;
+                    }
+                    if (++st == (uint32_t)S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
-            // no copy may still be in flight when the CTA exits (only possible after an abort)
+            // no copy may still be in flight when the CTA exits (only possible after an abort):
+            // the last min(S, issued) copies, newest first
             volatile int never = 0;
-            for (uint32_t i = idx > (uint32_t)S ? idx - (uint32_t)S : 0u; i < idx; ++i)
-                mbar_wait(&full[i % (uint32_t)S], (i / (uint32_t)S) & 1u, &never);
+            for (uint32_t i = 0; i < (uint32_t)S && i < issued; ++i) {
+                if (st == 0) {
+                    st = (uint32_t)S;
+                    ph ^= 1u;
+                }
+                --st;
+                mbar_wait(&full[st], ph, &never);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---- MMA issuer
+        // ---- MMA issuer: K slice k of every K block into accumulator chain k of the tile
         if (lane == 0) {
             const uint32_t id = idesc(TM, 16);
-            uint32_t idx = 0, u = 0, bph = 0;
+            const uint32_t ub_s = smem_u32(ub), ring_s = smem_u32(ring);
+            uint32_t st = 0, ph = 0, acc = 0, aph = 0, bph = 0;
             bool ok = true;
             for (int s = 0; s < nph && ok; ++s) {
                 const Shape sh = phase_shape(p, s);
                 int lo, hi;
                 my_range(sh, c, G, lo, hi);
-                if (!mbar_wait(b_full, bph & 1u, abort_flag)) break;  // the phase's operand is staged
-                ++bph;
+                if (!mbar_wait(b_full, bph, abort_flag)) break;  // the phase's operand is staged
+                bph ^= 1u;
                 mbar_arrive(b_taken);
                 tc_fence_after();
-                const int kb_first = lo % sh.nkb;
-                const uint32_t ub_s = smem_u32(ub);
+                int slot = 0;  // the i-th K block of the CTA's range is operand slot i mod nkb
                 for (int j = lo; j < hi && ok;) {
                     const int t = j / sh.nkb, kb0 = j - t * sh.nkb, kb1 = min(sh.nkb, kb0 + (hi - j));
-                    const int a = (int)(u % NACC);
-                    if (!mbar_wait(&acc_empty[a], ((u / NACC) & 1u) ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&acc_empty[acc], aph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(a * 16);
-                    for (int kb = kb0; kb < kb1; ++kb, ++idx) {
-                        const int st = (int)(idx % (uint32_t)S);
-                        if (!mbar_wait(&full[st], (idx / (uint32_t)S) & 1u, abort_flag)) {
+                    const uint32_t d_tmem = tmem + acc * (uint32_t)UCOLS;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full[st], ph, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const int slot = (kb - kb_first + sh.nkb) % sh.nkb;
-                        const uint64_t dw = sdesc(smem_u32(ring + (size_t)st * STAGE_BYTES));
-                        const uint64_t dx = sdesc(ub_s + (uint32_t)(slot * BSLOT_BYTES));
+                        const uint64_t dw = sdesc(ring_s + st * (uint32_t)STAGE_BYTES);
+                        const uint64_t dx = sdesc(ub_s + (uint32_t)slot * (uint32_t)BSLOT_BYTES);
 #pragma unroll
-                        for (int k = 0; k < KB / 16; ++k)
-                            umma(d_tmem, dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), id, (kb > kb0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < CH; ++k)
+                            umma(d_tmem + (uint32_t)(k * 16), dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), id,
+                                 kb > kb0 ? 1u : 0u);
                         umma_commit(&empty[st]);
+                        if (++st == (uint32_t)S) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
+                        if (++slot == sh.nkb) slot = 0;
                     }
                     if (!ok) break;
-                    umma_commit(&acc_full[a]);
-                    ++u;
+                    umma_commit(&acc_full[acc]);
+                    if (++acc == (uint32_t)NACC) {
+                        acc = 0;
+                        aph ^= 1u;
+                    }
                     j += kb1 - kb0;
                 }
             }
@@ -723,20 +830,39 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
         const int per = (n_keys + p.nchunks - 1) / p.nchunks;
         const int chunk = (per + TKA - 1) / TKA * TKA;
         const int n_real = (n_keys + chunk - 1) / chunk;
+        // buffers that phases add into: x starts as the block rows (the block build adds the anchor's
+        // projection to row 0), qkv and U at zero (later layers' qkv: zeroed after their attention);
+        // a grid barrier after the block build's operand orders these before any addition
+        {
+            const int64_t n4 = (int64_t)p.gamma * p.d / 4;
+            const int64_t a4 = n4 * c / G, b4 = n4 * (c + 1) / G;
+            for (int64_t i = a4 + tt; i < b4; i += NCT)
+                reinterpret_cast<float4*>(p.x)[i] = __ldg(reinterpret_cast<const float4*>(p.block_const) + i);
+        }
+        zero_share(p.qkv, (int64_t)p.gamma * 3 * p.d, c, G);
+        zero_share(p.U, (int64_t)p.gamma * p.V, c, G);
         unsigned long long nbar = 0;
-        uint32_t u = 0;
-        bool live = true;
-        for (int s = 0; s < nph && live; ++s) {
+        uint32_t acc = 0, aph = 0;
+        for (int s = 0; s < nph; ++s) {
             const Shape sh = phase_shape(p, s);
             int lo, hi;
             my_range(sh, c, G, lo, hi);
-            // row scales of the normalised operands, from the column tiles' sums of x^2
-            if (sh.kind == K_QKV || sh.kind == K_GU || sh.kind == K_OUT) {
-                if (tt < p.gamma) {
-                    float a = 0.f;
-                    for (int t2 = 0; t2 < p.d / TM; ++t2) a += __ldcg(p.ssq + t2 * 16 + tt);
-                    rs[tt] = rsqrtf(a / (float)p.d + p.eps);
-                }
+            const int kb_first = hi > lo ? lo % sh.nkb : 0;
+            const int nslots = min(sh.nkb, hi - lo);
+            const bool scaled = sh.kind == K_QKV || sh.kind == K_GU || sh.kind == K_OUT;
+            stage_operand(p, sh, kb_first, nslots, ub, anchor);
+            cons_sync();
+            if (tt == 0) {
+                // b_full completes once per phase: the MMA warp must have seen the previous one
+                if (s == 0 || mbar_wait(b_taken, (uint32_t)(s - 1) & 1u, abort_flag)) mbar_arrive(b_full);
+                else *abort_flag = 1;
+            }
+            // while the MMAs run: buffers for later phases, and the row scales of this one
+            if (s == 0 && grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;  // x, qkv, U set everywhere
+            if (sh.kind == K_QKV) zero_share(p.gu, (int64_t)p.gamma * 2 * p.F, c, G);
+            if (sh.kind == K_WO) zero_share(p.qkv, (int64_t)p.gamma * 3 * p.d, c, G);
+            if (scaled) {
+                row_scales(p, rs);
                 cons_sync();
             }
             if (sh.kind == K_OUT) {
@@ -747,90 +873,53 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
                     p.y[(int64_t)j * p.d + k] = __ldcg(p.x + (int64_t)j * p.d + k) * rs[j] * __ldg(p.out_norm + k);
                 }
             }
-            const int nslots = min(sh.nkb, hi - lo);
-            stage_operand(p, sh, hi > lo ? lo % sh.nkb : 0, nslots, ub, rs, anchor);
-            cons_sync();
-            if (tt == 0) {
-                // b_full completes once per phase: the MMA warp must have seen the previous one
-                if (s == 0 || mbar_wait(b_taken, (uint32_t)(s - 1) & 1u, abort_flag)) mbar_arrive(b_full);
-                else *abort_flag = 1;
-            }
             // epilogues of the CTA's tiles, in MMA order
             for (int j = lo; j < hi;) {
                 const int t = j / sh.nkb, kb0 = j - t * sh.nkb, kb1 = min(sh.nkb, kb0 + (hi - j));
                 j += kb1 - kb0;
-                const int a = (int)(u % NACC);
-                if (!mbar_wait(&acc_full[a], (u / NACC) & 1u, abort_flag)) *abort_flag = 1;
-                ++u;
+                const int a = (int)acc;
+                // one lane of the warp polls (the MMA thread shares the barrier unit), then the warp goes on
+                bool got = true;
+                if (lane == 0) got = mbar_wait_sleepy(&acc_full[a], aph, abort_flag);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (++acc == (uint32_t)NACC) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
                 tc_fence_after();
                 float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.f;
                 // tcgen05.ld is warp-wide: the whole warp takes the same branch
-                const bool ld_ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+                const bool ld_ok = got && __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
                 if (ld_ok && cg * 8 < p.gamma) {
-                    uint32_t rr[8];
-                    tmem_ld8(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(a * 16 + cg * 8), rr);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(rr[i]);
-                } else {
+                    for (int k = 0; k < CH; ++k) {
+                        uint32_t rr[8];
+                        tmem_ld8(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(a * UCOLS + k * 16 + cg * 8), rr);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                        for (int i = 0; i < 8; ++i) v[i] += __uint_as_float(rr[i]);
+                    }
                 }
                 tc_fence_before();
-                const bool stop = cons_sync_or(*abort_flag != 0);
-                if (tt == 0) mbar_arrive(&acc_empty[a]);  // TMEM columns free for the MMA warp
-                if (stop) {
-                    live = false;
-                    break;
-                }
-                const int cf = owner(sh, G, t * sh.nkb), cl = owner(sh, G, t * sh.nkb + sh.nkb - 1);
-                if (cf == cl) {
-                    finalize(p, sh, t, r, cg, v, red, L);
-                    continue;
-                }
-                // shared tile: this CTA's partial, then the last CTA of the tile adds them in CTA order
-                float* pp = p.part + (int64_t)(c + t) * p.gamma * TM;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[a]);  // this warp is done with the accumulators
+                if (!ld_ok) continue;
+                if (scaled)
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (cg * 8 + i < p.gamma) __stcg(pp + (cg * 8 + i) * TM + r, v[i]);
-                __threadfence();
-                cons_sync();
-                if (tt == 0) *flag = atomicAdd(&p.tickets[t], 1u) == (unsigned int)(cl - cf);
-                cons_sync();
-                if (*flag) {
-                    __threadfence();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
-                    for (int c2 = cf; c2 <= cl; ++c2) {
-                        const float* src = p.part + (int64_t)(c2 + t) * p.gamma * TM;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (cg * 8 + i < p.gamma) v[i] += __ldcg(src + (cg * 8 + i) * TM + r);
-                    }
-                    finalize(p, sh, t, r, cg, v, red, L);
-                    if (tt == 0) p.tickets[t] = 0u;
-                }
-                cons_sync();  // `flag` is rewritten by the next shared tile
+                    for (int i = 0; i < 8; ++i) v[i] *= rs[min(cg * 8 + i, GMAX - 1)];
+                epi_add(p, sh, t, r, cg, v);
             }
-            if (!live || s == nph - 1) break;
+            if (cons_sync_or(*abort_flag != 0) || s == nph - 1) break;
             if (grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;
             if (sh.kind == K_QKV) {
                 // ---- attention of layer sh.layer: item c = (head, key range) on warps 2-5
                 const int h = c / p.nchunks, rg = c - h * p.nchunks;
                 if (c < p.nh * p.nchunks && rg < n_real && warp < 6) {
                     const int start = rg * chunk, end = min(n_keys, start + chunk);
-                    attn_item<HD>(p, sh.layer, h, start, end, n_real, rg, ub);
-                    if (n_real > 1) {
-                        __threadfence();
-                        attn_sync();
-                        if (tt == 0) *flag = atomicAdd(&p.atickets[h], 1u) == (unsigned int)(n_real - 1);
-                        attn_sync();
-                        if (*flag) {
-                            __threadfence();
-                            attn_merge<HD>(p, h, n_real);
-                            if (tt == 0) p.atickets[h] = 0u;
-                        }
-                        attn_sync();
-                    }
+                    attn_item<HD>(p, sh.layer, h, start, end, L, rg, ub);
+                    attn_merge<HD>(p, p.hcnt + par * p.nh + h, (unsigned int)((sh.layer + 1) * n_real), h, rg, n_real,
+                                   abort_flag);
                 }
                 if (grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;
             }
@@ -863,6 +952,7 @@ int g_budget = 0;  // dynamic shared memory the kernel may take (0: unavailable)
 // Staging area: the operand slots of the widest phase, or the attention's two-stage ring and its
 // merge scratch, whichever is larger.
 int ubytes_for(const DraftStepArgs& a, int G) {
+    // (the operand slots of every phase, or the attention's ring and merge scratch)
     const int hd = a.d / a.nh;
     auto slots = [&](int N, int K) {
         const int nT = (N + TM - 1) / TM, nkb = (K + KB - 1) / KB;
@@ -901,13 +991,13 @@ cudaError_t draft_step_tc_init() {
     return cudaSuccess;
 }
 
-// Bytes after the ring and staging area: barriers, TMEM slot, flags, row scales and sums.
+// Bytes after the ring and staging area: barriers, TMEM slot, flags and row scales.
 static constexpr int kTail = 1024;
 
 static int stages_for(const DraftStepArgs& a, int G) {
     const int s = (g_budget - 1024 - ubytes_for(a, G) - kTail) / STAGE_BYTES;
-    // the tail holds 2 s + 2 NACC + 3 mbarriers, the TMEM slot and flags (16 B), rs[16] and red[64]
-    return (2 * s + 2 * NACC + 3) * 8 + 16 + 80 * 4 <= kTail ? s : 0;
+    // the tail holds 2 s + 2 NACC + 3 mbarriers, the TMEM slot and flags (16 B) and rs[16]
+    return (2 * s + 2 * NACC + 3) * 8 + 16 + 16 * 4 <= kTail ? s : 0;
 }
 
 bool draft_step_tc_ok(const DraftStepArgs& a, int G) {
@@ -916,29 +1006,21 @@ bool draft_step_tc_ok(const DraftStepArgs& a, int G) {
     if (a.gamma < 1 || a.gamma > GMAX || a.nL < 1 || a.nL > MAXL || (hd != 64 && hd != 128) || a.d % TM != 0 ||
         a.F % KB != 0 || a.H % 8 != 0 || a.d % a.nh != 0 || a.V < 1 || a.nchunks < 1)
         return false;
-    if (a.nh * a.nchunks > G) return false;  // one attention item per CTA
+    if (a.nh * a.nchunks > G || a.nh > NTHR) return false;  // one attention item per CTA
     return stages_for(a, G) >= 4;
-}
-
-size_t draft_step_tc_part_floats(const DraftStepArgs& a, int G) {
-    const int maxN = std::max({3 * a.d, 2 * a.F, a.V});
-    return ((size_t)(maxN + TM - 1) / TM + G) * a.gamma * TM;
 }
 
 cudaError_t draft_step_tc(const DraftStepArgs& a, int G, cudaStream_t st) {
     if (!draft_step_tc_ok(a, G)) return cudaErrorInvalidValue;
     StepParams p{};
     p.x = a.x;
-    p.q = a.q;
-    p.act = reinterpret_cast<bf16*>(a.act);
-    p.hact = reinterpret_cast<bf16*>(a.hact);
+    p.qkv = a.qkv;
+    p.gu = a.gu;
     p.y = a.y;
     p.U = a.U;
-    p.ssq = a.ssq;
-    p.part = a.part;
+    p.act = reinterpret_cast<bf16*>(a.act);
     p.apart = a.apart;
-    p.tickets = a.tickets;
-    p.atickets = a.atickets;
+    p.hcnt = a.hcnt;
     p.cache = reinterpret_cast<bf16*>(a.cache);
     p.layer_stride = a.layer_stride;
     p.kv_off = a.kv_off;

@@ -140,13 +140,11 @@ struct dspark_handle {
     unsigned long long* pk_bar = nullptr;    // persistent draft layers: 2 barrier counters, then the launch epoch
     TcWeightStream ts_tok_proj;              // tok_proj [d, H] as a 128-row weight stream
     void* ds_maps = nullptr;                 // one-launch tcgen05 step: [2 + 4 n_layers] weight tensor maps
-    float* ds_ssq = nullptr;                 // [d / 128, 16] column-tile sums of x^2
-    float* ds_part = nullptr;                // projection partials
-    size_t ds_part_floats = 0;
-    unsigned int* ds_tickets = nullptr;      // per weight tile
+    float* ds_qkv = nullptr;                 // [gamma, 3d] QKV products
+    float* ds_gu = nullptr;                  // [gamma, 2F] gate/up products
+    unsigned int* ds_hcnt = nullptr;         // [2, n_heads] arrivals of a head's key ranges
     float* ds_apart = nullptr;               // attention partials
     size_t ds_apart_floats = 0;
-    unsigned int* ds_atickets = nullptr;     // per head
     unsigned long long* ds_bar = nullptr;    // 2 barrier counters, then the launch epoch
     void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
     int pk_map3d = 0;
@@ -522,16 +520,13 @@ bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anc
     if (B != 1 || seq_ids || h->dt != DT_BF16 || !h->ds_maps || h->qk_rope || h->nkv != c.n_heads) return false;
     a = DraftStepArgs{};
     a.x = h->x;
-    a.q = h->q;
-    a.act = h->act_lp;
-    a.hact = h->h_lp;
+    a.qkv = h->ds_qkv;
+    a.gu = h->ds_gu;
     a.y = h->y;
     a.U = h->U;
-    a.ssq = h->ds_ssq;
-    a.part = h->ds_part;
+    a.act = h->act_lp;
     a.apart = h->ds_apart;
-    a.tickets = h->ds_tickets;
-    a.atickets = h->ds_atickets;
+    a.hcnt = h->ds_hcnt;
     a.cache = h->cache;
     a.layer_stride = h->layer_stride;
     a.kv_off = h->kv_off;
@@ -559,8 +554,7 @@ bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anc
     a.bar = h->ds_bar;
     a.epoch = reinterpret_cast<unsigned int*>(h->ds_bar + 2);
     a.err = h->d_err;
-    return draft_step_tc_ok(a, h->num_sms) && draft_step_tc_part_floats(a, h->num_sms) <= h->ds_part_floats &&
-           (size_t)c.n_heads * a.nchunks * c.gamma * (h->hd + 4) <= h->ds_apart_floats;
+    return draft_step_tc_ok(a, h->num_sms) && (size_t)c.n_heads * a.nchunks * c.gamma * (h->hd + 4) <= h->ds_apart_floats;
 }
 
 dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
@@ -629,7 +623,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             a.nL = c.n_layers;
             a.gamma = c.gamma;
             a.act_kind = c.act;
-            a.nchunks = std::max(1, std::min({32, h->num_sms / c.n_heads, (max_keys + 63) / 64}));
+            a.nchunks = std::max(1, std::min(h->num_sms / c.n_heads, (max_keys + 63) / 64));
             a.eps = c.eps;
             a.maps = h->pk_maps;
             a.map3d = h->pk_map3d;
@@ -1392,16 +1386,12 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             CTRY(cudaMemcpyAsync(h->ds_maps, maps.data(), maps.size() * sizeof(Map128), cudaMemcpyHostToDevice, st));
             CTRY(cudaStreamSynchronize(st));  // the host array goes out of scope
             const int G = h->num_sms;
-            const size_t max_tiles = (size_t)(std::max({3 * d, 2 * F, V}) + 127) / 128;
-            h->ds_part_floats = (max_tiles + G) * cfg->gamma * 128;
-            CTRY(dalloc(h, (void**)&h->ds_part, h->ds_part_floats * 4));
-            CTRY(dalloc(h, (void**)&h->ds_tickets, max_tiles * sizeof(unsigned int)));
-            CTRY(cudaMemsetAsync(h->ds_tickets, 0, max_tiles * sizeof(unsigned int), st));
-            CTRY(dalloc(h, (void**)&h->ds_ssq, (size_t)(d / 128) * 16 * sizeof(float)));
+            CTRY(dalloc(h, (void**)&h->ds_hcnt, 2 * (size_t)cfg->n_heads * sizeof(unsigned int)));
+            CTRY(cudaMemsetAsync(h->ds_hcnt, 0, 2 * (size_t)cfg->n_heads * sizeof(unsigned int), st));
+            CTRY(dalloc(h, (void**)&h->ds_qkv, (size_t)cfg->gamma * 3 * d * sizeof(float)));
+            CTRY(dalloc(h, (void**)&h->ds_gu, (size_t)cfg->gamma * 2 * F * sizeof(float)));
             h->ds_apart_floats = (size_t)G * cfg->gamma * (h->hd + 4);
             CTRY(dalloc(h, (void**)&h->ds_apart, h->ds_apart_floats * 4));
-            CTRY(dalloc(h, (void**)&h->ds_atickets, (size_t)cfg->n_heads * sizeof(unsigned int)));
-            CTRY(cudaMemsetAsync(h->ds_atickets, 0, (size_t)cfg->n_heads * sizeof(unsigned int), st));
             CTRY(dalloc(h, (void**)&h->ds_bar, 3 * sizeof(unsigned long long)));
             CTRY(cudaMemsetAsync(h->ds_bar, 0, 3 * sizeof(unsigned long long), st));
         }

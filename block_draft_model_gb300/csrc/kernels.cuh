@@ -196,16 +196,13 @@ cudaError_t draft_persistent(const DraftPersistArgs& a, int num_sms, cudaStream_
 // (draft_step_tc.cu): block build, every layer, out_norm and out_proj.
 struct DraftStepArgs {
     float* x;                   // [gamma, d]
-    float* q;                   // [gamma, d]
-    void* act;                  // [gamma, d] bf16
-    void* hact;                 // [gamma, F] bf16
+    float* qkv;                 // [gamma, 3d] (the kernel zeroes it before use)
+    float* gu;                  // [gamma, 2F] (idem)
     float* y;                   // [gamma, d]
     float* U;                   // [gamma, V]
-    float* ssq;                 // [d / 128, 16]
-    float* part;                // draft_step_tc_part_floats floats
+    void* act;                  // [gamma, d] bf16 attention output
     float* apart;               // n_heads * nchunks * gamma * (head_dim + 4) floats
-    unsigned int* tickets;      // [max(3d, 2F, V) / 128] zero-initialised
-    unsigned int* atickets;     // [n_heads] zero-initialised
+    unsigned int* hcnt;         // [2, n_heads] zero-initialised
     void* cache;                // layer 0 base (bf16), slot 0
     int64_t layer_stride, kv_off;
     int max_rows;
@@ -226,7 +223,6 @@ struct DraftStepArgs {
 };
 cudaError_t draft_step_tc_init();  // per device
 bool draft_step_tc_ok(const DraftStepArgs& a, int num_sms);
-size_t draft_step_tc_part_floats(const DraftStepArgs& a, int num_sms);
 cudaError_t draft_step_tc(const DraftStepArgs& a, int num_sms, cudaStream_t st);
 
 // ------------------------------------------------------------------ Markov chain, argmax, confidence
