@@ -63,6 +63,13 @@ def parse():
                     help="grouped-query variant: K/V heads of the drafter (0: one per query head)")
     ap.add_argument("--qk-norm", action="store_true", help="variant: per-head RMSNorm of Q and K")
     ap.add_argument("--rope-theta", type=float, default=0.0, help="variant: rotary embedding base (0: none)")
+    ap.add_argument("--oracle-single-thread", action="store_true",
+                    help="(internal) time the CPU oracle on a bounded sample in this process and print it as JSON")
+    ap.add_argument("--no-tc-phases", action="store_true",
+                    help="skip the tensor-core phases (32768-row ingest, batched out_proj GEMM) of the default run")
+    ap.add_argument("--record-traffic", nargs=6,
+                    metavar=("NCU_RAW_CSV", "CLASS", "WORKLOAD", "SOURCE", "LAUNCHES_PER_RANGE", "CAPTURE"),
+                    help="write the profiles/traffic.json entry of a kernel class from an ncu raw-page CSV, then exit")
     return ap.parse_args()
 
 
@@ -218,26 +225,82 @@ def load_peaks():
 
 
 def load_traffic(kernel_class: str, workload: str):
-    """DRAM bytes per range from the committed ncu traffic table (profiles/traffic.md),
-    if its row still matches the kernel source."""
+    """DRAM bytes per range of a kernel class from the committed ncu table (profiles/traffic.json,
+    written from captures by profiles/traffic_from_ncu.py), if its entry still matches the hash of
+    the kernel's source file; None otherwise."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "traffic.md")
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        lines = open(p).read().splitlines()
-    except OSError:
+        with open(p) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
         return None
-    for ln in lines:
-        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
-        if len(cells) != 7 or cells[0] != workload or cells[1] != kernel_class:
+    for e in table.get("entries", []):
+        if e.get("workload") != workload or e.get("class") != kernel_class:
             continue
         try:
-            digest = hashlib.sha256(open(os.path.join(ROOT, cells[2]), "rb").read()).hexdigest()[:16]
-            if digest != cells[3]:
-                return None
-            return int(cells[4]) * int(cells[5])
-        except (OSError, ValueError):
+            digest = hashlib.sha256(open(os.path.join(ROOT, e["source"]), "rb").read()).hexdigest()[:16]
+        except OSError:
             return None
+        if digest != e.get("source_sha16"):
+            return None
+        return int(e["dram_bytes_per_launch"]) * int(e.get("launches_per_range", 1))
     return None
+
+
+def record_traffic(csv_path, kernel_class, workload, source, launches_per_range, capture):
+    """Write (or replace) the entry of (workload, kernel_class) in profiles/traffic.json from an ncu
+    raw-page CSV (``ncu -i X.ncu-rep --page raw --csv``) of the kernel's captured launches: the
+    mean of dram__bytes_read.sum + dram__bytes_write.sum over them, keyed to the source file's hash."""
+    import csv
+    import hashlib
+    with open(csv_path, newline="") as f:
+        rows = list(csv.reader(f))
+    head = rows[0]
+    ir, iw = head.index("dram__bytes_read.sum"), head.index("dram__bytes_write.sum")
+    vals = []
+    for r in rows[1:]:
+        try:
+            vals.append(float(r[ir].replace(",", "")) + float(r[iw].replace(",", "")))
+        except (ValueError, IndexError):
+            continue  # the units row
+    if not vals:
+        raise SystemExit(f"no DRAM byte counters in {csv_path}")
+    digest = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:16]
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        table = {"about": "DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per launch of a bench "
+                          "kernel class, valid while the kernel source's SHA-256 prefix matches; written by "
+                          "bench.py --record-traffic", "entries": []}
+    table["entries"] = [e for e in table["entries"] if not (e["workload"] == workload and e["class"] == kernel_class)]
+    table["entries"].append({"workload": workload, "class": kernel_class, "source": source, "source_sha16": digest,
+                             "launches_per_range": int(launches_per_range),
+                             "dram_bytes_per_launch": int(round(sum(vals) / len(vals))), "launches_captured": len(vals),
+                             "capture": capture})
+    with open(p, "w") as f:
+        json.dump(table, f, indent=1)
+        f.write("\n")
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu / /proc/cpuinfo), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def cpu_cores():
@@ -334,13 +397,13 @@ class FreshContextRunner(Runner):
                 "draft_ms": ms_draft, "draft_blocks_per_s": 1e3 / ms_draft, "draft_bytes_min": bm,
                 "draft_gbs_of_bytes_min": bm / (ms_draft / 1e3) / 1e9}
 
-    def oracle_baseline(self, seconds, max_steps):
+    def oracle_baseline(self, seconds, max_steps, rows=4096):
         """The CPU oracle on a bounded sample of this workload, scaled to blocks/s of the full step:
-        ingest of up to 4096 rows and one draft are timed separately, the step time is
+        ingest of up to `rows` rows and one draft are timed separately, the step time is
         T / rows * t_ingest + drafts * t_draft."""
         import oracle
         dr = oracle.Drafter(self.cfg, self.W)
-        rows = min(self.T, 4096)
+        rows = min(self.T, rows)
         n, t_in, t_dr, t0 = 0, 0.0, 0.0, time.perf_counter()
         while n < max_steps:
             dr.reset(0)
@@ -486,6 +549,73 @@ def make_runner(name, dev, variant=None):
     raise SystemExit(f"unknown workload {name}")
 
 
+def oracle_single_thread(args):
+    """The same oracle on one host thread: a child process with the BLAS / OpenMP pools at one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-single-thread", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600).stdout
+        j = json.loads(out.strip().splitlines()[-1])
+        return {"value": j["value"], "unit": "blocks/s", "cores": 1, "sample": j["sample"]}
+    except (subprocess.SubprocessError, ValueError, IndexError, KeyError, OSError) as e:
+        return {"value": None, "unit": "blocks/s", "cores": 1, "error": str(e)[:200]}
+
+
+# --------------------------------------------------------------------------- tensor-core phases
+
+def tc_phases(dev, peaks, reps=5):
+    """The two contractions the drafter runs on the tensor cores at scale, on the Gemma-shaped
+    drafter (H 2560, m 4, d 1024, 5 layers, V 262144): a fresh 32768-row context ingested in one call
+    (Eq 2 projection + Eq 3 K/V of every layer, 1.374 TFLOP) and the batched out_proj product of 64
+    sequences x 5 block rows (320 x 1024 x 262144, 171.8 GFLOP).  Each is timed with CUDA events over
+    `reps` calls after one warm-up call and reported against the measured dense bf16 peak."""
+    import torch
+
+    import block_draft_model_gb300 as bdm
+    wl = syn.WORKLOADS["gemma_L32768_ingest"]
+    cfg, T = wl.cfg, wl.ctx_len
+    W = syn.make_weights(cfg, seed=0)
+    run = Runner(wl, dev)
+    g = run.make_drafter(W, max_ctx=T)
+    X = bf16_dev(syn.make_feats(cfg, T, seed=0), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    ms_in = timed(lambda: (g.reset(0), g.ingest_context(X)))
+    fl_in = ingest_flops(cfg, T)
+    rows = 64 * cfg.gamma
+    A = bf16_dev(syn.normal_bf16(5, 7, (rows, cfg.d_draft)), dev)
+    out = torch.empty(rows, cfg.vocab, dtype=torch.float32, device=dev)
+    Wo = run.Wd["out_proj"]
+    ms_op = timed(lambda: bdm.linear(A, Wo, out, kernel=bdm.KERNEL_TC))
+    fl_op = 2.0 * rows * cfg.d_draft * cfg.vocab
+    g.close()
+    del g, X, A, out, run
+    torch.cuda.empty_cache()
+    peak = peaks["bf16_tflops"]
+    res = {}
+    for name, ms, fl, note in (
+            ("ingest_L32768", ms_in, fl_in, "Gemma-shaped: fresh 32768-row context, Eq 2 + Eq 3 of 5 layers"),
+            ("batched_out_proj_320x1024x262144", ms_op, fl_op, "64 sequences x 5 rows against the 262144-row out_proj")):
+        tf = fl / (ms / 1e3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / peak, "flops": fl, "note": note}
+    res["peak_tflops"] = peak
+    res["peak_src"] = peaks["src"] + " (burst)"
+    return res
+
+
 # --------------------------------------------------------------------------- main
 
 def variant_of(args):
@@ -549,13 +679,27 @@ def reference_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": arm_config(wl, 1, args, variant),
             "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def main():
     args = parse()
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+        return
+    if args.oracle_single_thread:
+        # run with the BLAS and OpenMP pools at one thread (set by the parent before numpy loads)
+        wl = syn.WORKLOADS[args.workload]
+        run = FreshContextRunner(wl, None)
+        run.W = syn.make_weights(wl.cfg, seed=0)
+        run.pool_np = [syn.make_feats(wl.cfg, min(run.T, 128), seed=0, step=i) for i in range(2)]
+        run.npool = 2
+        run.anchors = syn.uniform_int(0, syn.STREAM_ANCHORS, (16,), 0, wl.cfg.vocab - 1)
+        v, sample = run.oracle_baseline(args.cpu_seconds, 20, rows=128)
+        print(json.dumps({"value": v, "sample": sample}), flush=True)
+        return
     if args.impl == "reference":
         reference_arm(args)
         return
@@ -648,6 +792,8 @@ def main():
         return a.elapsed_time(b) / n
 
     phases = run.phases(timed) if hasattr(run, "phases") else {}
+    if not args.no_tc_phases and world == 1 and args.workload == "minicpm_L1024":
+        phases["tensor_core"] = tc_phases(dev, load_peaks())
     phases["per_class_ms_per_step"] = {k: round(v[0] / nprof, 4) for k, v in prof_all.items() if v[1]}
     phases["note"] = ("per-class times come from a separate profiled pass whose event pairs break the "
                       "launch overlap; they rank the kernels, the step time is the timed region's")
@@ -679,7 +825,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(run, FreshContextRunner):
         v, sample = run.oracle_baseline(args.cpu_seconds, 50)
         line["cpu_baseline"] = {"value": v, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample, "cpu_model": cpu_model(),
+                                "single_thread": oracle_single_thread(args)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     g.close()

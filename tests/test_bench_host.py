@@ -58,15 +58,16 @@ def test_class_work_counts_kv_width(bench):
 def test_traffic_rows_follow_the_kernel_source(bench, tmp_path, monkeypatch):
     src = tmp_path / "k.cu"
     src.write_text("__global__ void k() {}\n")
-    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
     (tmp_path / "profiles").mkdir()
-    table = ("| workload | class | source | sha256[:16] | launches per range | DRAM bytes per launch | capture |\n"
-             "|---|---|---|---|---|---|---|\n"
-             f"| w | c | k.cu | {digest} | 3 | 1000 | x.md |\n")
-    (tmp_path / "profiles" / "traffic.md").write_text(table)
+    # an ncu raw-page CSV of two captured launches of the kernel: the table keeps their mean
+    csv = tmp_path / "raw.csv"
+    csv.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                   '"","","byte","byte"\n'
+                   '"0","k","900","100"\n'
+                   '"1","k","1100","100"\n')
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.load_traffic("c", "w") == 3000
+    bench.record_traffic(str(csv), "c", "w", "k.cu", 3, "x.md")
+    assert bench.load_traffic("c", "w") == 3 * 1100
     assert bench.load_traffic("c", "other") is None
     src.write_text("__global__ void k() { /* changed */ }\n")
     assert bench.load_traffic("c", "w") is None
-

@@ -497,8 +497,9 @@ def test_gemma_shaped_long_context(gemma):
 
 def test_gemma_shaped_batched_serving(gemma):
     """64 sequences with ragged contexts (512-8192 rows), 128 steps of 1-6 new
-    rows per sequence and one block per sequence; four sequences are checked at
-    steps 0 and 127."""
+    rows per sequence and one block per sequence.  Four sequences are checked
+    with every logit at steps 0 and 127, and the tokens and confidences of all
+    64 sequences at step 0 (the oracle re-ingests one sequence at a time)."""
     cfg, W, Wd, dr = gemma
     wl = syn.WORKLOADS["gemma_batched64"]
     n = wl.n_seqs
@@ -533,6 +534,8 @@ def test_gemma_shaped_batched_serving(gemma):
             torch.cuda.synchronize()
             results[s] = {i: (tok[i].cpu().numpy(), conf[i].cpu().numpy(), lg[i].cpu().numpy(),
                               len(kept[i])) for i in sample}
+            if s == 0:
+                first_tok, first_conf = tok.cpu().numpy().copy(), conf.cpu().numpy().copy()
     assert gdr.check() == 0
     for i in sample:
         assert gdr.context_length(i) == int(lens[i] + counts[:, i].sum())
@@ -542,4 +545,10 @@ def test_gemma_shaped_batched_serving(gemma):
             for part in kept[i][:nparts]:
                 dr.ingest(part)
             check_block(dr, 0, int(anchors[s, i]), t, c, l, label=f"batched step {s} seq {i}")
+    # the whole batch at step 0: every sequence's block must be one of the oracle's valid chains
+    for i in range(n):
+        dr.reset(0)
+        dr.ingest(syn.make_feats(cfg, int(lens[i]), seed=0, step=-1, seq=i))
+        dr.ingest(syn.make_feats(cfg, int(counts[0, i]), seed=0, step=0, seq=i))
+        check_block(dr, 0, int(anchors[0, i]), first_tok[i], first_conf[i], None, label=f"batched step 0 seq {i}")
     dr.reset(0)
