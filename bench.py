@@ -65,6 +65,11 @@ def parse():
     ap.add_argument("--rope-theta", type=float, default=0.0, help="variant: rotary embedding base (0: none)")
     ap.add_argument("--oracle-single-thread", action="store_true",
                     help="(internal) time the CPU oracle on a bounded sample in this process and print it as JSON")
+    ap.add_argument("--layers", choices=["auto", "per_kernel", "persistent_mma", "step_tc"], default="auto",
+                    help="form of the batch-1 draft layers (dspark_set_path): auto, one kernel per projection, "
+                         "every layer in one warp-MMA launch, or the whole step in one tcgen05 launch")
+    ap.add_argument("--tc-phase", choices=["ingest_L32768", "batched_out_proj"],
+                    help="run only this tensor-core phase (for a profiler), print its line and exit")
     ap.add_argument("--no-tc-phases", action="store_true",
                     help="skip the tensor-core phases (32768-row ingest, batched out_proj GEMM) of the default run")
     ap.add_argument("--record-traffic", nargs=6,
@@ -565,7 +570,7 @@ def oracle_single_thread(args):
 
 # --------------------------------------------------------------------------- tensor-core phases
 
-def tc_phases(dev, peaks, reps=5):
+def tc_phases(dev, peaks, reps=5, only=None):
     """The two contractions the drafter runs on the tensor cores at scale, on the Gemma-shaped
     drafter (H 2560, m 4, d 1024, 5 layers, V 262144): a fresh 32768-row context ingested in one call
     (Eq 2 projection + Eq 3 K/V of every layer, 1.374 TFLOP) and the batched out_proj product of 64
@@ -593,13 +598,14 @@ def tc_phases(dev, peaks, reps=5):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
-    ms_in = timed(lambda: (g.reset(0), g.ingest_context(X)))
+    ms_in = timed(lambda: (g.reset(0), g.ingest_context(X))) if only in (None, "ingest_L32768") else float("nan")
     fl_in = ingest_flops(cfg, T)
     rows = 64 * cfg.gamma
     A = bf16_dev(syn.normal_bf16(5, 7, (rows, cfg.d_draft)), dev)
     out = torch.empty(rows, cfg.vocab, dtype=torch.float32, device=dev)
     Wo = run.Wd["out_proj"]
-    ms_op = timed(lambda: bdm.linear(A, Wo, out, kernel=bdm.KERNEL_TC))
+    ms_op = (timed(lambda: bdm.linear(A, Wo, out, kernel=bdm.KERNEL_TC)) if only in (None, "batched_out_proj")
+             else float("nan"))
     fl_op = 2.0 * rows * cfg.d_draft * cfg.vocab
     g.close()
     del g, X, A, out, run
@@ -630,6 +636,7 @@ def arm_config(wl, world, args, variant=None):
     return {"workload": wl.name, "ctx_len": wl.ctx_len, "sequences": wl.n_seqs, "gamma": cfg.gamma,
             "d_draft": cfg.d_draft, "vocab": cfg.vocab,
             "parallelism": f"replicas{world}" if world > 1 else "single",
+            **({"layers": args.layers} if getattr(args, "layers", "auto") != "auto" else {}),
             "token_choice": (f"sampled (temperature {args.temperature}, top-k {args.top_k})"
                              if args.temperature > 0 else "argmax"),
             **({"variant": variant} if variant else {}),
@@ -711,9 +718,17 @@ def main():
     dev = torch.device("cuda", local)
     bdm.build()
     bdm.load()
+    if args.tc_phase:
+        print(json.dumps({"tc_phase": args.tc_phase, **tc_phases(dev, load_peaks(), reps=2, only=args.tc_phase)}),
+              flush=True)
+        return
     variant = variant_of(args)
     run = make_runner(args.workload, dev, variant)
     run.setup()
+    layers = {"auto": bdm.LAYERS_AUTO, "per_kernel": bdm.LAYERS_PER_KERNEL,
+              "persistent_mma": bdm.LAYERS_PERSISTENT_MMA, "step_tc": bdm.LAYERS_STEP_TC}[args.layers]
+    if layers != bdm.LAYERS_AUTO:
+        run.g.set_path(bdm.PATH_LAYERS, layers)
     if args.temperature > 0:
         run.g.set_sampling(args.temperature, args.top_k, 2024)
     cfg, g = run.cfg, run.g

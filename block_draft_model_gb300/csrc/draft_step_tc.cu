@@ -15,6 +15,9 @@
 //               GU   [gate | up] = RMSNorm(x) * ff_norm . W_gu^T
 //               DOWN x += (act(gate) * up) W_down^T
 //   OUT   U = RMSNorm(x) * out_norm . out_proj^T (and y)
+//   MKV   optionally the Markov chain ("module-dflash.ts" #markov, #confidence, forwardInfer):
+//         for k < gamma, l_k = U_k + w2 . w1[prev_k], tok_k = argmax l_k (lowest index on ties),
+//         prev_0 = anchor, prev_{k+1} = tok_k; conf_k = sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b)
 //
 // Every projection phase is a weight stream with at most 16 activation rows:
 // the weights are the MMA's M side (128-row tiles, 64-wide K blocks of 16 KB
@@ -103,6 +106,15 @@ struct StepParams {
     unsigned long long* bar;  // 2 arrival counters (launch parity)
     unsigned int* epoch;
     int* err;
+    // the Markov chain (chain != 0)
+    int chain, r;
+    const bf16* w1;           // [V, r]
+    const bf16* w2;           // [V, r]
+    const float* conf_w;      // [d + r + 1]: the weight, then the bias
+    int* tokens;              // [gamma]
+    float* conf;              // [gamma]
+    float* logits;            // [gamma, V] or nullptr
+    unsigned long long* mk;   // [2][GMAX + 1][G] per position: one word per CTA, then the arrival counters
 };
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -662,6 +674,175 @@ __device__ void attn_merge(const StepParams& p, unsigned int* cnt, unsigned int 
     }
 }
 
+// ---------------------------------------------------------------- the Markov chain
+// acc += the 8 bf16 products of w and e, each as one bf16 x bf16 + fp32 fused multiply-add
+__device__ __forceinline__ float fma_chunk(const uint4& w, const uint4& e, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\tmov.b32 {a2, a3}, %2;\n\tmov.b32 {a4, a5}, %3;\n\tmov.b32 {a6, a7}, %4;\n\t"
+        "mov.b32 {b0, b1}, %5;\n\tmov.b32 {b2, b3}, %6;\n\tmov.b32 {b4, b5}, %7;\n\tmov.b32 {b6, b7}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %0, a1, b1, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a2, b2, %0;\n\tfma.rn.f32.bf16 %0, a3, b3, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a4, b4, %0;\n\tfma.rn.f32.bf16 %0, a5, b5, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a6, b6, %0;\n\tfma.rn.f32.bf16 %0, a7, b7, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(e.x), "r"(e.y), "r"(e.z), "r"(e.w));
+    return acc;
+}
+
+// (value, index) as one word whose unsigned order is: larger value first, then lower index
+__device__ __forceinline__ unsigned long long best_key(float v, int i) {
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(~(uint32_t)i);
+}
+
+// The chain over the CTA's vocabulary rows [v0, v1) (consumer warps).  An 8-lane group takes a
+// row at a time (lane s holds the 16-byte chunks s, s + 8, ... of the w2 row and of e, so the
+// group reads whole 128-byte segments); w2 (read once per position) stays in L2 after the first.
+// Each position's argmax: the CTA's best word, then one word per CTA and an arrival counter; one
+// lane waits (bounded) for every CTA and its warp reads the words.
+template <int CPL>
+__device__ void markov_chain(const StepParams& p, int anchor, unsigned long long* words, int* toks, float* redv,
+                             int* redi, const uint8_t* w2s, int n_res, uint64_t* w2_full, float* us,
+                             volatile int* abort_flag) {
+    const int c = blockIdx.x, G = gridDim.x, V = p.V, r = p.r, gamma = p.gamma;
+    const int tt = threadIdx.x - 64, warp = tt >> 5, lane = threadIdx.x & 31, grp = tt >> 3, s = tt & 7;
+    constexpr int GROUPS = NCT / 8, UR = 4;  // row groups; rows of a group in flight together
+    constexpr int ROWB = CPL * 128;          // bytes of a w2 row
+    const int v0 = (int)((int64_t)c * V / G), v1 = (int)((int64_t)(c + 1) * V / G);
+    if (tt == 0) toks[0] = anchor;
+    // the slice's base logits of every position into shared memory at once: us[k * nrows + li]
+    const int nrows = v1 - v0;
+    for (int i = tt; i < gamma * nrows; i += NCT) {
+        const int k = i / nrows, li = i - k * nrows;
+        us[i] = __ldcg(p.U + (int64_t)k * V + v0 + li);
+    }
+    // the first n_res rows of the slice arrive in shared memory (row li at li * ROWB); an 8-lane group
+    // reads one whole 128-byte segment of a row at a time, so the rows need no swizzle
+    if (n_res > 0 && lane == 0 && !mbar_wait_sleepy(w2_full, 0, abort_flag)) atomicOr(p.err, DEVERR_TIMEOUT);
+    cons_sync();
+    for (int k = 0; k < gamma; ++k) {
+        const int prev = toks[k];
+        uint4 ev[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) ev[j] = __ldg(reinterpret_cast<const uint4*>(p.w1 + (int64_t)prev * r) + s + 8 * j);
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        // the loop bound is the same for every lane: the shuffles below take the whole warp.  The
+        // highest rows (past the resident ones, read from global memory) come first, so that their
+        // loads overlap the load of e.
+        for (int base = v0 + (nrows > 0 ? (nrows - 1) / (GROUPS * UR) : -1) * (GROUPS * UR); base >= v0;
+             base -= GROUPS * UR) {
+            uint4 w[UR][CPL];
+            float u[UR];
+#pragma unroll
+            for (int q = 0; q < UR; ++q) {
+                const int row = base + grp + GROUPS * q;
+                const bool ok = row < v1;
+                const bool res = row - v0 < n_res;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+                    w[q][j] = !ok ? make_uint4(0, 0, 0, 0)
+                                  : res ? *reinterpret_cast<const uint4*>(w2s + (size_t)(row - v0) * ROWB + (s + 8 * j) * 16)
+                                        : __ldg(reinterpret_cast<const uint4*>(p.w2 + (int64_t)row * r) + s + 8 * j);
+                u[q] = (ok && s == 0) ? us[k * nrows + (row - v0)] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < UR; ++q) {
+                float dot = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) dot = fma_chunk(w[q][j], ev[j], dot);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                const int row = base + grp + GROUPS * q;
+                if (s == 0 && row < v1) {
+                    const float l = u[q] + dot;
+                    if (p.logits) p.logits[(int64_t)k * V + row] = l;
+                    if (better(l, row, bv, bi)) {
+                        bv = l;
+                        bi = row;
+                    }
+                }
+            }
+        }
+        ArgBest b = warp_argbest({bv, bi});
+        if (lane == 0) {
+            redv[warp] = b.v;
+            redi[warp] = b.i;
+        }
+        cons_sync();
+        if (warp == 0) {
+            ArgBest cb{lane < NCW ? redv[lane] : -INFINITY, lane < NCW ? redi[lane] : INT_MAX};
+            cb = warp_argbest(cb);
+            unsigned long long* wk = words + (size_t)k * G;
+            unsigned long long* cnt = words + (size_t)GMAX * G + k;
+            if (lane == 0) {
+                // a CTA without rows still arrives, with a word below every real one
+                const unsigned long long key = cb.i != INT_MAX ? best_key(cb.v, cb.i) : 1ull;
+                if (cb.i != INT_MAX) {  // the next position's e wherever it comes from: this CTA's best row
+                    const char* row = reinterpret_cast<const char*>(p.w1 + (int64_t)cb.i * r);
+                    for (int o = 0; o < r * 2; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + o));
+                }
+                asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(wk + c), "l"(key) : "memory");
+                asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
+                const uint64_t t0 = globaltimer();
+                while (true) {
+                    unsigned long long cur;
+                    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(cnt) : "memory");
+                    if (cur >= (unsigned long long)G || *abort_flag) break;
+                    if (globaltimer() - t0 > TIMEOUT_NS) {
+                        atomicOr(p.err, DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+            unsigned long long m = 0ull;
+            for (int i = lane; i < G; i += 32) {
+                unsigned long long w;
+                asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(wk + i) : "memory");
+                m = w > m ? w : m;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long om = __shfl_xor_sync(0xffffffffu, m, o);
+                m = om > m ? om : m;
+            }
+            if (lane == 0) {
+                int tok = (int)(~(uint32_t)m);
+                if (m <= 1ull || tok < 0 || tok >= V) {  // no valid word (an aborted or broken exchange)
+                    if (c == 0) atomicOr(p.err, 8);
+                    tok = 0;
+                }
+                toks[k + 1] = tok;
+                if (c == 0) p.tokens[k] = tok;
+            }
+        }
+        cons_sync();
+    }
+    // confidences, by CTA 0: sigmoid(conf_w . [y_k ; w1[prev_k]] + conf_b)
+    if (c == 0) {
+        for (int k = 0; k < gamma; ++k) {
+            const float* yr = p.y + (int64_t)k * p.d;
+            const bf16* er = p.w1 + (int64_t)toks[k] * r;
+            float z = 0.f;
+            for (int i = tt; i < p.d; i += NCT) z = fmaf(__ldcg(yr + i), __ldg(p.conf_w + i), z);
+            for (int i = tt; i < r; i += NCT) z = fmaf(__bfloat162float(er[i]), __ldg(p.conf_w + p.d + i), z);
+            z = warp_sum(z);
+            if (lane == 0) redv[warp] = z;
+            cons_sync();
+            if (tt == 0) {
+                float a = 0.f;
+                for (int w2i = 0; w2i < NCW; ++w2i) a += redv[w2i];
+                p.conf[k] = 1.f / (1.f + expf(-(a + __ldg(p.conf_w + p.d + r))));
+            }
+            cons_sync();
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int HD>
 __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant__ StepParams p) {
@@ -677,14 +858,25 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
     uint64_t* b_full = acc_empty + NACC;
     uint64_t* b_taken = b_full + 1;  // the MMA warp has seen the phase's b_full
     uint64_t* drain = b_taken + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* w2_full = drain + 1;   // the Markov chain's resident w2 rows have arrived
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w2_full + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* rs = reinterpret_cast<float*>(tmem_slot + 4);   // [16] row scales
+    int* toks = reinterpret_cast<int*>(rs + GMAX);          // [GMAX + 1] the chain's tokens
+    float* redv = reinterpret_cast<float*>(toks + GMAX + 4);  // [NCW] the chain's per-warp bests
+    int* redi = reinterpret_cast<int*>(redv + NCW);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, G = gridDim.x;
     const int nph = 2 + 4 * p.nL;
     const int S = p.nstage;
+    // rows of this CTA's w2 slice kept in shared memory for the chain (the ring and staging area)
+    const int v0c = (int)((int64_t)c * p.V / G), v1c = (int)((int64_t)(c + 1) * p.V / G);
+    // (the slice's base logits of every position take the end of that area)
+    const size_t ures = ((size_t)p.gamma * (v1c - v0c) * 4 + 127) / 128 * 128;
+    const size_t area = (size_t)S * STAGE_BYTES + p.ubytes;
+    const int n_res = p.chain && area > ures ? min(v1c - v0c, (int)((area - ures) / ((size_t)p.r * 2))) : 0;
+    float* us = reinterpret_cast<float*>(ring + (area - ures));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -698,6 +890,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
         mbar_init(b_full, 1);
         mbar_init(b_taken, 1);
         mbar_init(drain, 1);
+        mbar_init(w2_full, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -711,6 +904,10 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
     unsigned long long* bar = p.bar + par;
     if (c == 0 && threadIdx.x == 0) p.bar[par ^ 1u] = 0ull;  // the next launch's counters
     if (c == 0 && threadIdx.x < p.nh) p.hcnt[(par ^ 1u) * p.nh + threadIdx.x] = 0u;
+    if (c == 0 && p.chain) {
+        unsigned long long* other = p.mk + (size_t)(par ^ 1u) * (GMAX + 1) * G;
+        for (int i = threadIdx.x; i < (GMAX + 1) * G; i += NTHR) other[i] = 0ull;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -745,6 +942,26 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
                         st = 0;
                         ph ^= 1u;
                     }
+                }
+            }
+            // the Markov chain's resident w2 rows, once every MMA (and so every read of the ring and of
+            // the operand slots) has retired: contiguous rows, in bulk copies of at most 32 KB
+            if (ok && n_res > 0) {
+                if (mbar_wait(drain, 0, abort_flag)) {
+                    const size_t bytes = (size_t)n_res * p.r * 2;
+                    const char* src = reinterpret_cast<const char*>(p.w2 + (int64_t)v0c * p.r);
+                    mbar_arrive_expect_tx(w2_full, (uint32_t)bytes);
+                    for (size_t o = 0; o < bytes; o += 32768) {
+                        const uint32_t n = (uint32_t)min((size_t)32768, bytes - o);
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                smem_u32(ring) + (uint32_t)o),
+                            "l"(src + o), "r"(n), "r"(smem_u32(w2_full))
+                            : "memory");
+                    }
+                    // wait for them here too: no copy may be in flight when the CTA exits
+                    volatile int never = 0;
+                    mbar_wait(w2_full, 0, &never);
                 }
             }
             // no copy may still be in flight when the CTA exits (only possible after an abort):
@@ -910,7 +1127,19 @@ __global__ void __launch_bounds__(NTHR, 1) k_draft_step_tc(const __grid_constant
                     for (int i = 0; i < 8; ++i) v[i] *= rs[min(cg * 8 + i, GMAX - 1)];
                 epi_add(p, sh, t, r, cg, v);
             }
-            if (cons_sync_or(*abort_flag != 0) || s == nph - 1) break;
+            if (cons_sync_or(*abort_flag != 0)) break;
+            if (s == nph - 1) {
+                if (p.chain && !grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) {
+                    // U, y and the logits' base are complete everywhere: the chain, in the staging area
+                    unsigned long long* words = p.mk + (size_t)par * (GMAX + 1) * G;
+                    const int cpl = p.r / 64;
+                    if (cpl == 4) markov_chain<4>(p, anchor, words, toks, redv, redi, ring, n_res, w2_full, us, abort_flag);
+                    else if (cpl == 2) markov_chain<2>(p, anchor, words, toks, redv, redi, ring, n_res, w2_full, us, abort_flag);
+                    else if (cpl == 1) markov_chain<1>(p, anchor, words, toks, redv, redi, ring, n_res, w2_full, us, abort_flag);
+                    else if (cpl == 8) markov_chain<8>(p, anchor, words, toks, redv, redi, ring, n_res, w2_full, us, abort_flag);
+                }
+                break;
+            }
             if (grid_barrier(bar, (++nbar) * G, p.err, abort_flag)) break;
             if (sh.kind == K_QKV) {
                 // ---- attention of layer sh.layer: item c = (head, key range) on warps 2-5
@@ -996,8 +1225,9 @@ static constexpr int kTail = 1024;
 
 static int stages_for(const DraftStepArgs& a, int G) {
     const int s = (g_budget - 1024 - ubytes_for(a, G) - kTail) / STAGE_BYTES;
-    // the tail holds 2 s + 2 NACC + 3 mbarriers, the TMEM slot and flags (16 B) and rs[16]
-    return (2 * s + 2 * NACC + 3) * 8 + 16 + 16 * 4 <= kTail ? s : 0;
+    // the tail holds 2 s + 2 NACC + 4 mbarriers, the TMEM slot and flags (16 B), rs[16], the chain's
+    // tokens [20] and per-warp bests [2][8]
+    return (2 * s + 2 * NACC + 4) * 8 + 16 + (16 + 20 + 16) * 4 <= kTail ? s : 0;
 }
 
 bool draft_step_tc_ok(const DraftStepArgs& a, int G) {
@@ -1007,7 +1237,16 @@ bool draft_step_tc_ok(const DraftStepArgs& a, int G) {
         a.F % KB != 0 || a.H % 8 != 0 || a.d % a.nh != 0 || a.V < 1 || a.nchunks < 1)
         return false;
     if (a.nh * a.nchunks > G || a.nh > NTHR) return false;  // one attention item per CTA
-    return stages_for(a, G) >= 4;
+    // the chain's lanes hold r / 64 16-byte chunks of a row: r in {64, 128, 256, 512}
+    if (a.chain && ((a.r != 64 && a.r != 128 && a.r != 256 && a.r != 512) || !a.mk || !a.w1 || !a.w2 || !a.conf_w ||
+                    !a.tokens || !a.conf))
+        return false;
+    const int S = stages_for(a, G);
+    if (S < 4) return false;
+    // the chain keeps its slice's base logits (every position) in the ring and staging area
+    if (a.chain && (size_t)a.gamma * ((a.V + G - 1) / G) * 4 + 128 > (size_t)S * STAGE_BYTES + ubytes_for(a, G))
+        return false;
+    return true;
 }
 
 cudaError_t draft_step_tc(const DraftStepArgs& a, int G, cudaStream_t st) {
@@ -1051,6 +1290,15 @@ cudaError_t draft_step_tc(const DraftStepArgs& a, int G, cudaStream_t st) {
     p.bar = a.bar;
     p.epoch = a.epoch;
     p.err = a.err;
+    p.chain = a.chain;
+    p.r = a.r;
+    p.w1 = reinterpret_cast<const bf16*>(a.w1);
+    p.w2 = reinterpret_cast<const bf16*>(a.w2);
+    p.conf_w = a.conf_w;
+    p.tokens = a.tokens;
+    p.conf = a.conf;
+    p.logits = a.logits;
+    p.mk = a.mk;
     const size_t smem = 1024 + (size_t)p.nstage * STAGE_BYTES + p.ubytes + kTail;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;

@@ -146,6 +146,7 @@ struct dspark_handle {
     float* ds_apart = nullptr;               // attention partials
     size_t ds_apart_floats = 0;
     unsigned long long* ds_bar = nullptr;    // 2 barrier counters, then the launch epoch
+    unsigned long long* ds_mk = nullptr;     // [2][17][num_sms] Markov exchange words and counters
     void* pk_maps = nullptr;                 // [n_layers][4] weight-slice tensor maps of the persistent layers
     int pk_map3d = 0;
     int layers_path = 0;                     // DSPARK_PATH_LAYERS: 0 auto, else the forced form
@@ -515,7 +516,7 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
 // The one-launch tcgen05 step (block build, every layer, out_norm, out_proj) for a batch-1 draft
 // of a bf16 multi-head drafter without the per-head Q/K transforms; false if it does not apply.
 bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
-                     DraftStepArgs& a) {
+                     int* tokens, float* conf, float* logits, DraftStepArgs& a) {
     const dspark_config& c = h->cfg;
     if (B != 1 || seq_ids || h->dt != DT_BF16 || !h->ds_maps || h->qk_rope || h->nkv != c.n_heads) return false;
     a = DraftStepArgs{};
@@ -554,6 +555,19 @@ bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anc
     a.bar = h->ds_bar;
     a.epoch = reinterpret_cast<unsigned int*>(h->ds_bar + 2);
     a.err = h->d_err;
+    // the Markov chain in the same launch, unless the tokens are sampled
+    const int r = c.markov_rank;
+    if (h->samp_t <= 0.f && h->ds_mk && (r == 64 || r == 128 || r == 256 || r == 512)) {
+        a.chain = 1;
+        a.r = c.markov_rank;
+        a.w1 = h->w1;
+        a.w2 = h->w2;
+        a.conf_w = h->conf_wb;
+        a.tokens = tokens;
+        a.conf = conf;
+        a.logits = logits;
+        a.mk = h->ds_mk;
+    }
     return draft_step_tc_ok(a, h->num_sms) && (size_t)c.n_heads * a.nchunks * c.gamma * (h->hd + 4) <= h->ds_apart_floats;
 }
 
@@ -563,10 +577,11 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
     DraftStepArgs dsa;
     const bool one_launch = h->layers_path == LAYERS_STEP_TC &&
-                            draft_step_args(h, B, seq_ids, anchors_dev, anchor, max_keys, dsa);
+                            draft_step_args(h, B, seq_ids, anchors_dev, anchor, max_keys, tokens, conf, logits, dsa);
     if (one_launch) {
         Prof pr(h, CAT_STEP, st);
         CUDA_TRY(h, draft_step_tc(dsa, h->num_sms, st));
+        if (dsa.chain) return DSPARK_OK;  // the chain, argmax and confidences ran in the same launch
     }
     if (!one_launch) {
         Prof pr_block(h, CAT_BLOCK, st);
@@ -1394,6 +1409,9 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             CTRY(dalloc(h, (void**)&h->ds_apart, h->ds_apart_floats * 4));
             CTRY(dalloc(h, (void**)&h->ds_bar, 3 * sizeof(unsigned long long)));
             CTRY(cudaMemsetAsync(h->ds_bar, 0, 3 * sizeof(unsigned long long), st));
+            const size_t nmk = 2 * (size_t)17 * G;
+            CTRY(dalloc(h, (void**)&h->ds_mk, nmk * sizeof(unsigned long long)));
+            CTRY(cudaMemsetAsync(h->ds_mk, 0, nmk * sizeof(unsigned long long), st));
         }
     }
     CTRY(cudaStreamSynchronize(st));

@@ -220,6 +220,15 @@ struct DraftStepArgs {
     unsigned long long* bar;    // 2 zero-initialised words
     unsigned int* epoch;        // zero-initialised
     int* err;
+    // the Markov chain, argmax and confidences in the same launch (chain != 0; bf16 w1/w2, r % 64 == 0)
+    int chain = 0, r = 0;
+    const void* w1 = nullptr;
+    const void* w2 = nullptr;
+    const float* conf_w = nullptr;      // [d + r + 1]
+    int* tokens = nullptr;              // [gamma]
+    float* conf = nullptr;              // [gamma]
+    float* logits = nullptr;            // [gamma, V] or nullptr
+    unsigned long long* mk = nullptr;   // [2][17][num_sms] zero-initialised exchange words and counters
 };
 cudaError_t draft_step_tc_init();  // per device
 bool draft_step_tc_ok(const DraftStepArgs& a, int num_sms);

@@ -227,32 +227,36 @@ def test_persistent_draft_layers(n_heads, gamma, L):
     check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
 
 
-# d, heads, gamma, L, vocab, hidden, layers
+# d, heads, gamma, L, vocab, hidden, layers, Markov rank
 STEP_SHAPES = [
-    (256, 2, 8, 300, 1000, 256, 2),     # head_dim 128, one key range per head over 2 x 76 CTAs
-    (128, 2, 16, 97, 777, 192, 2),      # head_dim 64, all 16 block rows (both TMEM column groups), H % 64 != 0
-    (384, 3, 5, 1500, 2053, 320, 3),    # three heads of 128, many key ranges merged, ragged vocabulary tile
-    (512, 8, 1, 40, 4096, 256, 1),      # gamma 1 (no mask rows), eight heads of 64
-    (256, 4, 7, 0, 1100, 256, 2),       # empty context: the block attends to itself only
+    (256, 2, 8, 300, 1000, 256, 2, 64),      # head_dim 128, one key range per head over 2 x 76 CTAs
+    (128, 2, 16, 97, 777, 192, 2, 128),      # head_dim 64, all 16 block rows (both TMEM column groups), H % 64 != 0
+    (384, 3, 5, 1500, 2053, 320, 3, 256),    # three heads of 128, many key ranges merged, ragged vocabulary tile
+    (512, 8, 1, 40, 4096, 256, 1, 64),       # gamma 1 (no mask rows), eight heads of 64
+    (256, 4, 7, 0, 1100, 256, 2, 32),        # empty context: the block attends to itself only; the separate chain
+    (128, 2, 4, 50, 100, 128, 1, 64),        # fewer vocabulary rows than CTAs: CTAs without rows in the chain
 ]
 
 
-@pytest.mark.parametrize("d,n_heads,gamma,L,vocab,hidden,n_layers", STEP_SHAPES)
-def test_one_launch_step_tc(d, n_heads, gamma, L, vocab, hidden, n_layers):
-    """The whole batch-1 step up to the logits in one launch with tcgen05 projections:
-    K blocks split over the CTAs with tiles shared by several CTAs (partials reduced by the
-    last one), key ranges of one head merged by the last range, ragged weight tiles,
-    three draws in a row on the same handle, then more context and another draw."""
+@pytest.mark.parametrize("d,n_heads,gamma,L,vocab,hidden,n_layers,rank", STEP_SHAPES)
+def test_one_launch_step_tc(d, n_heads, gamma, L, vocab, hidden, n_layers, rank):
+    """The whole batch-1 step in one launch with tcgen05 projections: K blocks split over the
+    CTAs with tiles shared by several CTAs (atomic reductions), key ranges of one head merged
+    cooperatively, ragged weight tiles, and (rank 64 / 128 / 256) the Markov chain, argmax and
+    confidences in the same launch; three draws in a row on the same handle, then more context
+    and another draw."""
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=hidden, n_taps=2, d_draft=d, n_heads=n_heads, n_layers=n_layers, ff_mult=2,
-                            gamma=gamma, vocab=vocab, markov_rank=32)
+                            gamma=gamma, vocab=vocab, markov_rank=rank)
     dr, gdr, _ = _small(cfg, L, seed=31, chunks=[L // 2] if L else [], anchors=[1, vocab - 1, vocab // 3],
                         max_ctx=L + 16, norm_std=0.3, paths=[(bdm.PATH_LAYERS, bdm.LAYERS_STEP_TC)])
     X = syn.make_feats(cfg, 3, seed=32)
     dr.ingest(X)
     gdr.ingest_context(to_torch(X))
-    tok, conf, lg = _draft(gdr, cfg, 77)
-    check_block(dr, 0, 77, tok, conf, lg, label="after 3 more rows")
+    tok, conf, lg = _draft(gdr, cfg, 77 % vocab)
+    check_block(dr, 0, 77 % vocab, tok, conf, lg, label="after 3 more rows")
+    tok, conf, _ = _draft(gdr, cfg, 5, want_logits=False)  # without the logits output
+    check_block(dr, 0, 5, tok, conf, None, label="no logits")
     assert gdr.check() == 0
 
 
@@ -262,7 +266,7 @@ def test_layer_forms_agree_without_graphs(layers):
     anchor passed by value."""
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=6,
-                            vocab=900, markov_rank=32)
+                            vocab=900, markov_rank=128)
     form = bdm.LAYERS_PER_KERNEL if layers == "per_kernel" else bdm.LAYERS_STEP_TC
     _small(cfg, 130, seed=33, chunks=[60], anchors=[3, 899, 450], norm_std=0.3,
            paths=[(bdm.PATH_GRAPHS, 1), (bdm.PATH_LAYERS, form)])
