@@ -263,10 +263,15 @@ def record_traffic(csv_path, kernel_class, workload, source, launches_per_range,
         rows = list(csv.reader(f))
     head = rows[0]
     ir, iw = head.index("dram__bytes_read.sum"), head.index("dram__bytes_write.sum")
+    # the second row names the units ncu chose (byte, Kbyte, Mbyte, Gbyte; decimal prefixes)
+    scale = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "": 1.0}
+    ur = rows[1] if len(rows) > 1 else []
+    sr = scale.get(ur[ir].strip().lower(), 1.0) if len(ur) > ir else 1.0
+    sw = scale.get(ur[iw].strip().lower(), 1.0) if len(ur) > iw else 1.0
     vals = []
     for r in rows[1:]:
         try:
-            vals.append(float(r[ir].replace(",", "")) + float(r[iw].replace(",", "")))
+            vals.append(float(r[ir].replace(",", "")) * sr + float(r[iw].replace(",", "")) * sw)
         except (ValueError, IndexError):
             continue  # the units row
     if not vals:

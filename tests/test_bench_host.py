@@ -68,6 +68,12 @@ def test_traffic_rows_follow_the_kernel_source(bench, tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     bench.record_traffic(str(csv), "c", "w", "k.cu", 3, "x.md")
     assert bench.load_traffic("c", "w") == 3 * 1100
+    # counters exported in scaled units
+    csv.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                   '"","","Mbyte","Kbyte"\n'
+                   '"0","k","33.5","1.5"\n')
+    bench.record_traffic(str(csv), "c", "w", "k.cu", 1, "x.md")
+    assert bench.load_traffic("c", "w") == 33501500
     assert bench.load_traffic("c", "other") is None
     src.write_text("__global__ void k() { /* changed */ }\n")
     assert bench.load_traffic("c", "w") is None
