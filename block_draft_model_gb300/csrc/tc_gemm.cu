@@ -35,7 +35,12 @@ constexpr int TMEM_COLS = 2 * BN;     // two accumulators
 constexpr int NTHREADS = 192;
 using namespace tc;
 
-constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + 256; }
+// Per epilogue warp, a 32 x 32 fp32 block (rows padded to 36 floats) through which the
+// plain fp32 store is transposed: each warp store then writes four whole 128-byte lines
+// instead of touching 32 lines with 16 bytes each.
+constexpr int STG_LD = 36;
+constexpr int STG_BYTES = 4 * 32 * STG_LD * 4;
+constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + 256 + STG_BYTES; }
 
 struct TileMap {
     int nM, nN;
@@ -78,6 +83,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* drain = bars + 2 * STAGES + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* stage_f32 = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = tm.nM * tm.nN * tm.ks * tm.groups;
@@ -192,6 +198,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int q = warp & 3;
         int buf = 0;
         uint32_t acc_phase = 0;
+        float* stg = stage_f32 + q * 32 * STG_LD;
+        const bool coalesce = ep.kind == EPI_STORE_F32 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             int m0, n0, s, g;
             tm.at(t, m0, n0, s, g);
@@ -206,7 +214,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (nb >= N) break;  // columns past N were not multiplied
                 uint32_t r[32];
                 tmem_ld32(base + c * 32, r);
-                if (ep.kind == EPI_MARKOV_T) {  // warp-wide: every lane takes part
+                if (coalesce && nb + 32 <= N) {  // warp-wide: every lane takes part
+                    // lane l's row (32 columns) into row l of the block, then each lane
+                    // takes 4 columns of rows l/8, l/8 + 4, ...: 8 lanes cover one row's 128 bytes
+                    float4* srow = reinterpret_cast<float4*>(stg + lane * STG_LD);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        srow[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    __syncwarp();
+                    const int c4 = (lane & 7) * 4;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = (lane >> 3) + 4 * i;
+                        const int mrow = m0 + q * 32 + rr;
+                        const float4 val = *reinterpret_cast<const float4*>(stg + rr * STG_LD + c4);
+                        if (mrow < M)
+                            *reinterpret_cast<float4*>(ep.out_f32 + (int64_t)(mrow + s * ep.split_rows) * ep.ldo + nb +
+                                                       c4) = val;
+                    }
+                    __syncwarp();
+                } else if (ep.kind == EPI_MARKOV_T) {  // warp-wide: every lane takes part
                     if (m0 + q * 32 < M) {
                         float v[32];
 #pragma unroll
