@@ -609,7 +609,7 @@ def tc_phases(dev, peaks, reps=5, only=None):
     A = bf16_dev(syn.normal_bf16(5, 7, (rows, cfg.d_draft)), dev)
     out = torch.empty(rows, cfg.vocab, dtype=torch.float32, device=dev)
     Wo = run.Wd["out_proj"]
-    ms_op = (timed(lambda: bdm.linear(A, Wo, out, kernel=bdm.KERNEL_TC)) if only in (None, "batched_out_proj")
+    ms_op = (timed(lambda: bdm.linear(A, Wo, out, kernel=bdm.KERNEL_AUTO)) if only in (None, "batched_out_proj")
              else float("nan"))
     fl_op = 2.0 * rows * cfg.d_draft * cfg.vocab
     g.close()

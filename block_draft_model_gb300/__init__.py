@@ -119,7 +119,7 @@ def _stream(stream) -> int:
     return int(getattr(stream, "cuda_stream", stream))
 
 
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_STREAM, KERNEL_TC, KERNEL_TC_STREAM = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_STREAM, KERNEL_TC, KERNEL_TC_STREAM, KERNEL_TC_WIDE = 0, 1, 2, 3, 4, 5
 
 
 def linear(A, W, out, kernel: int = KERNEL_AUTO, stream=None):

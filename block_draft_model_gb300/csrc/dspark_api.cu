@@ -253,6 +253,10 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     if (ep.ssp) return cudaErrorInvalidValue;  // only the weight-streaming epilogue hands over the next operand
     if (M <= 16 && skinny_ok(M, K))
         return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
+    if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_wide_preferred(M, N, h->num_sms) &&
+        tc_wide_ok(*tcw, M, N, K, ep))
+        return tc_gemm_wide((const char*)A + (size_t)a_row0 * lda * 2, lda, *tcw, M, N, K, ep, h->num_sms, h->d_err,
+                            st);
     if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_gemm_ok(M, N, K))
         return tc_gemm((const char*)A + (size_t)a_row0 * lda * 2, lda, *tcw, M, N, K, ep, h->num_sms, h->d_err, st);
     const char* a = (const char*)A;
@@ -1020,7 +1024,8 @@ dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const
     if (kernel == 0) {
         if (M <= 16 && dt == DT_BF16 && tc_stream_ok(M, N, K)) kernel = 4;
         else if (M <= 16 && skinny_ok(M, K)) kernel = 2;
-        else kernel = (dt == DT_BF16 && tc_available() && tc_gemm_ok(M, N, K)) ? 3 : 1;
+        else if (dt == DT_BF16 && tc_available() && tc_gemm_ok(M, N, K)) kernel = tc_wide_preferred(M, N, num_sms) ? 5 : 3;
+        else kernel = 1;
     }
     if (kernel == 1) {
         CUDA_TRY(nullptr, gemm_simt(dt, A_dev, lda, nullptr, dt, W_dev, M, N, K, ep, st));
@@ -1036,6 +1041,14 @@ dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const
         CUDA_TRY(nullptr, tc_prepare(w, W_dev, N, K));
         if (!w.ready) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "tensor map rejected");
         CUDA_TRY(nullptr, tc_gemm(A_dev, lda, w, M, N, K, ep, num_sms, err_word, st));
+    } else if (kernel == 5) {
+        if (dt != DT_BF16 || !tc_available() || lda % 8 != 0 || ((uintptr_t)A_dev & 15) || ((uintptr_t)W_dev & 15))
+            return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "shape not for the wide tensor-core GEMM");
+        if (!err_word) CUDA_TRY(nullptr, cudaMalloc((void**)&err_word, sizeof(int)));
+        TcWeight w;
+        CUDA_TRY(nullptr, tc_prepare(w, W_dev, N, K));
+        if (!tc_wide_ok(w, M, N, K, ep)) return fail(nullptr, DSPARK_ERR_UNSUPPORTED, "shape not for the wide tensor-core GEMM");
+        CUDA_TRY(nullptr, tc_gemm_wide(A_dev, lda, w, M, N, K, ep, num_sms, err_word, st));
     } else if (kernel == 4) {
         if (dt != DT_BF16 || !tc_stream_ok(M, N, K) || lda % 8 != 0 || ((uintptr_t)A_dev & 15) ||
             ((uintptr_t)W_dev & 15))

@@ -266,6 +266,191 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Wide form for few activation rows against many weight rows (the vocabulary projection of a
+// batched draft): the weights are the MMA's 128-row side and the activation rows its N side,
+// so the fp32 result rows are written along the vocabulary (a warp store covers 32 consecutive
+// entries of one output row) and no activation tile is padded to 128 rows.
+//   acc[n, m] = sum_k W[n, k] A[m, k]  for a 128-row weight tile and a group of <= 160 rows m.
+// The M rows are cut into ng groups of at most 160 (ng <= 2); tile t is weight tile t / ng and
+// group t % ng, so the groups of one weight tile run on neighbouring CTAs at the same time and
+// the weight tile comes from DRAM once.  Each tile's accumulator takes one of three 160-column
+// TMEM slots in turn (the CTA's u-th tile, slot u % 3): the MMAs of a tile overlap the epilogues
+// of the two before it.  Warps 2-5 drain the even tiles and warps 6-9 the odd ones; each set
+// waits on barriers of its own (u % 6), so it always observes its tiles' completions in order.
+namespace wide {
+constexpr int UW = 160;          // most columns per tile
+constexpr int SLOTS = 3;
+constexpr int NTHREADS = 320;    // producer, MMA, 2 x 4 epilogue warps
+constexpr int W_BYTES = 128 * BK * 2;  // 16 KB weight tile per stage
+constexpr int MAX_M = 2 * UW;
+constexpr int SMEM_MAX = 232448;  // 227 KB, the opt-in maximum per CTA
+constexpr int BAR_BYTES = 256;
+inline int groups(int M) { return M > UW ? 2 : 1; }
+// rows per group, a multiple of 16 (the last group may be narrower)
+inline int group_w(int M) {
+    const int na = (M + 15) & ~15, g = groups(M);
+    return (((na + g - 1) / g) + 15) & ~15;
+}
+inline int stage_bytes(int M) { return W_BYTES + group_w(M) * BK * 2; }
+inline int stages(int M) {
+    const int s = (SMEM_MAX - 1024 - BAR_BYTES) / stage_bytes(M);
+    return s > 8 ? 8 : s;
+}
+inline size_t smem(int M) { return 1024 + (size_t)stages(M) * stage_bytes(M) + BAR_BYTES; }
+}  // namespace wide
+
+__global__ void __launch_bounds__(wide::NTHREADS, 1)
+    k_tc_wide(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M, int N, int K,
+              int S, int gw, EpiParams ep, int* err) {
+    using namespace wide;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int na = (M + 15) & ~15;
+    const int ng = (na + gw - 1) / gw;
+    const uint32_t sbytes = W_BYTES + gw * BK * 2;
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * sbytes);
+    uint64_t* full = bars;                 // [S]
+    uint64_t* empty = bars + 8;            // [S]
+    uint64_t* acc_full = bars + 16;        // [6]
+    uint64_t* acc_empty = bars + 22;       // [SLOTS]
+    uint64_t* drain = bars + 25;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = ((N + 127) / 128) * ng;
+    const int nkb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 6; ++b) mbar_init(&acc_full[b], 1);
+        for (int b = 0; b < SLOTS; ++b) mbar_init(&acc_empty[b], 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int wt = t / ng, g = t - wt * ng;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sb = s0 + stage * sbytes;
+                    mbar_arrive_expect_tx(&full[stage], sbytes);
+                    tma_load_2d(sb, &tmW, &full[stage], kb * BK, wt * 128);
+                    tma_load_2d(sb + W_BYTES, &tmA, &full[stage], kb * BK, g * gw);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, u = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++u) {
+                const int g = t % ng;
+                const int width = na - g * gw < gw ? na - g * gw : gw;
+                const uint32_t id = idesc(128, width);
+                const uint32_t d_tmem = tmem + (u % SLOTS) * UW;
+                if (!mbar_wait(&acc_empty[u % SLOTS], ((u / SLOTS) & 1u) ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sb = s0 + stage * sbytes;
+                    const uint64_t dw = sdesc(sb), da = sdesc(sb + W_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma(d_tmem, dw + (uint64_t)(2 * k), da + (uint64_t)(2 * k), id, (kb || k) ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[u % 6]);
+            }
+            umma_commit(drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // epilogue: set h drains the CTA's tiles u with u % 2 == h; TMEM lanes 32*(warp % 4) .. +31
+        // are weight rows
+        const int h = (warp - 2) >> 2, q = warp & 3;
+        int u = h;
+        for (int t = blockIdx.x + h * gridDim.x; t < tiles; t += 2 * gridDim.x, u += 2) {
+            if (!mbar_wait(&acc_full[u % 6], (uint32_t)(u / 6) & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int wt = t / ng, g = t - wt * ng;
+            const int width = na - g * gw < gw ? na - g * gw : gw;
+            const int n = wt * 128 + q * 32 + lane;
+            const int mend = g * gw + width < M ? g * gw + width : M;  // the group's rows end here
+            const uint32_t base = tmem + (u % SLOTS) * UW + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < width; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(base + c, r);
+                const int m0 = g * gw + c;
+                if (n < N) {
+                    float* o = ep.out_f32 + (int64_t)m0 * ep.ldo + n;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (m0 + i < mend) o[(int64_t)i * ep.ldo] = __uint_as_float(r[i]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[u % SLOTS]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(err, DEVERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Per device (the shared-memory attribute belongs to the device's context):
 // -1 unknown, 0 unavailable, 1 available.
@@ -292,6 +477,8 @@ bool init_encode() {
     }
     if (cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
         return false;
+    if (cudaFuncSetAttribute(k_tc_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM_MAX) != cudaSuccess)
+        return false;
     g_state[dev] = 1;
     return true;
 }
@@ -314,6 +501,7 @@ bool tc_available() { return init_encode(); }
 
 bool tc_prepare_grouped(TcWeight& w, const void* ptr, int groups, int64_t group_stride, int rows, int K, bool a_side) {
     w.ready = false;
+    w.ready128 = false;
     w.ptr = ptr;
     w.N = rows;
     w.K = K;
@@ -374,6 +562,7 @@ bool tc_encode_slot_map(void* map, const void* W, int64_t rows, int64_t K, bool 
 
 cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K) {
     w.ready = false;
+    w.ready128 = false;
     w.ptr = ptr;
     w.N = N;
     w.K = K;
@@ -381,12 +570,42 @@ cudaError_t tc_prepare(TcWeight& w, const void* ptr, int N, int K) {
     if (K % 8 != 0 || ((uintptr_t)ptr & 15) != 0) return cudaSuccess;
     if (!encode(reinterpret_cast<CUtensorMap*>(w.tmap), ptr, N, K, K, BN)) return cudaSuccess;
     w.ready = true;
+    w.ready128 = encode(reinterpret_cast<CUtensorMap*>(w.tmap128), ptr, N, K, K, 128);
     return cudaSuccess;
 }
 
-void tc_release(TcWeight& w) { w.ready = false; }
+void tc_release(TcWeight& w) { w.ready = w.ready128 = false; }
 
 bool tc_gemm_ok(int M, int N, int K) { return init_encode() && M >= 1 && N >= 1 && K >= BK && K % 8 == 0; }
+
+// Measured on the 262144-row vocabulary projection (K 1024): the wide form wins at M <= 160 (one
+// group; the tiles pad M to 128 or 256) and at 257..320 (the tiles pad to 384); in between the
+// tiles' 256 rows carry little padding and they are the faster form.
+bool tc_wide_preferred(int M, int N, int num_sms) {
+    return (M <= wide::UW || (M > 2 * BM && M <= wide::MAX_M)) && (N + 127) / 128 >= num_sms;
+}
+
+bool tc_wide_ok(const TcWeight& w, int M, int N, int K, const EpiParams& ep) {
+    return w.ready128 && tc_gemm_ok(M, N, K) && M <= wide::MAX_M && N <= w.N && K == w.K &&
+           ep.kind == EPI_STORE_F32 && ep.out_f32 != nullptr;
+}
+
+cudaError_t tc_gemm_wide(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
+                         int num_sms, int* err, cudaStream_t st) {
+    if (!tc_wide_ok(w, M, N, K, ep)) return cudaErrorInvalidValue;
+    if (lda % 8 != 0 || ((uintptr_t)A & 15) != 0) return cudaErrorInvalidValue;
+    CUtensorMap tmA;
+    const int gw = wide::group_w(M);
+    if (!encode(&tmA, A, M, K, lda, gw)) return cudaErrorInvalidValue;
+    const int S = wide::stages(M);
+    if (S < 2) return cudaErrorInvalidValue;
+    const int tiles = (N + 127) / 128 * wide::groups(M);
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    launch(k_tc_wide, grid, wide::NTHREADS, wide::smem(M), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap128),
+           M, N, K, S, gw, ep, err);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
                     int num_sms, int* err, cudaStream_t st, int ksplit) {

@@ -12,9 +12,11 @@ namespace dspark {
 // A weight matrix W [N, K] (bf16, K contiguous) with its TMA descriptor.
 struct TcWeight {
     bool ready = false;
+    bool ready128 = false;  // tmap128 (128-row boxes, the wide form's weight side) is valid
     const void* ptr = nullptr;
     int N = 0, K = 0;
     alignas(64) unsigned char tmap[128];
+    alignas(64) unsigned char tmap128[128];
 };
 
 bool tc_available();
@@ -40,6 +42,14 @@ cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, in
 // of ep.out_f32, and the consumer sums the ranges.
 cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
                     int num_sms, int* err, cudaStream_t st, int ksplit = 1);
+// The wide form on its own: the weights are the MMA's 128-row side and all M <= 320 rows of A
+// its N side (EPI_STORE_F32; every weight tile read once).
+bool tc_wide_ok(const TcWeight& w, int M, int N, int K, const EpiParams& ep);
+// The shapes where the wide form beats the 128 x 256 tiles: M <= 160 or 257..320, and at
+// least one 128-row weight tile per SM.
+bool tc_wide_preferred(int M, int N, int num_sms);
+cudaError_t tc_gemm_wide(const void* A, int64_t lda, const TcWeight& w, int M, int N, int K, const EpiParams& ep,
+                         int num_sms, int* err, cudaStream_t st);
 
 // Weight-streaming variant for M <= 16 activation rows (tc_stream.cu): the
 // weights are the MMA's 128-row side.  `part`/`tickets` are scratch for the

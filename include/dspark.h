@@ -256,8 +256,11 @@ int32_t dspark_profile_read(dspark_handle* h, int32_t max, const char** names_ho
  * (dtype DSPARK_BF16) or both float32 (DSPARK_FP32); out_dev [M, N] float32
  * with row stride ldo.  `kernel` selects the implementation: 0 the one the step
  * would use for this shape, 1 SIMT tiles, 2 weight streaming (M <= 16, K % 8 == 0),
- * 3 tcgen05 tensor cores (bf16, K >= 64, K % 8 == 0, 16-byte aligned rows),
- * 4 tcgen05 weight streaming (as 3, and M <= 16).
+ * 3 tcgen05 tensor cores in 128 x 256 tiles (bf16, K >= 64, K % 8 == 0, 16-byte
+ * aligned rows), 4 tcgen05 weight streaming (as 3, and M <= 16), 5 the wide tcgen05
+ * form (as 3, and M <= 320): W's rows on the MMA's 128-row side and A's rows on its
+ * N side in one or two groups, so no A tile is padded to 128 rows; kernel 0 takes it
+ * where M <= 160 or 257 <= M <= 320, and N is at least 128 x the SM count.
  * DSPARK_ERR_UNSUPPORTED if the chosen kernel cannot take the shape. */
 dspark_status dspark_linear(int32_t dtype, const void* A_dev, int64_t lda, const void* W_dev, int32_t M, int32_t N,
                             int32_t K, float* out_dev, int64_t ldo, int32_t kernel, void* stream);
