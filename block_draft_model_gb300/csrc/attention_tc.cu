@@ -38,6 +38,7 @@ constexpr int NW = 4;       // warps per CTA, 16 keys of each tile per warp
 constexpr int NT = NW * 32;
 constexpr int GMAX = 16;    // queries per block (the M of the MMA)
 constexpr int CMAX = 128;   // largest number of key ranges per (sequence, head)
+constexpr int RFAST = 12;   // up to this many ranges the last CTA merges in one pass per thread
 static_assert(NT == GMAX * 8, "the merge gives each query eight threads");
 
 // NS: cp.async ring depth; 3 when two CTAs share an SM, 6 when one CTA has it alone
@@ -347,6 +348,52 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     // as many ranges as fit per piece (usually all: one round trip), and merged
     // piece by piece with a running max, sum and rescale per query.
     const float* all = p.part + bh * p.n_chunks * gamma * w;  // range cc, query j at (cc * gamma + j) * w
+    constexpr int ITEMS = (GMAX * (HD / 4) + NT - 1) / NT;  // (query, 4 columns) items per thread
+    const int rbytes = gamma * w * 4;
+    const uint32_t stg = ring + L::STG;
+    const float* S = reinterpret_cast<const float*>(sm + L::STG);
+    if (n_real <= RFAST && n_real <= (L::BYTES - L::STG) / rbytes) {
+        // Few ranges: one staging round trip, then each thread merges its own items over the
+        // ranges (two passes over the (m, l) pairs, no shared weight tables, no further block
+        // barriers).  The loops stay rolled: this code runs once per launch, cold in the
+        // instruction cache, and unrolled it is slower to fetch than to execute.  With more
+        // ranges the per-thread chain grows long and the piecewise merge below, which spreads
+        // the ranges of a query over eight threads, is faster.
+        const char* src = reinterpret_cast<const char*>(all);
+        for (int i = tid; i < n_real * rbytes / 16; i += NT) cp_async16(stg + i * 16, src + i * 16, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll 1
+        for (int k = 0; k < ITEMS; ++k) {
+            const int i = tid + k * NT;
+            if (i < gamma * (HD / 4)) {
+                const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+                const float* sj = S + j * w;  // range cc at sj + cc * gamma * w
+                const int cs = gamma * w;
+                float M = -INFINITY;
+#pragma unroll 1
+                for (int cc = 0; cc < n_real; ++cc) M = fmaxf(M, sj[cc * cs]);
+                const float Ms = M == -INFINITY ? 0.f : M;
+                float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < n_real; ++cc) {
+                    const float2 ml = *reinterpret_cast<const float2*>(sj + cc * cs);
+                    const float4 x = *reinterpret_cast<const float4*>(sj + cc * cs + 4 + e);
+                    const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - Ms);
+                    l = fmaf(wt, ml.y, l);
+                    a0 = fmaf(wt, x.x, a0);
+                    a1 = fmaf(wt, x.y, a1);
+                    a2 = fmaf(wt, x.z, a2);
+                    a3 = fmaf(wt, x.w, a3);
+                }
+                const float inv = 1.f / l;  // every range holds at least one key, so the sum is >= 1
+                store4<TO>(out + (int64_t)j * d + e, a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+            }
+        }
+        if (tid == 0) p.tickets[bh] = 0u;
+        return;
+    }
     float* Wm = reinterpret_cast<float*>(sm + L::WM);
     float* Mj = reinterpret_cast<float*>(sm + L::MJ);
     float* Lj = Mj + GMAX;
@@ -355,14 +402,10 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         Mj[tid] = -INFINITY;
         Lj[tid] = 0.f;
     }
-    constexpr int ITEMS = (GMAX * (HD / 4) + NT - 1) / NT;  // (query, 4 columns) items per thread
     float acc[ITEMS][4];
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
-    const int rbytes = gamma * w * 4;
     const int fit = min((L::BYTES - L::STG) / rbytes, CMAX);
-    const uint32_t stg = ring + L::STG;
-    const float* S = reinterpret_cast<const float*>(sm + L::STG);
     for (int c0 = 0; c0 < n_real; c0 += fit) {
         const int nr = min(fit, n_real - c0);
         __syncthreads();  // the previous piece has been consumed
@@ -464,8 +507,11 @@ int g_num_sms = 0;
 
 template <int HD, typename TO>
 void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
-    // a grid that fits one CTA per SM gives each CTA the SM's whole shared memory: a deeper ring
-    if ((int)(grid.x * grid.y * grid.z) <= g_num_sms)
+    // A grid that fits one CTA per SM gives each CTA the SM's whole shared memory: a deeper ring,
+    // where the ranges are long enough to use it.  Ranges of a few tiles keep the 3-stage ring, so
+    // that the next kernel's CTAs (launched early, programmatic dependent launch) fit beside them.
+    const int per_range = p.max_keys > 0 ? (p.max_keys + (int)grid.x * TK - 1) / ((int)grid.x * TK) : 1 << 30;
+    if ((int)(grid.x * grid.y * grid.z) <= g_num_sms && per_range > 2)
         launch(k_attention_tc<HD, TO, 6>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
     else
         launch(k_attention_tc<HD, TO, 3>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);

@@ -699,6 +699,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             ap.d_kv = h->dkv;
             ap.n_kv_heads = h->nkv;
             ap.n_chunks = attn_chunks(h, B, max_keys);
+            ap.max_keys = max_keys;
             ap.part = h->attn_part;
             ap.tickets = h->attn_tickets;
             ap.out = actA;

@@ -113,6 +113,7 @@ struct AttnParams {
     int d_kv = 0, n_kv_heads = 0;  // cache row width and K/V heads (0: d, n_heads); head h reads K/V head
                                    // h / (n_heads / n_kv_heads)
     int n_chunks;            // split of the (len + gamma) keys of one sequence, 1 .. attn_max_chunks()
+    int max_keys = 0;        // bound on any sequence's len + gamma (0: none known); picks the ring depth
     float* part;             // scratch: B * n_heads * n_chunks * gamma * (head_dim + 2) floats
     unsigned int* tickets;   // scratch: B * n_heads counters, zero before and after every launch
     void* out;               // [B*gamma, d] attention output, out_dtype

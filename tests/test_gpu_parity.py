@@ -361,12 +361,15 @@ def test_markov_chain_few_sequences(n_seq, rank, vocab, form):
                         label=f"one sequence, launch {rep}")
 
 
-def test_bf16_attention_many_key_ranges():
-    """head_dim 128, 1500 context rows: the keys of each head are split over
-    many CTAs (64-key tiles, a ragged last tile) and merged by the last one."""
+@pytest.mark.parametrize("ctx", [700, 1500, 1800])
+def test_bf16_attention_many_key_ranges(ctx):
+    """head_dim 128, two heads: the keys of each head are split over many CTAs
+    (64-key tiles, a ragged last tile) and merged by the last one: 707 keys give
+    12 ranges (the one-pass merge), 1507 keys 24 and 1807 keys 29 (the piecewise
+    merge, in one staged piece and in several)."""
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=7,
                             vocab=1000, markov_rank=64)
-    _small(cfg, 1500, seed=12, chunks=[700], anchors=[4, 998], max_ctx=1600)
+    _small(cfg, ctx, seed=12, chunks=[700], anchors=[4, 998], max_ctx=1900)
 
 
 def test_host_checked_errors():
