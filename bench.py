@@ -231,8 +231,8 @@ def load_peaks():
 
 def load_traffic(kernel_class: str, workload: str):
     """DRAM bytes per range of a kernel class from the committed ncu table (profiles/traffic.json,
-    written from captures by profiles/traffic_from_ncu.py), if its entry still matches the hash of
-    the kernel's source file; None otherwise."""
+    written by `bench.py --record-traffic` from an ncu capture), if its entry still matches the hash
+    of the kernel's source file; None otherwise."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
