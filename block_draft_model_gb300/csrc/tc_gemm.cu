@@ -200,6 +200,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t acc_phase = 0;
         float* stg = stage_f32 + q * 32 * STG_LD;
         const bool coalesce = ep.kind == EPI_STORE_F32 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0;
+        // bf16 K/V cache rows, 64 columns at a time (whole 128-byte lines); a 64-column pair never
+        // straddles K and V when the cache row width is a multiple of 64
+        const int kvw = ep.d_kv ? ep.d_kv : ep.d;
+        const bool kv16 = ep.kind == EPI_KV_CACHE && ep.cache_dtype == DT_BF16 && (kvw & 63) == 0 &&
+                          ((uintptr_t)ep.cache & 15) == 0 && ((ep.seq_stride | ep.kv_off | ep.group_stride) & 7) == 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             int m0, n0, s, g;
             tm.at(t, m0, n0, s, g);
@@ -208,10 +213,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int row = m0 + q * 32 + lane;
             const int orow = row + s * ep.split_rows;  // output row (K range s of a split product)
             const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
+            // K/V cache element offset of this lane's row (without the column), and whether it is stored
+            int64_t kv_row = 0;
+            int kv_ok = 0;
+            if (kv16 && row < M) {
+                const int slot = ep.row_seq ? ep.row_seq[row] : 0;
+                const int pos = ep.row_pos ? ep.row_pos[row] : (slot >= 0 ? ep.seq_len[slot] + row : -1);
+                kv_ok = slot >= 0 && pos >= 0 && pos < ep.max_rows;
+                kv_row = g * ep.group_stride + (int64_t)slot * ep.seq_stride + (int64_t)pos * kvw;
+            }
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int nb = n0 + c * 32;
                 if (nb >= N) break;  // columns past N were not multiplied
+                if (kv16 && (c & 1) == 0 && nb + 64 <= N) {  // warp-wide: every lane takes part
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(base + c * 32, r0);
+                    tmem_ld32(base + c * 32 + 32, r1);
+                    // lane l's 64 bf16 into row l of the block (144-byte rows), then 8 lanes per row
+                    // store its 128 bytes: 4 rows per warp store
+                    uint4* srow = reinterpret_cast<uint4*>(stg + lane * STG_LD);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t* rr = j < 4 ? r0 + 8 * j : r1 + 8 * (j - 4);
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+                            w4[i] = *reinterpret_cast<uint32_t*>(&pr);
+                        }
+                        srow[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    __syncwarp();
+                    const int64_t col = nb < kvw ? nb : ep.kv_off + (nb - kvw);
+                    bf16* cache = reinterpret_cast<bf16*>(ep.cache);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = (lane >> 3) + 4 * i;
+                        const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * STG_LD + (lane & 7) * 4);
+                        const int64_t rb = __shfl_sync(0xffffffffu, kv_row, rr);
+                        if (__shfl_sync(0xffffffffu, kv_ok, rr))
+                            *reinterpret_cast<uint4*>(cache + rb + col + (lane & 7) * 8) = val;
+                    }
+                    __syncwarp();
+                    ++c;
+                    continue;
+                }
                 uint32_t r[32];
                 tmem_ld32(base + c * 32, r);
                 if (coalesce && nb + 32 <= N) {  // warp-wide: every lane takes part
