@@ -83,8 +83,8 @@ __device__ __forceinline__ void unpack8(const uint8_t* p, float* f) {
 
 template <typename TC, typename TO>
 __global__ void __launch_bounds__(NT) k_attention(AttnParams p) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) uint8_t sm[];
     const int gamma = p.gamma, d = p.d, hd = d / p.n_heads;
     const Layout<TC> L(hd, gamma);

@@ -23,6 +23,7 @@
 // combination of V rows.  At the end the four warps merge through shared
 // memory into the range's (m, l, o) partial (log2 domain, rows of head_dim + 4
 // floats so that the last CTA can stage them with 16-byte cp.async copies).
+#include <limits.h>
 #include <math.h>
 #include <stdlib.h>
 
@@ -120,16 +121,18 @@ __device__ __forceinline__ void store4<bf16>(bf16* dst, float a, float b, float 
     *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// Copies of keys [t0, t0 + TK) into one ring stage; keys at or past `end` are zero-filled.
+// Copies of keys [t0, t0 + TK) into one ring stage; keys at or past `end` are zero-filled.  Only
+// the rows whose key lies in [klo, khi) are touched (the default: every row).
 template <int HD>
 __device__ __forceinline__ void load_kv(uint32_t dst, const bf16* Kb, const bf16* Vb, int64_t stride, int t0,
-                                        int end) {
+                                        int end, int klo = INT_MIN, int khi = INT_MAX) {
     constexpr int RB = HD * 2 + 16, TILE = TK * RB;  // as in TLayout
     constexpr int VPR = HD * 2 / 16;
 #pragma unroll 4
     for (int i = threadIdx.x; i < TK * VPR; i += NT) {
         const int r = i / VPR, v = i - r * VPR;
         const int key = t0 + r;
+        if (key < klo || key >= khi) continue;
         const bool ok = key < end;
         const int64_t off = (int64_t)(ok ? key : t0) * stride + v * 8;
         const uint32_t so = r * RB + v * 16;
@@ -142,18 +145,21 @@ template <int HD, typename TO, int NS>
 __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     using L = TLayout<HD, NS>;
     constexpr int KS = HD / 16;  // 16-wide k steps of Q K^T; pairs of 8-wide output tiles of P V
-    pdl_trigger();
-    pdl_wait();
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ int is_last;
 
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gamma = p.gamma, d = p.d;
+    // Up to pdl_wait() this kernel reads only what kernels at least two launches back wrote (the slot
+    // map, the context lengths and the context rows of the cache): its predecessor, the projection
+    // that wrote Q and the block's K/V rows, has passed its own wait before this kernel starts.
     const int slot = p.seq_ids ? p.seq_ids[b] : b;
     const int n_keys = slot < 0 ? 0 : p.seq_len[slot] + gamma;  // a rejected sequence has no keys
     TO* out = reinterpret_cast<TO*>(p.out) + (int64_t)b * gamma * d + h * HD;
     if (n_keys == 0) {
+        pdl_wait();
+        pdl_trigger();
         if (c == 0)
             for (int i = tid; i < gamma * (HD / 4); i += NT)
                 store4<TO>(out + (int64_t)(i / (HD / 4)) * d + (i % (HD / 4)) * 4, 0.f, 0.f, 0.f, 0.f);
@@ -162,7 +168,11 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const int per = (n_keys + p.n_chunks - 1) / p.n_chunks;
     const int chunk = (per + TK - 1) / TK * TK;
     const int n_real = (n_keys + chunk - 1) / chunk;
-    if (c >= n_real) return;
+    if (c >= n_real) {
+        pdl_wait();
+        pdl_trigger();
+        return;
+    }
     const int start = c * chunk, end = min(n_keys, start + chunk);
     const int n_tiles = (end - start + TK - 1) / TK;
 
@@ -173,11 +183,20 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const bf16* Kb = reinterpret_cast<const bf16*>(p.cache) + (int64_t)slot * p.seq_stride + kvh * HD;
     const bf16* Vb = Kb + p.kv_off;
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(sm);
+    const int n_ctx = n_keys - gamma;  // keys below this are context rows, written before the step
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
-        if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, dkv, start + s * TK, end);
+        if (s < n_tiles) load_kv<HD>(ring + s * L::STAGE, Kb, Vb, dkv, start + s * TK, end, INT_MIN, n_ctx);
         cp_async_commit();
     }
+    pdl_wait();
+    pdl_trigger();
+    // the block's own K/V rows of the tiles above (and the zero rows past the range end)
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s)
+        if (s < n_tiles && start + (s + 1) * TK > n_ctx)
+            load_kv<HD>(ring + s * L::STAGE, Kb, Vb, dkv, start + s * TK, end, n_ctx, INT_MAX);
+    cp_async_commit();
 
     // Q as A fragments: rows g and g+8, columns (lane % 4) * 2 (+8) of every 16-wide k step
     const int g = lane >> 2, cq = (lane & 3) * 2;
@@ -214,7 +233,8 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const uint32_t v_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * L::RB + (lm >> 1) * 16);
 
     for (int t = 0; t < n_tiles; ++t) {
-        cp_async_wait<NS - 2>();
+        if (t == 0) cp_async_wait<0>();  // the first tiles' context and block rows came in two groups
+        else cp_async_wait<NS - 2>();
         __syncthreads();  // tile t is visible; every warp is done with tile t-1, whose stage is refilled next
         {
             const int tn = t + NS - 1;

@@ -16,9 +16,12 @@ typedef __nv_bfloat16 bf16;
 // it may start while its predecessor is still running.  pdl_trigger() lets the
 // next kernel start launching; pdl_wait() blocks until every predecessor grid
 // has completed and its memory is visible.  Each kernel calls pdl_wait() before
-// it touches memory that an earlier kernel writes or reads, and before it
-// exits, so completion stays transitive along the stream.  Both are no-ops for
-// a kernel launched without the attribute.
+// it touches memory that its predecessor writes or reads, and before it exits,
+// so completion stays transitive along the stream; and it calls pdl_trigger()
+// only after its own pdl_wait() has returned.  So when a kernel starts, every
+// kernel before its predecessor has completed: a prologue may read, before its
+// pdl_wait(), whatever only those earlier kernels wrote.  Both are no-ops for a
+// kernel launched without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -19,8 +19,8 @@ __device__ __forceinline__ void load8(const T* row, int64_t k, int K, float* f) 
 template <typename TA, typename TW>
 __global__ void __launch_bounds__(NT) k_gemm_simt(const TA* __restrict__ A, int64_t lda, const int* __restrict__ a_rows,
                                                   const TW* __restrict__ W, int M, int N, int K, EpiParams ep) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     __shared__ float As[BK][BM + 4];
     __shared__ float Ws[BK][BN + 4];
     const int tid = threadIdx.x;

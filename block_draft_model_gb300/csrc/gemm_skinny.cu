@@ -24,8 +24,8 @@ template <typename TW, typename TA, int MR>
 __global__ void __launch_bounds__(NT) k_skinny(const TA* __restrict__ A, int64_t lda, const int* __restrict__ a_rows,
                                                int a_row0, const TW* __restrict__ W, int M, int N, int K,
                                                int k_per_split, EpiParams ep, float* __restrict__ ws) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     constexpr int VE = Vec16<TW>::N;         // weight elements per 16-byte vector
     constexpr int KC = SMEM_FLOATS / MR;     // activation chunk (columns)
     __shared__ __align__(16) float As[MR * KC];
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(NT) k_skinny(const TA* __restrict__ A, int64_t
 
 // Fixed-order sum of the split-K partials, then the epilogue.
 __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M, int N, EpiParams ep) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int64_t total = (int64_t)M * N;
     const bool pairs = ep.kind == EPI_SWIGLU;
     const int64_t items = pairs ? total / 2 : total;

@@ -32,8 +32,8 @@ constexpr int GMAX_CHAIN = 16; // largest block size (key words per sequence)
 
 template <typename TW>
 __global__ void __launch_bounds__(NT) k_markov(MarkovParams p) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     constexpr int VE = Vec16<TW>::N;
     __shared__ __align__(16) float e[RMAX];
     __shared__ float red_v[NT / 32];
@@ -860,8 +860,8 @@ cudaError_t res_attr(int bytes) {
 template <typename TW>
 __global__ void k_markov_gather(const TW* __restrict__ w1, int r, int V, const int* __restrict__ anchors,
                                 const int* __restrict__ tokens, int gamma, int k, TW* __restrict__ E) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     int prev = k == 0 ? anchors[b] : tokens[b * gamma + k - 1];
     prev = min(max(prev, 0), V - 1);
@@ -875,8 +875,8 @@ __global__ void __launch_bounds__(NT) k_markov_finish(const float* __restrict__ 
                                                       const float* __restrict__ y, const float* __restrict__ conf_w,
                                                       const int* __restrict__ anchors, int* tokens, float* conf,
                                                       int gamma, int k, int d, int r, int V, int* err) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     __shared__ float red_v[NT / 32];
     __shared__ int red_i[NT / 32];
     __shared__ float redf[32];

@@ -16,8 +16,8 @@ template <typename TO>
 __global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x, int64_t ldx,
                                                      const float* __restrict__ w, int n, float eps, TO* out,
                                                      int64_t ldo) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     __shared__ float red[32];
     const float* xr = x + (int64_t)blockIdx.x * ldx;
     float ss = 0.f;
@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
                                                          const float* __restrict__ ctx_norm,
                                                          const float* const* __restrict__ attn_norm, int n_layers,
                                                          TO* out, int64_t layer_stride, int rows_per_warp) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int nv = d / 4;
     const int lane = threadIdx.x & 31;
     const int row0 = (blockIdx.x * INW + (threadIdx.x >> 5)) * rows_per_warp;
@@ -116,8 +116,8 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
 }
 
 __global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc, int B, int gamma, int d) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int64_t total = (int64_t)B * gamma * d, per = (int64_t)gamma * d;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
         x[i] = bc[i % per];
@@ -126,8 +126,8 @@ __global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc
 __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int total,
                                 const int* __restrict__ seq_len, int max_seqs, int max_ctx, int* row_seq, int* row_pos,
                                 int* err) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
         // sequence i with cu[i] <= t < cu[i+1] (binary search over the prefix sums)
         int lo = 0, hi = n_seqs - 1;
@@ -157,8 +157,8 @@ __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __re
 
 __global__ void k_ingest_commit(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int* seq_len,
                                 int max_seqs, int max_ctx) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_seqs; i += gridDim.x * blockDim.x) {
         const int sid = seq_ids[i];
         if (sid < 0 || sid >= max_seqs) continue;
@@ -168,16 +168,16 @@ __global__ void k_ingest_commit(const int* __restrict__ seq_ids, const int* __re
 }
 
 __global__ void k_add_len(int* seq_len, int slot, int delta) {
-    pdl_trigger();
-    pdl_wait(); seq_len[slot] += delta; }
+    pdl_wait();
+    pdl_trigger(); seq_len[slot] += delta; }
 __global__ void k_set_len(int* seq_len, int slot, int value) {
-    pdl_trigger();
-    pdl_wait(); seq_len[slot] = value; }
+    pdl_wait();
+    pdl_trigger(); seq_len[slot] = value; }
 
 __global__ void k_check_draft(const int* __restrict__ seq_ids, const int* __restrict__ anchors, int n, int max_seqs,
                               int V, int* err, int* safe_ids, int* safe_anchors) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const int sid = seq_ids[i];
         const bool bad_id = sid < 0 || sid >= max_seqs;
@@ -192,8 +192,8 @@ __global__ void k_check_draft(const int* __restrict__ seq_ids, const int* __rest
 template <typename T>
 __global__ void k_block_const(const T* __restrict__ mask_emb, const T* __restrict__ block_pos, int gamma, int d,
                               float* __restrict__ out) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < gamma * d; i += gridDim.x * blockDim.x) {
         const int j = i / d;
         float v = to_f32(block_pos[i]);
@@ -204,8 +204,8 @@ __global__ void k_block_const(const T* __restrict__ mask_emb, const T* __restric
 
 template <typename T>
 __global__ void k_to_float(const T* __restrict__ in, int64_t n, float* __restrict__ out) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = to_f32(in[i]);
 }

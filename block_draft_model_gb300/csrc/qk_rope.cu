@@ -81,8 +81,8 @@ __device__ __forceinline__ void head_norm_rope(T* v, int hd, const float* w, flo
 // rows), the rest K heads of the block row in this layer's cache at position len + j.
 template <typename TC>
 __global__ void __launch_bounds__(32) k_qk_block(QkRope a) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x, head = blockIdx.y;
     const int b = m / a.gamma, j = m - b * a.gamma;
     const int slot = a.seq_ids ? a.seq_ids[b] : b;
@@ -102,8 +102,8 @@ __global__ void __launch_bounds__(32) k_qk_block(QkRope a) {
 // row_pos[m] (or len[slot] + m, the length before it moves).
 template <typename TC>
 __global__ void __launch_bounds__(32) k_qk_ingest(QkRope a) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x, kvh = blockIdx.y, layer = blockIdx.z;
     const int slot = a.row_seq ? a.row_seq[m] : 0;
     if (slot < 0) return;

@@ -183,8 +183,8 @@ __device__ __forceinline__ uint32_t sample_slot(const SampleParams& p, int b) {
 
 template <typename TW>
 __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     constexpr int VE = Vec16<TW>::N;
     __shared__ __align__(16) float e[RMAX_S];
     __shared__ unsigned long long keys[ROWS_MAX];
@@ -279,8 +279,8 @@ __global__ void __launch_bounds__(NT_L) k_sample_logits(SampleParams p) {
 
 template <typename TW>
 __global__ void __launch_bounds__(NT_P) k_sample_pick(SampleParams p, int ctas) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     extern __shared__ unsigned long long words[];  // [ctas * cand_stride]
     __shared__ KthShared ks;
     __shared__ unsigned long long red[32];

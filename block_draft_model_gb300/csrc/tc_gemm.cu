@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_trigger();
     pdl_wait();  // operands and outputs are shared with earlier kernels of the stream
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(wide::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {

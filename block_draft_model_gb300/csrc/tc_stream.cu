@@ -130,7 +130,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    pdl_trigger();
     if (warp == 0) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
@@ -144,6 +143,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 tma_load_2d(sW + i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0);
             }
             pdl_wait();
+            pdl_trigger();
             for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * X_BYTES, &tmX, &full[i], (kb0 + i) * BK, 0);
             int stage = pre % STAGES;
             uint32_t phase = pre == STAGES ? 1u : 0u;
@@ -159,10 +159,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         } else {
             pdl_wait();
+            pdl_trigger();
         }
         __syncwarp();  // lane 0 rejoins its warp before the CTA-wide barrier
     } else if (warp == 1) {
         pdl_wait();
+        pdl_trigger();
         if (lane == 0) {
             const uint32_t id = idesc(BM, BN);
             int stage = 0;
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
     } else {
         pdl_wait();  // the epilogue reads and writes buffers shared with earlier kernels
+        pdl_trigger();
         if (xpre_on) {
             const int t = threadIdx.x - 64, rps = BM / splits;
 #pragma unroll
