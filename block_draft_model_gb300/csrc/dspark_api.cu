@@ -168,6 +168,10 @@ struct dspark_handle {
     // CUDA graphs of the draft step
     bool use_graphs = true;
     cudaStream_t cap_stream = nullptr;
+    // side branch of the step: work that no launch on the main stream waits for right away
+    // (forked from and joined back into the main stream with the two events)
+    cudaStream_t side_stream = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     std::vector<DraftGraph> graphs;
     uint64_t graph_clock = 0;
     std::vector<ProfRange>* cap_ranges = nullptr;  // set while capturing
@@ -743,7 +747,17 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
                                  WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F, res, st));
             }
         }
-        {
+        if (chain) {
+            // out_proj takes its norm through the chain; y (the confidence head's input) is needed
+            // only by the Markov launch, so it is computed on a side branch beside out_proj
+            CUDA_TRY(h, cudaEventRecord(h->ev_fork, st));
+            CUDA_TRY(h, cudaStreamWaitEvent(h->side_stream, h->ev_fork, 0));
+            {
+                Prof pr(h, CAT_NORM, h->side_stream);
+                CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, h->side_stream));
+            }
+            CUDA_TRY(h, cudaEventRecord(h->ev_join, h->side_stream));
+        } else {
             Prof pr(h, CAT_NORM, st);
             CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
         }
@@ -755,6 +769,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             if (chain) {
                 CUDA_TRY(h, chained_gemm(h, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep, st,
                                          CAT_OUT_PROJ));
+                CUDA_TRY(h, cudaStreamWaitEvent(st, h->ev_join, 0));
             } else if (lowp) {
                 // norm_gemm opens its own normalisation and projection ranges
                 CUDA_TRY(h, norm_gemm(h, h->out_norm, R, WView{h->out_proj, &h->tc_out_proj, &h->ts_out_proj}, V, d, ep,
@@ -1106,6 +1121,9 @@ void dspark_destroy(dspark_handle* h) {
     if (h->stage_out.p) cudaFree(h->stage_out.p);
     for (auto& g : h->graphs) destroy_graph(g);
     if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+    if (h->side_stream) cudaStreamDestroy(h->side_stream);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
     tc_release(h->tc_wc);
     tc_release(h->tc_out_proj);
@@ -1324,6 +1342,9 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         }
     }
     CTRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+    CTRY(cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking));
+    CTRY(cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming));
+    CTRY(cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming));
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));
     CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
     h->ws_floats = (size_t)4 << 20;
