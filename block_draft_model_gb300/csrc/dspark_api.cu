@@ -254,7 +254,9 @@ cudaError_t gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, cons
     if (M <= 16 && wv.ts && wv.ts->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_stream_ok(M, N, K))
         return tc_stream((const char*)A + (size_t)a_row0 * lda * 2, lda, *wv.ts, M, N, K, ep, h->ts_part,
                          h->ts_part_floats, h->ts_tickets, h->ts_n_tickets, h->num_sms, h->d_err, st);
-    if (ep.ssp) return cudaErrorInvalidValue;  // only the weight-streaming epilogue hands over the next operand
+    // only the weight-streaming epilogues (tensor-core, and the SIMT one of a single row) hand over the
+    // next operand
+    if (ep.ssp && !(M <= 16 && skinny_ok(M, K))) return cudaErrorInvalidValue;
     if (M <= 16 && skinny_ok(M, K))
         return gemm_skinny(a_dtype, A, lda, a_rows, a_row0, h->dt, W, M, N, K, ep, h->ws, h->ws_floats, h->num_sms, st);
     if (tcw && tcw->ready && a_dtype == DT_BF16 && a_rows == nullptr && tc_wide_preferred(M, N, h->num_sms) &&
@@ -593,12 +595,24 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     }
     if (!one_launch) {
         Prof pr_block(h, CAT_BLOCK, st);
-        CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st));
+        const bool lowp0 = h->dt == DT_BF16;
+        // one sequence: the block build also writes layer 0's chained operand (bf16(x * attn_norm) and
+        // the 8-column sums of x^2), so the first QKV projection needs no normalisation launch
+        const bool chain0 = B == 1 && !seq_ids && norm_chain_ok(h, R, lowp0) && d % 8 == 0 && h->ws &&
+                            h->ws_floats >= 2 * (size_t)d && !(h->tc_tok_proj.ready && B >= 8);
+        CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st, chain0 ? h->xb : nullptr,
+                               chain0 ? h->attn_norm[0] : nullptr, chain0 ? h->ssp : nullptr));
         {
             EpiParams ep;
             ep.kind = EPI_ADD_F32;
             ep.out_f32 = h->x;
             ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
+            if (chain0) {
+                ep.xb = h->xb;
+                ep.ld_xb = d;
+                ep.ssp = h->ssp;
+                ep.xb_g = h->attn_norm[0];
+            }
             if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
                 // many sequences: gather the anchor embeddings, then one tensor-core GEMM
                 CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
@@ -673,7 +687,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             qkv.gamma = c.gamma;
             qkv.seq_ids = seq_ids;
             const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
-            if (chain && i > 0)
+            if (chain && (i > 0 || chain0))
                 CUDA_TRY(h, chained_gemm(h, R, wqkv, d + 2 * h->dkv, d, qkv, st, CAT_QKV));
             else
                 CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, d + 2 * h->dkv, d, qkv, actA, adt, st, CAT_QKV));

@@ -147,7 +147,22 @@ __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M,
             const int m = (int)(it / N), n = (int)(it - (int64_t)m * N);
             float v = 0.f;
             for (int s = 0; s < splits; ++s) v += ws[(int64_t)s * total + it];
-            epi_one(ep, m, n, v);
+            if (ep.ssp) {
+                // EPI_ADD_F32 of one row (M = 1, N a multiple of 8) that also writes the next projection's
+                // operand bf16(x * g) and the row's 8-column sums of x^2; whole 8-lane groups are active
+                float* px = ep.out_f32 + n;
+                const float x = *px + v;
+                *px = x;
+                reinterpret_cast<bf16*>(ep.xb)[n] = __float2bfloat16(x * ep.xb_g[n]);
+                float s2 = x * x;
+                const unsigned mask = __activemask();
+                s2 += __shfl_xor_sync(mask, s2, 1, 8);
+                s2 += __shfl_xor_sync(mask, s2, 2, 8);
+                s2 += __shfl_xor_sync(mask, s2, 4, 8);
+                if ((n & 7) == 0) ep.ssp[(n >> 3) * 16] = s2;
+            } else {
+                epi_one(ep, m, n, v);
+            }
         }
     }
 }
@@ -161,6 +176,7 @@ cudaError_t launch(const void* A, int64_t lda, const int* a_rows, int a_row0, co
     const int want = 4 * num_sms;
     while (row_ctas * splits < want && K / (splits * 2) >= 512 && splits < 32) splits *= 2;
     while (splits > 1 && (size_t)splits * M * N > ws_floats) splits /= 2;
+    if (ep.ssp && splits == 1) splits = 2;  // the chained operand is written by the reduce
     int kps = (K + splits - 1) / splits;
     kps = (kps + 7) / 8 * 8;
     splits = (K + kps - 1) / kps;
@@ -195,6 +211,9 @@ cudaError_t gemm_skinny(int a_dtype, const void* A, int64_t lda, const int* a_ro
                         int num_sms, cudaStream_t st) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (!skinny_ok(M, K)) return cudaErrorInvalidValue;
+    // the chained operand: one row, an added residual, whole 8-column groups, and a reduce to write it
+    if (ep.ssp && (M != 1 || ep.kind != EPI_ADD_F32 || N % 8 != 0 || K < 16 || !ws || ws_floats < 2 * (size_t)N))
+        return cudaErrorInvalidValue;
     if (w_dtype == DT_BF16) {
         if (a_dtype == DT_BF16)
             return dispatch_m<bf16, bf16>(A, lda, a_rows, a_row0, W, M, N, K, ep, ws, ws_floats, num_sms, st);

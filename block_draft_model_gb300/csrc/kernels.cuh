@@ -90,7 +90,10 @@ cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int ro
                         void* out, int64_t layer_stride, cudaStream_t st);
 
 // x[b * gamma + j] = block_const[j] for b < B, j < gamma (fp32).
-cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st);
+// x = the block rows of every sequence; with xb (one sequence only) also the first projection's
+// chained operand: xb = bf16(x * g) and the 8-column sums of x^2 (the layout of EpiParams::ssp).
+cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st,
+                       void* xb = nullptr, const float* g = nullptr, float* ssp = nullptr);
 // block_const[0] = block_pos[0]; block_const[j] = mask_emb[j-1] + block_pos[j] (fp32 out).
 cudaError_t block_const_init(int dtype, const void* mask_emb, const void* block_pos, int gamma, int d, float* out,
                              cudaStream_t st);

@@ -115,12 +115,27 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
     }
 }
 
-__global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc, int B, int gamma, int d) {
+// x = the block rows; with xb set (one sequence, d a multiple of 8) also the first projection's
+// operand xb = bf16(x * g) and the 8-column sums of x^2, ssp[(n / 8) * 16 + row].
+__global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc, int B, int gamma, int d,
+                             bf16* __restrict__ xb, const float* __restrict__ g, float* __restrict__ ssp) {
     pdl_wait();
     pdl_trigger();
     const int64_t total = (int64_t)B * gamma * d, per = (int64_t)gamma * d;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
-        x[i] = bc[i % per];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = bc[i % per];
+        x[i] = v;
+        if (xb) {  // whole 8-lane groups are active together: total and the strides are multiples of 8
+            const int row = (int)(i / d), n = (int)(i - (int64_t)row * d);
+            xb[i] = __float2bfloat16(v * g[n]);
+            float s2 = v * v;
+            const unsigned mask = __activemask();
+            s2 += __shfl_xor_sync(mask, s2, 1, 8);
+            s2 += __shfl_xor_sync(mask, s2, 2, 8);
+            s2 += __shfl_xor_sync(mask, s2, 4, 8);
+            if ((n & 7) == 0) ssp[(n >> 3) * 16 + row] = s2;
+        }
+    }
 }
 
 __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int total,
@@ -295,10 +310,13 @@ cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int ro
                                 layer_stride, st);
 }
 
-cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st) {
+cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st, void* xb_,
+                       const float* g, float* ssp) {
+    bf16* xb = static_cast<bf16*>(xb_);
+    if (xb && (B != 1 || gamma > 16 || d % 8 != 0 || !g || !ssp)) return cudaErrorInvalidValue;
     int64_t total = (int64_t)B * gamma * d;
     int blocks = (int)std::min<int64_t>((total + 255) / 256, 1024);
-    launch(k_block_init, blocks, 256, 0, st, x, block_const, B, gamma, d);
+    launch(k_block_init, blocks, 256, 0, st, x, block_const, B, gamma, d, xb, g, ssp);
     note_launch();
     return cudaGetLastError();
 }
