@@ -39,6 +39,8 @@ constexpr int NW = 4;       // warps per CTA, 16 keys of each tile per warp
 constexpr int NT = NW * 32;
 constexpr int GMAX = 16;    // queries per block (the M of the MMA)
 constexpr int CMAX = 128;   // largest number of key ranges per (sequence, head)
+constexpr int CL_MAX_TILES = 6;  // longest ranges (in 64-key tiles) merged as a cluster; longer ones keep the
+                                 // deep ring and the ticketed merge, which their length amortises
 constexpr int RFAST = 12;   // up to this many ranges the last CTA merges in one pass per thread
 static_assert(NT == GMAX * 8, "the merge gives each query eight threads");
 
@@ -55,6 +57,8 @@ struct TLayout {
     static constexpr int OW = 0;                            // [NW][GMAX][OWS] fp32
     static constexpr int ML = OW + NW * GMAX * OWS * 4;     // [NW][GMAX] m, then [NW][GMAX] l
     static_assert(ML + 2 * NW * GMAX * 4 <= BYTES, "warp merge buffers must fit in the tile ring");
+    //   the cluster form: this range's partial [GMAX][PW] (m, l, 2 unused, o[HD]), read by the cluster
+    static constexpr int CP = ML + 2 * NW * GMAX * 4;
     //   the last CTA's merge of the ranges, staged piece by piece: per query the
     //   piece's range weights, the running (max, sum, rescale), then the partials
     static constexpr int PW = HD + 4;                       // partial row: m, l, 2 unused, o[HD] (16-byte rows)
@@ -62,6 +66,7 @@ struct TLayout {
     static constexpr int MJ = WM + GMAX * CMAX * 4;         // [GMAX] running max, [GMAX] sum, [GMAX] rescale
     static constexpr int STG = MJ + 4 * GMAX * 4;           // staged partials (16-byte aligned)
     static_assert(STG + GMAX * PW * 4 <= BYTES, "one range of partials must fit beside the merge state");
+    static_assert(CP + GMAX * PW * 4 <= BYTES, "the cluster partial must fit in the tile ring");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
@@ -141,7 +146,29 @@ __device__ __forceinline__ void load_kv(uint32_t dst, const bf16* Kb, const bf16
     }
 }
 
-template <int HD, typename TO, int NS>
+// CL: the key ranges of one (sequence, head) are the CTAs of one thread-block cluster (grid.x =
+// cluster size = n_chunks <= 16) and merge through distributed shared memory: no partials in global
+// memory, no ticket, no restaging by a last CTA.
+__device__ __forceinline__ void cluster_sync_release_acquire() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t laddr, int rank) {
+    uint32_t ra;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(laddr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t laddr, int rank) {
+    uint32_t ra;
+    float4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(laddr), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra)
+                 : "memory");
+    return v;
+}
+
+template <int HD, typename TO, int NS, bool CL>
 __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     using L = TLayout<HD, NS>;
     constexpr int KS = HD / 16;  // 16-wide k steps of Q K^T; pairs of 8-wide output tiles of P V
@@ -168,13 +195,14 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     const int per = (n_keys + p.n_chunks - 1) / p.n_chunks;
     const int chunk = (per + TK - 1) / TK * TK;
     const int n_real = (n_keys + chunk - 1) / chunk;
-    if (c >= n_real) {
+    if (!CL && c >= n_real) {
         pdl_wait();
         pdl_trigger();
         return;
     }
+    // (in the cluster form a CTA past the last range stays for the cluster barriers, with no keys)
     const int start = c * chunk, end = min(n_keys, start + chunk);
-    const int n_tiles = (end - start + TK - 1) / TK;
+    const int n_tiles = c < n_real ? (end - start + TK - 1) / TK : 0;
 
     // K/V head of query head h, and the cache row width (grouped-query attention shares one K/V head
     // between n_heads / n_kv_heads query heads)
@@ -324,6 +352,56 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
 
     constexpr int w = L::PW;
     const int64_t bh = (int64_t)b * p.n_heads + h;
+    if (CL && n_real > 1) {
+        // this range's partial into shared memory, then the cluster merges every range's partial
+        float* cp = reinterpret_cast<float*>(sm + L::CP);
+        for (int i = tid; i < gamma * (HD / 4); i += NT) {
+            const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+            float M = -INFINITY;
+#pragma unroll
+            for (int v = 0; v < NW; ++v) M = fmaxf(M, Mw[v * GMAX + j]);
+            float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int v = 0; v < NW; ++v) {
+                const float mv = Mw[v * GMAX + j];
+                const float wt = mv == -INFINITY ? 0.f : ex2(mv - M);
+                l += wt * Lw[v * GMAX + j];
+                const float4 ov = *reinterpret_cast<const float4*>(Ow + (v * GMAX + j) * L::OWS + e);
+                acc[0] += wt * ov.x;
+                acc[1] += wt * ov.y;
+                acc[2] += wt * ov.z;
+                acc[3] += wt * ov.w;
+            }
+            *reinterpret_cast<float4*>(cp + j * w + 4 + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (e == 0) *reinterpret_cast<float2*>(cp + j * w) = make_float2(M, l);
+        }
+        cluster_sync_release_acquire();  // every range's partial is written and visible to the cluster
+        const uint32_t cpa = (uint32_t)__cvta_generic_to_shared(cp);
+        for (int i = c * NT + tid; i < gamma * (HD / 4); i += (int)gridDim.x * NT) {
+            const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
+            float M = -INFINITY;
+            for (int q = 0; q < n_real; ++q) M = fmaxf(M, ld_cluster_f32(cpa + j * w * 4, q));
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            for (int q = 0; q < n_real; ++q) {
+                const float mq = ld_cluster_f32(cpa + j * w * 4, q);
+                const float lq = ld_cluster_f32(cpa + (j * w + 1) * 4, q);
+                const float4 x = ld_cluster_f32x4(cpa + (j * w + 4 + e) * 4, q);
+                const float wt = mq == -INFINITY ? 0.f : ex2(mq - Ms);
+                l = fmaf(wt, lq, l);
+                a0 = fmaf(wt, x.x, a0);
+                a1 = fmaf(wt, x.y, a1);
+                a2 = fmaf(wt, x.z, a2);
+                a3 = fmaf(wt, x.w, a3);
+            }
+            const float inv = 1.f / l;  // every range holds at least one key, so the sum is >= 1
+            store4<TO>(out + (int64_t)j * d + e, a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+        }
+        // no CTA leaves while another may still read its partial
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+        return;
+    }
+    if (CL && c >= n_real) return;  // one range: the first CTA writes the output on its own
     float* part = p.part + (bh * p.n_chunks + c) * gamma * w;
     for (int i = tid; i < gamma * (HD / 4); i += NT) {
         const int j = i / (HD / 4), e = (i % (HD / 4)) * 4;
@@ -519,11 +597,19 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
 
 template <int HD, typename TO, int NS>
 cudaError_t set_attr_tc() {
-    return cudaFuncSetAttribute(k_attention_tc<HD, TO, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TLayout<HD, NS>::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_attention_tc<HD, TO, NS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TLayout<HD, NS>::BYTES);
+    if (e != cudaSuccess || NS != 3) return e;
+    e = cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TLayout<HD, 3>::BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 int g_num_sms = 0;
+// largest key-range count launched as one cluster (0: the cluster form is off); set at init from
+// how many clusters of that size the device can hold at once
+int g_cluster_max = 0;
 
 template <int HD, typename TO>
 void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
@@ -531,10 +617,28 @@ void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
     // where the ranges are long enough to use it.  Ranges of a few tiles keep the 3-stage ring, so
     // that the next kernel's CTAs (launched early, programmatic dependent launch) fit beside them.
     const int per_range = p.max_keys > 0 ? (p.max_keys + (int)grid.x * TK - 1) / ((int)grid.x * TK) : 1 << 30;
-    if ((int)(grid.x * grid.y * grid.z) <= g_num_sms && per_range > 2)
-        launch(k_attention_tc<HD, TO, 6>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
-    else
-        launch(k_attention_tc<HD, TO, 3>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);
+    if (grid.x >= 2 && (int)grid.x <= g_cluster_max && per_range <= CL_MAX_TILES) {
+        // the ranges of one (sequence, head) as one cluster, merged through distributed shared memory
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = grid.x;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = TLayout<HD, 3>::BYTES;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl_enabled() ? 2 : 1;
+        cudaLaunchKernelEx(&cfg, k_attention_tc<HD, TO, 3, true>, p);
+    } else if ((int)(grid.x * grid.y * grid.z) <= g_num_sms && per_range > 2) {
+        launch(k_attention_tc<HD, TO, 6, false>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
+    } else {
+        launch(k_attention_tc<HD, TO, 3, false>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);
+    }
 }
 
 }  // namespace
@@ -544,6 +648,12 @@ bool attention_tc_ok(int cache_dtype, int head_dim, int gamma) {
 }
 
 int attention_tc_max_chunks() { return CMAX; }
+
+int attention_tc_cluster_chunks(int max_keys) {
+    if (g_cluster_max < 2) return 0;
+    const int per_range = (max_keys + g_cluster_max * TK - 1) / (g_cluster_max * TK);
+    return per_range <= CL_MAX_TILES ? g_cluster_max : 0;
+}
 
 cudaError_t attention_tc_init() {
     cudaError_t e;
@@ -557,7 +667,30 @@ cudaError_t attention_tc_init() {
     if ((e = set_attr_tc<64, bf16, 6>()) != cudaSuccess) return e;
     if ((e = set_attr_tc<64, float, 6>()) != cudaSuccess) return e;
     if ((e = set_attr_tc<128, bf16, 6>()) != cudaSuccess) return e;
-    return set_attr_tc<128, float, 6>();
+    if ((e = set_attr_tc<128, float, 6>()) != cudaSuccess) return e;
+    // the largest cluster of the short-range form that the device can hold (16, else the portable 8)
+    g_cluster_max = 0;
+    for (int n : {16, 8}) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = n;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n, 1, 1);
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = TLayout<128, 3>::BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, k_attention_tc<128, float, 3, true>, &cfg) == cudaSuccess &&
+            clusters >= 1) {
+            g_cluster_max = n;
+            break;
+        }
+    }
+    (void)cudaGetLastError();  // a refused probe leaves nothing behind
+    return cudaSuccess;
 }
 
 cudaError_t attention_tc(const AttnParams& p, cudaStream_t st) {

@@ -228,7 +228,13 @@ int attn_chunks(const dspark_handle* h, int B, int max_keys) {
     const int pairs = nh * B;
     int want = pairs <= h->num_sms ? h->num_sms / pairs : (12 * h->num_sms + pairs - 1) / pairs;
     int by_keys = (max_keys + 63) / 64;
-    return std::max(1, std::min(std::min(want, by_keys), attn_max_chunks(h->dt, h->hd, h->cfg.gamma)));
+    int n = std::max(1, std::min(std::min(want, by_keys), attn_max_chunks(h->dt, h->hd, h->cfg.gamma)));
+    // short enough ranges merge inside a thread-block cluster, which holds at most so many of them
+    if (h->dt == DT_BF16 && attention_tc_ok(h->dt, h->hd, h->cfg.gamma)) {
+        const int cl = attention_tc_cluster_chunks(max_keys);
+        if (cl >= 2 && n > cl) n = cl;
+    }
+    return n;
 }
 
 // A weight and its tensor-core views.

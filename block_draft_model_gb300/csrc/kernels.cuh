@@ -130,6 +130,9 @@ cudaError_t attention_init();  // once per process/device, before any launch or 
 cudaError_t attention(const AttnParams& p, cudaStream_t st);
 bool attention_tc_ok(int cache_dtype, int head_dim, int gamma);
 int attention_tc_max_chunks();
+// The key-range count at which the tensor-core attention merges the ranges of a (sequence, head) as
+// one thread-block cluster, for sequences of up to max_keys keys; 0 when that form does not apply.
+int attention_tc_cluster_chunks(int max_keys);
 cudaError_t attention_tc_init();
 cudaError_t attention_tc(const AttnParams& p, cudaStream_t st);
 

@@ -361,15 +361,20 @@ def test_markov_chain_few_sequences(n_seq, rank, vocab, form):
                         label=f"one sequence, launch {rep}")
 
 
-@pytest.mark.parametrize("ctx", [700, 1500, 1800])
-def test_bf16_attention_many_key_ranges(ctx):
+# (context rows, capacity): the capacity bounds the keys the host plans the key ranges for, the
+# actual length sizes them on the device.  Two heads: 16 ranges merged inside a thread-block cluster
+# (707 and 1807 keys), 76 ranges with 8 of them filled (the one-pass merge by the last CTA) and 63 of
+# them filled (the piecewise merge, several staged pieces).
+ATTN_RANGES = [(700, 1900), (1800, 1900), (500, 8000), (7990, 8000)]
+
+
+@pytest.mark.parametrize("ctx,cap", ATTN_RANGES)
+def test_bf16_attention_many_key_ranges(ctx, cap):
     """head_dim 128, two heads: the keys of each head are split over many CTAs
-    (64-key tiles, a ragged last tile) and merged by the last one: 707 keys give
-    12 ranges (the one-pass merge), 1507 keys 24 and 1807 keys 29 (the piecewise
-    merge, in one staged piece and in several)."""
+    (64-key tiles, a ragged last tile) and merged, in each of the three forms."""
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=7,
                             vocab=1000, markov_rank=64)
-    _small(cfg, ctx, seed=12, chunks=[700], anchors=[4, 998], max_ctx=1900)
+    _small(cfg, ctx, seed=12, chunks=[700], anchors=[4, 998], max_ctx=cap)
 
 
 def test_host_checked_errors():
