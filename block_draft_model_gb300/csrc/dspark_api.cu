@@ -93,6 +93,10 @@ struct dspark_handle {
     TcWeight tc_wc, tc_out_proj;             // tensor-core views (bf16 only), rows >= 17
     std::vector<TcWeight> tc_kv, tc_qkv, tc_wo, tc_wgu, tc_wd;
     TcWeight tc_kv_a, tc_kv_w;               // every layer's ingest K/V product as one grouped GEMM (A: Nbuf)
+    // the same product with each layer's attn_norm folded into its K/V weights: A is one copy of
+    // RMSNorm(H_ctx) shared by every layer (tc_kv_a2, 2-D) and the weights are bf16([W_k; W_v] * g)
+    void* wkv_s = nullptr;                   // [n_layers][2 d_kv][d] bf16
+    TcWeight tc_kv_a2, tc_kv_ws;
     TcWeightStream ts_wc, ts_out_proj;       // weight-streaming tensor-core views, rows <= 16
     std::vector<TcWeightStream> ts_kv, ts_qkv, ts_wo, ts_wgu, ts_wd;
     float* ts_part = nullptr;                // split-K partials of the streaming GEMM
@@ -489,13 +493,17 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
             }
         }
         const int lp = h->dt;  // normalised rows in the storage type (bf16 feeds the tensor cores)
+        const bool grouped = n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * h->dkv, d);
+        // the attn_norm rides on the scaled K/V weights: one normalised copy serves every layer
+        const bool shared = grouped && h->tc_kv_ws.ready && h->tc_kv_a2.ready128;
         {
             Prof pr(h, CAT_INGEST_NORM, st);
-            CUDA_TRY(h, ingest_norm(h->P, ks, (int64_t)n * d, n, d, h->cfg.eps, h->ctx_norm, h->attn_norm_dev, nL, lp,
-                                    h->Nbuf, (int64_t)h->ingest_rows * d, st));
+            CUDA_TRY(h, ingest_norm(h->P, ks, (int64_t)n * d, n, d, h->cfg.eps, h->ctx_norm,
+                                    shared ? nullptr : h->attn_norm_dev, shared ? 1 : nL, lp, h->Nbuf,
+                                    (int64_t)h->ingest_rows * d, st));
         }
         Prof pr_kv(h, CAT_INGEST_KV, st);
-        if (n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * h->dkv, d)) {
+        if (grouped) {
             // all layers in one launch: [nL x row tiles x column tiles] work units
             EpiParams kv = cache_epi(h, 0);
             kv.kind = EPI_KV_CACHE;
@@ -504,7 +512,11 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
                 kv.row_seq = row_seq + t0;
                 kv.row_pos = row_pos + t0;
             }
-            CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * h->dkv, d, kv, h->num_sms, h->d_err, st));
+            if (shared)
+                CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a2, h->tc_kv_ws, nL, n, 2 * h->dkv, d, kv, h->num_sms, h->d_err, st,
+                                            true));
+            else
+                CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * h->dkv, d, kv, h->num_sms, h->d_err, st));
             CUDA_TRY(h, ingest_qk(h, n, row_seq ? row_seq + t0 : nullptr, row_seq ? row_pos + t0 : nullptr, st));
             if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
             continue;
@@ -1390,6 +1402,13 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
                 tc_prepare_grouped(h->tc_kv_a, h->Nbuf, nL, (int64_t)h->ingest_rows * d, h->ingest_rows, d, true);
                 tc_prepare_grouped(h->tc_kv_w, (char*)h->wqkv[0] + (size_t)d * d * es, nL,
                                    (int64_t)(d + 2 * dkv) * d, 2 * dkv, d, false);
+                // attn_norm folded into the ingest K/V weights (the grouped product's shared-operand form)
+                CTRY(dalloc(h, &h->wkv_s, (size_t)nL * 2 * dkv * d * es));
+                for (int l = 0; l < nL; ++l)
+                    CTRY(scale_cols((char*)h->wqkv[l] + (size_t)d * d * es, h->attn_norm[l], 2 * dkv, d,
+                                    (char*)h->wkv_s + (size_t)l * 2 * dkv * d * es, st));
+                tc_prepare_grouped(h->tc_kv_ws, h->wkv_s, nL, (int64_t)2 * dkv * d, 2 * dkv, d, false);
+                CTRY(tc_prepare(h->tc_kv_a2, h->Nbuf, h->ingest_rows, d));
             }
             CTRY(tc_prepare(h->tc_qkv[i], h->wqkv[i], d + 2 * dkv, d));
             CTRY(tc_prepare(h->tc_wo[i], h->wo[i], d, d));

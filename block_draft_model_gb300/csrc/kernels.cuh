@@ -92,6 +92,8 @@ cudaError_t ingest_norm(const float* P, int nsplit, int64_t split_stride, int ro
 // x[b * gamma + j] = block_const[j] for b < B, j < gamma (fp32).
 // x = the block rows of every sequence; with xb (one sequence only) also the first projection's
 // chained operand: xb = bf16(x * g) and the 8-column sums of x^2 (the layout of EpiParams::ssp).
+// Wd = bf16(W * g) column-wise: W, Wd bf16 [rows, K], g fp32 [K] (the attn_norm folded into weights).
+cudaError_t scale_cols(const void* W, const float* g, int rows, int K, void* Wd, cudaStream_t st);
 cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int d, cudaStream_t st,
                        void* xb = nullptr, const float* g = nullptr, float* ssp = nullptr);
 // block_const[0] = block_pos[0]; block_const[j] = mask_emb[j-1] + block_pos[j] (fp32 out).

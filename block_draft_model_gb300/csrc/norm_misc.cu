@@ -100,6 +100,15 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
         }
         ss2 = warp_sum(ss2);
         const float s2 = rsqrtf(ss2 / (float)d + eps);
+        if (!attn_norm) {  // one copy without a norm weight (the weights carry each layer's attn_norm)
+            TO* o = out + (int64_t)row * d;
+#pragma unroll
+            for (int i = 0; i < MAXV; ++i) {
+                const int v = lane + 32 * i;
+                if (v < nv) store4(o + 4 * v, h[i].x * s2, h[i].y * s2, h[i].z * s2, h[i].w * s2);
+            }
+            continue;
+        }
         for (int l = 0; l < n_layers; ++l) {
             const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
             TO* o = out + l * layer_stride + (int64_t)row * d;
@@ -136,6 +145,15 @@ __global__ void k_block_init(float* __restrict__ x, const float* __restrict__ bc
             if ((n & 7) == 0) ssp[(n >> 3) * 16 + row] = s2;
         }
     }
+}
+
+// Wd[r][k] = bf16(W[r][k] * g[k]) for r < rows, k < K (both bf16, K contiguous).
+__global__ void k_scale_cols(const bf16* __restrict__ W, const float* __restrict__ g, int rows, int K, bf16* __restrict__ Wd) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t total = (int64_t)rows * K;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+        Wd[i] = __float2bfloat16(__bfloat162float(W[i]) * g[i % K]);
 }
 
 __global__ void k_ingest_rowmap(const int* __restrict__ seq_ids, const int* __restrict__ cu, int n_seqs, int total,
@@ -317,6 +335,14 @@ cudaError_t block_init(float* x, const float* block_const, int B, int gamma, int
     int64_t total = (int64_t)B * gamma * d;
     int blocks = (int)std::min<int64_t>((total + 255) / 256, 1024);
     launch(k_block_init, blocks, 256, 0, st, x, block_const, B, gamma, d, xb, g, ssp);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t scale_cols(const void* W, const float* g, int rows, int K, void* Wd, cudaStream_t st) {
+    if (rows <= 0 || K <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>(((int64_t)rows * K + 255) / 256, 4096);
+    launch(k_scale_cols, blocks, 256, 0, st, (const bf16*)W, g, rows, K, (bf16*)Wd);
     note_launch();
     return cudaGetLastError();
 }

@@ -48,6 +48,7 @@ struct TileMap {
     int ks;      // K ranges per output tile (consecutive work units)
     int groups;  // independent problems of the same shape (third map coordinate = group)
     int map3d;   // the tensor maps are 3-D (grouped launches, also with one group)
+    int a2d;     // grouped launch whose A is one 2-D matrix shared by every group
     __device__ __forceinline__ void at(int t, int& m0, int& n0, int& s, int& g) const {
         const int per = nM * nN * ks;
         g = t / per;
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
                     if (tm.map3d) {
-                        tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0, g);
+                        if (tm.a2d) tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
+                        else tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0, g);
                         tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0, g);
                     } else {
                         tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
@@ -565,9 +567,10 @@ bool tc_prepare_grouped(TcWeight& w, const void* ptr, int groups, int64_t group_
 }
 
 cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, int M, int N, int K, const EpiParams& ep,
-                            int num_sms, int* err, cudaStream_t st) {
+                            int num_sms, int* err, cudaStream_t st, bool a_shared) {
     if (!a.ready || !w.ready || groups < 1 || !tc_gemm_ok(M, N, K) || M > a.N || N > w.N || K != w.K || K != a.K)
         return cudaErrorInvalidValue;
+    if (a_shared && !a.ready128) return cudaErrorInvalidValue;
     TileMap tm;
     tm.nM = (M + BM - 1) / BM;
     tm.nN = (N + BN - 1) / BN;
@@ -575,9 +578,11 @@ cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, in
     tm.ks = 1;
     tm.groups = groups;
     tm.map3d = 1;
+    tm.a2d = a_shared ? 1 : 0;
     const int tiles = tm.nM * tm.nN * groups;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, *reinterpret_cast<const CUtensorMap*>(a.tmap),
+    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st,
+           *reinterpret_cast<const CUtensorMap*>(a_shared ? a.tmap128 : a.tmap),
            *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
     note_launch();
     return cudaGetLastError();
@@ -669,6 +674,7 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.ks = ksplit;
     tm.groups = 1;
     tm.map3d = 0;
+    tm.a2d = 0;
     const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
     launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);

@@ -33,8 +33,9 @@ bool tc_gemm_ok(int M, int N, int K);
 // tc_prepare_grouped (a_side: 128-row boxes of A, else 256-row boxes of W); the
 // EPI_KV_CACHE epilogue of group g writes at ep.cache + g * ep.group_stride.
 bool tc_prepare_grouped(TcWeight& w, const void* ptr, int groups, int64_t group_stride, int rows, int K, bool a_side);
+// a_shared: A is one 2-D matrix (a made by tc_prepare, its 128-row boxes) read by every group.
 cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, int M, int N, int K, const EpiParams& ep,
-                            int num_sms, int* err, cudaStream_t st);
+                            int num_sms, int* err, cudaStream_t st, bool a_shared = false);
 // A: [M, K] bf16 with row stride lda (16-byte aligned).  A bounded device wait
 // that gives up sets bit 16 of *err (the handle's device error word).
 // ksplit > 1 (EPI_STORE_F32 only) cuts K into ksplit ranges, each a separate
