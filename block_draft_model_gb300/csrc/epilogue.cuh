@@ -105,17 +105,38 @@ __device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int
 // steps, halving the columns each time) leaves in lane l the best of the
 // warp's 32 rows for sequence nb + l: larger value, then lower index.  Called
 // by all 32 lanes; vrow - lane is the warp's first row, a multiple of 32.
-__device__ __forceinline__ void markov_t32(const EpiParams& ep, int vrow, bool valid, int nb, int N, const float* acc) {
-    const int lane = threadIdx.x & 31;
-    float val[32];
-    int idx[32];
-    // all 32 loads first: a logits store between them would have to wait for
-    // the load before it (the compiler cannot rule out that the buffers overlap)
+// The base logits of markov_t32: u[j] = U[(nb + j) * gamma + k][vrow] (0 where absent).  They do not
+// depend on the accumulators, so a caller may issue them before the accumulators are ready.
+__device__ __forceinline__ void markov_u32_load(const EpiParams& ep, int vrow, bool valid, int nb, int N, float* u) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const bool ok = valid && nb + j < N;
         const int64_t row = (int64_t)(nb + j) * ep.gamma + ep.mk_k;
-        val[j] = ok ? acc[j] + __ldcs(ep.mk_U + row * ep.ldo + vrow) : -INFINITY;
+        u[j] = ok ? __ldcs(ep.mk_U + row * ep.ldo + vrow) : 0.f;
+    }
+}
+
+// markov_t32 with the base logits already loaded (u from markov_u32_load).
+__device__ __forceinline__ void markov_t32_u(const EpiParams& ep, int vrow, bool valid, int nb, int N, const float* acc,
+                                             const float* u);
+
+__device__ __forceinline__ void markov_t32(const EpiParams& ep, int vrow, bool valid, int nb, int N, const float* acc) {
+    // all 32 loads first: a logits store between them would have to wait for
+    // the load before it (the compiler cannot rule out that the buffers overlap)
+    float u[32];
+    markov_u32_load(ep, vrow, valid, nb, N, u);
+    markov_t32_u(ep, vrow, valid, nb, N, acc, u);
+}
+
+__device__ __forceinline__ void markov_t32_u(const EpiParams& ep, int vrow, bool valid, int nb, int N, const float* acc,
+                                             const float* u) {
+    const int lane = threadIdx.x & 31;
+    float val[32];
+    int idx[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const bool ok = valid && nb + j < N;
+        val[j] = ok ? acc[j] + u[j] : -INFINITY;
         idx[j] = ok ? vrow : INT_MAX;
     }
     if (ep.mk_logits) {

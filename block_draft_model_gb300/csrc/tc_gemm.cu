@@ -68,7 +68,11 @@ struct TileMap {
     }
 };
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// MK: the instance for EPI_MARKOV_T, with eight epilogue warps (two per TMEM lane quarter, taking
+// alternate 32-column chunks) that issue their chunk's base-logit loads before the accumulator is ready.
+constexpr int NTHREADS_MK = 320;
+template <bool MK>
+__global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               TileMap tm, EpiParams ep, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], MK ? 8 : 4);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -195,6 +199,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         __syncwarp();
+    } else if constexpr (MK) {
+        // epilogue warps 2..9: TMEM lanes 32*(warp % 4) .. +31 (vocabulary rows), chunks half, half + 2, ...
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        int buf = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            int m0, n0, s, g;
+            tm.at(t, m0, n0, s, g);
+            const int row = m0 + q * 32 + lane;
+            const bool rows_in = m0 + q * 32 < M;  // warp-uniform
+            const int nb0 = n0 + half * 32;
+            float u[32];
+            // the base logits of the first chunk do not wait for the accumulator
+            if (rows_in && nb0 < N) markov_u32_load(ep, row, row < M, nb0, N, u);
+            if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+            for (int c = half; c < BN / 32; c += 2) {
+                const int nb = n0 + c * 32;
+                if (nb >= N) break;  // columns past N were not multiplied
+                uint32_t r[32];
+                tmem_ld32(base + c * 32, r);
+                if (rows_in) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (c != half) markov_u32_load(ep, row, row < M, nb, N, u);
+                    markov_t32_u(ep, row, row < M, nb, N, v, u);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (++buf == 2) {
+                buf = 0;
+                acc_phase ^= 1u;
+            }
+        }
     } else {
         // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31
         const int q = warp & 3;
@@ -524,7 +567,10 @@ bool init_encode() {
             return false;
         g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
     }
-    if (cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) !=
+            cudaSuccess)
         return false;
     if (cudaFuncSetAttribute(k_tc_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM_MAX) != cudaSuccess)
         return false;
@@ -581,7 +627,7 @@ cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, in
     tm.a2d = a_shared ? 1 : 0;
     const int tiles = tm.nM * tm.nN * groups;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st,
+    launch(k_tc_gemm<false>, grid, NTHREADS, smem_bytes(), st,
            *reinterpret_cast<const CUtensorMap*>(a_shared ? a.tmap128 : a.tmap),
            *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
     note_launch();
@@ -677,7 +723,12 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.a2d = 0;
     const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    launch(k_tc_gemm, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
+    if (ep.kind == EPI_MARKOV_T)
+        launch(k_tc_gemm<true>, grid, NTHREADS_MK, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
+               N, K, tm, ep, err);
+    else
+        launch(k_tc_gemm<false>, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
+               N, K, tm, ep, err);
     note_launch();
     return cudaGetLastError();
 }
