@@ -105,6 +105,32 @@ __device__ __forceinline__ void cache_store32(const EpiParams& ep, int slot, int
 // steps, halving the columns each time) leaves in lane l the best of the
 // warp's 32 rows for sequence nb + l: larger value, then lower index.  Called
 // by all 32 lanes; vrow - lane is the warp's first row, a multiple of 32.
+// Reduce-scatter over the warp's lanes (5 exchange steps, halving the columns each time): lane l
+// holds the best of the 32 lanes' column-l entries in val[0] / idx[0] (larger value, then lower
+// index).  Called by all 32 lanes.
+__device__ __forceinline__ void markov_reduce_scatter(float* val, int* idx) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;  // keep columns [w, 2w), else [0, w)
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float sv = upper ? val[i] : val[i + w];
+            const int si = upper ? idx[i] : idx[i + w];
+            float kv = upper ? val[i + w] : val[i];
+            int ki = upper ? idx[i + w] : idx[i];
+            const float ov = __shfl_xor_sync(0xffffffffu, sv, w);
+            const int oi = __shfl_xor_sync(0xffffffffu, si, w);
+            if (better(ov, oi, kv, ki)) {
+                kv = ov;
+                ki = oi;
+            }
+            val[i] = kv;
+            idx[i] = ki;
+        }
+    }
+}
+
 // The base logits of markov_t32: u[j] = U[(nb + j) * gamma + k][vrow] (0 where absent).  They do not
 // depend on the accumulators, so a caller may issue them before the accumulators are ready.
 __device__ __forceinline__ void markov_u32_load(const EpiParams& ep, int vrow, bool valid, int nb, int N, float* u) {
@@ -144,25 +170,7 @@ __device__ __forceinline__ void markov_t32_u(const EpiParams& ep, int vrow, bool
         for (int j = 0; j < 32; ++j)
             if (valid && nb + j < N) ep.mk_logits[((int64_t)(nb + j) * ep.gamma + ep.mk_k) * ep.ldo + vrow] = val[j];
     }
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool upper = (lane & w) != 0;  // keep columns [w, 2w), else [0, w)
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-            const float sv = upper ? val[i] : val[i + w];
-            const int si = upper ? idx[i] : idx[i + w];
-            float kv = upper ? val[i + w] : val[i];
-            int ki = upper ? idx[i + w] : idx[i];
-            const float ov = __shfl_xor_sync(0xffffffffu, sv, w);
-            const int oi = __shfl_xor_sync(0xffffffffu, si, w);
-            if (better(ov, oi, kv, ki)) {
-                kv = ov;
-                ki = oi;
-            }
-            val[i] = kv;
-            idx[i] = ki;
-        }
-    }
+    markov_reduce_scatter(val, idx);
     if (nb + lane < N) {
         const int64_t o = (int64_t)(nb + lane) * ep.mk_nch + ((vrow - lane) >> 5);
         ep.mk_part_v[o] = val[0];

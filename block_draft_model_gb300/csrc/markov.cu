@@ -881,15 +881,29 @@ __global__ void __launch_bounds__(NT) k_markov_finish(const float* __restrict__ 
     __shared__ int red_i[NT / 32];
     __shared__ float redf[32];
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ArgBest best{-INFINITY, INT_MAX};
-    for (int c = threadIdx.x; c < nchunks; c += NT) {
-        const float v = part_v[(int64_t)b * nchunks + c];
-        const int i = part_i[(int64_t)b * nchunks + c];
-        if (better(v, i, best.v, best.i)) {
-            best.v = v;
-            best.i = i;
+    // four independent running bests, so that the partials' loads are in flight together
+    ArgBest bq[4] = {{-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}};
+    const float* pv = part_v + (int64_t)b * nchunks;
+    const int* pi = part_i + (int64_t)b * nchunks;
+    int c = threadIdx.x;
+    for (; c + 3 * NT < nchunks; c += 4 * NT) {
+        float v[4];
+        int i[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = pv[c + q * NT];
+            i[q] = pi[c + q * NT];
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (better(v[q], i[q], bq[q].v, bq[q].i)) bq[q] = ArgBest{v[q], i[q]};
     }
+    for (; c < nchunks; c += NT)
+        if (better(pv[c], pi[c], bq[0].v, bq[0].i)) bq[0] = ArgBest{pv[c], pi[c]};
+    ArgBest best = bq[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q)
+        if (better(bq[q].v, bq[q].i, best.v, best.i)) best = bq[q];
     best = warp_argbest(best);
     if (lane == 0) {
         red_v[warp] = best.v;

@@ -130,6 +130,16 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 int m0, n0, s, g;
                 tm.at(t, m0, n0, s, g);
+                if constexpr (MK) {
+                    // the tile's base-logit rows into L2, a tile ahead of the epilogue that reads them
+                    const int span = (min(M, m0 + BM) - m0) * 4 & ~15;
+                    if (span > 0 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.mk_U & 15) == 0)
+                        for (int j = n0; j < min(N, n0 + BN); ++j)
+                            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                             ep.mk_U + ((int64_t)j * ep.gamma + ep.mk_k) * ep.ldo + m0),
+                                         "r"(span)
+                                         : "memory");
+                }
                 const int kb1 = (s + 1) * nkb / tm.ks;
                 for (int kb = s * nkb / tm.ks; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
