@@ -41,6 +41,12 @@ using namespace tc;
 constexpr int STG_LD = 36;
 constexpr int STG_BYTES = 4 * 32 * STG_LD * 4;
 constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + 256 + STG_BYTES; }
+// The EPI_MARKOV_T instance: B (the <= 128 sequences) in 128-row stages, and per epilogue warp two 32 x 32
+// fp32 buffers of base logits, filled by cp.async a tile ahead of their use.
+constexpr int BN_MK = 128;
+constexpr int B_BYTES_MK = BN_MK * BK * 2;      // 16 KB
+constexpr int UBUF_BYTES = 32 * 32 * 4;         // one warp's 32 sequences x 32 vocabulary rows
+constexpr size_t smem_bytes_mk() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES_MK) + 256 + 8 * 2 * UBUF_BYTES; }
 
 struct TileMap {
     int nM, nN;
@@ -49,6 +55,7 @@ struct TileMap {
     int groups;  // independent problems of the same shape (third map coordinate = group)
     int map3d;   // the tensor maps are 3-D (grouped launches, also with one group)
     int a2d;     // grouped launch whose A is one 2-D matrix shared by every group
+    int bn;      // columns per tile
     __device__ __forceinline__ void at(int t, int& m0, int& n0, int& s, int& g) const {
         const int per = nM * nN * ks;
         g = t / per;
@@ -64,7 +71,7 @@ struct TileMap {
             mi = t - ni * nM;
         }
         m0 = mi * BM;
-        n0 = ni * BN;
+        n0 = ni * bn;
     }
 };
 
@@ -79,8 +86,10 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sA = smem_u32(smem);
+    constexpr int BNk = MK ? BN_MK : BN;
+    constexpr int B_BYTESk = BNk * BK * 2;
     const uint32_t sB = sA + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTESk));
     uint64_t* full = bars;                      // [STAGES]
     uint64_t* empty = bars + STAGES;            // [STAGES]
     uint64_t* acc_full = bars + 2 * STAGES;     // [2]
@@ -88,7 +97,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
     uint64_t* drain = bars + 2 * STAGES + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* stage_f32 = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 256);
+    float* stage_f32 = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTESk) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = tm.nM * tm.nN * tm.ks * tm.groups;
@@ -134,7 +143,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                     // the tile's base-logit rows into L2, a tile ahead of the epilogue that reads them
                     const int span = (min(M, m0 + BM) - m0) * 4 & ~15;
                     if (span > 0 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.mk_U & 15) == 0)
-                        for (int j = n0; j < min(N, n0 + BN); ++j)
+                        for (int j = n0; j < min(N, n0 + BNk); ++j)
                             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
                                              ep.mk_U + ((int64_t)j * ep.gamma + ep.mk_k) * ep.ldo + m0),
                                          "r"(span)
@@ -146,14 +155,14 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTESk);
                     if (tm.map3d) {
                         if (tm.a2d) tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
                         else tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0, g);
-                        tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0, g);
+                        tma_load_3d(sB + stage * B_BYTESk, &tmB, &full[stage], kb * BK, n0, g);
                     } else {
                         tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
-                        tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
+                        tma_load_2d(sB + stage * B_BYTESk, &tmB, &full[stage], kb * BK, n0);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -176,8 +185,8 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                 const int kb0 = s * nkb / tm.ks, kb1 = (s + 1) * nkb / tm.ks;
                 // a narrow last (or only) column tile multiplies only its 16-aligned width
                 const int n_rem = N - n0;
-                const uint32_t id = idesc(BM, n_rem >= BN ? BN : (n_rem + 15) & ~15);
-                const uint32_t d_tmem = tmem + buf * BN;
+                const uint32_t id = idesc(BM, n_rem >= BNk ? BNk : (n_rem + 15) & ~15);
+                const uint32_t d_tmem = tmem + buf * BNk;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
@@ -185,7 +194,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                     }
                     tc_fence_after();
                     const uint64_t da = sdesc(sA + stage * A_BYTES);
-                    const uint64_t db = sdesc(sB + stage * B_BYTES);
+                    const uint64_t db = sdesc(sB + stage * B_BYTESk);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)  // +32 bytes per 16-wide K slice inside the swizzled row
                         umma(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > kb0 || k) ? 1u : 0u);
@@ -211,32 +220,59 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
         __syncwarp();
     } else if constexpr (MK) {
         // epilogue warps 2..9: TMEM lanes 32*(warp % 4) .. +31 (vocabulary rows), chunks half, half + 2, ...
+        // The base logits of the warp's first chunk come through its two shared-memory buffers, copied a
+        // tile ahead (cp.async, 16-byte pieces): tile t's block is [32 sequences][32 vocabulary rows].
         const int q = warp & 3, half = (warp - 2) >> 2;
-        int buf = 0;
+        float* ub = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTESk) + 256) + (warp - 2) * 2 * 1024;
+        const bool cp_ok = (ep.ldo & 3) == 0 && ((uintptr_t)ep.mk_U & 15) == 0;
+        auto fill = [&](int t, float* dst) {
+            int m0, n0, s, g;
+            tm.at(t, m0, n0, s, g);
+            const int nb0 = n0 + half * 32, c0 = m0 + q * 32;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // 256 pieces: sequence j = piece / 8, columns 4 * (piece % 8) ..
+                const int pc = lane + 32 * i, j = pc >> 3, col = c0 + (pc & 7) * 4;
+                const int bytes = nb0 + j < N && col < M ? min(4, M - col) * 4 : 0;
+                const float* src = bytes ? ep.mk_U + ((int64_t)(nb0 + j) * ep.gamma + ep.mk_k) * ep.ldo + col : ep.mk_U;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + j * 32 + (pc & 7) * 4)),
+                             "l"(src), "r"(bytes)
+                             : "memory");
+            }
+        };
+        int buf = 0, it = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        if (cp_ok && (int)blockIdx.x < tiles) fill(blockIdx.x, ub);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            __syncwarp();  // every lane is done with the buffer the next copy overwrites
+            if (cp_ok && t + (int)gridDim.x < tiles) fill(t + gridDim.x, ub + ((it + 1) & 1) * 1024);
+            asm volatile("cp.async.commit_group;" ::: "memory");
             int m0, n0, s, g;
             tm.at(t, m0, n0, s, g);
             const int row = m0 + q * 32 + lane;
             const bool rows_in = m0 + q * 32 < M;  // warp-uniform
-            const int nb0 = n0 + half * 32;
-            float u[32];
-            // the base logits of the first chunk do not wait for the accumulator
-            if (rows_in && nb0 < N) markov_u32_load(ep, row, row < M, nb0, N, u);
+            const float* us = ub + (it & 1) * 1024;
             if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) break;
             tc_fence_after();
-            const uint32_t base = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's block (the next may be in flight)
+            __syncwarp();
+            const uint32_t base = tmem + buf * BNk + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-            for (int c = half; c < BN / 32; c += 2) {
+            for (int c = half; c < BNk / 32; c += 2) {
                 const int nb = n0 + c * 32;
                 if (nb >= N) break;  // columns past N were not multiplied
                 uint32_t r[32];
                 tmem_ld32(base + c * 32, r);
                 if (rows_in) {
-                    float v[32];
+                    float v[32], u[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if (c != half) markov_u32_load(ep, row, row < M, nb, N, u);
+                    if (c == half && cp_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) u[j] = us[j * 32 + lane];
+                    } else {
+                        markov_u32_load(ep, row, row < M, nb, N, u);
+                    }
                     markov_t32_u(ep, row, row < M, nb, N, v, u);
                 }
             }
@@ -248,6 +284,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the kernel
     } else {
         // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31
         const int q = warp & 3;
@@ -579,7 +616,7 @@ bool init_encode() {
     }
     if (cudaFuncSetAttribute(k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) !=
+        cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_mk()) !=
             cudaSuccess)
         return false;
     if (cudaFuncSetAttribute(k_tc_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM_MAX) != cudaSuccess)
@@ -630,6 +667,7 @@ cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, in
     TileMap tm;
     tm.nM = (M + BM - 1) / BM;
     tm.nN = (N + BN - 1) / BN;
+    tm.bn = BN;
     tm.n_fast = tm.nN <= tm.nM;
     tm.ks = 1;
     tm.groups = groups;
@@ -723,9 +761,13 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     if (lda % 8 != 0 || ((uintptr_t)A & 15) != 0) return cudaErrorInvalidValue;
     CUtensorMap tmA;
     if (!encode(&tmA, A, M, K, lda, BM)) return cudaErrorInvalidValue;
+    // the Markov instance takes B (the sequences) in 128-row tiles through the 128-row-box map
+    const bool mk = ep.kind == EPI_MARKOV_T;
+    if (mk && !w.ready128) return cudaErrorInvalidValue;
     TileMap tm;
+    tm.bn = mk ? BN_MK : BN;
     tm.nM = (M + BM - 1) / BM;
-    tm.nN = (N + BN - 1) / BN;
+    tm.nN = (N + tm.bn - 1) / tm.bn;
     tm.n_fast = tm.nN <= tm.nM;
     tm.ks = ksplit;
     tm.groups = 1;
@@ -733,9 +775,9 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     tm.a2d = 0;
     const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    if (ep.kind == EPI_MARKOV_T)
-        launch(k_tc_gemm<true>, grid, NTHREADS_MK, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
-               N, K, tm, ep, err);
+    if (mk)
+        launch(k_tc_gemm<true>, grid, NTHREADS_MK, smem_bytes_mk(), st, tmA,
+               *reinterpret_cast<const CUtensorMap*>(w.tmap128), M, N, K, tm, ep, err);
     else
         launch(k_tc_gemm<false>, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
                N, K, tm, ep, err);
