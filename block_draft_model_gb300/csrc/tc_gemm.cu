@@ -46,7 +46,8 @@ constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTE
 constexpr int BN_MK = 128;
 constexpr int B_BYTES_MK = BN_MK * BK * 2;      // 16 KB
 constexpr int UBUF_BYTES = 32 * 32 * 4;         // one warp's 32 sequences x 32 vocabulary rows
-constexpr size_t smem_bytes_mk() { return 1024 + (size_t)STAGES * (A_BYTES + B_BYTES_MK) + 256 + 8 * 2 * UBUF_BYTES; }
+constexpr int STAGES_MK = 4;
+constexpr size_t smem_bytes_mk() { return 1024 + (size_t)STAGES_MK * (A_BYTES + B_BYTES_MK) + 256 + 8 * 2 * UBUF_BYTES; }
 
 struct TileMap {
     int nM, nN;
@@ -87,24 +88,25 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sA = smem_u32(smem);
     constexpr int BNk = MK ? BN_MK : BN;
+    constexpr int STAGESk = MK ? STAGES_MK : STAGES;
     constexpr int B_BYTESk = BNk * BK * 2;
-    const uint32_t sB = sA + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTESk));
-    uint64_t* full = bars;                      // [STAGES]
-    uint64_t* empty = bars + STAGES;            // [STAGES]
-    uint64_t* acc_full = bars + 2 * STAGES;     // [2]
-    uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
-    uint64_t* drain = bars + 2 * STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    const uint32_t sB = sA + STAGESk * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGESk * (A_BYTES + B_BYTESk));
+    uint64_t* full = bars;                      // [STAGESk]
+    uint64_t* empty = bars + STAGESk;            // [STAGESk]
+    uint64_t* acc_full = bars + 2 * STAGESk;     // [2]
+    uint64_t* acc_empty = bars + 2 * STAGESk + 2;  // [2]
+    uint64_t* drain = bars + 2 * STAGESk + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGESk + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* stage_f32 = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTESk) + 256);
+    float* stage_f32 = reinterpret_cast<float*>(smem + STAGESk * (A_BYTES + B_BYTESk) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = tm.nM * tm.nN * tm.ks * tm.groups;
     const int nkb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < STAGESk; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                         tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
                         tma_load_2d(sB + stage * B_BYTESk, &tmB, &full[stage], kb * BK, n0);
                     }
-                    if (++stage == STAGES) {
+                    if (++stage == STAGESk) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                     for (int k = 0; k < BK / 16; ++k)  // +32 bytes per 16-wide K slice inside the swizzled row
                         umma(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > kb0 || k) ? 1u : 0u);
                     umma_commit(&empty[stage]);
-                    if (++stage == STAGES) {
+                    if (++stage == STAGESk) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
         // The base logits of the warp's first chunk come through its two shared-memory buffers, copied a
         // tile ahead (cp.async, 16-byte pieces): tile t's block is [32 sequences][32 vocabulary rows].
         const int q = warp & 3, half = (warp - 2) >> 2;
-        float* ub = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTESk) + 256) + (warp - 2) * 2 * 1024;
+        float* ub = reinterpret_cast<float*>(smem + STAGESk * (A_BYTES + B_BYTESk) + 256) + (warp - 2) * 2 * 1024;
         const bool cp_ok = (ep.ldo & 3) == 0 && ((uintptr_t)ep.mk_U & 15) == 0;
         auto fill = [&](int t, float* dst) {
             int m0, n0, s, g;
