@@ -26,6 +26,17 @@ __device__ __forceinline__ void cache_store(const EpiParams& ep, int slot, int p
         reinterpret_cast<float*>(ep.cache)[off] = v;
 }
 
+// EPI_QKV for one element: Q columns to out_f32, K/V columns into the cache after the context.
+__device__ __forceinline__ void epi_qkv(const EpiParams& ep, int m, int n, float v) {
+    if (n < ep.d) {
+        ep.out_f32[(int64_t)m * ep.ldo + n] = v;
+    } else {
+        int b = m / ep.gamma, j = m - b * ep.gamma;
+        int slot = ep.seq_ids ? ep.seq_ids[b] : b;
+        if (slot >= 0) cache_store(ep, slot, ep.seq_len[slot] + j, n - ep.d, v);
+    }
+}
+
 // One output element (every kind except EPI_SWIGLU).
 __device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float v, int grp = 0) {
     switch (ep.kind) {
@@ -41,19 +52,22 @@ __device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float
             cache_store(ep, slot, pos, n, v, grp);
             break;
         }
-        case EPI_QKV: {
-            if (n < ep.d) {
-                ep.out_f32[(int64_t)m * ep.ldo + n] = v;
-            } else {
-                int b = m / ep.gamma, j = m - b * ep.gamma;
-                int slot = ep.seq_ids ? ep.seq_ids[b] : b;
-                if (slot >= 0) cache_store(ep, slot, ep.seq_len[slot] + j, n - ep.d, v);
-            }
+        case EPI_QKV:
+            epi_qkv(ep, m, n, v);
             break;
-        }
         default:
             break;
     }
+}
+
+// epi_one for a kernel instance compiled for one epilogue kind (EK >= 0; EK < 0: the kind of ep),
+// so that the instance carries only that kind's code.
+template <int EK>
+__device__ __forceinline__ void epi_one_k(const EpiParams& ep, int m, int n, float v) {
+    if constexpr (EK == EPI_STORE_F32) ep.out_f32[(int64_t)m * ep.ldo + n] = v;
+    else if constexpr (EK == EPI_ADD_F32) ep.out_f32[(int64_t)m * ep.ldo + n] += v;
+    else if constexpr (EK == EPI_QKV) epi_qkv(ep, m, n, v);
+    else if constexpr (EK < 0) epi_one(ep, m, n, v);
 }
 
 // A (gate, up) column pair of EPI_SWIGLU: columns 2f and 2f+1 give output f.

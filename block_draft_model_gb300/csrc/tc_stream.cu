@@ -78,6 +78,8 @@ __device__ __forceinline__ float epi_add_xb(const EpiParams& ep, int m, int n, f
 
 // grid: n_tiles * splits CTAs; CTA b handles tile b / splits, K blocks
 // [s * kb_per, min(nkb, (s + 1) * kb_per)) with s = b % splits.
+// EK: the epilogue kind the instance is compiled for (EK < 0: any, read from ep at run time).
+template <int EK>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_tc_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
                 int splits, int kb_per, int cluster_reduce, EpiParams ep, float* __restrict__ part,
@@ -97,11 +99,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float* rsc = reinterpret_cast<float*>(bars + 16);    // row scales [BN]
     float* rs_red = reinterpret_cast<float*>(bars + 32);  // row-sum partials [8][16]
     const bool rowscale = sn.ssp != nullptr;
-    const bool xbm = ep.ssp != nullptr;  // EPI_ADD_F32 that also writes the next operand and row sums
+    const int kind = EK >= 0 ? EK : ep.kind;
+    // EPI_ADD_F32 that also writes the next operand and row sums
+    const bool xbm = (EK < 0 || EK == EPI_ADD_F32) && ep.ssp != nullptr;
     // EPI_ADD_F32 reduced in the cluster: the residual entries this thread will own in the final
     // epilogue (at most two items of four activation rows), loaded while the weights stream; no other
     // thread of the kernel touches them
-    const bool xpre_on = splits > 1 && cluster_reduce && ep.kind == EPI_ADD_F32;
+    const bool xpre_on = splits > 1 && cluster_reduce && kind == EPI_ADD_F32;
     float xpre[2][4];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
         }
         if (final_ && have) {
-            if (ep.kind == EPI_SWIGLU) {
+            if (kind == EPI_SWIGLU) {
                 // (gate, up) rows are adjacent lanes: even lanes take their odd neighbour's value
 #pragma unroll
                 for (int m = 0; m < BN; ++m) {
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 for (int m = 0; m < BN; ++m)
                     if (m < M) {
                         if (xbm) v[m] = epi_add_xb(ep, m, n, v[m]);
-                        else epi_one(ep, m, n, v[m]);
+                        else epi_one_k<EK>(ep, m, n, v[m]);
                     }
             }
         }
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             // item are requested together, then added in split order
             const int t = threadIdx.x - 64;  // 0..127
             const int rps = BM / splits;
-            const bool swiglu = ep.kind == EPI_SWIGLU;
+            const bool swiglu = kind == EPI_SWIGLU;
             for (int it0 = 0; it0 < rps * 4; it0 += 128) {
                 const int it = it0 + t;
                 const bool mine = it < rps * 4;
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                                 } else if (xbm) {
                                     x2[q] = epi_add_xb(ep, 4 * cg + q, n, v4[q]);
                                 } else {
-                                    epi_one(ep, 4 * cg + q, n, v4[q]);
+                                    epi_one_k<EK>(ep, 4 * cg + q, n, v4[q]);
                                 }
                             }
                     }
@@ -433,8 +437,10 @@ bool ready() {
             return false;
         g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
     }
-    if (cudaFuncSetAttribute(k_tc_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
-        return false;
+    for (auto fn : {k_tc_stream<-1>, k_tc_stream<EPI_STORE_F32>, k_tc_stream<EPI_ADD_F32>, k_tc_stream<EPI_QKV>,
+                    k_tc_stream<EPI_SWIGLU>})
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
+            return false;
     g_ready[dev] = true;
     return true;
 }
@@ -470,6 +476,18 @@ cudaError_t mbar_wait_selftest(int* err, cudaStream_t st) {
     k_mbar_selftest<<<1, 32, 0, st>>>(err);
     note_launch();
     return cudaGetLastError();
+}
+
+// The instance for an epilogue kind: one per kind the step uses, so that each carries only its own
+// epilogue code (it runs once per launch, from a cold instruction cache); others take the generic one.
+decltype(&k_tc_stream<-1>) stream_kernel(int kind) {
+    switch (kind) {
+        case EPI_STORE_F32: return k_tc_stream<EPI_STORE_F32>;
+        case EPI_ADD_F32: return k_tc_stream<EPI_ADD_F32>;
+        case EPI_QKV: return k_tc_stream<EPI_QKV>;
+        case EPI_SWIGLU: return k_tc_stream<EPI_SWIGLU>;
+        default: return k_tc_stream<-1>;
+    }
 }
 
 bool tc_stream_ok(int M, int N, int K) { return ready() && M >= 1 && M <= BN && N >= 1 && K >= BK && K % 8 == 0; }
@@ -528,8 +546,8 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
                 cfg.stream = st;
                 cfg.attrs = attr;
                 cfg.numAttrs = pdl_enabled() ? 2 : 1;
-                cudaError_t e = cudaLaunchKernelEx(&cfg, k_tc_stream, tmW, tmX, M, N, K, cs, kbp, 1, ep, part, tickets,
-                                                   err, sn);
+                cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel(ep.kind), tmW, tmX, M, N, K, cs, kbp, 1, ep, part,
+                                                   tickets, err, sn);
                 note_launch();
                 if (e != cudaSuccess) return e;
                 return cudaGetLastError();
@@ -538,8 +556,8 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     }
     int kb_per = (nkb + splits - 1) / splits;
     splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
-    launch(k_tc_stream, nT * splits, NTHREADS, smem_bytes(), st, tmW, tmX, M, N, K, splits, kb_per, 0, ep, part,
-           tickets, err, sn);
+    launch(stream_kernel(ep.kind), nT * splits, NTHREADS, smem_bytes(), st, tmW, tmX, M, N, K, splits, kb_per, 0, ep,
+           part, tickets, err, sn);
     note_launch();
     return cudaGetLastError();
 }
