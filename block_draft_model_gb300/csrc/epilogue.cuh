@@ -70,6 +70,13 @@ __device__ __forceinline__ void epi_one_k(const EpiParams& ep, int m, int n, flo
     else if constexpr (EK < 0) epi_one(ep, m, n, v);
 }
 
+// epi_one_k with the group of a grouped launch (EPI_KV_CACHE).
+template <int EK>
+__device__ __forceinline__ void epi_one_kg(const EpiParams& ep, int m, int n, float v, int grp) {
+    if constexpr (EK == EPI_STORE_F32 || EK == EPI_ADD_F32 || EK == EPI_QKV) epi_one_k<EK>(ep, m, n, v);
+    else epi_one(ep, m, n, v, grp);
+}
+
 // A (gate, up) column pair of EPI_SWIGLU: columns 2f and 2f+1 give output f.
 __device__ __forceinline__ void epi_pair(const EpiParams& ep, int m, int n_even, float g, float u) {
     float h = act_fn(ep.act, g) * u;
@@ -192,14 +199,17 @@ __device__ __forceinline__ void markov_t32_u(const EpiParams& ep, int vrow, bool
     }
 }
 
-__device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v, int grp = 0) {
+// epi_row32 for a kernel instance compiled for one epilogue kind (EK >= 0; EK < 0: the kind of ep).
+template <int EK>
+__device__ __forceinline__ void epi_row32_k(const EpiParams& ep, int m, int n, int N, const float* v, int grp) {
+    const int kind = EK >= 0 ? EK : ep.kind;
     const bool full = n + 32 <= N;
-    switch (ep.kind) {
+    switch (kind) {
         case EPI_STORE_F32:
         case EPI_ADD_F32:
             if (full && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0) {
                 float* dst = ep.out_f32 + (int64_t)m * ep.ldo + n;
-                if (ep.kind == EPI_ADD_F32) {
+                if (kind == EPI_ADD_F32) {
                     float t[32];
                     const float4* s4 = reinterpret_cast<const float4*>(dst);
 #pragma unroll
@@ -271,15 +281,19 @@ __device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int
             return;
     }
     // unrolled so that v stays in registers
-    if (ep.kind == EPI_SWIGLU) {
+    if (kind == EPI_SWIGLU) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2)
             if (n + j + 1 < N) epi_pair(ep, m, n + j, v[j], v[j + 1]);
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (n + j < N) epi_one(ep, m, n + j, v[j], grp);
+            if (n + j < N) epi_one_kg<EK>(ep, m, n + j, v[j], grp);
     }
+}
+
+__device__ __forceinline__ void epi_row32(const EpiParams& ep, int m, int n, int N, const float* v, int grp = 0) {
+    epi_row32_k<-1>(ep, m, n, N, v, grp);
 }
 
 }  // namespace dspark

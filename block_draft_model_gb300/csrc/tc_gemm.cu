@@ -79,10 +79,14 @@ struct TileMap {
 // MK: the instance for EPI_MARKOV_T, with eight epilogue warps (two per TMEM lane quarter, taking
 // alternate 32-column chunks) that issue their chunk's base-logit loads before the accumulator is ready.
 constexpr int NTHREADS_MK = 320;
-template <bool MK>
-__global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
+// EK: the epilogue kind the instance is compiled for (EK < 0: any, read from ep at run time);
+// EPI_MARKOV_T is the instance MK described above.
+template <int EK>
+__global__ void __launch_bounds__(EK == EPI_MARKOV_T ? NTHREADS_MK : NTHREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               TileMap tm, EpiParams ep, int* err) {
+    constexpr bool MK = EK == EPI_MARKOV_T;
+    const int kind = EK >= 0 ? EK : ep.kind;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -293,11 +297,11 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
         int buf = 0;
         uint32_t acc_phase = 0;
         float* stg = stage_f32 + q * 32 * STG_LD;
-        const bool coalesce = ep.kind == EPI_STORE_F32 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0;
+        const bool coalesce = kind == EPI_STORE_F32 && (ep.ldo & 3) == 0 && ((uintptr_t)ep.out_f32 & 15) == 0;
         // bf16 K/V cache rows, 64 columns at a time (whole 128-byte lines); a 64-column pair never
         // straddles K and V when the cache row width is a multiple of 64
         const int kvw = ep.d_kv ? ep.d_kv : ep.d;
-        const bool kv16 = ep.kind == EPI_KV_CACHE && ep.cache_dtype == DT_BF16 && (kvw & 63) == 0 &&
+        const bool kv16 = kind == EPI_KV_CACHE && ep.cache_dtype == DT_BF16 && (kvw & 63) == 0 &&
                           ((uintptr_t)ep.cache & 15) == 0 && ((ep.seq_stride | ep.kv_off | ep.group_stride) & 7) == 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             int m0, n0, s, g;
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                                                        c4) = val;
                     }
                     __syncwarp();
-                } else if (ep.kind == EPI_MARKOV_T) {  // warp-wide: every lane takes part
+                } else if (EK < 0 && kind == EPI_MARKOV_T) {  // warp-wide: every lane takes part
                     if (m0 + q * 32 < M) {
                         float v[32];
 #pragma unroll
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(MK ? NTHREADS_MK : NTHREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi_row32(ep, orow, nb, N, v, g);
+                    epi_row32_k<EK>(ep, orow, nb, N, v, g);
                 }
             }
             tc_fence_before();
@@ -592,6 +596,19 @@ __global__ void __launch_bounds__(wide::NTHREADS, 1)
     }
 }
 
+// The instance for an epilogue kind (the Markov one is launched on its own): one per kind the path
+// uses, so that each carries only its own epilogue code; other kinds take the generic one.
+decltype(&k_tc_gemm<-1>) gemm_kernel(int kind) {
+    switch (kind) {
+        case EPI_STORE_F32: return k_tc_gemm<EPI_STORE_F32>;
+        case EPI_ADD_F32: return k_tc_gemm<EPI_ADD_F32>;
+        case EPI_QKV: return k_tc_gemm<EPI_QKV>;
+        case EPI_SWIGLU: return k_tc_gemm<EPI_SWIGLU>;
+        case EPI_KV_CACHE: return k_tc_gemm<EPI_KV_CACHE>;
+        default: return k_tc_gemm<-1>;
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Per device (the shared-memory attribute belongs to the device's context):
 // -1 unknown, 0 unavailable, 1 available.
@@ -616,10 +633,12 @@ bool init_encode() {
             return false;
         g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
     }
-    if (cudaFuncSetAttribute(k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_mk()) !=
-            cudaSuccess)
+    for (auto fn : {k_tc_gemm<-1>, k_tc_gemm<EPI_STORE_F32>, k_tc_gemm<EPI_ADD_F32>, k_tc_gemm<EPI_QKV>,
+                    k_tc_gemm<EPI_SWIGLU>, k_tc_gemm<EPI_KV_CACHE>})
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
+            return false;
+    if (cudaFuncSetAttribute(k_tc_gemm<EPI_MARKOV_T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes_mk()) != cudaSuccess)
         return false;
     if (cudaFuncSetAttribute(k_tc_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM_MAX) != cudaSuccess)
         return false;
@@ -677,7 +696,7 @@ cudaError_t tc_gemm_grouped(const TcWeight& a, const TcWeight& w, int groups, in
     tm.a2d = a_shared ? 1 : 0;
     const int tiles = tm.nM * tm.nN * groups;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    launch(k_tc_gemm<false>, grid, NTHREADS, smem_bytes(), st,
+    launch(gemm_kernel(ep.kind), grid, NTHREADS, smem_bytes(), st,
            *reinterpret_cast<const CUtensorMap*>(a_shared ? a.tmap128 : a.tmap),
            *reinterpret_cast<const CUtensorMap*>(w.tmap), M, N, K, tm, ep, err);
     note_launch();
@@ -778,10 +797,10 @@ cudaError_t tc_gemm(const void* A, int64_t lda, const TcWeight& w, int M, int N,
     const int tiles = tm.nM * tm.nN * ksplit;
     const int grid = tiles < num_sms ? tiles : num_sms;
     if (mk)
-        launch(k_tc_gemm<true>, grid, NTHREADS_MK, smem_bytes_mk(), st, tmA,
+        launch(k_tc_gemm<EPI_MARKOV_T>, grid, NTHREADS_MK, smem_bytes_mk(), st, tmA,
                *reinterpret_cast<const CUtensorMap*>(w.tmap128), M, N, K, tm, ep, err);
     else
-        launch(k_tc_gemm<false>, grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
+        launch(gemm_kernel(ep.kind), grid, NTHREADS, smem_bytes(), st, tmA, *reinterpret_cast<const CUtensorMap*>(w.tmap), M,
                N, K, tm, ep, err);
     note_launch();
     return cudaGetLastError();
