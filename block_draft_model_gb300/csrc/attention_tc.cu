@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         }
     }
     if (n_real == 1) return;
+    if constexpr (CL) return;  // (the cluster form has merged above; no ticketed merge in its code)
     // Ticket: after the barrier, one acquire-release atomic publishes this CTA's
     // partial (release, cumulative over the barrier) and, in the last CTA, makes
     // every other CTA's partial visible (acquire, passed on by the next barrier).

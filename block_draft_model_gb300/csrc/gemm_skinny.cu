@@ -126,12 +126,15 @@ __global__ void __launch_bounds__(NT) k_skinny(const TA* __restrict__ A, int64_t
     }
 }
 
-// Fixed-order sum of the split-K partials, then the epilogue.
+// Fixed-order sum of the split-K partials, then the epilogue.  ADD_XB: the instance for the one
+// row of a residual add that also hands over the next operand (only that code, which runs once
+// per launch from a cold instruction cache).
+template <bool ADD_XB>
 __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M, int N, EpiParams ep) {
     pdl_wait();
     pdl_trigger();
     const int64_t total = (int64_t)M * N;
-    const bool pairs = ep.kind == EPI_SWIGLU;
+    const bool pairs = !ADD_XB && ep.kind == EPI_SWIGLU;
     const int64_t items = pairs ? total / 2 : total;
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (int64_t)gridDim.x * blockDim.x) {
         if (pairs) {
@@ -147,7 +150,7 @@ __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M,
             const int m = (int)(it / N), n = (int)(it - (int64_t)m * N);
             float v = 0.f;
             for (int s = 0; s < splits; ++s) v += ws[(int64_t)s * total + it];
-            if (ep.ssp) {
+            if (ADD_XB) {
                 // EPI_ADD_F32 of one row (M = 1, N a multiple of 8) that also writes the next projection's
                 // operand bf16(x * g) and the row's 8-column sums of x^2; whole 8-lane groups are active
                 float* px = ep.out_f32 + n;
@@ -160,7 +163,7 @@ __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M,
                 s2 += __shfl_xor_sync(mask, s2, 2, 8);
                 s2 += __shfl_xor_sync(mask, s2, 4, 8);
                 if ((n & 7) == 0) ep.ssp[(n >> 3) * 16] = s2;
-            } else {
+            } else if constexpr (!ADD_XB) {
                 epi_one(ep, m, n, v);
             }
         }
@@ -187,7 +190,8 @@ cudaError_t launch(const void* A, int64_t lda, const int* a_rows, int a_row0, co
     if (e != cudaSuccess || splits == 1) return e;
     int64_t items = (int64_t)M * N;
     int blocks = (int)std::min<int64_t>((items + 255) / 256, 8 * num_sms);
-    launch(k_splitk_reduce, blocks, 256, 0, st, ws, splits, M, N, ep);
+    if (ep.ssp) launch(k_splitk_reduce<true>, blocks, 256, 0, st, ws, splits, M, N, ep);
+    else launch(k_splitk_reduce<false>, blocks, 256, 0, st, ws, splits, M, N, ep);
     note_launch();
     return cudaGetLastError();
 }
