@@ -50,7 +50,8 @@ __device__ __forceinline__ void store4(float* o, float a, float b, float c, floa
 // and many of them are resident at once.
 constexpr int INW = 4;  // warps per CTA
 
-template <typename TO, int MAXV>
+// ONE: the instance for one unweighted copy (attn_norm == nullptr), without the per-layer loop.
+template <typename TO, int MAXV, bool ONE>
 __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restrict__ P, int nsplit, int64_t split_stride,
                                                          int rows, int d, float eps,
                                                          const float* __restrict__ ctx_norm,
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
         }
         ss2 = warp_sum(ss2);
         const float s2 = rsqrtf(ss2 / (float)d + eps);
-        if (!attn_norm) {  // one copy without a norm weight (the weights carry each layer's attn_norm)
+        if (ONE) {  // one copy without a norm weight (the weights carry each layer's attn_norm)
             TO* o = out + (int64_t)row * d;
 #pragma unroll
             for (int i = 0; i < MAXV; ++i) {
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(INW * 32) k_ingest_norm(const float* __restric
             }
             continue;
         }
+        if constexpr (!ONE)
         for (int l = 0; l < n_layers; ++l) {
             const float4* an = reinterpret_cast<const float4*>(attn_norm[l]);
             TO* o = out + l * layer_stride + (int64_t)row * d;
@@ -296,8 +298,12 @@ cudaError_t launch_ingest_norm(const float* P, int nsplit, int64_t split_stride,
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int rpw = std::max(1, (rows + INW * 4 * sms - 1) / (INW * 4 * sms));
     const int blocks = (rows + INW * rpw - 1) / (INW * rpw);
-    launch(k_ingest_norm<TO, MAXV>, blocks, INW * 32, 0, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
-           attn_norm_dev, n_layers, (TO*)out, layer_stride, rpw);
+    if (attn_norm_dev)
+        launch(k_ingest_norm<TO, MAXV, false>, blocks, INW * 32, 0, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
+               attn_norm_dev, n_layers, (TO*)out, layer_stride, rpw);
+    else
+        launch(k_ingest_norm<TO, MAXV, true>, blocks, INW * 32, 0, st, P, nsplit, split_stride, rows, d, eps, ctx_norm,
+               attn_norm_dev, n_layers, (TO*)out, layer_stride, rpw);
     note_launch();
     return cudaGetLastError();
 }

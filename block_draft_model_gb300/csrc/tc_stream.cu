@@ -78,11 +78,12 @@ __device__ __forceinline__ float epi_add_xb(const EpiParams& ep, int m, int n, f
 
 // grid: n_tiles * splits CTAs; CTA b handles tile b / splits, K blocks
 // [s * kb_per, min(nkb, (s + 1) * kb_per)) with s = b % splits.
-// EK: the epilogue kind the instance is compiled for (EK < 0: any, read from ep at run time).
-template <int EK>
+// EK: the epilogue kind the instance is compiled for (EK < 0: any, read from ep at run time);
+// CLU: split-K partials reduced inside the cluster (else through scratch and tile tickets).
+template <int EK, bool CLU>
 __global__ void __launch_bounds__(NTHREADS, 2)
     k_tc_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
-                int splits, int kb_per, int cluster_reduce, EpiParams ep, float* __restrict__ part,
+                int splits, int kb_per, int cluster_reduce_arg, EpiParams ep, float* __restrict__ part,
                 unsigned int* __restrict__ tickets, int* err, StreamNorm sn) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -100,6 +101,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float* rs_red = reinterpret_cast<float*>(bars + 32);  // row-sum partials [8][16]
     const bool rowscale = sn.ssp != nullptr;
     const int kind = EK >= 0 ? EK : ep.kind;
+    constexpr bool cluster_reduce = CLU;
+    (void)cluster_reduce_arg;
     // EPI_ADD_F32 that also writes the next operand and row sums
     const bool xbm = (EK < 0 || EK == EPI_ADD_F32) && ep.ssp != nullptr;
     // EPI_ADD_F32 reduced in the cluster: the residual entries this thread will own in the final
@@ -437,8 +440,10 @@ bool ready() {
             return false;
         g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
     }
-    for (auto fn : {k_tc_stream<-1>, k_tc_stream<EPI_STORE_F32>, k_tc_stream<EPI_ADD_F32>, k_tc_stream<EPI_QKV>,
-                    k_tc_stream<EPI_SWIGLU>})
+    for (auto fn : {k_tc_stream<-1, false>, k_tc_stream<EPI_STORE_F32, false>, k_tc_stream<EPI_ADD_F32, false>,
+                    k_tc_stream<EPI_QKV, false>, k_tc_stream<EPI_SWIGLU, false>, k_tc_stream<-1, true>,
+                    k_tc_stream<EPI_STORE_F32, true>, k_tc_stream<EPI_ADD_F32, true>, k_tc_stream<EPI_QKV, true>,
+                    k_tc_stream<EPI_SWIGLU, true>})
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()) != cudaSuccess)
             return false;
     g_ready[dev] = true;
@@ -480,13 +485,14 @@ cudaError_t mbar_wait_selftest(int* err, cudaStream_t st) {
 
 // The instance for an epilogue kind: one per kind the step uses, so that each carries only its own
 // epilogue code (it runs once per launch, from a cold instruction cache); others take the generic one.
-decltype(&k_tc_stream<-1>) stream_kernel(int kind) {
+template <bool CLU>
+decltype(&k_tc_stream<-1, CLU>) stream_kernel(int kind) {
     switch (kind) {
-        case EPI_STORE_F32: return k_tc_stream<EPI_STORE_F32>;
-        case EPI_ADD_F32: return k_tc_stream<EPI_ADD_F32>;
-        case EPI_QKV: return k_tc_stream<EPI_QKV>;
-        case EPI_SWIGLU: return k_tc_stream<EPI_SWIGLU>;
-        default: return k_tc_stream<-1>;
+        case EPI_STORE_F32: return k_tc_stream<EPI_STORE_F32, CLU>;
+        case EPI_ADD_F32: return k_tc_stream<EPI_ADD_F32, CLU>;
+        case EPI_QKV: return k_tc_stream<EPI_QKV, CLU>;
+        case EPI_SWIGLU: return k_tc_stream<EPI_SWIGLU, CLU>;
+        default: return k_tc_stream<-1, CLU>;
     }
 }
 
@@ -546,8 +552,8 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
                 cfg.stream = st;
                 cfg.attrs = attr;
                 cfg.numAttrs = pdl_enabled() ? 2 : 1;
-                cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel(ep.kind), tmW, tmX, M, N, K, cs, kbp, 1, ep, part,
-                                                   tickets, err, sn);
+                cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel<true>(ep.kind), tmW, tmX, M, N, K, cs, kbp, 1, ep,
+                                                   part, tickets, err, sn);
                 note_launch();
                 if (e != cudaSuccess) return e;
                 return cudaGetLastError();
@@ -556,8 +562,8 @@ cudaError_t tc_stream(const void* X, int64_t ldx, const TcWeightStream& w, int M
     }
     int kb_per = (nkb + splits - 1) / splits;
     splits = (nkb + kb_per - 1) / kb_per;  // no empty splits
-    launch(stream_kernel(ep.kind), nT * splits, NTHREADS, smem_bytes(), st, tmW, tmX, M, N, K, splits, kb_per, 0, ep,
-           part, tickets, err, sn);
+    launch(stream_kernel<false>(ep.kind), nT * splits, NTHREADS, smem_bytes(), st, tmW, tmX, M, N, K, splits, kb_per, 0,
+           ep, part, tickets, err, sn);
     note_launch();
     return cudaGetLastError();
 }
