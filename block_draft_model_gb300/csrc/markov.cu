@@ -881,29 +881,23 @@ __global__ void __launch_bounds__(NT) k_markov_finish(const float* __restrict__ 
     __shared__ int red_i[NT / 32];
     __shared__ float redf[32];
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // four independent running bests, so that the partials' loads are in flight together
-    ArgBest bq[4] = {{-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}, {-INFINITY, INT_MAX}};
+    // every thread's first 32 partials are requested at once (one L2 round trip), the rest in turn
     const float* pv = part_v + (int64_t)b * nchunks;
     const int* pi = part_i + (int64_t)b * nchunks;
-    int c = threadIdx.x;
-    for (; c + 3 * NT < nchunks; c += 4 * NT) {
-        float v[4];
-        int i[4];
+    float v[32];
+    int iv[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[q] = pv[c + q * NT];
-            i[q] = pi[c + q * NT];
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (better(v[q], i[q], bq[q].v, bq[q].i)) bq[q] = ArgBest{v[q], i[q]};
+    for (int q = 0; q < 32; ++q) {
+        const int c = threadIdx.x + q * NT;
+        v[q] = c < nchunks ? pv[c] : -INFINITY;
+        iv[q] = c < nchunks ? pi[c] : INT_MAX;
     }
-    for (; c < nchunks; c += NT)
-        if (better(pv[c], pi[c], bq[0].v, bq[0].i)) bq[0] = ArgBest{pv[c], pi[c]};
-    ArgBest best = bq[0];
+    ArgBest best{-INFINITY, INT_MAX};
 #pragma unroll
-    for (int q = 1; q < 4; ++q)
-        if (better(bq[q].v, bq[q].i, best.v, best.i)) best = bq[q];
+    for (int q = 0; q < 32; ++q)
+        if (better(v[q], iv[q], best.v, best.i)) best = ArgBest{v[q], iv[q]};
+    for (int c = threadIdx.x + 32 * NT; c < nchunks; c += NT)
+        if (better(pv[c], pi[c], best.v, best.i)) best = ArgBest{pv[c], pi[c]};
     best = warp_argbest(best);
     if (lane == 0) {
         red_v[warp] = best.v;
