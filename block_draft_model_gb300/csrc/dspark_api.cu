@@ -99,6 +99,11 @@ struct dspark_handle {
     TcWeight tc_kv_a2, tc_kv_ws;
     TcWeightStream ts_wc, ts_out_proj;       // weight-streaming tensor-core views, rows <= 16
     std::vector<TcWeightStream> ts_kv, ts_qkv, ts_wo, ts_wgu, ts_wd;
+    // batched residual projections split over K: their partials wait here for the next row norm,
+    // which adds kp_pending of them into x in order
+    float* kp_part = nullptr;
+    size_t kp_floats = 0;
+    int kp_pending = 0;
     float* ts_part = nullptr;                // split-K partials of the streaming GEMM
     size_t ts_part_floats = 0;
     unsigned int* ts_tickets = nullptr;
@@ -340,7 +345,9 @@ cudaError_t norm_gemm(dspark_handle* h, const float* w, int R, const WView& wv, 
     const int d = h->d;
     {
         Prof pr(h, CAT_NORM, st);
-        cudaError_t e = rmsnorm_rows(h->x, d, w, R, d, h->cfg.eps, adt, actA, d, st);
+        cudaError_t e = rmsnorm_rows(h->x, d, w, R, d, h->cfg.eps, adt, actA, d, st,
+                                     h->kp_pending ? h->kp_part : nullptr, h->kp_pending, (int64_t)R * d);
+        h->kp_pending = 0;
         if (e != cudaSuccess) return e;
     }
     Prof pr(h, norm_cat, st);
@@ -357,6 +364,30 @@ cudaError_t chained_gemm(dspark_handle* h, int R, const WView& wv, int N, int K,
     sn.eps = h->cfg.eps;
     return tc_stream(h->xb, K, *wv.ts, R, N, K, ep, h->ts_part, h->ts_part_floats, h->ts_tickets, h->ts_n_tickets,
                      h->num_sms, h->d_err, st, &sn);
+}
+
+// x += A . W^T for many block rows.  When the output tiles would leave most SMs idle, K is cut into
+// ranges whose partial products wait in kp_part; the next row norm adds them into x in order.
+cudaError_t residual_gemm(dspark_handle* h, int a_dtype, const void* A, int64_t lda, const WView& wv, int R, int N, int K,
+                          const EpiParams& res, cudaStream_t st) {
+    if (R >= 17 && a_dtype == DT_BF16 && wv.tc && wv.tc->ready && tc_gemm_ok(R, N, K) && !res.ssp && h->kp_part &&
+        h->kp_pending == 0 && res.kind == EPI_ADD_F32 && res.out_f32 == h->x && res.ldo == N && N == h->d) {
+        const int tiles = ((R + 127) / 128) * ((N + 255) / 256);
+        const int nkb = (K + 63) / 64;
+        int ks = std::min({h->num_sms / tiles, nkb, 12});
+        while (ks > 1 && (size_t)ks * R * N > h->kp_floats) --ks;
+        if (ks >= 2) {
+            EpiParams ep;
+            ep.kind = EPI_STORE_F32;
+            ep.out_f32 = h->kp_part;
+            ep.ldo = N;
+            ep.split_rows = R;
+            cudaError_t e = tc_gemm(A, lda, *wv.tc, R, N, K, ep, h->num_sms, h->d_err, st, ks);
+            if (e == cudaSuccess) h->kp_pending = ks;
+            return e;
+        }
+    }
+    return gemm(h, a_dtype, A, lda, nullptr, 0, wv, R, N, K, res, st);
 }
 
 // Every batch-1 projection streams (so the residual epilogues can hand over the next norm's operand).
@@ -603,6 +634,7 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
                          int* tokens, float* conf, float* logits, cudaStream_t st) {
     const dspark_config& c = h->cfg;
     const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
+    h->kp_pending = 0;  // partials of an earlier, interrupted draft are never applied
     DraftStepArgs dsa;
     const bool one_launch = h->layers_path == LAYERS_STEP_TC &&
                             draft_step_args(h, B, seq_ids, anchors_dev, anchor, max_keys, tokens, conf, logits, dsa);
@@ -758,8 +790,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             }
             {
                 Prof pr(h, CAT_O, st);
-                CUDA_TRY(h, gemm(h, adt, actA, d, nullptr, 0,
-                                 WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d, res, st));
+                CUDA_TRY(h, residual_gemm(h, adt, actA, d,
+                                          WView{h->wo[i], at_or_null(h->tc_wo, i), at_or_null(h->ts_wo, i)}, R, d, d,
+                                          res, st));
             }
             EpiParams sw;
             sw.kind = EPI_SWIGLU;
@@ -775,8 +808,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             if (chain) res.xb_g = i + 1 < c.n_layers ? h->attn_norm[i + 1] : h->out_norm;
             {
                 Prof pr(h, CAT_DOWN, st);
-                CUDA_TRY(h, gemm(h, adt, sw.out_act, F, nullptr, 0,
-                                 WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F, res, st));
+                CUDA_TRY(h, residual_gemm(h, adt, sw.out_act, F,
+                                          WView{h->wd[i], at_or_null(h->tc_wd, i), at_or_null(h->ts_wd, i)}, R, d, F,
+                                          res, st));
             }
         }
         if (chain) {
@@ -791,7 +825,9 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
             CUDA_TRY(h, cudaEventRecord(h->ev_join, h->side_stream));
         } else {
             Prof pr(h, CAT_NORM, st);
-            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st));
+            CUDA_TRY(h, rmsnorm_rows(h->x, d, h->out_norm, R, d, c.eps, DT_F32, h->y, d, st,
+                                     h->kp_pending ? h->kp_part : nullptr, h->kp_pending, (int64_t)R * d));
+            h->kp_pending = 0;
         }
         {
             EpiParams ep;
@@ -1414,6 +1450,12 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
             CTRY(tc_prepare(h->tc_wo[i], h->wo[i], d, d));
             CTRY(tc_prepare(h->tc_wgu[i], h->wgu[i], 2 * F, d));
             CTRY(tc_prepare(h->tc_wd[i], h->wd[i], d, F));
+        }
+        // K-range partials of the batched residual projections: up to 12 ranges of every block row
+        const size_t rmax = (size_t)cfg->max_seqs * cfg->gamma;
+        if (rmax >= 17) {
+            h->kp_floats = std::min<size_t>(12 * rmax * d, (size_t)64 << 20);
+            CTRY(dalloc(h, (void**)&h->kp_part, h->kp_floats * 4));
         }
     }
     if (h->dt == DT_BF16 && tc_available() && cfg->max_seqs >= 8) {

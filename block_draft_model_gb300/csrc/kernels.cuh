@@ -79,8 +79,11 @@ cudaError_t gemm_skinny(int a_dtype, const void* A, int64_t lda, const int* a_ro
 
 // ------------------------------------------------------------------ norms and block set-up
 // out[r] = x[r] / sqrt(mean(x[r]^2) + eps) * w   (rows of length n, x fp32)
+// With parts (nparts > 0): x += the partial products parts[s * part_stride + row * ldx + col], s in
+// order, written back to x, before the norm (the residual of a K-split projection).
 cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, int n, float eps, int out_dtype,
-                         void* out, int64_t ldo, cudaStream_t st);
+                         void* out, int64_t ldo, cudaStream_t st, const float* parts = nullptr, int nparts = 0,
+                         int64_t part_stride = 0);
 
 // Ingest normalisation: H = RMSNorm(P) * ctx_norm, then for each layer i
 // N_i = RMSNorm(H) * attn_norm_i, written to out + i * layer_stride (out_dtype).

@@ -12,17 +12,32 @@ namespace {
 
 constexpr int NT = 256;
 
-template <typename TO>
-__global__ void __launch_bounds__(NT) k_rmsnorm_rows(const float* __restrict__ x, int64_t ldx,
+constexpr int KP_MAX = 12;  // most K-range partials a row norm adds
+
+// ACC: first x += the nparts partial products at parts + s * part_stride (same row layout as x), added
+// in order and written back (each element by the thread that later reads it), then the norm.
+template <typename TO, bool ACC>
+__global__ void __launch_bounds__(NT) k_rmsnorm_rows(float* __restrict__ x, int64_t ldx,
                                                      const float* __restrict__ w, int n, float eps, TO* out,
-                                                     int64_t ldo) {
+                                                     int64_t ldo, const float* __restrict__ parts, int nparts,
+                                                     int64_t part_stride) {
     pdl_wait();
     pdl_trigger();
     __shared__ float red[32];
-    const float* xr = x + (int64_t)blockIdx.x * ldx;
+    float* xr = x + (int64_t)blockIdx.x * ldx;
     float ss = 0.f;
     for (int c = threadIdx.x; c < n; c += NT) {
         float v = xr[c];
+        if constexpr (ACC) {
+            // every partial requested at once (at most KP_MAX of them), then added in order
+            const float* pr = parts + (int64_t)blockIdx.x * ldx + c;
+            float pv[KP_MAX];
+#pragma unroll
+            for (int sp = 0; sp < KP_MAX; ++sp) pv[sp] = sp < nparts ? pr[sp * part_stride] : 0.f;
+#pragma unroll
+            for (int sp = 0; sp < KP_MAX; ++sp) v += pv[sp];
+            xr[c] = v;
+        }
         ss = fmaf(v, v, ss);
     }
     ss = block_sum(ss, red);
@@ -277,12 +292,18 @@ cudaError_t to_float(int dtype, const void* in, int64_t n, float* out, cudaStrea
 }
 
 cudaError_t rmsnorm_rows(const float* x, int64_t ldx, const float* w, int rows, int n, float eps, int out_dtype,
-                         void* out, int64_t ldo, cudaStream_t st) {
+                         void* out, int64_t ldo, cudaStream_t st, const float* parts, int nparts, int64_t part_stride) {
     if (rows <= 0) return cudaSuccess;
-    if (out_dtype == DT_BF16)
-        launch(k_rmsnorm_rows<bf16>, rows, NT, 0, st, x, ldx, w, n, eps, (bf16*)out, ldo);
-    else
-        launch(k_rmsnorm_rows<float>, rows, NT, 0, st, x, ldx, w, n, eps, (float*)out, ldo);
+    float* xm = const_cast<float*>(x);  // written only when partials are added
+    const bool acc = parts && nparts > 0;
+    if (nparts > KP_MAX) return cudaErrorInvalidValue;
+    if (out_dtype == DT_BF16) {
+        if (acc) launch(k_rmsnorm_rows<bf16, true>, rows, NT, 0, st, xm, ldx, w, n, eps, (bf16*)out, ldo, parts, nparts, part_stride);
+        else launch(k_rmsnorm_rows<bf16, false>, rows, NT, 0, st, xm, ldx, w, n, eps, (bf16*)out, ldo, parts, 0, part_stride);
+    } else {
+        if (acc) launch(k_rmsnorm_rows<float, true>, rows, NT, 0, st, xm, ldx, w, n, eps, (float*)out, ldo, parts, nparts, part_stride);
+        else launch(k_rmsnorm_rows<float, false>, rows, NT, 0, st, xm, ldx, w, n, eps, (float*)out, ldo, parts, 0, part_stride);
+    }
     note_launch();
     return cudaGetLastError();
 }
