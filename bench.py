@@ -384,8 +384,10 @@ class FreshContextRunner(Runner):
     def step(self, i):
         g = self.g
         g.reset(0)
-        g.ingest_context(self.pool[i % self.npool])
-        for j in range(self.drafts):
+        # the context ingest and the first draft in one call (the block rows are built beside the ingest)
+        g.ingest_and_draft(self.pool[i % self.npool], int(self.anchors[(i * self.drafts) % len(self.anchors)]),
+                           self.tok, self.conf)
+        for j in range(1, self.drafts):
             g.draft(int(self.anchors[(i * self.drafts + j) % len(self.anchors)]), self.tok, self.conf)
 
     def host_step(self, i):
@@ -468,8 +470,7 @@ class StreamRunner(Runner):
         self.length += x.shape[0]
         if self.length > self.max_ctx:
             raise RuntimeError("context capacity exhausted; lower --steps")
-        self.g.ingest_context(x)
-        self.g.draft(int(self.anchors[i % len(self.anchors)]), self.tok, self.conf)
+        self.g.ingest_and_draft(x, int(self.anchors[i % len(self.anchors)]), self.tok, self.conf)
 
     def host_step(self, i):
         x = self.new_h[i % len(self.new_h)]

@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "CAPACITY", 3: "CUDA", 4: "UNSUPPO
 BF16, FP32 = 0, 1
 ACT_SILU, ACT_GELU_TANH = 0, 1
 
-EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_draft",
+EXPORTED = ["dspark_create", "dspark_destroy", "dspark_ingest_context", "dspark_draft", "dspark_ingest_and_draft",
             "dspark_ingest_context_batched", "dspark_draft_batched", "dspark_ingest_context_host",
             "dspark_draft_host", "dspark_reset", "dspark_context_length", "dspark_check", "dspark_get_cache",
             "dspark_last_error", "dspark_launch_count", "dspark_version", "dspark_profile",
@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_destroy": ([vp], None),
         "dspark_ingest_context": ([vp, vp, i32, vp], i32),
         "dspark_draft": ([vp, i32, vp, vp, vp, vp], i32),
+        "dspark_ingest_and_draft": ([vp, vp, i32, i32, vp, vp, vp, vp], i32),
         "dspark_ingest_context_batched": ([vp, i32, vp, vp, vp, i32, vp], i32),
         "dspark_draft_batched": ([vp, i32, vp, vp, vp, vp, vp, vp], i32),
         "dspark_ingest_context_host": ([vp, vp, i32, vp], i32),
@@ -258,6 +259,12 @@ class Drafter:
         self._check(self.lib.dspark_ingest_context_batched(self._h, int(seq_ids.shape[0]), _ptr(seq_ids),
                                                            _ptr(cu_tokens), _ptr(feats), int(feats.shape[0]),
                                                            _stream(stream)))
+
+    def ingest_and_draft(self, feats, last_token: int, tokens, conf, logits=None, stream=None):
+        """ingest_context(feats) then draft(last_token, ...) in one call: the block rows are built on a
+        side stream while the context is ingested."""
+        self._check(self.lib.dspark_ingest_and_draft(self._h, _ptr(feats), int(feats.shape[0]), int(last_token),
+                                                     _ptr(tokens), _ptr(conf), _ptr(logits), _stream(stream)))
 
     def draft_batched(self, seq_ids, last_tokens, tokens, conf, logits=None, stream=None):
         self._check(self.lib.dspark_draft_batched(self._h, int(seq_ids.shape[0]), _ptr(seq_ids), _ptr(last_tokens),

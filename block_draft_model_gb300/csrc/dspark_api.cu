@@ -181,6 +181,7 @@ struct dspark_handle {
     // (forked from and joined back into the main stream with the two events)
     cudaStream_t side_stream = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    cudaEvent_t ev_block = nullptr;          // the block build of dspark_ingest_and_draft, on the side stream
     std::vector<DraftGraph> graphs;
     uint64_t graph_clock = 0;
     std::vector<ProfRange>* cap_ranges = nullptr;  // set while capturing
@@ -630,8 +631,48 @@ bool draft_step_args(dspark_handle* h, int B, const int* seq_ids, const int* anc
     return draft_step_tc_ok(a, h->num_sms) && (size_t)c.n_heads * a.nchunks * c.gamma * (h->hd + 4) <= h->ds_apart_floats;
 }
 
+// The block rows ("module-dflash.ts" #buildBlock: x_0 = E[anchor] tok_proj^T + block_pos[0], x_j =
+// mask_emb[j-1] + block_pos[j]) and, for one sequence, layer 0's chained operand; *chain0 says whether
+// that operand was written.  Reads no context: it may run beside an ingest.
+dspark_status block_build(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor,
+                          cudaStream_t st, bool* chain0_out) {
+    const dspark_config& c = h->cfg;
+    const int d = h->d, R = B * c.gamma;
+    const bool lowp0 = h->dt == DT_BF16;
+    // one sequence: the block build also writes layer 0's chained operand (bf16(x * attn_norm) and
+    // the 8-column sums of x^2), so the first QKV projection needs no normalisation launch
+    const bool chain0 = B == 1 && !seq_ids && norm_chain_ok(h, R, lowp0) && d % 8 == 0 && h->ws &&
+                        h->ws_floats >= 2 * (size_t)d && !(h->tc_tok_proj.ready && B >= 8);
+    CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st, chain0 ? h->xb : nullptr,
+                           chain0 ? h->attn_norm[0] : nullptr, chain0 ? h->ssp : nullptr));
+    {
+        EpiParams ep;
+        ep.kind = EPI_ADD_F32;
+        ep.out_f32 = h->x;
+        ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
+        if (chain0) {
+            ep.xb = h->xb;
+            ep.ld_xb = d;
+            ep.ssp = h->ssp;
+            ep.xb_g = h->attn_norm[0];
+        }
+        if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
+            // many sequences: gather the anchor embeddings, then one tensor-core GEMM
+            CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
+            CUDA_TRY(h, tc_gemm(h->emb_rows, c.hidden, h->tc_tok_proj, B, d, c.hidden, ep, h->num_sms, h->d_err, st));
+        } else {
+            CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
+                             WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
+        }
+    }
+    *chain0_out = chain0;
+    return DSPARK_OK;
+}
+
+// prebuilt: -1 the draft builds its block rows; 0 / 1 block_build already ran on st's behalf (and
+// wrote layer 0's chained operand when 1).
 dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
-                         int* tokens, float* conf, float* logits, cudaStream_t st) {
+                         int* tokens, float* conf, float* logits, cudaStream_t st, int prebuilt = -1) {
     const dspark_config& c = h->cfg;
     const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
     h->kp_pending = 0;  // partials of an earlier, interrupted draft are never applied
@@ -645,32 +686,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
     }
     if (!one_launch) {
         Prof pr_block(h, CAT_BLOCK, st);
-        const bool lowp0 = h->dt == DT_BF16;
-        // one sequence: the block build also writes layer 0's chained operand (bf16(x * attn_norm) and
-        // the 8-column sums of x^2), so the first QKV projection needs no normalisation launch
-        const bool chain0 = B == 1 && !seq_ids && norm_chain_ok(h, R, lowp0) && d % 8 == 0 && h->ws &&
-                            h->ws_floats >= 2 * (size_t)d && !(h->tc_tok_proj.ready && B >= 8);
-        CUDA_TRY(h, block_init(h->x, h->block_const, B, c.gamma, d, st, chain0 ? h->xb : nullptr,
-                               chain0 ? h->attn_norm[0] : nullptr, chain0 ? h->ssp : nullptr));
-        {
-            EpiParams ep;
-            ep.kind = EPI_ADD_F32;
-            ep.out_f32 = h->x;
-            ep.ldo = (int64_t)c.gamma * d;  // row b of the product lands on block row 0 of sequence b
-            if (chain0) {
-                ep.xb = h->xb;
-                ep.ld_xb = d;
-                ep.ssp = h->ssp;
-                ep.xb_g = h->attn_norm[0];
-            }
-            if (B >= 8 && h->tc_tok_proj.ready && h->emb_rows && anchors_dev && tc_gemm_ok(B, d, c.hidden)) {
-                // many sequences: gather the anchor embeddings, then one tensor-core GEMM
-                CUDA_TRY(h, markov_gather(h->embed, c.hidden, c.vocab, anchors_dev, nullptr, c.gamma, 0, B, h->emb_rows, st));
-                CUDA_TRY(h, tc_gemm(h->emb_rows, c.hidden, h->tc_tok_proj, B, d, c.hidden, ep, h->num_sms, h->d_err, st));
-            } else {
-                CUDA_TRY(h, gemm(h, h->dt, h->embed, c.hidden, anchors_dev, anchors_dev ? 0 : anchor,
-                                 WView{h->tok_proj, nullptr, nullptr}, B, d, c.hidden, ep, st));
-            }
+        bool chain0 = prebuilt > 0;
+        if (prebuilt < 0) {
+            const dspark_status bs = block_build(h, B, seq_ids, anchors_dev, anchor, st, &chain0);
+            if (bs != DSPARK_OK) return bs;
         }
         const bool lowp = (h->dt == DT_BF16);  // the tensor-core kernels take bf16 activations
         void* actA = lowp ? h->act_lp : (void*)h->act;
@@ -1192,6 +1211,7 @@ void dspark_destroy(dspark_handle* h) {
     if (h->side_stream) cudaStreamDestroy(h->side_stream);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->ev_block) cudaEventDestroy(h->ev_block);
     for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
     tc_release(h->tc_wc);
     tc_release(h->tc_out_proj);
@@ -1413,6 +1433,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking));
     CTRY(cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming));
     CTRY(cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming));
+    CTRY(cudaEventCreateWithFlags(&h->ev_block, cudaEventDisableTiming));
     CTRY(dalloc(h, (void**)&h->safe_anchors, (size_t)cfg->max_seqs * 4));
     CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
     h->ws_floats = (size_t)4 << 20;
@@ -1568,6 +1589,46 @@ dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens
     if (s != DSPARK_OK) return s;
     return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
                       logits_dev, st);
+}
+
+dspark_status dspark_ingest_and_draft(dspark_handle* h, const void* feats_dev, int32_t T, int32_t last_token,
+                                      int32_t* tokens_dev, float* conf_dev, float* logits_dev, void* stream) {
+    if (!h) return fail(nullptr, DSPARK_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0) return fail(h, DSPARK_ERR_INVALID_ARG, "T < 0");
+    if (T > 0 && !feats_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "feats is NULL");
+    if (!tokens_dev || !conf_dev) return fail(h, DSPARK_ERR_INVALID_ARG, "tokens or conf is NULL");
+    if (last_token < 0 || last_token >= h->cfg.vocab)
+        return fail(h, DSPARK_ERR_INVALID_ARG, "last_token " + std::to_string(last_token) + " outside [0, vocab)");
+    dspark_status s = sync_len(h, 0);
+    if (s != DSPARK_OK) return s;
+    if ((int64_t)h->len_host[0] + T > h->cfg.max_ctx)
+        return fail(h, DSPARK_ERR_CAPACITY, "context would exceed max_ctx (" + std::to_string(h->len_host[0]) + " + " +
+                                                std::to_string(T) + " > " + std::to_string(h->cfg.max_ctx) + ")");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (h->layers_path == LAYERS_STEP_TC) {  // the one-launch step builds its block itself
+        if (T > 0) {
+            s = ingest_rows(h, feats_dev, T, nullptr, nullptr, st);
+            if (s != DSPARK_OK) return s;
+            h->len_host[0] += T;
+        }
+        return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
+                          logits_dev, st);
+    }
+    // the block rows read no context: they are built on the side stream while the context is ingested
+    CUDA_TRY(h, cudaEventRecord(h->ev_fork, st));
+    CUDA_TRY(h, cudaStreamWaitEvent(h->side_stream, h->ev_fork, 0));
+    bool chain0 = false;
+    s = block_build(h, 1, nullptr, nullptr, last_token, h->side_stream, &chain0);
+    if (s != DSPARK_OK) return s;
+    CUDA_TRY(h, cudaEventRecord(h->ev_block, h->side_stream));
+    if (T > 0) {
+        s = ingest_rows(h, feats_dev, T, nullptr, nullptr, st);
+        if (s != DSPARK_OK) return s;
+        h->len_host[0] += T;
+    }
+    CUDA_TRY(h, cudaStreamWaitEvent(st, h->ev_block, 0));
+    return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
+                      logits_dev, st, chain0 ? 1 : 0);
 }
 
 dspark_status dspark_ingest_context_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,

@@ -154,6 +154,15 @@ dspark_status dspark_ingest_context(dspark_handle* h, const void* feats_dev, int
 dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens_dev, float* conf_dev,
                            float* logits_dev, void* stream);
 
+/* dspark_ingest_context(h, feats_dev, T) followed by dspark_draft(h, last_token, ...), with the same
+ * arguments, errors and results (page 1's updateContext then propose, "src/dspark-runtime.js"), as one
+ * call: the block rows, which read no context, are built on the handle's side stream while the T
+ * rows are ingested on `stream`, and the draft continues on `stream` once both are done.  The draft
+ * runs without the handle's captured graph.  The call returns once everything is enqueued on
+ * `stream`; feats_dev must stay valid until the work completes.  T = 0 drafts only. */
+dspark_status dspark_ingest_and_draft(dspark_handle* h, const void* feats_dev, int32_t T, int32_t last_token,
+                                      int32_t* tokens_dev, float* conf_dev, float* logits_dev, void* stream);
+
 /* Batched ingest: sequences seq_ids_dev[i] (i < n_seqs) receive the feature rows
  * cu_tokens_dev[i] .. cu_tokens_dev[i+1]-1 of feats_dev [total_tokens, m*H]
  * (cu_tokens_dev: n_seqs+1 prefix sums, cu[0] = 0, cu[n] = total_tokens).  Each

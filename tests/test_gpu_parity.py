@@ -564,3 +564,36 @@ def test_gemma_shaped_batched_serving(gemma):
         dr.ingest(syn.make_feats(cfg, int(counts[0, i]), seed=0, step=0, seq=i))
         check_block(dr, 0, int(anchors[0, i]), first_tok[i], first_conf[i], None, label=f"batched step 0 seq {i}")
     dr.reset(0)
+
+
+def test_ingest_and_draft_matches_two_calls():
+    """dspark_ingest_and_draft = dspark_ingest_context then dspark_draft: the same tokens, confidences
+    and logits, bit for bit (its block rows are built on a side stream while the rows are ingested),
+    over several steps, one of them with no new rows."""
+    import block_draft_model_gb300 as bdm
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=6,
+                            vocab=1000, markov_rank=64)
+    W = syn.make_weights(cfg, seed=21)
+    Wd = weights_to_device(W)
+    feats = to_torch(syn.make_feats(cfg, 300, seed=21))
+    a = make_gpu_drafter(cfg, Wd, max_ctx=400)
+    b = make_gpu_drafter(cfg, Wd, max_ctx=400)
+    for g in (a, b):  # the graphed draft plans its key ranges for the capacity, not the length
+        g.set_path(bdm.PATH_GRAPHS, 0)
+    for lo, hi, anchor in [(0, 200, 5), (200, 250, 17), (250, 250, 999), (250, 300, 3)]:
+        ta = torch.empty(cfg.gamma, dtype=torch.int32, device="cuda")
+        tb = torch.empty_like(ta)
+        ca = torch.empty(cfg.gamma, dtype=torch.float32, device="cuda")
+        cb = torch.empty_like(ca)
+        la = torch.empty(cfg.gamma, cfg.vocab, dtype=torch.float32, device="cuda")
+        lb = torch.empty_like(la)
+        if hi > lo:
+            a.ingest_context(feats[lo:hi])
+        a.draft(anchor, ta, ca, la)
+        b.ingest_and_draft(feats[lo:hi], anchor, tb, cb, lb)
+        torch.cuda.synchronize()
+        assert torch.equal(ta, tb), (lo, hi)
+        assert torch.equal(ca, cb), (lo, hi)
+        assert torch.equal(la, lb), (lo, hi)
+        assert a.context_length() == b.context_length() == hi
+    assert a.check() == 0 and b.check() == 0
