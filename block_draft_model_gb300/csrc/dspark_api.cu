@@ -695,15 +695,10 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         void* actA = lowp ? h->act_lp : (void*)h->act;
         const int adt = lowp ? DT_BF16 : DT_F32;
         bool layers_done = false;
-        // One persistent launch for every layer pays off while a layer's weights are
-        // a few slices per SM (its projections run on the legacy warp MMA); larger
-        // layers stream faster through the per-kernel tcgen05 path.
-        const double layer_bytes = (4.0 * d * d + 3.0 * F * d) * 2.0;
-        const bool persistent_fits = layer_bytes <= (double)h->num_sms * 256.0 * 1024.0;
+        // Every layer in one persistent launch on the warp MMA, only when asked for: the per-kernel
+        // tcgen05 path is faster on both drafter shapes (for the small Gemma-shaped layers too).
         // (the one-launch layers keep one K/V head per query head and no per-head transform)
-        if (B == 1 && !seq_ids && lowp &&
-            (h->layers_path == LAYERS_PERSISTENT_MMA || (h->layers_path == LAYERS_AUTO && persistent_fits)) &&
-            !h->qk_rope &&
+        if (B == 1 && !seq_ids && lowp && h->layers_path == LAYERS_PERSISTENT_MMA && !h->qk_rope &&
             h->nkv == c.n_heads) {
             // every layer in one persistent launch
             DraftPersistArgs a{};

@@ -308,8 +308,8 @@ const char* dspark_noalloc_last_error(void);
  * by shape when a choice is 0, its default).  The forms compute the same
  * function up to floating-point rounding order; the choice exists so that each
  * form can be exercised and measured.  Captured draft graphs are dropped.
- *   DSPARK_PATH_LAYERS      batch-1 draft layers: 0 auto, 1 one kernel per
- *                           projection, 2 every layer in one launch on warp
+ *   DSPARK_PATH_LAYERS      batch-1 draft layers: 0 auto (the same as 1), 1 one
+ *                           kernel per projection, 2 every layer in one launch on warp
  *                           MMAs, 3 the whole step up to the logits in one
  *                           launch on tcgen05 (block build, layers, out_proj)
  *   DSPARK_PATH_MARKOV      Markov chain of 1-2 sequences: 0 FMA-pipe chain,
