@@ -616,6 +616,15 @@ __device__ __forceinline__ bool wait_arrivals(const unsigned long long* counter,
     }
 }
 
+// 16-byte read-only load with an L2 eviction policy (from createpolicy)
+__device__ __forceinline__ uint4 ld_nc_policy(const uint4* a, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(a), "l"(pol));
+    return v;
+}
+
 // acc += sum over the 8 bf16 pairs of w and e, in order
 __device__ __forceinline__ float fma_chunk(const uint4& w, const uint4& e, float acc) {
     asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
@@ -648,7 +657,7 @@ __device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int s) {
 }
 
 template <int KD, int NF>  // r = 32 * KD, NF sequences
-__global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, int n_cache) {
+__global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, int n_cache, int n_keep) {
     constexpr int R = KD * 32;
     constexpr int ROWB = R * 2;
     constexpr int CPR = ROWB / 16;  // 16-byte chunks per row
@@ -702,10 +711,19 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
     }
     if (tid < NF) toks[tid][0] = min(max(p.anchors ? p.anchors[tid] : p.anchor, 0), V - 1);
 
+    // The rows past the resident ones are read again at every position, and together they can
+    // exceed what L2 keeps: least-recently-used replacement then drops each line before its
+    // next use. The first n_keep of them (a share of L2 chosen by the host) are loaded with
+    // evict-last and the rest with evict-first, so the kept share hits in L2 at every position
+    // after the first; the last position loads everything evict-first to release the lines.
+    uint64_t pol_keep, pol_pass;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_pass));
     for (int k = 0; k < gamma; ++k) {
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
         const float* uk = ubuf + (k & 1) * NF * rows;
+        const int keep_end = k + 1 < gamma ? nc + n_keep : nc;
         uint4 ev[NF][CPL];
 #pragma unroll
         for (int n = 0; n < NF; ++n)
@@ -727,8 +745,9 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
                     for (int j = 0; j < CPL; ++j)
                         w[j] = *reinterpret_cast<const uint4*>(w2s + li * ROWB + (((s + 8 * j) ^ (li & 7)) * 16));
                 } else if (li < nrows) {
+                    const uint64_t pol = li < keep_end ? pol_keep : pol_pass;
 #pragma unroll
-                    for (int j = 0; j < CPL; ++j) w[j] = __ldg(w2g + (int64_t)li * CPR + s + 8 * j);
+                    for (int j = 0; j < CPL; ++j) w[j] = ld_nc_policy(w2g + (int64_t)li * CPR + s + 8 * j, pol);
                 } else {
 #pragma unroll
                     for (int j = 0; j < CPL; ++j) w[j] = make_uint4(0, 0, 0, 0);
@@ -830,6 +849,7 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
 
 int g_res_ok[3] = {0, 0, 0};  // the resident chain's kernels for r = 64, 128, 256
 int g_res_budget = 0;         // its dynamic shared memory
+int g_l2_bytes = 0;           // the device's L2 size
 
 bool g_fma_ok = false;         // the FMA chain's kernels
 
@@ -1008,6 +1028,7 @@ cudaError_t markov_chain_resident_init() {
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
     g_res_budget = (optin - 4096) / 16 * 16;  // static shared memory and headroom
+    if ((e = cudaDeviceGetAttribute(&g_l2_bytes, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
     g_res_ok[0] = res_attr<2>(g_res_budget) == cudaSuccess;
     g_res_ok[1] = res_attr<4>(g_res_budget) == cudaSuccess;
     g_res_ok[2] = res_attr<8>(g_res_budget) == cudaSuccess;
@@ -1069,6 +1090,8 @@ cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st
     const int n_cache = std::max(0, std::min(rows, (g_res_budget - ubytes) / (p.r * 2)));
     const size_t smem = (size_t)n_cache * p.r * 2 + ubytes;
     if ((int)smem > g_res_budget) return cudaErrorInvalidValue;
+    // streamed rows kept in L2 across positions: 60% of L2 over the grid (the best of 25, 40, 60, 80%)
+    const int n_keep = (int)std::min<int64_t>(rows, (int64_t)g_l2_bytes * 3 / 5 / ((int64_t)num_sms * p.r * 2));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;  // every CTA polls the others' words
     attr[0].val.cooperative = 1;
@@ -1081,12 +1104,12 @@ cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st
     cfg.numAttrs = 1;
     cudaError_t e;
     const bool one = p.B == 1;
-    if (kd == 2) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 1>, p, n_cache)
-                         : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 2>, p, n_cache);
-    else if (kd == 4) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 1>, p, n_cache)
-                              : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 2>, p, n_cache);
-    else e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 1>, p, n_cache)
-                 : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 2>, p, n_cache);
+    if (kd == 2) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 1>, p, n_cache, n_keep)
+                         : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 2>, p, n_cache, n_keep);
+    else if (kd == 4) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 1>, p, n_cache, n_keep)
+                              : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 2>, p, n_cache, n_keep);
+    else e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 1>, p, n_cache, n_keep)
+                 : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 2>, p, n_cache, n_keep);
     note_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
