@@ -12,13 +12,14 @@
 //
 // Inside a CTA (4 warps) the keys stream through a 3-stage cp.async ring of
 // 64-key K and V tiles (rows padded by 16 bytes, so ldmatrix is conflict-free).
-// Each warp owns 16 keys of every tile and keeps its own running softmax state:
-//   S   = Q K^T  mma.m16n8k16 bf16, the (<= 16) queries as the M dimension,
-//                Q (pre-scaled by head_dim^-1/2 log2 e, rounded to bf16) held in
-//                registers as A fragments, K fragments from ldmatrix;
-//   P   = 2^(S - m)   in registers; the S accumulator layout is the A fragment
-//                layout of the next product, P rounded to bf16;
-//   O  += P V    mma.m16n8k16, V fragments from ldmatrix.trans.
+// Each warp owns 16 keys of every tile and keeps its own running softmax state,
+// with the keys on the 16-row M side of mma.m16n8k16 and the block queries on
+// its 8-wide N side (one or two tiles of 8):
+//   S^T  = K Q^T  K fragments from ldmatrix, Q (pre-scaled by head_dim^-1/2
+//                 log2 e, rounded to bf16) held in registers as B fragments;
+//   P^T  = 2^(S^T - m)  in registers, rounded to bf16; movmatrix transposes
+//                 each 8 x 8 block into the B fragment of the next product;
+//   O^T += V^T P^T  V^T fragments from ldmatrix.trans of the V tile.
 // The row sums add the bf16-rounded P, so every range's output is a convex
 // combination of V rows.  At the end the four warps merge through shared
 // memory into the range's (m, l, o) partial (log2 domain, rows of head_dim + 4
@@ -168,10 +169,11 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t laddr, int rank) {
     return v;
 }
 
-template <int HD, typename TO, int NS, bool CL>
+// NQ: tiles of 8 block queries (1 up to 8 queries, 2 up to 16)
+template <int HD, typename TO, int NS, bool CL, int NQ>
 __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     using L = TLayout<HD, NS>;
-    constexpr int KS = HD / 16;  // 16-wide k steps of Q K^T; pairs of 8-wide output tiles of P V
+    constexpr int KS = HD / 16;  // 16-wide head_dim steps of K Q^T; 16-row head_dim tiles of V^T P^T
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ int is_last;
 
@@ -226,39 +228,50 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
             load_kv<HD>(ring + s * L::STAGE, Kb, Vb, dkv, start + s * TK, end, n_ctx, INT_MAX);
     cp_async_commit();
 
-    // Q as A fragments: rows g and g+8, columns (lane % 4) * 2 (+8) of every 16-wide k step
+    // Keys are the MMA's 16-row M side and the block queries its 8-wide N side (NQ tiles of 8), so
+    // at most 8 queries no MMA column is spent on rows that do not exist:
+    //   S^T = K Q^T  (A: 16 keys x 16 of head_dim from ldmatrix, B: Q^T from registers),
+    //   O^T += V^T P^T  (A: 16 of head_dim x 16 keys, ldmatrix.trans of the V tile; B: P^T).
+    // The S^T accumulator of each 8 x 8 (keys x queries) block is, once rounded to bf16 pairs, the
+    // register layout of an 8 x 8 matrix; movmatrix transposes it into the B fragment of P^T.
+    // Thread (g = lane / 4, cq = 2 * (lane % 4)) holds keys g, g + 8 and queries cq, cq + 1 of every
+    // query tile; the per-query max is reduced over the 8 threads that share cq.
     const int g = lane >> 2, cq = (lane & 3) * 2;
-    uint32_t qf[KS][4];
+    uint32_t qb[KS][NQ][2];  // B fragments of Q^T: query nq * 8 + g, head_dim ks * 16 + cq (+1) and + 8 (+9)
     {
         const float qs = rsqrtf((float)HD) * 1.4426950408889634f;
-        const float* q0 = p.q + (int64_t)(b * gamma + g) * d + h * HD;
-        const float* q1 = q0 + (int64_t)8 * d;
-        const bool v0 = g < gamma, v1 = g + 8 < gamma;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int col = ks * 16 + cq;
-            float2 a = v0 ? *reinterpret_cast<const float2*>(q0 + col) : make_float2(0.f, 0.f);
-            float2 bq = v1 ? *reinterpret_cast<const float2*>(q1 + col) : make_float2(0.f, 0.f);
-            float2 cc = v0 ? *reinterpret_cast<const float2*>(q0 + col + 8) : make_float2(0.f, 0.f);
-            float2 dd = v1 ? *reinterpret_cast<const float2*>(q1 + col + 8) : make_float2(0.f, 0.f);
-            float x0 = a.x * qs, x1 = a.y * qs, y0 = bq.x * qs, y1 = bq.y * qs;
-            float z0 = cc.x * qs, z1 = cc.y * qs, w0 = dd.x * qs, w1 = dd.y * qs;
-            qf[ks][0] = pack_round(x0, x1);
-            qf[ks][1] = pack_round(y0, y1);
-            qf[ks][2] = pack_round(z0, z1);
-            qf[ks][3] = pack_round(w0, w1);
+        for (int nq = 0; nq < NQ; ++nq) {
+            const int qi = nq * 8 + g;
+            const bool v = qi < gamma;
+            const float* q0 = p.q + (int64_t)(b * gamma + (v ? qi : 0)) * d + h * HD;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int col = ks * 16 + cq;
+                float2 x = v ? *reinterpret_cast<const float2*>(q0 + col) : make_float2(0.f, 0.f);
+                float2 y = v ? *reinterpret_cast<const float2*>(q0 + col + 8) : make_float2(0.f, 0.f);
+                float x0 = x.x * qs, x1 = x.y * qs, y0 = y.x * qs, y1 = y.y * qs;
+                qb[ks][nq][0] = pack_round(x0, x1);
+                qb[ks][nq][1] = pack_round(y0, y1);
+            }
         }
     }
 
-    float o[2 * KS][4];
+    float o[KS][NQ][4];  // O^T: head_dim ks * 16 + g (+8) x queries nq * 8 + cq (+1)
 #pragma unroll
-    for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g, g+8 (l: this thread's columns)
+    for (int n = 0; n < KS; ++n)
+#pragma unroll
+        for (int nq = 0; nq < NQ; ++nq) o[n][nq][0] = o[n][nq][1] = o[n][nq][2] = o[n][nq][3] = 0.f;
+    float mq[NQ][2], lq[NQ][2];  // queries nq * 8 + cq (+1): running max; this thread's keys' sum
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq) mq[nq][0] = mq[nq][1] = -INFINITY, lq[nq][0] = lq[nq][1] = 0.f;
 
-    // ldmatrix row addresses: lane -> matrix lane/8, row lane%8
+    // ldmatrix row addresses: lane -> matrix lane/8, row lane%8.  K as A (non-transposed): matrices
+    // (keys 0-7 | 8-15) x (head_dim 0-7 | 8-15) in fragment order; V^T as A (transposed): the V rows
+    // of keys 0-7 | 8-15, columns head_dim 0-7 | 8-15, in the order that transposes into fragments.
     const int lr = lane & 7, lm = lane >> 3, kw = warp * 16;
-    const uint32_t k_lane = (uint32_t)((kw + (lm >> 1) * 8 + lr) * L::RB + (lm & 1) * 16);
-    const uint32_t v_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * L::RB + (lm >> 1) * 16);
+    const uint32_t k_lane = (uint32_t)((kw + (lm & 1) * 8 + lr) * L::RB + (lm >> 1) * 16);
+    const uint32_t v_lane = (uint32_t)((kw + (lm >> 1) * 8 + lr) * L::RB + (lm & 1) * 16);
 
     for (int t = 0; t < n_tiles; ++t) {
         if (t == 0) cp_async_wait<0>();  // the first tiles' context and block rows came in two groups
@@ -274,79 +287,93 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
         const uint32_t kbase = ring + (t % NS) * L::STAGE;
         const uint32_t vbase = kbase + L::TILE;
 
-        float s[2][4];
+        float s[NQ][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int nq = 0; nq < NQ; ++nq) s[nq][0] = s[nq][1] = s[nq][2] = s[nq][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + k_lane + ks * 32, b0, b1, b2, b3);
-            mma16816(s[0], qf[ks], b0, b1);
-            mma16816(s[1], qf[ks], b2, b3);
+            uint32_t ka[4];
+            ldsm_x4(kbase + k_lane + ks * 32, ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq) mma16816(s[nq], ka, qb[ks][nq][0], qb[ks][nq][1]);
         }
-        if (kw + 16 > nk) {
+        if (kw + 16 > nk) {  // keys past the range end (zero rows) take no weight
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    if (kw + n * 8 + cq + e >= nk) s[n][e] = s[n][2 + e] = -INFINITY;
+            for (int nq = 0; nq < NQ; ++nq) {
+                if (kw + g >= nk) s[nq][0] = s[nq][1] = -INFINITY;
+                if (kw + g + 8 >= nk) s[nq][2] = s[nq][3] = -INFINITY;
+            }
         }
-        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float a0 = ex2(m0 - ms0), a1 = ex2(m1 - ms1);
-        m0 = mn0;
-        m1 = mn1;
-        float p00 = ex2(s[0][0] - ms0), p01 = ex2(s[0][1] - ms0), p02 = ex2(s[0][2] - ms1), p03 = ex2(s[0][3] - ms1);
-        float p10 = ex2(s[1][0] - ms0), p11 = ex2(s[1][1] - ms0), p12 = ex2(s[1][2] - ms1), p13 = ex2(s[1][3] - ms1);
-        uint32_t pf[4];
-        pf[0] = pack_round(p00, p01);  // row g,   keys cq, cq+1
-        pf[1] = pack_round(p02, p03);  // row g+8, keys cq, cq+1
-        pf[2] = pack_round(p10, p11);  // row g,   keys 8+cq, 9+cq
-        pf[3] = pack_round(p12, p13);  // row g+8, keys 8+cq, 9+cq
-        l0 = l0 * a0 + ((p00 + p01) + (p10 + p11));
-        l1 = l1 * a1 + ((p02 + p03) + (p12 + p13));
+        uint32_t pb[NQ][2];
+        float al[NQ][2];
 #pragma unroll
-        for (int n = 0; n < 2 * KS; ++n) {
-            o[n][0] *= a0;
-            o[n][1] *= a0;
-            o[n][2] *= a1;
-            o[n][3] *= a1;
+        for (int nq = 0; nq < NQ; ++nq) {
+            float mx0 = fmaxf(s[nq][0], s[nq][2]), mx1 = fmaxf(s[nq][1], s[nq][3]);
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+            }
+            const float mn0 = fmaxf(mq[nq][0], mx0), mn1 = fmaxf(mq[nq][1], mx1);
+            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+            al[nq][0] = ex2(mq[nq][0] - ms0);
+            al[nq][1] = ex2(mq[nq][1] - ms1);
+            mq[nq][0] = mn0;
+            mq[nq][1] = mn1;
+            float p0 = ex2(s[nq][0] - ms0), p1 = ex2(s[nq][1] - ms1);  // key g:     queries cq, cq+1
+            float p2 = ex2(s[nq][2] - ms0), p3 = ex2(s[nq][3] - ms1);  // key g + 8: queries cq, cq+1
+            const uint32_t x0 = pack_round(p0, p1), x1 = pack_round(p2, p3);
+            lq[nq][0] = lq[nq][0] * al[nq][0] + (p0 + p2);
+            lq[nq][1] = lq[nq][1] * al[nq][1] + (p1 + p3);
+            asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb[nq][0]) : "r"(x0));
+            asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb[nq][1]) : "r"(x1));
         }
 #pragma unroll
-        for (int n2 = 0; n2 < KS; ++n2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + v_lane + n2 * 32, b0, b1, b2, b3);
-            mma16816(o[2 * n2], pf, b0, b1);
-            mma16816(o[2 * n2 + 1], pf, b2, b3);
+        for (int n = 0; n < KS; ++n)
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq) {
+                o[n][nq][0] *= al[nq][0];
+                o[n][nq][1] *= al[nq][1];
+                o[n][nq][2] *= al[nq][0];
+                o[n][nq][3] *= al[nq][1];
+            }
+#pragma unroll
+        for (int n = 0; n < KS; ++n) {
+            uint32_t va[4];
+            ldsm_x4_t(vbase + v_lane + n * 32, va[0], va[1], va[2], va[3]);
+#pragma unroll
+            for (int nq = 0; nq < NQ; ++nq) mma16816(o[n][nq], va, pb[nq][0], pb[nq][1]);
         }
     }
     cp_async_wait<0>();
     __syncthreads();  // the ring is free for the merge buffers
 
     // ---- merge the four warps into this range's partial
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     float* Ow = reinterpret_cast<float*>(sm + L::OW);
     float* Mw = reinterpret_cast<float*>(sm + L::ML);
     float* Lw = Mw + NW * GMAX;
 #pragma unroll
-    for (int n = 0; n < 2 * KS; ++n) {
-        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g) * L::OWS + n * 8 + cq) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(Ow + (warp * GMAX + g + 8) * L::OWS + n * 8 + cq) = make_float2(o[n][2], o[n][3]);
-    }
-    if ((lane & 3) == 0) {
-        Mw[warp * GMAX + g] = m0;
-        Mw[warp * GMAX + g + 8] = m1;
-        Lw[warp * GMAX + g] = l0;
-        Lw[warp * GMAX + g + 8] = l1;
+    for (int nq = 0; nq < NQ; ++nq) {
+        float l0 = lq[nq][0], l1 = lq[nq][1];
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+        }
+        const int q0 = warp * GMAX + nq * 8 + cq;
+#pragma unroll
+        for (int n = 0; n < KS; ++n) {
+            Ow[q0 * L::OWS + n * 16 + g] = o[n][nq][0];
+            Ow[(q0 + 1) * L::OWS + n * 16 + g] = o[n][nq][1];
+            Ow[q0 * L::OWS + n * 16 + g + 8] = o[n][nq][2];
+            Ow[(q0 + 1) * L::OWS + n * 16 + g + 8] = o[n][nq][3];
+        }
+        if (g == 0) {
+            Mw[q0] = mq[nq][0];
+            Mw[q0 + 1] = mq[nq][1];
+            Lw[q0] = l0;
+            Lw[q0 + 1] = l1;
+        }
     }
     __syncthreads();
 
@@ -596,15 +623,20 @@ __global__ void __launch_bounds__(NT, 2) k_attention_tc(AttnParams p) {
     if (tid == 0) p.tickets[bh] = 0u;
 }
 
-template <int HD, typename TO, int NS>
-cudaError_t set_attr_tc() {
-    cudaError_t e = cudaFuncSetAttribute(k_attention_tc<HD, TO, NS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TLayout<HD, NS>::BYTES);
+template <int HD, typename TO, int NS, int NQ>
+cudaError_t set_attr_tc_q() {
+    cudaError_t e = cudaFuncSetAttribute(k_attention_tc<HD, TO, NS, false, NQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TLayout<HD, NS>::BYTES);
     if (e != cudaSuccess || NS != 3) return e;
-    e = cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TLayout<HD, 3>::BYTES);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(k_attention_tc<HD, TO, 3, true, NQ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+template <int HD, typename TO, int NS>
+cudaError_t set_attr_tc() {
+    cudaError_t e = set_attr_tc_q<HD, TO, NS, 1>();
+    return e != cudaSuccess ? e : set_attr_tc_q<HD, TO, NS, 2>();
 }
 
 int g_num_sms = 0;
@@ -612,7 +644,7 @@ int g_num_sms = 0;
 // how many clusters of that size the device can hold at once
 int g_cluster_max = 0;
 
-template <int HD, typename TO>
+template <int HD, typename TO, int NQ>
 void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
     // A grid that fits one CTA per SM gives each CTA the SM's whole shared memory: a deeper ring,
     // where the ranges are long enough to use it.  Ranges of a few tiles keep the 3-stage ring, so
@@ -634,11 +666,11 @@ void launch_tc(const AttnParams& p, dim3 grid, cudaStream_t st) {
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = pdl_enabled() ? 2 : 1;
-        cudaLaunchKernelEx(&cfg, k_attention_tc<HD, TO, 3, true>, p);
+        cudaLaunchKernelEx(&cfg, k_attention_tc<HD, TO, 3, true, NQ>, p);
     } else if ((int)(grid.x * grid.y * grid.z) <= g_num_sms && per_range > 2) {
-        launch(k_attention_tc<HD, TO, 6, false>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
+        launch(k_attention_tc<HD, TO, 6, false, NQ>, grid, NT, (size_t)TLayout<HD, 6>::BYTES, st, p);
     } else {
-        launch(k_attention_tc<HD, TO, 3, false>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);
+        launch(k_attention_tc<HD, TO, 3, false, NQ>, grid, NT, (size_t)TLayout<HD, 3>::BYTES, st, p);
     }
 }
 
@@ -684,7 +716,7 @@ cudaError_t attention_tc_init() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, k_attention_tc<128, float, 3, true>, &cfg) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveClusters(&clusters, k_attention_tc<128, float, 3, true, 2>, &cfg) == cudaSuccess &&
             clusters >= 1) {
             g_cluster_max = n;
             break;
@@ -701,12 +733,13 @@ cudaError_t attention_tc(const AttnParams& p, cudaStream_t st) {
         return cudaErrorInvalidValue;
     dim3 grid(p.n_chunks, p.n_heads, p.B);
     const bool o16 = p.out_dtype == DT_BF16;
+    const bool q8 = p.gamma <= 8;
     if (hd == 64) {
-        if (o16) launch_tc<64, bf16>(p, grid, st);
-        else launch_tc<64, float>(p, grid, st);
+        if (o16) q8 ? launch_tc<64, bf16, 1>(p, grid, st) : launch_tc<64, bf16, 2>(p, grid, st);
+        else q8 ? launch_tc<64, float, 1>(p, grid, st) : launch_tc<64, float, 2>(p, grid, st);
     } else {
-        if (o16) launch_tc<128, bf16>(p, grid, st);
-        else launch_tc<128, float>(p, grid, st);
+        if (o16) q8 ? launch_tc<128, bf16, 1>(p, grid, st) : launch_tc<128, bf16, 2>(p, grid, st);
+        else q8 ? launch_tc<128, float, 1>(p, grid, st) : launch_tc<128, float, 2>(p, grid, st);
     }
     note_launch();
     return cudaGetLastError();
