@@ -377,6 +377,14 @@ def test_bf16_attention_many_key_ranges(ctx, cap):
     _small(cfg, ctx, seed=12, chunks=[700], anchors=[4, 998], max_ctx=cap)
 
 
+def test_bf16_attention_long_ranges_head_dim_64():
+    """head_dim 64, eight heads, about 10000 keys: one long range per SM (the deep cp.async ring),
+    merged by the ticketed last CTA in staged pieces; gamma 8 fills the one 8-wide query tile."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=512, n_heads=8, n_layers=1, ff_mult=2, gamma=8,
+                            vocab=1000, markov_rank=64)
+    _small(cfg, 10000, seed=13, chunks=[4000], anchors=[3, 997], max_ctx=10100)
+
+
 def test_host_checked_errors():
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=2,
