@@ -385,6 +385,16 @@ def test_bf16_attention_long_ranges_head_dim_64():
     _small(cfg, 10000, seed=13, chunks=[4000], anchors=[3, 997], max_ctx=10100)
 
 
+@pytest.mark.parametrize("ctx,cap", [(2000, 2100), (9000, 9100)])
+def test_bf16_attention_partial_second_query_tile(ctx, cap):
+    """gamma 11: the block queries fill one 8-wide tile and 3 rows of a second; four heads of 64.
+    2000 keys: 16 short ranges merged inside a cluster; 9000 keys: 38 long ranges (one CTA per SM,
+    the deep ring) merged by the ticketed last CTA in staged pieces."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=4, n_layers=1, ff_mult=2, gamma=11,
+                            vocab=1000, markov_rank=64)
+    _small(cfg, ctx, seed=14, chunks=[ctx // 3], anchors=[7, 990], max_ctx=cap)
+
+
 def test_host_checked_errors():
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=2,
