@@ -31,11 +31,14 @@ struct DevBuf {
 // Kernel classes of the step, timed by dspark_profile.
 enum Cat {
     CAT_INGEST_PROJ, CAT_INGEST_NORM, CAT_INGEST_KV, CAT_BLOCK, CAT_NORM, CAT_QKV, CAT_ATTN, CAT_O, CAT_GATE_UP,
-    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_LAYERS, CAT_STEP, CAT_COUNT
+    CAT_DOWN, CAT_OUT_PROJ, CAT_MARKOV, CAT_LAYERS, CAT_STEP,
+    CAT_QKV_SIDE,  // layer 0's QKV beside an ingest (its range spans the ingest it overlaps)
+    CAT_COUNT
 };
 const char* const kCatNames[CAT_COUNT] = {"ingest_proj", "ingest_norm", "ingest_kv", "block_build", "rmsnorm",
                                           "qkv_proj", "attention", "o_proj", "gate_up_proj", "down_proj",
-                                          "out_proj", "markov_argmax", "draft_layers", "draft_step"};
+                                          "out_proj", "markov_argmax", "draft_layers", "draft_step",
+                                          "qkv_proj_beside_ingest"};
 
 struct ProfRange {
     int cat;
@@ -112,6 +115,7 @@ struct dspark_handle {
     void* cache = nullptr;
     int64_t rows = 0, seq_stride = 0, kv_off = 0, layer_stride = 0;
     int* d_len = nullptr;
+    int* d_len_next = nullptr;  // sequence 0's length after an ingest in flight (the early layer-0 QKV)
     int* d_err = nullptr;
     std::vector<int> len_host;
     std::vector<char> len_known;
@@ -161,6 +165,14 @@ struct dspark_handle {
     int layers_path = 0;                     // DSPARK_PATH_LAYERS: 0 auto, else the forced form
     float* ws = nullptr;
     size_t ws_floats = 0;
+    // a second set of split-K scratch (SIMT and weight-streaming) for launches on the side stream
+    // beside an ingest (SideScratch)
+    float* ws_side = nullptr;
+    size_t ws_side_floats = 0;
+    float* ts_part_side = nullptr;
+    size_t ts_part_side_floats = 0;
+    unsigned int* ts_tickets_side = nullptr;
+    size_t ts_n_tickets_side = 0;
     int* safe_ids = nullptr;                 // [max_seqs] validated batched sequence slots (-1: rejected)
     int* safe_anchors = nullptr;             // [max_seqs] batched anchors clamped into [0, V)
     // ingest workspaces
@@ -671,8 +683,40 @@ dspark_status block_build(dspark_handle* h, int B, const int* seq_ids, const int
 
 // prebuilt: -1 the draft builds its block rows; 0 / 1 block_build already ran on st's behalf (and
 // wrote layer 0's chained operand when 1).
+// The QKV epilogue of layer `layer`: Q rows to h->q, the block's K/V rows into the cache after the
+// context (whose lengths are read from seq_len).
+EpiParams qkv_epi(const dspark_handle* h, int layer, const int* seq_ids, const int* seq_len) {
+    EpiParams qkv = cache_epi(h, layer);
+    qkv.kind = EPI_QKV;
+    qkv.out_f32 = h->q;
+    qkv.ldo = h->d;
+    qkv.gamma = h->cfg.gamma;
+    qkv.seq_ids = seq_ids;
+    qkv.seq_len = seq_len;
+    return qkv;
+}
+
+// While alive, the handle's split-K scratch is the side stream's set: launches on the side stream
+// beside an ingest never share scratch with the ingest's own GEMMs.
+struct SideScratch {
+    dspark_handle* h;
+    explicit SideScratch(dspark_handle* hh) : h(hh) { swap(); }
+    ~SideScratch() { swap(); }
+    void swap() {
+        std::swap(h->ws, h->ws_side);
+        std::swap(h->ws_floats, h->ws_side_floats);
+        std::swap(h->ts_part, h->ts_part_side);
+        std::swap(h->ts_part_floats, h->ts_part_side_floats);
+        std::swap(h->ts_tickets, h->ts_tickets_side);
+        std::swap(h->ts_n_tickets, h->ts_n_tickets_side);
+    }
+};
+
+// prebuilt: -1 build the block rows here, 0 / 1 already built (1: with the chained operand);
+// qkv0_done: layer 0's QKV projection has been issued already (dspark_ingest_and_draft)
 dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int* anchors_dev, int anchor, int max_keys,
-                         int* tokens, float* conf, float* logits, cudaStream_t st, int prebuilt = -1) {
+                         int* tokens, float* conf, float* logits, cudaStream_t st, int prebuilt = -1,
+                         bool qkv0_done = false) {
     const dspark_config& c = h->cfg;
     const int d = h->d, F = h->F, R = B * c.gamma, V = c.vocab;
     h->kp_pending = 0;  // partials of an earlier, interrupted draft are never applied
@@ -744,14 +788,11 @@ dspark_status draft_rows(dspark_handle* h, int B, const int* seq_ids, const int*
         const bool chain = !layers_done && norm_chain_ok(h, R, lowp);
         for (int i = 0; i < c.n_layers && !layers_done; ++i) {
             if (i == 0) pr_block.end();
-            EpiParams qkv = cache_epi(h, i);
-            qkv.kind = EPI_QKV;
-            qkv.out_f32 = h->q;
-            qkv.ldo = d;
-            qkv.gamma = c.gamma;
-            qkv.seq_ids = seq_ids;
+            const EpiParams qkv = qkv_epi(h, i, seq_ids, h->d_len);
             const WView wqkv{h->wqkv[i], at_or_null(h->tc_qkv, i), at_or_null(h->ts_qkv, i)};
-            if (chain && (i > 0 || chain0))
+            if (i == 0 && qkv0_done && chain && chain0) {
+                // issued beside the ingest
+            } else if (chain && (i > 0 || chain0))
                 CUDA_TRY(h, chained_gemm(h, R, wqkv, d + 2 * h->dkv, d, qkv, st, CAT_QKV));
             else
                 CUDA_TRY(h, norm_gemm(h, h->attn_norm[i], R, wqkv, d + 2 * h->dkv, d, qkv, actA, adt, st, CAT_QKV));
@@ -1346,6 +1387,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     h->layer_stride = h->seq_stride * cfg->max_seqs;
     CTRY(dalloc(h, &h->cache, (size_t)h->layer_stride * nL * es));
     CTRY(dalloc(h, (void**)&h->d_len, sizeof(int) * cfg->max_seqs));
+    CTRY(dalloc(h, (void**)&h->d_len_next, sizeof(int)));
     CTRY(cudaMemsetAsync(h->d_len, 0, sizeof(int) * cfg->max_seqs, st));
     CTRY(dalloc(h, (void**)&h->d_err, sizeof(int)));
     CTRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), st));
@@ -1433,6 +1475,8 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
     CTRY(cudaMemsetAsync(h->mk_cnt, 0, (size_t)cfg->max_seqs * 4, st));
     h->ws_floats = (size_t)4 << 20;
     CTRY(dalloc(h, (void**)&h->ws, h->ws_floats * 4));
+    h->ws_side_floats = (size_t)1 << 20;
+    CTRY(dalloc(h, (void**)&h->ws_side, h->ws_side_floats * 4));
     // ingest workspaces
     h->ingest_rows = std::max(1, std::min(std::max(cfg->max_ctx, 16), 16384));
     h->P_rows = h->ingest_rows * (h->ingest_rows <= 4096 ? 4 : 1);
@@ -1509,6 +1553,12 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         CTRY(dalloc(h, (void**)&h->ts_part, std::max<size_t>(part, 4) * 4));
         CTRY(dalloc(h, (void**)&h->ts_tickets, tiles * sizeof(unsigned int)));
         CTRY(cudaMemsetAsync(h->ts_tickets, 0, tiles * sizeof(unsigned int), st));
+        // the side stream's set, for layer 0's QKV projection beside an ingest
+        h->ts_part_side_floats = tc_stream_scratch_floats(d + 2 * dkv, d, h->num_sms);
+        h->ts_n_tickets_side = (size_t)(d + 2 * dkv + 127) / 128;
+        CTRY(dalloc(h, (void**)&h->ts_part_side, std::max<size_t>(h->ts_part_side_floats, 4) * 4));
+        CTRY(dalloc(h, (void**)&h->ts_tickets_side, h->ts_n_tickets_side * sizeof(unsigned int)));
+        CTRY(cudaMemsetAsync(h->ts_tickets_side, 0, h->ts_n_tickets_side * sizeof(unsigned int), st));
         // the one-launch tcgen05 draft step: its weight maps in launch order, and its scratch
         CTRY(tc_stream_prepare(h->ts_tok_proj, h->tok_proj, d, H));
         CTRY(draft_step_tc_init());
@@ -1609,12 +1659,27 @@ dspark_status dspark_ingest_and_draft(dspark_handle* h, const void* feats_dev, i
         return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
                           logits_dev, st);
     }
-    // the block rows read no context: they are built on the side stream while the context is ingested
+    // The block rows read no context: they are built on the side stream while the context is
+    // ingested.  So is layer 0's QKV projection when its norm comes through the block build: it
+    // reads only the block rows, and it writes the block's K/V rows after the new context, at the
+    // length the host already knows (a word of its own, as the ingest updates the device length).
     CUDA_TRY(h, cudaEventRecord(h->ev_fork, st));
     CUDA_TRY(h, cudaStreamWaitEvent(h->side_stream, h->ev_fork, 0));
-    bool chain0 = false;
-    s = block_build(h, 1, nullptr, nullptr, last_token, h->side_stream, &chain0);
-    if (s != DSPARK_OK) return s;
+    bool chain0 = false, qkv0_early = false;
+    {
+        SideScratch side(h);
+        s = block_build(h, 1, nullptr, nullptr, last_token, h->side_stream, &chain0);
+        if (s != DSPARK_OK) return s;
+        qkv0_early = T > 0 && chain0 && !h->qk_rope && h->ts_part &&
+                     (h->layers_path == LAYERS_AUTO || h->layers_path == LAYERS_PER_KERNEL) &&
+                     norm_chain_ok(h, h->cfg.gamma, h->dt == DT_BF16);
+        if (qkv0_early) {
+            CUDA_TRY(h, set_len(h->d_len_next, 0, h->len_host[0] + T, h->side_stream));
+            const WView wqkv{h->wqkv[0], at_or_null(h->tc_qkv, 0), at_or_null(h->ts_qkv, 0)};
+            CUDA_TRY(h, chained_gemm(h, h->cfg.gamma, wqkv, h->d + 2 * h->dkv, h->d,
+                                     qkv_epi(h, 0, nullptr, h->d_len_next), h->side_stream, CAT_QKV_SIDE));
+        }
+    }
     CUDA_TRY(h, cudaEventRecord(h->ev_block, h->side_stream));
     if (T > 0) {
         s = ingest_rows(h, feats_dev, T, nullptr, nullptr, st);
@@ -1623,7 +1688,7 @@ dspark_status dspark_ingest_and_draft(dspark_handle* h, const void* feats_dev, i
     }
     CUDA_TRY(h, cudaStreamWaitEvent(st, h->ev_block, 0));
     return draft_rows(h, 1, nullptr, nullptr, last_token, h->len_host[0] + h->cfg.gamma, tokens_dev, conf_dev,
-                      logits_dev, st, chain0 ? 1 : 0);
+                      logits_dev, st, chain0 ? 1 : 0, qkv0_early);
 }
 
 dspark_status dspark_ingest_context_batched(dspark_handle* h, int32_t n_seqs, const int32_t* seq_ids_dev,

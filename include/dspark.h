@@ -157,7 +157,9 @@ dspark_status dspark_draft(dspark_handle* h, int32_t last_token, int32_t* tokens
 /* dspark_ingest_context(h, feats_dev, T) followed by dspark_draft(h, last_token, ...), with the same
  * arguments, errors and results (page 1's updateContext then propose, "src/dspark-runtime.js"), as one
  * call: the block rows, which read no context, are built on the handle's side stream while the T
- * rows are ingested on `stream`, and the draft continues on `stream` once both are done.  The draft
+ * rows are ingested on `stream`, and so is layer 0's QKV projection where its norm comes through the
+ * block build (it writes the block's K/V rows at the length after the ingest); the draft continues
+ * on `stream` once both are done.  The side stream's launches use scratch of their own.  The draft
  * runs without the handle's captured graph.  The call returns once everything is enqueued on
  * `stream`; feats_dev must stay valid until the work completes.  T = 0 drafts only. */
 dspark_status dspark_ingest_and_draft(dspark_handle* h, const void* feats_dev, int32_t T, int32_t last_token,
