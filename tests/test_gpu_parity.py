@@ -584,21 +584,25 @@ def test_gemma_shaped_batched_serving(gemma):
     dr.reset(0)
 
 
-def test_ingest_and_draft_matches_two_calls():
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_ingest_and_draft_matches_two_calls(dtype):
     """dspark_ingest_and_draft = dspark_ingest_context then dspark_draft: the same tokens, confidences
-    and logits, bit for bit (its block rows are built on a side stream while the rows are ingested),
-    over several steps, one of them with no new rows."""
+    and logits, bit for bit (its block rows, and for bf16 layer 0's QKV projection, run on a side
+    stream while the rows are ingested), over several steps: long ingests (tile GEMMs), short ones
+    (weight-streaming or SIMT GEMMs, beside the side stream's own split-K launches) and one with no
+    new rows."""
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=256, n_heads=2, n_layers=2, ff_mult=2, gamma=6,
-                            vocab=1000, markov_rank=64)
+                            vocab=1000, markov_rank=64, dtype=dtype)
     W = syn.make_weights(cfg, seed=21)
     Wd = weights_to_device(W)
     feats = to_torch(syn.make_feats(cfg, 300, seed=21))
     a = make_gpu_drafter(cfg, Wd, max_ctx=400)
     b = make_gpu_drafter(cfg, Wd, max_ctx=400)
-    for g in (a, b):  # the graphed draft plans its key ranges for the capacity, not the length
-        g.set_path(bdm.PATH_GRAPHS, 0)
-    for lo, hi, anchor in [(0, 200, 5), (200, 250, 17), (250, 250, 999), (250, 300, 3)]:
+    for g in (a, b):  # launched directly: the graphed draft plans its key ranges for the capacity, not the length
+        g.set_path(bdm.PATH_GRAPHS, 1)
+    for lo, hi, anchor in [(0, 200, 5), (200, 250, 17), (250, 250, 999), (250, 255, 3), (255, 256, 640),
+                           (256, 300, 8)]:
         ta = torch.empty(cfg.gamma, dtype=torch.int32, device="cuda")
         tb = torch.empty_like(ta)
         ca = torch.empty(cfg.gamma, dtype=torch.float32, device="cuda")
