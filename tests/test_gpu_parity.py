@@ -305,6 +305,14 @@ def test_norm_chain_through_residual_epilogues(d, n_heads, gamma, L, vocab):
     check_block(dr, 0, 11, tok, conf, lg, label="after 2 more rows")
 
 
+def test_grouped_kv_more_tiles_than_sms():
+    """Eq 3 K/V of 4 layers over 1280 new rows (d 512): 10 x 4 x 4 = 160 output tiles, more than one
+    per SM, so the persistent CTAs take a second tile; every cache row is compared."""
+    cfg = syn.DrafterConfig(hidden=256, n_taps=2, d_draft=512, n_heads=4, n_layers=4, ff_mult=2, gamma=4,
+                            vocab=600, markov_rank=32)
+    _small(cfg, 1280, seed=23, chunks=[], anchors=[9], max_ctx=1300)
+
+
 def test_ingest_projection_split_over_k():
     """A context projection with few output tiles (300 rows, d 256) and a long
     K (4 taps x 512): the tensor-core GEMM cuts K into ranges whose partial
