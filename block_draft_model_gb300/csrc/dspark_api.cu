@@ -681,8 +681,6 @@ dspark_status block_build(dspark_handle* h, int B, const int* seq_ids, const int
     return DSPARK_OK;
 }
 
-// prebuilt: -1 the draft builds its block rows; 0 / 1 block_build already ran on st's behalf (and
-// wrote layer 0's chained operand when 1).
 // The QKV epilogue of layer `layer`: Q rows to h->q, the block's K/V rows into the cache after the
 // context (whose lengths are read from seq_len).
 EpiParams qkv_epi(const dspark_handle* h, int layer, const int* seq_ids, const int* seq_len) {
