@@ -656,7 +656,14 @@ __device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int s) {
     return ((s & 1) ? q[1] : q[0]) + __shfl_xor_sync(0xffffffffu, give, 1);
 }
 
-template <int KD, int NF>  // r = 32 * KD, NF sequences
+// NSTG > 0: the rows past the resident ones stream through a per-thread cp.async ring of NSTG
+// 64-row blocks (n_cache a multiple of 64), so that their loads run ahead across passes and across
+// the argmax exchange; each thread copies exactly the 16-byte chunks it reads, and its own copy
+// groups are its only synchronisation.  The arithmetic is the same as without the ring.
+constexpr int MAX_SBLK = 64;  // streamed 64-row blocks per CTA in the ring form
+constexpr int RING_STAGES = 3;
+
+template <int KD, int NF, int NSTG = 0>  // r = 32 * KD, NF sequences
 __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, int n_cache, int n_keep) {
     constexpr int R = KD * 32;
     constexpr int ROWB = R * 2;
@@ -679,7 +686,11 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
     const int nrows = max(0, min(V, v_begin + rows) - v_begin);
     const int nc = min(n_cache, nrows);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, s = lane & 7, grp = tid >> 3;
-    float* ubuf = reinterpret_cast<float*>(w2s + (size_t)n_cache * ROWB);  // [2][NF][rows]
+    constexpr int RING_BYTES = NSTG * 64 * ROWB;
+    float* ubuf = reinterpret_cast<float*>(w2s + (size_t)n_cache * ROWB + RING_BYTES);  // [2][NF][rows]
+    const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(w2s + (size_t)n_cache * ROWB);
+    __shared__ short sblk[NSTG > 0 ? MAX_SBLK : 1];  // first rows of the streamed blocks, in consumption order
+    __shared__ int n_sblk;
     const uint32_t ubuf_s = (uint32_t)__cvta_generic_to_shared(ubuf);
     const uint32_t w2s_s = (uint32_t)__cvta_generic_to_shared(w2s);
     const uint4* __restrict__ w2g = reinterpret_cast<const uint4*>(w2 + (int64_t)v_begin * R);
@@ -719,6 +730,39 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
     uint64_t pol_keep, pol_pass;
     asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
     asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_pass));
+    // ring form: the streamed blocks in the order the passes take them (rows ascending by pass,
+    // blocks descending inside a pass), then the first NSTG - 1 of them requested
+    int nsb = 0, qc = 0;
+    auto issue = [&](int q) {  // this thread's chunks of the q-th streamed block, over all positions
+        if (q < gamma * nsb) {
+            const int kq = q / nsb, li = sblk[q - kq * nsb] + grp;
+            const bool in = li < nrows;
+            const uint64_t pol = (kq + 1 < gamma && li < nc + n_keep) ? pol_keep : pol_pass;
+            const uint4* src = w2g + (int64_t)(in ? li : 0) * CPR;
+            const uint32_t dst = ring_s + (uint32_t)((q % (NSTG > 0 ? NSTG : 1)) * 64 + grp) * ROWB;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+                asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                                 dst + (uint32_t)((s + 8 * j) * 16)),
+                             "l"(src + s + 8 * j), "r"(in ? 16 : 0), "l"(pol)
+                             : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if constexpr (NSTG > 0) {
+        if (tid == 0) {
+            int n = 0;
+            for (int base = 0; base < nrows; base += PASS)
+                for (int i = 7; i >= 0; --i) {
+                    const int row0 = base + 64 * i;
+                    if (row0 >= nc && row0 < nrows && n < MAX_SBLK) sblk[n++] = (short)row0;
+                }
+            n_sblk = n;
+        }
+        __syncthreads();
+        nsb = n_sblk;
+        for (int q = 0; q < NSTG - 1; ++q) issue(q);
+    }
     for (int k = 0; k < gamma; ++k) {
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
@@ -740,10 +784,19 @@ __global__ void __launch_bounds__(NT_FMA, 1) k_markov_chain_fma(MarkovParams p, 
             for (int i = 7; i >= 0; --i) {
                 const int li = base + grp + GROUPS * i;
                 uint4 w[CPL];
+                const int row0 = base + GROUPS * i;  // the first row of this 64-row block (warp-uniform)
                 if (li < nc) {
 #pragma unroll
                     for (int j = 0; j < CPL; ++j)
                         w[j] = *reinterpret_cast<const uint4*>(w2s + li * ROWB + (((s + 8 * j) ^ (li & 7)) * 16));
+                } else if (NSTG > 0 && row0 >= nc && row0 < nrows) {
+                    // (every thread of the CTA takes this branch for the block, so the group counts agree)
+                    issue(qc + NSTG - 1);
+                    asm volatile("cp.async.wait_group %0;" ::"n"(NSTG > 0 ? NSTG - 1 : 0) : "memory");
+                    const uint8_t* rr = w2s + (size_t)n_cache * ROWB + (size_t)((qc % (NSTG > 0 ? NSTG : 1)) * 64 + grp) * ROWB;
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) w[j] = *reinterpret_cast<const uint4*>(rr + (s + 8 * j) * 16);
+                    ++qc;
                 } else if (li < nrows) {
                     const uint64_t pol = li < keep_end ? pol_keep : pol_pass;
 #pragma unroll
@@ -866,9 +919,9 @@ __global__ void k_wait_selftest(int which, unsigned long long* w64, unsigned int
     }
 }
 
-template <int KD, int NF>
+template <int KD, int NF, int NSTG = 0>
 cudaError_t fma_attr(int bytes) {
-    return cudaFuncSetAttribute(k_markov_chain_fma<KD, NF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return cudaFuncSetAttribute(k_markov_chain_fma<KD, NF, NSTG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 template <int KD>
@@ -1034,7 +1087,8 @@ cudaError_t markov_chain_resident_init() {
     g_res_ok[2] = res_attr<8>(g_res_budget) == cudaSuccess;
     g_fma_ok = fma_attr<2, 1>(g_res_budget) == cudaSuccess && fma_attr<2, 2>(g_res_budget) == cudaSuccess &&
                fma_attr<4, 1>(g_res_budget) == cudaSuccess && fma_attr<4, 2>(g_res_budget) == cudaSuccess &&
-               fma_attr<8, 1>(g_res_budget) == cudaSuccess && fma_attr<8, 2>(g_res_budget) == cudaSuccess;
+               fma_attr<8, 1>(g_res_budget) == cudaSuccess && fma_attr<8, 2>(g_res_budget) == cudaSuccess &&
+               fma_attr<8, 1, RING_STAGES>(g_res_budget) == cudaSuccess;
     (void)cudaGetLastError();
     return cudaSuccess;
 }
@@ -1087,8 +1141,15 @@ cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st
     const int kd = p.r / 32;
     const int rows = (p.V + num_sms - 1) / num_sms;
     const int ubytes = (2 * p.B * rows * 4 + 15) / 16 * 16;
-    const int n_cache = std::max(0, std::min(rows, (g_res_budget - ubytes) / (p.r * 2)));
-    const size_t smem = (size_t)n_cache * p.r * 2 + ubytes;
+    int n_cache = std::max(0, std::min(rows, (g_res_budget - ubytes) / (p.r * 2)));
+    // Where most of a CTA's rows do not fit in shared memory, the rest stream through the ring form:
+    // fewer resident rows (a multiple of 64) make room for the ring's blocks.
+    const int ring_bytes = RING_STAGES * 64 * p.r * 2;
+    const int n_cache_ring = std::max(0, (g_res_budget - ubytes - ring_bytes) / (p.r * 2)) & ~63;
+    const bool ring = kd == 8 && p.B == 1 && rows - n_cache >= 6 * 64 && n_cache_ring > 0 &&
+                      (rows - n_cache_ring + 63) / 64 <= MAX_SBLK;
+    if (ring) n_cache = n_cache_ring;
+    const size_t smem = (size_t)n_cache * p.r * 2 + (ring ? ring_bytes : 0) + ubytes;
     if ((int)smem > g_res_budget) return cudaErrorInvalidValue;
     // streamed rows kept in L2 across positions: 60% of L2 over the grid (the best of 25, 40, 60, 80%)
     const int n_keep = (int)std::min<int64_t>(rows, (int64_t)g_l2_bytes * 3 / 5 / ((int64_t)num_sms * p.r * 2));
@@ -1108,6 +1169,7 @@ cudaError_t markov_chain_fma(const MarkovParams& p, int num_sms, cudaStream_t st
                          : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<2, 2>, p, n_cache, n_keep);
     else if (kd == 4) e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 1>, p, n_cache, n_keep)
                               : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<4, 2>, p, n_cache, n_keep);
+    else if (ring) e = cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 1, RING_STAGES>, p, n_cache, n_keep);
     else e = one ? cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 1>, p, n_cache, n_keep)
                  : cudaLaunchKernelEx(&cfg, k_markov_chain_fma<8, 2>, p, n_cache, n_keep);
     note_launch();

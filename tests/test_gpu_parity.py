@@ -325,6 +325,7 @@ def test_ingest_projection_split_over_k():
 @pytest.mark.parametrize("n_seq,rank,vocab,form", [
     (3, 64, 1000, "mma"), (1, 128, 5003, "mma"), (7, 256, 2048, "mma"),
     (3, 64, 1000, "fma"), (2, 128, 5003, "fma"), (1, 256, 73448, "fma"), (2, 256, 100003, "fma"),
+    (1, 256, 150001, "fma"),
 ])
 def test_markov_chain_few_sequences(n_seq, rank, vocab, form):
     """1 to 7 sequences with r in {64, 128, 256}: the whole Markov chain in one
@@ -333,6 +334,8 @@ def test_markov_chain_few_sequences(n_seq, rank, vocab, form):
     FMA pipes with the argmax exchanged through per-CTA words ("fma").
     Vocabularies that leave ragged slices, CTAs without rows (V 1000), rows
     past the resident ones (V 73448) and several 512-row passes (V 100003);
+    V 150001 with one sequence streams most of each slice through the
+    per-thread copy ring (a ragged last block, a shorter last slice);
     three sequences then one on the same handle switch between the forms."""
     import block_draft_model_gb300 as bdm
     cfg = syn.DrafterConfig(hidden=128, n_taps=2, d_draft=128, n_heads=2, n_layers=1, ff_mult=2, gamma=6,
