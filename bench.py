@@ -205,6 +205,15 @@ def class_work(cls: str, cfg, T: int, L_total: int, B: int):
     return dict(bytes=0, flops=0, bound="hbm")
 
 
+def dominant_class(prof_all, cfg, L_total, B):
+    """The kernel class with the most device time per step among those with a work model (a class
+    without one, such as a launch overlapped with another stream, is taken only if none has one).
+    prof_all: {class: (ms, ranges, launches, index)} from the profiled pass."""
+    modelled = [k for k in prof_all
+                if class_work(k, cfg, 1, L_total, B)["bytes"] or class_work(k, cfg, 1, L_total, B)["flops"]]
+    return max(modelled or list(prof_all), key=lambda k: prof_all[k][0])
+
+
 def draft_bytes_min(cfg, L_total, B=1):
     """Algorithmic bytes of one draft call: every weight once (w2 once), the
     caches of all layers for every sequence, the embedding rows."""
@@ -755,9 +764,7 @@ def main():
     torch.cuda.synchronize()
     prof_all = g.profile_read()
     g.profile(0)
-    modelled = {k: v for k, v in prof_all.items()
-                if class_work(k, cfg, 1, run.L_total, B)["bytes"] or class_work(k, cfg, 1, run.L_total, B)["flops"]}
-    dominant = max(modelled or prof_all, key=lambda k: prof_all[k][0])
+    dominant = dominant_class(prof_all, cfg, run.L_total, B)
 
     # timed region: K steps, no profiling (event pairs inside the draft graph would break the launch overlap)
     clocks = ClockSampler(local)

@@ -55,6 +55,18 @@ def test_class_work_counts_kv_width(bench):
     assert bench.draft_bytes_min(gqa, 1024) < bench.draft_bytes_min(mha, 1024)
 
 
+def test_dominant_class_skips_unmodelled_overlap(bench):
+    """Layer 0's QKV projection beside the ingest has no work model (its event range spans the
+    ingest it overlaps): it is never the roofline's class, even with the longest range."""
+    cfg = syn.MINICPM
+    assert bench.class_work("qkv_proj_beside_ingest", cfg, 1, 1024, 1)["bytes"] == 0
+    prof = {"ingest_kv": (0.074, 2, 2, 2), "gate_up_proj": (0.073, 5, 5, 8),
+            "qkv_proj_beside_ingest": (0.2, 1, 1, 14)}
+    assert bench.dominant_class(prof, cfg, 1024, 1) == "ingest_kv"
+    assert bench.dominant_class({"qkv_proj_beside_ingest": (0.2, 1, 1, 14)}, cfg, 1024, 1) == \
+        "qkv_proj_beside_ingest"
+
+
 def test_traffic_rows_follow_the_kernel_source(bench, tmp_path, monkeypatch):
     src = tmp_path / "k.cu"
     src.write_text("__global__ void k() {}\n")
