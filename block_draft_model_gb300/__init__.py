@@ -261,8 +261,9 @@ class Drafter:
                                                            _stream(stream)))
 
     def ingest_and_draft(self, feats, last_token: int, tokens, conf, logits=None, stream=None):
-        """ingest_context(feats) then draft(last_token, ...) in one call: the block rows are built on a
-        side stream while the context is ingested."""
+        """ingest_context(feats) then draft(last_token, ...) in one call, with the same results: the
+        block rows, and layer 0's QKV projection where its norm comes through the block build, run on
+        a side stream while the context is ingested."""
         self._check(self.lib.dspark_ingest_and_draft(self._h, _ptr(feats), int(feats.shape[0]), int(last_token),
                                                      _ptr(tokens), _ptr(conf), _ptr(logits), _stream(stream)))
 
