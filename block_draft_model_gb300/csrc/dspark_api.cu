@@ -101,6 +101,7 @@ struct dspark_handle {
     void* wkv_s = nullptr;                   // [n_layers][2 d_kv][d] bf16
     TcWeight tc_kv_a2, tc_kv_ws;
     TcWeightStream ts_wc, ts_out_proj;       // weight-streaming tensor-core views, rows <= 16
+    TcWeightStream ts_kv_all;                // wkv_s as one [n_layers * 2 d_kv, d] weight (short ingests)
     std::vector<TcWeightStream> ts_kv, ts_qkv, ts_wo, ts_wgu, ts_wd;
     // batched residual projections split over K: their partials wait here for the next row norm,
     // which adds kp_pending of them into x in order
@@ -538,8 +539,11 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
         }
         const int lp = h->dt;  // normalised rows in the storage type (bf16 feeds the tensor cores)
         const bool grouped = n > 16 && h->tc_kv_a.ready && h->tc_kv_w.ready && tc_gemm_ok(n, 2 * h->dkv, d);
+        // a short ingest streams every layer's scaled K/V weights in one launch
+        const bool stream_all = !grouped && n <= 16 && lp == DT_BF16 && h->ts_kv_all.ready &&
+                                tc_stream_ok(n, nL * 2 * h->dkv, d);
         // the attn_norm rides on the scaled K/V weights: one normalised copy serves every layer
-        const bool shared = grouped && h->tc_kv_ws.ready && h->tc_kv_a2.ready128;
+        const bool shared = (grouped && h->tc_kv_ws.ready && h->tc_kv_a2.ready128) || stream_all;
         {
             Prof pr(h, CAT_INGEST_NORM, st);
             CUDA_TRY(h, ingest_norm(h->P, ks, (int64_t)n * d, n, d, h->cfg.eps, h->ctx_norm,
@@ -561,6 +565,22 @@ dspark_status ingest_rows(dspark_handle* h, const void* feats, int T, const int*
                                             true));
             else
                 CUDA_TRY(h, tc_gemm_grouped(h->tc_kv_a, h->tc_kv_w, nL, n, 2 * h->dkv, d, kv, h->num_sms, h->d_err, st));
+            CUDA_TRY(h, ingest_qk(h, n, row_seq ? row_seq + t0 : nullptr, row_seq ? row_pos + t0 : nullptr, st));
+            if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
+            continue;
+        }
+        if (stream_all) {
+            // one product [n, nL * 2 d_kv]: column block l is layer l's K/V rows
+            EpiParams kv = cache_epi(h, 0);
+            kv.kind = EPI_KV_CACHE;
+            kv.group_stride = h->layer_stride;
+            kv.group_cols = 2 * h->dkv;
+            if (row_seq) {
+                kv.row_seq = row_seq + t0;
+                kv.row_pos = row_pos + t0;
+            }
+            CUDA_TRY(h, tc_stream(h->Nbuf, d, h->ts_kv_all, n, nL * 2 * h->dkv, d, kv, h->ts_part, h->ts_part_floats,
+                                  h->ts_tickets, h->ts_n_tickets, h->num_sms, h->d_err, st));
             CUDA_TRY(h, ingest_qk(h, n, row_seq ? row_seq + t0 : nullptr, row_seq ? row_pos + t0 : nullptr, st));
             if (!row_seq) CUDA_TRY(h, add_len(h->d_len, 0, n, st));
             continue;
@@ -1534,6 +1554,7 @@ dspark_status dspark_create(const dspark_config* cfg, const dspark_weights* w, v
         };
         CTRY(prep(h->ts_wc, h->W_c, d, h->mH));
         CTRY(prep(h->ts_out_proj, h->out_proj, V, d));
+        if (h->wkv_s) CTRY(prep(h->ts_kv_all, h->wkv_s, nL * 2 * dkv, d));
         h->ts_kv.resize(nL);
         h->ts_qkv.resize(nL);
         h->ts_wo.resize(nL);

@@ -49,6 +49,10 @@ __device__ __forceinline__ void epi_one(const EpiParams& ep, int m, int n, float
         case EPI_KV_CACHE: {
             int slot = ep.row_seq ? ep.row_seq[m] : 0;
             int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
+            if (ep.group_cols > 0) {  // the groups side by side in one product
+                grp = n / ep.group_cols;
+                n -= grp * ep.group_cols;
+            }
             cache_store(ep, slot, pos, n, v, grp);
             break;
         }
@@ -229,7 +233,8 @@ __device__ __forceinline__ void epi_row32_k(const EpiParams& ep, int m, int n, i
             break;
         case EPI_KV_CACHE:
             // 32 columns never straddle K and V when the cache row width is a multiple of 32
-            if (full && (ep.d & 31) == 0 && ((ep.d_kv ? ep.d_kv : ep.d) & 31) == 0 && ((uintptr_t)ep.cache & 15) == 0) {
+            if (full && ep.group_cols == 0 && (ep.d & 31) == 0 && ((ep.d_kv ? ep.d_kv : ep.d) & 31) == 0 &&
+                ((uintptr_t)ep.cache & 15) == 0) {
                 const int slot = ep.row_seq ? ep.row_seq[m] : 0;
                 const int pos = ep.row_pos ? ep.row_pos[m] : ep.seq_len[slot] + m;
                 cache_store32(ep, slot, pos, n, v, grp);

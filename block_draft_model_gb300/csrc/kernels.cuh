@@ -28,6 +28,8 @@ struct EpiParams {
     int64_t ldo = 0;
     int split_rows = 0;          // EPI_STORE_F32 of a K-split tensor-core GEMM: rows between the ranges' outputs
     int64_t group_stride = 0;    // EPI_KV_CACHE of a grouped tensor-core GEMM: cache elements between groups
+    int group_cols = 0;          // EPI_KV_CACHE of one product over several groups side by side: columns per
+                                 // group (group = n / group_cols); 0: one group
     void* out_act = nullptr;     // EPI_SWIGLU output, element type act_dtype
     int act_dtype = DT_F32;
     int64_t ld_act = 0;
